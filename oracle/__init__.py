@@ -1,0 +1,160 @@
+"""fp64 CPU oracle for sparse multi-head attention -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports, links or runs anything here, and this
+package imports nothing from the product.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision); this module
+compiles it with gcc on first use and wraps it with ctypes.  See ``oracle.c``
+for the passages each function follows and the readings taken.
+
+Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
+brute-force dense masked softmax, closed forms and invariants (no function is
+unpinned).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``oracle/_build/liboracle.so`` (gcc, -O2,
+    IEEE semantics: no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, i32, vp, dbl = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_double
+            lib.gto_check_csr.argtypes = [i64, i64, vp, vp]
+            lib.gto_check_csr.restype = ctypes.c_int
+            lib.gto_sparse_mha_rows.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, dbl,
+                                                vp, i64, vp, vp, vp]
+            lib.gto_sparse_mha_rows.restype = ctypes.c_int
+            lib.gto_dense_attention.argtypes = [i64, i32, i32, vp, vp, vp, dbl, vp]
+            lib.gto_dense_attention.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def check_csr(indptr, indices, n: int) -> bool:
+    """True when indptr runs monotonically from 0 to nnz and every index is
+    in [0, n)."""
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    return _load().gto_check_csr(n, int(indptr[-1]), _ptr(indptr), _ptr(indices)) == 0
+
+
+def sparse_mha(indptr, indices, Q, K, V, scale, rows=None, want_probs=False,
+               threads: int = 1):
+    """Sparse MHA forward in fp64.
+
+    ``indptr`` int32 [N+1], ``indices`` int32 [nnz] (CSR by destination),
+    ``Q, K, V`` float32 [N, H, D] (bf16 inputs passed as their exact float32
+    values), ``scale`` the float32 scale (promoted to double).  ``rows``
+    limits the computation to a list of rows (outputs then follow that list).
+    Returns ``dict(out=[R,H,D] f64, logits=[nnz,H] f64 | None, probs=... )``;
+    logits/probs entries of rows not computed stay NaN.
+    ``threads`` > 1 splits the rows over host threads (each thread calls the
+    same single-threaded C routine on a contiguous slice of rows).
+    """
+    lib = _load()
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    Q = np.ascontiguousarray(Q, dtype=np.float32)
+    K = np.ascontiguousarray(K, dtype=np.float32)
+    V = np.ascontiguousarray(V, dtype=np.float32)
+    N, H, D = Q.shape
+    nnz = int(indptr[-1])
+    if rows is None:
+        rows_arr = np.arange(N, dtype=np.int64)
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+    R = len(rows_arr)
+    out = np.zeros((R, H, D), dtype=np.float64)
+    logits = np.full((nnz, H), np.nan) if want_probs else None
+    probs = np.full((nnz, H), np.nan) if want_probs else None
+    s = float(np.float32(scale))
+
+    def run(r0, r1):
+        rc = lib.gto_sparse_mha_rows(
+            N, nnz, H, D, _ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), s,
+            _ptr(rows_arr[r0:r1]), r1 - r0, _ptr(out[r0:r1]),
+            _ptr(logits), _ptr(probs))
+        if rc != 0:
+            raise OracleError(f"gto_sparse_mha_rows failed with code {rc}")
+
+    threads = max(1, min(int(threads), R if R > 0 else 1))
+    if threads == 1:
+        run(0, R)
+    else:
+        # split by edge count so each thread gets a similar amount of work
+        deg = (indptr[1:].astype(np.int64) - indptr[:-1])[rows_arr] + 1
+        cum = np.cumsum(deg)
+        cuts = [0] + [int(np.searchsorted(cum, cum[-1] * t / threads)) for t in range(1, threads)] + [R]
+        errs = []
+
+        def worker(a, b):
+            try:
+                if b > a:
+                    run(a, b)
+            except Exception as exc:  # pragma: no cover - re-raised below
+                errs.append(exc)
+
+        ts = [threading.Thread(target=worker, args=(cuts[t], cuts[t + 1])) for t in range(threads)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+        if errs:
+            raise errs[0]
+    return dict(out=out, logits=logits, probs=probs)
+
+
+def dense_attention(Q, K, V, scale):
+    """All-pairs attention softmax(scale * Q K^T) V per head, fp64.
+    ``Q, K, V`` float32 [n, H, D]; returns float64 [n, H, D]."""
+    lib = _load()
+    Q = np.ascontiguousarray(Q, dtype=np.float32)
+    K = np.ascontiguousarray(K, dtype=np.float32)
+    V = np.ascontiguousarray(V, dtype=np.float32)
+    n, H, D = Q.shape
+    out = np.zeros((n, H, D), dtype=np.float64)
+    rc = lib.gto_dense_attention(n, H, D, _ptr(Q), _ptr(K), _ptr(V),
+                                 float(np.float32(scale)), _ptr(out))
+    if rc != 0:
+        raise OracleError(f"gto_dense_attention failed with code {rc}")
+    return out

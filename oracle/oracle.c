@@ -1,0 +1,181 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for sparse multi-head attention.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the bench's
+ * CPU-baseline leg may call this code.  It shares nothing with the CUDA
+ * library: no headers, helpers or constants.
+ *
+ * What it computes (per CSR row i, per head h):
+ *
+ *   SparseAttn(Q, K, V, A) = softmax((Q K^T) o A / sqrt(d)) V
+ *     -- "Graph Transformer in a Nutshell", section "Sparse Multi-head
+ *        Attention", equation SparseAttn; SparseMHA.forward (bsddmm ->
+ *        sparse softmax over the last sparse dimension -> bspmm).
+ *
+ *   e = u_dot_v(g, k, q);  a = edge_softmax(g, e / sqrt(d_qkv));
+ *   wv = u_mul_e_sum(g, v, a)
+ *     -- "Efficient Sparse Transformer implementation with DGL's builtin
+ *        operators", TransLayer.forward.
+ *
+ *   e_ij = q_i . k_j / sqrt(d_k);  alpha_ij = exp(e_ij) / sum_j' exp(e_ij');
+ *   h_i = sum_j alpha_ij v_j
+ *     -- "Graph Transformer theory, derivation and implementation"
+ *        (グラフTransformerの理論と導出と実装), section "review of scaled
+ *        dot-product attention" (スケール付きドット積注意の復習).
+ *
+ * Readings taken where the pages leave a step open:
+ *  - the softmax runs over the stored entries of the row only; non-edges are
+ *    excluded (weight 0, i.e. logit -inf as in the same page's shortest-path
+ *    bias section, b_inf = -inf), not treated as logit 0;
+ *  - A is binary (the spmatrix is built from an edge list with no values);
+ *  - row i lists the nodes j it attends to (CSR by destination: node i
+ *    aggregates over its in-edges j -> i);
+ *  - a row with no entries gives exact zeros;
+ *  - every CSR entry is its own edge (duplicates count twice);
+ *  - `scale` is an argument (normally 1/sqrt(D)); the logit is
+ *    scale * (q . k) in fp64;
+ *  - the max is subtracted before exp (does not change the result);
+ *  - no dropout (evaluation mode).
+ *
+ * Arithmetic: inputs are float32 (bf16 inputs arrive as their exact float32
+ * widening), every operation is double, the reductions run in index order,
+ * exp is the C library's double exp.  Two passes per (row, head): logits and
+ * max, then normalised weights and the weighted sum of V.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define GTO_OK 0
+#define GTO_BAD_CSR -1
+#define GTO_BAD_ARG -2
+#define GTO_NO_MEMORY -3
+
+/* Check indptr monotone from 0 to nnz and every index in [0, N). */
+int gto_check_csr(int64_t N, int64_t nnz, const int32_t* indptr, const int32_t* indices)
+{
+    if (N < 0 || nnz < 0 || !indptr) return GTO_BAD_ARG;
+    if (indptr[0] != 0 || (int64_t)indptr[N] != nnz) return GTO_BAD_CSR;
+    for (int64_t i = 0; i < N; ++i)
+        if (indptr[i + 1] < indptr[i]) return GTO_BAD_CSR;
+    for (int64_t e = 0; e < nnz; ++e)
+        if (indices[e] < 0 || (int64_t)indices[e] >= N) return GTO_BAD_CSR;
+    return GTO_OK;
+}
+
+/*
+ * Sparse MHA forward for a list of rows.
+ *   Q, K, V : float32 [N, H, D] row-major (D innermost).
+ *   rows    : the rows to compute (NULL: rows 0..N-1, then nrows must be N).
+ *   out     : double [nrows, H, D], row r of the list at out + r*H*D.
+ *   logits, probs : double [nnz, H] indexed by CSR position (may be NULL);
+ *             only the entries of the listed rows are written.
+ * Returns 0, or a negative code for bad arguments / bad CSR / no memory.
+ */
+int gto_sparse_mha_rows(int64_t N, int64_t nnz, int32_t H, int32_t D,
+                        const int32_t* indptr, const int32_t* indices,
+                        const float* Q, const float* K, const float* V, double scale,
+                        const int64_t* rows, int64_t nrows,
+                        double* out, double* logits, double* probs)
+{
+    if (N < 0 || nnz < 0 || H <= 0 || D <= 0 || nrows < 0 || !indptr || !out) return GTO_BAD_ARG;
+    if (!rows && nrows != N) return GTO_BAD_ARG;
+    if (nnz > 0 && (!indices || !K || !V)) return GTO_BAD_ARG;
+    if (N > 0 && !Q) return GTO_BAD_ARG;
+    if (gto_check_csr(N, nnz, indptr, indices) != GTO_OK) return GTO_BAD_CSR;
+
+    int64_t max_deg = 0;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        if (i < 0 || i >= N) return GTO_BAD_ARG;
+        int64_t deg = (int64_t)indptr[i + 1] - indptr[i];
+        if (deg > max_deg) max_deg = deg;
+    }
+    double* l = (double*)malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    double* p = (double*)malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    if (!l || !p) { free(l); free(p); return GTO_NO_MEMORY; }
+
+    const int64_t HD = (int64_t)H * D;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        const int64_t beg = indptr[i], end = indptr[i + 1];
+        const int64_t deg = end - beg;
+        double* o_row = out + r * HD;
+        for (int32_t h = 0; h < H; ++h) {
+            double* o = o_row + (int64_t)h * D;
+            for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+            if (deg == 0) continue;                       /* empty row: zeros */
+            const float* q = Q + i * HD + (int64_t)h * D;
+            /* pass 1: logits l_e = scale * <q_i, k_j> and their max */
+            double m = -INFINITY;
+            for (int64_t k = 0; k < deg; ++k) {
+                const int64_t j = indices[beg + k];
+                const float* kj = K + j * HD + (int64_t)h * D;
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += (double)q[d] * (double)kj[d];
+                l[k] = scale * dot;
+                if (l[k] > m) m = l[k];
+            }
+            /* pass 2: softmax weights over the row's stored entries */
+            double S = 0.0;
+            for (int64_t k = 0; k < deg; ++k) { p[k] = exp(l[k] - m); S += p[k]; }
+            for (int64_t k = 0; k < deg; ++k) p[k] /= S;
+            /* weighted sum of the neighbours' values */
+            for (int64_t k = 0; k < deg; ++k) {
+                const int64_t j = indices[beg + k];
+                const float* vj = V + j * HD + (int64_t)h * D;
+                for (int32_t d = 0; d < D; ++d) o[d] += p[k] * (double)vj[d];
+            }
+            if (logits) for (int64_t k = 0; k < deg; ++k) logits[(beg + k) * H + h] = l[k];
+            if (probs) for (int64_t k = 0; k < deg; ++k) probs[(beg + k) * H + h] = p[k];
+        }
+    }
+    free(l);
+    free(p);
+    return GTO_OK;
+}
+
+/*
+ * Dense scaled-dot-product attention, all pairs, per head:
+ *   out[i,h,:] = sum_j softmax_j(scale * q_i . k_j) v_j
+ * -- "Graph Transformer in a Nutshell", the all-pairs Attn equation, and
+ *    "Graph Transformer theory, derivation and implementation", review of
+ *    scaled dot-product attention.  Q, K, V float32 [n, H, D]; out double.
+ * This is the result a complete graph (with self-loops) must reproduce.
+ */
+int gto_dense_attention(int64_t n, int32_t H, int32_t D, const float* Q, const float* K,
+                        const float* V, double scale, double* out)
+{
+    if (n < 0 || H <= 0 || D <= 0 || !out) return GTO_BAD_ARG;
+    if (n == 0) return GTO_OK;
+    if (!Q || !K || !V) return GTO_BAD_ARG;
+    double* w = (double*)malloc(sizeof(double) * (size_t)n);
+    if (!w) return GTO_NO_MEMORY;
+    const int64_t HD = (int64_t)H * D;
+    for (int64_t i = 0; i < n; ++i) {
+        for (int32_t h = 0; h < H; ++h) {
+            const float* q = Q + i * HD + (int64_t)h * D;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+                const float* kj = K + j * HD + (int64_t)h * D;
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += (double)q[d] * (double)kj[d];
+                w[j] = scale * dot;
+                if (w[j] > m) m = w[j];
+            }
+            double S = 0.0;
+            for (int64_t j = 0; j < n; ++j) { w[j] = exp(w[j] - m); S += w[j]; }
+            double* o = out + i * HD + (int64_t)h * D;
+            for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                const double a = w[j] / S;
+                const float* vj = V + j * HD + (int64_t)h * D;
+                for (int32_t d = 0; d < D; ++d) o[d] += a * (double)vj[d];
+            }
+        }
+    }
+    free(w);
+    return GTO_OK;
+}

@@ -1,0 +1,349 @@
+"""Pins for the fp64 oracle (CPU only).
+
+The oracle is checked against things other than itself:
+  * a hand-derived worked example (tests/golden/hand_worked_example.json);
+  * brute-force dense masked softmax attention on tiny graphs, built from the
+    COO edge list (not the CSR) -- the masked-softmax pattern of the GAT
+    comparison in "Graph Transformer theory, derivation and implementation"
+    and its b_inf = -inf reading of disconnected pairs;
+  * closed forms: complete graph == dense attention (scipy's softmax),
+    single neighbour -> v_j exactly, q = 0 or scale = 0 -> neighbour mean,
+    V constant -> constant, empty row -> exact 0, duplicate entries weigh
+    twice;
+  * invariants: probabilities sum to one; permutation equivariance (same
+    page, "permutation equivariant"); invariance to shifting every key by
+    one vector;
+  * mutation checks: plausible mistakes planted in a copy of oracle.c (the
+    query taken from the wrong node, a dropped scale, a wrong head offset,
+    values gathered from the destination, a sign error in the exponent, a
+    missing normalisation, a dropped last edge) each fail the brute-force
+    pin.
+"""
+import json
+import math
+import os
+import re
+import subprocess
+import tempfile
+import ctypes
+
+import numpy as np
+import pytest
+from scipy.special import softmax as sp_softmax
+
+import oracle
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked_example.json")
+
+
+# --------------------------------------------------------------------------
+# helpers (independent of the oracle's code)
+# --------------------------------------------------------------------------
+def _val(x):
+    if isinstance(x, str):
+        table = {"ln3": math.log(3.0), "-ln3": -math.log(3.0)}
+        if x in table:
+            return table[x]
+        num, den = x.split("/")
+        return float(num) / float(den)
+    return float(x)
+
+
+def _arr(nested):
+    if isinstance(nested, list):
+        return [_arr(v) for v in nested]
+    return _val(nested)
+
+
+def brute_force(src, dst, n, Q, K, V, scale):
+    """Dense route: count matrix A[i, j] = #edges j -> i, logits
+    scale * q_i.k_j (+ log count), non-edges -inf, row softmax, times V.
+    Rows without edges give 0."""
+    A = np.zeros((n, n))
+    np.add.at(A, (np.asarray(dst), np.asarray(src)), 1.0)
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (Q, K, V))
+    logits = scale * np.einsum("ihd,jhd->hij", q, k)
+    with np.errstate(divide="ignore"):
+        logits = logits + np.log(A)[None]          # log 0 = -inf masks non-edges
+    has = (A.sum(1) > 0)
+    out = np.zeros_like(q)
+    lg = logits[:, has, :]
+    m = lg.max(axis=2, keepdims=True)
+    w = np.exp(lg - m)
+    p = w / w.sum(axis=2, keepdims=True)
+    out[has] = np.einsum("hij,jhd->ihd", p, v)
+    return out
+
+
+def _csr_coo(indptr, indices):
+    dst = np.repeat(np.arange(len(indptr) - 1), np.diff(indptr))
+    return np.asarray(indices, dtype=np.int64), dst
+
+
+def _rand_feats(rng, n, h, d, std=1.0):
+    return [(rng.standard_normal((n, h, d)) * std).astype(np.float32) for _ in range(3)]
+
+
+# --------------------------------------------------------------------------
+# the worked example
+# --------------------------------------------------------------------------
+def test_hand_worked_example():
+    g = json.load(open(GOLDEN))
+    Q = np.array(_arr(g["Q"]), dtype=np.float32)
+    K = np.array(_arr(g["K"]), dtype=np.float32)
+    V = np.array(_arr(g["V"]), dtype=np.float32)
+    r = oracle.sparse_mha(np.array(g["indptr"]), np.array(g["indices"]), Q, K, V,
+                          g["scale"], want_probs=True)
+    np.testing.assert_allclose(r["out"], np.array(_arr(g["expected_out"])), rtol=1e-6, atol=1e-6)
+    np.testing.assert_allclose(r["probs"], np.array(_arr(g["expected_probs"])), rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(r["logits"], np.array(_arr(g["expected_logits"])), rtol=1e-6, atol=1e-7)
+    # the empty row is exactly zero, the single-neighbour row is v exactly
+    assert np.all(r["out"][1] == 0.0)
+    assert np.array_equal(r["out"][2], V[2].astype(np.float64))
+
+
+# --------------------------------------------------------------------------
+# brute force
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(6))
+def test_brute_force_random_tiny(seed):
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(2, 48))
+    e = int(rng.integers(0, n * n // 2 + 1))
+    H = int(rng.integers(1, 5))
+    D = int(rng.integers(1, 9))
+    pick = rng.choice(n * n, size=e, replace=False)
+    src, dst = pick // n, pick % n
+    indptr, indices = wl.csr_by_destination(src, dst, n)
+    Q, K, V = _rand_feats(rng, n, H, D)
+    scale = float(np.float32(1 / math.sqrt(D)))
+    got = oracle.sparse_mha(indptr, indices, Q, K, V, scale)["out"]
+    ref = brute_force(src, dst, n, Q, K, V, scale)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_brute_force_tiny_random_workload():
+    w = wl.make_workload("tiny_random")
+    src, dst = _csr_coo(w.indptr, w.indices)
+    got = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale)["out"]
+    ref = brute_force(src, dst, w.N, w.Q, w.K, w.V, w.scale)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_duplicates_count_twice():
+    rng = np.random.default_rng(7)
+    n, H, D = 9, 3, 4
+    src = rng.integers(0, n, 40)
+    dst = rng.integers(0, n, 40)                 # with repeats
+    indptr, indices = wl.csr_by_destination(src, dst, n)
+    Q, K, V = _rand_feats(rng, n, H, D)
+    got = oracle.sparse_mha(indptr, indices, Q, K, V, 0.5)["out"]
+    ref = brute_force(src, dst, n, Q, K, V, 0.5)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_direction_matters():
+    """Row i attends over its sources j (edges j -> i): a one-way edge
+    0 -> 1 gives row 1 = v_0 and leaves row 0 empty."""
+    rng = np.random.default_rng(3)
+    Q, K, V = _rand_feats(rng, 2, 2, 3)
+    indptr, indices = wl.csr_by_destination([0], [1], 2)
+    out = oracle.sparse_mha(indptr, indices, Q, K, V, 1.0)["out"]
+    assert np.all(out[0] == 0)
+    assert np.array_equal(out[1], V[0].astype(np.float64))
+
+
+# --------------------------------------------------------------------------
+# closed forms
+# --------------------------------------------------------------------------
+def test_complete_graph_equals_dense_attention():
+    rng = np.random.default_rng(11)
+    n, H, D = 23, 3, 16
+    Q, K, V = _rand_feats(rng, n, H, D)
+    scale = float(np.float32(1 / math.sqrt(D)))
+    indptr, indices, _ = wl.dense_block_csr(n_blocks=1, block=n)
+    got = oracle.sparse_mha(indptr, indices, Q, K, V, scale)["out"]
+    # library route: scipy softmax over all pairs, per head
+    S = scale * np.einsum("ihd,jhd->hij", Q.astype(np.float64), K.astype(np.float64))
+    ref = np.einsum("hij,jhd->ihd", sp_softmax(S, axis=2), V.astype(np.float64))
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+    dense = oracle.dense_attention(Q, K, V, scale)
+    np.testing.assert_allclose(dense, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_dense_blocks_equal_blockwise_dense_attention():
+    w = wl.make_workload("dense_blocks", n_blocks=2, block=32)
+    got = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale)["out"]
+    for b in range(2):
+        sl = slice(32 * b, 32 * (b + 1))
+        S = w.scale * np.einsum("ihd,jhd->hij", w.Q[sl].astype(np.float64), w.K[sl].astype(np.float64))
+        ref = np.einsum("hij,jhd->ihd", sp_softmax(S, axis=2), w.V[sl].astype(np.float64))
+        np.testing.assert_allclose(got[sl], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_single_neighbour_is_exact():
+    rng = np.random.default_rng(5)
+    n, H, D = 50, 4, 7
+    Q, K, V = _rand_feats(rng, n, H, D, std=30.0)
+    src = rng.integers(0, n, n)
+    indptr, indices = wl.csr_by_destination(src, np.arange(n), n)
+    out = oracle.sparse_mha(indptr, indices, Q, K, V, 0.125)["out"]
+    assert np.array_equal(out, V[src].astype(np.float64))
+
+
+@pytest.mark.parametrize("how", ["q_zero", "scale_zero"])
+def test_uniform_weights_give_neighbour_mean(how):
+    rng = np.random.default_rng(9)
+    w = wl.make_workload("molecules", n_graphs=6)
+    Q, K, V = w.Q.copy(), w.K, w.V
+    scale = w.scale
+    if how == "q_zero":
+        Q[:] = 0
+    else:
+        scale = 0.0
+    out = oracle.sparse_mha(w.indptr, w.indices, Q, K, V, scale)["out"]
+    ref = np.zeros_like(out)
+    for i in range(w.N):
+        nb = w.indices[w.indptr[i]:w.indptr[i + 1]]
+        if len(nb):
+            ref[i] = V[nb].astype(np.float64).mean(axis=0)
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_constant_values_and_empty_rows():
+    rng = np.random.default_rng(12)
+    indptr, indices = wl.random_csr(rng, 40, 90, self_loops=True)
+    Q, K, _ = _rand_feats(rng, 40, 2, 5)
+    V = np.full((40, 2, 5), 1.75, dtype=np.float32)
+    out = oracle.sparse_mha(indptr, indices, Q, K, V, 0.4)["out"]
+    deg = np.diff(indptr)
+    assert (deg == 0).any()
+    assert np.all(out[deg == 0] == 0.0)
+    np.testing.assert_allclose(out[deg > 0], 1.75, rtol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# invariants
+# --------------------------------------------------------------------------
+def test_probs_sum_to_one():
+    w = wl.small_workload("rmat")
+    r = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, want_probs=True)
+    p = r["probs"]
+    assert np.all(p > 0) and np.all(p <= 1)
+    sums = np.add.reduceat(p, w.indptr[:-1][np.diff(w.indptr) > 0], axis=0)
+    np.testing.assert_allclose(sums, 1.0, rtol=0, atol=1e-14)
+    # logits are scale * q.k at the CSR position
+    dst = np.repeat(np.arange(w.N), np.diff(w.indptr))
+    lref = w.scale * np.einsum("ehd,ehd->eh", w.Q[dst].astype(np.float64),
+                               w.K[w.indices].astype(np.float64))
+    np.testing.assert_allclose(r["logits"], lref, rtol=1e-12, atol=1e-12)
+
+
+def test_permutation_equivariance():
+    rng = np.random.default_rng(21)
+    w = wl.small_workload("molecules")
+    src, dst = _csr_coo(w.indptr, w.indices)
+    perm = rng.permutation(w.N)                      # node i -> perm[i]
+    inv = np.argsort(perm)
+    ip2, ix2 = wl.csr_by_destination(perm[src], perm[dst], w.N)
+    Q2, K2, V2 = w.Q[inv], w.K[inv], w.V[inv]
+    a = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale)["out"]
+    b = oracle.sparse_mha(ip2, ix2, Q2, K2, V2, w.scale)["out"]
+    np.testing.assert_allclose(b[perm], a, rtol=1e-12, atol=1e-14)
+
+
+def test_key_shift_invariance():
+    rng = np.random.default_rng(22)
+    indptr, indices = wl.random_csr(rng, 60, 400, self_loops=True)
+    Q, K, V = _rand_feats(rng, 60, 3, 8)
+    # keys and shift on coarse grids so that K + u is exact in float32
+    K = (np.round(K * 64) / 64).astype(np.float32)
+    u = np.round(rng.standard_normal((1, 3, 8)) * 4) / 4
+    a = oracle.sparse_mha(indptr, indices, Q, K, V, 0.3)["out"]
+    K2 = (K.astype(np.float64) + u).astype(np.float32)
+    assert np.array_equal(K2.astype(np.float64), K.astype(np.float64) + u)
+    b = oracle.sparse_mha(indptr, indices, Q, K2, V, 0.3)["out"]
+    np.testing.assert_allclose(b, a, rtol=1e-10, atol=1e-12)
+
+
+def test_rows_subset_matches_full():
+    w = wl.small_workload("erdos_renyi")
+    full = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, threads=4)["out"]
+    rows = np.array([0, 17, 4000, 5999, 17])
+    part = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, rows=rows)["out"]
+    assert np.array_equal(part, full[rows])
+
+
+def test_bad_csr_is_rejected():
+    indptr = np.array([0, 2, 1], dtype=np.int32)
+    assert not oracle.check_csr(indptr, np.array([0, 1], dtype=np.int32), 2)
+    assert not oracle.check_csr(np.array([0, 1, 2], dtype=np.int32), np.array([0, 5], dtype=np.int32), 2)
+    assert oracle.check_csr(np.array([0, 1, 2], dtype=np.int32), np.array([0, 1], dtype=np.int32), 2)
+    Q = np.zeros((2, 1, 1), np.float32)
+    with pytest.raises(oracle.OracleError):
+        oracle.sparse_mha(indptr, np.array([0, 1], dtype=np.int32), Q, Q, Q, 1.0)
+
+
+# --------------------------------------------------------------------------
+# mutation checks: each planted mistake must fail a pin
+# --------------------------------------------------------------------------
+MUTATIONS = {
+    # q_i . k_j with the operands' node indices swapped (transposed product)
+    "swap_qk_nodes": ("const float* q = Q + i * HD + (int64_t)h * D;",
+                      "const float* q = Q + (int64_t)indices[beg] * HD + (int64_t)h * D;"),
+    "drop_scale": ("l[k] = scale * dot;", "l[k] = dot;"),
+    "wrong_head_offset": ("const float* kj = K + j * HD + (int64_t)h * D;",
+                          "const float* kj = K + j * HD;"),
+    "values_from_destination": ("const float* vj = V + j * HD + (int64_t)h * D;",
+                                "const float* vj = V + i * HD + (int64_t)h * D;"),
+    "sign_error": ("p[k] = exp(l[k] - m);", "p[k] = exp(m - l[k]);"),
+    "no_normalisation": ("for (int64_t k = 0; k < deg; ++k) p[k] /= S;", ""),
+    "last_edge_dropped": ("for (int64_t k = 0; k < deg; ++k) {\n                const int64_t j = indices[beg + k];\n                const float* vj",
+                          "for (int64_t k = 0; k + 1 < deg; ++k) {\n                const int64_t j = indices[beg + k];\n                const float* vj"),
+}
+
+
+def _compile_mutant(src_text, tmpdir, name):
+    path = os.path.join(tmpdir, name + ".c")
+    with open(path, "w") as f:
+        f.write(src_text)
+    so = os.path.join(tmpdir, name + ".so")
+    subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", path, "-o", so, "-lm"], check=True)
+    lib = ctypes.CDLL(so)
+    i64, i32, vp, dbl = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_double
+    lib.gto_sparse_mha_rows.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, dbl, vp, i64, vp, vp, vp]
+    lib.gto_sparse_mha_rows.restype = ctypes.c_int
+    return lib
+
+
+def _run_mutant(lib, indptr, indices, Q, K, V, scale):
+    N, H, D = Q.shape
+    out = np.zeros((N, H, D))
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    indptr = np.ascontiguousarray(indptr, np.int32)
+    indices = np.ascontiguousarray(indices, np.int32)
+    rc = lib.gto_sparse_mha_rows(N, int(indptr[-1]), H, D, p(indptr), p(indices), p(Q), p(K), p(V),
+                                 float(scale), None, N, p(out), None, None)
+    assert rc == 0
+    return out
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistakes(name):
+    text = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    old, new = MUTATIONS[name]
+    # plant the mistake in the sparse routine (the first occurrence)
+    assert 0 <= text.find(old) < text.index("int gto_dense_attention("), f"anchor for {name} missing"
+    mutant = text.replace(old, new, 1)
+    rng = np.random.default_rng(1234)
+    n, H, D = 17, 3, 5
+    pick = rng.choice(n * n, size=80, replace=False)
+    src, dst = pick // n, pick % n
+    indptr, indices = wl.csr_by_destination(src, dst, n)
+    Q, K, V = _rand_feats(rng, n, H, D)
+    ref = brute_force(src, dst, n, Q, K, V, 0.7)
+    with tempfile.TemporaryDirectory() as td:
+        lib = _compile_mutant(mutant, td, name)
+        got = _run_mutant(lib, indptr, indices, Q, K, V, 0.7)
+    assert not np.allclose(got, ref, rtol=1e-9, atol=1e-12), f"pin missed mutation {name}"

@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark: sparse multi-head attention forward on GB300.
+
+One step = one call of ``gtattn_fwd`` (degree binning on the fly, the fused
+row kernel, the split-row combine) over the whole R-MAT graph (2^20 nodes,
+~17.1M entries, 4 heads x 32, bf16) with inputs resident in HBM.  Prints one
+JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--path fwd|plan|probs] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload
+(weak scaling, no collective on the data path); the timed region is
+bracketed by a barrier and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "sparse MHA fwd edge·heads/sec and achieved HBM GB/s (% of roofline), 1 GB300"
+UNIT = "edge·heads/s"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def compulsory_bytes(N, nnz, H, D, esize):
+    """Algorithmic bytes of one forward: indptr + indices + Q + out + every
+    K/V row gather (each edge reads one K row and one V row)."""
+    row = H * D * esize
+    return 4 * (N + 1) + 4 * nnz + 2 * N * row + 2 * nnz * row
+
+
+def unique_bytes(N, nnz, H, D, esize):
+    """Each array touched once: the DRAM floor when L2 holds every reuse."""
+    row = H * D * esize
+    return 4 * (N + 1) + 4 * nnz + 4 * N * row
+
+
+def dense_flops(n_blocks, n, H, D):
+    return 4.0 * n * n * D * H * n_blocks
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def ncu_traffic(kernel_tag: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel source changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m_b or not m_h:
+        return None
+    src = os.path.join(ROOT, "graph_transformer_sparse_gb300", "csrc", "rows.cu")
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != m_h.group(1):
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gtattn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, group=None) -> float:
+    """Max of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def reduce_sum(value: float, group=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item())
+
+
+def job_throughput(local_units: float, local_ms: float, group=None):
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    total_units = reduce_sum(local_units, group)
+    worst_ms = reduce_max(local_ms, group)
+    return total_units / (worst_ms / 1e3), worst_ms, total_units
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def device_inputs(w, dev):
+    import torch
+    d = dict(indptr=torch.from_numpy(w.indptr).to(dev), indices=torch.from_numpy(w.indices).to(dev))
+    for name in ("Q", "K", "V"):
+        if w.dtype == "bf16":
+            d[name] = torch.from_numpy(w.bits[name].view(np.int16)).to(dev).view(torch.bfloat16)
+        else:
+            d[name] = torch.from_numpy(getattr(w, name)).to(dev)
+    d["out"] = torch.empty_like(d["Q"])
+    return d
+
+
+def make_step(w, d, path, gt, plan=None, probs_bufs=None):
+    dt = gt.GTATTN_BF16 if w.dtype == "bf16" else gt.GTATTN_F32
+    if path == "fwd":
+        return lambda: gt.gtattn_fwd(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], w.N, w.nnz,
+                                     w.H, w.D, w.scale, dt)
+    if path == "plan":
+        return lambda: gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"],
+                                          w.H, w.D, w.scale, dt)
+    if path == "probs":
+        lg, pr = probs_bufs
+        return lambda: gt.gtattn_fwd_probs(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], lg, pr,
+                                           w.N, w.nnz, w.H, w.D, w.scale, dt)
+    raise ValueError(path)
+
+
+def time_steps(step, steps, flush):
+    """Per-step CUDA-event times (ms) on the current stream, L2 flushed
+    before every step (outside the events)."""
+    import torch
+    s = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush.zero_()
+        a.record(s)
+        step()
+        b.record(s)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_gpu_workload(w, path, steps, warmup, gt, dev, flush, want_profile=True, detect_dense=False):
+    import torch
+    d = device_inputs(w, dev)
+    plan = None
+    probs_bufs = None
+    if path == "plan":
+        plan = gt.Plan(d["indptr"], d["indices"], detect_dense=detect_dense)
+    if path == "probs":
+        probs_bufs = (torch.empty(w.nnz, w.H, device=dev), torch.empty(w.nnz, w.H, device=dev))
+    step = make_step(w, d, path, gt, plan, probs_bufs)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    times = time_steps(step, steps, flush)
+    prof = None
+    if want_profile:
+        gt.gtattn_profile_enable(True)
+        gt.gtattn_profile_read(reset=True)
+        time_steps(step, steps, flush)
+        prof = gt.gtattn_profile_read(reset=True)
+        gt.gtattn_profile_enable(False)
+    info = plan.info() if plan is not None else None
+    return w, d, step, times, prof, info, plan
+
+
+def e2e_measure(w, gt, dev, steps, warmup):
+    """Same metric end to end through the C ABI with host (pinned) buffers:
+    H2D of the step's inputs, gtattn_fwd, D2H of the output, every step."""
+    import torch
+    host = {}
+    host["indptr"] = torch.from_numpy(w.indptr).pin_memory()
+    host["indices"] = torch.from_numpy(w.indices).pin_memory()
+    for name in ("Q", "K", "V"):
+        if w.dtype == "bf16":
+            host[name] = torch.from_numpy(w.bits[name].view(np.int16)).view(torch.bfloat16).pin_memory()
+        else:
+            host[name] = torch.from_numpy(getattr(w, name)).pin_memory()
+    host_out = torch.empty(host["Q"].shape, dtype=host["Q"].dtype).pin_memory()
+    dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    dout = torch.empty_like(dbuf["Q"])
+    dt = gt.GTATTN_BF16 if w.dtype == "bf16" else gt.GTATTN_F32
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def step():
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        gt.gtattn_fwd(dbuf["indptr"], dbuf["indices"], dbuf["Q"], dbuf["K"], dbuf["V"], dout, w.N, w.nnz, w.H,
+                      w.D, w.scale, dt)
+        host_out.copy_(dout, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(steps):
+        step()
+    b.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return ms, h2d, d2h
+
+
+def cpu_baseline(w, budget_s=20.0):
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample
+    of rows of the same workload (random rows, so the degree mix matches)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    deg = np.diff(w.indptr)
+    # size the sample for about `budget_s` seconds: probe a small sample first
+    probe = rng.choice(w.N, size=min(w.N, 2000), replace=False)
+    t0 = time.perf_counter()
+    oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, rows=probe, threads=cores)
+    t_probe = max(time.perf_counter() - t0, 1e-3)
+    rate = (deg[probe].sum() + len(probe)) / t_probe
+    want = rate * budget_s * 0.5
+    frac = min(1.0, want / (deg.sum() + w.N))
+    rows = np.sort(rng.choice(w.N, size=max(1, int(frac * w.N)), replace=False))
+    t0 = time.perf_counter()
+    oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, rows=rows, threads=cores)
+    dt = time.perf_counter() - t0
+    eh = float(deg[rows].sum()) * w.H
+    return dict(value=eh / dt, unit=UNIT, cores=cores, kind="oracle",
+                sample=f"{len(rows)} random rows of {w.N} ({eh / (w.nnz * w.H):.1%} of the edge-heads), "
+                       f"{dt:.1f} s, fp64 C oracle split over {cores} host threads")
+
+
+def gpu_arm(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    import graph_transformer_sparse_gb300 as gt
+    gt.build()
+    gt.load()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peaks = measured_peaks()
+
+    name = args.workload
+    w = wl.make_workload(name)
+    barrier()
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        w, d, step, times, prof, info, plan = run_gpu_workload(w, args.path, args.steps, args.warmup, gt, dev,
+                                                               flush, detect_dense=(name == "dense_blocks"))
+        torch.cuda.synchronize()
+        barrier()
+    clocks = clk.summary()
+    esize = 2 if w.dtype == "bf16" else 4
+    local_ms = sum(times)
+    units = float(w.nnz) * w.H * args.steps
+    value, worst_ms, _ = job_throughput(units, local_ms)
+    ms_per_step = worst_ms / args.steps
+    cbytes = compulsory_bytes(w.N, w.nnz, w.H, w.D, esize)
+    ubytes = unique_bytes(w.N, w.nnz, w.H, w.D, esize)
+
+    rows_ms = prof["rows"]["ms"] / max(prof["rows"]["groups"], 1)
+    launches_per_step = sum(v["launches"] for v in prof.values()) / args.steps
+    achieved = cbytes / (rows_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "k_rows_vec (fused row kernel)", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": ncu_traffic("k_rows_vec", name),
+                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": cbytes, "unique_bytes_floor": ubytes,
+                "kernel_ms": round(rows_ms, 5),
+                "kernel_shares": {k: round(v["ms"] / max(sum(x["ms"] for x in prof.values()), 1e-9), 4)
+                                  for k, v in prof.items() if v["launches"]}}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"{name}: {w.desc}", "N": w.N, "nnz": w.nnz, "H": w.H, "D": w.D,
+                   "path": {"fwd": "gtattn_fwd (binning on the fly + fused rows + combine)",
+                            "plan": "gtattn_fwd_plan (prebuilt plan)",
+                            "probs": "gtattn_fwd_probs (unfused SDDMM/softmax/SpMM)"}[args.path],
+                   "l2": "flushed before every timed step (512 MiB memset, outside the events)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "achieved_gbs_step": round(cbytes / (ms_per_step / 1e3) / 1e9, 1),
+        "hbm_frac_step": round(cbytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+        "roofline": roofline,
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "clocks": clocks,
+    }
+    if info is not None:
+        line["config"]["plan"] = {k: info[k] for k in ("n_long_rows", "n_chunks", "n_dense_blocks", "max_degree")}
+
+    if rank == 0 and not args.no_e2e:
+        e_ms, h2d, d2h = e2e_measure(w, gt, dev, max(2, min(args.steps, 5)), 1)
+        line["e2e"] = {"value": round(w.nnz * w.H / (e_ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
+    if rank == 0 and not args.no_extra:
+        extra = {}
+        for other, pth in (("erdos_renyi", "fwd"), ("molecules", "fwd"), ("tiny_random", "fwd"),
+                           ("dense_blocks", "plan"), ("rmat", "probs")):
+            if other == name and pth == args.path:
+                continue
+            try:
+                wo, _, _, t_o, p_o, inf_o, pl_o = run_gpu_workload(wl.make_workload(other), pth,
+                                                                   max(3, args.steps // 2), 3, gt, dev, flush,
+                                                                   detect_dense=True)
+            except Exception as exc:  # report, do not hide
+                extra[f"{other}/{pth}"] = {"error": str(exc)}
+                continue
+            ms = statistics.median(t_o)
+            es = 2 if wo.dtype == "bf16" else 4
+            cb = compulsory_bytes(wo.N, wo.nnz, wo.H, wo.D, es)
+            ent = {"ms": round(ms, 5), "edge_heads_per_s": round(wo.nnz * wo.H / (ms / 1e3), 1),
+                   "gbs_compulsory": round(cb / (ms / 1e3) / 1e9, 1),
+                   "hbm_frac": round(cb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                   "kernel_ms": {k: round(v["ms"] / max(v["groups"], 1), 5) for k, v in p_o.items() if v["groups"]}}
+            if other == "dense_blocks" and inf_o and inf_o.get("n_dense_blocks"):
+                tf = dense_flops(inf_o["n_dense_blocks"], 512, wo.H, wo.D) / (ms / 1e3) / 1e12
+                ent["tflops"] = round(tf, 1)
+                ent["tensor_frac"] = round(tf / peaks["bf16_tflops"], 4)
+            extra[f"{other}/{pth}"] = ent
+            if pl_o is not None:
+                pl_o.close()
+        line["per_workload"] = extra
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if plan is not None:
+        plan.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def reference_arm(args):
+    """The oracle as the reference arm: timed on the host cores on a bounded
+    sample per step; rank 0 only."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = wl.make_workload(args.workload)
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    deg = np.diff(w.indptr)
+    rows = np.sort(rng.choice(w.N, size=min(w.N, max(1, w.N // 64)), replace=False))
+    eh = float(deg[rows].sum()) * w.H
+    for _ in range(args.warmup):
+        oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, rows=rows[: len(rows) // 8 + 1],
+                          threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, rows=rows, threads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = eh / dt
+    sample = (f"{len(rows)} random rows of {w.N} per step ({eh / (w.nnz * w.H):.2%} of the edge-heads), "
+              f"fp64 C oracle over {cores} host threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": f"{args.workload}: {w.desc}", "N": w.N, "nnz": w.nnz,
+                                             "H": w.H, "D": w.D, "path": "fp64 CPU oracle"},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="rmat", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

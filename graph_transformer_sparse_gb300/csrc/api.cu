@@ -1,0 +1,367 @@
+// api.cu -- the C ABI: argument checks, temporaries, dispatch.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "dense.cuh"
+#include "plan.cuh"
+#include "rows.cuh"
+
+namespace gt {
+
+static thread_local char g_last_error[256] = "";
+
+void set_last_error(const char* msg) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg ? msg : "");
+}
+
+gtattn_status cuda_status(cudaError_t e) {
+    set_last_error(cudaGetErrorString(e));
+    if (e == cudaErrorMemoryAllocation) return GTATTN_ERR_NO_MEMORY;
+    return GTATTN_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+
+int num_sms() {
+    static int cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// One library-owned memory pool per device; freed blocks stay cached in the
+// pool (release threshold: unlimited) so per-call temporaries cost no
+// driver allocation after the first call.
+cudaMemPool_t pool() {
+    static std::mutex mu;
+    static cudaMemPool_t pools[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> g(mu);
+    if (!pools[dev]) {
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess) return nullptr;
+        uint64_t thresh = ~0ull;
+        cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &thresh);
+        pools[dev] = p;
+    }
+    return pools[dev];
+}
+
+gtattn_status pool_alloc(void** p, size_t bytes, cudaStream_t s) {
+    *p = nullptr;
+    cudaMemPool_t mp = pool();
+    if (!mp) return GTATTN_ERR_CUDA;
+    cudaError_t e = cudaMallocFromPoolAsync(p, std::max<size_t>(bytes, 256), mp, s);
+    return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+}
+
+void pool_free(void* p, cudaStream_t s) {
+    if (p) cudaFreeAsync(p, s);
+}
+
+// ---------------------------------------------------------------------------
+// benchmark instrumentation
+// ---------------------------------------------------------------------------
+struct ProfRecord {
+    int cat;
+    cudaEvent_t a, b;
+};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<ProfRecord> g_prof;
+static int g_prof_launches[GTATTN_KCAT_COUNT] = {};
+
+ProfScope::ProfScope(int category, int launches, cudaStream_t s) : cat_(category), s_(s), start_(nullptr) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    if (!g_prof_on) return;
+    g_prof_launches[category] += launches;
+    cudaEvent_t a;
+    if (cudaEventCreate(&a) != cudaSuccess) return;
+    cudaEventRecord(a, s);
+    start_ = a;
+}
+
+ProfScope::~ProfScope() {
+    if (!start_) return;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    cudaEvent_t b;
+    if (cudaEventCreate(&b) != cudaSuccess) return;
+    cudaEventRecord(b, s_);
+    g_prof.push_back(ProfRecord{cat_, static_cast<cudaEvent_t>(start_), b});
+}
+
+static size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Checks shared by the forward entry points.
+static gtattn_status check_fwd(const int32_t* indptr, const int32_t* indices, const void* Q,
+                               const void* K, const void* V, const void* out, int64_t N, int64_t nnz,
+                               int H, int D, gtattn_dtype dtype) {
+    if (N < 0 || nnz < 0 || N >= (1ll << 31) - 1 || nnz >= (1ll << 31) - 1) return GTATTN_ERR_INVALID_ARG;
+    if (H < 1 || D < 1 || (int64_t)H * D > kMaxHD) return GTATTN_ERR_INVALID_ARG;
+    if (dtype != GTATTN_F32 && dtype != GTATTN_BF16) return GTATTN_ERR_INVALID_ARG;
+    if (!indptr) return GTATTN_ERR_INVALID_ARG;
+    if (N > 0 && (!Q || !out)) return GTATTN_ERR_INVALID_ARG;
+    if (nnz > 0 && (!indices || !K || !V)) return GTATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(indptr) | reinterpret_cast<uintptr_t>(indices)) & 3u)
+        return GTATTN_ERR_INVALID_ARG;
+    const uintptr_t esz = dtype == GTATTN_BF16 ? 2 : 4;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
+    if (al & (esz - 1)) return GTATTN_ERR_INVALID_ARG;
+    return GTATTN_OK;
+}
+
+// Stream-ordered temporaries of a plan-less call: one pool block carved up.
+struct Scratch {
+    void* base = nullptr;
+    TaskLists lists{};
+    Partials part{};
+    float* logits = nullptr;
+    float* probs = nullptr;
+};
+
+static gtattn_status scratch_alloc(int64_t N, int64_t nnz, int H, int HD, int long_min, int chunk,
+                                   bool need_logits, bool need_probs, Scratch* sc, int** hdr,
+                                   int** rows, int2** chunks, int2** longs, cudaStream_t s) {
+    int64_t n_long = 0, n_chunks = 0;
+    worst_case_sizes(N, nnz, long_min, chunk, &n_long, &n_chunks);
+    size_t off = 0;
+    const size_t o_hdr = off; off = align_up(off + sizeof(int) * HdrLayout::kWords);
+    const size_t o_rows = off; off = align_up(off + sizeof(int) * (size_t)N);
+    const size_t o_chunks = off; off = align_up(off + sizeof(int2) * (size_t)n_chunks);
+    const size_t o_longs = off; off = align_up(off + sizeof(int2) * (size_t)n_long);
+    const size_t o_m = off; off = align_up(off + sizeof(float) * (size_t)n_chunks * H);
+    const size_t o_s = off; off = align_up(off + sizeof(float) * (size_t)n_chunks * H);
+    const size_t o_acc = off; off = align_up(off + sizeof(float) * (size_t)n_chunks * HD);
+    const size_t o_lg = off; if (need_logits) off = align_up(off + sizeof(float) * (size_t)nnz * H);
+    const size_t o_pr = off; if (need_probs) off = align_up(off + sizeof(float) * (size_t)nnz * H);
+    GT_TRY(pool_alloc(&sc->base, off, s));
+    char* b = static_cast<char*>(sc->base);
+    *hdr = reinterpret_cast<int*>(b + o_hdr);
+    *rows = reinterpret_cast<int*>(b + o_rows);
+    *chunks = reinterpret_cast<int2*>(b + o_chunks);
+    *longs = reinterpret_cast<int2*>(b + o_longs);
+    sc->part.m = reinterpret_cast<float*>(b + o_m);
+    sc->part.s = reinterpret_cast<float*>(b + o_s);
+    sc->part.acc = reinterpret_cast<float*>(b + o_acc);
+    if (need_logits) sc->logits = reinterpret_cast<float*>(b + o_lg);
+    if (need_probs) sc->probs = reinterpret_cast<float*>(b + o_pr);
+    sc->lists = TaskLists{*hdr, *rows, *chunks, *longs, chunk, 1};
+    return GTATTN_OK;
+}
+
+static RowParams make_params(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                             const void* V, void* out, int64_t N, int H, int D, float qscale,
+                             const RowChoice& c, const TaskLists& L, const Partials& part) {
+    RowParams p{};
+    p.indptr = indptr;
+    p.indices = indices;
+    p.Q = Q;
+    p.K = K;
+    p.V = V;
+    p.out = out;
+    p.qscale = qscale;
+    p.N = (int)N;
+    p.H = H;
+    p.D = D;
+    p.HD = H * D;
+    p.G = c.G;
+    p.lph = c.lph;
+    p.lists = L;
+    p.part = part;
+    return p;
+}
+
+}  // namespace gt
+
+using namespace gt;
+
+extern "C" const char* gtattn_status_string(gtattn_status s) {
+    switch (s) {
+        case GTATTN_OK: return "ok";
+        case GTATTN_ERR_INVALID_ARG: return "invalid argument";
+        case GTATTN_ERR_BAD_CSR: return "malformed CSR";
+        case GTATTN_ERR_UNSUPPORTED: return "unsupported";
+        case GTATTN_ERR_CUDA: return "CUDA error";
+        case GTATTN_ERR_NO_MEMORY: return "out of memory";
+        case GTATTN_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+extern "C" const char* gtattn_last_error(void) { return g_last_error; }
+
+extern "C" gtattn_status gtattn_profile_enable(int on) {
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    g_prof_on = on != 0;
+    return GTATTN_OK;
+}
+
+extern "C" gtattn_status gtattn_profile_read(gtattn_profile* out, int reset) {
+    if (!out) return GTATTN_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    std::memset(out, 0, sizeof(*out));
+    gtattn_status st = GTATTN_OK;
+    for (auto& r : g_prof) {
+        float ms = 0.f;
+        cudaError_t e = cudaEventSynchronize(r.b);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
+        if (e != cudaSuccess) st = cuda_status(e);
+        out->ms[r.cat] += ms;
+        out->groups[r.cat] += 1;
+    }
+    for (int c = 0; c < GTATTN_KCAT_COUNT; ++c) out->launches[c] = g_prof_launches[c];
+    if (reset) {
+        for (auto& r : g_prof) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+        g_prof.clear();
+        std::memset(g_prof_launches, 0, sizeof(g_prof_launches));
+    }
+    return st;
+}
+
+extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indices, const void* Q,
+                                    const void* K, const void* V, void* out, int64_t N, int64_t nnz,
+                                    int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
+    GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    RowChoice c;
+    if (!choose_row_kernel(H, D, dtype, Q, K, V, out, GTATTN_KERNEL_AUTO, &c)) return GTATTN_ERR_UNSUPPORTED;
+    if (N == 0) return GTATTN_OK;
+    gtattn_plan_opts o;
+    resolve_opts(nullptr, &o);
+    Scratch sc;
+    int *hdr, *rows;
+    int2 *chunks, *longs;
+    GT_TRY(scratch_alloc(N, nnz, H, H * D, o.long_row_min, o.chunk_edges, false, false, &sc, &hdr, &rows,
+                         &chunks, &longs, stream));
+    gtattn_status st;
+    {
+        ProfScope ps(GTATTN_KCAT_BIN, 3, stream);
+        st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
+    }
+    RowParams p = make_params(indptr, indices, Q, K, V, out, N, H, D, scale * kLog2e, c, sc.lists, sc.part);
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+        st = launch_rows(kFused, dtype, c, p, stream);
+    }
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
+        st = launch_combine(kFused, dtype, p, stream);
+    }
+    pool_free(sc.base, stream);
+    return st;
+}
+
+extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t* indptr,
+                                         const int32_t* indices, const void* Q, const void* K,
+                                         const void* V, void* out, int H, int D, float scale,
+                                         gtattn_dtype dtype, cudaStream_t stream) {
+    if (!plan) return GTATTN_ERR_INVALID_ARG;
+    const int64_t N = plan->N, nnz = plan->nnz;
+    GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    RowChoice c;
+    if (!choose_row_kernel(H, D, dtype, Q, K, V, out, plan->opts.kernel, &c)) return GTATTN_ERR_UNSUPPORTED;
+    if (N == 0) return GTATTN_OK;
+    const int HD = H * D;
+    const int n_chunks = plan->hdr_host[HdrLayout::kChunks];
+    const int n_long = plan->hdr_host[HdrLayout::kLong];
+    const int n_blocks = plan->hdr_host[HdrLayout::kDenseBlocks];
+    const bool dense = n_blocks > 0 && dense_supported(H, D, dtype, Q, K, V, out);
+
+    Partials part{};
+    if (n_chunks > 0) {
+        const size_t need = align_up(sizeof(float) * (size_t)n_chunks * H) * 2 +
+                            align_up(sizeof(float) * (size_t)n_chunks * HD);
+        if (plan->ws_bytes < need) {
+            pool_free(plan->ws, stream);
+            plan->ws = nullptr;
+            plan->ws_bytes = 0;
+            GT_TRY(pool_alloc(&plan->ws, need, stream));
+            plan->ws_bytes = need;
+        }
+        char* b = static_cast<char*>(plan->ws);
+        part.m = reinterpret_cast<float*>(b);
+        part.s = reinterpret_cast<float*>(b + align_up(sizeof(float) * (size_t)n_chunks * H));
+        part.acc = reinterpret_cast<float*>(b + 2 * align_up(sizeof(float) * (size_t)n_chunks * H));
+    }
+    TaskLists L{plan->hdr, plan->rows, plan->chunks, plan->longs, plan->opts.chunk_edges, dense ? 0 : 1};
+    RowParams p = make_params(indptr, indices, Q, K, V, out, N, H, D, scale * kLog2e, c, L, part);
+    gtattn_status st = GTATTN_OK;
+    if (dense) {
+        ProfScope ps(GTATTN_KCAT_DENSE, 1, stream);
+        st = launch_dense(plan->blocks, n_blocks, Q, K, V, out, H, D, scale, stream);
+    }
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+        st = launch_rows(kFused, dtype, c, p, stream);
+    }
+    if (st == GTATTN_OK && n_long > 0) {
+        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
+        st = launch_combine(kFused, dtype, p, stream);
+    }
+    return st;
+}
+
+extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* indices, const void* Q,
+                                          const void* K, const void* V, void* out, float* logits,
+                                          float* probs, int64_t N, int64_t nnz, int H, int D, float scale,
+                                          gtattn_dtype dtype, cudaStream_t stream) {
+    GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(probs)) & 3u)
+        return GTATTN_ERR_INVALID_ARG;
+    RowChoice c;
+    if (!choose_row_kernel(H, D, dtype, Q, K, V, out, GTATTN_KERNEL_AUTO, &c)) return GTATTN_ERR_UNSUPPORTED;
+    if (N == 0) return GTATTN_OK;
+    gtattn_plan_opts o;
+    resolve_opts(nullptr, &o);
+    Scratch sc;
+    int *hdr, *rows;
+    int2 *chunks, *longs;
+    GT_TRY(scratch_alloc(N, nnz, H, H * D, o.long_row_min, o.chunk_edges, logits == nullptr,
+                         probs == nullptr, &sc, &hdr, &rows, &chunks, &longs, stream));
+    float* lg = logits ? logits : sc.logits;
+    float* pr = probs ? probs : sc.probs;
+    gtattn_status st;
+    {
+        ProfScope ps(GTATTN_KCAT_BIN, 3, stream);
+        st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
+    }
+    RowParams p = make_params(indptr, indices, Q, K, V, out, N, H, D, scale, c, sc.lists, sc.part);
+    p.logits = lg;
+    p.probs = pr;
+    // (1) SDDMM: logits
+    if (st == GTATTN_OK && nnz > 0) {
+        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+        st = launch_rows(kSddmm, dtype, c, p, stream);
+    }
+    // (2) edge softmax: probs
+    if (st == GTATTN_OK && nnz > 0) {
+        ProfScope ps(GTATTN_KCAT_SOFTMAX, 2, stream);
+        st = launch_edge_softmax(indptr, (int)N, H, o.long_row_min, sc.lists, lg, pr, stream);
+    }
+    // (3) SpMM: out
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+        st = launch_rows(kSpmm, dtype, c, p, stream);
+    }
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
+        st = launch_combine(kSpmm, dtype, p, stream);
+    }
+    pool_free(sc.base, stream);
+    return st;
+}

@@ -1,0 +1,146 @@
+// common.cuh -- internal definitions shared by the library's CUDA sources.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "gtattn.h"
+
+namespace gt {
+
+// ---------------------------------------------------------------------------
+// Degree buckets.  Rows with degree 0..32 get one bucket per degree; larger
+// degrees fall into roughly x1.5 steps.  Bucket ids grow with degree; row
+// lists are laid out from the highest bucket down so heavy rows start first.
+// ---------------------------------------------------------------------------
+constexpr int kExactBuckets = 33;
+constexpr int kLogBuckets = 15;
+constexpr int kNumBuckets = kExactBuckets + kLogBuckets;   // 48
+constexpr int kMaxHD = 1024;
+constexpr int kDenseTile = 128;   // dense blocks: size multiple of this
+
+// upper bounds (inclusive) of the log buckets
+__host__ __device__ inline int log_bucket_hi(int k) {
+    switch (k) {
+        case 0: return 48;    case 1: return 64;    case 2: return 96;    case 3: return 128;
+        case 4: return 192;   case 5: return 256;   case 6: return 384;   case 7: return 512;
+        case 8: return 768;   case 9: return 1024;  case 10: return 1536; case 11: return 2048;
+        case 12: return 3072; case 13: return 4096; default: return 0x7fffffff;
+    }
+}
+
+__host__ __device__ inline int bucket_of(int deg) {
+    if (deg < kExactBuckets) return deg;
+    int k = 0;
+    while (k < kLogBuckets - 1 && deg > log_bucket_hi(k)) ++k;
+    return kExactBuckets + k;
+}
+
+__host__ __device__ inline int bucket_lo(int b) {
+    if (b < kExactBuckets) return b;
+    return b == kExactBuckets ? kExactBuckets : log_bucket_hi(b - kExactBuckets - 1) + 1;
+}
+
+// Device-side plan header (int32 words).
+struct HdrLayout {
+    static constexpr int kLong = 0;          // rows split into chunks
+    static constexpr int kChunks = 1;        // chunks over split rows
+    static constexpr int kDenseRows = 2;     // rows in the dense segment
+    static constexpr int kDenseBlocks = 3;   // complete blocks found
+    static constexpr int kMaxDeg = 4;
+    static constexpr int kCount = 8;                           // [NB] rows per bucket
+    static constexpr int kOffset = kCount + kNumBuckets;       // [NB] start in row list
+    static constexpr int kCursor = kOffset + kNumBuckets;      // [NB] scatter cursors
+    static constexpr int kCurLong = kCursor + kNumBuckets;     // cursor: long rows
+    static constexpr int kCurChunk = kCurLong + 1;             // cursor: chunks
+    static constexpr int kCurDense = kCurChunk + 1;            // cursor: dense rows
+    static constexpr int kDenseSeg = kCurDense + 1;            // start of dense segment in row list
+    static constexpr int kWords = kDenseSeg + 8;
+};
+
+// Work lists consumed by the row kernels.
+struct TaskLists {
+    const int* hdr;          // HdrLayout words (device)
+    const int* rows;         // bucketed row list, then the dense segment
+    const int2* chunks;      // (row, first entry) per chunk
+    const int2* longs;       // (row, first chunk) per split row
+    int chunk_edges;
+    int include_dense;       // 1: the dense segment is processed by the row kernels
+};
+
+// Split-row partial results: per chunk c, m[c*H+h], s[c*H+h] (log2 domain
+// running max and sum) and acc[c*HD + t].
+struct Partials {
+    float* m;
+    float* s;
+    float* acc;
+};
+
+enum Mode { kFused = 0, kSpmm = 1, kSddmm = 2 };
+
+// ---------------------------------------------------------------------------
+// small device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {   // 2^x, PTX ex2.approx (ftz)
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float load_elem(const float* p, int64_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16* p, int64_t i) {
+    return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void store_elem(float* p, int64_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void store_elem(__nv_bfloat16* p, int64_t i, float v) {
+    p[i] = __float2bfloat16_rn(v);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace gt
+
+// ---------------------------------------------------------------------------
+// host-side helpers (defined in api.cu)
+// ---------------------------------------------------------------------------
+namespace gt {
+gtattn_status cuda_status(cudaError_t e);
+void set_last_error(const char* msg);
+int num_sms();
+cudaMemPool_t pool();
+gtattn_status pool_alloc(void** p, size_t bytes, cudaStream_t s);
+void pool_free(void* p, cudaStream_t s);
+
+// Benchmark instrumentation: brackets a launch group with CUDA events when
+// profiling is enabled (see gtattn_profile_enable).
+class ProfScope {
+  public:
+    ProfScope(int category, int launches, cudaStream_t s);
+    ~ProfScope();
+  private:
+    int cat_;
+    cudaStream_t s_;
+    void* start_;
+};
+}  // namespace gt
+
+#define GT_CUDA(call)                                           \
+    do {                                                        \
+        cudaError_t _e = (call);                                \
+        if (_e != cudaSuccess) return gt::cuda_status(_e);      \
+    } while (0)
+
+#define GT_TRY(call)                                            \
+    do {                                                        \
+        gtattn_status _s = (call);                              \
+        if (_s != GTATTN_OK) return _s;                         \
+    } while (0)

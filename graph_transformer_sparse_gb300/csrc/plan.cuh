@@ -1,0 +1,35 @@
+// plan.cuh -- the plan object and the binning entry points used by api.cu.
+#pragma once
+
+#include "common.cuh"
+
+struct gtattn_plan {
+    int64_t N = 0, nnz = 0;
+    gtattn_plan_opts opts{};
+    int device = -1;
+    cudaStream_t stream = nullptr;          // stream the plan was built on
+    int* hdr = nullptr;                     // device header (HdrLayout words)
+    int hdr_host[gt::HdrLayout::kWords] = {};
+    int* rows = nullptr;                    // bucketed rows, then the dense segment
+    int2* chunks = nullptr;                 // (row, first entry) per chunk
+    int2* longs = nullptr;                  // (row, first chunk) per split row
+    int2* blocks = nullptr;                 // (first row, size) per dense block
+    int* dense_flag = nullptr;              // 1 for rows inside a dense block
+    mutable void* ws = nullptr;             // split-row partials workspace
+    mutable size_t ws_bytes = 0;
+};
+
+namespace gt {
+
+constexpr int kDefaultLongMin = 256;
+constexpr int kDefaultChunk = 256;
+
+void resolve_opts(const gtattn_plan_opts* in, gtattn_plan_opts* out);
+void worst_case_sizes(int64_t N, int64_t nnz, int long_min, int chunk, int64_t* n_long,
+                      int64_t* n_chunks);
+// Bins rows into the given arrays on stream `s` without synchronising:
+// zeroes the header, counts, lays out offsets and scatters rows/chunks.
+gtattn_status bin_rows(const int* indptr, int N, int long_min, int chunk, const int* dense_flag,
+                       int* hdr, int* rows, int2* chunks, int2* longs, cudaStream_t s);
+
+}  // namespace gt

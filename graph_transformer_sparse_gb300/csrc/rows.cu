@@ -1,0 +1,666 @@
+// rows.cu -- the sparse row kernels.
+//
+// One pass per row computes, for every head h, the logits
+// l_e = scale * <q_i, k_j> of the row's entries, their softmax and the
+// weighted sum of v_j ("Graph Transformer in a Nutshell", Sparse Multi-head
+// Attention: bsddmm -> softmax -> bspmm; "Efficient Sparse Transformer
+// implementation with DGL's builtin operators", TransLayer.forward:
+// u_dot_v -> edge_softmax -> u_mul_e_sum).  The pages run these as three
+// library calls with the per-edge scores in memory; here they are fused:
+// logits live in registers, the softmax is an online one (running max m and
+// sum s, rescaled by 2^(m_old - m_new) when the max grows), accumulation is
+// fp32.  Logits are kept in log2 units (q pre-multiplied by scale*log2(e))
+// so every exponential is one ex2.
+//
+// Lane layout of the vector kernel: a group of G lanes covers one feature row
+// of H*D elements, E = 16*VPL/sizeof(T) contiguous elements per lane, so a
+// gather of K_j or V_j is G 16-byte-vector loads per lane-group.  lph = D/E
+// lanes share a head and reduce their partial dot products with xor
+// shuffles.  A warp holds P = 32/G groups; a task assigns them as R rows x S
+// edge slots (R*S = P), chosen per degree bucket so short rows share a warp
+// and longer rows spread their edges over slots; slots merge their softmax
+// states with shuffles at the end.  Rows longer than the split threshold are
+// cut into chunks; a chunk writes its (m, s, acc) partial and the combine
+// kernel merges them: m* = max m_c, s* = sum s_c 2^(m_c-m*),
+// out = sum acc_c 2^(m_c-m*) / s*.
+#include "rows.cuh"
+
+#include <algorithm>
+#include <mutex>
+#include <unordered_map>
+
+namespace gt {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+enum SegKind { kSegChunk = 0, kSegRows = 1 };
+
+struct Seg {
+    int first_task;
+    int list_begin;
+    int count;
+    int R, S;
+    int kind;
+};
+
+constexpr int kMaxSegs = kNumBuckets + 2;
+
+// Builds the task table of a launch in shared memory (one warp).
+// P = edge slots per warp; U = edges per slot per loop iteration.
+__device__ void build_segments(const TaskLists& L, int P, int U, Seg* segs, int* nseg, int* total) {
+    __shared__ int h[HdrLayout::kWords];
+    for (int k = threadIdx.x; k < HdrLayout::kWords; k += blockDim.x) h[k] = L.hdr[k];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int t = 0, k = 0;
+        int nch = h[HdrLayout::kChunks];
+        if (nch > 0) { segs[k++] = Seg{t, 0, nch, 1, P, kSegChunk}; t += nch; }
+        for (int b = kNumBuckets - 1; b >= 0; --b) {
+            int cnt = h[HdrLayout::kCount + b];
+            if (cnt == 0) continue;
+            int lo = bucket_lo(b);
+            int need = (lo + U - 1) / U;          // slots to cover the row in one iteration
+            int S = 1;
+            while (S < need && S < P) S <<= 1;
+            int R = P / S;
+            segs[k++] = Seg{t, h[HdrLayout::kOffset + b], cnt, R, S, kSegRows};
+            t += (cnt + R - 1) / R;
+        }
+        if (L.include_dense) {
+            int cnt = h[HdrLayout::kDenseRows];
+            if (cnt > 0) { segs[k++] = Seg{t, h[HdrLayout::kDenseSeg], cnt, 1, P, kSegRows}; t += cnt; }
+        }
+        *nseg = k;
+        *total = t;
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte fragments
+// ---------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> { static constexpr int kPerVec = 4; };
+template <> struct Elem<__nv_bfloat16> { static constexpr int kPerVec = 8; };
+
+template <typename T, int VPL>
+struct Frag {
+    static constexpr int E = VPL * Elem<T>::kPerVec;
+    uint4 v[VPL];
+    __device__ __forceinline__ void load(const T* p) {
+        const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) v[k] = __ldg(q + k);
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) v[k] = make_uint4(0, 0, 0, 0);
+    }
+    __device__ __forceinline__ float get(int e) const {   // e compile-time after unrolling
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(v);
+        if constexpr (sizeof(T) == 4) return __uint_as_float(w[e]);
+        else return (e & 1) ? bf16hi(w[e >> 1]) : bf16lo(w[e >> 1]);
+    }
+};
+
+template <typename T, int E>
+__device__ __forceinline__ void store_frag(T* p, const float* x) {
+    if constexpr (sizeof(T) == 4) {
+        float4* q = reinterpret_cast<float4*>(p);
+#pragma unroll
+        for (int k = 0; k < E / 4; ++k) q[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+    } else {
+        uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+        for (int k = 0; k < E / 8; ++k)
+            q[k] = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
+                              pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// vector row kernel
+// ---------------------------------------------------------------------------
+template <typename T, int VPL, int MODE>
+__global__ void __launch_bounds__(256)
+k_rows_vec(RowParams p) {
+    using F = Frag<T, VPL>;
+    constexpr int E = F::E;
+    constexpr int U = (8 / VPL) > 0 ? (8 / VPL) : 1;
+
+    __shared__ Seg segs[kMaxSegs];
+    __shared__ int s_nseg, s_total;
+    const int G = p.G;
+    const int P = 32 / G;
+    build_segments(p.lists, P, U, segs, &s_nseg, &s_total);
+
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / G;
+    const int gl = lane - grp * G;
+    const int head = gl / p.lph;
+    const T* __restrict__ Q = static_cast<const T*>(p.Q);
+    const T* __restrict__ K = static_cast<const T*>(p.K);
+    const T* __restrict__ V = static_cast<const T*>(p.V);
+    T* __restrict__ O = static_cast<T*>(p.out);
+    const int64_t HD = p.HD;
+    const int lane_off = gl * E;
+
+    const int warps_total = gridDim.x * (blockDim.x >> 5);
+    int seg = 0;
+    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < s_total; t += warps_total) {
+        while (seg + 1 < s_nseg && segs[seg + 1].first_task <= t) ++seg;
+        const Seg sg = segs[seg];
+        const int S = sg.S;
+        const int r = grp / S;
+        const int sl = grp - r * S;
+        const int pos = (t - sg.first_task) * sg.R + r;
+        const bool valid = pos < sg.count;
+        int row = 0, beg = 0, end = 0, chunk = -1;
+        if (valid) {
+            if (sg.kind == kSegChunk) {
+                chunk = sg.list_begin + pos;
+                int2 c = p.lists.chunks[chunk];
+                row = c.x;
+                beg = c.y;
+                end = min(beg + p.lists.chunk_edges, p.indptr[row + 1]);
+            } else {
+                row = p.lists.rows[sg.list_begin + pos];
+                beg = p.indptr[row];
+                end = p.indptr[row + 1];
+            }
+        }
+        const int step = S * U;
+        int n_iter = (end - beg + step - 1) / step;
+        n_iter = __reduce_max_sync(kFull, n_iter);
+
+        float q[E];
+        if constexpr (MODE != kSpmm) {
+            F fq;
+            if (valid) fq.load(Q + (int64_t)row * HD + lane_off); else fq.zero();
+            const float qs = MODE == kFused ? p.qscale : 1.f;   // SDDMM scales at the store
+#pragma unroll
+            for (int e = 0; e < E; ++e) q[e] = fq.get(e) * qs;
+        }
+        float acc[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = 0.f;
+        float m = -INFINITY, ssum = 0.f;
+
+        for (int it = 0; it < n_iter; ++it) {
+            const int e0 = beg + it * step + sl;
+            int j[U];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                int e = e0 + u * S;
+                ok[u] = e < end;
+                j[u] = ok[u] ? __ldg(p.indices + e) : 0;
+            }
+            float l[U];
+            if constexpr (MODE != kSpmm) {
+                F fk[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (ok[u]) fk[u].load(K + (int64_t)j[u] * HD + lane_off); else fk[u].zero();
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float d = 0.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) d = fmaf(q[e], fk[u].get(e), d);
+                    l[u] = d;
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    for (int o = 1; o < p.lph; o <<= 1) l[u] += __shfl_xor_sync(kFull, l[u], o);
+            }
+            if constexpr (MODE == kSddmm) {
+                if (gl % p.lph == 0) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (ok[u]) p.logits[(int64_t)(e0 + u * S) * p.H + head] = l[u] * p.qscale;
+                }
+            } else {
+                F fv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (ok[u]) fv[u].load(V + (int64_t)j[u] * HD + lane_off); else fv[u].zero();
+                }
+                if constexpr (MODE == kFused) {
+                    float mx = m;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        if (!ok[u]) l[u] = -INFINITY;
+                        mx = fmaxf(mx, l[u]);
+                    }
+                    const float mref = (mx == -INFINITY) ? 0.f : mx;
+                    const float c = ex2(m - mref);
+                    ssum *= c;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] *= c;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const float w = ex2(l[u] - mref);
+                        ssum += w;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, fv[u].get(e), acc[e]);
+                    }
+                    m = mx;
+                } else {   // kSpmm: weights are the given probabilities
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const float w = ok[u] ? p.probs[(int64_t)(e0 + u * S) * p.H + head] : 0.f;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, fv[u].get(e), acc[e]);
+                    }
+                }
+            }
+        }
+        if constexpr (MODE == kSddmm) continue;
+
+        // merge the S edge slots of each row (lanes G, 2G, ... apart)
+        for (int o = G; o < S * G; o <<= 1) {
+            if constexpr (MODE == kFused) {
+                const float m2 = __shfl_xor_sync(kFull, m, o);
+                const float s2 = __shfl_xor_sync(kFull, ssum, o);
+                const float M = fmaxf(m, m2);
+                const float Mref = (M == -INFINITY) ? 0.f : M;
+                const float c1 = ex2(m - Mref), c2 = ex2(m2 - Mref);
+                ssum = ssum * c1 + s2 * c2;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float a2 = __shfl_xor_sync(kFull, acc[e], o);
+                    acc[e] = acc[e] * c1 + a2 * c2;
+                }
+                m = M;
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] += __shfl_xor_sync(kFull, acc[e], o);
+            }
+        }
+        if (!valid || sl != 0) continue;
+        if (chunk >= 0) {
+            float* pa = p.part.acc + (int64_t)chunk * HD + lane_off;
+#pragma unroll
+            for (int k = 0; k < E / 4; ++k)
+                reinterpret_cast<float4*>(pa)[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+            if (MODE == kFused && gl % p.lph == 0) {
+                p.part.m[(int64_t)chunk * p.H + head] = m;
+                p.part.s[(int64_t)chunk * p.H + head] = ssum;
+            }
+        } else {
+            if constexpr (MODE == kFused) {
+                const float inv = ssum > 0.f ? 1.f / ssum : 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[e] = ssum > 0.f ? acc[e] * inv : 0.f;
+            }
+            store_frag<T, E>(O + (int64_t)row * HD + lane_off, acc);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// generic row kernel: any H, D with H*D <= 1024 and H <= 256.  One warp per
+// task; lane holds elements t = lane + 32k of the feature row; per-head dot
+// products are summed from shared memory by one lane per head.
+// ---------------------------------------------------------------------------
+constexpr int kGenWarps = 4;
+constexpr int kGenMaxH = 256;
+constexpr int kGenK = kMaxHD / 32;   // elements per lane
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kGenWarps * 32)
+k_rows_generic(RowParams p) {
+    __shared__ Seg segs[kMaxSegs];
+    __shared__ int s_nseg, s_total;
+    __shared__ float sm_prod[kGenWarps][kMaxHD];
+    __shared__ float sm_m[kGenWarps][kGenMaxH];
+    __shared__ float sm_s[kGenWarps][kGenMaxH];
+    __shared__ float sm_w[kGenWarps][kGenMaxH];
+    __shared__ float sm_c[kGenWarps][kGenMaxH];
+    build_segments(p.lists, 1, 1, segs, &s_nseg, &s_total);
+
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    const T* __restrict__ Q = static_cast<const T*>(p.Q);
+    const T* __restrict__ K = static_cast<const T*>(p.K);
+    const T* __restrict__ V = static_cast<const T*>(p.V);
+    T* __restrict__ O = static_cast<T*>(p.out);
+    const int H = p.H, D = p.D, HD = p.HD;
+    float* prod = sm_prod[wid];
+    float* hm = sm_m[wid];
+    float* hs = sm_s[wid];
+    float* hw = sm_w[wid];
+    float* hc = sm_c[wid];
+
+    const int warps_total = gridDim.x * kGenWarps;
+    int seg = 0;
+    for (int t = blockIdx.x * kGenWarps + wid; t < s_total; t += warps_total) {
+        while (seg + 1 < s_nseg && segs[seg + 1].first_task <= t) ++seg;
+        const Seg sg = segs[seg];
+        const int pos = t - sg.first_task;
+        int row, beg, end, chunk = -1;
+        if (sg.kind == kSegChunk) {
+            chunk = sg.list_begin + pos;
+            int2 c = p.lists.chunks[chunk];
+            row = c.x;
+            beg = c.y;
+            end = min(beg + p.lists.chunk_edges, p.indptr[row + 1]);
+        } else {
+            row = p.lists.rows[sg.list_begin + pos];
+            beg = p.indptr[row];
+            end = p.indptr[row + 1];
+        }
+        float q[kGenK], acc[kGenK];
+        const float qs = MODE == kFused ? p.qscale : 1.f;   // SDDMM scales at the store
+#pragma unroll
+        for (int k = 0; k < kGenK; ++k) {
+            const int el = lane + 32 * k;
+            q[k] = (MODE != kSpmm && el < HD) ? load_elem(Q, (int64_t)row * HD + el) * qs : 0.f;
+            acc[k] = 0.f;
+        }
+        for (int h = lane; h < H; h += 32) { hm[h] = -INFINITY; hs[h] = 0.f; }
+        __syncwarp();
+        for (int e = beg; e < end; ++e) {
+            const int64_t j = __ldg(p.indices + e);
+            if constexpr (MODE != kSpmm) {
+#pragma unroll
+                for (int k = 0; k < kGenK; ++k) {
+                    const int el = lane + 32 * k;
+                    if (el < HD) prod[el] = q[k] * load_elem(K, j * HD + el);
+                }
+                __syncwarp();
+            }
+            for (int h = lane; h < H; h += 32) {
+                float l = 0.f;
+                if constexpr (MODE != kSpmm)
+                    for (int d = 0; d < D; ++d) l += prod[h * D + d];
+                if constexpr (MODE == kSddmm) {
+                    p.logits[(int64_t)e * H + h] = l * p.qscale;
+                } else if constexpr (MODE == kFused) {
+                    const float mo = hm[h];
+                    const float mn = fmaxf(mo, l);
+                    const float c = ex2(mo - mn);
+                    const float w = ex2(l - mn);
+                    hs[h] = hs[h] * c + w;
+                    hm[h] = mn;
+                    hc[h] = c;
+                    hw[h] = w;
+                } else {
+                    hc[h] = 1.f;
+                    hw[h] = p.probs[(int64_t)e * H + h];
+                }
+            }
+            __syncwarp();
+            if constexpr (MODE != kSddmm) {
+#pragma unroll
+                for (int k = 0; k < kGenK; ++k) {
+                    const int el = lane + 32 * k;
+                    if (el < HD) {
+                        const int h = el / D;
+                        acc[k] = acc[k] * hc[h] + hw[h] * load_elem(V, j * HD + el);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        if constexpr (MODE == kSddmm) continue;
+        if (chunk >= 0) {
+#pragma unroll
+            for (int k = 0; k < kGenK; ++k) {
+                const int el = lane + 32 * k;
+                if (el < HD) p.part.acc[(int64_t)chunk * HD + el] = acc[k];
+            }
+            if (MODE == kFused)
+                for (int h = lane; h < H; h += 32) {
+                    p.part.m[(int64_t)chunk * H + h] = hm[h];
+                    p.part.s[(int64_t)chunk * H + h] = hs[h];
+                }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kGenK; ++k) {
+                const int el = lane + 32 * k;
+                if (el < HD) {
+                    float v = acc[k];
+                    if (MODE == kFused) {
+                        const float s = hs[el / D];
+                        v = s > 0.f ? v / s : 0.f;
+                    }
+                    store_elem(O, (int64_t)row * HD + el, v);
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// combine split-row partials: one block per split row
+// ---------------------------------------------------------------------------
+template <typename T, int MODE>
+__global__ void __launch_bounds__(256)
+k_combine(RowParams p) {
+    __shared__ float sM[kMaxHD];
+    __shared__ float sS[kMaxHD];
+    const int n_long = p.lists.hdr[HdrLayout::kLong];
+    const int H = p.H, D = p.D, HD = p.HD;
+    T* __restrict__ O = static_cast<T*>(p.out);
+    for (int li = blockIdx.x; li < n_long; li += gridDim.x) {
+        const int2 lr = p.lists.longs[li];
+        const int row = lr.x, c0 = lr.y;
+        const int deg = p.indptr[row + 1] - p.indptr[row];
+        const int nch = (deg + p.lists.chunk_edges - 1) / p.lists.chunk_edges;
+        if (MODE == kFused) {
+            for (int h = threadIdx.x; h < H; h += blockDim.x) {
+                float M = -INFINITY;
+                for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part.m[(int64_t)(c0 + c) * H + h]);
+                float S = 0.f;
+                for (int c = 0; c < nch; ++c)
+                    S += p.part.s[(int64_t)(c0 + c) * H + h] * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M);
+                sM[h] = M;
+                sS[h] = S;
+            }
+            __syncthreads();
+        }
+        for (int el = threadIdx.x; el < HD; el += blockDim.x) {
+            float v = 0.f;
+            if (MODE == kFused) {
+                const int h = el / D;
+                const float M = sM[h];
+                for (int c = 0; c < nch; ++c)
+                    v += p.part.acc[(int64_t)(c0 + c) * HD + el] * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M);
+                v = v / sS[h];
+            } else {
+                for (int c = 0; c < nch; ++c) v += p.part.acc[(int64_t)(c0 + c) * HD + el];
+            }
+            store_elem(O, (int64_t)row * HD + el, v);
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// unfused edge softmax: warp per ordinary row, block per split row
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(256)
+k_softmax_rows(const int* __restrict__ indptr, int N, int H, int long_min,
+               const float* __restrict__ logits, float* __restrict__ probs) {
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < N; i += warps) {
+        const int beg = indptr[i], end = indptr[i + 1];
+        const int deg = end - beg;
+        if (deg == 0 || deg > long_min) continue;
+        for (int h = 0; h < H; ++h) {
+            float m = -INFINITY;
+            for (int e = beg + lane; e < end; e += 32) m = fmaxf(m, logits[(int64_t)e * H + h]);
+            m = warp_max(m);
+            float s = 0.f;
+            for (int e = beg + lane; e < end; e += 32) s += expf(logits[(int64_t)e * H + h] - m);
+            s = warp_sum(s);
+            const float inv = 1.f / s;
+            for (int e = beg + lane; e < end; e += 32)
+                probs[(int64_t)e * H + h] = expf(logits[(int64_t)e * H + h] - m) * inv;
+        }
+    }
+}
+
+__device__ float block_reduce(float v, bool is_max, float* red) {
+    v = is_max ? warp_max(v) : warp_sum(v);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float r = is_max ? -INFINITY : 0.f;
+    for (int k = 0; k < nw; ++k) r = is_max ? fmaxf(r, red[k]) : r + red[k];
+    return r;
+}
+
+__global__ void __launch_bounds__(256)
+k_softmax_long(const int* __restrict__ indptr, const int* __restrict__ hdr, const int2* __restrict__ longs,
+               int H, const float* __restrict__ logits, float* __restrict__ probs) {
+    __shared__ float red[32];
+    const int n_long = hdr[HdrLayout::kLong];
+    for (int li = blockIdx.x; li < n_long; li += gridDim.x) {
+        const int row = longs[li].x;
+        const int beg = indptr[row], end = indptr[row + 1];
+        for (int h = 0; h < H; ++h) {
+            float m = -INFINITY;
+            for (int e = beg + threadIdx.x; e < end; e += blockDim.x) m = fmaxf(m, logits[(int64_t)e * H + h]);
+            m = block_reduce(m, true, red);
+            float s = 0.f;
+            for (int e = beg + threadIdx.x; e < end; e += blockDim.x) s += expf(logits[(int64_t)e * H + h] - m);
+            s = block_reduce(s, false, red);
+            const float inv = 1.f / s;
+            for (int e = beg + threadIdx.x; e < end; e += blockDim.x)
+                probs[(int64_t)e * H + h] = expf(logits[(int64_t)e * H + h] - m) * inv;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+bool choose_row_kernel(int H, int D, gtattn_dtype dt, const void* Q, const void* K, const void* V,
+                       const void* out, int force, RowChoice* c) {
+    const int esz = dt == GTATTN_BF16 ? 2 : 4;
+    const int HD = H * D;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
+    if (force != GTATTN_KERNEL_GENERIC && (al & 15u) == 0) {
+        const int per_vec = 16 / esz;
+        const int max_vpl = dt == GTATTN_BF16 ? 2 : 4;
+        for (int vpl = 1; vpl <= max_vpl; vpl <<= 1) {
+            const int E = vpl * per_vec;
+            if (D % E != 0) continue;
+            const int lph = D / E;
+            const int G = HD / E;
+            if (!is_pow2(lph) || !is_pow2(G) || G > 32) continue;
+            *c = RowChoice{RowKernel::kVector, vpl, G, lph};
+            return true;
+        }
+    }
+    if (force == GTATTN_KERNEL_VECTOR) return false;
+    if (H > kGenMaxH || HD > kMaxHD) return false;
+    *c = RowChoice{RowKernel::kGeneric, 0, 0, 0};
+    return true;
+}
+
+template <typename K>
+static int grid_persistent(K kernel, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::unordered_map<const void*, int> cache;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(reinterpret_cast<const void*>(kernel));
+    if (it != cache.end()) return it->second;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    int grid = per_sm * num_sms();
+    cache[reinterpret_cast<const void*>(kernel)] = grid;
+    return grid;
+}
+
+template <typename T, int MODE>
+static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
+    auto go = [&](auto kernel) {
+        kernel<<<grid_persistent(kernel, 256, 0), 256, 0, s>>>(p);
+        return cudaGetLastError();
+    };
+    cudaError_t e;
+    switch (vpl) {
+        case 1: e = go(k_rows_vec<T, 1, MODE>); break;
+        case 2: e = go(k_rows_vec<T, 2, MODE>); break;
+        case 4:
+            if constexpr (sizeof(T) == 4) { e = go(k_rows_vec<T, 4, MODE>); break; }
+            return GTATTN_ERR_UNSUPPORTED;
+        default: return GTATTN_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+}
+
+template <typename T>
+static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParams& p, cudaStream_t s) {
+    if (c.kind == RowKernel::kVector) {
+        switch (mode) {
+            case kFused: return launch_vec_t<T, kFused>(c.vpl, p, s);
+            case kSpmm: return launch_vec_t<T, kSpmm>(c.vpl, p, s);
+            case kSddmm: return launch_vec_t<T, kSddmm>(c.vpl, p, s);
+        }
+        return GTATTN_ERR_UNSUPPORTED;
+    }
+    auto go = [&](auto kernel) {
+        kernel<<<grid_persistent(kernel, kGenWarps * 32, 0), kGenWarps * 32, 0, s>>>(p);
+        return cudaGetLastError();
+    };
+    cudaError_t e;
+    switch (mode) {
+        case kFused: e = go(k_rows_generic<T, kFused>); break;
+        case kSpmm: e = go(k_rows_generic<T, kSpmm>); break;
+        default: e = go(k_rows_generic<T, kSddmm>); break;
+    }
+    return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+}
+
+gtattn_status launch_rows(Mode mode, gtattn_dtype dt, const RowChoice& c, const RowParams& p,
+                          cudaStream_t s) {
+    if (dt == GTATTN_BF16) return launch_rows_t<__nv_bfloat16>(mode, c, p, s);
+    return launch_rows_t<float>(mode, c, p, s);
+}
+
+gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cudaStream_t s) {
+    auto go = [&](auto kernel) {
+        kernel<<<grid_persistent(kernel, 256, 0), 256, 0, s>>>(p);
+        return cudaGetLastError();
+    };
+    cudaError_t e;
+    if (dt == GTATTN_BF16)
+        e = mode == kFused ? go(k_combine<__nv_bfloat16, kFused>) : go(k_combine<__nv_bfloat16, kSpmm>);
+    else
+        e = mode == kFused ? go(k_combine<float, kFused>) : go(k_combine<float, kSpmm>);
+    return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+}
+
+gtattn_status launch_edge_softmax(const int* indptr, int N, int H, int long_min, const TaskLists& L,
+                                  const float* logits, float* probs, cudaStream_t s) {
+    if (N == 0) return GTATTN_OK;
+    const int lm = long_min < 0 ? 0 : long_min;   // long_min -1: every non-empty row is split
+    k_softmax_rows<<<grid_persistent(k_softmax_rows, 256, 0), 256, 0, s>>>(indptr, N, H, lm, logits, probs);
+    k_softmax_long<<<grid_persistent(k_softmax_long, 256, 0), 256, 0, s>>>(indptr, L.hdr, L.longs, H,
+                                                                            logits, probs);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+}
+
+}  // namespace gt

@@ -1,0 +1,49 @@
+// rows.cuh -- launch interface of the row kernels (fused, SpMM, SDDMM modes),
+// the split-row combine and the unfused edge softmax.
+#pragma once
+
+#include "common.cuh"
+
+namespace gt {
+
+struct RowParams {
+    const int* indptr;
+    const int* indices;
+    const void* Q;
+    const void* K;
+    const void* V;
+    void* out;
+    const float* probs;     // SpMM mode: fp32 [nnz, H]
+    float* logits;          // SDDMM mode: fp32 [nnz, H]
+    float qscale;           // fused: scale*log2(e); SDDMM: scale
+    int N, H, D, HD;
+    int G, lph;             // vector kernel: lanes per feature row, lanes per head
+    TaskLists lists;
+    Partials part;
+};
+
+enum class RowKernel { kVector, kGeneric };
+
+struct RowChoice {
+    RowKernel kind;
+    int vpl;    // 16-byte vectors per lane (vector kernel)
+    int G, lph;
+};
+
+// Picks the row kernel for a shape; `force` is a gtattn_kernel value.
+// Returns false when no kernel supports the shape (or the forced one does not).
+bool choose_row_kernel(int H, int D, gtattn_dtype dt, const void* Q, const void* K, const void* V,
+                       const void* out, int force, RowChoice* c);
+
+// Launches the persistent row kernel over every task of `p.lists`.
+gtattn_status launch_rows(Mode mode, gtattn_dtype dt, const RowChoice& c, const RowParams& p,
+                          cudaStream_t s);
+
+// Combines split-row partials into `out` for every split row (mode kFused or kSpmm).
+gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cudaStream_t s);
+
+// Unfused edge softmax: probs[e,h] from logits[e,h] over each row's entries.
+gtattn_status launch_edge_softmax(const int* indptr, int N, int H, int long_min, const TaskLists& L,
+                                  const float* logits, float* probs, cudaStream_t s);
+
+}  // namespace gt

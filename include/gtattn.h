@@ -1,0 +1,224 @@
+/*
+ * gtattn.h -- C ABI of the GB300 sparse multi-head attention library.
+ *
+ * The operation (per CSR row i and head h):
+ *
+ *   out[i,h,:] = sum_{e in row i} p[e,h] * V[indices[e],h,:]
+ *   p[e,h]     = exp(l[e,h]) / sum_{e' in row i} exp(l[e',h])
+ *   l[e,h]     = scale * <Q[i,h,:], K[indices[e],h,:]>
+ *
+ * i.e. SparseAttn(Q, K, V, A) = softmax((Q K^T) o A / sqrt(d)) V from
+ * "Graph Transformer in a Nutshell" (section "Sparse Multi-head Attention",
+ * equation SparseAttn and SparseMHA.forward: bsddmm, sparse softmax over the
+ * last sparse dimension, bspmm), in the destination-row orientation of
+ * "Efficient Sparse Transformer implementation with DGL's builtin
+ * operators" (TransLayer.forward: u_dot_v, edge_softmax of e/sqrt(d_qkv),
+ * u_mul_e_sum).  The softmax runs over the row's stored entries only
+ * (non-edges are excluded, as b_inf = -inf excludes disconnected pairs in
+ * "Graph Transformer theory, derivation and implementation", shortest-path
+ * bias section).  A row with no entries yields zeros.  Every CSR entry is
+ * one edge (duplicates weigh twice).  There is no dropout.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Graph:     CSR by destination.  indptr: int32 [N+1], indptr[0] = 0,
+ *            non-decreasing, indptr[N] = nnz.  indices: int32 [nnz], each in
+ *            [0, N): row i attends over nodes indices[indptr[i]..indptr[i+1]).
+ *            N < 2^31, nnz < 2^31.
+ * Features:  Q, K, V, out: [N, H, D] row-major, D innermost, all of the type
+ *            `dtype` (fp32, or bf16 as raw 16-bit patterns).  Accumulation is
+ *            fp32; bf16 `out` is rounded to nearest-even.  1 <= H, 1 <= D,
+ *            H*D <= 1024.  Pointers must be aligned to the element size.
+ *            `out` must not overlap Q, K or V.
+ * Memory:    every pointer argument is a DEVICE pointer (cudaMalloc'd or
+ *            managed memory) owned by the caller unless noted; the library
+ *            never frees caller memory.  Library temporaries come from a
+ *            library-owned stream-ordered memory pool (cudaMallocAsync).
+ * Streams:   work is enqueued on `stream` (0 = legacy default stream) and the
+ *            call returns once it is enqueued, except where noted.
+ * Errors:    every call returns a gtattn_status; nothing throws across the
+ *            ABI.  Argument checks run on the host before any launch.  CSR
+ *            contents are NOT checked on the fast path (use
+ *            gtattn_csr_validate); an invalid CSR gives undefined results.
+ *            GTATTN_ERR_CUDA reports a CUDA runtime error (the last CUDA
+ *            error string is available from gtattn_last_error).
+ * Threads:   entry points are thread-safe, except that one plan must not be
+ *            used by two calls that may run concurrently (it owns a workspace).
+ */
+#ifndef GTATTN_H
+#define GTATTN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GTATTN_OK = 0,
+    GTATTN_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer ... */
+    GTATTN_ERR_BAD_CSR = 2,       /* gtattn_csr_validate found a malformed CSR */
+    GTATTN_ERR_UNSUPPORTED = 3,   /* valid request outside what this build implements */
+    GTATTN_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+    GTATTN_ERR_NO_MEMORY = 5,     /* a device or host allocation failed */
+    GTATTN_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up */
+} gtattn_status;
+
+typedef enum { GTATTN_F32 = 0, GTATTN_BF16 = 1 } gtattn_dtype;
+
+/* Which row kernel a plan uses (tests force each one; AUTO picks the fastest
+ * that supports the shape). */
+typedef enum {
+    GTATTN_KERNEL_AUTO = 0,
+    GTATTN_KERNEL_VECTOR = 1,   /* 16-byte gathers, lanes split a feature row */
+    GTATTN_KERNEL_GENERIC = 2   /* any H, D; one warp per row */
+} gtattn_kernel;
+
+/* Plan-building options.  Zero-initialise and set what you need; a field
+ * left at 0 takes its default. */
+typedef struct {
+    int32_t long_row_min;   /* rows with more entries than this are split into
+                               chunks (default 256; -1: split every non-empty row) */
+    int32_t chunk_edges;    /* entries per chunk of a split row (default 256) */
+    int32_t detect_dense;   /* 1: find complete blocks for the dense tensor-core path */
+    int32_t kernel;         /* a gtattn_kernel value */
+} gtattn_plan_opts;
+
+/* What a plan found (host copy). */
+typedef struct {
+    int64_t N, nnz;
+    int32_t n_long_rows;     /* rows split into chunks */
+    int32_t n_chunks;        /* chunks over all split rows */
+    int32_t n_dense_blocks;  /* complete blocks found (detect_dense) */
+    int32_t n_dense_rows;    /* rows inside those blocks */
+    int32_t n_empty_rows;    /* rows with no entries */
+    int32_t max_degree;
+    int32_t n_buckets;       /* entries of bucket_rows used */
+    int32_t bucket_rows[64]; /* rows per degree bucket (bucket b < 33: degree b) */
+} gtattn_plan_info;
+
+typedef struct gtattn_plan gtattn_plan;   /* opaque, library-owned */
+
+/* Human-readable name of a status code (static string). */
+const char* gtattn_status_string(gtattn_status s);
+
+/* Text of the last CUDA error seen by this thread ("" if none). */
+const char* gtattn_last_error(void);
+
+/*
+ * gtattn_csr_build -- degree binning of a CSR graph (the plan).
+ * Sorts rows into degree buckets, lists split chunks for long rows and, with
+ * opts->detect_dense, finds complete blocks (rows r0..r0+n-1 whose entries are
+ * exactly r0..r0+n-1 in order, n a multiple of 128).  Binning is this
+ * library's design; the pages define only the operation.
+ *   indptr, indices: device CSR as above (not copied: the same arrays must be
+ *   passed to the forward calls that use the plan).
+ *   opts: may be NULL for defaults.
+ *   plan_out: receives a new plan; free it with gtattn_plan_destroy.
+ * Synchronises `stream` once (to size the plan).  Errors: INVALID_ARG,
+ * NO_MEMORY, CUDA.
+ */
+gtattn_status gtattn_csr_build(const int32_t* indptr, const int32_t* indices, int64_t N,
+                               int64_t nnz, const gtattn_plan_opts* opts,
+                               gtattn_plan** plan_out, cudaStream_t stream);
+
+/* Frees a plan (after synchronising the device work that may still use it).
+ * NULL is accepted. */
+gtattn_status gtattn_plan_destroy(gtattn_plan* plan);
+
+/* Copies the plan's counts to *info (host). */
+gtattn_status gtattn_plan_get_info(const gtattn_plan* plan, gtattn_plan_info* info);
+
+/*
+ * gtattn_fwd -- fused sparse MHA forward, no plan: bins the rows on the fly
+ * on `stream` (stream-ordered temporaries, no host synchronisation), then
+ * runs the fused single-pass row kernels and the split-row combine.  No
+ * dense-block path.  Operation and conventions: see the top of this file.
+ *   scale: multiplies q.k (normally 1/sqrt(D)).
+ * Errors: INVALID_ARG (null pointer with N > 0 / nnz > 0, N or nnz negative
+ * or >= 2^31, H or D < 1, H*D > 1024, bad dtype, misaligned pointer),
+ * NO_MEMORY, CUDA.
+ */
+gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indices, const void* Q,
+                         const void* K, const void* V, void* out, int64_t N, int64_t nnz,
+                         int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
+
+/*
+ * gtattn_fwd_plan -- as gtattn_fwd with a prebuilt plan: no binning per
+ * call, and complete blocks (if the plan found any) go to the dense
+ * tensor-core kernel when dtype is bf16 and D == 64.  indptr/indices must be
+ * the arrays the plan was built from.  Grows the plan's workspace on demand
+ * (stream-ordered).
+ */
+gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t* indptr,
+                              const int32_t* indices, const void* Q, const void* K,
+                              const void* V, void* out, int H, int D, float scale,
+                              gtattn_dtype dtype, cudaStream_t stream);
+
+/*
+ * gtattn_fwd_probs -- the unfused path: SDDMM (logits), edge softmax
+ * (probs), SpMM (out) as three kernel stages with the per-edge values
+ * materialised in global memory -- the bsddmm / softmax / bspmm and
+ * u_dot_v / edge_softmax / u_mul_e_sum decompositions of the pages.
+ *   logits: fp32 [nnz, H] in CSR order, scale * q.k (may be NULL).
+ *   probs:  fp32 [nnz, H] in CSR order (may be NULL).
+ *   out:    as gtattn_fwd.
+ * When logits or probs is NULL the library uses a temporary in its place.
+ */
+gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* indices, const void* Q,
+                               const void* K, const void* V, void* out, float* logits,
+                               float* probs, int64_t N, int64_t nnz, int H, int D,
+                               float scale, gtattn_dtype dtype, cudaStream_t stream);
+
+/*
+ * gtattn_coo_to_csr -- builds CSR by destination from a COO edge list
+ * (src[e] -> dst[e]); within a row, entries are sorted by source and
+ * duplicates are kept ("Graph Transformer in a Nutshell" builds A from
+ * g.edges() with no values).  indptr: int32 [N+1], indices: int32 [nnz],
+ * both caller-allocated.  Node ids out of range give INVALID_ARG-free
+ * undefined output; validate the result if unsure.  Uses temporaries.
+ */
+gtattn_status gtattn_coo_to_csr(const int32_t* src, const int32_t* dst, int64_t nnz, int64_t N,
+                                int32_t* indptr, int32_t* indices, cudaStream_t stream);
+
+/*
+ * gtattn_csr_validate -- checks indptr[0] == 0, indptr non-decreasing,
+ * indptr[N] == nnz and every index in [0, N) on the device.  Synchronous
+ * (waits for `stream`).  Returns GTATTN_OK or GTATTN_ERR_BAD_CSR.
+ */
+gtattn_status gtattn_csr_validate(const int32_t* indptr, const int32_t* indices, int64_t N,
+                                  int64_t nnz, cudaStream_t stream);
+
+/*
+ * Benchmark instrumentation (not part of the pages' operation).  While
+ * enabled, the library brackets each of its kernel launches (or a launch
+ * group, for binning) with a pair of CUDA events on the launching stream and
+ * counts the launches, by category.  Process-wide and not thread-safe; meant
+ * for benchmarks and profiling runs.  gtattn_profile_read synchronises on
+ * the recorded events, adds their elapsed times into *out and, with `reset`,
+ * clears the record.
+ */
+typedef enum {
+    GTATTN_KCAT_BIN = 0,      /* degree binning (launch group) */
+    GTATTN_KCAT_ROWS = 1,     /* row kernels: fused, SDDMM, SpMM modes */
+    GTATTN_KCAT_COMBINE = 2,  /* split-row combine */
+    GTATTN_KCAT_SOFTMAX = 3,  /* unfused edge softmax */
+    GTATTN_KCAT_DENSE = 4,    /* dense-block tensor-core kernel */
+    GTATTN_KCAT_COUNT = 8
+} gtattn_kernel_category;
+
+typedef struct {
+    int32_t launches[GTATTN_KCAT_COUNT];  /* kernel launches recorded */
+    int32_t groups[GTATTN_KCAT_COUNT];    /* event pairs recorded */
+    double ms[GTATTN_KCAT_COUNT];         /* summed event-pair durations */
+} gtattn_profile;
+
+gtattn_status gtattn_profile_enable(int on);
+gtattn_status gtattn_profile_read(gtattn_profile* out, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GTATTN_H */

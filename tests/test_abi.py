@@ -1,0 +1,75 @@
+"""The C-ABI library: it builds, loads and exports every declared symbol,
+and host-side argument checks reject bad calls before any GPU work (CPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import graph_transformer_sparse_gb300 as gt
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "gtattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gtattn_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gt.build()
+    return gt.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ("gtattn_csr_build", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
+                 "gtattn_coo_to_csr", "gtattn_csr_validate", "gtattn_status_string"):
+        assert must in names
+    assert set(names) == set(gt.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert gt.gtattn_status_string(0) == "ok"
+    assert gt.gtattn_status_string(2) == "malformed CSR"
+    assert gt.gtattn_status_string(99) == "unknown status"
+
+
+def test_host_argument_checks(lib):
+    # rejected before any device work: no GPU needed
+    INV = gt.GTATTN_ERR_INVALID_ARG
+    f = lib.gtattn_fwd
+    assert f(None, None, None, None, None, None, 4, 4, 2, 8, 1.0, 0, None) == INV      # null indptr
+    assert f(16, 16, 16, 16, 16, 16, -1, 4, 2, 8, 1.0, 0, None) == INV                # N < 0
+    assert f(16, 16, 16, 16, 16, 16, 4, 4, 0, 8, 1.0, 0, None) == INV                 # H < 1
+    assert f(16, 16, 16, 16, 16, 16, 4, 4, 2, 1000, 1.0, 0, None) == INV              # H*D > 1024
+    assert f(16, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 7, None) == INV                 # dtype
+    assert f(16, 16, 18, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV                 # misaligned f32
+    assert f(16, 16, 16, None, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV               # null K, nnz > 0
+    assert f(16, 16, 16, 16, 16, 16, 1 << 31, 4, 2, 8, 1.0, 0, None) == INV           # N too large
+    assert lib.gtattn_fwd_plan(None, 16, 16, 16, 16, 16, 16, 2, 8, 1.0, 0, None) == INV
+    assert lib.gtattn_fwd_probs(16, 16, 16, 16, 16, 16, 18, 16, 4, 4, 2, 8, 1.0, 0, None) == INV
+    assert lib.gtattn_csr_build(16, 16, 4, 4, None, None, None) == INV                 # null plan_out
+    plan = ctypes.c_void_p()
+    assert lib.gtattn_csr_build(16, 16, -3, 4, None, ctypes.byref(plan), None) == INV
+    assert lib.gtattn_csr_validate(None, None, 3, 0, None) == INV
+    assert lib.gtattn_coo_to_csr(None, None, 4, 4, 16, 16, None) == INV
+    assert lib.gtattn_plan_destroy(None) == 0
+    assert lib.gtattn_plan_get_info(None, None) == INV
+
+
+def test_product_path_has_no_oracle_dependency():
+    # the package and its sources never import or link the oracle
+    pkg = os.path.join(ROOT, "graph_transformer_sparse_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in text.lower(), f"{fn} mentions the oracle"

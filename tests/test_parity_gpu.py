@@ -1,0 +1,318 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Reduced-size versions of the five workloads run through every path (plan-less
+fused, planned fused, every row split into chunks, the generic kernel, the
+unfused SDDMM/softmax/SpMM trio) and are compared element by element; the
+full-size workloads are compared on sampled rows (hub rows included).
+"""
+import numpy as np
+import pytest
+
+import workloads as wl
+from gpu_helpers import (PROB_TOL, TOL, assert_close, oracle_rows, out_to_numpy, sample_rows,
+                         to_device)
+
+torch = pytest.importorskip("torch")
+gt = pytest.importorskip("graph_transformer_sparse_gb300")
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ["tiny_random", "molecules", "erdos_renyi", "rmat", "dense_blocks"]
+_small_cache = {}
+
+
+def small(name):
+    if name not in _small_cache:
+        _small_cache[name] = wl.small_workload(name)
+    return _small_cache[name]
+
+
+def _dt(w):
+    return gt.GTATTN_BF16 if w.dtype == "bf16" else gt.GTATTN_F32
+
+
+def run(w, d, path, **plan_kw):
+    """Run one path; returns (out as float64 numpy, logits, probs)."""
+    H, D = w.H, w.D
+    d["out"].fill_(float("nan")) if d["out"].dtype == torch.float32 else d["out"].zero_()
+    logits = probs = None
+    if path == "fwd":
+        gt.gtattn_fwd(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], w.N, w.nnz, H, D,
+                      w.scale, _dt(w))
+    elif path == "plan":
+        plan = gt.Plan(d["indptr"], d["indices"], **plan_kw)
+        gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], H, D,
+                           w.scale, _dt(w))
+        torch.cuda.synchronize()
+        plan.close()
+    elif path == "probs":
+        logits = torch.full((w.nnz, H), float("nan"), device="cuda")
+        probs = torch.full((w.nnz, H), float("nan"), device="cuda")
+        gt.gtattn_fwd_probs(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], logits, probs,
+                            w.N, w.nnz, H, D, w.scale, _dt(w))
+    else:
+        raise ValueError(path)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy() if logits is not None else None
+    pr = probs.cpu().numpy() if probs is not None else None
+    return out_to_numpy(d["out"]), lg, pr
+
+
+PATHS = [
+    ("fwd", {}),
+    ("plan", {}),
+    ("plan", dict(long_row_min=-1, chunk_edges=3)),          # every non-empty row split into chunks
+    ("plan", dict(long_row_min=8, chunk_edges=5)),           # mixed: short rows whole, others split
+    ("plan", dict(kernel=gt.GTATTN_KERNEL_GENERIC)),         # generic row kernel
+    ("plan", dict(kernel=gt.GTATTN_KERNEL_GENERIC, long_row_min=4, chunk_edges=3)),
+    ("plan", dict(detect_dense=True)),
+    ("probs", {}),
+]
+
+
+@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("path,kw", PATHS, ids=lambda x: str(x) if not isinstance(x, dict) else
+                         ",".join(f"{k}={v}" for k, v in x.items()) or "default")
+def test_small_workloads_all_paths(name, path, kw):
+    w = small(name)
+    d = to_device(w)
+    ref = oracle_rows(w, want_probs=(path == "probs"))
+    got, lg, pr = run(w, d, path, **kw)
+    assert_close(got, ref["out"], w.dtype)
+    if path == "probs":
+        assert_close(pr, ref["probs"], w.dtype, "probs", PROB_TOL)
+        # logits: condition-aware bound 1e-5 * scale * sum|q k| + 1e-6
+        dst = np.repeat(np.arange(w.N), np.diff(w.indptr))
+        cond = w.scale * np.einsum("ehd,ehd->eh", np.abs(w.Q[dst].astype(np.float64)),
+                                   np.abs(w.K[w.indices].astype(np.float64)))
+        err = np.abs(lg - ref["logits"])
+        assert np.all(err <= 1e-5 * cond + 1e-6), float((err - 1e-5 * cond).max())
+
+
+@pytest.mark.parametrize("name", ["tiny_random", "molecules"])
+def test_full_small_configs_exact_oracle(name):
+    # these two are small enough for the oracle at full size
+    w = wl.make_workload(name)
+    d = to_device(w)
+    ref = oracle_rows(w)
+    for path in ("fwd", "plan"):
+        got, _, _ = run(w, d, path)
+        assert_close(got, ref["out"], w.dtype)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["erdos_renyi", "rmat", "dense_blocks"])
+def test_full_size_sampled_rows(name):
+    w = wl.make_workload(name)
+    d = to_device(w)
+    rows = sample_rows(w)
+    ref = oracle_rows(w, rows=rows)["out"]
+    for path, kw in (("fwd", {}), ("plan", dict(detect_dense=True))):
+        got, _, _ = run(w, d, path, **kw)
+        assert_close(got[rows], ref, w.dtype, f"{name}/{path}")
+    # every output is finite and every row was written
+    assert np.isfinite(got).all()
+
+
+# ---------------------------------------------------------------------------
+# closed forms and edge cases on the GPU
+# ---------------------------------------------------------------------------
+def _mk(indptr, indices, Q, K, V, dtype="f32"):
+    n, H, D = Q.shape
+    w = wl.Workload("case", n, H, D, "f32", np.asarray(indptr, np.int32), np.asarray(indices, np.int32),
+                    Q.astype(np.float32), K.astype(np.float32), V.astype(np.float32),
+                    float(np.float32(1 / np.sqrt(D))))
+    if dtype == "bf16":
+        w.dtype = "bf16"
+        for name in ("Q", "K", "V"):
+            vals, bits = wl.bf16_round(getattr(w, name))
+            setattr(w, name, vals)
+            w.bits[name] = bits
+    return w
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("path", ["fwd", "probs"])
+def test_single_neighbour_is_exact(dtype, path):
+    rng = np.random.default_rng(1)
+    n, H, D = 300, 8, 64
+    Q, K, V = (rng.standard_normal((n, H, D)) * 4 for _ in range(3))
+    src = rng.integers(0, n, n)
+    ip, ix = wl.csr_by_destination(src, np.arange(n), n)
+    w = _mk(ip, ix, Q, K, V, dtype)
+    got, _, _ = run(w, to_device(w), path)
+    assert np.array_equal(got, w.V[src].astype(np.float64))
+
+
+def test_empty_graph_and_empty_rows():
+    rng = np.random.default_rng(2)
+    n, H, D = 50, 4, 32
+    Q, K, V = (rng.standard_normal((n, H, D)) for _ in range(3))
+    w = _mk(np.zeros(n + 1), np.zeros(0), Q, K, V)
+    for path in ("fwd", "plan", "probs"):
+        got, _, _ = run(w, to_device(w), path)
+        assert np.all(got == 0.0)
+    # N == 0 is a no-op
+    z = torch.zeros(0, 4, 32, device="cuda")
+    gt.gtattn_fwd(torch.zeros(1, dtype=torch.int32, device="cuda"), None, z, z, z, z, 0, 0, 4, 32, 1.0,
+                  gt.GTATTN_F32)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_query_gives_neighbour_mean(dtype):
+    w = wl.small_workload("erdos_renyi") if dtype == "bf16" else wl.make_workload("tiny_random")
+    Q0 = np.zeros_like(w.Q)
+    w2 = _mk(w.indptr, w.indices, Q0, w.K, w.V, dtype)
+    got, _, _ = run(w2, to_device(w2), "fwd")
+    ref = np.zeros_like(got)
+    for i in range(w2.N):
+        nb = w2.indices[w2.indptr[i]:w2.indptr[i + 1]]
+        if len(nb):
+            ref[i] = w2.V[nb].astype(np.float64).mean(axis=0)
+    assert_close(got, ref, dtype)
+
+
+@pytest.mark.parametrize("H,D,dtype", [(3, 5, "f32"), (1, 1, "f32"), (16, 64, "bf16"), (8, 128, "bf16"),
+                                        (2, 512, "f32"), (1, 1024, "bf16"), (4, 16, "f32"), (32, 32, "bf16"),
+                                        (7, 12, "bf16")])
+def test_shapes(H, D, dtype):
+    rng = np.random.default_rng(H * 1000 + D)
+    n = 700
+    ip, ix = wl.random_csr(rng, n, 9000, self_loops=True, degree_skew=1.1)
+    Q, K, V = (rng.standard_normal((n, H, D)) for _ in range(3))
+    w = _mk(ip, ix, Q, K, V, dtype)
+    ref = oracle_rows(w)["out"]
+    d = to_device(w)
+    for path, kw in (("fwd", {}), ("plan", dict(long_row_min=40, chunk_edges=17)), ("probs", {})):
+        got, _, _ = run(w, d, path, **kw)
+        assert_close(got, ref, dtype, f"H={H} D={D} {path}")
+
+
+def test_duplicate_entries_weigh_twice():
+    rng = np.random.default_rng(4)
+    n, H, D = 40, 2, 16
+    src = rng.integers(0, n, 400)
+    dst = rng.integers(0, n, 400)
+    ip, ix = wl.csr_by_destination(src, dst, n)
+    Q, K, V = (rng.standard_normal((n, H, D)) for _ in range(3))
+    w = _mk(ip, ix, Q, K, V)
+    ref = oracle_rows(w)["out"]
+    for path in ("fwd", "probs"):
+        got, _, _ = run(w, to_device(w), path)
+        assert_close(got, ref, "f32")
+
+
+def test_misaligned_features_take_the_generic_kernel():
+    w = wl.make_workload("tiny_random")
+    d = to_device(w)
+    HD = w.H * w.D
+    # views offset by one element: 4-byte aligned, not 16-byte aligned
+    buf = {k: torch.empty(w.N * HD + 1, device="cuda") for k in ("Q", "K", "V", "out")}
+    views = {}
+    for k in ("Q", "K", "V"):
+        buf[k][1:].copy_(d[k].reshape(-1))
+        views[k] = buf[k][1:].view(w.N, w.H, w.D)
+    views["out"] = buf["out"][1:].view(w.N, w.H, w.D)
+    gt.gtattn_fwd(d["indptr"], d["indices"], views["Q"], views["K"], views["V"], views["out"], w.N, w.nnz,
+                  w.H, w.D, w.scale, gt.GTATTN_F32)
+    torch.cuda.synchronize()
+    assert_close(views["out"].cpu().numpy(), oracle_rows(w)["out"], "f32")
+
+
+def test_guard_bands_untouched():
+    w = small("rmat")
+    d = to_device(w)
+    HD = w.H * w.D
+    pad = 4096
+    big = torch.full((w.N * HD + 2 * pad,), 12345, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    out = big[pad:pad + w.N * HD].view(w.N, w.H, w.D)
+    for long_min in (0, -1):
+        plan = gt.Plan(d["indptr"], d["indices"], long_row_min=long_min, chunk_edges=7)
+        gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], out, w.H, w.D, w.scale,
+                           gt.GTATTN_BF16)
+        torch.cuda.synchronize()
+        plan.close()
+    raw = big.view(torch.int16)
+    assert torch.all(raw[:pad] == 12345) and torch.all(raw[-pad:] == 12345)
+
+
+def test_deterministic():
+    w = small("rmat")
+    d = to_device(w)
+    a, _, _ = run(w, d, "fwd")
+    b, _, _ = run(w, d, "fwd")
+    assert np.array_equal(a, b)
+
+
+def test_fused_equals_unfused():
+    w = small("erdos_renyi")
+    d = to_device(w)
+    a, _, _ = run(w, d, "fwd")
+    b, _, _ = run(w, d, "probs")
+    assert_close(a, b, "bf16")
+
+
+# ---------------------------------------------------------------------------
+# plan, CSR helpers
+# ---------------------------------------------------------------------------
+def test_plan_bins_match_degree_histogram():
+    w = wl.make_workload("rmat", scale=14, draws=1 << 18)
+    d = to_device(w)
+    plan = gt.Plan(d["indptr"], d["indices"], long_row_min=100, chunk_edges=64)
+    info = plan.info()
+    plan.close()
+    deg = np.diff(w.indptr)
+    long = deg > 100
+    assert info["n_long_rows"] == int(long.sum())
+    assert info["n_chunks"] == int(((deg[long] + 63) // 64).sum())
+    assert info["max_degree"] == int(deg.max())
+    assert info["n_empty_rows"] == int((deg == 0).sum())
+    hist = np.bincount(np.minimum(deg[~long], 33), minlength=34)
+    assert info["bucket_rows"][:33] == hist[:33].tolist()
+    assert sum(info["bucket_rows"]) == int((~long).sum())
+
+
+def test_dense_blocks_detected():
+    w = small("dense_blocks")
+    d = to_device(w)
+    plan = gt.Plan(d["indptr"], d["indices"], detect_dense=True)
+    info = plan.info()
+    plan.close()
+    assert info["n_dense_blocks"] == 3 and info["n_dense_rows"] == w.N
+
+
+def test_coo_to_csr_matches_host():
+    rng = np.random.default_rng(8)
+    for n, e in ((1, 0), (100, 5000), (3000, 200_000)):
+        src = rng.integers(0, n, e).astype(np.int32)
+        dst = (rng.zipf(1.5, e) % n).astype(np.int32)
+        ip_ref, ix_ref = wl.csr_by_destination(src, dst, n)
+        ip = torch.empty(n + 1, dtype=torch.int32, device="cuda")
+        ix = torch.empty(max(e, 1), dtype=torch.int32, device="cuda")
+        gt.gtattn_coo_to_csr(torch.from_numpy(src).cuda() if e else None,
+                             torch.from_numpy(dst).cuda() if e else None, e, n, ip, ix)
+        torch.cuda.synchronize()
+        assert np.array_equal(ip.cpu().numpy(), ip_ref)
+        assert np.array_equal(ix.cpu().numpy()[:e], ix_ref)
+
+
+def test_csr_validate():
+    w = wl.make_workload("tiny_random")
+    d = to_device(w)
+    assert gt.gtattn_csr_validate(d["indptr"], d["indices"], w.N, w.nnz)
+    bad = d["indices"].clone()
+    bad[5] = w.N
+    assert not gt.gtattn_csr_validate(d["indptr"], bad, w.N, w.nnz)
+    badp = d["indptr"].clone()
+    badp[3] = badp[4] + 1
+    assert not gt.gtattn_csr_validate(badp, d["indices"], w.N, w.nnz)
+    assert not gt.gtattn_csr_validate(d["indptr"], d["indices"], w.N, w.nnz - 1)
+
+
+def test_bad_arguments_raise():
+    w = wl.make_workload("tiny_random")
+    d = to_device(w)
+    with pytest.raises(gt.GtattnError) as e:
+        gt.gtattn_fwd(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], w.N, w.nnz, w.H, 2000,
+                      w.scale, gt.GTATTN_F32)
+    assert e.value.status == gt.GTATTN_ERR_INVALID_ARG

@@ -135,7 +135,7 @@ __global__ void k_dense_blocks(const int* __restrict__ indptr, int N, const int*
     for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < N; r += warps) {
         if (cand[r] != r) continue;
         int n = indptr[r + 1] - indptr[r];
-        if (r + n > N) continue;
+        if ((long long)r + n > N) continue;
         bool ok = true;
         for (int k = lane; ok && k < n; k += 32)
             ok = cand[r + k] == r && (indptr[r + k + 1] - indptr[r + k]) == n;
@@ -356,9 +356,11 @@ extern "C" gtattn_status gtattn_csr_validate(const int32_t* indptr, const int32_
 // ---------------------------------------------------------------------------
 // COO -> CSR by destination: count, scan, scatter, sort each row by source
 // ---------------------------------------------------------------------------
-__global__ void k_coo_count(const int* __restrict__ dst, int nnz, int* __restrict__ cnt) {
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nnz; e += gridDim.x * blockDim.x)
-        atomicAdd(&cnt[dst[e]], 1);
+__global__ void k_coo_count(const int* __restrict__ dst, int nnz, int N, int* __restrict__ cnt) {
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nnz; e += gridDim.x * blockDim.x) {
+        int d = dst[e];
+        if (d >= 0 && d < N) atomicAdd(&cnt[d], 1);    // out-of-range edges are dropped
+    }
 }
 
 // exclusive scan of cnt[0..N) into indptr[0..N], single pass per block of
@@ -392,11 +394,12 @@ __global__ void k_scan_add(int* __restrict__ out, int n, const int* __restrict__
     if (i < n) out[i] += sums[blockIdx.x];
 }
 
-__global__ void k_coo_scatter(const int* __restrict__ src, const int* __restrict__ dst, int nnz,
+__global__ void k_coo_scatter(const int* __restrict__ src, const int* __restrict__ dst, int nnz, int N,
                               const int* __restrict__ indptr, int* __restrict__ cursor,
                               int* __restrict__ indices) {
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < nnz; e += gridDim.x * blockDim.x) {
         int d = dst[e];
+        if (d < 0 || d >= N) continue;
         int pos = indptr[d] + atomicAdd(&cursor[d], 1);
         indices[pos] = src[e];
     }
@@ -459,14 +462,14 @@ extern "C" gtattn_status gtattn_coo_to_csr(const int32_t* src, const int32_t* ds
     if (st != GTATTN_OK) { pool_free(cnt, stream); return st; }
     cudaError_t e = cudaMemsetAsync(cnt, 0, sizeof(int) * (size_t)n, stream);
     if (e == cudaSuccess) {
-        if (m > 0) k_coo_count<<<grid_for(m, 256), 256, 0, stream>>>(dst, m, cnt);
+        if (m > 0) k_coo_count<<<grid_for(m, 256), 256, 0, stream>>>(dst, m, n, cnt);
         k_block_scan<<<nb, 1024, 0, stream>>>(cnt, n, indptr, sums);
         k_scan_sums<<<1, 32, 0, stream>>>(sums, nb, indptr + n);
         k_scan_add<<<nb, 1024, 0, stream>>>(indptr, n, sums);
         e = cudaMemsetAsync(cnt, 0, sizeof(int) * (size_t)n, stream);
     }
     if (e == cudaSuccess && m > 0) {
-        k_coo_scatter<<<grid_for(m, 256), 256, 0, stream>>>(src, dst, m, indptr, cnt, indices);
+        k_coo_scatter<<<grid_for(m, 256), 256, 0, stream>>>(src, dst, m, n, indptr, cnt, indices);
         k_row_sort<<<std::min(n, num_sms() * 8), 256, 0, stream>>>(indptr, n, indices);
     }
     if (e == cudaSuccess) e = cudaGetLastError();

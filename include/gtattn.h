@@ -176,8 +176,9 @@ gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* indices, co
  * (src[e] -> dst[e]); within a row, entries are sorted by source and
  * duplicates are kept ("Graph Transformer in a Nutshell" builds A from
  * g.edges() with no values).  indptr: int32 [N+1], indices: int32 [nnz],
- * both caller-allocated.  Node ids out of range give INVALID_ARG-free
- * undefined output; validate the result if unsure.  Uses temporaries.
+ * both caller-allocated.  Edges whose destination is outside [0, N) are
+ * dropped (indptr[N] then counts the kept edges); sources are not checked.
+ * Uses stream-ordered temporaries.
  */
 gtattn_status gtattn_coo_to_csr(const int32_t* src, const int32_t* dst, int64_t nnz, int64_t N,
                                 int32_t* indptr, int32_t* indices, cudaStream_t stream);

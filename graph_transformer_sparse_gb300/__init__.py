@@ -24,13 +24,13 @@ __all__ = [
     "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
     "gtattn_csr_build", "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
     "gtattn_csr_validate", "gtattn_status_string", "gtattn_profile_enable", "gtattn_profile_read",
-    "sparse_mha", "GTATTN_F32", "GTATTN_BF16",
+    "sparse_mha", "GTATTN_F32", "GTATTN_BF16", "GTATTN_BF16_OUT_F32",
     "GTATTN_KERNEL_AUTO", "GTATTN_KERNEL_VECTOR", "GTATTN_KERNEL_GENERIC", "EXPORTED_SYMBOLS",
 ]
 
 GTATTN_OK, GTATTN_ERR_INVALID_ARG, GTATTN_ERR_BAD_CSR, GTATTN_ERR_UNSUPPORTED = 0, 1, 2, 3
 GTATTN_ERR_CUDA, GTATTN_ERR_NO_MEMORY, GTATTN_ERR_TIMEOUT = 4, 5, 6
-GTATTN_F32, GTATTN_BF16 = 0, 1
+GTATTN_F32, GTATTN_BF16, GTATTN_BF16_OUT_F32 = 0, 1, 2
 GTATTN_KERNEL_AUTO, GTATTN_KERNEL_VECTOR, GTATTN_KERNEL_GENERIC = 0, 1, 2
 
 EXPORTED_SYMBOLS = (
@@ -144,13 +144,16 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _dtype_code(t):
+def _dtype_code(q, out=None):
+    """gtattn_dtype of (Q, out): fp32/fp32, bf16/bf16 or bf16/fp32."""
     import torch
-    if t.dtype == torch.float32:
+    if q.dtype == torch.float32 and (out is None or out.dtype == torch.float32):
         return GTATTN_F32
-    if t.dtype == torch.bfloat16:
+    if q.dtype == torch.bfloat16 and (out is None or out.dtype == torch.bfloat16):
         return GTATTN_BF16
-    raise ValueError(f"unsupported dtype {t.dtype}")
+    if q.dtype == torch.bfloat16 and out.dtype == torch.float32:
+        return GTATTN_BF16_OUT_F32
+    raise ValueError(f"unsupported dtypes {q.dtype} -> {None if out is None else out.dtype}")
 
 
 def _check(status, what):
@@ -263,7 +266,7 @@ def sparse_mha(indptr, indices, Q, K, V, scale=None, out=None, plan=None, stream
         scale = 1.0 / float(D) ** 0.5
     if out is None:
         out = torch.empty_like(Q)
-    dt = _dtype_code(Q)
+    dt = _dtype_code(Q, out)
     if plan is not None:
         gtattn_fwd_plan(plan, indptr, indices, Q, K, V, out, H, D, scale, dt, stream)
     else:

@@ -113,16 +113,18 @@ static gtattn_status check_fwd(const int32_t* indptr, const int32_t* indices, co
                                int H, int D, gtattn_dtype dtype) {
     if (N < 0 || nnz < 0 || N >= (1ll << 31) - 1 || nnz >= (1ll << 31) - 1) return GTATTN_ERR_INVALID_ARG;
     if (H < 1 || D < 1 || (int64_t)H * D > kMaxHD) return GTATTN_ERR_INVALID_ARG;
-    if (dtype != GTATTN_F32 && dtype != GTATTN_BF16) return GTATTN_ERR_INVALID_ARG;
+    if (dtype != GTATTN_F32 && dtype != GTATTN_BF16 && dtype != GTATTN_BF16_OUT_F32)
+        return GTATTN_ERR_INVALID_ARG;
     if (!indptr) return GTATTN_ERR_INVALID_ARG;
     if (N > 0 && (!Q || !out)) return GTATTN_ERR_INVALID_ARG;
     if (nnz > 0 && (!indices || !K || !V)) return GTATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(indptr) | reinterpret_cast<uintptr_t>(indices)) & 3u)
         return GTATTN_ERR_INVALID_ARG;
-    const uintptr_t esz = dtype == GTATTN_BF16 ? 2 : 4;
+    const uintptr_t esz = dtype == GTATTN_F32 ? 4 : 2;
+    const uintptr_t osz = dtype == GTATTN_BF16 ? 2 : 4;
     const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
-                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
-    if (al & (esz - 1)) return GTATTN_ERR_INVALID_ARG;
+                         reinterpret_cast<uintptr_t>(V);
+    if ((al & (esz - 1)) || (reinterpret_cast<uintptr_t>(out) & (osz - 1))) return GTATTN_ERR_INVALID_ARG;
     return GTATTN_OK;
 }
 

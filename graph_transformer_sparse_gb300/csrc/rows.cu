@@ -121,7 +121,7 @@ __device__ __forceinline__ void store_frag(T* p, const float* x) {
 // ---------------------------------------------------------------------------
 // vector row kernel
 // ---------------------------------------------------------------------------
-template <typename T, int VPL, int MODE>
+template <typename T, typename TO, int VPL, int MODE>
 __global__ void __launch_bounds__(256)
 k_rows_vec(RowParams p) {
     using F = Frag<T, VPL>;
@@ -141,7 +141,7 @@ k_rows_vec(RowParams p) {
     const T* __restrict__ Q = static_cast<const T*>(p.Q);
     const T* __restrict__ K = static_cast<const T*>(p.K);
     const T* __restrict__ V = static_cast<const T*>(p.V);
-    T* __restrict__ O = static_cast<T*>(p.out);
+    TO* __restrict__ O = static_cast<TO*>(p.out);
     const int64_t HD = p.HD;
     const int lane_off = gl * E;
 
@@ -294,7 +294,7 @@ k_rows_vec(RowParams p) {
 #pragma unroll
                 for (int e = 0; e < E; ++e) acc[e] = ssum > 0.f ? acc[e] * inv : 0.f;
             }
-            store_frag<T, E>(O + (int64_t)row * HD + lane_off, acc);
+            store_frag<TO, E>(O + (int64_t)row * HD + lane_off, acc);
         }
     }
 }
@@ -308,7 +308,7 @@ constexpr int kGenWarps = 4;
 constexpr int kGenMaxH = 256;
 constexpr int kGenK = kMaxHD / 32;   // elements per lane
 
-template <typename T, int MODE>
+template <typename T, typename TO, int MODE>
 __global__ void __launch_bounds__(kGenWarps * 32)
 k_rows_generic(RowParams p) {
     __shared__ Seg segs[kMaxSegs];
@@ -325,7 +325,7 @@ k_rows_generic(RowParams p) {
     const T* __restrict__ Q = static_cast<const T*>(p.Q);
     const T* __restrict__ K = static_cast<const T*>(p.K);
     const T* __restrict__ V = static_cast<const T*>(p.V);
-    T* __restrict__ O = static_cast<T*>(p.out);
+    TO* __restrict__ O = static_cast<TO*>(p.out);
     const int H = p.H, D = p.D, HD = p.HD;
     float* prod = sm_prod[wid];
     float* hm = sm_m[wid];
@@ -437,14 +437,14 @@ k_rows_generic(RowParams p) {
 // ---------------------------------------------------------------------------
 // combine split-row partials: one block per split row
 // ---------------------------------------------------------------------------
-template <typename T, int MODE>
+template <typename TO, int MODE>
 __global__ void __launch_bounds__(256)
 k_combine(RowParams p) {
     __shared__ float sM[kMaxHD];
     __shared__ float sS[kMaxHD];
     const int n_long = p.lists.hdr[HdrLayout::kLong];
     const int H = p.H, D = p.D, HD = p.HD;
-    T* __restrict__ O = static_cast<T*>(p.out);
+    TO* __restrict__ O = static_cast<TO*>(p.out);
     for (int li = blockIdx.x; li < n_long; li += gridDim.x) {
         const int2 lr = p.lists.longs[li];
         const int row = lr.x, c0 = lr.y;
@@ -554,13 +554,13 @@ static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 bool choose_row_kernel(int H, int D, gtattn_dtype dt, const void* Q, const void* K, const void* V,
                        const void* out, int force, RowChoice* c) {
-    const int esz = dt == GTATTN_BF16 ? 2 : 4;
+    const int esz = dt == GTATTN_F32 ? 4 : 2;   // input element size
     const int HD = H * D;
     const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                          reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
     if (force != GTATTN_KERNEL_GENERIC && (al & 15u) == 0) {
         const int per_vec = 16 / esz;
-        const int max_vpl = dt == GTATTN_BF16 ? 2 : 4;
+        const int max_vpl = esz == 2 ? 2 : 4;
         for (int vpl = 1; vpl <= max_vpl; vpl <<= 1) {
             const int E = vpl * per_vec;
             if (D % E != 0) continue;
@@ -592,7 +592,7 @@ static int grid_persistent(K kernel, int threads, size_t smem) {
     return grid;
 }
 
-template <typename T, int MODE>
+template <typename T, typename TO, int MODE>
 static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
     auto go = [&](auto kernel) {
         kernel<<<grid_persistent(kernel, 256, 0), 256, 0, s>>>(p);
@@ -600,23 +600,23 @@ static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
     };
     cudaError_t e;
     switch (vpl) {
-        case 1: e = go(k_rows_vec<T, 1, MODE>); break;
-        case 2: e = go(k_rows_vec<T, 2, MODE>); break;
+        case 1: e = go(k_rows_vec<T, TO, 1, MODE>); break;
+        case 2: e = go(k_rows_vec<T, TO, 2, MODE>); break;
         case 4:
-            if constexpr (sizeof(T) == 4) { e = go(k_rows_vec<T, 4, MODE>); break; }
+            if constexpr (sizeof(T) == 4) { e = go(k_rows_vec<T, TO, 4, MODE>); break; }
             return GTATTN_ERR_UNSUPPORTED;
         default: return GTATTN_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
 }
 
-template <typename T>
+template <typename T, typename TO>
 static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParams& p, cudaStream_t s) {
     if (c.kind == RowKernel::kVector) {
         switch (mode) {
-            case kFused: return launch_vec_t<T, kFused>(c.vpl, p, s);
-            case kSpmm: return launch_vec_t<T, kSpmm>(c.vpl, p, s);
-            case kSddmm: return launch_vec_t<T, kSddmm>(c.vpl, p, s);
+            case kFused: return launch_vec_t<T, TO, kFused>(c.vpl, p, s);
+            case kSpmm: return launch_vec_t<T, TO, kSpmm>(c.vpl, p, s);
+            case kSddmm: return launch_vec_t<T, TO, kSddmm>(c.vpl, p, s);
         }
         return GTATTN_ERR_UNSUPPORTED;
     }
@@ -626,17 +626,21 @@ static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParam
     };
     cudaError_t e;
     switch (mode) {
-        case kFused: e = go(k_rows_generic<T, kFused>); break;
-        case kSpmm: e = go(k_rows_generic<T, kSpmm>); break;
-        default: e = go(k_rows_generic<T, kSddmm>); break;
+        case kFused: e = go(k_rows_generic<T, TO, kFused>); break;
+        case kSpmm: e = go(k_rows_generic<T, TO, kSpmm>); break;
+        default: e = go(k_rows_generic<T, TO, kSddmm>); break;
     }
     return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
 }
 
 gtattn_status launch_rows(Mode mode, gtattn_dtype dt, const RowChoice& c, const RowParams& p,
                           cudaStream_t s) {
-    if (dt == GTATTN_BF16) return launch_rows_t<__nv_bfloat16>(mode, c, p, s);
-    return launch_rows_t<float>(mode, c, p, s);
+    switch (dt) {
+        case GTATTN_BF16: return launch_rows_t<__nv_bfloat16, __nv_bfloat16>(mode, c, p, s);
+        case GTATTN_BF16_OUT_F32: return launch_rows_t<__nv_bfloat16, float>(mode, c, p, s);
+        case GTATTN_F32: return launch_rows_t<float, float>(mode, c, p, s);
+    }
+    return GTATTN_ERR_INVALID_ARG;
 }
 
 gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cudaStream_t s) {

@@ -25,10 +25,10 @@
  *            non-decreasing, indptr[N] = nnz.  indices: int32 [nnz], each in
  *            [0, N): row i attends over nodes indices[indptr[i]..indptr[i+1]).
  *            N < 2^31, nnz < 2^31.
- * Features:  Q, K, V, out: [N, H, D] row-major, D innermost, all of the type
- *            `dtype` (fp32, or bf16 as raw 16-bit patterns).  Accumulation is
- *            fp32; bf16 `out` is rounded to nearest-even.  1 <= H, 1 <= D,
- *            H*D <= 1024.  Pointers must be aligned to the element size.
+ * Features:  Q, K, V, out: [N, H, D] row-major, D innermost, of the types
+ *            `dtype` names (fp32, or bf16 as raw 16-bit patterns).  Accumulation
+ *            is fp32; a bf16 `out` is rounded to nearest-even.  1 <= H, 1 <= D,
+ *            H*D <= 1024.  Pointers must be aligned to their element size.
  *            `out` must not overlap Q, K or V.
  * Memory:    every pointer argument is a DEVICE pointer (cudaMalloc'd or
  *            managed memory) owned by the caller unless noted; the library
@@ -65,7 +65,9 @@ typedef enum {
     GTATTN_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up */
 } gtattn_status;
 
-typedef enum { GTATTN_F32 = 0, GTATTN_BF16 = 1 } gtattn_dtype;
+/* Element types: Q, K, V and out share the type, except GTATTN_BF16_OUT_F32
+ * (bf16 Q, K, V; fp32 out: the accumulator without the final rounding). */
+typedef enum { GTATTN_F32 = 0, GTATTN_BF16 = 1, GTATTN_BF16_OUT_F32 = 2 } gtattn_dtype;
 
 /* Which row kernel a plan uses (tests force each one; AUTO picks the fastest
  * that supports the shape). */

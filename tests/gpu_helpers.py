@@ -18,7 +18,9 @@ def torch_mod():
     return torch
 
 
-def to_device(w: wl.Workload, dev="cuda"):
+def to_device(w: wl.Workload, dev="cuda", out32=False):
+    """Device copies of the workload; ``out32`` gives an fp32 output buffer
+    for bf16 inputs (the GTATTN_BF16_OUT_F32 variant)."""
     torch = torch_mod()
     d = dict(indptr=torch.from_numpy(w.indptr).to(dev), indices=torch.from_numpy(w.indices).to(dev))
     for name in ("Q", "K", "V"):
@@ -27,7 +29,7 @@ def to_device(w: wl.Workload, dev="cuda"):
             d[name] = torch.from_numpy(bits).to(dev).view(torch.bfloat16)
         else:
             d[name] = torch.from_numpy(getattr(w, name)).to(dev)
-    d["out"] = torch.empty_like(d["Q"])
+    d["out"] = torch.empty(d["Q"].shape, dtype=torch.float32 if out32 else d["Q"].dtype, device=dev)
     return d
 
 
@@ -39,13 +41,25 @@ def out_to_numpy(t):
     return t.cpu().numpy().astype(np.float64)
 
 
-def assert_close(got, ref, dtype, what="out", tol=None):
+def half_ulp_bf16(x):
+    """Half the bf16 spacing at |x| (bf16 keeps 8 significant bits): the
+    largest error of rounding x to bf16."""
+    m, e = np.frexp(np.abs(np.asarray(x, dtype=np.float64)))
+    return np.ldexp(1.0, e - 9) * (m > 0)
+
+
+def assert_close(got, ref, dtype, what="out", tol=None, rounded_bf16=False):
+    """|got - ref| <= rtol*|ref| + atol.  With ``rounded_bf16`` the output was
+    rounded to bf16 after the arithmetic, so the bound also allows that
+    rounding: half a bf16 ulp of ref (up to 2^-8 relative)."""
     rtol, atol = tol or TOL[dtype]
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     err = np.abs(got - ref)
     bound = rtol * np.abs(ref) + atol
+    if rounded_bf16:
+        bound = bound + half_ulp_bf16(ref)
     bad = err > bound
     if bad.any():
         idx = np.argwhere(bad)[:5]

@@ -373,8 +373,19 @@ k_rows_generic(RowParams p) {
             }
             for (int h = lane; h < H; h += 32) {
                 float l = 0.f;
-                if constexpr (MODE != kSpmm)
-                    for (int d = 0; d < D; ++d) l += prod[h * D + d];
+                if constexpr (MODE != kSpmm) {
+                    // eight interleaved partial sums, combined pairwise (error
+                    // grows with D/8 instead of D)
+                    const float* pr = prod + h * D;
+                    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    int d = 0;
+                    for (; d + 8 <= D; d += 8) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) a[k] += pr[d + k];
+                    }
+                    for (; d < D; ++d) a[0] += pr[d];
+                    l = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+                }
                 if constexpr (MODE == kSddmm) {
                     p.logits[(int64_t)e * H + h] = l * p.qscale;
                 } else if constexpr (MODE == kFused) {

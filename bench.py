@@ -346,7 +346,7 @@ def gpu_arm(args):
         torch.cuda.synchronize()
         w, d, step, times, prof, info, plan = run_gpu_workload(w, args.path, args.steps, args.warmup, gt, dev,
                                                                flush, detect_dense=(name == "dense_blocks"),
-                                                               soak_s=2.0)
+                                                               soak_s=args.soak)
         torch.cuda.synchronize()
         barrier()
     clocks = clk.summary()
@@ -379,7 +379,8 @@ def gpu_arm(args):
                             "plan": "gtattn_fwd_plan (prebuilt plan)",
                             "probs": "gtattn_fwd_probs (unfused SDDMM/softmax/SpMM)"}[args.path],
                    "l2": "flushed before every timed step (512 MiB memset, outside the events)",
-                   "clock_soak": "2 s of untimed steps before the warm-up; clocks sampled from then to the end",
+                   "clock_soak": f"{args.soak:g} s of untimed steps before the warm-up; clocks sampled from "
+                                 f"then to the end",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "achieved_gbs_step": round(cbytes / (ms_per_step / 1e3) / 1e9, 1),
         "hbm_frac_step": round(cbytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -476,6 +477,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="rmat", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs"])
+    ap.add_argument("--soak", type=float, default=2.0,
+                    help="seconds of untimed steps before the warm-up (clock record under load)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end timing")

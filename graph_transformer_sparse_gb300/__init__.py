@@ -22,7 +22,7 @@ from ._build import LIB, build
 
 __all__ = [
     "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
-    "gtattn_csr_build", "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
+    "gtattn_fwd_noalloc", "gtattn_csr_build", "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
     "gtattn_csr_validate", "gtattn_status_string", "gtattn_profile_enable", "gtattn_profile_read",
     "sparse_mha", "GTATTN_F32", "GTATTN_BF16", "GTATTN_BF16_OUT_F32",
     "GTATTN_KERNEL_AUTO", "GTATTN_KERNEL_VECTOR", "GTATTN_KERNEL_GENERIC", "EXPORTED_SYMBOLS",
@@ -37,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "gtattn_status_string", "gtattn_last_error", "gtattn_csr_build", "gtattn_plan_destroy",
     "gtattn_plan_get_info", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
     "gtattn_coo_to_csr", "gtattn_csr_validate", "gtattn_profile_enable", "gtattn_profile_read",
+    "gtattn_fwd_noalloc",
 )
 KCAT_NAMES = ("bin", "rows", "combine", "softmax", "dense")
 
@@ -100,6 +101,7 @@ def load(path: str | None = None):
             "gtattn_fwd_probs": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
             "gtattn_coo_to_csr": ([vp, vp, i64, i64, vp, vp, vp], i32),
             "gtattn_csr_validate": ([vp, vp, i64, i64, vp], i32),
+            "gtattn_fwd_noalloc": ([vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
             "gtattn_profile_enable": ([i32], i32),
             "gtattn_profile_read": ([vp, i32], i32),
         }
@@ -169,6 +171,15 @@ def gtattn_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, stream
     _check(load().gtattn_fwd(_ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(out),
                              int(N), int(nnz), int(H), int(D), float(scale), int(dtype),
                              _stream(stream)), "gtattn_fwd")
+
+
+def gtattn_fwd_noalloc(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, stream=None):
+    """gtattn_fwd for callers that cannot allocate device memory: temporaries
+    live in the library's fixed 32 MiB device array (see include/gtattn.h for
+    the size limit and why overlapping calls race)."""
+    _check(load().gtattn_fwd_noalloc(_ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(out),
+                                     int(N), int(nnz), int(H), int(D), float(scale), int(dtype),
+                                     _stream(stream)), "gtattn_fwd_noalloc")
 
 
 def gtattn_fwd_plan(plan, indptr, indices, Q, K, V, out, H, D, scale, dtype, stream=None):

@@ -174,6 +174,34 @@ gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* indices, co
                                float scale, gtattn_dtype dtype, cudaStream_t stream);
 
 /*
+ * gtattn_fwd_noalloc -- gtattn_fwd without any allocation.  The pages have
+ * no counterpart: this exists for callers that cannot allocate device memory
+ * when they run attention -- code running inside an allocator or memory-pool
+ * callback, runtimes that forbid cudaMalloc after start-up (fixed budgets,
+ * pre-planned arenas), frameworks that own the whole device heap.
+ * Same arguments, operation and argument checks as gtattn_fwd.  Its
+ * temporaries live in one fixed 32 MiB device array inside the library
+ * (every GPU that loads the library holds it until the process exits); it
+ * calls no cudaMalloc/cudaFree or other allocating routine.  Rows with more
+ * than 1024 entries are split into chunks of 1024.
+ *   Size limit: the call needs, in bytes, about
+ *     4*N + 8*(C + L) + 4*C*(H*D + 2*H) (+ a little alignment),
+ *   with L = min(N, nnz/1025) and C = nnz/1024 + L; above 32 MiB it returns
+ *   GTATTN_ERR_UNSUPPORTED before any GPU work (gtattn_last_error then says
+ *   how many bytes were needed).  Example: 2^20 rows, 17.1M entries, 4x32 fits.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Concurrency: every call shares the one array and leaves its contents
+ *   behind (each call re-initialises what it reads), so calls whose GPU work
+ *   may overlap -- on different streams, or from different threads -- race
+ *   and corrupt each other's results.  Serialise them.
+ */
+gtattn_status gtattn_fwd_noalloc(const int32_t* indptr, const int32_t* indices, const void* Q,
+                                 const void* K, const void* V, void* out, int64_t N, int64_t nnz,
+                                 int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
+
+/*
  * gtattn_coo_to_csr -- builds CSR by destination from a COO edge list
  * (src[e] -> dst[e]); within a row, entries are sorted by source and
  * duplicates are kept ("Graph Transformer in a Nutshell" builds A from

@@ -61,7 +61,7 @@ class PlanInfo(ctypes.Structure):
                 ("n_chunks", ctypes.c_int32), ("n_dense_blocks", ctypes.c_int32),
                 ("n_dense_rows", ctypes.c_int32), ("n_empty_rows", ctypes.c_int32),
                 ("max_degree", ctypes.c_int32), ("n_buckets", ctypes.c_int32),
-                ("bucket_rows", ctypes.c_int32 * 64)]
+                ("bucket_rows", ctypes.c_int32 * 64), ("device_error", ctypes.c_int32)]
 
     def as_dict(self):
         d = {k: getattr(self, k) for k, _ in self._fields_ if k != "bucket_rows"}

@@ -305,7 +305,8 @@ extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t*
     gtattn_status st = GTATTN_OK;
     if (dense) {
         ProfScope ps(GTATTN_KCAT_DENSE, 1, stream);
-        st = launch_dense(plan->blocks, n_blocks, Q, K, V, out, H, D, scale, stream);
+        st = launch_dense(plan->dense_tiles, plan->n_dense_tiles, N, Q, K, V, out, H, D, scale, dtype,
+                          plan->hdr + HdrLayout::kErr, stream);
     }
     if (st == GTATTN_OK) {
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);

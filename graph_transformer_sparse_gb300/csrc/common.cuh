@@ -56,6 +56,7 @@ struct HdrLayout {
     static constexpr int kCurChunk = kCurLong + 1;             // cursor: chunks
     static constexpr int kCurDense = kCurChunk + 1;            // cursor: dense rows
     static constexpr int kDenseSeg = kCurDense + 1;            // start of dense segment in row list
+    static constexpr int kErr = kDenseSeg + 1;                 // device-side error bits (bounded waits)
     static constexpr int kWords = kDenseSeg + 8;
 };
 

@@ -1,16 +1,479 @@
-// dense.cu -- dense-block attention path (placeholder until the tensor-core
-// kernel lands: reports no support, so complete blocks take the row kernels).
+// dense.cu -- attention over complete blocks on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory, operands staged by TMA).
+//
+// A complete block (rows r0..r0+n-1 attending to exactly r0..r0+n-1) is
+// dense scaled-dot-product attention: out = softmax(scale * Q K^T) V per head
+// ("Graph Transformer in a Nutshell", the all-pairs Attn equation;
+// "Graph Transformer theory, derivation and implementation", review of
+// scaled dot-product attention; a complete graph with self-loops makes the
+// sparse definition reduce to it).
+//
+// One CTA = one 128-row query tile of one block and one head; 4 warps, one
+// thread per query row.  Per 128-row key/value tile j:
+//   S_j = Q K_j^T      tcgen05.mma (M=128, N=128, K=64), fp32 in TMEM cols [0,128)
+//   softmax            each thread reads its row of S from TMEM, keeps a running
+//                      max m (log2 units) that is raised only when a tile's max
+//                      exceeds it by more than 8 (then O and l are rescaled), and
+//                      writes P = 2^(s*scale*log2e - m) back over S as two bf16
+//                      halves P_hi = bf16(P), P_lo = bf16(P - P_hi)
+//   O += P_hi V_j + P_lo V_j   tcgen05.mma with A = P from TMEM (M=128, N=64, K=128)
+// and out = O / l at the end.  Splitting P in two bf16 terms keeps the
+// product at ~16-bit precision on the bf16 tensor path (a single bf16 P would
+// cost ~2^-9 relative per weight, far outside the accuracy the oracle checks).
+// Q, K and V tiles arrive by TMA (128-byte swizzle, 2-stage K/V ring).  Every
+// mbarrier wait is bounded: on timeout the CTA records an error code, waits
+// (bounded) for its own copies and MMAs in flight, frees its tensor memory
+// and returns.
 #include "dense.cuh"
+
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
 
 namespace gt {
 
-bool dense_supported(int, int, gtattn_dtype, const void*, const void*, const void*, const void*) {
-    return false;
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kTile = 128;              // rows per Q / K / V tile
+constexpr int kD = 64;                  // head width handled here
+constexpr uint32_t kTileBytes = kTile * kD * 2;   // 16 KB bf16
+constexpr uint32_t kTmemCols = 256;     // S/P: [0,128), O: [128,192)
+constexpr uint32_t kColO = 128;
+constexpr float kRescaleThreshold = 8.f;          // log2 units
+constexpr long long kWaitCycles = 2000000000ll;   // ~1 s at 2 GHz
+
+constexpr size_t kSmemQ = 0;
+constexpr size_t kSmemK = kTileBytes;               // 2 stages
+constexpr size_t kSmemV = 3 * kTileBytes;           // 2 stages
+constexpr size_t kSmemBytes = 5 * kTileBytes;       // 80 KB
+constexpr size_t kSmemAlloc = kSmemBytes + 1024;    // + alignment slack
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-gtattn_status launch_dense(const int2*, int, const void*, const void*, const void*, void*, int, int,
-                           float, cudaStream_t) {
-    return GTATTN_ERR_UNSUPPORTED;
+// ---- mbarrier --------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, long long limit = kWaitCycles) {
+    const long long t0 = clock64();
+    while (!mbar_test(b, parity)) {
+        if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
+// ---- TMA -------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
+        : "memory");
+}
+
+// ---- tcgen05 ---------------------------------------------------------------
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                 : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, 128-byte swizzle (start, leading and
+// stride byte offsets in 16-byte units; descriptor version 1; layout 2).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M and N;
+// b_mn_major selects an MN-major B operand.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
+    return (1u << 4)                                   // D: fp32
+           | (1u << 7)                                 // A: bf16
+           | (1u << 10)                                // B: bf16
+           | (static_cast<uint32_t>(b_mn_major) << 16) // B major
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+struct DenseErr {
+    static constexpr int kTimeout = 1;
+};
+
+template <typename TO>
+__global__ void __launch_bounds__(kThreads, 1)
+k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+             const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ tiles, TO* __restrict__ out,
+             int HD, float sl2, int* __restrict__ err) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t bar_q, bar_s, bar_o, bar_kv[2];
+    __shared__ uint32_t s_tmem;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int4 tinfo = tiles[blockIdx.x];
+    const int r0 = tinfo.x, n = tinfo.y, q0 = tinfo.z;
+    const int h = blockIdx.y;
+    const int T = n / kTile;
+    const int xh = h * kD;
+
+    unsigned char* sQ = smem + kSmemQ;
+    auto sK = [&](int stage) { return smem + kSmemK + stage * kTileBytes; };
+    auto sV = [&](int stage) { return smem + kSmemV + stage * kTileBytes; };
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        mbar_init(&bar_q, 1);
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_o, 1);
+        mbar_init(&bar_kv[0], 1);
+        mbar_init(&bar_kv[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t tS = tmem;            // S / P columns [0,128)
+    const uint32_t tO = tmem + kColO;    // O columns [128,192)
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    // issue bookkeeping (thread 0), one counter per stage
+    int kv_issued0 = 0, kv_issued1 = 0, kv_done0 = 0, kv_done1 = 0;
+    int s_issued = 0, s_done = 0, o_issued = 0, o_done = 0;
+    bool q_issued = false, q_done = false;
+
+    if (tid == 0) {
+        mbar_expect_tx(&bar_q, kTileBytes);
+        tma_load_2d(sQ, &tmQ, xh, q0, &bar_q);
+        q_issued = true;
+        for (int t = 0; t < 2 && t < T; ++t) {
+            mbar_expect_tx(&bar_kv[t], 2 * kTileBytes);
+            tma_load_2d(sK(t), &tmK, xh, r0 + t * kTile, &bar_kv[t]);
+            tma_load_2d(sV(t), &tmV, xh, r0 + t * kTile, &bar_kv[t]);
+            if (t == 0) kv_issued0 = 1; else kv_issued1 = 1;
+        }
+    }
+
+    const uint32_t idS = idesc_bf16(128, 128, 0);
+    const uint32_t idO = idesc_bf16(128, 64, 1);
+    const uint64_t dQ = smem_desc_sw128(su32(sQ), 16, 1024);
+
+    float m_used = -INFINITY, l = 0.f;
+    bool aborted = false;
+
+    for (int j = 0; j < T; ++j) {
+        const int st = j & 1;
+        int fail = 0;
+        if (tid == 0) {
+            if (j > 0) {   // PV_{j-1} done: its K/V stage and the P columns are free
+                fail |= !mbar_wait(&bar_o, (o_done) & 1);
+                if (!fail) ++o_done;
+                if (!fail && j >= 1 && j + 1 < T) {
+                    const int ps = (j + 1) & 1;
+                    mbar_expect_tx(&bar_kv[ps], 2 * kTileBytes);
+                    tma_load_2d(sK(ps), &tmK, xh, r0 + (j + 1) * kTile, &bar_kv[ps]);
+                    tma_load_2d(sV(ps), &tmV, xh, r0 + (j + 1) * kTile, &bar_kv[ps]);
+                    if (ps == 0) ++kv_issued0; else ++kv_issued1;
+                }
+            }
+            if (!fail && !q_done) {
+                fail |= !mbar_wait(&bar_q, 0);
+                if (!fail) q_done = true;
+            }
+            if (!fail) {
+                const int kd = st == 0 ? kv_done0 : kv_done1;
+                fail |= !mbar_wait(&bar_kv[st], kd & 1);
+                if (!fail) { if (st == 0) ++kv_done0; else ++kv_done1; }
+            }
+            if (!fail) {
+                tc_fence_after();
+                const uint64_t dK = smem_desc_sw128(su32(sK(st)), 16, 1024);
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k)   // 32 bytes of K per step
+                    mma_ss(tS, dQ + (uint64_t)(2 * k), dK + (uint64_t)(2 * k), idS, k > 0);
+                tc_commit(&bar_s);
+                ++s_issued;
+            }
+        }
+        if (__syncthreads_or(fail)) { aborted = true; break; }
+        fail = !mbar_wait(&bar_s, j & 1);
+        if (__syncthreads_or(fail)) { aborted = true; break; }
+        if (tid == 0) s_done = j + 1;
+        tc_fence_after();
+
+        // ---- softmax over this thread's row of S_j ----
+        uint32_t r[32];
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tS + lane_base + 32 * c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(r[i]) * sl2);
+        }
+        bool need = false;
+        float alpha = 1.f;
+        if (j == 0) {
+            m_used = mt;
+        } else if (mt > m_used + kRescaleThreshold) {
+            need = true;
+            alpha = ex2(m_used - mt);
+            m_used = mt;
+        }
+        if (__any_sync(0xffffffffu, need)) {   // rescale O (warp-collective TMEM access)
+            l *= alpha;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                tmem_ld32(tO + lane_base + 32 * c, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                tmem_st32(tO + lane_base + 32 * c, r);
+            }
+            tmem_st_wait();
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tS + lane_base + 32 * c, r);
+            tmem_ld_wait();
+            uint32_t pk[32];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float p0 = ex2(__uint_as_float(r[2 * q]) * sl2 - m_used);
+                const float p1 = ex2(__uint_as_float(r[2 * q + 1]) * sl2 - m_used);
+                l += p0 + p1;
+                const uint32_t hi = pack2_bf16(p0, p1);
+                const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+                pk[q] = hi;
+                pk[16 + q] = pack2_bf16(p0 - h0, p1 - h1);
+            }
+            // kv 32c..32c+31: P_hi in cols 32c..32c+15, P_lo in cols 32c+16..32c+31
+            tmem_st32(tS + lane_base + 32 * c, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint64_t dV = smem_desc_sw128(su32(sV(st)), 8192, 1024);
+#pragma unroll
+            for (int s = 0; s < kTile / 16; ++s) {    // 16 kv rows per step
+                const uint32_t a_hi = tS + 32 * (s >> 1) + 8 * (s & 1);
+                const uint32_t a_lo = a_hi + 16;
+                const uint64_t b = dV + (uint64_t)(s * (2048 >> 4));
+                mma_ts(tO, a_hi, b, idO, (j > 0 || s > 0) ? 1u : 0u);
+                mma_ts(tO, a_lo, b, idO, 1u);
+            }
+            tc_commit(&bar_o);
+            ++o_issued;
+        }
+    }
+
+    if (!aborted) {
+        int fail = 0;
+        if (tid == 0) {
+            fail = !mbar_wait(&bar_o, o_done & 1);
+            if (!fail) ++o_done;
+        }
+        aborted = __syncthreads_or(fail) != 0;
+    }
+    if (!aborted) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        TO* o = out + static_cast<int64_t>(q0 + tid) * HD + xh;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + lane_base + 32 * c, r);
+            tmem_ld_wait();
+            if constexpr (sizeof(TO) == 2) {
+                uint4* o4 = reinterpret_cast<uint4*>(o + 32 * c);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    o4[v] = make_uint4(pack2_bf16(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
+                                       pack2_bf16(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
+                                       pack2_bf16(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
+                                       pack2_bf16(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
+            } else {
+                float4* o4 = reinterpret_cast<float4*>(o + 32 * c);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    o4[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                        __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+            }
+        }
+    } else if (tid == 0) {
+        // record the timeout, then drain what this CTA still has in flight
+        // (bounded) before its tensor memory is released
+        atomicOr(err, DenseErr::kTimeout);
+        const long long drain = kWaitCycles / 4;
+        if (q_issued && !q_done) mbar_wait(&bar_q, 0, drain);
+        while (kv_done0 < kv_issued0 && mbar_wait(&bar_kv[0], kv_done0 & 1, drain)) ++kv_done0;
+        while (kv_done1 < kv_issued1 && mbar_wait(&bar_kv[1], kv_done1 & 1, drain)) ++kv_done1;
+        while (s_done < s_issued && mbar_wait(&bar_s, s_done & 1, drain)) ++s_done;
+        while (o_done < o_issued && mbar_wait(&bar_o, o_done & 1, drain)) ++o_done;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ---- host ------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [N, HD] bf16 matrix, box 64 (one head) x 128 rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t N, int HD) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(HD) * 2};
+    cuuint32_t box[2] = {kD, kTile};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool dense_supported(int H, int D, gtattn_dtype dt, const void* Q, const void* K, const void* V,
+                     const void* out) {
+    if (dt != GTATTN_BF16 && dt != GTATTN_BF16_OUT_F32) return false;
+    if (D != kD || H < 1 || H * D > kMaxHD) return false;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
+    if (al & 15u) return false;
+    return encode_fn() != nullptr;
+}
+
+gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void* Q, const void* K,
+                           const void* V, void* out, int H, int D, float scale, gtattn_dtype dt, int* err,
+                           cudaStream_t s) {
+    if (n_tiles <= 0) return GTATTN_OK;
+    const int HD = H * D;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, Q, N, HD) || !make_map(&mk, K, N, HD) || !make_map(&mv, V, N, HD))
+        return GTATTN_ERR_UNSUPPORTED;
+    const float sl2 = scale * kLog2e;
+    dim3 grid(n_tiles, H);
+    cudaError_t e;
+    if (dt == GTATTN_BF16) {
+        auto k = k_dense_attn<__nv_bfloat16>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+        if (e == cudaSuccess) {
+            k<<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, tiles, static_cast<__nv_bfloat16*>(out), HD, sl2, err);
+            e = cudaGetLastError();
+        }
+    } else {
+        auto k = k_dense_attn<float>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+        if (e == cudaSuccess) {
+            k<<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, tiles, static_cast<float*>(out), HD, sl2, err);
+            e = cudaGetLastError();
+        }
+    }
+    return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
 }
 
 }  // namespace gt

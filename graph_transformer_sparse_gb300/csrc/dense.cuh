@@ -5,13 +5,17 @@
 
 namespace gt {
 
-// True when launch_dense handles this shape: bf16, D == 64, 16-byte aligned.
+// True when launch_dense handles this shape: bf16 inputs (bf16 or fp32 out),
+// D == 64, 16-byte aligned pointers.
 bool dense_supported(int H, int D, gtattn_dtype dt, const void* Q, const void* K, const void* V,
                      const void* out);
 
-// out_b = softmax(scale * Q_b K_b^T) V_b per head for each block b =
-// (first row, size) in `blocks` (device array of n_blocks entries).
-gtattn_status launch_dense(const int2* blocks, int n_blocks, const void* Q, const void* K,
-                           const void* V, void* out, int H, int D, float scale, cudaStream_t s);
+// out = softmax(scale * Q K^T) V per head over complete blocks, one CTA per
+// (128-row query tile, head).  tiles: device array of (first row of the
+// block, block size, first row of the query tile, 0).  A bounded device wait
+// that times out ORs an error code into *err.
+gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void* Q, const void* K,
+                           const void* V, void* out, int H, int D, float scale, gtattn_dtype dt, int* err,
+                           cudaStream_t s);
 
 }  // namespace gt

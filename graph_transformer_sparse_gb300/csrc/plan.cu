@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cstring>
 #include <new>
+#include <vector>
 
 namespace gt {
 
@@ -273,6 +274,21 @@ extern "C" gtattn_status gtattn_csr_build(const int32_t* indptr, const int32_t* 
                                   cudaMemcpyDeviceToHost, stream))) != GTATTN_OK)
         return fail(st);
     if ((st = chk(cudaStreamSynchronize(stream))) != GTATTN_OK) return fail(st);
+    // dense blocks -> one work item per 128-row query tile
+    const int nb = p->hdr_host[HdrLayout::kDenseBlocks];
+    if (nb > 0) {
+        std::vector<int2> hb(nb);
+        if ((st = chk(cudaMemcpy(hb.data(), p->blocks, sizeof(int2) * nb, cudaMemcpyDeviceToHost))) != GTATTN_OK)
+            return fail(st);
+        std::vector<int4> tiles;
+        for (const int2& b : hb)
+            for (int q0 = b.x; q0 < b.x + b.y; q0 += kDenseTile) tiles.push_back(make_int4(b.x, b.y, q0, 0));
+        if ((st = chk(cudaMalloc(&p->dense_tiles, sizeof(int4) * tiles.size()))) != GTATTN_OK) return fail(st);
+        if ((st = chk(cudaMemcpy(p->dense_tiles, tiles.data(), sizeof(int4) * tiles.size(),
+                                 cudaMemcpyHostToDevice))) != GTATTN_OK)
+            return fail(st);
+        p->n_dense_tiles = static_cast<int>(tiles.size());
+    }
     *plan_out = p;
     return GTATTN_OK;
 }
@@ -288,6 +304,7 @@ extern "C" gtattn_status gtattn_plan_destroy(gtattn_plan* p) {
     cudaFree(p->chunks);
     cudaFree(p->longs);
     cudaFree(p->blocks);
+    cudaFree(p->dense_tiles);
     cudaFree(p->dense_flag);
     if (p->ws) cudaFree(p->ws);
     if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
@@ -308,6 +325,10 @@ extern "C" gtattn_status gtattn_plan_get_info(const gtattn_plan* p, gtattn_plan_
     info->max_degree = p->hdr_host[HdrLayout::kMaxDeg];
     info->n_buckets = kNumBuckets;
     for (int b = 0; b < kNumBuckets; ++b) info->bucket_rows[b] = p->hdr_host[HdrLayout::kCount + b];
+    int dev_err = 0;
+    cudaError_t e = cudaMemcpy(&dev_err, p->hdr + HdrLayout::kErr, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+    info->device_error = dev_err;
     return GTATTN_OK;
 }
 

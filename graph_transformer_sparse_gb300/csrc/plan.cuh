@@ -14,6 +14,8 @@ struct gtattn_plan {
     int2* chunks = nullptr;                 // (row, first entry) per chunk
     int2* longs = nullptr;                  // (row, first chunk) per split row
     int2* blocks = nullptr;                 // (first row, size) per dense block
+    int4* dense_tiles = nullptr;            // (block row, block size, query-tile row, 0)
+    int n_dense_tiles = 0;
     int* dense_flag = nullptr;              // 1 for rows inside a dense block
     mutable void* ws = nullptr;             // split-row partials workspace
     mutable size_t ws_bytes = 0;

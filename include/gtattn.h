@@ -98,6 +98,8 @@ typedef struct {
     int32_t max_degree;
     int32_t n_buckets;       /* entries of bucket_rows used */
     int32_t bucket_rows[64]; /* rows per degree bucket (bucket b < 33: degree b) */
+    int32_t device_error;    /* nonzero if a bounded device wait of a forward
+                                call with this plan gave up (1: timeout) */
 } gtattn_plan_info;
 
 typedef struct gtattn_plan gtattn_plan;   /* opaque, library-owned */
@@ -129,7 +131,8 @@ gtattn_status gtattn_csr_build(const int32_t* indptr, const int32_t* indices, in
  * NULL is accepted. */
 gtattn_status gtattn_plan_destroy(gtattn_plan* plan);
 
-/* Copies the plan's counts to *info (host). */
+/* Copies the plan's counts to *info (host).  Reads the plan's device error
+ * word, so it waits for work already queued that uses the plan. */
 gtattn_status gtattn_plan_get_info(const gtattn_plan* plan, gtattn_plan_info* info);
 
 /*

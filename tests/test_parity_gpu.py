@@ -330,3 +330,75 @@ def test_bad_arguments_raise():
         gt.gtattn_fwd(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], w.N, w.nnz, w.H, 2000,
                       w.scale, gt.GTATTN_F32)
     assert e.value.status == gt.GTATTN_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------------------
+# dense-block tensor-core path
+# ---------------------------------------------------------------------------
+def _mixed_dense_graph(rng, sizes, n_sparse, sparse_edges):
+    """Complete blocks of the given sizes (self-loops included) followed by
+    `n_sparse` rows of a random sparse graph that also points into the
+    blocks; returns COO (src, dst) and n."""
+    src, dst = [], []
+    base = 0
+    for n in sizes:
+        r = np.arange(base, base + n)
+        src.append(np.tile(r, n))
+        dst.append(np.repeat(r, n))
+        base += n
+    n_total = base + n_sparse
+    s = rng.integers(0, n_total, sparse_edges)
+    d = rng.integers(base, n_total, sparse_edges)
+    src.append(s)
+    dst.append(d)
+    return np.concatenate(src), np.concatenate(dst), n_total
+
+
+@pytest.mark.parametrize("out32", [True, False])
+def test_dense_path_mixed_graph(out32):
+    rng = np.random.default_rng(77)
+    src, dst, n = _mixed_dense_graph(rng, [128, 384, 256], 500, 6000)
+    ip, ix = wl.csr_by_destination(src, dst, n)
+    Q, K, V = (0.5 * rng.standard_normal((n, 8, 64)) for _ in range(3))
+    w = _mk(ip, ix, Q, K, V, "bf16")
+    ref = oracle_rows(w)["out"]
+    d = to_device(w, out32=out32)
+    plan = gt.Plan(d["indptr"], d["indices"], detect_dense=True)
+    info = plan.info()
+    assert info["n_dense_blocks"] == 3 and info["n_dense_rows"] == 768
+    gt.gtattn_profile_enable(True)
+    gt.gtattn_profile_read(reset=True)
+    d["out"].fill_(float("nan"))
+    gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], 8, 64, w.scale,
+                       _dt(d))
+    torch.cuda.synchronize()
+    prof = gt.gtattn_profile_read(reset=True)
+    gt.gtattn_profile_enable(False)
+    assert prof["dense"]["launches"] == 1, prof
+    assert plan.info()["device_error"] == 0
+    plan.close()
+    got = out_to_numpy(d["out"])
+    check_out(w, got, ref, f"mixed dense+sparse out32={out32}", out32=out32)
+
+
+def test_dense_path_large_scores():
+    # logits spread over a wide range: the running max is raised mid-row and
+    # O is rescaled
+    rng = np.random.default_rng(5)
+    n = 512
+    src, dst, _ = _mixed_dense_graph(rng, [n], 0, 0)
+    ip, ix = wl.csr_by_destination(src, dst, n)
+    Q = rng.standard_normal((n, 2, 64)) * 3
+    K = rng.standard_normal((n, 2, 64)) * 3
+    K[:, :, :] *= np.linspace(0.1, 2.0, n)[:, None, None]     # later keys larger: max grows across tiles
+    V = rng.standard_normal((n, 2, 64))
+    w = _mk(ip, ix, Q, K, V, "bf16")
+    ref = oracle_rows(w)["out"]
+    d = to_device(w, out32=True)
+    plan = gt.Plan(d["indptr"], d["indices"], detect_dense=True)
+    gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], 2, 64, w.scale,
+                       _dt(d))
+    torch.cuda.synchronize()
+    assert plan.info()["device_error"] == 0
+    plan.close()
+    check_out(w, out_to_numpy(d["out"]), ref, "dense large scores", out32=True)

@@ -19,7 +19,7 @@
 //   O += P_hi V_j + P_lo V_j   tcgen05.mma with A = P from TMEM (M=128, N=64, K=128)
 // and out = O / l at the end.  Splitting P in two bf16 terms keeps the
 // product at ~16-bit precision on the bf16 tensor path (a single bf16 P would
-// cost ~2^-9 relative per weight, far outside the accuracy the oracle checks).
+// cost ~2^-9 relative per weight, outside the bf16 accuracy bound of the path).
 // Q, K and V tiles arrive by TMA (128-byte swizzle, 2-stage K/V ring).  Every
 // mbarrier wait is bounded: on timeout the CTA records an error code, waits
 // (bounded) for its own copies and MMAs in flight, frees its tensor memory

@@ -308,7 +308,9 @@ extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t*
         st = launch_dense(plan->dense_tiles, plan->n_dense_tiles, N, Q, K, V, out, H, D, scale, dtype,
                           plan->hdr + HdrLayout::kErr, stream);
     }
-    if (st == GTATTN_OK) {
+    int row_tasks = n_chunks + (dense ? 0 : plan->hdr_host[HdrLayout::kDenseRows]);
+    for (int b = 0; b < kNumBuckets; ++b) row_tasks += plan->hdr_host[HdrLayout::kCount + b];
+    if (st == GTATTN_OK && row_tasks > 0) {
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
         st = launch_rows(kFused, dtype, c, p, stream);
     }

@@ -8,22 +8,24 @@
 // scaled dot-product attention; a complete graph with self-loops makes the
 // sparse definition reduce to it).
 //
-// One CTA = one 128-row query tile of one block and one head; 4 warps, one
-// thread per query row.  Per 128-row key/value tile j:
-//   S_j = Q K_j^T      tcgen05.mma (M=128, N=128, K=64), fp32 in TMEM cols [0,128)
-//   softmax            each thread reads its row of S from TMEM, keeps a running
-//                      max m (log2 units) that is raised only when a tile's max
-//                      exceeds it by more than 8 (then O and l are rescaled), and
-//                      writes P = 2^(s*scale*log2e - m) back over S as two bf16
-//                      halves P_hi = bf16(P), P_lo = bf16(P - P_hi)
-//   O += P_hi V_j + P_lo V_j   tcgen05.mma with A = P from TMEM (M=128, N=64, K=128)
-// and out = O / l at the end.  Splitting P in two bf16 terms keeps the
-// product at ~16-bit precision on the bf16 tensor path (a single bf16 P would
-// cost ~2^-9 relative per weight, outside the bf16 accuracy bound of the path).
-// Q, K and V tiles arrive by TMA (128-byte swizzle, 2-stage K/V ring).  Every
-// mbarrier wait is bounded: on timeout the CTA records an error code, waits
-// (bounded) for its own copies and MMAs in flight, frees its tensor memory
-// and returns.
+// One CTA = two 128-row query tiles (A, B) of one block and one head, sharing
+// every K/V tile; warp-specialised:
+//   warp 9      TMA: Q_A, Q_B once, then K_j, V_j into a 3-stage ring (128-byte swizzle)
+//   warp 8      MMA (one thread): S_g = Q_g K_j^T (tcgen05.mma M=128 N=128 K=64,
+//               fp32 in TMEM), then O_g += P_g V_j once softmax g has written P_g
+//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B (one thread per
+//               query row): read the row of S_g from TMEM, keep a running max m
+//               (log2 units) raised only when a tile's max exceeds it by more
+//               than 8 (then O_g and l are rescaled), write
+//               P = 2^(s*scale*log2e - m) back over S_g as two bf16 terms
+//               P_hi = bf16(P), P_lo = bf16(P - P_hi); O_g += P_hi V + P_lo V
+// The MMA warp alternates A and B, so one tile's softmax overlaps the other's
+// matrix products; out = O / l at the end.  Splitting P in two bf16 terms
+// keeps the product at ~16-bit precision on the bf16 tensor path (a single
+// bf16 P would cost ~2^-9 relative per weight, outside the bf16 accuracy
+// bound of the path).  Every mbarrier wait is bounded: on timeout the CTA
+// records an error code, drains (bounded) the copies and MMAs it issued, frees
+// its tensor memory and returns.
 #include "dense.cuh"
 
 #include <cuda.h>
@@ -36,20 +38,12 @@ namespace gt {
 
 namespace {
 
-constexpr int kThreads = 128;
 constexpr int kTile = 128;              // rows per Q / K / V tile
 constexpr int kD = 64;                  // head width handled here
 constexpr uint32_t kTileBytes = kTile * kD * 2;   // 16 KB bf16
-constexpr uint32_t kTmemCols = 256;     // S/P: [0,128), O: [128,192)
-constexpr uint32_t kColO = 128;
 constexpr float kRescaleThreshold = 8.f;          // log2 units
 constexpr long long kWaitCycles = 2000000000ll;   // ~1 s at 2 GHz
 
-constexpr size_t kSmemQ = 0;
-constexpr size_t kSmemK = kTileBytes;               // 2 stages
-constexpr size_t kSmemV = 3 * kTileBytes;           // 2 stages
-constexpr size_t kSmemBytes = 5 * kTileBytes;       // 80 KB
-constexpr size_t kSmemAlloc = kSmemBytes + 1024;    // + alignment slack
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -174,232 +168,276 @@ struct DenseErr {
     static constexpr int kTimeout = 1;
 };
 
+// Warp roles of the CTA (10 warps): warps 0-3 run the softmax of query tile
+// A, warps 4-7 that of query tile B (the next 128 rows of the same block and
+// head), warp 8 issues the MMAs (one thread), warp 9 the TMA loads (one
+// thread).  The two query tiles share every K/V tile in shared memory.
+constexpr int kWarps = 10;
+constexpr int kThreadsWS = kWarps * 32;
+constexpr int kStages = 3;                        // K/V ring
+constexpr uint32_t kTmemAll = 512;                // S_A, S_B, O_A, O_B
+// TMEM columns of S_g / P_g and O_g for query tile g
+__host__ __device__ constexpr uint32_t col_s(int g) { return g == 0 ? 0u : 128u; }
+__host__ __device__ constexpr uint32_t col_o(int g) { return g == 0 ? 256u : 320u; }
+constexpr size_t kWsSmemQ = 0;                    // 2 query tiles
+constexpr size_t kWsSmemKV = 2 * kTileBytes;      // stage s: K at +0, V at +kTileBytes
+constexpr size_t kWsSmemBytes = 2 * kTileBytes + kStages * 2 * kTileBytes;   // 128 KB
+constexpr size_t kWsSmemAlloc = kWsSmemBytes + 1024;
+
+struct WsBars {
+    uint64_t q;
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t s[2];      // S_g of the current tile is in TMEM (MMA -> softmax g)
+    uint64_t p[2];      // P_g written over S_g (softmax g -> MMA), 4 arrivals
+    uint64_t o[2];      // PV_g done (MMA -> softmax g, waited for the epilogue)
+    uint64_t drain;
+};
+
 template <typename TO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsWS, 1)
 k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-             const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ tiles, TO* __restrict__ out,
+             const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ items, TO* __restrict__ out,
              int HD, float sl2, int* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t bar_q, bar_s, bar_o, bar_kv[2];
+    __shared__ __align__(8) WsBars bars;
     __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int4 tinfo = tiles[blockIdx.x];
-    const int r0 = tinfo.x, n = tinfo.y, q0 = tinfo.z;
+    const int lane = tid & 31;
+    const int4 it = items[blockIdx.x];
+    const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w;   // nq: query tiles in this item (1 or 2)
     const int h = blockIdx.y;
     const int T = n / kTile;
     const int xh = h * kD;
-
-    unsigned char* sQ = smem + kSmemQ;
-    auto sK = [&](int stage) { return smem + kSmemK + stage * kTileBytes; };
-    auto sV = [&](int stage) { return smem + kSmemV + stage * kTileBytes; };
+    auto sQ = [&](int g) { return smem + kWsSmemQ + g * kTileBytes; };
+    auto sK = [&](int st) { return smem + kWsSmemKV + st * 2 * kTileBytes; };
+    auto sV = [&](int st) { return smem + kWsSmemKV + st * 2 * kTileBytes + kTileBytes; };
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&s_tmem)),
-                     "r"(kTmemCols)
+                     "r"(kTmemAll)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        mbar_init(&bar_q, 1);
-        mbar_init(&bar_s, 1);
-        mbar_init(&bar_o, 1);
-        mbar_init(&bar_kv[0], 1);
-        mbar_init(&bar_kv[1], 1);
+        s_abort = 0;
+        mbar_init(&bars.q, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&bars.kv_full[i], 1);
+            mbar_init(&bars.kv_empty[i], 1);
+        }
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(&bars.s[g], 1);
+            mbar_init(&bars.p[g], 4);
+            mbar_init(&bars.o[g], 1);
+        }
+        mbar_init(&bars.drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t tS = tmem;            // S / P columns [0,128)
-    const uint32_t tO = tmem + kColO;    // O columns [128,192)
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    bool failed = false;
 
-    // issue bookkeeping (thread 0), one counter per stage
-    int kv_issued0 = 0, kv_issued1 = 0, kv_done0 = 0, kv_done1 = 0;
-    int s_issued = 0, s_done = 0, o_issued = 0, o_done = 0;
-    bool q_issued = false, q_done = false;
-
-    if (tid == 0) {
-        mbar_expect_tx(&bar_q, kTileBytes);
-        tma_load_2d(sQ, &tmQ, xh, q0, &bar_q);
-        q_issued = true;
-        for (int t = 0; t < 2 && t < T; ++t) {
-            mbar_expect_tx(&bar_kv[t], 2 * kTileBytes);
-            tma_load_2d(sK(t), &tmK, xh, r0 + t * kTile, &bar_kv[t]);
-            tma_load_2d(sV(t), &tmV, xh, r0 + t * kTile, &bar_kv[t]);
-            if (t == 0) kv_issued0 = 1; else kv_issued1 = 1;
+    if (warp == 9) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int issued[kStages] = {0, 0, 0};
+            mbar_expect_tx(&bars.q, nq * kTileBytes);
+            for (int g = 0; g < nq; ++g) tma_load_2d(sQ(g), &tmQ, xh, q0 + g * kTile, &bars.q);
+            for (int j = 0; j < T && !failed; ++j) {
+                const int st = j % kStages;
+                if (j >= kStages && !mbar_wait(&bars.kv_empty[st], ((j / kStages) - 1) & 1)) { failed = true; break; }
+                mbar_expect_tx(&bars.kv_full[st], 2 * kTileBytes);
+                tma_load_2d(sK(st), &tmK, xh, r0 + j * kTile, &bars.kv_full[st]);
+                tma_load_2d(sV(st), &tmV, xh, r0 + j * kTile, &bars.kv_full[st]);
+                ++issued[st];
+            }
+            if (failed) {
+                atomicOr(err, DenseErr::kTimeout);
+                atomicExch(&s_abort, 1);
+                // drain this thread's copies in flight (bounded)
+                for (int st = 0; st < kStages; ++st)
+                    if (issued[st] > 0) mbar_wait(&bars.kv_full[st], (issued[st] - 1) & 1, kWaitCycles / 4);
+                mbar_wait(&bars.q, 0, kWaitCycles / 4);
+            }
         }
-    }
-
-    const uint32_t idS = idesc_bf16(128, 128, 0);
-    const uint32_t idO = idesc_bf16(128, 64, 1);
-    const uint64_t dQ = smem_desc_sw128(su32(sQ), 16, 1024);
-
-    float m_used = -INFINITY, l = 0.f;
-    bool aborted = false;
-
-    for (int j = 0; j < T; ++j) {
-        const int st = j & 1;
-        int fail = 0;
-        if (tid == 0) {
-            if (j > 0) {   // PV_{j-1} done: its K/V stage and the P columns are free
-                fail |= !mbar_wait(&bar_o, (o_done) & 1);
-                if (!fail) ++o_done;
-                if (!fail && j >= 1 && j + 1 < T) {
-                    const int ps = (j + 1) & 1;
-                    mbar_expect_tx(&bar_kv[ps], 2 * kTileBytes);
-                    tma_load_2d(sK(ps), &tmK, xh, r0 + (j + 1) * kTile, &bar_kv[ps]);
-                    tma_load_2d(sV(ps), &tmV, xh, r0 + (j + 1) * kTile, &bar_kv[ps]);
-                    if (ps == 0) ++kv_issued0; else ++kv_issued1;
-                }
-            }
-            if (!fail && !q_done) {
-                fail |= !mbar_wait(&bar_q, 0);
-                if (!fail) q_done = true;
-            }
-            if (!fail) {
-                const int kd = st == 0 ? kv_done0 : kv_done1;
-                fail |= !mbar_wait(&bar_kv[st], kd & 1);
-                if (!fail) { if (st == 0) ++kv_done0; else ++kv_done1; }
-            }
-            if (!fail) {
-                tc_fence_after();
+    } else if (warp == 8) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16(128, 128, 0);
+            const uint32_t idO = idesc_bf16(128, 64, 1);
+            auto issue_s = [&](int g, int st) {
+                const uint64_t dQ = smem_desc_sw128(su32(sQ(g)), 16, 1024);
                 const uint64_t dK = smem_desc_sw128(su32(sK(st)), 16, 1024);
 #pragma unroll
-                for (int k = 0; k < kD / 16; ++k)   // 32 bytes of K per step
-                    mma_ss(tS, dQ + (uint64_t)(2 * k), dK + (uint64_t)(2 * k), idS, k > 0);
-                tc_commit(&bar_s);
-                ++s_issued;
+                for (int k = 0; k < kD / 16; ++k)
+                    mma_ss(tmem + col_s(g), dQ + (uint64_t)(2 * k), dK + (uint64_t)(2 * k), idS, k > 0);
+                tc_commit(&bars.s[g]);
+            };
+            auto issue_pv = [&](int g, int st, int j) {
+                const uint64_t dV = smem_desc_sw128(su32(sV(st)), 8192, 1024);
+#pragma unroll
+                for (int s = 0; s < kTile / 16; ++s) {
+                    const uint32_t a_hi = tmem + col_s(g) + 32 * (s >> 1) + 8 * (s & 1);
+                    const uint64_t b = dV + (uint64_t)(s * (2048 >> 4));
+                    mma_ts(tmem + col_o(g), a_hi, b, idO, (j > 0 || s > 0) ? 1u : 0u);
+                    mma_ts(tmem + col_o(g), a_hi + 16, b, idO, 1u);
+                }
+                tc_commit(&bars.o[g]);
+            };
+            bool ok = mbar_wait(&bars.q, 0) && mbar_wait(&bars.kv_full[0], 0);
+            if (ok) {
+                tc_fence_after();
+                for (int g = 0; g < nq; ++g) issue_s(g, 0);
             }
-        }
-        if (__syncthreads_or(fail)) { aborted = true; break; }
-        fail = !mbar_wait(&bar_s, j & 1);
-        if (__syncthreads_or(fail)) { aborted = true; break; }
-        if (tid == 0) s_done = j + 1;
-        tc_fence_after();
-
-        // ---- softmax over this thread's row of S_j ----
-        uint32_t r[32];
-        float mt = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tS + lane_base + 32 * c, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mt = fmaxf(mt, __uint_as_float(r[i]) * sl2);
-        }
-        bool need = false;
-        float alpha = 1.f;
-        if (j == 0) {
-            m_used = mt;
-        } else if (mt > m_used + kRescaleThreshold) {
-            need = true;
-            alpha = ex2(m_used - mt);
-            m_used = mt;
-        }
-        if (__any_sync(0xffffffffu, need)) {   // rescale O (warp-collective TMEM access)
-            l *= alpha;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                tmem_ld32(tO + lane_base + 32 * c, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                tmem_st32(tO + lane_base + 32 * c, r);
+            for (int j = 0; ok && j < T; ++j) {
+                const int st = j % kStages;
+                const int nst = (j + 1) % kStages;
+                const bool more = j + 1 < T;
+                for (int g = 0; ok && g < nq; ++g) {
+                    ok = mbar_wait(&bars.p[g], j & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(g, st, j);
+                    if (more) {
+                        if (g == 0) ok = mbar_wait(&bars.kv_full[nst], ((j + 1) / kStages) & 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(g, nst);
+                    }
+                }
+                if (ok) tc_commit(&bars.kv_empty[st]);   // stage st free once these MMAs finish
             }
-            tmem_st_wait();
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tS + lane_base + 32 * c, r);
-            tmem_ld_wait();
-            uint32_t pk[32];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const float p0 = ex2(__uint_as_float(r[2 * q]) * sl2 - m_used);
-                const float p1 = ex2(__uint_as_float(r[2 * q + 1]) * sl2 - m_used);
-                l += p0 + p1;
-                const uint32_t hi = pack2_bf16(p0, p1);
-                const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
-                pk[q] = hi;
-                pk[16 + q] = pack2_bf16(p0 - h0, p1 - h1);
+            if (!ok) {
+                failed = true;
+                atomicOr(err, DenseErr::kTimeout);
+                atomicExch(&s_abort, 1);
             }
-            // kv 32c..32c+31: P_hi in cols 32c..32c+15, P_lo in cols 32c+16..32c+31
-            tmem_st32(tS + lane_base + 32 * c, pk);
+            // drain: everything this thread issued has finished before TMEM is freed
+            tc_commit(&bars.drain);
+            mbar_wait(&bars.drain, 0, kWaitCycles / 4);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint64_t dV = smem_desc_sw128(su32(sV(st)), 8192, 1024);
+    } else {
+        // ---------------- softmax warpgroups ----------------
+        const int g = warp >> 2;                       // query tile of this warpgroup
+        if (g < nq) {
+            const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            const uint32_t tS = tmem + col_s(g) + lane_base;
+            const uint32_t tO = tmem + col_o(g) + lane_base;
+            float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;
+            const bool pos = sl2 >= 0.f;
+            for (int j = 0; j < T; ++j) {
+                // warp-uniform decision: tcgen05.ld/st below are warp-collective
+                const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.s[g], j & 1) && !s_abort);
+                if (!ok) { failed = true; break; }
+                tc_fence_after();
+                uint32_t r[32];
+                float mraw = pos ? -INFINITY : INFINITY;
 #pragma unroll
-            for (int s = 0; s < kTile / 16; ++s) {    // 16 kv rows per step
-                const uint32_t a_hi = tS + 32 * (s >> 1) + 8 * (s & 1);
-                const uint32_t a_lo = a_hi + 16;
-                const uint64_t b = dV + (uint64_t)(s * (2048 >> 4));
-                mma_ts(tO, a_hi, b, idO, (j > 0 || s > 0) ? 1u : 0u);
-                mma_ts(tO, a_lo, b, idO, 1u);
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tS + 32 * c, r);
+                    tmem_ld_wait();
+                    if (pos) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, __uint_as_float(r[i]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) mraw = fminf(mraw, __uint_as_float(r[i]));
+                    }
+                }
+                const float mt = mraw * sl2;
+                bool need = false;
+                float alpha = 1.f;
+                if (j == 0) {
+                    m_used = mt;
+                } else if (mt > m_used + kRescaleThreshold) {
+                    need = true;
+                    alpha = ex2(m_used - mt);
+                    m_used = mt;
+                }
+                if (__any_sync(0xffffffffu, need)) {
+                    // PV_g of the previous tile is complete: this tile's S was
+                    // committed after it
+                    l0 *= alpha;
+                    l1 *= alpha;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_ld32(tO + 32 * c, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(tO + 32 * c, r);
+                    }
+                }
+                const float nm = -m_used;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(tS + 32 * c, r);
+                    tmem_ld_wait();
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float p0 = ex2(fmaf(__uint_as_float(r[2 * q]), sl2, nm));
+                        const float p1 = ex2(fmaf(__uint_as_float(r[2 * q + 1]), sl2, nm));
+                        l0 += p0;
+                        l1 += p1;
+                        const uint32_t hi = pack2_bf16(p0, p1);
+                        pk[q] = hi;
+                        pk[16 + q] = pack2_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
+                    }
+                    tmem_st32(tS + 32 * c, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(&bars.p[g])) : "memory");
             }
-            tc_commit(&bar_o);
-            ++o_issued;
-        }
-    }
-
-    if (!aborted) {
-        int fail = 0;
-        if (tid == 0) {
-            fail = !mbar_wait(&bar_o, o_done & 1);
-            if (!fail) ++o_done;
-        }
-        aborted = __syncthreads_or(fail) != 0;
-    }
-    if (!aborted) {
-        tc_fence_after();
-        const float inv = 1.f / l;
-        TO* o = out + static_cast<int64_t>(q0 + tid) * HD + xh;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + lane_base + 32 * c, r);
-            tmem_ld_wait();
-            if constexpr (sizeof(TO) == 2) {
-                uint4* o4 = reinterpret_cast<uint4*>(o + 32 * c);
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    o4[v] = make_uint4(pack2_bf16(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
-                                       pack2_bf16(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
-                                       pack2_bf16(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
-                                       pack2_bf16(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
+            if (!failed) failed = !__all_sync(0xffffffffu, mbar_wait(&bars.o[g], (T - 1) & 1));
+            if (failed) {
+                atomicOr(err, DenseErr::kTimeout);
+                atomicExch(&s_abort, 1);
             } else {
-                float4* o4 = reinterpret_cast<float4*>(o + 32 * c);
+                tc_fence_after();
+                const float inv = 1.f / (l0 + l1);
+                const int row = q0 + g * kTile + (warp & 3) * 32 + lane;
+                TO* o = out + static_cast<int64_t>(row) * HD + xh;
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    o4[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                        __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tO + 32 * c, r);
+                    tmem_ld_wait();
+                    if constexpr (sizeof(TO) == 2) {
+                        uint4* o4 = reinterpret_cast<uint4*>(o + 32 * c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            o4[v] = make_uint4(
+                                pack2_bf16(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
+                                pack2_bf16(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
+                                pack2_bf16(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
+                                pack2_bf16(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
+                    } else {
+                        float4* o4 = reinterpret_cast<float4*>(o + 32 * c);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v)
+                            o4[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                                __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+                    }
+                }
             }
         }
-    } else if (tid == 0) {
-        // record the timeout, then drain what this CTA still has in flight
-        // (bounded) before its tensor memory is released
-        atomicOr(err, DenseErr::kTimeout);
-        const long long drain = kWaitCycles / 4;
-        if (q_issued && !q_done) mbar_wait(&bar_q, 0, drain);
-        while (kv_done0 < kv_issued0 && mbar_wait(&bar_kv[0], kv_done0 & 1, drain)) ++kv_done0;
-        while (kv_done1 < kv_issued1 && mbar_wait(&bar_kv[1], kv_done1 & 1, drain)) ++kv_done1;
-        while (s_done < s_issued && mbar_wait(&bar_s, s_done & 1, drain)) ++s_done;
-        while (o_done < o_issued && mbar_wait(&bar_o, o_done & 1, drain)) ++o_done;
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemAll) : "memory");
     }
 }
 
@@ -460,16 +498,17 @@ gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void
     cudaError_t e;
     if (dt == GTATTN_BF16) {
         auto k = k_dense_attn<__nv_bfloat16>;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
         if (e == cudaSuccess) {
-            k<<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, tiles, static_cast<__nv_bfloat16*>(out), HD, sl2, err);
+            k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, static_cast<__nv_bfloat16*>(out), HD, sl2,
+                                                     err);
             e = cudaGetLastError();
         }
     } else {
         auto k = k_dense_attn<float>;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
         if (e == cudaSuccess) {
-            k<<<grid, kThreads, kSmemAlloc, s>>>(mq, mk, mv, tiles, static_cast<float*>(out), HD, sl2, err);
+            k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, static_cast<float*>(out), HD, sl2, err);
             e = cudaGetLastError();
         }
     }

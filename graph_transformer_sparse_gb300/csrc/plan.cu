@@ -280,9 +280,12 @@ extern "C" gtattn_status gtattn_csr_build(const int32_t* indptr, const int32_t* 
         std::vector<int2> hb(nb);
         if ((st = chk(cudaMemcpy(hb.data(), p->blocks, sizeof(int2) * nb, cudaMemcpyDeviceToHost))) != GTATTN_OK)
             return fail(st);
+        // one work item per pair of 128-row query tiles: (block row, block size,
+        // first query row, query tiles in the item)
         std::vector<int4> tiles;
         for (const int2& b : hb)
-            for (int q0 = b.x; q0 < b.x + b.y; q0 += kDenseTile) tiles.push_back(make_int4(b.x, b.y, q0, 0));
+            for (int q0 = b.x; q0 < b.x + b.y; q0 += 2 * kDenseTile)
+                tiles.push_back(make_int4(b.x, b.y, q0, std::min(2, (b.x + b.y - q0) / kDenseTile)));
         if ((st = chk(cudaMalloc(&p->dense_tiles, sizeof(int4) * tiles.size()))) != GTATTN_OK) return fail(st);
         if ((st = chk(cudaMemcpy(p->dense_tiles, tiles.data(), sizeof(int4) * tiles.size(),
                                  cudaMemcpyHostToDevice))) != GTATTN_OK)

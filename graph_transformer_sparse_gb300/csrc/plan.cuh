@@ -14,7 +14,7 @@ struct gtattn_plan {
     int2* chunks = nullptr;                 // (row, first entry) per chunk
     int2* longs = nullptr;                  // (row, first chunk) per split row
     int2* blocks = nullptr;                 // (first row, size) per dense block
-    int4* dense_tiles = nullptr;            // (block row, block size, query-tile row, 0)
+    int4* dense_tiles = nullptr;            // (block row, block size, first query row, query tiles)
     int n_dense_tiles = 0;
     int* dense_flag = nullptr;              // 1 for rows inside a dense block
     mutable void* ws = nullptr;             // split-row partials workspace

@@ -358,18 +358,30 @@ def gpu_arm(args):
     cbytes = compulsory_bytes(w.N, w.nnz, w.H, w.D, esize)
     ubytes = unique_bytes(w.N, w.nnz, w.H, w.D, esize)
 
-    rows_ms = prof["rows"]["ms"] / max(prof["rows"]["groups"], 1)
     launches_per_step = sum(v["launches"] for v in prof.values()) / args.steps
-    achieved = cbytes / (rows_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "k_rows_vec (fused row kernel)", "achieved": round(achieved, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": ncu_traffic("k_rows_vec", name),
-                "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
-                else "fallback 6.8 TB/s",
-                "algorithmic_bytes_per_launch": cbytes, "unique_bytes_floor": ubytes,
-                "kernel_ms": round(rows_ms, 5),
-                "kernel_shares": {k: round(v["ms"] / max(sum(x["ms"] for x in prof.values()), 1e-9), 4)
-                                  for k, v in prof.items() if v["launches"]}}
+    total_prof_ms = max(sum(x["ms"] for x in prof.values()), 1e-9)
+    shares = {k: round(v["ms"] / total_prof_ms, 4) for k, v in prof.items() if v["launches"]}
+    dominant = max(prof, key=lambda k: prof[k]["ms"])
+    kern_ms = prof[dominant]["ms"] / max(prof[dominant]["groups"], 1)
+    if dominant == "dense":
+        flops = dense_flops(info["n_dense_blocks"], w.N // max(info["n_dense_blocks"], 1), w.H, w.D)
+        achieved = flops / (kern_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "k_dense_attn (tcgen05 dense-block kernel)",
+                    "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "traffic": None,
+                    "peak_source": f"{peaks['source']} bf16_tflops (burst: the kernel is timed per launch)",
+                    "algorithmic_flops_per_launch": flops, "kernel_ms": round(kern_ms, 5),
+                    "kernel_shares": shares}
+    else:
+        achieved = cbytes / (kern_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "k_rows_vec (fused row kernel)", "achieved": round(achieved, 1),
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "traffic": ncu_traffic("k_rows_vec", name),
+                    "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
+                    if peaks["source"] == "measured" else "fallback 6.8 TB/s",
+                    "algorithmic_bytes_per_launch": cbytes, "unique_bytes_floor": ubytes,
+                    "kernel_ms": round(kern_ms, 5), "kernel_shares": shares}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,

@@ -171,7 +171,11 @@ struct DenseErr {
 // Warp roles of the CTA (10 warps): warps 0-3 run the softmax of query tile
 // A, warps 4-7 that of query tile B (the next 128 rows of the same block and
 // head), warp 8 issues the MMAs (one thread), warp 9 the TMA loads (one
-// thread).  The two query tiles share every K/V tile in shared memory.
+// thread).  The two query tiles share every K/V tile in shared memory.  The
+// grid is persistent (one CTA per SM): each CTA walks work items (a pair of
+// query tiles and a head); Q tiles are double-buffered and the K/V ring runs
+// on across items, so the next item's loads and first products overlap the
+// current item's last softmax and epilogue.
 constexpr int kWarps = 10;
 constexpr int kThreadsWS = kWarps * 32;
 constexpr int kStages = 3;                        // K/V ring
@@ -179,26 +183,65 @@ constexpr uint32_t kTmemAll = 512;                // S_A, S_B, O_A, O_B
 // TMEM columns of S_g / P_g and O_g for query tile g
 __host__ __device__ constexpr uint32_t col_s(int g) { return g == 0 ? 0u : 128u; }
 __host__ __device__ constexpr uint32_t col_o(int g) { return g == 0 ? 256u : 320u; }
-constexpr size_t kWsSmemQ = 0;                    // 2 query tiles
-constexpr size_t kWsSmemKV = 2 * kTileBytes;      // stage s: K at +0, V at +kTileBytes
-constexpr size_t kWsSmemBytes = 2 * kTileBytes + kStages * 2 * kTileBytes;   // 128 KB
+constexpr size_t kWsSmemQ = 0;                    // 2 buffers x 2 query tiles
+constexpr size_t kWsSmemKV = 4 * kTileBytes;      // stage s: K at +0, V at +kTileBytes
+constexpr size_t kWsSmemBytes = 4 * kTileBytes + kStages * 2 * kTileBytes;   // 160 KB
 constexpr size_t kWsSmemAlloc = kWsSmemBytes + 1024;
 
 struct WsBars {
-    uint64_t q;
+    uint64_t q_full[2], q_empty[2];   // Q buffers (TMA <-> MMA)
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s[2];      // S_g of the current tile is in TMEM (MMA -> softmax g)
-    uint64_t p[2];      // P_g written over S_g (softmax g -> MMA), 4 arrivals
-    uint64_t o[2];      // PV_g done (MMA -> softmax g, waited for the epilogue)
+    uint64_t s[2];       // S_g of the current tile is in TMEM (MMA -> softmax g)
+    uint64_t p[2];       // P_g written over S_g (softmax g -> MMA), 4 arrivals
+    uint64_t o[2];       // PV_g done (MMA -> softmax g, waited for the epilogue)
+    uint64_t o_free[2];  // softmax g has read O_g in its epilogue (-> MMA), 4 arrivals
     uint64_t drain;
 };
 
+// Work item w -> (block row, block size, first query row, query tiles) and head.
+__device__ __forceinline__ int4 item_of(const int4* items, int w, int H, int* head) {
+    *head = w % H;
+    return items[w / H];
+}
+
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {   // d += a
+    asm("{\n\t.reg .b64 ra, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+        "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+__device__ __forceinline__ void fsub2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 template <typename TO>
-__global__ void __launch_bounds__(kThreadsWS, 1)
+__global__ void __maxnreg__(200)
 k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-             const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ items, TO* __restrict__ out,
-             int HD, float sl2, int* __restrict__ err) {
+             const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ items, int n_work, int H,
+             TO* __restrict__ out, int HD, float sl2, int* __restrict__ err) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -209,12 +252,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int4 it = items[blockIdx.x];
-    const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w;   // nq: query tiles in this item (1 or 2)
-    const int h = blockIdx.y;
-    const int T = n / kTile;
-    const int xh = h * kD;
-    auto sQ = [&](int g) { return smem + kWsSmemQ + g * kTileBytes; };
+    auto sQ = [&](int buf, int g) { return smem + kWsSmemQ + (2 * buf + g) * kTileBytes; };
     auto sK = [&](int st) { return smem + kWsSmemKV + st * 2 * kTileBytes; };
     auto sV = [&](int st) { return smem + kWsSmemKV + st * 2 * kTileBytes + kTileBytes; };
 
@@ -226,7 +264,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     }
     if (tid == 0) {
         s_abort = 0;
-        mbar_init(&bars.q, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars.q_full[b], 1);
+            mbar_init(&bars.q_empty[b], 1);
+        }
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&bars.kv_full[i], 1);
             mbar_init(&bars.kv_empty[i], 1);
@@ -235,6 +276,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             mbar_init(&bars.s[g], 1);
             mbar_init(&bars.p[g], 4);
             mbar_init(&bars.o[g], 1);
+            mbar_init(&bars.o_free[g], 4);
         }
         mbar_init(&bars.drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -243,29 +285,42 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    bool failed = false;
 
     if (warp == 9) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            int issued[kStages] = {0, 0, 0};
-            mbar_expect_tx(&bars.q, nq * kTileBytes);
-            for (int g = 0; g < nq; ++g) tma_load_2d(sQ(g), &tmQ, xh, q0 + g * kTile, &bars.q);
-            for (int j = 0; j < T && !failed; ++j) {
-                const int st = j % kStages;
-                if (j >= kStages && !mbar_wait(&bars.kv_empty[st], ((j / kStages) - 1) & 1)) { failed = true; break; }
-                mbar_expect_tx(&bars.kv_full[st], 2 * kTileBytes);
-                tma_load_2d(sK(st), &tmK, xh, r0 + j * kTile, &bars.kv_full[st]);
-                tma_load_2d(sV(st), &tmV, xh, r0 + j * kTile, &bars.kv_full[st]);
-                ++issued[st];
+            bool ok = true;
+            int kv_tile = 0;   // running K/V tile counter over all items of this CTA
+            int q_issued[2] = {0, 0}, kv_issued[kStages] = {0, 0, 0};
+            int local = 0;
+            for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++local) {
+                int h;
+                const int4 it = item_of(items, w, H, &h);
+                const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = n / kTile, xh = h * kD;
+                const int qb = local & 1;
+                if (local >= 2) ok = mbar_wait(&bars.q_empty[qb], ((local >> 1) - 1) & 1);
+                if (!ok) break;
+                mbar_expect_tx(&bars.q_full[qb], nq * kTileBytes);
+                for (int g = 0; g < nq; ++g) tma_load_2d(sQ(qb, g), &tmQ, xh, q0 + g * kTile, &bars.q_full[qb]);
+                ++q_issued[qb];
+                for (int j = 0; j < T; ++j, ++kv_tile) {
+                    const int st = kv_tile % kStages;
+                    if (kv_tile >= kStages) ok = mbar_wait(&bars.kv_empty[st], ((kv_tile / kStages) - 1) & 1);
+                    if (!ok) break;
+                    mbar_expect_tx(&bars.kv_full[st], 2 * kTileBytes);
+                    tma_load_2d(sK(st), &tmK, xh, r0 + j * kTile, &bars.kv_full[st]);
+                    tma_load_2d(sV(st), &tmV, xh, r0 + j * kTile, &bars.kv_full[st]);
+                    ++kv_issued[st];
+                }
             }
-            if (failed) {
+            if (!ok) {
                 atomicOr(err, DenseErr::kTimeout);
                 atomicExch(&s_abort, 1);
                 // drain this thread's copies in flight (bounded)
                 for (int st = 0; st < kStages; ++st)
-                    if (issued[st] > 0) mbar_wait(&bars.kv_full[st], (issued[st] - 1) & 1, kWaitCycles / 4);
-                mbar_wait(&bars.q, 0, kWaitCycles / 4);
+                    if (kv_issued[st] > 0) mbar_wait(&bars.kv_full[st], (kv_issued[st] - 1) & 1, kWaitCycles / 4);
+                for (int b = 0; b < 2; ++b)
+                    if (q_issued[b] > 0) mbar_wait(&bars.q_full[b], (q_issued[b] - 1) & 1, kWaitCycles / 4);
             }
         }
     } else if (warp == 8) {
@@ -273,50 +328,67 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, 128, 0);
             const uint32_t idO = idesc_bf16(128, 64, 1);
-            auto issue_s = [&](int g, int st) {
-                const uint64_t dQ = smem_desc_sw128(su32(sQ(g)), 16, 1024);
-                const uint64_t dK = smem_desc_sw128(su32(sK(st)), 16, 1024);
+            bool ok = true;
+            int kv_tile = 0;
+            int p_cnt[2] = {0, 0}, item_g[2] = {0, 0};
+            int local = 0;
+            for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++local) {
+                int h;
+                const int4 it = item_of(items, w, H, &h);
+                const int nq = it.w, T = it.y / kTile;
+                const int qb = local & 1;
+                auto issue_s = [&](int g, int st) {
+                    const uint64_t dQ = smem_desc_sw128(su32(sQ(qb, g)), 16, 1024);
+                    const uint64_t dK = smem_desc_sw128(su32(sK(st)), 16, 1024);
 #pragma unroll
-                for (int k = 0; k < kD / 16; ++k)
-                    mma_ss(tmem + col_s(g), dQ + (uint64_t)(2 * k), dK + (uint64_t)(2 * k), idS, k > 0);
-                tc_commit(&bars.s[g]);
-            };
-            auto issue_pv = [&](int g, int st, int j) {
-                const uint64_t dV = smem_desc_sw128(su32(sV(st)), 8192, 1024);
+                    for (int k = 0; k < kD / 16; ++k)
+                        mma_ss(tmem + col_s(g), dQ + (uint64_t)(2 * k), dK + (uint64_t)(2 * k), idS, k > 0);
+                    tc_commit(&bars.s[g]);
+                };
+                auto issue_pv = [&](int g, int st, int j) {
+                    const uint64_t dV = smem_desc_sw128(su32(sV(st)), 8192, 1024);
 #pragma unroll
-                for (int s = 0; s < kTile / 16; ++s) {
-                    const uint32_t a_hi = tmem + col_s(g) + 32 * (s >> 1) + 8 * (s & 1);
-                    const uint64_t b = dV + (uint64_t)(s * (2048 >> 4));
-                    mma_ts(tmem + col_o(g), a_hi, b, idO, (j > 0 || s > 0) ? 1u : 0u);
-                    mma_ts(tmem + col_o(g), a_hi + 16, b, idO, 1u);
-                }
-                tc_commit(&bars.o[g]);
-            };
-            bool ok = mbar_wait(&bars.q, 0) && mbar_wait(&bars.kv_full[0], 0);
-            if (ok) {
+                    for (int s = 0; s < kTile / 16; ++s) {
+                        const uint32_t a_hi = tmem + col_s(g) + 32 * (s >> 1) + 8 * (s & 1);
+                        const uint64_t b = dV + (uint64_t)(s * (2048 >> 4));
+                        mma_ts(tmem + col_o(g), a_hi, b, idO, (j > 0 || s > 0) ? 1u : 0u);
+                        mma_ts(tmem + col_o(g), a_hi + 16, b, idO, 1u);
+                    }
+                    tc_commit(&bars.o[g]);
+                };
+                ok = mbar_wait(&bars.q_full[qb], (local >> 1) & 1) &&
+                     mbar_wait(&bars.kv_full[kv_tile % kStages], (kv_tile / kStages) & 1);
+                if (!ok) break;
                 tc_fence_after();
-                for (int g = 0; g < nq; ++g) issue_s(g, 0);
-            }
-            for (int j = 0; ok && j < T; ++j) {
-                const int st = j % kStages;
-                const int nst = (j + 1) % kStages;
-                const bool more = j + 1 < T;
-                for (int g = 0; ok && g < nq; ++g) {
-                    ok = mbar_wait(&bars.p[g], j & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(g, st, j);
-                    if (more) {
-                        if (g == 0) ok = mbar_wait(&bars.kv_full[nst], ((j + 1) / kStages) & 1);
+                for (int g = 0; g < nq; ++g) issue_s(g, kv_tile % kStages);
+                for (int j = 0; ok && j < T; ++j) {
+                    const int st = (kv_tile + j) % kStages;
+                    const int nt = kv_tile + j + 1;
+                    const bool more = j + 1 < T;
+                    for (int g = 0; ok && g < nq; ++g) {
+                        ok = mbar_wait(&bars.p[g], p_cnt[g] & 1);
+                        if (!ok) break;
+                        ++p_cnt[g];
+                        // the first product of an item overwrites O_g: the previous
+                        // item's epilogue must have read it
+                        if (j == 0 && item_g[g] > 0) ok = mbar_wait(&bars.o_free[g], (item_g[g] - 1) & 1);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_s(g, nst);
+                        issue_pv(g, st, j);
+                        if (more) {
+                            if (g == 0) ok = mbar_wait(&bars.kv_full[nt % kStages], (nt / kStages) & 1);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_s(g, nt % kStages);
+                        }
                     }
+                    if (ok) tc_commit(&bars.kv_empty[st]);   // stage free once these MMAs finish
                 }
-                if (ok) tc_commit(&bars.kv_empty[st]);   // stage st free once these MMAs finish
+                if (ok) tc_commit(&bars.q_empty[qb]);        // Q buffer free after this item's products
+                for (int g = 0; g < nq; ++g) ++item_g[g];
+                kv_tile += T;
             }
             if (!ok) {
-                failed = true;
                 atomicOr(err, DenseErr::kTimeout);
                 atomicExch(&s_abort, 1);
             }
@@ -327,32 +399,45 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     } else {
         // ---------------- softmax warpgroups ----------------
         const int g = warp >> 2;                       // query tile of this warpgroup
-        if (g < nq) {
-            const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            const uint32_t tS = tmem + col_s(g) + lane_base;
-            const uint32_t tO = tmem + col_o(g) + lane_base;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + col_s(g) + lane_base;
+        const uint32_t tO = tmem + col_o(g) + lane_base;
+        const bool pos = sl2 >= 0.f;
+        int s_cnt = 0, o_cnt = 0;
+        bool failed = false;
+        for (int w = blockIdx.x; !failed && w < n_work; w += gridDim.x) {
+            int h;
+            const int4 it = item_of(items, w, H, &h);
+            const int n = it.y, q0 = it.z, nq = it.w, T = n / kTile, xh = h * kD;
+            if (g >= nq) continue;
             float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;
-            const bool pos = sl2 >= 0.f;
             for (int j = 0; j < T; ++j) {
                 // warp-uniform decision: tcgen05.ld/st below are warp-collective
-                const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.s[g], j & 1) && !s_abort);
+                const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.s[g], s_cnt & 1) && !s_abort);
                 if (!ok) { failed = true; break; }
+                ++s_cnt;
                 tc_fence_after();
-                uint32_t r[32];
-                float mraw = pos ? -INFINITY : INFINITY;
+                uint32_t r[128];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tS + 32 * c, r);
-                    tmem_ld_wait();
-                    if (pos) {
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, r + 32 * c);
+                tmem_ld_wait();
+                float ma = pos ? -INFINITY : INFINITY, mb = ma;
+                if (pos) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, __uint_as_float(r[i]));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) mraw = fminf(mraw, __uint_as_float(r[i]));
+                    for (int i = 0; i < 128; i += 4) {
+                        ma = max3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                        mb = max3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
                     }
+                    ma = fmaxf(ma, mb);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 128; i += 4) {
+                        ma = min3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                        mb = min3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                    }
+                    ma = fminf(ma, mb);
                 }
-                const float mt = mraw * sl2;
+                const float mt = ma * sl2;
                 bool need = false;
                 float alpha = 1.f;
                 if (j == 0) {
@@ -367,31 +452,35 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     // committed after it
                     l0 *= alpha;
                     l1 *= alpha;
+                    uint32_t o[32];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        tmem_ld32(tO + 32 * c, r);
+                        tmem_ld32(tO + 32 * c, o);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tO + 32 * c, r);
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(tO + 32 * c, o);
+                        tmem_st_wait();
                     }
                 }
                 const float nm = -m_used;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(tS + 32 * c, r);
-                    tmem_ld_wait();
                     uint32_t pk[32];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
-                        const float p0 = ex2(fmaf(__uint_as_float(r[2 * q]), sl2, nm));
-                        const float p1 = ex2(fmaf(__uint_as_float(r[2 * q + 1]), sl2, nm));
-                        l0 += p0;
-                        l1 += p1;
+                        float t0, t1;
+                        ffma2(t0, t1, __uint_as_float(r[32 * c + 2 * q]), __uint_as_float(r[32 * c + 2 * q + 1]),
+                              sl2, nm);
+                        const float p0 = ex2(t0), p1 = ex2(t1);
+                        fadd2(l0, l1, p0, p1);
                         const uint32_t hi = pack2_bf16(p0, p1);
+                        float d0, d1;
+                        fsub2(d0, d1, p0, p1, __uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
                         pk[q] = hi;
-                        pk[16 + q] = pack2_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
+                        pk[16 + q] = pack2_bf16(d0, d1);
                     }
+                    // kv 32c..32c+31: P_hi in cols 32c..32c+15, P_lo in cols 32c+16..32c+31
                     tmem_st32(tS + 32 * c, pk);
                 }
                 tmem_st_wait();
@@ -399,38 +488,41 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 __syncwarp();
                 if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(&bars.p[g])) : "memory");
             }
-            if (!failed) failed = !__all_sync(0xffffffffu, mbar_wait(&bars.o[g], (T - 1) & 1));
-            if (failed) {
-                atomicOr(err, DenseErr::kTimeout);
-                atomicExch(&s_abort, 1);
+            if (failed) break;
+            // epilogue: O_g after the item's last product
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars.o[g], (o_cnt + T - 1) & 1))) { failed = true; break; }
+            o_cnt += T;
+            tc_fence_after();
+            uint32_t o[64];
+            tmem_ld32(tO, o);
+            tmem_ld32(tO + 32, o + 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(&bars.o_free[g])) : "memory");
+            const float inv = 1.f / (l0 + l1);
+            const int row = q0 + g * kTile + (warp & 3) * 32 + lane;
+            TO* op = out + static_cast<int64_t>(row) * HD + xh;
+            if constexpr (sizeof(TO) == 2) {
+                uint4* o4 = reinterpret_cast<uint4*>(op);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    o4[v] = make_uint4(
+                        pack2_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
+                        pack2_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
+                        pack2_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
+                        pack2_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
             } else {
-                tc_fence_after();
-                const float inv = 1.f / (l0 + l1);
-                const int row = q0 + g * kTile + (warp & 3) * 32 + lane;
-                TO* o = out + static_cast<int64_t>(row) * HD + xh;
+                float4* o4 = reinterpret_cast<float4*>(op);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + 32 * c, r);
-                    tmem_ld_wait();
-                    if constexpr (sizeof(TO) == 2) {
-                        uint4* o4 = reinterpret_cast<uint4*>(o + 32 * c);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            o4[v] = make_uint4(
-                                pack2_bf16(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
-                                pack2_bf16(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
-                                pack2_bf16(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
-                                pack2_bf16(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
-                    } else {
-                        float4* o4 = reinterpret_cast<float4*>(o + 32 * c);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            o4[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                                __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
-                    }
-                }
+                for (int v = 0; v < 16; ++v)
+                    o4[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                        __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
             }
+        }
+        if (failed) {
+            atomicOr(err, DenseErr::kTimeout);
+            atomicExch(&s_abort, 1);
         }
     }
     tc_fence_before();
@@ -494,21 +586,23 @@ gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void
     if (!make_map(&mq, Q, N, HD) || !make_map(&mk, K, N, HD) || !make_map(&mv, V, N, HD))
         return GTATTN_ERR_UNSUPPORTED;
     const float sl2 = scale * kLog2e;
-    dim3 grid(n_tiles, H);
+    const int n_work = n_tiles * H;
+    const int grid = std::min(n_work, num_sms());
     cudaError_t e;
     if (dt == GTATTN_BF16) {
         auto k = k_dense_attn<__nv_bfloat16>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
         if (e == cudaSuccess) {
-            k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, static_cast<__nv_bfloat16*>(out), HD, sl2,
-                                                     err);
+            k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, n_work, H,
+                                                     static_cast<__nv_bfloat16*>(out), HD, sl2, err);
             e = cudaGetLastError();
         }
     } else {
         auto k = k_dense_attn<float>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
         if (e == cudaSuccess) {
-            k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, static_cast<float*>(out), HD, sl2, err);
+            k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, n_work, H, static_cast<float*>(out), HD,
+                                                     sl2, err);
             e = cudaGetLastError();
         }
     }

@@ -238,7 +238,7 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
 }
 
 template <typename TO>
-__global__ void __maxnreg__(200)
+__global__ void __maxnreg__(168)   // 3 warps share an SM sub-partition: 3 x 168 x 32 <= 16384
 k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ items, int n_work, int H,
              TO* __restrict__ out, int HD, float sl2, int* __restrict__ err) {
@@ -417,27 +417,29 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 if (!ok) { failed = true; break; }
                 ++s_cnt;
                 tc_fence_after();
-                uint32_t r[128];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, r + 32 * c);
-                tmem_ld_wait();
+                // pass 1: row max over the 128 scores (two 64-column halves)
+                uint32_t r[64];
                 float ma = pos ? -INFINITY : INFINITY, mb = ma;
-                if (pos) {
 #pragma unroll
-                    for (int i = 0; i < 128; i += 4) {
-                        ma = max3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                        mb = max3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                    }
-                    ma = fmaxf(ma, mb);
-                } else {
+                for (int half = 0; half < 2; ++half) {
+                    tmem_ld32(tS + 64 * half, r);
+                    tmem_ld32(tS + 64 * half + 32, r + 32);
+                    tmem_ld_wait();
+                    if (pos) {
 #pragma unroll
-                    for (int i = 0; i < 128; i += 4) {
-                        ma = min3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                        mb = min3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                        for (int i = 0; i < 64; i += 4) {
+                            ma = max3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                            mb = max3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; i += 4) {
+                            ma = min3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                            mb = min3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                        }
                     }
-                    ma = fminf(ma, mb);
                 }
-                const float mt = ma * sl2;
+                const float mt = (pos ? fmaxf(ma, mb) : fminf(ma, mb)) * sl2;
                 bool need = false;
                 float alpha = 1.f;
                 if (j == 0) {
@@ -452,36 +454,42 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     // committed after it
                     l0 *= alpha;
                     l1 *= alpha;
-                    uint32_t o[32];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        tmem_ld32(tO + 32 * c, o);
+                        tmem_ld32(tO + 32 * c, r);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(tO + 32 * c, o);
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(tO + 32 * c, r);
                         tmem_st_wait();
                     }
                 }
+                // pass 2: P = 2^(s*scale*log2e - m) as bf16 hi/lo over S
                 const float nm = -m_used;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[32];
+                for (int half = 0; half < 2; ++half) {
+                    tmem_ld32(tS + 64 * half, r);
+                    tmem_ld32(tS + 64 * half + 32, r + 32);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        float t0, t1;
-                        ffma2(t0, t1, __uint_as_float(r[32 * c + 2 * q]), __uint_as_float(r[32 * c + 2 * q + 1]),
-                              sl2, nm);
-                        const float p0 = ex2(t0), p1 = ex2(t1);
-                        fadd2(l0, l1, p0, p1);
-                        const uint32_t hi = pack2_bf16(p0, p1);
-                        float d0, d1;
-                        fsub2(d0, d1, p0, p1, __uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
-                        pk[q] = hi;
-                        pk[16 + q] = pack2_bf16(d0, d1);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            float t0, t1;
+                            ffma2(t0, t1, __uint_as_float(r[32 * cc + 2 * q]), __uint_as_float(r[32 * cc + 2 * q + 1]),
+                                  sl2, nm);
+                            const float p0 = ex2(t0), p1 = ex2(t1);
+                            fadd2(l0, l1, p0, p1);
+                            const uint32_t hi = pack2_bf16(p0, p1);
+                            float d0, d1;
+                            fsub2(d0, d1, p0, p1, __uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+                            pk[q] = hi;
+                            pk[16 + q] = pack2_bf16(d0, d1);
+                        }
+                        // kv 32c..32c+31: P_hi in cols 32c..32c+15, P_lo in cols 32c+16..32c+31
+                        tmem_st32(tS + 64 * half + 32 * cc, pk);
                     }
-                    // kv 32c..32c+31: P_hi in cols 32c..32c+15, P_lo in cols 32c+16..32c+31
-                    tmem_st32(tS + 32 * c, pk);
                 }
                 tmem_st_wait();
                 tc_fence_before();

@@ -168,16 +168,22 @@ struct DenseErr {
     static constexpr int kTimeout = 1;
 };
 
-// Warp roles of the CTA (10 warps): warps 0-3 run the softmax of query tile
-// A, warps 4-7 that of query tile B (the next 128 rows of the same block and
-// head), warp 8 issues the MMAs (one thread), warp 9 the TMA loads (one
-// thread).  The two query tiles share every K/V tile in shared memory.  The
-// grid is persistent (one CTA per SM): each CTA walks work items (a pair of
-// query tiles and a head); Q tiles are double-buffered and the K/V ring runs
-// on across items, so the next item's loads and first products overlap the
-// current item's last softmax and epilogue.
-constexpr int kWarps = 10;
+// Warp roles of the CTA (20 warps).  Two query tiles per work item (A: rows
+// q0.., B: rows q0+128..) share every K/V tile.  Each query tile has two
+// softmax warpgroups that split the 128 key columns of a tile (half 0: keys
+// 0-63, half 1: keys 64-127) and exchange row maxima through shared memory:
+//   warps 0-3 / 4-7     tile A, halves 0 / 1
+//   warps 8-11 / 12-15  tile B, halves 0 / 1
+//   warp 16             MMA issue (one thread)
+//   warp 17             TMA loads (one thread); warps 18-19 idle
+// The grid is persistent (one CTA per SM): each CTA walks work items (a pair
+// of query tiles and a head); Q tiles are double-buffered and the K/V ring
+// runs on across items, so the next item's loads and first products overlap
+// the current item's last softmax and epilogue.
+constexpr int kWarps = 20;
 constexpr int kThreadsWS = kWarps * 32;
+constexpr int kMmaWarp = 16;
+constexpr int kTmaWarp = 17;
 constexpr int kStages = 3;                        // K/V ring
 constexpr uint32_t kTmemAll = 512;                // S_A, S_B, O_A, O_B
 // TMEM columns of S_g / P_g and O_g for query tile g
@@ -193,9 +199,9 @@ struct WsBars {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s[2];       // S_g of the current tile is in TMEM (MMA -> softmax g)
-    uint64_t p[2];       // P_g written over S_g (softmax g -> MMA), 4 arrivals
+    uint64_t p[2];       // P_g written over S_g (softmax g -> MMA), 8 warp arrivals
     uint64_t o[2];       // PV_g done (MMA -> softmax g, waited for the epilogue)
-    uint64_t o_free[2];  // softmax g has read O_g in its epilogue (-> MMA), 4 arrivals
+    uint64_t o_free[2];  // softmax g has read O_g in its epilogue (-> MMA), 8 arrivals
     uint64_t drain;
 };
 
@@ -236,9 +242,28 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
     asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
+// barrier over the 256 threads (8 warps) of one query tile's two warpgroups
+__device__ __forceinline__ void tile_bar(int g) {
+    asm volatile("bar.sync %0, 256;" ::"r"(1 + g) : "memory");
+}
+// OR of `pred` over the same 256 threads, returned to all of them (also a
+// barrier): keeps every decision that precedes a tile_bar uniform
+__device__ __forceinline__ bool tile_any(int g, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(1 + g)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
 
 template <typename TO>
-__global__ void __maxnreg__(168)   // 3 warps share an SM sub-partition: 3 x 168 x 32 <= 16384
+__global__ void __maxnreg__(96)   // 5 warps share an SM sub-partition: 5 x 96 x 32 <= 16384
 k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ items, int n_work, int H,
              TO* __restrict__ out, int HD, float sl2, int* __restrict__ err) {
@@ -248,6 +273,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     __shared__ __align__(8) WsBars bars;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
+    __shared__ float s_red[2][2][2][kTile];   // [tile g][parity][half][row]: row maxima, then row sums
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -274,9 +300,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(&bars.s[g], 1);
-            mbar_init(&bars.p[g], 4);
+            mbar_init(&bars.p[g], 8);
             mbar_init(&bars.o[g], 1);
-            mbar_init(&bars.o_free[g], 4);
+            mbar_init(&bars.o_free[g], 8);
         }
         mbar_init(&bars.drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -286,12 +312,11 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (warp == 9) {
+    if (warp == kTmaWarp) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             bool ok = true;
             int kv_tile = 0;   // running K/V tile counter over all items of this CTA
-            int q_issued[2] = {0, 0}, kv_issued[kStages] = {0, 0, 0};
             int local = 0;
             for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++local) {
                 int h;
@@ -302,7 +327,6 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 if (!ok) break;
                 mbar_expect_tx(&bars.q_full[qb], nq * kTileBytes);
                 for (int g = 0; g < nq; ++g) tma_load_2d(sQ(qb, g), &tmQ, xh, q0 + g * kTile, &bars.q_full[qb]);
-                ++q_issued[qb];
                 for (int j = 0; j < T; ++j, ++kv_tile) {
                     const int st = kv_tile % kStages;
                     if (kv_tile >= kStages) ok = mbar_wait(&bars.kv_empty[st], ((kv_tile / kStages) - 1) & 1);
@@ -310,27 +334,31 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     mbar_expect_tx(&bars.kv_full[st], 2 * kTileBytes);
                     tma_load_2d(sK(st), &tmK, xh, r0 + j * kTile, &bars.kv_full[st]);
                     tma_load_2d(sV(st), &tmV, xh, r0 + j * kTile, &bars.kv_full[st]);
-                    ++kv_issued[st];
                 }
             }
             if (!ok) {
                 atomicOr(err, DenseErr::kTimeout);
                 atomicExch(&s_abort, 1);
-                // drain this thread's copies in flight (bounded)
-                for (int st = 0; st < kStages; ++st)
-                    if (kv_issued[st] > 0) mbar_wait(&bars.kv_full[st], (kv_issued[st] - 1) & 1, kWaitCycles / 4);
-                for (int b = 0; b < 2; ++b)
-                    if (q_issued[b] > 0) mbar_wait(&bars.q_full[b], (q_issued[b] - 1) & 1, kWaitCycles / 4);
+                // drain this thread's copies in flight (bounded): the last use
+                // of every stage and of both Q buffers
+                for (int st = 0; st < kStages; ++st) {
+                    const int uses = kv_tile / kStages + (st < kv_tile % kStages ? 1 : 0);
+                    if (uses > 0) mbar_wait(&bars.kv_full[st], (uses - 1) & 1, kWaitCycles / 4);
+                }
+                for (int b = 0; b < 2; ++b) {
+                    const int uses = (local + 1 - b) / 2;
+                    if (uses > 0) mbar_wait(&bars.q_full[b], (uses - 1) & 1, kWaitCycles / 4);
+                }
             }
         }
-    } else if (warp == 8) {
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, 128, 0);
             const uint32_t idO = idesc_bf16(128, 64, 1);
             bool ok = true;
             int kv_tile = 0;
-            int p_cnt[2] = {0, 0}, item_g[2] = {0, 0};
+            int p_cnt0 = 0, p_cnt1 = 0, items0 = 0, items1 = 0;
             int local = 0;
             for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++local) {
                 int h;
@@ -366,12 +394,14 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     const int nt = kv_tile + j + 1;
                     const bool more = j + 1 < T;
                     for (int g = 0; ok && g < nq; ++g) {
-                        ok = mbar_wait(&bars.p[g], p_cnt[g] & 1);
+                        int& pc = g == 0 ? p_cnt0 : p_cnt1;
+                        const int done_items = g == 0 ? items0 : items1;
+                        ok = mbar_wait(&bars.p[g], pc & 1);
                         if (!ok) break;
-                        ++p_cnt[g];
+                        ++pc;
                         // the first product of an item overwrites O_g: the previous
                         // item's epilogue must have read it
-                        if (j == 0 && item_g[g] > 0) ok = mbar_wait(&bars.o_free[g], (item_g[g] - 1) & 1);
+                        if (j == 0 && done_items > 0) ok = mbar_wait(&bars.o_free[g], (done_items - 1) & 1);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(g, st, j);
@@ -385,7 +415,8 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     if (ok) tc_commit(&bars.kv_empty[st]);   // stage free once these MMAs finish
                 }
                 if (ok) tc_commit(&bars.q_empty[qb]);        // Q buffer free after this item's products
-                for (int g = 0; g < nq; ++g) ++item_g[g];
+                ++items0;
+                if (nq > 1) ++items1;
                 kv_tile += T;
             }
             if (!ok) {
@@ -396,14 +427,16 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             tc_commit(&bars.drain);
             mbar_wait(&bars.drain, 0, kWaitCycles / 4);
         }
-    } else {
+    } else if (warp < kMmaWarp) {
         // ---------------- softmax warpgroups ----------------
-        const int g = warp >> 2;                       // query tile of this warpgroup
+        const int g = warp >> 3;                       // query tile
+        const int half = (warp >> 2) & 1;              // key columns 64*half .. 64*half+63
+        const int row = (warp & 3) * 32 + lane;        // row of the query tile (= TMEM lane)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + col_s(g) + lane_base;
-        const uint32_t tO = tmem + col_o(g) + lane_base;
+        const uint32_t tS = tmem + col_s(g) + lane_base + 64 * half;
+        const uint32_t tO = tmem + col_o(g) + lane_base + 32 * half;
         const bool pos = sl2 >= 0.f;
-        int s_cnt = 0, o_cnt = 0;
+        int s_cnt = 0, o_cnt = 0, par = 0;
         bool failed = false;
         for (int w = blockIdx.x; !failed && w < n_work; w += gridDim.x) {
             int h;
@@ -412,34 +445,39 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             if (g >= nq) continue;
             float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;
             for (int j = 0; j < T; ++j) {
-                // warp-uniform decision: tcgen05.ld/st below are warp-collective
-                const bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.s[g], s_cnt & 1) && !s_abort);
-                if (!ok) { failed = true; break; }
+                // decision uniform over the tile's 8 warps (tcgen05.ld/st are
+                // warp-collective and the row-max exchange is a tile barrier)
+                const bool mine = !mbar_wait(&bars.s[g], s_cnt & 1) || s_abort;
+                if (tile_any(g, mine)) { failed = true; break; }
                 ++s_cnt;
                 tc_fence_after();
-                // pass 1: row max over the 128 scores (two 64-column halves)
                 uint32_t r[64];
+                tmem_ld32(tS, r);
+                tmem_ld32(tS + 32, r + 32);
+                tmem_ld_wait();
                 float ma = pos ? -INFINITY : INFINITY, mb = ma;
+                if (pos) {
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tS + 64 * half, r);
-                    tmem_ld32(tS + 64 * half + 32, r + 32);
-                    tmem_ld_wait();
-                    if (pos) {
-#pragma unroll
-                        for (int i = 0; i < 64; i += 4) {
-                            ma = max3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                            mb = max3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 64; i += 4) {
-                            ma = min3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                            mb = min3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                        }
+                    for (int i = 0; i < 64; i += 4) {
+                        ma = max3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                        mb = max3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
                     }
+                    ma = fmaxf(ma, mb);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; i += 4) {
+                        ma = min3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                        mb = min3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                    }
+                    ma = fminf(ma, mb);
                 }
-                const float mt = (pos ? fmaxf(ma, mb) : fminf(ma, mb)) * sl2;
+                // the other half's extreme (parity double-buffer: the slot written
+                // now was last read before the previous tile's barrier)
+                s_red[g][par][half][row] = ma;
+                tile_bar(g);
+                const float other = s_red[g][par][half ^ 1][row];
+                par ^= 1;
+                const float mt = (pos ? fmaxf(ma, other) : fminf(ma, other)) * sl2;
                 bool need = false;
                 float alpha = 1.f;
                 if (j == 0) {
@@ -450,71 +488,67 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     m_used = mt;
                 }
                 if (__any_sync(0xffffffffu, need)) {
-                    // PV_g of the previous tile is complete: this tile's S was
-                    // committed after it
+                    // PV_g of the previous tile is complete (this tile's S was
+                    // committed after it): rescale this half's 32 columns of O_g
                     l0 *= alpha;
                     l1 *= alpha;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        tmem_ld32(tO + 32 * c, r);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tO + 32 * c, r);
-                        tmem_st_wait();
-                    }
-                }
-                // pass 2: P = 2^(s*scale*log2e - m) as bf16 hi/lo over S
-                const float nm = -m_used;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(tS + 64 * half, r);
-                    tmem_ld32(tS + 64 * half + 32, r + 32);
+                    uint32_t o[32];
+                    tmem_ld32(tO, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t pk[32];
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(tO, o);
+                    tmem_st_wait();
+                }
+                // P = 2^(s*scale*log2e - m) as bf16 hi/lo over this half of S,
+                // 32 keys at a time (re-read from TMEM to keep registers low)
+                const float nm = -m_used;
+#pragma unroll 1
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t x[32], pk[32];
+                    tmem_ld32(tS + 32 * cc, x);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) {
-                            float t0, t1;
-                            ffma2(t0, t1, __uint_as_float(r[32 * cc + 2 * q]), __uint_as_float(r[32 * cc + 2 * q + 1]),
-                                  sl2, nm);
-                            const float p0 = ex2(t0), p1 = ex2(t1);
-                            fadd2(l0, l1, p0, p1);
-                            const uint32_t hi = pack2_bf16(p0, p1);
-                            float d0, d1;
-                            fsub2(d0, d1, p0, p1, __uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
-                            pk[q] = hi;
-                            pk[16 + q] = pack2_bf16(d0, d1);
-                        }
-                        // kv 32c..32c+31: P_hi in cols 32c..32c+15, P_lo in cols 32c+16..32c+31
-                        tmem_st32(tS + 64 * half + 32 * cc, pk);
+                    for (int q = 0; q < 16; ++q) {
+                        float t0, t1;
+                        ffma2(t0, t1, __uint_as_float(x[2 * q]), __uint_as_float(x[2 * q + 1]), sl2, nm);
+                        const float p0 = ex2(t0), p1 = ex2(t1);
+                        fadd2(l0, l1, p0, p1);
+                        const uint32_t hi = pack2_bf16(p0, p1);
+                        float d0, d1;
+                        fsub2(d0, d1, p0, p1, __uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+                        pk[q] = hi;
+                        pk[16 + q] = pack2_bf16(d0, d1);
                     }
+                    // keys 32c..32c+31 (c = 2*half + cc): P_hi in cols 32c..32c+15,
+                    // P_lo in cols 32c+16..32c+31
+                    tmem_st32(tS + 32 * cc, pk);
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(&bars.p[g])) : "memory");
+                if (lane == 0) mbar_arrive(&bars.p[g]);
             }
             if (failed) break;
-            // epilogue: O_g after the item's last product
-            if (!__all_sync(0xffffffffu, mbar_wait(&bars.o[g], (o_cnt + T - 1) & 1))) { failed = true; break; }
+            // epilogue: O_g after the item's last product; row sum from both halves
+            if (tile_any(g, !mbar_wait(&bars.o[g], (o_cnt + T - 1) & 1))) { failed = true; break; }
             o_cnt += T;
             tc_fence_after();
-            uint32_t o[64];
+            uint32_t o[32];
             tmem_ld32(tO, o);
-            tmem_ld32(tO + 32, o + 32);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(&bars.o_free[g])) : "memory");
-            const float inv = 1.f / (l0 + l1);
-            const int row = q0 + g * kTile + (warp & 3) * 32 + lane;
-            TO* op = out + static_cast<int64_t>(row) * HD + xh;
+            if (lane == 0) mbar_arrive(&bars.o_free[g]);
+            s_red[g][par][half][row] = l0 + l1;
+            tile_bar(g);
+            const float inv = 1.f / (l0 + l1 + s_red[g][par][half ^ 1][row]);
+            par ^= 1;
+            TO* op = out + static_cast<int64_t>(q0 + g * kTile + row) * HD + xh + 32 * half;
             if constexpr (sizeof(TO) == 2) {
                 uint4* o4 = reinterpret_cast<uint4*>(op);
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
+                for (int v = 0; v < 4; ++v)
                     o4[v] = make_uint4(
                         pack2_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
                         pack2_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
@@ -523,7 +557,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             } else {
                 float4* o4 = reinterpret_cast<float4*>(op);
 #pragma unroll
-                for (int v = 0; v < 16; ++v)
+                for (int v = 0; v < 8; ++v)
                     o4[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
                                         __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
             }

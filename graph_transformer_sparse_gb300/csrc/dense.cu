@@ -184,21 +184,25 @@ constexpr int kWarps = 20;
 constexpr int kThreadsWS = kWarps * 32;
 constexpr int kMmaWarp = 16;
 constexpr int kTmaWarp = 17;
-constexpr int kStages = 3;                        // K/V ring
-constexpr uint32_t kTmemAll = 512;                // S_A, S_B, O_A, O_B
-// TMEM columns of S_g / P_g and O_g for query tile g
-__host__ __device__ constexpr uint32_t col_s(int g) { return g == 0 ? 0u : 128u; }
-__host__ __device__ constexpr uint32_t col_o(int g) { return g == 0 ? 256u : 320u; }
+constexpr int kStages = 4;                        // K/V ring
+constexpr uint32_t kTmemAll = 512;
+// TMEM: three S/P buffers (128 columns each) used in rotation by the S tiles
+// of both query tiles -- S number k (A0, B0, A1, B1, ... within the CTA's
+// sequence) lives in buffer k % 3 and its P is written over it -- then O_A, O_B.
+__host__ __device__ constexpr uint32_t col_buf(int b) { return 128u * static_cast<uint32_t>(b); }
+__host__ __device__ constexpr uint32_t col_o(int g) { return g == 0 ? 384u : 448u; }
 constexpr size_t kWsSmemQ = 0;                    // 2 buffers x 2 query tiles
 constexpr size_t kWsSmemKV = 4 * kTileBytes;      // stage s: K at +0, V at +kTileBytes
-constexpr size_t kWsSmemBytes = 4 * kTileBytes + kStages * 2 * kTileBytes;   // 160 KB
+constexpr size_t kWsSmemBytes = 4 * kTileBytes + kStages * 2 * kTileBytes;   // 192 KB
 constexpr size_t kWsSmemAlloc = kWsSmemBytes + 1024;
 
 struct WsBars {
     uint64_t q_full[2], q_empty[2];   // Q buffers (TMA <-> MMA)
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s[2];       // S_g of the current tile is in TMEM (MMA -> softmax g)
+    uint64_t s[2][2];    // S tile n of query tile g is in TMEM: barrier s[g][n & 1]
+                         // (MMA -> softmax g; two barriers because an S tile
+                         // can run two ahead of its softmax)
     uint64_t p[2];       // P_g written over S_g (softmax g -> MMA), 8 warp arrivals
     uint64_t o[2];       // PV_g done (MMA -> softmax g, waited for the epilogue)
     uint64_t o_free[2];  // softmax g has read O_g in its epilogue (-> MMA), 8 arrivals
@@ -299,7 +303,8 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             mbar_init(&bars.kv_empty[i], 1);
         }
         for (int g = 0; g < 2; ++g) {
-            mbar_init(&bars.s[g], 1);
+            mbar_init(&bars.s[g][0], 1);
+            mbar_init(&bars.s[g][1], 1);
             mbar_init(&bars.p[g], 8);
             mbar_init(&bars.o[g], 1);
             mbar_init(&bars.o_free[g], 8);
@@ -353,11 +358,17 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
+        // Order per item (two query tiles): S_A0 S_B0 S_A1, then per key tile j:
+        // PV_Aj, S_B(j+1), PV_Bj, S_A(j+2).  An S tile is computed one step ahead
+        // of its softmax; a buffer is reused only after the PV that read its P
+        // (the tensor pipe executes one thread's MMAs in issue order).
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, 128, 0);
             const uint32_t idO = idesc_bf16(128, 64, 1);
             bool ok = true;
-            int kv_tile = 0;
+            int kv_tile = 0;   // first K/V tile of the current item in the CTA's sequence
+            int snum = 0;      // S tiles issued so far (buffer = snum % 3)
+            int sg0 = 0, sg1 = 0;   // S tiles issued per query tile (barrier s[g][n & 1])
             int p_cnt0 = 0, p_cnt1 = 0, items0 = 0, items1 = 0;
             int local = 0;
             for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++local) {
@@ -365,54 +376,60 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 const int4 it = item_of(items, w, H, &h);
                 const int nq = it.w, T = it.y / kTile;
                 const int qb = local & 1;
-                auto issue_s = [&](int g, int st) {
+                const int s0 = snum;   // S number of (g, j) = s0 + nq*j + g
+                auto bufk = [&](int g, int j) { return (s0 + nq * j + g) % 3; };
+                auto issue_s = [&](int g, int j) {
+                    const int kt = kv_tile + j;
+                    if (g == 0 && !mbar_wait(&bars.kv_full[kt % kStages], (kt / kStages) & 1)) return false;
+                    tc_fence_after();
                     const uint64_t dQ = smem_desc_sw128(su32(sQ(qb, g)), 16, 1024);
-                    const uint64_t dK = smem_desc_sw128(su32(sK(st)), 16, 1024);
+                    const uint64_t dK = smem_desc_sw128(su32(sK(kt % kStages)), 16, 1024);
+                    const uint32_t d = tmem + col_buf(bufk(g, j));
 #pragma unroll
                     for (int k = 0; k < kD / 16; ++k)
-                        mma_ss(tmem + col_s(g), dQ + (uint64_t)(2 * k), dK + (uint64_t)(2 * k), idS, k > 0);
-                    tc_commit(&bars.s[g]);
+                        mma_ss(d, dQ + (uint64_t)(2 * k), dK + (uint64_t)(2 * k), idS, k > 0);
+                    int& sn = g == 0 ? sg0 : sg1;
+                    tc_commit(&bars.s[g][sn & 1]);
+                    ++sn;
+                    ++snum;
+                    return true;
                 };
-                auto issue_pv = [&](int g, int st, int j) {
-                    const uint64_t dV = smem_desc_sw128(su32(sV(st)), 8192, 1024);
+                auto issue_pv = [&](int g, int j) {
+                    int& pc = g == 0 ? p_cnt0 : p_cnt1;
+                    const int done_items = g == 0 ? items0 : items1;
+                    if (!mbar_wait(&bars.p[g], pc & 1)) return false;
+                    ++pc;
+                    // the first product of an item overwrites O_g: the previous
+                    // item's epilogue must have read it
+                    if (j == 0 && done_items > 0 && !mbar_wait(&bars.o_free[g], (done_items - 1) & 1)) return false;
+                    tc_fence_after();
+                    const int kt = kv_tile + j;
+                    const uint64_t dV = smem_desc_sw128(su32(sV(kt % kStages)), 8192, 1024);
+                    const uint32_t pbuf = tmem + col_buf(bufk(g, j));
 #pragma unroll
                     for (int s = 0; s < kTile / 16; ++s) {
-                        const uint32_t a_hi = tmem + col_s(g) + 32 * (s >> 1) + 8 * (s & 1);
+                        const uint32_t a_hi = pbuf + 32 * (s >> 1) + 8 * (s & 1);
                         const uint64_t b = dV + (uint64_t)(s * (2048 >> 4));
                         mma_ts(tmem + col_o(g), a_hi, b, idO, (j > 0 || s > 0) ? 1u : 0u);
                         mma_ts(tmem + col_o(g), a_hi + 16, b, idO, 1u);
                     }
                     tc_commit(&bars.o[g]);
+                    return true;
                 };
-                ok = mbar_wait(&bars.q_full[qb], (local >> 1) & 1) &&
-                     mbar_wait(&bars.kv_full[kv_tile % kStages], (kv_tile / kStages) & 1);
+                ok = mbar_wait(&bars.q_full[qb], (local >> 1) & 1);
                 if (!ok) break;
-                tc_fence_after();
-                for (int g = 0; g < nq; ++g) issue_s(g, kv_tile % kStages);
+                // S tiles ahead of the loop: A0 (B0) and A1
+                for (int g = 0; ok && g < nq; ++g) ok = issue_s(g, 0);
+                if (ok && T > 1) ok = issue_s(0, 1);
+                if (ok && nq == 1 && T > 1) { /* A1 already issued */ }
                 for (int j = 0; ok && j < T; ++j) {
-                    const int st = (kv_tile + j) % kStages;
-                    const int nt = kv_tile + j + 1;
-                    const bool more = j + 1 < T;
-                    for (int g = 0; ok && g < nq; ++g) {
-                        int& pc = g == 0 ? p_cnt0 : p_cnt1;
-                        const int done_items = g == 0 ? items0 : items1;
-                        ok = mbar_wait(&bars.p[g], pc & 1);
-                        if (!ok) break;
-                        ++pc;
-                        // the first product of an item overwrites O_g: the previous
-                        // item's epilogue must have read it
-                        if (j == 0 && done_items > 0) ok = mbar_wait(&bars.o_free[g], (done_items - 1) & 1);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(g, st, j);
-                        if (more) {
-                            if (g == 0) ok = mbar_wait(&bars.kv_full[nt % kStages], (nt / kStages) & 1);
-                            if (!ok) break;
-                            tc_fence_after();
-                            issue_s(g, nt % kStages);
-                        }
+                    ok = issue_pv(0, j);
+                    if (ok && nq > 1) {
+                        if (j + 1 < T) ok = issue_s(1, j + 1);
+                        if (ok) ok = issue_pv(1, j);
                     }
-                    if (ok) tc_commit(&bars.kv_empty[st]);   // stage free once these MMAs finish
+                    if (ok) tc_commit(&bars.kv_empty[(kv_tile + j) % kStages]);   // K_j, V_j free after these
+                    if (ok && j + 2 < T) ok = issue_s(0, j + 2);
                 }
                 if (ok) tc_commit(&bars.q_empty[qb]);        // Q buffer free after this item's products
                 ++items0;
@@ -433,21 +450,27 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         const int half = (warp >> 2) & 1;              // key columns 64*half .. 64*half+63
         const int row = (warp & 3) * 32 + lane;        // row of the query tile (= TMEM lane)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + col_s(g) + lane_base + 64 * half;
         const uint32_t tO = tmem + col_o(g) + lane_base + 32 * half;
         const bool pos = sl2 >= 0.f;
-        int s_cnt = 0, o_cnt = 0, par = 0;
+        int s_cnt = 0;      // S tiles of this query tile consumed so far
+        int o_cnt = 0;      // PV_g products of finished items
+        int o_conf = 0;     // o[g] phases confirmed (waited) so far
+        int par = 0;
+        int snum = 0;   // S tiles of the CTA's sequence before the current item (both query tiles)
         bool failed = false;
         for (int w = blockIdx.x; !failed && w < n_work; w += gridDim.x) {
             int h;
             const int4 it = item_of(items, w, H, &h);
             const int n = it.y, q0 = it.z, nq = it.w, T = n / kTile, xh = h * kD;
+            const int s0 = snum;
+            snum += nq * T;
             if (g >= nq) continue;
             float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;
             for (int j = 0; j < T; ++j) {
+                const uint32_t tS = tmem + col_buf((s0 + nq * j + g) % 3) + lane_base + 64 * half;
                 // decision uniform over the tile's 8 warps (tcgen05.ld/st are
                 // warp-collective and the row-max exchange is a tile barrier)
-                const bool mine = !mbar_wait(&bars.s[g], s_cnt & 1) || s_abort;
+                const bool mine = !mbar_wait(&bars.s[g][s_cnt & 1], (s_cnt >> 1) & 1) || s_abort;
                 if (tile_any(g, mine)) { failed = true; break; }
                 ++s_cnt;
                 tc_fence_after();
@@ -487,9 +510,14 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     alpha = ex2(m_used - mt);
                     m_used = mt;
                 }
-                if (__any_sync(0xffffffffu, need)) {
-                    // PV_g of the previous tile is complete (this tile's S was
-                    // committed after it): rescale this half's 32 columns of O_g
+                if (j > 0 && tile_any(g, need)) {
+                    // wait for PV_g of the previous tile (no later PV_g can have
+                    // been issued: it needs this tile's P), then rescale this
+                    // half's 32 columns of O_g
+                    // o_conf == o_cnt + j - 1 here: PV_g(j-1) is the one pending phase
+                    if (tile_any(g, !mbar_wait(&bars.o[g], o_conf & 1))) { failed = true; break; }
+                    ++o_conf;
+                    tc_fence_after();
                     l0 *= alpha;
                     l1 *= alpha;
                     uint32_t o[32];
@@ -525,13 +553,21 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tmem_st32(tS + 32 * cc, pk);
                 }
                 tmem_st_wait();
+                // confirm PV_g(j-1) before releasing P_g(j): PV_g(j) cannot be
+                // issued before that release, so the o[g] barrier is never more
+                // than one phase ahead of this wait
+                if (j > 0 && o_conf < o_cnt + j) {
+                    if (tile_any(g, !mbar_wait(&bars.o[g], o_conf & 1))) { failed = true; break; }
+                    ++o_conf;
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.p[g]);
             }
             if (failed) break;
             // epilogue: O_g after the item's last product; row sum from both halves
-            if (tile_any(g, !mbar_wait(&bars.o[g], (o_cnt + T - 1) & 1))) { failed = true; break; }
+            if (tile_any(g, !mbar_wait(&bars.o[g], o_conf & 1))) { failed = true; break; }
+            ++o_conf;
             o_cnt += T;
             tc_fence_after();
             uint32_t o[32];

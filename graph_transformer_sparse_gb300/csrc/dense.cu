@@ -93,20 +93,44 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// The MMA batches of the dense kernel, each in one asm block so the issuing
+// thread needs few issue slots (it shares its SM sub-partition with busy
+// softmax warps).
+// S (+)= Q K^T over K = 64: four K-steps of 32 bytes (descriptor start +2).
+__device__ __forceinline__ void mma_s_batch(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, 0, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %5, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %7, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %9, %3, q;\n\t}"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "l"(a + 2), "l"(b + 2), "l"(a + 4), "l"(b + 4), "l"(a + 6), "l"(b + 6)
         : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// O (+)= P_hi V + P_lo V over 128 keys: eight 16-key steps; P_hi of keys
+// 32c..32c+31 in columns 32c..32c+15, P_lo in 32c+16..32c+31; the V rows of a
+// step start 2048 bytes (128 descriptor units) after the previous step's.
+__device__ __forceinline__ void mma_pv_batch(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+0], %2, %3, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %2, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], %5, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], %5, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], %6, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], %6, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], %7, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], %7, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+64], %8, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+80], %8, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+72], %9, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+88], %9, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+96], %10, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+112], %10, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+104], %11, %3, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+120], %11, %3, q;\n\t}"
+        ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc), "l"(b + 128), "l"(b + 256), "l"(b + 384), "l"(b + 512),
+          "l"(b + 640), "l"(b + 768), "l"(b + 896)
         : "memory");
 }
 
@@ -384,10 +408,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tc_fence_after();
                     const uint64_t dQ = smem_desc_sw128(su32(sQ(qb, g)), 16, 1024);
                     const uint64_t dK = smem_desc_sw128(su32(sK(kt % kStages)), 16, 1024);
-                    const uint32_t d = tmem + col_buf(bufk(g, j));
-#pragma unroll
-                    for (int k = 0; k < kD / 16; ++k)
-                        mma_ss(d, dQ + (uint64_t)(2 * k), dK + (uint64_t)(2 * k), idS, k > 0);
+                    mma_s_batch(tmem + col_buf(bufk(g, j)), dQ, dK, idS);
                     int& sn = g == 0 ? sg0 : sg1;
                     tc_commit(&bars.s[g][sn & 1]);
                     ++sn;
@@ -405,14 +426,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tc_fence_after();
                     const int kt = kv_tile + j;
                     const uint64_t dV = smem_desc_sw128(su32(sV(kt % kStages)), 8192, 1024);
-                    const uint32_t pbuf = tmem + col_buf(bufk(g, j));
-#pragma unroll
-                    for (int s = 0; s < kTile / 16; ++s) {
-                        const uint32_t a_hi = pbuf + 32 * (s >> 1) + 8 * (s & 1);
-                        const uint64_t b = dV + (uint64_t)(s * (2048 >> 4));
-                        mma_ts(tmem + col_o(g), a_hi, b, idO, (j > 0 || s > 0) ? 1u : 0u);
-                        mma_ts(tmem + col_o(g), a_hi + 16, b, idO, 1u);
-                    }
+                    mma_pv_batch(tmem + col_o(g), tmem + col_buf(bufk(g, j)), dV, idO, j > 0 ? 1u : 0u);
                     tc_commit(&bars.o[g]);
                     return true;
                 };

@@ -121,12 +121,22 @@ __device__ __forceinline__ void store_frag(T* p, const float* x) {
 // ---------------------------------------------------------------------------
 // vector row kernel
 // ---------------------------------------------------------------------------
+// Tuning knobs (compile time): edges gathered per lane group per loop
+// iteration is GT_ROWS_UNROLL / VPL; GT_ROWS_MIN_BLOCKS bounds registers so
+// that many 256-thread blocks fit on an SM.
+#ifndef GT_ROWS_UNROLL
+#define GT_ROWS_UNROLL 8
+#endif
+#ifndef GT_ROWS_MIN_BLOCKS
+#define GT_ROWS_MIN_BLOCKS 1
+#endif
+
 template <typename T, typename TO, int VPL, int MODE>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, GT_ROWS_MIN_BLOCKS)
 k_rows_vec(RowParams p) {
     using F = Frag<T, VPL>;
     constexpr int E = F::E;
-    constexpr int U = (8 / VPL) > 0 ? (8 / VPL) : 1;
+    constexpr int U = (GT_ROWS_UNROLL / VPL) > 0 ? (GT_ROWS_UNROLL / VPL) : 1;
 
     __shared__ Seg segs[kMaxSegs];
     __shared__ int s_nseg, s_total;

@@ -125,14 +125,28 @@ __device__ __forceinline__ void store_frag(T* p, const float* x) {
 // iteration is GT_ROWS_UNROLL / VPL; GT_ROWS_MIN_BLOCKS bounds registers so
 // that many 256-thread blocks fit on an SM.
 #ifndef GT_ROWS_UNROLL
-#define GT_ROWS_UNROLL 8
+#define GT_ROWS_UNROLL 4
 #endif
 #ifndef GT_ROWS_MIN_BLOCKS
-#define GT_ROWS_MIN_BLOCKS 1
+#define GT_ROWS_MIN_BLOCKS 4
 #endif
 
+// Where a task's rows and edges are: one lane group's share of a task.
+struct TaskMeta {
+    int seg;        // segment of the task table
+    int row, beg, end, chunk;
+    bool valid;
+};
+
+// Blocks per SM the register budget allows: lanes holding 16 values per
+// operand (two or four 16-byte vectors) get more registers than one-vector lanes.
+template <typename T, int VPL>
+constexpr int rows_min_blocks() {
+    return VPL >= 4 ? 2 : (VPL == 2 ? (GT_ROWS_MIN_BLOCKS > 3 ? 3 : GT_ROWS_MIN_BLOCKS) : GT_ROWS_MIN_BLOCKS);
+}
+
 template <typename T, typename TO, int VPL, int MODE>
-__global__ void __launch_bounds__(256, GT_ROWS_MIN_BLOCKS)
+__global__ void __launch_bounds__(256, rows_min_blocks<T, VPL>())
 k_rows_vec(RowParams p) {
     using F = Frag<T, VPL>;
     constexpr int E = F::E;
@@ -156,29 +170,47 @@ k_rows_vec(RowParams p) {
     const int lane_off = gl * E;
 
     const int warps_total = gridDim.x * (blockDim.x >> 5);
-    int seg = 0;
-    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < s_total; t += warps_total) {
+    // task metadata (segment, row, edge range) of task t for this lane group
+    auto load_meta = [&](int t, int seg_hint, TaskMeta& m) {
+        int seg = seg_hint;
         while (seg + 1 < s_nseg && segs[seg + 1].first_task <= t) ++seg;
-        const Seg sg = segs[seg];
+        const Seg& sg = segs[seg];
+        const int r = grp / sg.S;
+        const int pos = (t - sg.first_task) * sg.R + r;
+        m.seg = seg;
+        m.valid = pos < sg.count;
+        m.row = 0;
+        m.beg = 0;
+        m.end = 0;
+        m.chunk = -1;
+        if (m.valid) {
+            if (sg.kind == kSegChunk) {
+                m.chunk = sg.list_begin + pos;
+                const int2 c = p.lists.chunks[m.chunk];
+                m.row = c.x;
+                m.beg = c.y;
+                m.end = min(m.beg + p.lists.chunk_edges, p.indptr[m.row + 1]);
+            } else {
+                m.row = p.lists.rows[sg.list_begin + pos];
+                m.beg = p.indptr[m.row];
+                m.end = p.indptr[m.row + 1];
+            }
+        }
+    };
+    int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    TaskMeta cur, nxt;
+    if (t < s_total) load_meta(t, 0, cur);
+    for (; t < s_total; t += warps_total, cur = nxt) {
+        // the next task's metadata loads are issued now and consumed on the
+        // next iteration, off this task's critical path
+        const int tn = t + warps_total;
+        if (tn < s_total) load_meta(tn, cur.seg, nxt);
+        const Seg sg = segs[cur.seg];
         const int S = sg.S;
         const int r = grp / S;
         const int sl = grp - r * S;
-        const int pos = (t - sg.first_task) * sg.R + r;
-        const bool valid = pos < sg.count;
-        int row = 0, beg = 0, end = 0, chunk = -1;
-        if (valid) {
-            if (sg.kind == kSegChunk) {
-                chunk = sg.list_begin + pos;
-                int2 c = p.lists.chunks[chunk];
-                row = c.x;
-                beg = c.y;
-                end = min(beg + p.lists.chunk_edges, p.indptr[row + 1]);
-            } else {
-                row = p.lists.rows[sg.list_begin + pos];
-                beg = p.indptr[row];
-                end = p.indptr[row + 1];
-            }
-        }
+        const bool valid = cur.valid;
+        const int row = cur.row, beg = cur.beg, end = cur.end, chunk = cur.chunk;
         const int step = S * U;
         int n_iter = (end - beg + step - 1) / step;
         n_iter = __reduce_max_sync(kFull, n_iter);
@@ -266,8 +298,7 @@ k_rows_vec(RowParams p) {
                 }
             }
         }
-        if constexpr (MODE == kSddmm) continue;
-
+        if constexpr (MODE != kSddmm) {
         // merge the S edge slots of each row (lanes G, 2G, ... apart)
         for (int o = G; o < S * G; o <<= 1) {
             if constexpr (MODE == kFused) {
@@ -306,6 +337,7 @@ k_rows_vec(RowParams p) {
             }
             store_frag<TO, E>(O + (int64_t)row * HD + lane_off, acc);
         }
+        }   // MODE != kSddmm
     }
 }
 

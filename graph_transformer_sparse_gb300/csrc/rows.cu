@@ -228,15 +228,27 @@ k_rows_vec(RowParams p) {
         for (int e = 0; e < E; ++e) acc[e] = 0.f;
         float m = -INFINITY, ssum = 0.f;
 
+        // neighbour indices run one iteration ahead of the K/V gathers, so
+        // each iteration waits on one memory round trip instead of two
+        int jn[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = beg + u * S + sl;
+            jn[u] = e < end ? __ldg(p.indices + e) : 0;
+        }
         for (int it = 0; it < n_iter; ++it) {
             const int e0 = beg + it * step + sl;
             int j[U];
             bool ok[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                int e = e0 + u * S;
-                ok[u] = e < end;
-                j[u] = ok[u] ? __ldg(p.indices + e) : 0;
+                ok[u] = e0 + u * S < end;
+                j[u] = jn[u];
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int e = e0 + step + u * S;
+                jn[u] = e < end ? __ldg(p.indices + e) : 0;
             }
             float l[U];
             if constexpr (MODE != kSpmm) {

@@ -125,10 +125,13 @@ __device__ __forceinline__ void store_frag(T* p, const float* x) {
 // iteration is GT_ROWS_UNROLL / VPL; GT_ROWS_MIN_BLOCKS bounds registers so
 // that many 256-thread blocks fit on an SM.
 #ifndef GT_ROWS_UNROLL
-#define GT_ROWS_UNROLL 4
+#define GT_ROWS_UNROLL 2
 #endif
-#ifndef GT_ROWS_MIN_BLOCKS
-#define GT_ROWS_MIN_BLOCKS 4
+#ifndef GT_ROWS_MIN_BLOCKS1
+#define GT_ROWS_MIN_BLOCKS1 3   // one 16-byte vector per lane
+#endif
+#ifndef GT_ROWS_MIN_BLOCKS2
+#define GT_ROWS_MIN_BLOCKS2 2   // two or more vectors per lane
 #endif
 
 // Where a task's rows and edges are: one lane group's share of a task.
@@ -141,9 +144,7 @@ struct TaskMeta {
 // Blocks per SM the register budget allows: lanes holding 16 values per
 // operand (two or four 16-byte vectors) get more registers than one-vector lanes.
 template <typename T, int VPL>
-constexpr int rows_min_blocks() {
-    return VPL >= 4 ? 2 : (VPL == 2 ? (GT_ROWS_MIN_BLOCKS > 3 ? 3 : GT_ROWS_MIN_BLOCKS) : GT_ROWS_MIN_BLOCKS);
-}
+constexpr int rows_min_blocks() { return VPL == 1 ? GT_ROWS_MIN_BLOCKS1 : GT_ROWS_MIN_BLOCKS2; }
 
 template <typename T, typename TO, int VPL, int MODE>
 __global__ void __launch_bounds__(256, rows_min_blocks<T, VPL>())
@@ -228,40 +229,45 @@ k_rows_vec(RowParams p) {
         for (int e = 0; e < E; ++e) acc[e] = 0.f;
         float m = -INFINITY, ssum = 0.f;
 
-        // neighbour indices run one iteration ahead of the K/V gathers, so
-        // each iteration waits on one memory round trip instead of two
+        // Two-stage software pipeline over the row's edges: the K/V rows of
+        // iteration it+1 and the neighbour indices of iteration it+2 are in
+        // flight while iteration it is computed.
+        constexpr bool kNeedK = MODE != kSpmm;
+        constexpr bool kNeedV = MODE != kSddmm;
         int jn[U];
+        bool okc[U];
+        F kc[U], vc[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int e = beg + u * S + sl;
-            jn[u] = e < end ? __ldg(p.indices + e) : 0;
+            okc[u] = e < end;
+            const int j = okc[u] ? __ldg(p.indices + e) : 0;
+            if (kNeedK) { if (okc[u]) kc[u].load(K + (int64_t)j * HD + lane_off); else kc[u].zero(); }
+            if (kNeedV) { if (okc[u]) vc[u].load(V + (int64_t)j * HD + lane_off); else vc[u].zero(); }
+            const int e1 = e + step;
+            jn[u] = e1 < end ? __ldg(p.indices + e1) : 0;
         }
         for (int it = 0; it < n_iter; ++it) {
             const int e0 = beg + it * step + sl;
-            int j[U];
-            bool ok[U];
+            // issue iteration it+1's gathers and iteration it+2's indices
+            bool okn[U];
+            F kn[U], vn[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                ok[u] = e0 + u * S < end;
-                j[u] = jn[u];
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int e = e0 + step + u * S;
-                jn[u] = e < end ? __ldg(p.indices + e) : 0;
+                const int e1 = e0 + step + u * S;
+                okn[u] = e1 < end;
+                if (kNeedK) { if (okn[u]) kn[u].load(K + (int64_t)jn[u] * HD + lane_off); else kn[u].zero(); }
+                if (kNeedV) { if (okn[u]) vn[u].load(V + (int64_t)jn[u] * HD + lane_off); else vn[u].zero(); }
+                const int e2 = e1 + step;
+                jn[u] = e2 < end ? __ldg(p.indices + e2) : 0;
             }
             float l[U];
-            if constexpr (MODE != kSpmm) {
-                F fk[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (ok[u]) fk[u].load(K + (int64_t)j[u] * HD + lane_off); else fk[u].zero();
-                }
+            if constexpr (kNeedK) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     float d = 0.f;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) d = fmaf(q[e], fk[u].get(e), d);
+                    for (int e = 0; e < E; ++e) d = fmaf(q[e], kc[u].get(e), d);
                     l[u] = d;
                 }
 #pragma unroll
@@ -272,42 +278,41 @@ k_rows_vec(RowParams p) {
                 if (gl % p.lph == 0) {
 #pragma unroll
                     for (int u = 0; u < U; ++u)
-                        if (ok[u]) p.logits[(int64_t)(e0 + u * S) * p.H + head] = l[u] * p.qscale;
+                        if (okc[u]) p.logits[(int64_t)(e0 + u * S) * p.H + head] = l[u] * p.qscale;
                 }
-            } else {
-                F fv[U];
+            } else if constexpr (MODE == kFused) {
+                float mx = m;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    if (ok[u]) fv[u].load(V + (int64_t)j[u] * HD + lane_off); else fv[u].zero();
+                    if (!okc[u]) l[u] = -INFINITY;
+                    mx = fmaxf(mx, l[u]);
                 }
-                if constexpr (MODE == kFused) {
-                    float mx = m;
+                const float mref = (mx == -INFINITY) ? 0.f : mx;
+                const float c = ex2(m - mref);
+                ssum *= c;
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        if (!ok[u]) l[u] = -INFINITY;
-                        mx = fmaxf(mx, l[u]);
-                    }
-                    const float mref = (mx == -INFINITY) ? 0.f : mx;
-                    const float c = ex2(m - mref);
-                    ssum *= c;
+                for (int e = 0; e < E; ++e) acc[e] *= c;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) acc[e] *= c;
+                for (int u = 0; u < U; ++u) {
+                    const float w = ex2(l[u] - mref);
+                    ssum += w;
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const float w = ex2(l[u] - mref);
-                        ssum += w;
-#pragma unroll
-                        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, fv[u].get(e), acc[e]);
-                    }
-                    m = mx;
-                } else {   // kSpmm: weights are the given probabilities
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const float w = ok[u] ? p.probs[(int64_t)(e0 + u * S) * p.H + head] : 0.f;
-#pragma unroll
-                        for (int e = 0; e < E; ++e) acc[e] = fmaf(w, fv[u].get(e), acc[e]);
-                    }
+                    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, vc[u].get(e), acc[e]);
                 }
+                m = mx;
+            } else {   // kSpmm: weights are the given probabilities
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float w = okc[u] ? p.probs[(int64_t)(e0 + u * S) * p.H + head] : 0.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, vc[u].get(e), acc[e]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                okc[u] = okn[u];
+                kc[u] = kn[u];
+                vc[u] = vn[u];
             }
         }
         if constexpr (MODE != kSddmm) {

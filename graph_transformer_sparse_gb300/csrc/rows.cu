@@ -131,7 +131,7 @@ __device__ __forceinline__ void store_frag(T* p, const float* x) {
 #define GT_ROWS_MIN_BLOCKS1 3   // one 16-byte vector per lane
 #endif
 #ifndef GT_ROWS_MIN_BLOCKS2
-#define GT_ROWS_MIN_BLOCKS2 2   // two or more vectors per lane
+#define GT_ROWS_MIN_BLOCKS2 3   // two or more vectors per lane
 #endif
 
 // Where a task's rows and edges are: one lane group's share of a task.

@@ -242,7 +242,7 @@ k_rows_vec(RowParams p) {
             const int e = beg + u * S + sl;
             okc[u] = e < end;
             const int j = okc[u] ? __ldg(p.indices + e) : 0;
-            if (kNeedK && okc[u]) kc[u].load(K + (int64_t)j * HD + lane_off);   // masked: logit -> -inf
+            if (kNeedK) { if (okc[u]) kc[u].load(K + (int64_t)j * HD + lane_off); else kc[u].zero(); }
             if (kNeedV) { if (okc[u]) vc[u].load(V + (int64_t)j * HD + lane_off); else vc[u].zero(); }
             const int e1 = e + step;
             jn[u] = e1 < end ? __ldg(p.indices + e1) : 0;
@@ -256,7 +256,7 @@ k_rows_vec(RowParams p) {
             for (int u = 0; u < U; ++u) {
                 const int e1 = e0 + step + u * S;
                 okn[u] = e1 < end;
-                if (kNeedK && okn[u]) kn[u].load(K + (int64_t)jn[u] * HD + lane_off);
+                if (kNeedK) { if (okn[u]) kn[u].load(K + (int64_t)jn[u] * HD + lane_off); else kn[u].zero(); }
                 if (kNeedV) { if (okn[u]) vn[u].load(V + (int64_t)jn[u] * HD + lane_off); else vn[u].zero(); }
                 const int e2 = e1 + step;
                 jn[u] = e2 < end ? __ldg(p.indices + e2) : 0;
@@ -281,25 +281,17 @@ k_rows_vec(RowParams p) {
                         if (okc[u]) p.logits[(int64_t)(e0 + u * S) * p.H + head] = l[u] * p.qscale;
                 }
             } else if constexpr (MODE == kFused) {
-                // lazy online softmax: the reference max m is raised (and acc,
-                // s rescaled) only when a logit exceeds it by more than 8 (log2
-                // units), so weights stay <= 2^8; the first edges set m
-                float mx = -INFINITY;
+                float mx = m;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     if (!okc[u]) l[u] = -INFINITY;
                     mx = fmaxf(mx, l[u]);
                 }
-                const bool raise = mx > m + 8.f;
-                if (__any_sync(kFull, raise)) {
-                    const float mn = raise ? mx : m;
-                    const float c = (m == -INFINITY) ? 0.f : ex2(m - mn);
-                    ssum *= c;
+                const float mref = (mx == -INFINITY) ? 0.f : mx;
+                const float c = ex2(m - mref);
+                ssum *= c;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) acc[e] *= c;
-                    m = mn;
-                }
-                const float mref = (m == -INFINITY) ? 0.f : m;
+                for (int e = 0; e < E; ++e) acc[e] *= c;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const float w = ex2(l[u] - mref);
@@ -307,6 +299,7 @@ k_rows_vec(RowParams p) {
 #pragma unroll
                     for (int e = 0; e < E; ++e) acc[e] = fmaf(w, vc[u].get(e), acc[e]);
                 }
+                m = mx;
             } else {   // kSpmm: weights are the given probabilities
 #pragma unroll
                 for (int u = 0; u < U; ++u) {

@@ -552,15 +552,27 @@ k_combine(RowParams p) {
 // ---------------------------------------------------------------------------
 // unfused edge softmax: warp per ordinary row, block per split row
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float warp_max(float v) {
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-    return v;
+// Online (max, sum) of exponentials, merged pairwise.
+__device__ __forceinline__ void ms_add(float& m, float& s, float x) {
+    if (x > m) {
+        s = s * expf(m - x) + 1.f;
+        m = x;
+    } else {
+        s += expf(x - m);
+    }
 }
-__device__ __forceinline__ float warp_sum(float v) {
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
+__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
+    if (m2 > m) {
+        s = s * expf(m - m2) + s2;
+        m = m2;
+    } else if (m2 != -INFINITY) {
+        s += s2 * expf(m2 - m);
+    }
 }
 
+// Ordinary rows, H dividing 32: a warp per row; lane l walks the row's
+// logits in memory order (entry-major, head-minor), so its head is l % H and
+// the per-head statistics combine over lanes H, 2H, ... apart.
 __global__ void __launch_bounds__(256)
 k_softmax_rows(const int* __restrict__ indptr, int N, int H, int long_min,
                const float* __restrict__ logits, float* __restrict__ probs) {
@@ -570,50 +582,78 @@ k_softmax_rows(const int* __restrict__ indptr, int N, int H, int long_min,
         const int beg = indptr[i], end = indptr[i + 1];
         const int deg = end - beg;
         if (deg == 0 || deg > long_min) continue;
+        const int64_t base = (int64_t)beg * H;
+        const int total = deg * H;
+        float m = -INFINITY, sum = 0.f;
+        for (int t = lane; t < total; t += 32) ms_add(m, sum, logits[base + t]);
+        for (int o = H; o < 32; o <<= 1) {
+            const float m2 = __shfl_xor_sync(kFull, m, o);
+            const float s2 = __shfl_xor_sync(kFull, sum, o);
+            ms_merge(m, sum, m2, s2);
+        }
+        const float inv = 1.f / sum;
+        for (int t = lane; t < total; t += 32) probs[base + t] = expf(logits[base + t] - m) * inv;
+    }
+}
+
+// Ordinary rows, any H: a warp per row, heads one after another.
+__global__ void __launch_bounds__(256)
+k_softmax_rows_anyh(const int* __restrict__ indptr, int N, int H, int long_min,
+                    const float* __restrict__ logits, float* __restrict__ probs) {
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < N; i += warps) {
+        const int beg = indptr[i], end = indptr[i + 1];
+        const int deg = end - beg;
+        if (deg == 0 || deg > long_min) continue;
         for (int h = 0; h < H; ++h) {
-            float m = -INFINITY;
-            for (int e = beg + lane; e < end; e += 32) m = fmaxf(m, logits[(int64_t)e * H + h]);
-            m = warp_max(m);
-            float s = 0.f;
-            for (int e = beg + lane; e < end; e += 32) s += expf(logits[(int64_t)e * H + h] - m);
-            s = warp_sum(s);
-            const float inv = 1.f / s;
+            float m = -INFINITY, sum = 0.f;
+            for (int e = beg + lane; e < end; e += 32) ms_add(m, sum, logits[(int64_t)e * H + h]);
+            for (int o = 16; o > 0; o >>= 1) {
+                const float m2 = __shfl_xor_sync(kFull, m, o);
+                const float s2 = __shfl_xor_sync(kFull, sum, o);
+                ms_merge(m, sum, m2, s2);
+            }
+            const float inv = 1.f / sum;
             for (int e = beg + lane; e < end; e += 32)
                 probs[(int64_t)e * H + h] = expf(logits[(int64_t)e * H + h] - m) * inv;
         }
     }
 }
 
-__device__ float block_reduce(float v, bool is_max, float* red) {
-    v = is_max ? warp_max(v) : warp_sum(v);
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    __syncthreads();
-    if (lane == 0) red[w] = v;
-    __syncthreads();
-    float r = is_max ? -INFINITY : 0.f;
-    for (int k = 0; k < nw; ++k) r = is_max ? fmaxf(r, red[k]) : r + red[k];
-    return r;
-}
-
+// Split rows: a block per row, threads walk the row's logits in memory
+// order; per-head statistics go through shared memory.
 __global__ void __launch_bounds__(256)
 k_softmax_long(const int* __restrict__ indptr, const int* __restrict__ hdr, const int2* __restrict__ longs,
                int H, const float* __restrict__ logits, float* __restrict__ probs) {
-    __shared__ float red[32];
+    __shared__ float sm_m[256], sm_s[256];
+    __shared__ float head_m[kGenMaxH], head_inv[kGenMaxH];
     const int n_long = hdr[HdrLayout::kLong];
+    const int per = (256 / H) * H;            // threads in use: a multiple of H
     for (int li = blockIdx.x; li < n_long; li += gridDim.x) {
         const int row = longs[li].x;
         const int beg = indptr[row], end = indptr[row + 1];
-        for (int h = 0; h < H; ++h) {
-            float m = -INFINITY;
-            for (int e = beg + threadIdx.x; e < end; e += blockDim.x) m = fmaxf(m, logits[(int64_t)e * H + h]);
-            m = block_reduce(m, true, red);
-            float s = 0.f;
-            for (int e = beg + threadIdx.x; e < end; e += blockDim.x) s += expf(logits[(int64_t)e * H + h] - m);
-            s = block_reduce(s, false, red);
-            const float inv = 1.f / s;
-            for (int e = beg + threadIdx.x; e < end; e += blockDim.x)
-                probs[(int64_t)e * H + h] = expf(logits[(int64_t)e * H + h] - m) * inv;
+        const int64_t base = (int64_t)beg * H;
+        const int total = (end - beg) * H;
+        float m = -INFINITY, sum = 0.f;
+        if (threadIdx.x < per)
+            for (int t = threadIdx.x; t < total; t += per) ms_add(m, sum, logits[base + t]);
+        sm_m[threadIdx.x] = m;
+        sm_s[threadIdx.x] = sum;
+        __syncthreads();
+        for (int h = threadIdx.x; h < H; h += blockDim.x) {   // thread h merges the threads of head h
+            float hm = -INFINITY, hs = 0.f;
+            for (int k = h; k < per; k += H) ms_merge(hm, hs, sm_m[k], sm_s[k]);
+            head_m[h] = hm;
+            head_inv[h] = 1.f / hs;
         }
+        __syncthreads();
+        if (threadIdx.x < per) {
+            const int h = threadIdx.x % H;
+            const float hm = head_m[h], hi = head_inv[h];
+            for (int t = threadIdx.x; t < total; t += per) probs[base + t] = expf(logits[base + t] - hm) * hi;
+        }
+        __syncthreads();
     }
 }
 
@@ -729,8 +769,13 @@ gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cud
 gtattn_status launch_edge_softmax(const int* indptr, int N, int H, int long_min, const TaskLists& L,
                                   const float* logits, float* probs, cudaStream_t s) {
     if (N == 0) return GTATTN_OK;
+    if (H > kGenMaxH) return GTATTN_ERR_UNSUPPORTED;
     const int lm = long_min < 0 ? 0 : long_min;   // long_min -1: every non-empty row is split
-    k_softmax_rows<<<grid_persistent(k_softmax_rows, 256, 0), 256, 0, s>>>(indptr, N, H, lm, logits, probs);
+    if (32 % H == 0)
+        k_softmax_rows<<<grid_persistent(k_softmax_rows, 256, 0), 256, 0, s>>>(indptr, N, H, lm, logits, probs);
+    else
+        k_softmax_rows_anyh<<<grid_persistent(k_softmax_rows_anyh, 256, 0), 256, 0, s>>>(indptr, N, H, lm,
+                                                                                      logits, probs);
     k_softmax_long<<<grid_persistent(k_softmax_long, 256, 0), 256, 0, s>>>(indptr, L.hdr, L.longs, H,
                                                                             logits, probs);
     cudaError_t e = cudaGetLastError();

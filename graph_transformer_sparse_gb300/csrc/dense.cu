@@ -198,22 +198,23 @@ struct DenseErr {
 // 0-63, half 1: keys 64-127) and exchange row maxima through shared memory:
 //   warps 0-3 / 4-7     tile A, halves 0 / 1
 //   warps 8-11 / 12-15  tile B, halves 0 / 1
-//   warps 16 / 17       MMA issue for tiles A / B (one thread each)
-//   warp 18             TMA loads (one thread); warp 19 idle
+//   warp 16             MMA issue (one thread)
+//   warp 17             TMA loads (one thread); warps 18-19 idle
 // The grid is persistent (one CTA per SM): each CTA walks work items (a pair
 // of query tiles and a head); Q tiles are double-buffered and the K/V ring
 // runs on across items, so the next item's loads and first products overlap
 // the current item's last softmax and epilogue.
 constexpr int kWarps = 20;
 constexpr int kThreadsWS = kWarps * 32;
-constexpr int kMmaWarp = 16;                      // warps 16, 17: MMA issue for query tiles A, B
-constexpr int kTmaWarp = 18;                      // warp 19 idle
+constexpr int kMmaWarp = 16;
+constexpr int kTmaWarp = 17;
 constexpr int kStages = 4;                        // K/V ring
 constexpr uint32_t kTmemAll = 512;
-// TMEM: S_g (128 columns, P_g is written over it) and O_g (64 columns) per
-// query tile g.
-__host__ __device__ constexpr uint32_t col_s(int g) { return g == 0 ? 0u : 128u; }
-__host__ __device__ constexpr uint32_t col_o(int g) { return g == 0 ? 256u : 320u; }
+// TMEM: three S/P buffers (128 columns each) used in rotation by the S tiles
+// of both query tiles -- S number k (A0, B0, A1, B1, ... within the CTA's
+// sequence) lives in buffer k % 3 and its P is written over it -- then O_A, O_B.
+__host__ __device__ constexpr uint32_t col_buf(int b) { return 128u * static_cast<uint32_t>(b); }
+__host__ __device__ constexpr uint32_t col_o(int g) { return g == 0 ? 384u : 448u; }
 constexpr size_t kWsSmemQ = 0;                    // 2 buffers x 2 query tiles
 constexpr size_t kWsSmemKV = 4 * kTileBytes;      // stage s: K at +0, V at +kTileBytes
 constexpr size_t kWsSmemBytes = 4 * kTileBytes + kStages * 2 * kTileBytes;   // 192 KB
@@ -223,11 +224,13 @@ struct WsBars {
     uint64_t q_full[2], q_empty[2];   // Q buffers (TMA <-> MMA)
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s[2];       // S_g of the current tile is in TMEM (MMA -> softmax g)
+    uint64_t s[2][2];    // S tile n of query tile g is in TMEM: barrier s[g][n & 1]
+                         // (MMA -> softmax g; two barriers because an S tile
+                         // can run two ahead of its softmax)
     uint64_t p[2];       // P_g written over S_g (softmax g -> MMA), 8 warp arrivals
     uint64_t o[2];       // PV_g done (MMA -> softmax g, waited for the epilogue)
     uint64_t o_free[2];  // softmax g has read O_g in its epilogue (-> MMA), 8 arrivals
-    uint64_t drain[2];
+    uint64_t drain;
 };
 
 // Work item w -> (block row, block size, first query row, query tiles) and head.
@@ -315,24 +318,22 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     }
     if (tid == 0) {
         s_abort = 0;
-        // Q buffers and K/V stages are released by both MMA issuers (the A
-        // issuer releases twice for an item with one query tile)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars.q_full[b], 1);
-            mbar_init(&bars.q_empty[b], 2);
+            mbar_init(&bars.q_empty[b], 1);
         }
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&bars.kv_full[i], 1);
-            mbar_init(&bars.kv_empty[i], 2);
+            mbar_init(&bars.kv_empty[i], 1);
         }
         for (int g = 0; g < 2; ++g) {
-            mbar_init(&bars.s[g], 1);
+            mbar_init(&bars.s[g][0], 1);
+            mbar_init(&bars.s[g][1], 1);
             mbar_init(&bars.p[g], 8);
             mbar_init(&bars.o[g], 1);
             mbar_init(&bars.o_free[g], 8);
         }
-        mbar_init(&bars.drain[0], 1);
-        mbar_init(&bars.drain[1], 1);
+        mbar_init(&bars.drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     tc_fence_before();
@@ -379,66 +380,83 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 }
             }
         }
-    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-        // ---------------- MMA issue, one thread per query tile ----------------
-        // Tile g's thread issues S_g(j) = Q_g K_j^T and, once softmax g has
-        // written P_g(j) over it, O_g += P_g(j) V_j, then S_g(j+1) into the same
-        // columns (one thread's MMAs execute in issue order).  Two issuers on
-        // two SM sub-partitions halve the issue load per thread.
-        const int g = warp - kMmaWarp;
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issuer ----------------
+        // Order per item (two query tiles): S_A0 S_B0 S_A1, then per key tile j:
+        // PV_Aj, S_B(j+1), PV_Bj, S_A(j+2).  An S tile is computed one step ahead
+        // of its softmax; a buffer is reused only after the PV that read its P
+        // (the tensor pipe executes one thread's MMAs in issue order).
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, 128, 0);
             const uint32_t idO = idesc_bf16(128, 64, 1);
             bool ok = true;
-            int kv_tile = 0;
-            int p_cnt = 0, done_items = 0;
+            int kv_tile = 0;   // first K/V tile of the current item in the CTA's sequence
+            int snum = 0;      // S tiles issued so far (buffer = snum % 3)
+            int sg0 = 0, sg1 = 0;   // S tiles issued per query tile (barrier s[g][n & 1])
+            int p_cnt0 = 0, p_cnt1 = 0, items0 = 0, items1 = 0;
             int local = 0;
             for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++local) {
                 int h;
                 const int4 it = item_of(items, w, H, &h);
                 const int nq = it.w, T = it.y / kTile;
                 const int qb = local & 1;
-                const int kt0 = kv_tile;
-                kv_tile += T;
-                if (g >= nq) continue;
-                const int rel = nq == 1 ? 2 : 1;   // releases owed per stage / Q buffer
-                auto issue_s = [&](int j) {
-                    const int kt = kt0 + j;
-                    if (!mbar_wait(&bars.kv_full[kt % kStages], (kt / kStages) & 1)) return false;
+                const int s0 = snum;   // S number of (g, j) = s0 + nq*j + g
+                auto bufk = [&](int g, int j) { return (s0 + nq * j + g) % 3; };
+                auto issue_s = [&](int g, int j) {
+                    const int kt = kv_tile + j;
+                    if (g == 0 && !mbar_wait(&bars.kv_full[kt % kStages], (kt / kStages) & 1)) return false;
                     tc_fence_after();
                     const uint64_t dQ = smem_desc_sw128(su32(sQ(qb, g)), 16, 1024);
                     const uint64_t dK = smem_desc_sw128(su32(sK(kt % kStages)), 16, 1024);
-                    mma_s_batch(tmem + col_s(g), dQ, dK, idS);
-                    tc_commit(&bars.s[g]);
+                    mma_s_batch(tmem + col_buf(bufk(g, j)), dQ, dK, idS);
+                    int& sn = g == 0 ? sg0 : sg1;
+                    tc_commit(&bars.s[g][sn & 1]);
+                    ++sn;
+                    ++snum;
                     return true;
                 };
-                ok = mbar_wait(&bars.q_full[qb], (local >> 1) & 1) && issue_s(0);
-                for (int j = 0; ok && j < T; ++j) {
-                    ok = mbar_wait(&bars.p[g], p_cnt & 1);
-                    if (!ok) break;
-                    ++p_cnt;
+                auto issue_pv = [&](int g, int j) {
+                    int& pc = g == 0 ? p_cnt0 : p_cnt1;
+                    const int done_items = g == 0 ? items0 : items1;
+                    if (!mbar_wait(&bars.p[g], pc & 1)) return false;
+                    ++pc;
                     // the first product of an item overwrites O_g: the previous
                     // item's epilogue must have read it
-                    if (j == 0 && done_items > 0) ok = mbar_wait(&bars.o_free[g], (done_items - 1) & 1);
-                    if (!ok) break;
+                    if (j == 0 && done_items > 0 && !mbar_wait(&bars.o_free[g], (done_items - 1) & 1)) return false;
                     tc_fence_after();
-                    const int kt = kt0 + j;
+                    const int kt = kv_tile + j;
                     const uint64_t dV = smem_desc_sw128(su32(sV(kt % kStages)), 8192, 1024);
-                    mma_pv_batch(tmem + col_o(g), tmem + col_s(g), dV, idO, j > 0 ? 1u : 0u);
+                    mma_pv_batch(tmem + col_o(g), tmem + col_buf(bufk(g, j)), dV, idO, j > 0 ? 1u : 0u);
                     tc_commit(&bars.o[g]);
-                    if (j + 1 < T) ok = issue_s(j + 1);
-                    for (int r = 0; ok && r < rel; ++r) tc_commit(&bars.kv_empty[kt % kStages]);
+                    return true;
+                };
+                ok = mbar_wait(&bars.q_full[qb], (local >> 1) & 1);
+                if (!ok) break;
+                // S tiles ahead of the loop: A0 (B0) and A1
+                for (int g = 0; ok && g < nq; ++g) ok = issue_s(g, 0);
+                if (ok && T > 1) ok = issue_s(0, 1);
+                if (ok && nq == 1 && T > 1) { /* A1 already issued */ }
+                for (int j = 0; ok && j < T; ++j) {
+                    ok = issue_pv(0, j);
+                    if (ok && nq > 1) {
+                        if (j + 1 < T) ok = issue_s(1, j + 1);
+                        if (ok) ok = issue_pv(1, j);
+                    }
+                    if (ok) tc_commit(&bars.kv_empty[(kv_tile + j) % kStages]);   // K_j, V_j free after these
+                    if (ok && j + 2 < T) ok = issue_s(0, j + 2);
                 }
-                for (int r = 0; ok && r < rel; ++r) tc_commit(&bars.q_empty[qb]);
-                ++done_items;
+                if (ok) tc_commit(&bars.q_empty[qb]);        // Q buffer free after this item's products
+                ++items0;
+                if (nq > 1) ++items1;
+                kv_tile += T;
             }
             if (!ok) {
                 atomicOr(err, DenseErr::kTimeout);
                 atomicExch(&s_abort, 1);
             }
             // drain: everything this thread issued has finished before TMEM is freed
-            tc_commit(&bars.drain[g]);
-            mbar_wait(&bars.drain[g], 0, kWaitCycles / 4);
+            tc_commit(&bars.drain);
+            mbar_wait(&bars.drain, 0, kWaitCycles / 4);
         }
     } else if (warp < kMmaWarp) {
         // ---------------- softmax warpgroups ----------------
@@ -450,19 +468,23 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         const bool pos = sl2 >= 0.f;
         int s_cnt = 0;      // S tiles of this query tile consumed so far
         int o_cnt = 0;      // PV_g products of finished items
+        int o_conf = 0;     // o[g] phases confirmed (waited) so far
         int par = 0;
-        const uint32_t tS = tmem + col_s(g) + lane_base + 64 * half;
+        int snum = 0;   // S tiles of the CTA's sequence before the current item (both query tiles)
         bool failed = false;
         for (int w = blockIdx.x; !failed && w < n_work; w += gridDim.x) {
             int h;
             const int4 it = item_of(items, w, H, &h);
             const int n = it.y, q0 = it.z, nq = it.w, T = n / kTile, xh = h * kD;
+            const int s0 = snum;
+            snum += nq * T;
             if (g >= nq) continue;
             float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;
             for (int j = 0; j < T; ++j) {
+                const uint32_t tS = tmem + col_buf((s0 + nq * j + g) % 3) + lane_base + 64 * half;
                 // decision uniform over the tile's 8 warps (tcgen05.ld/st are
                 // warp-collective and the row-max exchange is a tile barrier)
-                const bool mine = !mbar_wait(&bars.s[g], s_cnt & 1) || s_abort;
+                const bool mine = !mbar_wait(&bars.s[g][s_cnt & 1], (s_cnt >> 1) & 1) || s_abort;
                 if (tile_any(g, mine)) { failed = true; break; }
                 ++s_cnt;
                 tc_fence_after();
@@ -503,9 +525,13 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     m_used = mt;
                 }
                 if (j > 0 && tile_any(g, need)) {
-                    // PV_g of the previous tile is complete (this tile's S was
-                    // committed after it by the same thread): rescale this
+                    // wait for PV_g of the previous tile (no later PV_g can have
+                    // been issued: it needs this tile's P), then rescale this
                     // half's 32 columns of O_g
+                    // o_conf == o_cnt + j - 1 here: PV_g(j-1) is the one pending phase
+                    if (tile_any(g, !mbar_wait(&bars.o[g], o_conf & 1))) { failed = true; break; }
+                    ++o_conf;
+                    tc_fence_after();
                     l0 *= alpha;
                     l1 *= alpha;
                     uint32_t o[32];
@@ -541,15 +567,21 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tmem_st32(tS + 32 * cc, pk);
                 }
                 tmem_st_wait();
+                // confirm PV_g(j-1) before releasing P_g(j): PV_g(j) cannot be
+                // issued before that release, so the o[g] barrier is never more
+                // than one phase ahead of this wait
+                if (j > 0 && o_conf < o_cnt + j) {
+                    if (tile_any(g, !mbar_wait(&bars.o[g], o_conf & 1))) { failed = true; break; }
+                    ++o_conf;
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars.p[g]);
             }
             if (failed) break;
             // epilogue: O_g after the item's last product; row sum from both halves
-            // PV_g(T-2) is complete (S_g(T-1) was committed after it), so the
-            // o[g] barrier is at most one phase from this wait
-            if (tile_any(g, !mbar_wait(&bars.o[g], (o_cnt + T - 1) & 1))) { failed = true; break; }
+            if (tile_any(g, !mbar_wait(&bars.o[g], o_conf & 1))) { failed = true; break; }
+            ++o_conf;
             o_cnt += T;
             tc_fence_after();
             uint32_t o[32];

@@ -103,6 +103,44 @@ struct Frag {
     }
 };
 
+// c + a.lo*b.lo + a.hi*b.hi for two packed bf16 pairs: products of bf16
+// values are exact in fp32, the sums are fp32 (mixed-precision FMA).
+__device__ __forceinline__ float dot2_bf16(uint32_t a, uint32_t b, float c) {
+    float r;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %3;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "=f"(r)
+        : "r"(a), "r"(b), "f"(c));
+    return r;
+}
+// (a0, a1) += w * (v.lo, v.hi) for a packed bf16 pair v: one f32x2 FMA.
+__device__ __forceinline__ void axpy2_bf16(float& a0, float& a1, float w, uint32_t v) {
+    asm("{\n\t.reg .b64 rv, rw, ra;\n\t.reg .b32 lo, hi;\n\t"
+        "shl.b32 lo, %3, 16;\n\tand.b32 hi, %3, 0xffff0000;\n\t"
+        "mov.b64 rv, {lo, hi};\n\tmov.b64 rw, {%2, %2};\n\tmov.b64 ra, {%0, %1};\n\t"
+        "fma.rn.f32x2 ra, rv, rw, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(w), "r"(v));
+}
+// (a0, a1) += (x0, x1) * (y0, y1): one f32x2 FMA.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float y0, float y1) {
+    asm("{\n\t.reg .b64 rx, ry, ra;\n\t"
+        "mov.b64 rx, {%2, %3};\n\tmov.b64 ry, {%4, %5};\n\tmov.b64 ra, {%0, %1};\n\t"
+        "fma.rn.f32x2 ra, rx, ry, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
+// (a0, a1) *= c: one f32x2 multiply.
+__device__ __forceinline__ void scale2(float& a0, float& a1, float c) {
+    asm("{\n\t.reg .b64 rc, ra;\n\t"
+        "mov.b64 rc, {%2, %2};\n\tmov.b64 ra, {%0, %1};\n\t"
+        "mul.rn.f32x2 ra, ra, rc;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(c));
+}
+
 template <typename T, int E>
 __device__ __forceinline__ void store_frag(T* p, const float* x) {
     if constexpr (sizeof(T) == 4) {
@@ -142,9 +180,13 @@ struct TaskMeta {
 };
 
 // Blocks per SM the register budget allows: lanes holding 16 values per
-// operand (two or four 16-byte vectors) get more registers than one-vector lanes.
+// operand (two 16-byte vectors) get more registers than one-vector lanes, and
+// fp32 lanes holding four vectors (16 values) two blocks' worth, so that their
+// operands and next-iteration copies stay out of local memory.
 template <typename T, int VPL>
-constexpr int rows_min_blocks() { return VPL == 1 ? GT_ROWS_MIN_BLOCKS1 : GT_ROWS_MIN_BLOCKS2; }
+constexpr int rows_min_blocks() {
+    return VPL == 1 ? GT_ROWS_MIN_BLOCKS1 : VPL == 2 ? GT_ROWS_MIN_BLOCKS2 : 2;
+}
 
 template <typename T, typename TO, int VPL, int MODE>
 __global__ void __launch_bounds__(256, rows_min_blocks<T, VPL>())
@@ -216,13 +258,16 @@ k_rows_vec(RowParams p) {
         int n_iter = (end - beg + step - 1) / step;
         n_iter = __reduce_max_sync(kFull, n_iter);
 
-        float q[E];
+        constexpr bool kBf16 = sizeof(T) == 2;
+        float q[E];          // fp32 inputs: q pre-scaled
+        F fq;                // bf16 inputs: q kept packed, the scale multiplies the dot
         if constexpr (MODE != kSpmm) {
-            F fq;
             if (valid) fq.load(Q + (int64_t)row * HD + lane_off); else fq.zero();
-            const float qs = MODE == kFused ? p.qscale : 1.f;   // SDDMM scales at the store
+            if constexpr (!kBf16) {
+                const float qs = MODE == kFused ? p.qscale : 1.f;   // SDDMM scales at the store
 #pragma unroll
-            for (int e = 0; e < E; ++e) q[e] = fq.get(e) * qs;
+                for (int e = 0; e < E; ++e) q[e] = fq.get(e) * qs;
+            }
         }
         float acc[E];
 #pragma unroll
@@ -265,10 +310,22 @@ k_rows_vec(RowParams p) {
             if constexpr (kNeedK) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    float d = 0.f;
+                    if constexpr (kBf16) {
+                        const uint32_t* qw = reinterpret_cast<const uint32_t*>(fq.v);
+                        const uint32_t* kw = reinterpret_cast<const uint32_t*>(kc[u].v);
+                        float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) d = fmaf(q[e], kc[u].get(e), d);
-                    l[u] = d;
+                        for (int w = 0; w < E / 2; w += 2) {
+                            d0 = dot2_bf16(qw[w], kw[w], d0);
+                            d1 = dot2_bf16(qw[w + 1], kw[w + 1], d1);
+                        }
+                        l[u] = (d0 + d1) * (MODE == kFused ? p.qscale : 1.f);
+                    } else {
+                        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                        for (int e = 0; e < E; e += 2) fma2(d0, d1, q[e], q[e + 1], kc[u].get(e), kc[u].get(e + 1));
+                        l[u] = d0 + d1;
+                    }
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u)
@@ -291,21 +348,33 @@ k_rows_vec(RowParams p) {
                 const float c = ex2(m - mref);
                 ssum *= c;
 #pragma unroll
-                for (int e = 0; e < E; ++e) acc[e] *= c;
+                for (int e = 0; e < E; e += 2) scale2(acc[e], acc[e + 1], c);
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const float w = ex2(l[u] - mref);
                     ssum += w;
+                    if constexpr (kBf16) {
+                        const uint32_t* vw = reinterpret_cast<const uint32_t*>(vc[u].v);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, vc[u].get(e), acc[e]);
+                        for (int e = 0; e < E; e += 2) axpy2_bf16(acc[e], acc[e + 1], w, vw[e >> 1]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < E; e += 2) fma2(acc[e], acc[e + 1], w, w, vc[u].get(e), vc[u].get(e + 1));
+                    }
                 }
                 m = mx;
             } else {   // kSpmm: weights are the given probabilities
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const float w = okc[u] ? p.probs[(int64_t)(e0 + u * S) * p.H + head] : 0.f;
+                    if constexpr (kBf16) {
+                        const uint32_t* vw = reinterpret_cast<const uint32_t*>(vc[u].v);
 #pragma unroll
-                    for (int e = 0; e < E; ++e) acc[e] = fmaf(w, vc[u].get(e), acc[e]);
+                        for (int e = 0; e < E; e += 2) axpy2_bf16(acc[e], acc[e + 1], w, vw[e >> 1]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < E; e += 2) fma2(acc[e], acc[e + 1], w, w, vc[u].get(e), vc[u].get(e + 1));
+                    }
                 }
             }
 #pragma unroll

@@ -8,24 +8,28 @@
 // scaled dot-product attention; a complete graph with self-loops makes the
 // sparse definition reduce to it).
 //
-// One CTA = two 128-row query tiles (A, B) of one block and one head, sharing
-// every K/V tile; warp-specialised:
-//   warp 9      TMA: Q_A, Q_B once, then K_j, V_j into a 3-stage ring (128-byte swizzle)
-//   warp 8      MMA (one thread): S_g = Q_g K_j^T (tcgen05.mma M=128 N=128 K=64,
-//               fp32 in TMEM), then O_g += P_g V_j once softmax g has written P_g
-//   warps 0-3   softmax of tile A, warps 4-7 softmax of tile B (one thread per
-//               query row): read the row of S_g from TMEM, keep a running max m
-//               (log2 units) raised only when a tile's max exceeds it by more
-//               than 8 (then O_g and l are rescaled), write
-//               P = 2^(s*scale*log2e - m) back over S_g as two bf16 terms
-//               P_hi = bf16(P), P_lo = bf16(P - P_hi); O_g += P_hi V + P_lo V
-// The MMA warp alternates A and B, so one tile's softmax overlaps the other's
-// matrix products; out = O / l at the end.  Splitting P in two bf16 terms
-// keeps the product at ~16-bit precision on the bf16 tensor path (a single
-// bf16 P would cost ~2^-9 relative per weight, outside the bf16 accuracy
-// bound of the path).  Every mbarrier wait is bounded: on timeout the CTA
-// records an error code, drains (bounded) the copies and MMAs it issued, frees
-// its tensor memory and returns.
+// A persistent CTA per SM walks work items: two 128-row query tiles (A, B)
+// of one block and one head, which share every K/V tile.  Warp roles:
+//   warps 0-7 / 8-15  softmax of tile A / B: two warpgroups per tile, each
+//                     thread one query row (= TMEM lane) and 64 of a key
+//                     tile's 128 columns
+//   warp 16           MMA issue: the whole warp runs the loop, one elected
+//                     lane issues S_g = Q_g K_j^T (tcgen05.mma M=128 N=128,
+//                     fp32 in TMEM) and O_g += P_g V_j (M=128 N=64, P read
+//                     from TMEM) once softmax g has written P_g
+//   warp 17           TMA: Q tiles (double-buffered across items), K_j and V_j
+//                     into a 4-stage ring (128-byte swizzle)
+// TMEM holds three S/P buffers used in rotation (the next S tile is computed
+// while the softmax works on the current one) and O_A, O_B.  The softmax
+// keeps a running row maximum m (log2 units) that is raised only when a
+// tile's maximum exceeds it by more than 8 (then O_g and the row sum are
+// rescaled), and writes P = 2^(s*scale*log2e - m) back over S_g as two bf16
+// terms P_hi = bf16(P), P_lo = bf16(P - P_hi); O_g += P_hi V + P_lo V keeps
+// the product at ~16-bit precision on the bf16 tensor path (a single bf16 P
+// would cost ~2^-9 relative per weight, outside the accuracy bound of the
+// bf16 path).  out = O / l at the end of an item.  Every mbarrier wait is
+// bounded: on timeout the CTA records an error code, drains (bounded) the
+// copies and MMAs it issued, frees its tensor memory and returns.
 #include "dense.cuh"
 
 #include <cuda.h>
@@ -67,11 +71,62 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// The same test, but a thread whose phase is not complete yet is suspended
+// (it takes no issue slots) until the phase completes or about 1 ms passes.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity), "r"(1000000u)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait for the phase with the given parity; false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, long long limit = kWaitCycles) {
+    if (mbar_test(b, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_test(b, parity)) {
+    while (!mbar_test_sleep(b, parity)) {
         if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
+// Non-blocking test (never suspends the thread).  The MMA warp issues it
+// before a batch of MMAs and reads the answer after the batch, so the test's
+// latency overlaps the batch instead of leaving the tensor pipe idle.
+__device__ __forceinline__ uint32_t mbar_probe(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+    return ok;
+}
+// Warp vote kept in program order with the surrounding asm (so a probe's
+// answer is consumed only where this vote stands).
+__device__ __forceinline__ bool warp_any_ordered(uint32_t v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "vote.sync.any.pred q, p, 0xffffffff;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v)
+        : "memory");
+    return r != 0;
+}
+// The same wait made by a whole converged warp; the result is uniform over
+// the warp (a completed phase stays completed, so any lane's success counts).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* b, uint32_t parity, long long limit = kWaitCycles) {
+    if (__any_sync(0xffffffffu, mbar_test(b, parity))) return true;
+    const long long t0 = clock64();
+    while (!__any_sync(0xffffffffu, mbar_test_sleep(b, parity))) {
+        if (__any_sync(0xffffffffu, clock64() - t0 > limit)) return false;
     }
     return true;
 }
@@ -88,22 +143,28 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// Called by a whole converged warp: one elected lane commits.  Issuing
+// tcgen05 work from a converged warp (rather than from inside a one-lane
+// branch) keeps its operands warp-uniform, and back-to-back MMAs then reach
+// the tensor pipe's rate.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(su32(bar))
+        : "memory");
 }
 
-// The MMA batches of the dense kernel, each in one asm block so the issuing
-// thread needs few issue slots (it shares its SM sub-partition with busy
-// softmax warps).
+// The MMA batches of the dense kernel, each in one asm block issued by one
+// elected lane of the converged MMA warp.
 // S (+)= Q K^T over K = 64: four K-steps of 32 bytes (descriptor start +2).
 __device__ __forceinline__ void mma_s_batch(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
     asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, 0, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %5, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %7, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %9, %3, q;\n\t}"
+        "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, 0, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %5, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %7, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %9, %3, q;\n\t}"
         ::"r"(d), "l"(a), "l"(b), "r"(idesc), "l"(a + 2), "l"(b + 2), "l"(a + 4), "l"(b + 4), "l"(a + 6), "l"(b + 6)
         : "memory");
 }
@@ -112,23 +173,24 @@ __device__ __forceinline__ void mma_s_batch(uint32_t d, uint64_t a, uint64_t b, 
 // step start 2048 bytes (128 descriptor units) after the previous step's.
 __device__ __forceinline__ void mma_pv_batch(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+0], %2, %3, p;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %2, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], %5, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], %5, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], %6, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], %6, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], %7, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], %7, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+64], %8, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+80], %8, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+72], %9, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+88], %9, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+96], %10, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+112], %10, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+104], %11, %3, q;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+120], %11, %3, q;\n\t}"
+        "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+0], %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %2, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], %5, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], %5, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], %6, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], %6, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], %7, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], %7, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+64], %8, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+80], %8, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+72], %9, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+88], %9, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+96], %10, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+112], %10, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+104], %11, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+120], %11, %3, q;\n\t}"
         ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc), "l"(b + 128), "l"(b + 256), "l"(b + 384), "l"(b + 512),
           "l"(b + 640), "l"(b + 768), "l"(b + 896)
         : "memory");
@@ -198,7 +260,7 @@ struct DenseErr {
 // 0-63, half 1: keys 64-127) and exchange row maxima through shared memory:
 //   warps 0-3 / 4-7     tile A, halves 0 / 1
 //   warps 8-11 / 12-15  tile B, halves 0 / 1
-//   warp 16             MMA issue (one thread)
+//   warp 16             MMA issue (one elected lane of the converged warp)
 //   warp 17             TMA loads (one thread); warps 18-19 idle
 // The grid is persistent (one CTA per SM): each CTA walks work items (a pair
 // of query tiles and a head); Q tiles are double-buffered and the K/V ring
@@ -270,12 +332,10 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
     asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
-// barrier over the 256 threads (8 warps) of one query tile's two warpgroups
-__device__ __forceinline__ void tile_bar(int g) {
-    asm volatile("bar.sync %0, 256;" ::"r"(1 + g) : "memory");
-}
-// OR of `pred` over the same 256 threads, returned to all of them (also a
-// barrier): keeps every decision that precedes a tile_bar uniform
+// OR of `pred` over the 256 threads (8 warps) of one query tile's two
+// warpgroups, returned to all of them; also a barrier over those threads.
+// Every decision that leads to a later barrier is taken from such a vote, so
+// the 8 warps always meet at the same barriers.
 __device__ __forceinline__ bool tile_any(int g, bool pred) {
     uint32_t r;
     asm volatile(
@@ -347,9 +407,12 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             bool ok = true;
             int kv_tile = 0;   // running K/V tile counter over all items of this CTA
             int local = 0;
+            int h_next = 0;
+            int4 it_next = blockIdx.x < n_work ? item_of(items, blockIdx.x, H, &h_next) : make_int4(0, 0, 0, 0);
             for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++local) {
-                int h;
-                const int4 it = item_of(items, w, H, &h);
+                const int h = h_next;
+                const int4 it = it_next;   // the next item's entry is loaded one item ahead
+                if (w + gridDim.x < n_work) it_next = item_of(items, w + gridDim.x, H, &h_next);
                 const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = n / kTile, xh = h * kD;
                 const int qb = local & 1;
                 if (local >= 2) ok = mbar_wait(&bars.q_empty[qb], ((local >> 1) - 1) & 1);
@@ -385,8 +448,15 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         // Order per item (two query tiles): S_A0 S_B0 S_A1, then per key tile j:
         // PV_Aj, S_B(j+1), PV_Bj, S_A(j+2).  An S tile is computed one step ahead
         // of its softmax; a buffer is reused only after the PV that read its P
-        // (the tensor pipe executes one thread's MMAs in issue order).
-        if (lane == 0) {
+        // (the tensor pipe executes one thread's MMAs in issue order).  The
+        // whole warp runs this loop; elect.sync picks the same lane (the
+        // lowest) for every batch and commit, so one thread issues them all.
+        // Barrier states needed after a batch are probed before it (non-
+        // blocking) and read after it, so a test's latency overlaps the
+        // batch; the waits follow S batches where possible (the tensor pipe's
+        // short queue covers ~300 cycles of non-MMA work after 4 S MMAs but
+        // only ~170 after 16 PV MMAs).
+        {
             const uint32_t idS = idesc_bf16(128, 128, 0);
             const uint32_t idO = idesc_bf16(128, 64, 1);
             bool ok = true;
@@ -402,10 +472,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 const int qb = local & 1;
                 const int s0 = snum;   // S number of (g, j) = s0 + nq*j + g
                 auto bufk = [&](int g, int j) { return (s0 + nq * j + g) % 3; };
+                // S_g(j); the K tile's readiness was established before
                 auto issue_s = [&](int g, int j) {
                     const int kt = kv_tile + j;
-                    if (g == 0 && !mbar_wait(&bars.kv_full[kt % kStages], (kt / kStages) & 1)) return false;
-                    tc_fence_after();
                     const uint64_t dQ = smem_desc_sw128(su32(sQ(qb, g)), 16, 1024);
                     const uint64_t dK = smem_desc_sw128(su32(sK(kt % kStages)), 16, 1024);
                     mma_s_batch(tmem + col_buf(bufk(g, j)), dQ, dK, idS);
@@ -413,50 +482,79 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tc_commit(&bars.s[g][sn & 1]);
                     ++sn;
                     ++snum;
-                    return true;
+                };
+                auto kv_probe = [&](int j) {
+                    const int kt = kv_tile + j;
+                    return mbar_probe(&bars.kv_full[kt % kStages], (kt / kStages) & 1);
+                };
+                auto kv_wait = [&](int j, uint32_t probed) {
+                    const int kt = kv_tile + j;
+                    if (warp_any_ordered(probed)) return true;
+                    return mbar_wait_warp(&bars.kv_full[kt % kStages], (kt / kStages) & 1);
+                };
+                auto p_probe = [&](int g) { return mbar_probe(&bars.p[g], (g == 0 ? p_cnt0 : p_cnt1) & 1); };
+                // P_g(j) written (probe answer `probed`, else a blocking wait)
+                auto p_wait = [&](int g, uint32_t probed) {
+                    int& pc = g == 0 ? p_cnt0 : p_cnt1;
+                    const bool r = warp_any_ordered(probed) || mbar_wait_warp(&bars.p[g], pc & 1);
+                    ++pc;
+                    return r;
                 };
                 auto issue_pv = [&](int g, int j) {
-                    int& pc = g == 0 ? p_cnt0 : p_cnt1;
-                    const int done_items = g == 0 ? items0 : items1;
-                    if (!mbar_wait(&bars.p[g], pc & 1)) return false;
-                    ++pc;
-                    // the first product of an item overwrites O_g: the previous
-                    // item's epilogue must have read it
-                    if (j == 0 && done_items > 0 && !mbar_wait(&bars.o_free[g], (done_items - 1) & 1)) return false;
-                    tc_fence_after();
                     const int kt = kv_tile + j;
                     const uint64_t dV = smem_desc_sw128(su32(sV(kt % kStages)), 8192, 1024);
                     mma_pv_batch(tmem + col_o(g), tmem + col_buf(bufk(g, j)), dV, idO, j > 0 ? 1u : 0u);
                     tc_commit(&bars.o[g]);
-                    return true;
                 };
-                ok = mbar_wait(&bars.q_full[qb], (local >> 1) & 1);
+                ok = mbar_wait_warp(&bars.q_full[qb], (local >> 1) & 1);
                 if (!ok) break;
                 // S tiles ahead of the loop: A0 (B0) and A1
-                for (int g = 0; ok && g < nq; ++g) ok = issue_s(g, 0);
-                if (ok && T > 1) ok = issue_s(0, 1);
-                if (ok && nq == 1 && T > 1) { /* A1 already issued */ }
+                ok = kv_wait(0, 0u);
+                if (ok) {
+                    tc_fence_after();
+                    for (int g = 0; g < nq; ++g) issue_s(g, 0);
+                }
+                if (ok && T > 1) {
+                    ok = kv_wait(1, 0u);
+                    tc_fence_after();
+                    if (ok) issue_s(0, 1);
+                }
+                uint32_t pa = p_probe(0);
                 for (int j = 0; ok && j < T; ++j) {
-                    ok = issue_pv(0, j);
+                    // the first product of an item overwrites O_g: the previous
+                    // item's epilogue must have read it
+                    ok = p_wait(0, pa);
+                    if (ok && j == 0 && items0 > 0) ok = mbar_wait_warp(&bars.o_free[0], (items0 - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t pb = nq > 1 ? p_probe(1) : 0u;
+                    const uint32_t kv = j + 2 < T ? kv_probe(j + 2) : 0u;
+                    issue_pv(0, j);
+                    if (nq > 1 && j + 1 < T) issue_s(1, j + 1);
+                    if (j + 2 < T) ok = kv_wait(j + 2, kv);
                     if (ok && nq > 1) {
-                        if (j + 1 < T) ok = issue_s(1, j + 1);
-                        if (ok) ok = issue_pv(1, j);
+                        ok = p_wait(1, pb);
+                        if (ok && j == 0 && items1 > 0) ok = mbar_wait_warp(&bars.o_free[1], (items1 - 1) & 1);
                     }
-                    if (ok) tc_commit(&bars.kv_empty[(kv_tile + j) % kStages]);   // K_j, V_j free after these
-                    if (ok && j + 2 < T) ok = issue_s(0, j + 2);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (nq > 1) issue_pv(1, j);
+                    tc_commit(&bars.kv_empty[(kv_tile + j) % kStages]);   // K_j, V_j free after these
+                    pa = p_probe(0);
+                    if (j + 2 < T) issue_s(0, j + 2);
                 }
                 if (ok) tc_commit(&bars.q_empty[qb]);        // Q buffer free after this item's products
                 ++items0;
                 if (nq > 1) ++items1;
                 kv_tile += T;
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 atomicOr(err, DenseErr::kTimeout);
                 atomicExch(&s_abort, 1);
             }
-            // drain: everything this thread issued has finished before TMEM is freed
+            // drain: everything the elected lane issued has finished before TMEM is freed
             tc_commit(&bars.drain);
-            mbar_wait(&bars.drain, 0, kWaitCycles / 4);
+            mbar_wait_warp(&bars.drain, 0, kWaitCycles / 4);
         }
     } else if (warp < kMmaWarp) {
         // ---------------- softmax warpgroups ----------------
@@ -472,9 +570,12 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         int par = 0;
         int snum = 0;   // S tiles of the CTA's sequence before the current item (both query tiles)
         bool failed = false;
+        int h_next = 0;
+        int4 it_next = blockIdx.x < n_work ? item_of(items, blockIdx.x, H, &h_next) : make_int4(0, 0, 0, 0);
         for (int w = blockIdx.x; !failed && w < n_work; w += gridDim.x) {
-            int h;
-            const int4 it = item_of(items, w, H, &h);
+            const int h = h_next;
+            const int4 it = it_next;   // the next item's entry is loaded one item ahead
+            if (w + gridDim.x < n_work) it_next = item_of(items, w + gridDim.x, H, &h_next);
             const int n = it.y, q0 = it.z, nq = it.w, T = n / kTile, xh = h * kD;
             const int s0 = snum;
             snum += nq * T;
@@ -482,10 +583,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;
             for (int j = 0; j < T; ++j) {
                 const uint32_t tS = tmem + col_buf((s0 + nq * j + g) % 3) + lane_base + 64 * half;
-                // decision uniform over the tile's 8 warps (tcgen05.ld/st are
-                // warp-collective and the row-max exchange is a tile barrier)
-                const bool mine = !mbar_wait(&bars.s[g][s_cnt & 1], (s_cnt >> 1) & 1) || s_abort;
-                if (tile_any(g, mine)) { failed = true; break; }
+                // a wait that runs out marks the CTA aborted; the tile leaves
+                // its loop together at the next vote, so every barrier below
+                // is reached by all of its 8 warps
+                bool bad = !mbar_wait(&bars.s[g][s_cnt & 1], (s_cnt >> 1) & 1);
                 ++s_cnt;
                 tc_fence_after();
                 uint32_t r[64];
@@ -508,40 +609,48 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     }
                     ma = fminf(ma, mb);
                 }
-                // the other half's extreme (parity double-buffer: the slot written
-                // now was last read before the previous tile's barrier)
+                // This half's extreme goes to shared memory (parity double
+                // buffer: the slot written now was last read before the
+                // previous tile's vote).  The row maximum is needed only on the
+                // first tile of an item and when this tile's maximum exceeds
+                // the one in use by more than the threshold; otherwise P keeps
+                // the maximum in use (P <= 2^threshold) and no exchange is made.
                 s_red[g][par][half][row] = ma;
-                tile_bar(g);
-                const float other = s_red[g][par][half ^ 1][row];
-                par ^= 1;
-                const float mt = (pos ? fmaxf(ma, other) : fminf(ma, other)) * sl2;
-                bool need = false;
-                float alpha = 1.f;
-                if (j == 0) {
-                    m_used = mt;
-                } else if (mt > m_used + kRescaleThreshold) {
-                    need = true;
-                    alpha = ex2(m_used - mt);
-                    m_used = mt;
-                }
-                if (j > 0 && tile_any(g, need)) {
-                    // wait for PV_g of the previous tile (no later PV_g can have
-                    // been issued: it needs this tile's P), then rescale this
-                    // half's 32 columns of O_g
-                    // o_conf == o_cnt + j - 1 here: PV_g(j-1) is the one pending phase
-                    if (tile_any(g, !mbar_wait(&bars.o[g], o_conf & 1))) { failed = true; break; }
-                    ++o_conf;
-                    tc_fence_after();
-                    l0 *= alpha;
-                    l1 *= alpha;
-                    uint32_t o[32];
-                    tmem_ld32(tO, o);
-                    tmem_ld_wait();
+                if (bad) atomicExch(&s_abort, 1);
+                const bool abort_seen = bad || *reinterpret_cast<volatile int*>(&s_abort) != 0;
+                const bool need = j == 0 || ma * sl2 > m_used + kRescaleThreshold;
+                if (tile_any(g, need || abort_seen)) {
+                    if (tile_any(g, abort_seen)) { failed = true; break; }
+                    const float other = s_red[g][par][half ^ 1][row];
+                    const float mt = (pos ? fmaxf(ma, other) : fminf(ma, other)) * sl2;
+                    if (j == 0) {
+                        m_used = mt;
+                    } else {
+                        const bool up = mt > m_used + kRescaleThreshold;
+                        if (__any_sync(0xffffffffu, up)) {
+                            // O_g may be rescaled only after PV_g(j-1); no later
+                            // PV_g can have been issued (it needs this tile's P)
+                            if (!mbar_wait(&bars.o[g], o_conf & 1)) {
+                                bad = true;
+                                atomicExch(&s_abort, 1);
+                            }
+                            ++o_conf;
+                            tc_fence_after();
+                            const float alpha = up ? ex2(m_used - mt) : 1.f;
+                            if (up) m_used = mt;
+                            l0 *= alpha;
+                            l1 *= alpha;
+                            uint32_t o[32];
+                            tmem_ld32(tO, o);
+                            tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tO, o);
-                    tmem_st_wait();
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            tmem_st32(tO, o);
+                            tmem_st_wait();
+                        }
+                    }
                 }
+                par ^= 1;
                 // P = 2^(s*scale*log2e - m) as bf16 hi/lo over this half of S,
                 // 32 keys at a time (re-read from TMEM to keep registers low)
                 const float nm = -m_used;
@@ -567,11 +676,11 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tmem_st32(tS + 32 * cc, pk);
                 }
                 tmem_st_wait();
-                // confirm PV_g(j-1) before releasing P_g(j): PV_g(j) cannot be
-                // issued before that release, so the o[g] barrier is never more
-                // than one phase ahead of this wait
+                // confirm PV_g(j-1) (this warp) before releasing P_g(j): PV_g(j)
+                // cannot be issued before that release, so the o[g] barrier is
+                // never more than one phase ahead of a wait on it
                 if (j > 0 && o_conf < o_cnt + j) {
-                    if (tile_any(g, !mbar_wait(&bars.o[g], o_conf & 1))) { failed = true; break; }
+                    if (!mbar_wait(&bars.o[g], o_conf & 1)) atomicExch(&s_abort, 1);
                     ++o_conf;
                 }
                 tc_fence_before();
@@ -580,7 +689,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             }
             if (failed) break;
             // epilogue: O_g after the item's last product; row sum from both halves
-            if (tile_any(g, !mbar_wait(&bars.o[g], o_conf & 1))) { failed = true; break; }
+            bool bad = !mbar_wait(&bars.o[g], o_conf & 1);
             ++o_conf;
             o_cnt += T;
             tc_fence_after();
@@ -591,7 +700,8 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.o_free[g]);
             s_red[g][par][half][row] = l0 + l1;
-            tile_bar(g);
+            if (bad) atomicExch(&s_abort, 1);
+            if (tile_any(g, bad || *reinterpret_cast<volatile int*>(&s_abort) != 0)) { failed = true; break; }
             const float inv = 1.f / (l0 + l1 + s_red[g][par][half ^ 1][row]);
             par ^= 1;
             TO* op = out + static_cast<int64_t>(q0 + g * kTile + row) * HD + xh + 32 * half;

@@ -10,10 +10,11 @@ namespace gt {
 bool dense_supported(int H, int D, gtattn_dtype dt, const void* Q, const void* K, const void* V,
                      const void* out);
 
-// out = softmax(scale * Q K^T) V per head over complete blocks, one CTA per
-// (128-row query tile, head).  tiles: device array of (first row of the
-// block, block size, first row of the query tile, 0).  A bounded device wait
-// that times out ORs an error code into *err.
+// out = softmax(scale * Q K^T) V per head over complete blocks on a
+// persistent grid (one CTA per SM).  tiles: device array of work items
+// (first row of the block, block size, first row of the item's query rows,
+// number of 128-row query tiles (1 or 2)); block sizes are multiples of 128.
+// A bounded device wait that times out ORs an error code into *err.
 gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void* Q, const void* K,
                            const void* V, void* out, int H, int D, float scale, gtattn_dtype dt, int* err,
                            cudaStream_t s);

@@ -289,8 +289,13 @@ struct WsBars {
     uint64_t s[2][2];    // S tile n of query tile g is in TMEM: barrier s[g][n & 1]
                          // (MMA -> softmax g; two barriers because an S tile
                          // can run two ahead of its softmax)
-    uint64_t p[2];       // P_g written over S_g (softmax g -> MMA), 8 warp arrivals
-    uint64_t o[2];       // PV_g done (MMA -> softmax g, waited for the epilogue)
+    uint64_t p[2][2];    // P_g number n written over its S: barrier p[g][n & 1], phase n >> 1
+                         // (softmax g -> MMA), 8 warp arrivals.  Two barriers because
+                         // the softmax may finish P_g(n+1) before the MMA warp has
+                         // waited for P_g(n); P_g(n+2) needs S_g(n+2), which the MMA
+                         // warp issues only after PV_g(n).
+    uint64_t o[2][2];    // PV_g number n of the CTA is done: barrier o[g][n & 1], phase n >> 1
+                         // (MMA -> softmax g, waited at a rescale and the epilogue)
     uint64_t o_free[2];  // softmax g has read O_g in its epilogue (-> MMA), 8 arrivals
     uint64_t drain;
 };
@@ -332,19 +337,45 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
     asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
-// OR of `pred` over the 256 threads (8 warps) of one query tile's two
-// warpgroups, returned to all of them; also a barrier over those threads.
-// Every decision that leads to a later barrier is taken from such a vote, so
-// the 8 warps always meet at the same barriers.
-__device__ __forceinline__ bool tile_any(int g, bool pred) {
+// OR of `pred` over the two warps that hold the two halves (key columns
+// 0-63 and 64-127) of the same 32 query rows -- the only warps that exchange
+// data -- returned to both; also a barrier over those 64 threads (named
+// barrier `id`).  Every decision that leads to a later barrier of the pair is
+// taken from such a vote, so both warps always meet at the same barriers.
+__device__ __forceinline__ bool pair_any(int id, bool pred) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "bar.red.or.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(1 + g)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id)
         : "memory");
     return r != 0;
+}
+// 4x4 transpose of 16-byte chunks over the four lanes of a quad: on entry
+// lane l of the quad holds chunks 0-3 of its own row; on exit c[k] is chunk l
+// of the quad's row k.  The quad then stores one row's four chunks per
+// instruction (64 contiguous bytes) instead of four rows' single chunks.
+__device__ __forceinline__ void quad_transpose(uint4 (&c)[4], int lane) {
+    const bool b0 = lane & 1, b1 = (lane & 2) != 0;
+    auto xchg = [](uint4 v, int m) {
+        uint4 r;
+        r.x = __shfl_xor_sync(0xffffffffu, v.x, m);
+        r.y = __shfl_xor_sync(0xffffffffu, v.y, m);
+        r.z = __shfl_xor_sync(0xffffffffu, v.z, m);
+        r.w = __shfl_xor_sync(0xffffffffu, v.w, m);
+        return r;
+    };
+#pragma unroll
+    for (int q = 0; q < 4; q += 2) {   // across lane bit 0: positions (0,1) and (2,3)
+        const uint4 r = xchg(b0 ? c[q] : c[q + 1], 1);
+        if (b0) c[q] = r; else c[q + 1] = r;
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {      // across lane bit 1: positions (0,2) and (1,3)
+        const uint4 r = xchg(b1 ? c[q] : c[q + 2], 2);
+        if (b1) c[q] = r; else c[q + 2] = r;
+    }
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
@@ -389,8 +420,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         for (int g = 0; g < 2; ++g) {
             mbar_init(&bars.s[g][0], 1);
             mbar_init(&bars.s[g][1], 1);
-            mbar_init(&bars.p[g], 8);
-            mbar_init(&bars.o[g], 1);
+            mbar_init(&bars.p[g][0], 8);
+            mbar_init(&bars.p[g][1], 8);
+            mbar_init(&bars.o[g][0], 1);
+            mbar_init(&bars.o[g][1], 1);
             mbar_init(&bars.o_free[g], 8);
         }
         mbar_init(&bars.drain, 1);
@@ -464,6 +497,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             int snum = 0;      // S tiles issued so far (buffer = snum % 3)
             int sg0 = 0, sg1 = 0;   // S tiles issued per query tile (barrier s[g][n & 1])
             int p_cnt0 = 0, p_cnt1 = 0, items0 = 0, items1 = 0;
+            int pv0 = 0, pv1 = 0;   // products issued per query tile (barrier o[g][n & 1])
             int local = 0;
             for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++local) {
                 int h;
@@ -492,11 +526,14 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     if (warp_any_ordered(probed)) return true;
                     return mbar_wait_warp(&bars.kv_full[kt % kStages], (kt / kStages) & 1);
                 };
-                auto p_probe = [&](int g) { return mbar_probe(&bars.p[g], (g == 0 ? p_cnt0 : p_cnt1) & 1); };
+                auto p_probe = [&](int g) {
+                    const int pc = g == 0 ? p_cnt0 : p_cnt1;
+                    return mbar_probe(&bars.p[g][pc & 1], (pc >> 1) & 1);
+                };
                 // P_g(j) written (probe answer `probed`, else a blocking wait)
                 auto p_wait = [&](int g, uint32_t probed) {
                     int& pc = g == 0 ? p_cnt0 : p_cnt1;
-                    const bool r = warp_any_ordered(probed) || mbar_wait_warp(&bars.p[g], pc & 1);
+                    const bool r = warp_any_ordered(probed) || mbar_wait_warp(&bars.p[g][pc & 1], (pc >> 1) & 1);
                     ++pc;
                     return r;
                 };
@@ -504,7 +541,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     const int kt = kv_tile + j;
                     const uint64_t dV = smem_desc_sw128(su32(sV(kt % kStages)), 8192, 1024);
                     mma_pv_batch(tmem + col_o(g), tmem + col_buf(bufk(g, j)), dV, idO, j > 0 ? 1u : 0u);
-                    tc_commit(&bars.o[g]);
+                    int& pn = g == 0 ? pv0 : pv1;
+                    tc_commit(&bars.o[g][pn & 1]);
+                    ++pn;
                 };
                 ok = mbar_wait_warp(&bars.q_full[qb], (local >> 1) & 1);
                 if (!ok) break;
@@ -564,9 +603,16 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tO = tmem + col_o(g) + lane_base + 32 * half;
         const bool pos = sl2 >= 0.f;
+        const int pair_id = 1 + g * 4 + (warp & 3);    // named barrier of this warp and its other half
         int s_cnt = 0;      // S tiles of this query tile consumed so far
         int o_cnt = 0;      // PV_g products of finished items
-        int o_conf = 0;     // o[g] phases confirmed (waited) so far
+        // Wait for PV_g number n.  Two barriers keep each wait inside the
+        // barrier's two-phase window without confirming every product: when
+        // the softmax waits for PV_g(n) it has seen S_g complete for a tile
+        // whose S was issued after PV_g(n-2) (S_g(j) follows PV_g(j-2) in the
+        // MMA order, and the S commit tracks every earlier MMA), so the
+        // previous phase of barrier o[g][n & 1] has completed.
+        auto o_wait = [&](int n) { return mbar_wait(&bars.o[g][n & 1], (n >> 1) & 1); };
         int par = 0;
         int snum = 0;   // S tiles of the CTA's sequence before the current item (both query tiles)
         bool failed = false;
@@ -619,8 +665,8 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 if (bad) atomicExch(&s_abort, 1);
                 const bool abort_seen = bad || *reinterpret_cast<volatile int*>(&s_abort) != 0;
                 const bool need = j == 0 || ma * sl2 > m_used + kRescaleThreshold;
-                if (tile_any(g, need || abort_seen)) {
-                    if (tile_any(g, abort_seen)) { failed = true; break; }
+                if (pair_any(pair_id, need || abort_seen)) {
+                    if (pair_any(pair_id, abort_seen)) { failed = true; break; }
                     const float other = s_red[g][par][half ^ 1][row];
                     const float mt = (pos ? fmaxf(ma, other) : fminf(ma, other)) * sl2;
                     if (j == 0) {
@@ -630,11 +676,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                         if (__any_sync(0xffffffffu, up)) {
                             // O_g may be rescaled only after PV_g(j-1); no later
                             // PV_g can have been issued (it needs this tile's P)
-                            if (!mbar_wait(&bars.o[g], o_conf & 1)) {
+                            if (!o_wait(o_cnt + j - 1)) {
                                 bad = true;
                                 atomicExch(&s_abort, 1);
                             }
-                            ++o_conf;
                             tc_fence_after();
                             const float alpha = up ? ex2(m_used - mt) : 1.f;
                             if (up) m_used = mt;
@@ -676,21 +721,13 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tmem_st32(tS + 32 * cc, pk);
                 }
                 tmem_st_wait();
-                // confirm PV_g(j-1) (this warp) before releasing P_g(j): PV_g(j)
-                // cannot be issued before that release, so the o[g] barrier is
-                // never more than one phase ahead of a wait on it
-                if (j > 0 && o_conf < o_cnt + j) {
-                    if (!mbar_wait(&bars.o[g], o_conf & 1)) atomicExch(&s_abort, 1);
-                    ++o_conf;
-                }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.p[g]);
+                if (lane == 0) mbar_arrive(&bars.p[g][(o_cnt + j) & 1]);
             }
             if (failed) break;
             // epilogue: O_g after the item's last product; row sum from both halves
-            bool bad = !mbar_wait(&bars.o[g], o_conf & 1);
-            ++o_conf;
+            bool bad = !o_wait(o_cnt + T - 1);
             o_cnt += T;
             tc_fence_after();
             uint32_t o[32];
@@ -701,25 +738,41 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             if (lane == 0) mbar_arrive(&bars.o_free[g]);
             s_red[g][par][half][row] = l0 + l1;
             if (bad) atomicExch(&s_abort, 1);
-            if (tile_any(g, bad || *reinterpret_cast<volatile int*>(&s_abort) != 0)) { failed = true; break; }
+            if (pair_any(pair_id, bad || *reinterpret_cast<volatile int*>(&s_abort) != 0)) { failed = true; break; }
             const float inv = 1.f / (l0 + l1 + s_red[g][par][half ^ 1][row]);
             par ^= 1;
-            TO* op = out + static_cast<int64_t>(q0 + g * kTile + row) * HD + xh + 32 * half;
+            // rows of this lane's quad after the transpose: quad base + k
+            TO* op = out + static_cast<int64_t>(q0 + g * kTile + (row & ~3)) * HD + xh + 32 * half;
+            const int ql = lane & 3;
             if constexpr (sizeof(TO) == 2) {
-                uint4* o4 = reinterpret_cast<uint4*>(op);
+                uint4 c[4];
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
-                    o4[v] = make_uint4(
+                    c[v] = make_uint4(
                         pack2_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
                         pack2_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
                         pack2_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
                         pack2_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
-            } else {
-                float4* o4 = reinterpret_cast<float4*>(op);
+                quad_transpose(c, lane);
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    o4[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                        __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+                for (int k = 0; k < 4; ++k) reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD)[ql] = c[k];
+            } else {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {   // columns 16*hh .. 16*hh+15 of this half
+                    uint4 c[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int e = 16 * hh + 4 * v;
+                        c[v] = make_uint4(__float_as_uint(__uint_as_float(o[e]) * inv),
+                                          __float_as_uint(__uint_as_float(o[e + 1]) * inv),
+                                          __float_as_uint(__uint_as_float(o[e + 2]) * inv),
+                                          __float_as_uint(__uint_as_float(o[e + 3]) * inv));
+                    }
+                    quad_transpose(c, lane);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD + 16 * hh)[ql] = c[k];
+                }
             }
         }
         if (failed) {

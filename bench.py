@@ -64,9 +64,10 @@ def measured_peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def ncu_traffic(kernel_tag: str, workload: str):
+def ncu_traffic(kernel_tag: str, workload: str, src_name: str = "rows.cu"):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, or None when there is none or the kernel source changed since."""
+    workload, or None when there is none or the kernel source (`src_name`
+    under csrc/) changed since."""
     import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
     if not os.path.exists(path):
@@ -76,7 +77,7 @@ def ncu_traffic(kernel_tag: str, workload: str):
     m_h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m_b or not m_h:
         return None
-    src = os.path.join(ROOT, "graph_transformer_sparse_gb300", "csrc", "rows.cu")
+    src = os.path.join(ROOT, "graph_transformer_sparse_gb300", "csrc", src_name)
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != m_h.group(1):
         return None
     return float(m_b.group(1))
@@ -369,7 +370,7 @@ def gpu_arm(args):
         roofline = {"bound": "tensor", "kernel": "k_dense_attn (tcgen05 dense-block kernel)",
                     "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": round(achieved / peaks["bf16_tflops"], 4),
-                    "traffic": None,
+                    "traffic": ncu_traffic("k_dense_attn", name, "dense.cu"),
                     "peak_source": f"{peaks['source']} bf16_tflops (burst: the kernel is timed per launch)",
                     "algorithmic_flops_per_launch": flops, "kernel_ms": round(kern_ms, 5),
                     "kernel_shares": shares}

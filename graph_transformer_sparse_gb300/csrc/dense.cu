@@ -711,8 +711,13 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                         const float p0 = ex2(t0), p1 = ex2(t1);
                         fadd2(l0, l1, p0, p1);
                         const uint32_t hi = pack2_bf16(p0, p1);
+                        // P_lo = bf16(P - P_hi): the differences, exact in fp32, come
+                        // from mixed bf16 x bf16 + fp32 FMAs on the packed P_hi halves
+                        // (times -1) -- no unpacking of P_hi
                         float d0, d1;
-                        fsub2(d0, d1, p0, p1, __uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+                        asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+                            "fma.rn.f32.bf16 %0, h0, %5, %3;\n\tfma.rn.f32.bf16 %1, h1, %5, %4;\n\t}"
+                            : "=f"(d0), "=f"(d1) : "r"(hi), "f"(p0), "f"(p1), "h"((unsigned short)0xBF80));
                         pk[q] = hi;
                         pk[16 + q] = pack2_bf16(d0, d1);
                     }

@@ -10,14 +10,14 @@
 //
 // A persistent CTA per SM walks work items: two 128-row query tiles (A, B)
 // of one block and one head, which share every K/V tile.  Warp roles:
-//   warps 0-7 / 8-15  softmax of tile A / B: two warpgroups per tile, each
-//                     thread one query row (= TMEM lane) and 64 of a key
-//                     tile's 128 columns
-//   warp 16           MMA issue: the whole warp runs the loop, one elected
+//   warps 0-3 / 4-7   softmax of tile A / B: one warpgroup per tile, each
+//                     thread one query row (= TMEM lane) over all 128 key
+//                     columns of a tile (no exchange between warps)
+//   warp 8            MMA issue: the whole warp runs the loop, one elected
 //                     lane issues S_g = Q_g K_j^T (tcgen05.mma M=128 N=128,
 //                     fp32 in TMEM) and O_g += P_g V_j (M=128 N=64, P read
 //                     from TMEM) once softmax g has written P_g
-//   warp 17           TMA: Q tiles (double-buffered across items), K_j and V_j
+//   warp 9            TMA: Q tiles (double-buffered across items), K_j and V_j
 //                     into a 4-stage ring (128-byte swizzle)
 // TMEM holds three S/P buffers used in rotation (the next S tile is computed
 // while the softmax works on the current one) and O_A, O_B.  The softmax
@@ -254,22 +254,20 @@ struct DenseErr {
     static constexpr int kTimeout = 1;
 };
 
-// Warp roles of the CTA (20 warps).  Two query tiles per work item (A: rows
-// q0.., B: rows q0+128..) share every K/V tile.  Each query tile has two
-// softmax warpgroups that split the 128 key columns of a tile (half 0: keys
-// 0-63, half 1: keys 64-127) and exchange row maxima through shared memory:
-//   warps 0-3 / 4-7     tile A, halves 0 / 1
-//   warps 8-11 / 12-15  tile B, halves 0 / 1
-//   warp 16             MMA issue (one elected lane of the converged warp)
-//   warp 17             TMA loads (one thread); warps 18-19 idle
+// Warp roles of the CTA (10 warps).  Two query tiles per work item (A: rows
+// q0.., B: rows q0+128..) share every K/V tile.  Each query tile has one
+// softmax warpgroup, a thread per query row over all 128 key columns:
+//   warps 0-3 / 4-7     softmax of tile A / B
+//   warp 8              MMA issue (one elected lane of the converged warp)
+//   warp 9              TMA loads (one thread)
 // The grid is persistent (one CTA per SM): each CTA walks work items (a pair
 // of query tiles and a head); Q tiles are double-buffered and the K/V ring
 // runs on across items, so the next item's loads and first products overlap
 // the current item's last softmax and epilogue.
-constexpr int kWarps = 20;
+constexpr int kWarps = 10;
 constexpr int kThreadsWS = kWarps * 32;
-constexpr int kMmaWarp = 16;
-constexpr int kTmaWarp = 17;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
 constexpr int kStages = 4;                        // K/V ring
 constexpr uint32_t kTmemAll = 512;
 // TMEM: three S/P buffers (128 columns each) used in rotation by the S tiles
@@ -290,13 +288,13 @@ struct WsBars {
                          // (MMA -> softmax g; two barriers because an S tile
                          // can run two ahead of its softmax)
     uint64_t p[2][2];    // P_g number n written over its S: barrier p[g][n & 1], phase n >> 1
-                         // (softmax g -> MMA), 8 warp arrivals.  Two barriers because
+                         // (softmax g -> MMA), 4 warp arrivals.  Two barriers because
                          // the softmax may finish P_g(n+1) before the MMA warp has
                          // waited for P_g(n); P_g(n+2) needs S_g(n+2), which the MMA
                          // warp issues only after PV_g(n).
     uint64_t o[2][2];    // PV_g number n of the CTA is done: barrier o[g][n & 1], phase n >> 1
                          // (MMA -> softmax g, waited at a rescale and the epilogue)
-    uint64_t o_free[2];  // softmax g has read O_g in its epilogue (-> MMA), 8 arrivals
+    uint64_t o_free[2];  // softmax g has read O_g in its epilogue (-> MMA), 4 arrivals
     uint64_t drain;
 };
 
@@ -320,13 +318,6 @@ __device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) 
         : "+f"(d0), "+f"(d1)
         : "f"(a0), "f"(a1));
 }
-__device__ __forceinline__ void fsub2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d0), "=f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -336,21 +327,6 @@ __device__ __forceinline__ float min3(float a, float b, float c) {
     float d;
     asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
-}
-// OR of `pred` over the two warps that hold the two halves (key columns
-// 0-63 and 64-127) of the same 32 query rows -- the only warps that exchange
-// data -- returned to both; also a barrier over those 64 threads (named
-// barrier `id`).  Every decision that leads to a later barrier of the pair is
-// taken from such a vote, so both warps always meet at the same barriers.
-__device__ __forceinline__ bool pair_any(int id, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id)
-        : "memory");
-    return r != 0;
 }
 // 4x4 transpose of 16-byte chunks over the four lanes of a quad: on entry
 // lane l of the quad holds chunks 0-3 of its own row; on exit c[k] is chunk l
@@ -382,7 +358,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
 }
 
 template <typename TO>
-__global__ void __maxnreg__(96)   // 5 warps share an SM sub-partition: 5 x 96 x 32 <= 16384
+__global__ void __maxnreg__(168)   // 3 warps share an SM sub-partition: 3 x 168 x 32 <= 16384
 k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ items, int n_work, int H,
              TO* __restrict__ out, int HD, float sl2, int* __restrict__ err) {
@@ -392,7 +368,6 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     __shared__ __align__(8) WsBars bars;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
-    __shared__ float s_red[2][2][2][kTile];   // [tile g][parity][half][row]: row maxima, then row sums
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -420,11 +395,11 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         for (int g = 0; g < 2; ++g) {
             mbar_init(&bars.s[g][0], 1);
             mbar_init(&bars.s[g][1], 1);
-            mbar_init(&bars.p[g][0], 8);
-            mbar_init(&bars.p[g][1], 8);
+            mbar_init(&bars.p[g][0], 4);
+            mbar_init(&bars.p[g][1], 4);
             mbar_init(&bars.o[g][0], 1);
             mbar_init(&bars.o[g][1], 1);
-            mbar_init(&bars.o_free[g], 8);
+            mbar_init(&bars.o_free[g], 4);
         }
         mbar_init(&bars.drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -597,13 +572,14 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         }
     } else if (warp < kMmaWarp) {
         // ---------------- softmax warpgroups ----------------
-        const int g = warp >> 3;                       // query tile
-        const int half = (warp >> 2) & 1;              // key columns 64*half .. 64*half+63
+        // One thread per query row (= TMEM lane) and all 128 key columns of a
+        // tile: a row's running maximum and sum live in one thread, so the
+        // warps of a tile never exchange data and never wait for each other.
+        const int g = warp >> 2;                       // query tile
         const int row = (warp & 3) * 32 + lane;        // row of the query tile (= TMEM lane)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tO = tmem + col_o(g) + lane_base + 32 * half;
+        const uint32_t tO = tmem + col_o(g) + lane_base;
         const bool pos = sl2 >= 0.f;
-        const int pair_id = 1 + g * 4 + (warp & 3);    // named barrier of this warp and its other half
         int s_cnt = 0;      // S tiles of this query tile consumed so far
         int o_cnt = 0;      // PV_g products of finished items
         // Wait for PV_g number n.  Two barriers keep each wait inside the
@@ -613,7 +589,6 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         // MMA order, and the S commit tracks every earlier MMA), so the
         // previous phase of barrier o[g][n & 1] has completed.
         auto o_wait = [&](int n) { return mbar_wait(&bars.o[g][n & 1], (n >> 1) & 1); };
-        int par = 0;
         int snum = 0;   // S tiles of the CTA's sequence before the current item (both query tiles)
         bool failed = false;
         int h_next = 0;
@@ -628,82 +603,87 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             if (g >= nq) continue;
             float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;
             for (int j = 0; j < T; ++j) {
-                const uint32_t tS = tmem + col_buf((s0 + nq * j + g) % 3) + lane_base + 64 * half;
-                // a wait that runs out marks the CTA aborted; the tile leaves
-                // its loop together at the next vote, so every barrier below
-                // is reached by all of its 8 warps
-                bool bad = !mbar_wait(&bars.s[g][s_cnt & 1], (s_cnt >> 1) & 1);
+                const uint32_t tS = tmem + col_buf((s0 + nq * j + g) % 3) + lane_base;
+                // a wait that runs out marks the CTA aborted; the warp leaves
+                // its loop (the decision is uniform over the warp)
+                const bool bad = !mbar_wait(&bars.s[g][s_cnt & 1], (s_cnt >> 1) & 1);
                 ++s_cnt;
-                tc_fence_after();
-                uint32_t r[64];
-                tmem_ld32(tS, r);
-                tmem_ld32(tS + 32, r + 32);
-                tmem_ld_wait();
-                float ma = pos ? -INFINITY : INFINITY, mb = ma;
-                if (pos) {
-#pragma unroll
-                    for (int i = 0; i < 64; i += 4) {
-                        ma = max3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                        mb = max3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                    }
-                    ma = fmaxf(ma, mb);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 64; i += 4) {
-                        ma = min3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                        mb = min3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                    }
-                    ma = fminf(ma, mb);
-                }
-                // This half's extreme goes to shared memory (parity double
-                // buffer: the slot written now was last read before the
-                // previous tile's vote).  The row maximum is needed only on the
-                // first tile of an item and when this tile's maximum exceeds
-                // the one in use by more than the threshold; otherwise P keeps
-                // the maximum in use (P <= 2^threshold) and no exchange is made.
-                s_red[g][par][half][row] = ma;
                 if (bad) atomicExch(&s_abort, 1);
-                const bool abort_seen = bad || *reinterpret_cast<volatile int*>(&s_abort) != 0;
-                const bool need = j == 0 || ma * sl2 > m_used + kRescaleThreshold;
-                if (pair_any(pair_id, need || abort_seen)) {
-                    if (pair_any(pair_id, abort_seen)) { failed = true; break; }
-                    const float other = s_red[g][par][half ^ 1][row];
-                    const float mt = (pos ? fmaxf(ma, other) : fminf(ma, other)) * sl2;
-                    if (j == 0) {
-                        m_used = mt;
+                if (__any_sync(0xffffffffu, bad || *reinterpret_cast<volatile int*>(&s_abort) != 0)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                // the row's extreme over the tile's 128 keys (max for a
+                // positive scale, min for a negative one)
+                float ma, mb, mc, md;
+                {
+                    uint32_t r[128];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, r + 32 * c);
+                    tmem_ld_wait();
+                    ma = mb = mc = md = pos ? -INFINITY : INFINITY;
+                    if (pos) {
+#pragma unroll
+                        for (int i = 0; i < 128; i += 8) {
+                            ma = max3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                            mb = max3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                            mc = max3(mc, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+                            md = max3(md, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                        }
+                        ma = fmaxf(fmaxf(ma, mb), fmaxf(mc, md));
                     } else {
-                        const bool up = mt > m_used + kRescaleThreshold;
-                        if (__any_sync(0xffffffffu, up)) {
-                            // O_g may be rescaled only after PV_g(j-1); no later
-                            // PV_g can have been issued (it needs this tile's P)
-                            if (!o_wait(o_cnt + j - 1)) {
-                                bad = true;
-                                atomicExch(&s_abort, 1);
-                            }
-                            tc_fence_after();
-                            const float alpha = up ? ex2(m_used - mt) : 1.f;
-                            if (up) m_used = mt;
-                            l0 *= alpha;
-                            l1 *= alpha;
+#pragma unroll
+                        for (int i = 0; i < 128; i += 8) {
+                            ma = min3(ma, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                            mb = min3(mb, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                            mc = min3(mc, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+                            md = min3(md, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                        }
+                        ma = fminf(fminf(ma, mb), fminf(mc, md));
+                    }
+                }
+                const float mt = ma * sl2;
+                if (j == 0) {
+                    m_used = mt;
+                } else {
+                    // the maximum in use is raised only when the tile's exceeds
+                    // it by more than the threshold (P <= 2^threshold otherwise)
+                    const bool up = mt > m_used + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, up)) {
+                        // O_g may be rescaled only after PV_g(j-1); no later PV_g
+                        // can have been issued (it needs this tile's P)
+                        if (!o_wait(o_cnt + j - 1)) atomicExch(&s_abort, 1);
+                        tc_fence_after();
+                        const float alpha = up ? ex2(m_used - mt) : 1.f;
+                        if (up) m_used = mt;
+                        l0 *= alpha;
+                        l1 *= alpha;
+#pragma unroll 1
+                        for (int c = 0; c < 2; ++c) {
                             uint32_t o[32];
-                            tmem_ld32(tO, o);
+                            tmem_ld32(tO + 32 * c, o);
                             tmem_ld_wait();
 #pragma unroll
                             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tmem_st32(tO, o);
-                            tmem_st_wait();
+                            tmem_st32(tO + 32 * c, o);
                         }
+                        tmem_st_wait();
                     }
                 }
-                par ^= 1;
-                // P = 2^(s*scale*log2e - m) as bf16 hi/lo over this half of S,
-                // 32 keys at a time (re-read from TMEM to keep registers low)
+                // P = 2^(s*scale*log2e - m) as bf16 hi/lo, 32 keys at a time
+                // (S re-read from TMEM; the next chunk's load is issued before
+                // the current chunk's arithmetic)
                 const float nm = -m_used;
-#pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t x[32], pk[32];
-                    tmem_ld32(tS + 32 * cc, x);
-                    tmem_ld_wait();
+                uint32_t xa[32], xb[32];
+                tmem_ld32(tS, xa);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t* x = (c & 1) ? xb : xa;
+                    uint32_t* xn = (c & 1) ? xa : xb;
+                    if (c + 1 < 4) tmem_ld32(tS + 32 * (c + 1), xn);
+                    uint32_t pk[32];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
                         float t0, t1;
@@ -721,9 +701,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                         pk[q] = hi;
                         pk[16 + q] = pack2_bf16(d0, d1);
                     }
-                    // keys 32c..32c+31 (c = 2*half + cc): P_hi in cols 32c..32c+15,
-                    // P_lo in cols 32c+16..32c+31
-                    tmem_st32(tS + 32 * cc, pk);
+                    // keys 32c..32c+31: P_hi in columns 32c..32c+15, P_lo in 32c+16..32c+31
+                    tmem_st32(tS + 32 * c, pk);
+                    if (c + 1 < 4) tmem_ld_wait();
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -731,43 +711,48 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 if (lane == 0) mbar_arrive(&bars.p[g][(o_cnt + j) & 1]);
             }
             if (failed) break;
-            // epilogue: O_g after the item's last product; row sum from both halves
-            bool bad = !o_wait(o_cnt + T - 1);
+            // epilogue: O_g after the item's last product
+            const bool bad = !o_wait(o_cnt + T - 1);
             o_cnt += T;
+            if (bad) atomicExch(&s_abort, 1);
+            if (__any_sync(0xffffffffu, bad)) { failed = true; break; }
             tc_fence_after();
-            uint32_t o[32];
+            uint32_t o[64];
             tmem_ld32(tO, o);
+            tmem_ld32(tO + 32, o + 32);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.o_free[g]);
-            s_red[g][par][half][row] = l0 + l1;
-            if (bad) atomicExch(&s_abort, 1);
-            if (pair_any(pair_id, bad || *reinterpret_cast<volatile int*>(&s_abort) != 0)) { failed = true; break; }
-            const float inv = 1.f / (l0 + l1 + s_red[g][par][half ^ 1][row]);
-            par ^= 1;
-            // rows of this lane's quad after the transpose: quad base + k
-            TO* op = out + static_cast<int64_t>(q0 + g * kTile + (row & ~3)) * HD + xh + 32 * half;
+            const float inv = 1.f / (l0 + l1);
+            // rows of this lane's quad after each transpose: quad base + k
+            TO* op = out + static_cast<int64_t>(q0 + g * kTile + (row & ~3)) * HD + xh;
             const int ql = lane & 3;
             if constexpr (sizeof(TO) == 2) {
-                uint4 c[4];
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    c[v] = make_uint4(
-                        pack2_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
-                        pack2_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
-                        pack2_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
-                        pack2_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
-                quad_transpose(c, lane);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD)[ql] = c[k];
-            } else {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {   // columns 16*hh .. 16*hh+15 of this half
+                for (int gg = 0; gg < 2; ++gg) {   // 16-byte chunks 4gg..4gg+3 (columns 32gg..32gg+31)
                     uint4 c[4];
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        const int e = 16 * hh + 4 * v;
+                        const int e = 32 * gg + 8 * v;
+                        c[v] = make_uint4(
+                            pack2_bf16(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv),
+                            pack2_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                            pack2_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                            pack2_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+                    }
+                    quad_transpose(c, lane);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD)[4 * gg + ql] = c[k];
+                }
+            } else {
+#pragma unroll
+                for (int gg = 0; gg < 4; ++gg) {   // 16-byte chunks 4gg..4gg+3 (columns 16gg..16gg+15)
+                    uint4 c[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int e = 16 * gg + 4 * v;
                         c[v] = make_uint4(__float_as_uint(__uint_as_float(o[e]) * inv),
                                           __float_as_uint(__uint_as_float(o[e + 1]) * inv),
                                           __float_as_uint(__uint_as_float(o[e + 2]) * inv),
@@ -776,7 +761,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     quad_transpose(c, lane);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD + 16 * hh)[ql] = c[k];
+                        reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD)[4 * gg + ql] = c[k];
                 }
             }
         }

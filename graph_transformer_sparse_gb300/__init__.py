@@ -22,7 +22,7 @@ from ._build import LIB, build
 
 __all__ = [
     "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
-    "gtattn_fwd_noalloc", "gtattn_csr_build", "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
+    "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_csr_build", "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
     "gtattn_csr_validate", "gtattn_status_string", "gtattn_profile_enable", "gtattn_profile_read",
     "sparse_mha", "GTATTN_F32", "GTATTN_BF16", "GTATTN_BF16_OUT_F32",
     "GTATTN_KERNEL_AUTO", "GTATTN_KERNEL_VECTOR", "GTATTN_KERNEL_GENERIC", "EXPORTED_SYMBOLS",
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "gtattn_status_string", "gtattn_last_error", "gtattn_csr_build", "gtattn_plan_destroy",
     "gtattn_plan_get_info", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
     "gtattn_coo_to_csr", "gtattn_csr_validate", "gtattn_profile_enable", "gtattn_profile_read",
-    "gtattn_fwd_noalloc",
+    "gtattn_fwd_noalloc", "gtattn_fwd_host",
 )
 KCAT_NAMES = ("bin", "rows", "combine", "softmax", "dense")
 
@@ -102,6 +102,7 @@ def load(path: str | None = None):
             "gtattn_coo_to_csr": ([vp, vp, i64, i64, vp, vp, vp], i32),
             "gtattn_csr_validate": ([vp, vp, i64, i64, vp], i32),
             "gtattn_fwd_noalloc": ([vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
+            "gtattn_fwd_host": ([vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
             "gtattn_profile_enable": ([i32], i32),
             "gtattn_profile_read": ([vp, i32], i32),
         }
@@ -135,6 +136,17 @@ def _ptr(x):
             raise ValueError("expected a contiguous tensor")
         return x.data_ptr() or None
     raise TypeError(f"cannot take a device pointer of {type(x)}")
+
+
+def _host_ptr(x):
+    """Pointer of a contiguous host (CPU) tensor, or None."""
+    if x is None:
+        return None
+    if getattr(x, "is_cuda", False):
+        raise ValueError("expected a host (CPU) tensor")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.data_ptr() or None
 
 
 def _stream(stream):
@@ -180,6 +192,16 @@ def gtattn_fwd_noalloc(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype
     _check(load().gtattn_fwd_noalloc(_ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(out),
                                      int(N), int(nnz), int(H), int(D), float(scale), int(dtype),
                                      _stream(stream)), "gtattn_fwd_noalloc")
+
+
+def gtattn_fwd_host(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, stream=None):
+    """gtattn_fwd on host (CPU, preferably pinned) tensors: copies in,
+    computes and copies the output back, overlapped, ordered on `stream`;
+    `out` is complete once `stream` has passed the call."""
+    _check(load().gtattn_fwd_host(_host_ptr(indptr), _host_ptr(indices), _host_ptr(Q), _host_ptr(K),
+                                  _host_ptr(V), _host_ptr(out),
+                                  int(N), int(nnz), int(H), int(D), float(scale), int(dtype),
+                                  _stream(stream)), "gtattn_fwd_host")
 
 
 def gtattn_fwd_plan(plan, indptr, indices, Q, K, V, out, H, D, scale, dtype, stream=None):

@@ -150,6 +150,31 @@ gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indices, const vo
                          int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
 
 /*
+ * gtattn_fwd_host -- gtattn_fwd on HOST buffers: the same operation, with
+ * the graph and features copied to the device and the output copied back
+ * inside the call, all ordered on `stream`.  The copies overlap the
+ * computation: K and V are copied first, then the rows are cut into chunks
+ * of about equal work whose indptr, indices and Q are copied while earlier
+ * chunks are computed, and whose output rows are copied back while later
+ * chunks are copied and computed (two library-owned copy streams per device).
+ * The pages define no host-buffer call: this one is a convenience of this
+ * library for callers whose data lives in host memory.
+ *   indptr, indices, Q, K, V: host memory, same layouts as gtattn_fwd; out:
+ *   host memory, written when `stream` reaches the end of the call.  Host
+ *   buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for the
+ *   copies to be asynchronous and at full speed; the caller keeps every host
+ *   buffer valid and unchanged until `stream` has passed the call.  indptr is
+ *   also read by the host during the call (chunk boundaries).
+ *   Device temporaries (about the size of the inputs plus the output) come
+ *   from the library's stream-ordered pool and return to it at the end.
+ * Errors: those of gtattn_fwd; BAD_CSR when indptr[0] != 0 or
+ * indptr[N] != nnz.
+ */
+gtattn_status gtattn_fwd_host(const int32_t* indptr, const int32_t* indices, const void* Q,
+                              const void* K, const void* V, void* out, int64_t N, int64_t nnz,
+                              int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
+
+/*
  * gtattn_fwd_plan -- as gtattn_fwd with a prebuilt plan: no binning per
  * call, and complete blocks (if the plan found any) go to the dense
  * tensor-core kernel when dtype is bf16 and D == 64.  indptr/indices must be

@@ -739,8 +739,15 @@ bool choose_row_kernel(int H, int D, gtattn_dtype dt, const void* Q, const void*
                          reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
     if (force != GTATTN_KERNEL_GENERIC && (al & 15u) == 0) {
         const int per_vec = 16 / esz;
-        const int max_vpl = esz == 2 ? 2 : 4;
-        for (int vpl = 1; vpl <= max_vpl; vpl <<= 1) {
+        // Preference: two 16-byte vectors per lane, then one, then four
+        // (fp32 only).  Two vectors put twice as many rows in a warp as one
+        // (R-MAT, 4 x 32 bf16: 8 lanes and 4 rows per warp instead of 16 and
+        // 2), halving the per-row work per warp instruction on graphs of
+        // mostly short rows (R-MAT 1.48 -> 1.25 ms); four need too many
+        // registers for the K/V pipeline in bf16 (1.52 ms).
+        static constexpr int kOrder[3] = {2, 1, 4};
+        for (int vpl : kOrder) {
+            if (esz == 2 && vpl > 2) continue;
             const int E = vpl * per_vec;
             if (D % E != 0) continue;
             const int lph = D / E;

@@ -355,8 +355,8 @@ extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* 
     }
     // (2) edge softmax: probs
     if (st == GTATTN_OK && nnz > 0) {
-        ProfScope ps(GTATTN_KCAT_SOFTMAX, 2, stream);
-        st = launch_edge_softmax(indptr, (int)N, H, o.long_row_min, sc.lists, lg, pr, stream);
+        ProfScope ps(GTATTN_KCAT_SOFTMAX, 4, stream);
+        st = launch_edge_softmax(indptr, (int)N, H, sc.lists, sc.part, lg, pr, stream);
     }
     // (3) SpMM: out
     if (st == GTATTN_OK) {

@@ -619,110 +619,101 @@ k_combine(RowParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// unfused edge softmax: warp per ordinary row, block per split row
+// unfused edge softmax
 // ---------------------------------------------------------------------------
-// Online (max, sum) of exponentials, merged pairwise.
-__device__ __forceinline__ void ms_add(float& m, float& s, float x) {
-    if (x > m) {
-        s = s * expf(m - x) + 1.f;
-        m = x;
-    } else {
-        s += expf(x - m);
-    }
-}
-__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
-    if (m2 > m) {
-        s = s * expf(m - m2) + s2;
-        m = m2;
-    } else if (m2 != -INFINITY) {
-        s += s2 * expf(m2 - m);
-    }
-}
-
-// Ordinary rows, H dividing 32: a warp per row; lane l walks the row's
-// logits in memory order (entry-major, head-minor), so its head is l % H and
-// the per-head statistics combine over lanes H, 2H, ... apart.
+// p[e,h] = exp(l[e,h] - M_h) / S_h over each row's entries, with accurate
+// expf, in three walks per element: the maximum, the sum, the write.
+//
+// Ordinary rows (the bucketed row list, rows of equal degree side by side):
+// a thread per (row, head), so neighbouring threads have the same amount of
+// work; the H threads of a row read its logits together (entry-major,
+// head-minor), and the second and third walks hit in L1.
 __global__ void __launch_bounds__(256)
-k_softmax_rows(const int* __restrict__ indptr, int N, int H, int long_min,
-               const float* __restrict__ logits, float* __restrict__ probs) {
-    const int lane = threadIdx.x & 31;
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < N; i += warps) {
-        const int beg = indptr[i], end = indptr[i + 1];
-        const int deg = end - beg;
-        if (deg == 0 || deg > long_min) continue;
-        const int64_t base = (int64_t)beg * H;
-        const int total = deg * H;
-        float m = -INFINITY, sum = 0.f;
-        for (int t = lane; t < total; t += 32) ms_add(m, sum, logits[base + t]);
-        for (int o = H; o < 32; o <<= 1) {
-            const float m2 = __shfl_xor_sync(kFull, m, o);
-            const float s2 = __shfl_xor_sync(kFull, sum, o);
-            ms_merge(m, sum, m2, s2);
-        }
+k_softmax_short(const int* __restrict__ indptr, const int* __restrict__ hdr, const int* __restrict__ rows,
+                int H, const float* __restrict__ logits, float* __restrict__ probs) {
+    int n_rows = 0;   // length of the bucketed list (the buckets are contiguous)
+    for (int b = 0; b < kNumBuckets; ++b)
+        n_rows = max(n_rows, hdr[HdrLayout::kOffset + b] + hdr[HdrLayout::kCount + b]);
+    const int64_t total = (int64_t)n_rows * H;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int pos = (int)(t / H), h = (int)(t - (int64_t)pos * H);
+        const int row = rows[pos];
+        const int beg = indptr[row], deg = indptr[row + 1] - beg;
+        const float* lr = logits + (int64_t)beg * H + h;
+        float* pr = probs + (int64_t)beg * H + h;
+        float m = -INFINITY;
+        for (int e = 0; e < deg; ++e) m = fmaxf(m, lr[(int64_t)e * H]);
+        float sum = 0.f;
+        for (int e = 0; e < deg; ++e) sum += expf(lr[(int64_t)e * H] - m);
         const float inv = 1.f / sum;
-        for (int t = lane; t < total; t += 32) probs[base + t] = expf(logits[base + t] - m) * inv;
+        for (int e = 0; e < deg; ++e) pr[(int64_t)e * H] = expf(lr[(int64_t)e * H] - m) * inv;
     }
 }
 
-// Ordinary rows, any H: a warp per row, heads one after another.
+// Split rows, in their chunks (a thread per (chunk, head)): step 1, each
+// chunk's maximum M_c and sum S_c = sum exp(l - M_c) into the partials.
 __global__ void __launch_bounds__(256)
-k_softmax_rows_anyh(const int* __restrict__ indptr, int N, int H, int long_min,
-                    const float* __restrict__ logits, float* __restrict__ probs) {
-    const int lane = threadIdx.x & 31;
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < N; i += warps) {
-        const int beg = indptr[i], end = indptr[i + 1];
-        const int deg = end - beg;
-        if (deg == 0 || deg > long_min) continue;
-        for (int h = 0; h < H; ++h) {
-            float m = -INFINITY, sum = 0.f;
-            for (int e = beg + lane; e < end; e += 32) ms_add(m, sum, logits[(int64_t)e * H + h]);
-            for (int o = 16; o > 0; o >>= 1) {
-                const float m2 = __shfl_xor_sync(kFull, m, o);
-                const float s2 = __shfl_xor_sync(kFull, sum, o);
-                ms_merge(m, sum, m2, s2);
-            }
-            const float inv = 1.f / sum;
-            for (int e = beg + lane; e < end; e += 32)
-                probs[(int64_t)e * H + h] = expf(logits[(int64_t)e * H + h] - m) * inv;
-        }
+k_softmax_chunk_stats(const int* __restrict__ indptr, const int* __restrict__ hdr, const int2* __restrict__ chunks,
+                      int chunk_edges, int H, const float* __restrict__ logits, Partials part) {
+    const int64_t total = (int64_t)hdr[HdrLayout::kChunks] * H;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(t / H), h = (int)(t - (int64_t)c * H);
+        const int2 ck = chunks[c];
+        const int beg = ck.y, n = min(ck.y + chunk_edges, indptr[ck.x + 1]) - ck.y;
+        const float* lr = logits + (int64_t)beg * H + h;
+        float m = -INFINITY;
+        for (int e = 0; e < n; ++e) m = fmaxf(m, lr[(int64_t)e * H]);
+        float sum = 0.f;
+        for (int e = 0; e < n; ++e) sum += expf(lr[(int64_t)e * H] - m);
+        part.m[t] = m;
+        part.s[t] = sum;
     }
 }
 
-// Split rows: a block per row, threads walk the row's logits in memory
-// order; per-head statistics go through shared memory.
+// Step 2, a thread per (split row, head): the row's statistics from its
+// chunks' (M = max M_c, S = sum S_c exp(M_c - M)), stored as (M, 1/S) in the
+// slot of the row's first chunk.
 __global__ void __launch_bounds__(256)
-k_softmax_long(const int* __restrict__ indptr, const int* __restrict__ hdr, const int2* __restrict__ longs,
-               int H, const float* __restrict__ logits, float* __restrict__ probs) {
-    __shared__ float sm_m[256], sm_s[256];
-    __shared__ float head_m[kGenMaxH], head_inv[kGenMaxH];
-    const int n_long = hdr[HdrLayout::kLong];
-    const int per = (256 / H) * H;            // threads in use: a multiple of H
-    for (int li = blockIdx.x; li < n_long; li += gridDim.x) {
-        const int row = longs[li].x;
-        const int beg = indptr[row], end = indptr[row + 1];
-        const int64_t base = (int64_t)beg * H;
-        const int total = (end - beg) * H;
-        float m = -INFINITY, sum = 0.f;
-        if (threadIdx.x < per)
-            for (int t = threadIdx.x; t < total; t += per) ms_add(m, sum, logits[base + t]);
-        sm_m[threadIdx.x] = m;
-        sm_s[threadIdx.x] = sum;
-        __syncthreads();
-        for (int h = threadIdx.x; h < H; h += blockDim.x) {   // thread h merges the threads of head h
-            float hm = -INFINITY, hs = 0.f;
-            for (int k = h; k < per; k += H) ms_merge(hm, hs, sm_m[k], sm_s[k]);
-            head_m[h] = hm;
-            head_inv[h] = 1.f / hs;
+k_softmax_long_merge(const int* __restrict__ indptr, const int* __restrict__ hdr, const int2* __restrict__ longs,
+                     int chunk_edges, int H, Partials part) {
+    const int64_t total = (int64_t)hdr[HdrLayout::kLong] * H;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int li = (int)(t / H), h = (int)(t - (int64_t)li * H);
+        const int2 lg = longs[li];
+        const int deg = indptr[lg.x + 1] - indptr[lg.x];
+        const int nch = (deg + chunk_edges - 1) / chunk_edges;
+        float M = -INFINITY;
+        for (int c = 0; c < nch; ++c) M = fmaxf(M, part.m[(int64_t)(lg.y + c) * H + h]);
+        float S = 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const int64_t k = (int64_t)(lg.y + c) * H + h;
+            S += part.s[k] * expf(part.m[k] - M);
         }
-        __syncthreads();
-        if (threadIdx.x < per) {
-            const int h = threadIdx.x % H;
-            const float hm = head_m[h], hi = head_inv[h];
-            for (int t = threadIdx.x; t < total; t += per) probs[base + t] = expf(logits[base + t] - hm) * hi;
-        }
-        __syncthreads();
+        part.m[(int64_t)lg.y * H + h] = M;
+        part.s[(int64_t)lg.y * H + h] = 1.f / S;
+    }
+}
+
+// Step 3, a thread per (chunk, head): p = exp(l - M) / S with the row's
+// (M, 1/S) from its first chunk (a split row's chunks are consecutive).
+__global__ void __launch_bounds__(256)
+k_softmax_chunk_write(const int* __restrict__ indptr, const int* __restrict__ hdr, const int2* __restrict__ chunks,
+                      int chunk_edges, int H, const float* __restrict__ logits, float* __restrict__ probs,
+                      Partials part) {
+    const int64_t total = (int64_t)hdr[HdrLayout::kChunks] * H;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(t / H), h = (int)(t - (int64_t)c * H);
+        const int2 ck = chunks[c];
+        const int beg = ck.y, n = min(ck.y + chunk_edges, indptr[ck.x + 1]) - ck.y;
+        const int c0 = c - (beg - indptr[ck.x]) / chunk_edges;
+        const float M = part.m[(int64_t)c0 * H + h], inv = part.s[(int64_t)c0 * H + h];
+        const float* lr = logits + (int64_t)beg * H + h;
+        float* pr = probs + (int64_t)beg * H + h;
+        for (int e = 0; e < n; ++e) pr[(int64_t)e * H] = expf(lr[(int64_t)e * H] - M) * inv;
     }
 }
 
@@ -842,18 +833,16 @@ gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cud
     return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
 }
 
-gtattn_status launch_edge_softmax(const int* indptr, int N, int H, int long_min, const TaskLists& L,
+gtattn_status launch_edge_softmax(const int* indptr, int N, int H, const TaskLists& L, const Partials& part,
                                   const float* logits, float* probs, cudaStream_t s) {
     if (N == 0) return GTATTN_OK;
-    if (H > kGenMaxH) return GTATTN_ERR_UNSUPPORTED;
-    const int lm = long_min < 0 ? 0 : long_min;   // long_min -1: every non-empty row is split
-    if (32 % H == 0)
-        k_softmax_rows<<<grid_persistent(k_softmax_rows, 256, 0), 256, 0, s>>>(indptr, N, H, lm, logits, probs);
-    else
-        k_softmax_rows_anyh<<<grid_persistent(k_softmax_rows_anyh, 256, 0), 256, 0, s>>>(indptr, N, H, lm,
-                                                                                      logits, probs);
-    k_softmax_long<<<grid_persistent(k_softmax_long, 256, 0), 256, 0, s>>>(indptr, L.hdr, L.longs, H,
-                                                                            logits, probs);
+    k_softmax_short<<<grid_persistent(k_softmax_short, 256, 0), 256, 0, s>>>(indptr, L.hdr, L.rows, H, logits, probs);
+    k_softmax_chunk_stats<<<grid_persistent(k_softmax_chunk_stats, 256, 0), 256, 0, s>>>(
+        indptr, L.hdr, L.chunks, L.chunk_edges, H, logits, part);
+    k_softmax_long_merge<<<grid_persistent(k_softmax_long_merge, 256, 0), 256, 0, s>>>(
+        indptr, L.hdr, L.longs, L.chunk_edges, H, part);
+    k_softmax_chunk_write<<<grid_persistent(k_softmax_chunk_write, 256, 0), 256, 0, s>>>(
+        indptr, L.hdr, L.chunks, L.chunk_edges, H, logits, probs, part);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
 }

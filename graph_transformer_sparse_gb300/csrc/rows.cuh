@@ -43,7 +43,7 @@ gtattn_status launch_rows(Mode mode, gtattn_dtype dt, const RowChoice& c, const 
 gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cudaStream_t s);
 
 // Unfused edge softmax: probs[e,h] from logits[e,h] over each row's entries.
-gtattn_status launch_edge_softmax(const int* indptr, int N, int H, int long_min, const TaskLists& L,
+gtattn_status launch_edge_softmax(const int* indptr, int N, int H, const TaskLists& L, const Partials& part,
                                   const float* logits, float* probs, cudaStream_t s);
 
 }  // namespace gt

@@ -576,13 +576,21 @@ k_rows_generic(RowParams p) {
 // ---------------------------------------------------------------------------
 // combine split-row partials: one block per split row
 // ---------------------------------------------------------------------------
+// The row's chunks are spread over groups of threads (a group per head for
+// the statistics, per output element for the sums); group partials meet in
+// shared memory.  A hub row of hundreds of chunks then costs a few chunk
+// loads per thread instead of a serial walk over all of them.
+constexpr int kCombThreads = 512;
+
 template <typename TO, int MODE>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kCombThreads)
 k_combine(RowParams p) {
-    __shared__ float sM[kMaxHD];
-    __shared__ float sS[kMaxHD];
+    __shared__ float sM[kGenMaxH];
+    __shared__ float sS[kGenMaxH];
+    __shared__ float red[kCombThreads];
     const int n_long = p.lists.hdr[HdrLayout::kLong];
     const int H = p.H, D = p.D, HD = p.HD;
+    const int t = threadIdx.x;
     TO* __restrict__ O = static_cast<TO*>(p.out);
     for (int li = blockIdx.x; li < n_long; li += gridDim.x) {
         const int2 lr = p.lists.longs[li];
@@ -590,29 +598,71 @@ k_combine(RowParams p) {
         const int deg = p.indptr[row + 1] - p.indptr[row];
         const int nch = (deg + p.lists.chunk_edges - 1) / p.lists.chunk_edges;
         if (MODE == kFused) {
-            for (int h = threadIdx.x; h < H; h += blockDim.x) {
+            // per head: M = max_c m_c, S = sum_c s_c 2^(m_c - M)
+            const int G = kCombThreads / H;   // H <= 256: at least two groups
+            const int h = t % H, g = t / H;
+            float m = -INFINITY;
+            if (g < G)
+                for (int c = g; c < nch; c += G) m = fmaxf(m, p.part.m[(int64_t)(c0 + c) * H + h]);
+            red[t] = m;
+            __syncthreads();
+            if (t < H) {
                 float M = -INFINITY;
-                for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part.m[(int64_t)(c0 + c) * H + h]);
+                for (int k = 0; k < G; ++k) M = fmaxf(M, red[k * H + t]);
+                sM[t] = M;
+            }
+            __syncthreads();
+            float sum = 0.f;
+            if (g < G) {
+                const float M = sM[h];
+                for (int c = g; c < nch; c += G) {
+                    const int64_t k = (int64_t)(c0 + c) * H + h;
+                    sum += p.part.s[k] * ex2(p.part.m[k] - M);
+                }
+            }
+            __syncthreads();   // everyone has read red[] for M
+            red[t] = sum;
+            __syncthreads();
+            if (t < H) {
                 float S = 0.f;
-                for (int c = 0; c < nch; ++c)
-                    S += p.part.s[(int64_t)(c0 + c) * H + h] * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M);
-                sM[h] = M;
-                sS[h] = S;
+                for (int k = 0; k < G; ++k) S += red[k * H + t];
+                sS[t] = S;
             }
             __syncthreads();
         }
-        for (int el = threadIdx.x; el < HD; el += blockDim.x) {
+        const int Ge = kCombThreads / HD;   // element groups over the chunks
+        if (Ge >= 2) {
+            const int el = t % HD, g = t / HD;
+            const int h = el / D;
             float v = 0.f;
-            if (MODE == kFused) {
-                const int h = el / D;
-                const float M = sM[h];
-                for (int c = 0; c < nch; ++c)
-                    v += p.part.acc[(int64_t)(c0 + c) * HD + el] * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M);
-                v = v / sS[h];
-            } else {
-                for (int c = 0; c < nch; ++c) v += p.part.acc[(int64_t)(c0 + c) * HD + el];
+            if (g < Ge) {
+                const float M = MODE == kFused ? sM[h] : 0.f;
+                for (int c = g; c < nch; c += Ge) {
+                    const float a = p.part.acc[(int64_t)(c0 + c) * HD + el];
+                    v += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M) : a;
+                }
             }
-            store_elem(O, (int64_t)row * HD + el, v);
+            red[t] = v;
+            __syncthreads();
+            if (t < HD) {
+                float tot = 0.f;
+                for (int k = 0; k < Ge; ++k) tot += red[k * HD + t];
+                if (MODE == kFused) tot /= sS[h];
+                store_elem(O, (int64_t)row * HD + t, tot);
+            }
+        } else {
+            for (int el = t; el < HD; el += kCombThreads) {
+                const int h = el / D;
+                const float M = MODE == kFused ? sM[h] : 0.f;
+                float v = 0.f;
+#pragma unroll 4
+                for (int c = 0; c < nch; ++c) {
+                    const float a = p.part.acc[(int64_t)(c0 + c) * HD + el];
+                    v += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M) : a;
+                }
+                if (MODE == kFused) v /= sS[h];
+                store_elem(O, (int64_t)row * HD + el, v);
+            }
         }
         __syncthreads();
     }
@@ -822,7 +872,7 @@ gtattn_status launch_rows(Mode mode, gtattn_dtype dt, const RowChoice& c, const 
 
 gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cudaStream_t s) {
     auto go = [&](auto kernel) {
-        kernel<<<grid_persistent(kernel, 256, 0), 256, 0, s>>>(p);
+        kernel<<<grid_persistent(kernel, kCombThreads, 0), kCombThreads, 0, s>>>(p);
         return cudaGetLastError();
     };
     cudaError_t e;

@@ -99,6 +99,32 @@ def test_small_workloads_all_paths(name, path, kw):
         assert np.all(err <= 1e-5 * cond + 1e-6), float((err - 1e-5 * cond).max())
 
 
+def test_probs_split_row_boundaries():
+    # degrees on both sides of the 256-entry split threshold and of chunk
+    # boundaries (the unfused softmax merges chunk statistics per split row)
+    rng = np.random.default_rng(21)
+    degs = [0, 1, 2, 255, 256, 257, 511, 512, 513, 768, 2000, 3]
+    n = 2400
+    indptr = np.zeros(n + 1, np.int64)
+    deg = np.zeros(n, np.int64)
+    deg[: len(degs)] = degs
+    deg[len(degs):] = rng.integers(0, 6, n - len(degs))
+    np.cumsum(deg, out=indptr[1:])
+    indices = rng.integers(0, n, int(indptr[-1])).astype(np.int32)
+    Q, K, V = (rng.standard_normal((n, 4, 16)) for _ in range(3))
+    Q *= 2.0   # sharper distributions: chunk maxima differ
+    w = _mk(indptr, indices, Q, K, V, "f32")
+    ref = oracle_rows(w, want_probs=True)
+    got, _, pr = run(w, to_device(w), "probs")
+    check_out(w, got, ref["out"])
+    assert_close(pr, ref["probs"], w.dtype, "probs", PROB_TOL)
+    # each stored row's probabilities sum to 1 per head
+    for i in range(len(degs)):
+        if degs[i]:
+            s = pr[indptr[i]:indptr[i + 1]].astype(np.float64).sum(axis=0)
+            assert np.allclose(s, 1.0, atol=1e-5), (i, s)
+
+
 @pytest.mark.parametrize("name", ["tiny_random", "molecules"])
 def test_full_small_configs_exact_oracle(name):
     # these two are small enough for the oracle at full size

@@ -574,17 +574,20 @@ k_rows_generic(RowParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// combine split-row partials: one block per split row
+// combine split-row partials
 // ---------------------------------------------------------------------------
-// The row's chunks are spread over groups of threads (a group per head for
-// the statistics, per output element for the sums); group partials meet in
-// shared memory.  A hub row of hundreds of chunks then costs a few chunk
-// loads per thread instead of a serial walk over all of them.
+// Phase 1, a block per split row of many chunks: the row's chunks are spread
+// over groups of threads (a group per head for the statistics, per output
+// element for the sums) whose partials meet in shared memory, so a hub row
+// of hundreds of chunks costs a few chunk loads per thread.  Phase 2, a warp
+// per split row of at most kWarpCombineMax chunks (when H divides 32; else
+// phase 1 takes every split row).
 constexpr int kCombThreads = 512;
+constexpr int kWarpCombineMax = 32;   // split rows up to this many chunks: a warp each (phase 2)
 
 template <typename TO, int MODE>
 __global__ void __launch_bounds__(kCombThreads)
-k_combine(RowParams p) {
+k_combine(RowParams p, int warp_rows) {
     __shared__ float sM[kGenMaxH];
     __shared__ float sS[kGenMaxH];
     __shared__ float red[kCombThreads];
@@ -597,6 +600,7 @@ k_combine(RowParams p) {
         const int row = lr.x, c0 = lr.y;
         const int deg = p.indptr[row + 1] - p.indptr[row];
         const int nch = (deg + p.lists.chunk_edges - 1) / p.lists.chunk_edges;
+        if (warp_rows && nch <= kWarpCombineMax) continue;   // done by a warp in phase 2
         if (MODE == kFused) {
             // per head: M = max_c m_c, S = sum_c s_c 2^(m_c - M)
             const int G = kCombThreads / H;   // H <= 256: at least two groups
@@ -637,10 +641,22 @@ k_combine(RowParams p) {
             float v = 0.f;
             if (g < Ge) {
                 const float M = MODE == kFused ? sM[h] : 0.f;
-                for (int c = g; c < nch; c += Ge) {
-                    const float a = p.part.acc[(int64_t)(c0 + c) * HD + el];
-                    v += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M) : a;
+                // four independent partial sums keep four chunks' loads in flight
+                float v4[4] = {0.f, 0.f, 0.f, 0.f};
+                int c = g;
+                for (; c + 3 * Ge < nch; c += 4 * Ge) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int cu = c + u * Ge;
+                        const float a = p.part.acc[(int64_t)(c0 + cu) * HD + el];
+                        v4[u] += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + cu) * H + h] - M) : a;
+                    }
                 }
+                for (; c < nch; c += Ge) {
+                    const float a = p.part.acc[(int64_t)(c0 + c) * HD + el];
+                    v4[0] += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M) : a;
+                }
+                v = (v4[0] + v4[1]) + (v4[2] + v4[3]);
             }
             red[t] = v;
             __syncthreads();
@@ -666,7 +682,64 @@ k_combine(RowParams p) {
         }
         __syncthreads();
     }
+    // phase 2: rows of at most kWarpCombineMax chunks (most of them), a warp
+    // per row: lanes over (chunk, head) pairs for the statistics (H divides
+    // 32), over output elements for the sums
+    if (warp_rows) {
+        const int lane = t & 31;
+        const int warps = gridDim.x * (blockDim.x >> 5);
+        for (int li = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); li < n_long; li += warps) {
+            const int2 lr = p.lists.longs[li];
+            const int row = lr.x, c0 = lr.y;
+            const int deg = p.indptr[row + 1] - p.indptr[row];
+            const int nch = (deg + p.lists.chunk_edges - 1) / p.lists.chunk_edges;
+            if (nch > kWarpCombineMax) continue;
+            // lane l: head l % H, chunks l / H, l / H + 32 / H, ...; lanes H
+            // apart combine, so lane h < H ends with head h's (M, S)
+            float M = -INFINITY, S = 0.f;
+            if (MODE == kFused) {
+                const int h = lane % H, step = 32 / H;
+                for (int c = lane / H; c < nch; c += step) M = fmaxf(M, p.part.m[(int64_t)(c0 + c) * H + h]);
+                for (int o = H; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+                for (int c = lane / H; c < nch; c += step) {
+                    const int64_t k = (int64_t)(c0 + c) * H + h;
+                    S += p.part.s[k] * ex2(p.part.m[k] - M);
+                }
+                for (int o = H; o < 32; o <<= 1) S += __shfl_xor_sync(kFull, S, o);
+            }
+            for (int el0 = 0; el0 < HD; el0 += 32) {
+                const int el = el0 + lane;
+                const int h = min(el, HD - 1) / D;
+                const float Mh = __shfl_sync(kFull, M, h);
+                const float Sh = __shfl_sync(kFull, S, h);
+                if (el < HD) {
+                    // four independent partial sums keep four chunks' loads in flight
+                    float v4[4] = {0.f, 0.f, 0.f, 0.f};
+                    int c = 0;
+                    for (; c + 3 < nch; c += 4) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float a = p.part.acc[(int64_t)(c0 + c + u) * HD + el];
+                            v4[u] += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c + u) * H + h] - Mh) : a;
+                        }
+                    }
+                    for (; c < nch; ++c) {
+                        const float a = p.part.acc[(int64_t)(c0 + c) * HD + el];
+                        v4[0] += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - Mh) : a;
+                    }
+                    float v = (v4[0] + v4[1]) + (v4[2] + v4[3]);
+                    if (MODE == kFused) v /= Sh;
+                    store_elem(O, (int64_t)row * HD + el, v);
+                }
+            }
+        }
+    }
 }
+
+// (rows of few chunks: phase 2 of k_combine)
+// row: lanes over (chunk, head) pairs for the statistics, over output
+// elements for the sums.  Needs H to divide 32; larger rows and other head
+// counts go to k_combine.
 
 // ---------------------------------------------------------------------------
 // unfused edge softmax
@@ -871,8 +944,10 @@ gtattn_status launch_rows(Mode mode, gtattn_dtype dt, const RowChoice& c, const 
 }
 
 gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cudaStream_t s) {
+    // rows of few chunks a warp each (when H divides 32), the others a block each
+    const int warp_rows = (32 % p.H == 0) ? 1 : 0;
     auto go = [&](auto kernel) {
-        kernel<<<grid_persistent(kernel, kCombThreads, 0), kCombThreads, 0, s>>>(p);
+        kernel<<<grid_persistent(kernel, kCombThreads, 0), kCombThreads, 0, s>>>(p, warp_rows);
         return cudaGetLastError();
     };
     cudaError_t e;

@@ -33,7 +33,10 @@ namespace gt {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-enum SegKind { kSegChunk = 0, kSegRows = 1 };
+// kSegCopy: rows of exactly one entry, whose output is that neighbour's V
+// row (the softmax of one score is 1), taken by the fused kernel without
+// reading q or k.
+enum SegKind { kSegChunk = 0, kSegRows = 1, kSegCopy = 2 };
 
 struct Seg {
     int first_task;
@@ -47,7 +50,8 @@ constexpr int kMaxSegs = kNumBuckets + 2;
 
 // Builds the task table of a launch in shared memory (one warp).
 // P = edge slots per warp; U = edges per slot per loop iteration.
-__device__ void build_segments(const TaskLists& L, int P, int U, Seg* segs, int* nseg, int* total) {
+__device__ void build_segments(const TaskLists& L, int P, int U, Seg* segs, int* nseg, int* total,
+                               bool copy_deg1 = false) {
     __shared__ int h[HdrLayout::kWords];
     for (int k = threadIdx.x; k < HdrLayout::kWords; k += blockDim.x) h[k] = L.hdr[k];
     __syncthreads();
@@ -59,6 +63,11 @@ __device__ void build_segments(const TaskLists& L, int P, int U, Seg* segs, int*
             int cnt = h[HdrLayout::kCount + b];
             if (cnt == 0) continue;
             int lo = bucket_lo(b);
+            if (copy_deg1 && lo == 1 && bucket_lo(b + 1) == 2) {   // the degree-1 bucket
+                segs[k++] = Seg{t, h[HdrLayout::kOffset + b], cnt, P, 1, kSegCopy};
+                t += (cnt + P - 1) / P;
+                continue;
+            }
             int need = (lo + U - 1) / U;          // slots to cover the row in one iteration
             int S = 1;
             while (S < need && S < P) S <<= 1;
@@ -199,7 +208,7 @@ k_rows_vec(RowParams p) {
     __shared__ int s_nseg, s_total;
     const int G = p.G;
     const int P = 32 / G;
-    build_segments(p.lists, P, U, segs, &s_nseg, &s_total);
+    build_segments(p.lists, P, U, segs, &s_nseg, &s_total, MODE == kFused);
 
     const int lane = threadIdx.x & 31;
     const int grp = lane / G;
@@ -249,6 +258,19 @@ k_rows_vec(RowParams p) {
         const int tn = t + warps_total;
         if (tn < s_total) load_meta(tn, cur.seg, nxt);
         const Seg sg = segs[cur.seg];
+        if (MODE == kFused && sg.kind == kSegCopy) {   // uniform over the warp (one task)
+            // a row of one entry: its softmax weight is 1, out = V[j]
+            if (cur.valid) {
+                const int j = __ldg(p.indices + cur.beg);
+                F fv;
+                fv.load(V + (int64_t)j * HD + lane_off);
+                float x[E];
+#pragma unroll
+                for (int e = 0; e < E; ++e) x[e] = fv.get(e);
+                store_frag<TO, E>(O + (int64_t)cur.row * HD + lane_off, x);
+            }
+            continue;
+        }
         const int S = sg.S;
         const int r = grp / S;
         const int sl = grp - r * S;

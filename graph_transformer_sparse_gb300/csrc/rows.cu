@@ -175,16 +175,18 @@ __device__ __forceinline__ void store_frag(T* p, const float* x) {
 // ---------------------------------------------------------------------------
 // Tuning knobs (compile time): edges gathered per lane group per loop
 // iteration is GT_ROWS_UNROLL / VPL; GT_ROWS_MIN_BLOCKS bounds registers so
-// that many 256-thread blocks fit on an SM.
+// that many blocks of kRowThreads fit on an SM (the kernel is latency-bound:
+// more resident warps hide more of the gathers' latency).
 #ifndef GT_ROWS_UNROLL
 #define GT_ROWS_UNROLL 2
 #endif
 #ifndef GT_ROWS_MIN_BLOCKS1
-#define GT_ROWS_MIN_BLOCKS1 3   // one 16-byte vector per lane
+#define GT_ROWS_MIN_BLOCKS1 6   // one 16-byte vector per lane (85 registers)
 #endif
 #ifndef GT_ROWS_MIN_BLOCKS2
-#define GT_ROWS_MIN_BLOCKS2 3   // two or more vectors per lane
+#define GT_ROWS_MIN_BLOCKS2 7   // two vectors per lane: 72 registers, 28 warps per SM
 #endif
+constexpr int kRowThreads = 128;
 
 // Where a task's rows and edges are: one lane group's share of a task.
 struct TaskMeta {
@@ -193,17 +195,18 @@ struct TaskMeta {
     bool valid;
 };
 
-// Blocks per SM the register budget allows: lanes holding 16 values per
-// operand (two 16-byte vectors) get more registers than one-vector lanes, and
-// fp32 lanes holding four vectors (16 values) two blocks' worth, so that their
-// operands and next-iteration copies stay out of local memory.
+// Blocks of kRowThreads per SM the register budget allows.  Two vectors
+// per lane at 72 registers (28 warps) beat 79 registers without spills (24
+// warps) by 2-3 % on R-MAT despite a few spilled bytes; fp32 lanes holding
+// four vectors (16 values) get 4 blocks' worth so that their operands and
+// next-iteration copies stay out of local memory.
 template <typename T, int VPL>
 constexpr int rows_min_blocks() {
-    return VPL == 1 ? GT_ROWS_MIN_BLOCKS1 : VPL == 2 ? GT_ROWS_MIN_BLOCKS2 : 2;
+    return VPL == 1 ? GT_ROWS_MIN_BLOCKS1 : VPL == 2 ? GT_ROWS_MIN_BLOCKS2 : 4;
 }
 
 template <typename T, typename TO, int VPL, int MODE>
-__global__ void __launch_bounds__(256, rows_min_blocks<T, VPL>())
+__global__ void __launch_bounds__(kRowThreads, rows_min_blocks<T, VPL>())
 k_rows_vec(RowParams p) {
     using F = Frag<T, VPL>;
     constexpr int E = F::E;
@@ -922,7 +925,7 @@ static int grid_persistent(K kernel, int threads, size_t smem) {
 template <typename T, typename TO, int MODE>
 static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
     auto go = [&](auto kernel) {
-        kernel<<<grid_persistent(kernel, 256, 0), 256, 0, s>>>(p);
+        kernel<<<grid_persistent(kernel, kRowThreads, 0), kRowThreads, 0, s>>>(p);
         return cudaGetLastError();
     };
     cudaError_t e;

@@ -464,14 +464,15 @@ k_rows_vec(RowParams p) {
 // ---------------------------------------------------------------------------
 constexpr int kGenWarps = 4;
 constexpr int kGenMaxH = 256;
-constexpr int kGenK = kMaxHD / 32;   // elements per lane
 
-template <typename T, typename TO, int MODE>
+// KPL: elements of the feature row per lane (ceil(H*D/32) rounded up to 4,
+// 8 or 32), so small rows keep few registers per lane.
+template <typename T, typename TO, int MODE, int KPL>
 __global__ void __launch_bounds__(kGenWarps * 32)
 k_rows_generic(RowParams p) {
     __shared__ Seg segs[kMaxSegs];
     __shared__ int s_nseg, s_total;
-    __shared__ float sm_prod[kGenWarps][kMaxHD];
+    __shared__ float sm_prod[kGenWarps][KPL * 32];
     __shared__ float sm_m[kGenWarps][kGenMaxH];
     __shared__ float sm_s[kGenWarps][kGenMaxH];
     __shared__ float sm_w[kGenWarps][kGenMaxH];
@@ -509,10 +510,10 @@ k_rows_generic(RowParams p) {
             beg = p.indptr[row];
             end = p.indptr[row + 1];
         }
-        float q[kGenK], acc[kGenK];
+        float q[KPL], acc[KPL];
         const float qs = MODE == kFused ? p.qscale : 1.f;   // SDDMM scales at the store
 #pragma unroll
-        for (int k = 0; k < kGenK; ++k) {
+        for (int k = 0; k < KPL; ++k) {
             const int el = lane + 32 * k;
             q[k] = (MODE != kSpmm && el < HD) ? load_elem(Q, (int64_t)row * HD + el) * qs : 0.f;
             acc[k] = 0.f;
@@ -523,7 +524,7 @@ k_rows_generic(RowParams p) {
             const int64_t j = __ldg(p.indices + e);
             if constexpr (MODE != kSpmm) {
 #pragma unroll
-                for (int k = 0; k < kGenK; ++k) {
+                for (int k = 0; k < KPL; ++k) {
                     const int el = lane + 32 * k;
                     if (el < HD) prod[el] = q[k] * load_elem(K, j * HD + el);
                 }
@@ -563,7 +564,7 @@ k_rows_generic(RowParams p) {
             __syncwarp();
             if constexpr (MODE != kSddmm) {
 #pragma unroll
-                for (int k = 0; k < kGenK; ++k) {
+                for (int k = 0; k < KPL; ++k) {
                     const int el = lane + 32 * k;
                     if (el < HD) {
                         const int h = el / D;
@@ -576,7 +577,7 @@ k_rows_generic(RowParams p) {
         if constexpr (MODE == kSddmm) continue;
         if (chunk >= 0) {
 #pragma unroll
-            for (int k = 0; k < kGenK; ++k) {
+            for (int k = 0; k < KPL; ++k) {
                 const int el = lane + 32 * k;
                 if (el < HD) p.part.acc[(int64_t)chunk * HD + el] = acc[k];
             }
@@ -587,7 +588,7 @@ k_rows_generic(RowParams p) {
                 }
         } else {
 #pragma unroll
-            for (int k = 0; k < kGenK; ++k) {
+            for (int k = 0; k < KPL; ++k) {
                 const int el = lane + 32 * k;
                 if (el < HD) {
                     float v = acc[k];
@@ -954,11 +955,24 @@ static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParam
         kernel<<<grid_persistent(kernel, kGenWarps * 32, 0), kGenWarps * 32, 0, s>>>(p);
         return cudaGetLastError();
     };
+    auto by_kpl = [&](auto kpl4, auto kpl8, auto kpl32) {
+        const int kpl = (p.HD + 31) / 32;
+        return kpl <= 4 ? go(kpl4) : kpl <= 8 ? go(kpl8) : go(kpl32);
+    };
     cudaError_t e;
     switch (mode) {
-        case kFused: e = go(k_rows_generic<T, TO, kFused>); break;
-        case kSpmm: e = go(k_rows_generic<T, TO, kSpmm>); break;
-        default: e = go(k_rows_generic<T, TO, kSddmm>); break;
+        case kFused:
+            e = by_kpl(k_rows_generic<T, TO, kFused, 4>, k_rows_generic<T, TO, kFused, 8>,
+                       k_rows_generic<T, TO, kFused, 32>);
+            break;
+        case kSpmm:
+            e = by_kpl(k_rows_generic<T, TO, kSpmm, 4>, k_rows_generic<T, TO, kSpmm, 8>,
+                       k_rows_generic<T, TO, kSpmm, 32>);
+            break;
+        default:
+            e = by_kpl(k_rows_generic<T, TO, kSddmm, 4>, k_rows_generic<T, TO, kSddmm, 8>,
+                       k_rows_generic<T, TO, kSddmm, 32>);
+            break;
     }
     return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
 }

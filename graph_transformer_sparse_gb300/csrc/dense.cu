@@ -12,24 +12,29 @@
 // of one block and one head, which share every K/V tile.  Warp roles:
 //   warps 0-3 / 4-7   softmax of tile A / B: one warpgroup per tile, each
 //                     thread one query row (= TMEM lane) over all 128 key
-//                     columns of a tile (no exchange between warps)
+//                     columns of a tile, held in registers (no exchange
+//                     between warps, one TMEM read of S per tile)
 //   warp 8            MMA issue: the whole warp runs the loop, one elected
 //                     lane issues S_g = Q_g K_j^T (tcgen05.mma M=128 N=128,
 //                     fp32 in TMEM) and O_g += P_g V_j (M=128 N=64, P read
 //                     from TMEM) once softmax g has written P_g
 //   warp 9            TMA: Q tiles (double-buffered across items), K_j and V_j
 //                     into a 4-stage ring (128-byte swizzle)
+//   warps 10-11       idle; warps 8-11 hand registers to the softmax
+//                     warpgroups (setmaxnreg)
 // TMEM holds three S/P buffers used in rotation (the next S tile is computed
 // while the softmax works on the current one) and O_A, O_B.  The softmax
-// keeps a running row maximum m (log2 units) that is raised only when a
-// tile's maximum exceeds it by more than 8 (then O_g and the row sum are
-// rescaled), and writes P = 2^(s*scale*log2e - m) back over S_g as two bf16
-// terms P_hi = bf16(P), P_lo = bf16(P - P_hi); O_g += P_hi V + P_lo V keeps
-// the product at ~16-bit precision on the bf16 tensor path (a single bf16 P
-// would cost ~2^-9 relative per weight, outside the accuracy bound of the
-// bf16 path).  out = O / l at the end of an item.  Every mbarrier wait is
-// bounded: on timeout the CTA records an error code, drains (bounded) the
-// copies and MMAs it issued, frees its tensor memory and returns.
+// takes the row maximum m (log2 units) of an item's first key tile and keeps
+// it while later tiles' P sums stay below a limit (P stays small and finite);
+// a row whose tile sum goes over takes that tile's exact maximum, and O_g and
+// the row sum are rescaled.  It writes P = 2^(s*scale*log2e - m) back over
+// S_g as two bf16 terms P_hi = bf16(P), P_lo = bf16(P - P_hi); O_g += P_hi V +
+// P_lo V keeps the product at ~16-bit precision on the bf16 tensor path (a
+// single bf16 P would cost ~2^-9 relative per weight, outside the accuracy
+// bound of the bf16 path).  out = O / l at the end of an item.  Every
+// mbarrier wait is bounded: on timeout the CTA records an error code, drains
+// (bounded) the copies and MMAs it issued, frees its tensor memory and
+// returns.
 #include "dense.cuh"
 
 #include <cuda.h>
@@ -45,7 +50,6 @@ namespace {
 constexpr int kTile = 128;              // rows per Q / K / V tile
 constexpr int kD = 64;                  // head width handled here
 constexpr uint32_t kTileBytes = kTile * kD * 2;   // 16 KB bf16
-constexpr float kRescaleThreshold = 8.f;          // log2 units
 constexpr long long kWaitCycles = 2000000000ll;   // ~1 s at 2 GHz
 
 
@@ -168,31 +172,50 @@ __device__ __forceinline__ void mma_s_batch(uint32_t d, uint64_t a, uint64_t b, 
         ::"r"(d), "l"(a), "l"(b), "r"(idesc), "l"(a + 2), "l"(b + 2), "l"(a + 4), "l"(b + 4), "l"(a + 6), "l"(b + 6)
         : "memory");
 }
-// O (+)= P_hi V + P_lo V over 128 keys: eight 16-key steps; P_hi of keys
-// 32c..32c+31 in columns 32c..32c+15, P_lo in 32c+16..32c+31; the V rows of a
-// step start 2048 bytes (128 descriptor units) after the previous step's.
-__device__ __forceinline__ void mma_pv_batch(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// Half a key-tile step of the MMA warp in one asm block (one elected lane):
+//   [do_pv] O (+)= P_hi V + P_lo V over 128 keys in eight 16-key steps (P_hi
+//           of keys 32c..32c+31 in columns 32c..32c+15, P_lo in 32c+16..
+//           32c+31; the V rows of a step start 2048 bytes (128 descriptor
+//           units) after the previous step's), commit -> bar_o
+//   [do_x]  commit -> bar_x (tracks every MMA issued so far)
+//   [do_s]  S = Q K^T over K = 64 (as mma_s_batch), commit -> bar_s
+// Fewer asm blocks per step leave fewer gaps in the tensor pipe's short queue.
+__device__ __forceinline__ void mma_half_step(uint32_t d_o, uint32_t a_p, uint64_t b_v, uint32_t id_o, uint32_t acc,
+                                              uint32_t bar_o, uint32_t do_pv, uint32_t bar_x, uint32_t do_x,
+                                              uint32_t d_s, uint64_t a_q, uint64_t b_k, uint32_t id_s,
+                                              uint32_t bar_s, uint32_t do_s) {
     asm volatile(
-        "{\n\t.reg .pred p, q, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "{\n\t.reg .pred p, q, f, e, pv, px, ps;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\tsetp.ne.b32 f, 0, 0;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+0], %2, %3, p;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %2, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], %5, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], %5, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], %6, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], %6, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], %7, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], %7, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+64], %8, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+80], %8, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+72], %9, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+88], %9, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+96], %10, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+112], %10, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+104], %11, %3, q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+120], %11, %3, q;\n\t}"
-        ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc), "l"(b + 128), "l"(b + 256), "l"(b + 384), "l"(b + 512),
-          "l"(b + 640), "l"(b + 768), "l"(b + 896)
+        "setp.ne.and.b32 pv, %6, 0, e;\n\tsetp.ne.and.b32 px, %8, 0, e;\n\tsetp.ne.and.b32 ps, %14, 0, e;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+0], %2, %3, p;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %2, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], %15, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], %15, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], %16, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], %16, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], %17, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], %17, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+64], %18, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+80], %18, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+72], %19, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+88], %19, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+96], %20, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+112], %20, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+104], %21, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+120], %21, %3, q;\n\t"
+        "@pv tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+        "@px tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], %10, %11, %12, f;\n\t"
+        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], %22, %23, %12, q;\n\t"
+        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], %24, %25, %12, q;\n\t"
+        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], %26, %27, %12, q;\n\t"
+        "@ps tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%13];\n\t}"
+        ::"r"(d_o), "r"(a_p), "l"(b_v), "r"(id_o), "r"(acc), "r"(bar_o), "r"(do_pv), "r"(bar_x), "r"(do_x),
+          "r"(d_s), "l"(a_q), "l"(b_k), "r"(id_s), "r"(bar_s), "r"(do_s),
+          "l"(b_v + 128), "l"(b_v + 256), "l"(b_v + 384), "l"(b_v + 512), "l"(b_v + 640), "l"(b_v + 768),
+          "l"(b_v + 896), "l"(a_q + 2), "l"(b_k + 2), "l"(a_q + 4), "l"(b_k + 4), "l"(a_q + 6), "l"(b_k + 6)
         : "memory");
 }
 
@@ -254,20 +277,34 @@ struct DenseErr {
     static constexpr int kTimeout = 1;
 };
 
-// Warp roles of the CTA (10 warps).  Two query tiles per work item (A: rows
-// q0.., B: rows q0+128..) share every K/V tile.  Each query tile has one
-// softmax warpgroup, a thread per query row over all 128 key columns:
+// Warp roles of the CTA (12 warps, three warpgroups).  Two query tiles per
+// work item (A: rows q0.., B: rows q0+128..) share every K/V tile.  Each query
+// tile has one softmax warpgroup, a thread per query row over all 128 key
+// columns:
 //   warps 0-3 / 4-7     softmax of tile A / B
 //   warp 8              MMA issue (one elected lane of the converged warp)
 //   warp 9              TMA loads (one thread)
+//   warps 10-11         idle (they complete the third warpgroup, whose
+//                       registers move to the softmax warpgroups)
 // The grid is persistent (one CTA per SM): each CTA walks work items (a pair
 // of query tiles and a head); Q tiles are double-buffered and the K/V ring
 // runs on across items, so the next item's loads and first products overlap
 // the current item's last softmax and epilogue.
-constexpr int kWarps = 10;
+constexpr int kWarps = 12;
 constexpr int kThreadsWS = kWarps * 32;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
+// Register split (setmaxnreg): the CTA is launched with kRegsLaunch per
+// thread; the third warpgroup gives registers up so that each softmax thread
+// can hold a whole 128-key row of S.  The split must fit the launch's total.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsOther = 88;
+static_assert(kRegsLaunch == 65536 / kThreadsWS / 8 * 8, "the launch bound gives each thread kRegsLaunch");
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kRegsLaunch * kThreadsWS, "register split");
+// A tile's P sum above this (or not finite) makes the softmax take the exact
+// tile maximum and raise its running maximum (P <= 2^12 otherwise).
+constexpr float kTileSumLimit = 4096.f;
 constexpr int kStages = 4;                        // K/V ring
 constexpr uint32_t kTmemAll = 512;
 // TMEM: three S/P buffers (128 columns each) used in rotation by the S tiles
@@ -358,7 +395,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
 }
 
 template <typename TO>
-__global__ void __maxnreg__(168)   // 3 warps share an SM sub-partition: 3 x 168 x 32 <= 16384
+__global__ void __launch_bounds__(kThreadsWS, 1)
 k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ items, int n_work, int H,
              TO* __restrict__ out, int HD, float sl2, int* __restrict__ err) {
@@ -408,7 +445,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-
+    // The register change is made at the head of each warpgroup's branch, by
+    // all four of its warps at the same instruction.
+    if (warp >= kMmaWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
     if (warp == kTmaWarp) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
@@ -453,17 +493,16 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
-        // Order per item (two query tiles): S_A0 S_B0 S_A1, then per key tile j:
-        // PV_Aj, S_B(j+1), PV_Bj, S_A(j+2).  An S tile is computed one step ahead
-        // of its softmax; a buffer is reused only after the PV that read its P
-        // (the tensor pipe executes one thread's MMAs in issue order).  The
-        // whole warp runs this loop; elect.sync picks the same lane (the
-        // lowest) for every batch and commit, so one thread issues them all.
-        // Barrier states needed after a batch are probed before it (non-
-        // blocking) and read after it, so a test's latency overlaps the
-        // batch; the waits follow S batches where possible (the tensor pipe's
-        // short queue covers ~300 cycles of non-MMA work after 4 S MMAs but
-        // only ~170 after 16 PV MMAs).
+        // Order per item (two query tiles): S_A0 S_B0 S_A1, then per key tile j
+        // two asm blocks: [PV_Aj, S_B(j+1)] and [PV_Bj, S_A(j+2)].  An S tile is
+        // computed one step ahead of its softmax; a buffer is reused only after
+        // the PV that read its P (the tensor pipe executes one thread's MMAs in
+        // issue order).  The whole warp runs this loop; elect.sync picks the
+        // same lane (the lowest) for every batch and commit, so one thread
+        // issues them all.  The tensor pipe queues only a few MMAs ahead, so
+        // every gap between asm blocks risks leaving it idle: each half step
+        // is one block, and the barrier states needed after a block are probed
+        // before it (non-blocking) and read after it.
         {
             const uint32_t idS = idesc_bf16(128, 128, 0);
             const uint32_t idO = idesc_bf16(128, 64, 1);
@@ -512,14 +551,6 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     ++pc;
                     return r;
                 };
-                auto issue_pv = [&](int g, int j) {
-                    const int kt = kv_tile + j;
-                    const uint64_t dV = smem_desc_sw128(su32(sV(kt % kStages)), 8192, 1024);
-                    mma_pv_batch(tmem + col_o(g), tmem + col_buf(bufk(g, j)), dV, idO, j > 0 ? 1u : 0u);
-                    int& pn = g == 0 ? pv0 : pv1;
-                    tc_commit(&bars.o[g][pn & 1]);
-                    ++pn;
-                };
                 ok = mbar_wait_warp(&bars.q_full[qb], (local >> 1) & 1);
                 if (!ok) break;
                 // S tiles ahead of the loop: A0 (B0) and A1
@@ -533,6 +564,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tc_fence_after();
                     if (ok) issue_s(0, 1);
                 }
+                // descriptors of S_g(j) and PV_g(j)
+                auto dq = [&](int g) { return smem_desc_sw128(su32(sQ(qb, g)), 16, 1024); };
+                auto dk = [&](int j) { return smem_desc_sw128(su32(sK((kv_tile + j) % kStages)), 16, 1024); };
+                auto dv = [&](int j) { return smem_desc_sw128(su32(sV((kv_tile + j) % kStages)), 8192, 1024); };
                 uint32_t pa = p_probe(0);
                 for (int j = 0; ok && j < T; ++j) {
                     // the first product of an item overwrites O_g: the previous
@@ -543,8 +578,15 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tc_fence_after();
                     const uint32_t pb = nq > 1 ? p_probe(1) : 0u;
                     const uint32_t kv = j + 2 < T ? kv_probe(j + 2) : 0u;
-                    issue_pv(0, j);
-                    if (nq > 1 && j + 1 < T) issue_s(1, j + 1);
+                    {   // PV_A(j), then S_B(j+1) into the buffer PV_A(j) has just read
+                        const bool sb = nq > 1 && j + 1 < T;
+                        mma_half_step(tmem + col_o(0), tmem + col_buf(bufk(0, j)), dv(j), idO, j > 0 ? 1u : 0u,
+                                      su32(&bars.o[0][pv0 & 1]), 1u, 0u, 0u,
+                                      tmem + col_buf(sb ? bufk(1, j + 1) : 0), dq(1), dk(j + 1), idS,
+                                      su32(&bars.s[1][sg1 & 1]), sb ? 1u : 0u);
+                        ++pv0;
+                        if (sb) { ++sg1; ++snum; }
+                    }
                     if (j + 2 < T) ok = kv_wait(j + 2, kv);
                     if (ok && nq > 1) {
                         ok = p_wait(1, pb);
@@ -552,10 +594,17 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     }
                     if (!ok) break;
                     tc_fence_after();
-                    if (nq > 1) issue_pv(1, j);
-                    tc_commit(&bars.kv_empty[(kv_tile + j) % kStages]);   // K_j, V_j free after these
                     pa = p_probe(0);
-                    if (j + 2 < T) issue_s(0, j + 2);
+                    {   // PV_B(j); K_j, V_j free once it (and PV_A(j)) are done; S_A(j+2)
+                        const bool sa = j + 2 < T;
+                        mma_half_step(tmem + col_o(1), tmem + col_buf(nq > 1 ? bufk(1, j) : 0), dv(j), idO,
+                                      j > 0 ? 1u : 0u, su32(&bars.o[1][pv1 & 1]), nq > 1 ? 1u : 0u,
+                                      su32(&bars.kv_empty[(kv_tile + j) % kStages]), 1u,
+                                      tmem + col_buf(sa ? bufk(0, j + 2) : 0), dq(0), dk(sa ? j + 2 : j), idS,
+                                      su32(&bars.s[0][sg0 & 1]), sa ? 1u : 0u);
+                        if (nq > 1) ++pv1;
+                        if (sa) { ++sg0; ++snum; }
+                    }
                 }
                 if (ok) tc_commit(&bars.q_empty[qb]);        // Q buffer free after this item's products
                 ++items0;
@@ -570,7 +619,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             tc_commit(&bars.drain);
             mbar_wait_warp(&bars.drain, 0, kWaitCycles / 4);
         }
-    } else if (warp < kMmaWarp) {
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ---------------- softmax warpgroups ----------------
         // One thread per query row (= TMEM lane) and all 128 key columns of a
         // tile: a row's running maximum and sum live in one thread, so the
@@ -614,14 +665,16 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     break;
                 }
                 tc_fence_after();
-                // the row's extreme over the tile's 128 keys (max for a
-                // positive scale, min for a negative one)
-                float ma, mb, mc, md;
-                {
-                    uint32_t r[128];
+                // the tile's S row, read once: the P pass and (rarely) the
+                // maximum work from registers
+                uint32_t r[128];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, r + 32 * c);
-                    tmem_ld_wait();
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, r + 32 * c);
+                tmem_ld_wait();
+                // the row's largest t = s*scale*log2e over the tile (from its
+                // largest s for a positive scale, its smallest for a negative one)
+                auto tile_top = [&]() {
+                    float ma, mb, mc, md;
                     ma = mb = mc = md = pos ? -INFINITY : INFINITY;
                     if (pos) {
 #pragma unroll
@@ -642,21 +695,59 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                         }
                         ma = fminf(fminf(ma, mb), fminf(mc, md));
                     }
-                }
-                const float mt = ma * sl2;
-                if (j == 0) {
-                    m_used = mt;
-                } else {
-                    // the maximum in use is raised only when the tile's exceeds
-                    // it by more than the threshold (P <= 2^threshold otherwise)
-                    const bool up = mt > m_used + kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, up)) {
+                    return ma * sl2;
+                };
+                // P = 2^(t - m) as bf16 hi/lo written over S, 32 keys at a time;
+                // (la, lb) = the tile's sum of P
+                float la = 0.f, lb = 0.f;
+                auto write_p = [&]() {
+                    const float nm = -m_used;
+                    la = lb = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t* x = r + 32 * c;
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            float t0, t1;
+                            ffma2(t0, t1, __uint_as_float(x[2 * q]), __uint_as_float(x[2 * q + 1]), sl2, nm);
+                            const float p0 = ex2(t0), p1 = ex2(t1);
+                            fadd2(la, lb, p0, p1);
+                            const uint32_t hi = pack2_bf16(p0, p1);
+                            // P_lo = bf16(P - P_hi): the differences, exact in fp32, come
+                            // from mixed bf16 x bf16 + fp32 FMAs on the packed P_hi halves
+                            // (times -1) -- no unpacking of P_hi
+                            float d0, d1;
+                            asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+                                "fma.rn.f32.bf16 %0, h0, %5, %3;\n\tfma.rn.f32.bf16 %1, h1, %5, %4;\n\t}"
+                                : "=f"(d0), "=f"(d1) : "r"(hi), "f"(p0), "f"(p1), "h"((unsigned short)0xBF80));
+                            pk[q] = hi;
+                            pk[16 + q] = pack2_bf16(d0, d1);
+                        }
+                        // keys 32c..32c+31: P_hi in columns 32c..32c+15, P_lo in 32c+16..32c+31
+                        tmem_st32(tS + 32 * c, pk);
+                    }
+                };
+                // The first tile sets the running maximum m; later tiles use it
+                // as it stands, unless a row's tile sum exceeds kTileSumLimit
+                // (some P above the limit, or not finite): that row takes the
+                // exact maximum of the tile, O_g and its sum are rescaled, and
+                // the warp writes the tile's P again.
+                if (j == 0) m_used = tile_top();
+                write_p();
+                if (j > 0) {
+                    const bool over = !(la + lb <= kTileSumLimit);
+                    if (__any_sync(0xffffffffu, over)) {
                         // O_g may be rescaled only after PV_g(j-1); no later PV_g
                         // can have been issued (it needs this tile's P)
                         if (!o_wait(o_cnt + j - 1)) atomicExch(&s_abort, 1);
                         tc_fence_after();
-                        const float alpha = up ? ex2(m_used - mt) : 1.f;
-                        if (up) m_used = mt;
+                        float alpha = 1.f;
+                        if (over) {
+                            const float mt = fmaxf(tile_top(), m_used);
+                            alpha = ex2(m_used - mt);
+                            m_used = mt;
+                        }
                         l0 *= alpha;
                         l1 *= alpha;
 #pragma unroll 1
@@ -669,42 +760,11 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                             tmem_st32(tO + 32 * c, o);
                         }
                         tmem_st_wait();
+                        write_p();
                     }
                 }
-                // P = 2^(s*scale*log2e - m) as bf16 hi/lo, 32 keys at a time
-                // (S re-read from TMEM; the next chunk's load is issued before
-                // the current chunk's arithmetic)
-                const float nm = -m_used;
-                uint32_t xa[32], xb[32];
-                tmem_ld32(tS, xa);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t* x = (c & 1) ? xb : xa;
-                    uint32_t* xn = (c & 1) ? xa : xb;
-                    if (c + 1 < 4) tmem_ld32(tS + 32 * (c + 1), xn);
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        float t0, t1;
-                        ffma2(t0, t1, __uint_as_float(x[2 * q]), __uint_as_float(x[2 * q + 1]), sl2, nm);
-                        const float p0 = ex2(t0), p1 = ex2(t1);
-                        fadd2(l0, l1, p0, p1);
-                        const uint32_t hi = pack2_bf16(p0, p1);
-                        // P_lo = bf16(P - P_hi): the differences, exact in fp32, come
-                        // from mixed bf16 x bf16 + fp32 FMAs on the packed P_hi halves
-                        // (times -1) -- no unpacking of P_hi
-                        float d0, d1;
-                        asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
-                            "fma.rn.f32.bf16 %0, h0, %5, %3;\n\tfma.rn.f32.bf16 %1, h1, %5, %4;\n\t}"
-                            : "=f"(d0), "=f"(d1) : "r"(hi), "f"(p0), "f"(p1), "h"((unsigned short)0xBF80));
-                        pk[q] = hi;
-                        pk[16 + q] = pack2_bf16(d0, d1);
-                    }
-                    // keys 32c..32c+31: P_hi in columns 32c..32c+15, P_lo in 32c+16..32c+31
-                    tmem_st32(tS + 32 * c, pk);
-                    if (c + 1 < 4) tmem_ld_wait();
-                }
+                l0 += la;
+                l1 += lb;
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -810,6 +870,21 @@ bool make_map(CUtensorMap* m, const void* base, int64_t N, int HD) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The register split of the kernel (setmaxnreg) waits until the registers it
+// asks for are free; it is only valid when the CTA was launched with
+// kRegsLaunch registers per thread.  Checked once per kernel instance.
+template <typename K>
+bool regs_fit(K kernel) {
+    static std::once_flag once;
+    static bool fit = false;
+    std::call_once(once, [&] {
+        cudaFuncAttributes a{};
+        fit = cudaFuncGetAttributes(&a, kernel) == cudaSuccess && a.numRegs == kRegsLaunch &&
+              a.maxThreadsPerBlock >= kThreadsWS;
+    });
+    return fit;
+}
+
 }  // namespace
 
 bool dense_supported(int H, int D, gtattn_dtype dt, const void* Q, const void* K, const void* V,
@@ -836,6 +911,7 @@ gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void
     cudaError_t e;
     if (dt == GTATTN_BF16) {
         auto k = k_dense_attn<__nv_bfloat16>;
+        if (!regs_fit(k)) return GTATTN_ERR_UNSUPPORTED;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
         if (e == cudaSuccess) {
             k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, n_work, H,
@@ -844,6 +920,7 @@ gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void
         }
     } else {
         auto k = k_dense_attn<float>;
+        if (!regs_fit(k)) return GTATTN_ERR_UNSUPPORTED;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
         if (e == cudaSuccess) {
             k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, n_work, H, static_cast<float*>(out), HD,

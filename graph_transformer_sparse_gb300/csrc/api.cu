@@ -168,7 +168,7 @@ static gtattn_status scratch_alloc(int64_t N, int64_t nnz, int H, int HD, int lo
 }
 
 static RowParams make_params(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
-                             const void* V, void* out, int64_t N, int H, int D, float qscale,
+                             const void* V, void* out, int64_t N, int64_t nnz, int H, int D, float qscale,
                              const RowChoice& c, const TaskLists& L, const Partials& part) {
     RowParams p{};
     p.indptr = indptr;
@@ -186,6 +186,7 @@ static RowParams make_params(const int32_t* indptr, const int32_t* indices, cons
     p.lph = c.lph;
     p.lists = L;
     p.part = part;
+    p.task_bound = row_task_bound(N, nnz, L.chunk_edges);
     return p;
 }
 
@@ -252,15 +253,15 @@ extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indice
                          &chunks, &longs, stream));
     gtattn_status st;
     {
-        ProfScope ps(GTATTN_KCAT_BIN, 3, stream);
+        ProfScope ps(GTATTN_KCAT_BIN, bin_launches((int)N, nullptr), stream);
         st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
     }
-    RowParams p = make_params(indptr, indices, Q, K, V, out, N, H, D, scale * kLog2e, c, sc.lists, sc.part);
+    RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale * kLog2e, c, sc.lists, sc.part);
     if (st == GTATTN_OK) {
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
         st = launch_rows(kFused, dtype, c, p, stream);
     }
-    if (st == GTATTN_OK) {
+    if (st == GTATTN_OK && nnz > o.long_row_min) {   // else no row is split
         ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
         st = launch_combine(kFused, dtype, p, stream);
     }
@@ -301,7 +302,7 @@ extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t*
         part.acc = reinterpret_cast<float*>(b + 2 * align_up(sizeof(float) * (size_t)n_chunks * H));
     }
     TaskLists L{plan->hdr, plan->rows, plan->chunks, plan->longs, plan->opts.chunk_edges, dense ? 0 : 1};
-    RowParams p = make_params(indptr, indices, Q, K, V, out, N, H, D, scale * kLog2e, c, L, part);
+    RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale * kLog2e, c, L, part);
     gtattn_status st = GTATTN_OK;
     if (dense) {
         ProfScope ps(GTATTN_KCAT_DENSE, 1, stream);
@@ -342,10 +343,10 @@ extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* 
     float* pr = probs ? probs : sc.probs;
     gtattn_status st;
     {
-        ProfScope ps(GTATTN_KCAT_BIN, 3, stream);
+        ProfScope ps(GTATTN_KCAT_BIN, bin_launches((int)N, nullptr), stream);
         st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
     }
-    RowParams p = make_params(indptr, indices, Q, K, V, out, N, H, D, scale, c, sc.lists, sc.part);
+    RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, c, sc.lists, sc.part);
     p.logits = lg;
     p.probs = pr;
     // (1) SDDMM: logits
@@ -363,7 +364,7 @@ extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* 
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
         st = launch_rows(kSpmm, dtype, c, p, stream);
     }
-    if (st == GTATTN_OK) {
+    if (st == GTATTN_OK && nnz > o.long_row_min) {   // else no row is split
         ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
         st = launch_combine(kSpmm, dtype, p, stream);
     }

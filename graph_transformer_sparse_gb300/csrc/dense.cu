@@ -178,44 +178,50 @@ __device__ __forceinline__ void mma_s_batch(uint32_t d, uint64_t a, uint64_t b, 
 //           32c+31; the V rows of a step start 2048 bytes (128 descriptor
 //           units) after the previous step's), commit -> bar_o
 //   [do_x]  commit -> bar_x (tracks every MMA issued so far)
-//   [do_s]  S = Q K^T over K = 64 (as mma_s_batch), commit -> bar_s
-// Fewer asm blocks per step leave fewer gaps in the tensor pipe's short queue.
+//   [do_s]  S = Q K^T over K = 64 in four 16-element steps (descriptor start
+//           +2 per step), commit -> bar_s
+// The per-step descriptors are formed inside the block from the bases, so
+// the MMA warp does little between blocks: the tensor pipe queues only a few
+// MMAs ahead, and every gap between blocks risks leaving it idle.
 __device__ __forceinline__ void mma_half_step(uint32_t d_o, uint32_t a_p, uint64_t b_v, uint32_t id_o, uint32_t acc,
                                               uint32_t bar_o, uint32_t do_pv, uint32_t bar_x, uint32_t do_x,
                                               uint32_t d_s, uint64_t a_q, uint64_t b_k, uint32_t id_s,
                                               uint32_t bar_s, uint32_t do_s) {
     asm volatile(
         "{\n\t.reg .pred p, q, f, e, pv, px, ps;\n\t"
+        ".reg .b64 v1, v2, v3, v4, v5, v6, v7, q2, q4, q6, k2, k4, k6;\n\t"
         "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\tsetp.ne.b32 f, 0, 0;\n\t"
+        "add.s64 v1, %2, 128;\n\tadd.s64 v2, %2, 256;\n\tadd.s64 v3, %2, 384;\n\tadd.s64 v4, %2, 512;\n\t"
+        "add.s64 v5, %2, 640;\n\tadd.s64 v6, %2, 768;\n\tadd.s64 v7, %2, 896;\n\t"
+        "add.s64 q2, %10, 2;\n\tadd.s64 q4, %10, 4;\n\tadd.s64 q6, %10, 6;\n\t"
+        "add.s64 k2, %11, 2;\n\tadd.s64 k4, %11, 4;\n\tadd.s64 k6, %11, 6;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.and.b32 pv, %6, 0, e;\n\tsetp.ne.and.b32 px, %8, 0, e;\n\tsetp.ne.and.b32 ps, %14, 0, e;\n\t"
         "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+0], %2, %3, p;\n\t"
         "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %2, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], %15, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], %15, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], %16, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], %16, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], %17, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], %17, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+64], %18, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+80], %18, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+72], %19, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+88], %19, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+96], %20, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+112], %20, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+104], %21, %3, q;\n\t"
-        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+120], %21, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], v1, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], v1, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], v2, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], v2, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], v3, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], v3, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+64], v4, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+80], v4, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+72], v5, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+88], v5, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+96], v6, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+112], v6, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+104], v7, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+120], v7, %3, q;\n\t"
         "@pv tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
         "@px tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
         "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], %10, %11, %12, f;\n\t"
-        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], %22, %23, %12, q;\n\t"
-        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], %24, %25, %12, q;\n\t"
-        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], %26, %27, %12, q;\n\t"
+        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], q2, k2, %12, q;\n\t"
+        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], q4, k4, %12, q;\n\t"
+        "@ps tcgen05.mma.cta_group::1.kind::f16 [%9], q6, k6, %12, q;\n\t"
         "@ps tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%13];\n\t}"
         ::"r"(d_o), "r"(a_p), "l"(b_v), "r"(id_o), "r"(acc), "r"(bar_o), "r"(do_pv), "r"(bar_x), "r"(do_x),
-          "r"(d_s), "l"(a_q), "l"(b_k), "r"(id_s), "r"(bar_s), "r"(do_s),
-          "l"(b_v + 128), "l"(b_v + 256), "l"(b_v + 384), "l"(b_v + 512), "l"(b_v + 640), "l"(b_v + 768),
-          "l"(b_v + 896), "l"(a_q + 2), "l"(b_k + 2), "l"(a_q + 4), "l"(b_k + 4), "l"(a_q + 6), "l"(b_k + 6)
+          "r"(d_s), "l"(a_q), "l"(b_k), "r"(id_s), "r"(bar_s), "r"(do_s)
         : "memory");
 }
 
@@ -316,6 +322,12 @@ constexpr size_t kWsSmemQ = 0;                    // 2 buffers x 2 query tiles
 constexpr size_t kWsSmemKV = 4 * kTileBytes;      // stage s: K at +0, V at +kTileBytes
 constexpr size_t kWsSmemBytes = 4 * kTileBytes + kStages * 2 * kTileBytes;   // 192 KB
 constexpr size_t kWsSmemAlloc = kWsSmemBytes + 1024;
+// Descriptor start-address units (16 bytes) between K/V stages and between Q tiles.
+constexpr uint64_t kStageUnits = (2 * kTileBytes) >> 4;
+constexpr uint64_t kQUnits = kTileBytes >> 4;
+static_assert((kStages & (kStages - 1)) == 0, "stages are stepped with a mask");
+static_assert((kWsSmemAlloc + 1024) >> 4 < (1u << 14), "descriptor start addresses fit 14 bits");
+__device__ __forceinline__ int mod3(int x) { return x >= 3 ? x - 3 : x; }   // x < 6
 
 struct WsBars {
     uint64_t q_full[2], q_empty[2];   // Q buffers (TMA <-> MMA)
@@ -506,6 +518,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         {
             const uint32_t idS = idesc_bf16(128, 128, 0);
             const uint32_t idO = idesc_bf16(128, 64, 1);
+            const uint64_t dQ0 = smem_desc_sw128(su32(sQ(0, 0)), 16, 1024);
+            const uint64_t dK0 = smem_desc_sw128(su32(sK(0)), 16, 1024);
+            const uint64_t dV0 = smem_desc_sw128(su32(sV(0)), 8192, 1024);
             bool ok = true;
             int kv_tile = 0;   // first K/V tile of the current item in the CTA's sequence
             int snum = 0;      // S tiles issued so far (buffer = snum % 3)
@@ -564,12 +579,13 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tc_fence_after();
                     if (ok) issue_s(0, 1);
                 }
-                // descriptors of S_g(j) and PV_g(j)
-                auto dq = [&](int g) { return smem_desc_sw128(su32(sQ(qb, g)), 16, 1024); };
-                auto dk = [&](int j) { return smem_desc_sw128(su32(sK((kv_tile + j) % kStages)), 16, 1024); };
-                auto dv = [&](int j) { return smem_desc_sw128(su32(sV((kv_tile + j) % kStages)), 8192, 1024); };
+                // descriptors: the bases plus a stage's or a Q buffer's offset
+                // (the start address field is linear in the byte address)
+                const uint64_t dQa = dQ0 + static_cast<uint64_t>(2 * qb) * kQUnits, dQb = dQa + kQUnits;
+                int st = kv_tile & (kStages - 1);   // stage of K_j, V_j
+                int bA = s0 % 3;                    // buffer of S_A(j); S_B(j) is in the next one
                 uint32_t pa = p_probe(0);
-                for (int j = 0; ok && j < T; ++j) {
+                for (int j = 0; ok && j < T; ++j, st = (st + 1) & (kStages - 1), bA = mod3(bA + nq)) {
                     // the first product of an item overwrites O_g: the previous
                     // item's epilogue must have read it
                     ok = p_wait(0, pa);
@@ -578,11 +594,12 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tc_fence_after();
                     const uint32_t pb = nq > 1 ? p_probe(1) : 0u;
                     const uint32_t kv = j + 2 < T ? kv_probe(j + 2) : 0u;
+                    const uint64_t dVj = dV0 + static_cast<uint64_t>(st) * kStageUnits;
                     {   // PV_A(j), then S_B(j+1) into the buffer PV_A(j) has just read
                         const bool sb = nq > 1 && j + 1 < T;
-                        mma_half_step(tmem + col_o(0), tmem + col_buf(bufk(0, j)), dv(j), idO, j > 0 ? 1u : 0u,
-                                      su32(&bars.o[0][pv0 & 1]), 1u, 0u, 0u,
-                                      tmem + col_buf(sb ? bufk(1, j + 1) : 0), dq(1), dk(j + 1), idS,
+                        mma_half_step(tmem + col_o(0), tmem + col_buf(bA), dVj, idO, j > 0 ? 1u : 0u,
+                                      su32(&bars.o[0][pv0 & 1]), 1u, 0u, 0u, tmem + col_buf(bA), dQb,
+                                      dK0 + static_cast<uint64_t>((st + 1) & (kStages - 1)) * kStageUnits, idS,
                                       su32(&bars.s[1][sg1 & 1]), sb ? 1u : 0u);
                         ++pv0;
                         if (sb) { ++sg1; ++snum; }
@@ -596,11 +613,13 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     tc_fence_after();
                     pa = p_probe(0);
                     {   // PV_B(j); K_j, V_j free once it (and PV_A(j)) are done; S_A(j+2)
+                        // into the buffer of S_B(j) (one query tile: of S_A(j+1)'s successor)
                         const bool sa = j + 2 < T;
-                        mma_half_step(tmem + col_o(1), tmem + col_buf(nq > 1 ? bufk(1, j) : 0), dv(j), idO,
-                                      j > 0 ? 1u : 0u, su32(&bars.o[1][pv1 & 1]), nq > 1 ? 1u : 0u,
-                                      su32(&bars.kv_empty[(kv_tile + j) % kStages]), 1u,
-                                      tmem + col_buf(sa ? bufk(0, j + 2) : 0), dq(0), dk(sa ? j + 2 : j), idS,
+                        const int bS = (bA + 2 * nq) % 3;
+                        mma_half_step(tmem + col_o(1), tmem + col_buf(mod3(bA + 1)), dVj, idO, j > 0 ? 1u : 0u,
+                                      su32(&bars.o[1][pv1 & 1]), nq > 1 ? 1u : 0u, su32(&bars.kv_empty[st]), 1u,
+                                      tmem + col_buf(bS), dQa,
+                                      dK0 + static_cast<uint64_t>((st + 2) & (kStages - 1)) * kStageUnits, idS,
                                       su32(&bars.s[0][sg0 & 1]), sa ? 1u : 0u);
                         if (nq > 1) ++pv1;
                         if (sa) { ++sg0; ++snum; }

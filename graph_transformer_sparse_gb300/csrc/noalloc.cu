@@ -141,7 +141,9 @@ extern "C" gtattn_status gtattn_fwd_noalloc(const int32_t* indptr, const int32_t
     p.lph = c.lph;
     p.lists = TaskLists{hdr, rows, chunks, longs, kNoAllocChunk, 1};
     p.part = part;
+    p.task_bound = row_task_bound(N, nnz, kNoAllocChunk);
     st = launch_rows(kFused, dtype, c, p, stream);
-    if (st == GTATTN_OK) st = launch_combine(kFused, dtype, p, stream);
+    // no row can be split when nnz is at most the split threshold
+    if (st == GTATTN_OK && nnz > kNoAllocLongMin) st = launch_combine(kFused, dtype, p, stream);
     return st;
 }

@@ -20,14 +20,17 @@ namespace gt {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool is_long(int deg, int long_min) { return deg > 0 && deg > long_min; }
 
-__global__ void k_bin_count(const int* __restrict__ indptr, int N, int long_min, int chunk,
-                            const int* __restrict__ dense_flag, int* __restrict__ hdr) {
+// The three binning steps as block-level functions over blocks bid of nb,
+// run as three kernels (large graphs) or all three by one block (small ones).
+__device__ __forceinline__ void bin_count_part(const int* __restrict__ indptr, int N, int long_min, int chunk,
+                                               const int* __restrict__ dense_flag, int* __restrict__ hdr, int bid,
+                                               int nb) {
     __shared__ int hist[kNumBuckets];
     __shared__ int s_long, s_chunks, s_dense, s_max;
     for (int b = threadIdx.x; b < kNumBuckets; b += blockDim.x) hist[b] = 0;
     if (threadIdx.x == 0) { s_long = 0; s_chunks = 0; s_dense = 0; s_max = 0; }
     __syncthreads();
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < N; i += gridDim.x * blockDim.x) {
+    for (int i = bid * blockDim.x + threadIdx.x; i < N; i += nb * blockDim.x) {
         int deg = indptr[i + 1] - indptr[i];
         atomicMax(&s_max, deg);
         if (dense_flag && dense_flag[i]) {
@@ -50,14 +53,22 @@ __global__ void k_bin_count(const int* __restrict__ indptr, int N, int long_min,
     }
 }
 
-__global__ void k_bin_offsets(int* hdr) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+__global__ void k_bin_count(const int* __restrict__ indptr, int N, int long_min, int chunk,
+                            const int* __restrict__ dense_flag, int* __restrict__ hdr) {
+    bin_count_part(indptr, N, long_min, chunk, dense_flag, hdr, blockIdx.x, gridDim.x);
+}
+
+__device__ __forceinline__ void bin_offsets_part(int* hdr) {   // one thread
     int off = 0;
     for (int b = kNumBuckets - 1; b >= 0; --b) {
         hdr[HdrLayout::kOffset + b] = off;
         off += hdr[HdrLayout::kCount + b];
     }
     hdr[HdrLayout::kDenseSeg] = off;
+}
+
+__global__ void k_bin_offsets(int* hdr) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) bin_offsets_part(hdr);
 }
 
 // Scatter of rows into the bucket lists, the split-row list and the dense
@@ -68,13 +79,13 @@ __global__ void k_bin_offsets(int* hdr) {
 constexpr int kScatterThreads = 512;
 constexpr int kScatterKeys = kNumBuckets + 3;   // buckets, split rows (NB), dense segment (NB + 2)
 
-__global__ void __launch_bounds__(kScatterThreads)
-k_bin_scatter(const int* __restrict__ indptr, int N, int long_min, int chunk,
-              const int* __restrict__ dense_flag, int* __restrict__ hdr,
-              int* __restrict__ rows, int2* __restrict__ chunks, int2* __restrict__ longs) {
+__device__ __forceinline__ void bin_scatter_part(const int* __restrict__ indptr, int N, int long_min, int chunk,
+                                                 const int* __restrict__ dense_flag, int* __restrict__ hdr,
+                                                 int* __restrict__ rows, int2* __restrict__ chunks,
+                                                 int2* __restrict__ longs, int bid, int nb) {
     __shared__ int cnt[kScatterKeys], base[kScatterKeys];
     __shared__ int s_chunks, s_chunk_base;
-    for (int t0 = blockIdx.x * blockDim.x; t0 < N; t0 += gridDim.x * blockDim.x) {
+    for (int t0 = bid * blockDim.x; t0 < N; t0 += nb * blockDim.x) {
         for (int k = threadIdx.x; k < kScatterKeys; k += blockDim.x) cnt[k] = 0;
         if (threadIdx.x == 0) s_chunks = 0;
         __syncthreads();
@@ -112,6 +123,83 @@ k_bin_scatter(const int* __restrict__ indptr, int N, int long_min, int chunk,
             }
         }
         __syncthreads();   // cnt / base are reset for the next tile
+    }
+}
+
+__global__ void __launch_bounds__(kScatterThreads)
+k_bin_scatter(const int* __restrict__ indptr, int N, int long_min, int chunk,
+              const int* __restrict__ dense_flag, int* __restrict__ hdr,
+              int* __restrict__ rows, int2* __restrict__ chunks, int2* __restrict__ longs) {
+    bin_scatter_part(indptr, N, long_min, chunk, dense_flag, hdr, rows, chunks, longs, blockIdx.x, gridDim.x);
+}
+
+// Small graphs (N <= kBinSmallRows): one block of kSmallThreads bins every
+// row in one launch.  Each thread keeps kSmallRowsPerThread rows in
+// registers (their indptr loads all in flight at once); counts, offsets and
+// cursors stay in shared memory, and the header is written whole (the same
+// words the three-kernel path leaves), so no memset is needed.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallRowsPerThread = kBinSmallRows / kSmallThreads;
+static_assert(kSmallRowsPerThread * kSmallThreads == kBinSmallRows, "small binning covers kBinSmallRows");
+
+__global__ void __launch_bounds__(kSmallThreads)
+k_bin_small(const int* __restrict__ indptr, int N, int long_min, int chunk, int* __restrict__ hdr,
+            int* __restrict__ rows, int2* __restrict__ chunks, int2* __restrict__ longs) {
+    __shared__ int cnt[kNumBuckets + 1];   // rows per bucket, then split rows
+    __shared__ int off[kNumBuckets];
+    __shared__ int s_chunks, s_max;
+    for (int k = threadIdx.x; k <= kNumBuckets; k += blockDim.x) cnt[k] = 0;
+    if (threadIdx.x == 0) { s_chunks = 0; s_max = 0; }
+    __syncthreads();
+    int beg[kSmallRowsPerThread], deg[kSmallRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kSmallRowsPerThread; ++r) {
+        const int i = threadIdx.x + r * blockDim.x;
+        beg[r] = i < N ? indptr[i] : 0;
+        deg[r] = i < N ? indptr[i + 1] - beg[r] : -1;
+    }
+    int key[kSmallRowsPerThread], pos[kSmallRowsPerThread], c0[kSmallRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kSmallRowsPerThread; ++r) {
+        key[r] = -1;
+        pos[r] = c0[r] = 0;
+        if (deg[r] < 0) continue;
+        atomicMax(&s_max, deg[r]);
+        key[r] = is_long(deg[r], long_min) ? kNumBuckets : bucket_of(deg[r]);
+        pos[r] = atomicAdd(&cnt[key[r]], 1);
+        if (key[r] == kNumBuckets) c0[r] = atomicAdd(&s_chunks, (deg[r] + chunk - 1) / chunk);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {   // bucket lists laid out from the heaviest bucket down
+        int o = 0;
+        for (int b = kNumBuckets - 1; b >= 0; --b) {
+            off[b] = o;
+            o += cnt[b];
+        }
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < HdrLayout::kWords; k += blockDim.x) {
+        int v = 0;
+        if (k == HdrLayout::kLong || k == HdrLayout::kCurLong) v = cnt[kNumBuckets];
+        else if (k == HdrLayout::kChunks || k == HdrLayout::kCurChunk) v = s_chunks;
+        else if (k == HdrLayout::kMaxDeg) v = s_max;
+        else if (k >= HdrLayout::kCount && k < HdrLayout::kCount + kNumBuckets) v = cnt[k - HdrLayout::kCount];
+        else if (k >= HdrLayout::kOffset && k < HdrLayout::kOffset + kNumBuckets) v = off[k - HdrLayout::kOffset];
+        else if (k >= HdrLayout::kCursor && k < HdrLayout::kCursor + kNumBuckets) v = cnt[k - HdrLayout::kCursor];
+        else if (k == HdrLayout::kDenseSeg) v = off[0] + cnt[0];
+        hdr[k] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < kSmallRowsPerThread; ++r) {
+        const int i = threadIdx.x + r * blockDim.x;
+        if (key[r] < 0) continue;
+        if (key[r] < kNumBuckets) {
+            rows[off[key[r]] + pos[r]] = i;
+        } else {
+            longs[pos[r]] = make_int2(i, c0[r]);
+            const int nch = (deg[r] + chunk - 1) / chunk;
+            for (int c = 0; c < nch; ++c) chunks[c0[r] + c] = make_int2(i, beg[r] + c * chunk);
+        }
     }
 }
 static_assert(HdrLayout::kCurLong == HdrLayout::kCursor + kNumBuckets, "cursor layout");
@@ -171,8 +259,15 @@ static int grid_for(int64_t work, int threads) {
     return (int)std::max<int64_t>(1, std::min(blocks, cap));
 }
 
+int bin_launches(int N, const int* dense_flag) { return N <= kBinSmallRows && !dense_flag ? 1 : 3; }
+
 gtattn_status bin_rows(const int* indptr, int N, int long_min, int chunk, const int* dense_flag,
                        int* hdr, int* rows, int2* chunks, int2* longs, cudaStream_t s) {
+    if (N <= kBinSmallRows && !dense_flag) {
+        k_bin_small<<<1, kSmallThreads, 0, s>>>(indptr, N, long_min, chunk, hdr, rows, chunks, longs);
+        GT_CUDA(cudaGetLastError());
+        return GTATTN_OK;
+    }
     GT_CUDA(cudaMemsetAsync(hdr, 0, sizeof(int) * HdrLayout::kWords, s));
     if (N == 0) return GTATTN_OK;
     const int T = 256;

@@ -29,9 +29,13 @@ constexpr int kDefaultChunk = 256;
 void resolve_opts(const gtattn_plan_opts* in, gtattn_plan_opts* out);
 void worst_case_sizes(int64_t N, int64_t nnz, int long_min, int chunk, int64_t* n_long,
                       int64_t* n_chunks);
+// Graphs of at most this many rows are binned by a single block in one launch.
+constexpr int kBinSmallRows = 4096;
 // Bins rows into the given arrays on stream `s` without synchronising:
 // zeroes the header, counts, lays out offsets and scatters rows/chunks.
 gtattn_status bin_rows(const int* indptr, int N, int long_min, int chunk, const int* dense_flag,
                        int* hdr, int* rows, int2* chunks, int2* longs, cudaStream_t s);
+// Kernel launches bin_rows makes for N rows (1 for small graphs, else 3).
+int bin_launches(int N, const int* dense_flag);
 
 }  // namespace gt

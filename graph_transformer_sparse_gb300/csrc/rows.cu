@@ -47,6 +47,7 @@ struct Seg {
 };
 
 constexpr int kMaxSegs = kNumBuckets + 2;
+constexpr float kLazyMax = 8.f;   // fused row kernel: slack of the running maximum (log2 units)
 
 // Builds the task table of a launch in shared memory (one warp).
 // P = edge slots per warp; U = edges per slot per loop iteration.
@@ -368,17 +369,26 @@ k_rows_vec(RowParams p) {
                         if (okc[u]) p.logits[(int64_t)(e0 + u * S) * p.H + head] = l[u] * p.qscale;
                 }
             } else if constexpr (MODE == kFused) {
-                float mx = m;
+                // The running maximum m is raised only when a score exceeds it
+                // by more than kLazyMax (log2 units; the weights stay <= 2^kLazyMax),
+                // and the rescale of the sum and accumulators is skipped when no
+                // lane of the warp raises it -- after a row's first entries,
+                // almost always.
+                float mx = -INFINITY;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     if (!okc[u]) l[u] = -INFINITY;
                     mx = fmaxf(mx, l[u]);
                 }
-                const float mref = (mx == -INFINITY) ? 0.f : mx;
-                const float c = ex2(m - mref);
-                ssum *= c;
+                const bool raise = mx > m + kLazyMax;   // false for mx = -inf
+                if (__any_sync(kFull, raise)) {
+                    const float c = raise ? ex2(m - mx) : 1.f;   // m = -inf: c = 0 (nothing accumulated)
+                    if (raise) m = mx;
+                    ssum *= c;
 #pragma unroll
-                for (int e = 0; e < E; e += 2) scale2(acc[e], acc[e + 1], c);
+                    for (int e = 0; e < E; e += 2) scale2(acc[e], acc[e + 1], c);
+                }
+                const float mref = (m == -INFINITY) ? 0.f : m;
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const float w = ex2(l[u] - mref);
@@ -392,7 +402,6 @@ k_rows_vec(RowParams p) {
                         for (int e = 0; e < E; e += 2) fma2(acc[e], acc[e + 1], w, w, vc[u].get(e), vc[u].get(e + 1));
                     }
                 }
-                m = mx;
             } else {   // kSpmm: weights are the given probabilities
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -923,10 +932,19 @@ static int grid_persistent(K kernel, int threads, size_t smem) {
     return grid;
 }
 
+// The persistent grid, but no more blocks than the tasks can occupy (small
+// graphs: a few blocks instead of several per SM).
+static int grid_for_tasks(int persistent, int task_bound, int warps_per_block) {
+    if (task_bound <= 0) return persistent;
+    const int need = (task_bound + warps_per_block - 1) / warps_per_block;
+    return need < persistent ? need : persistent;
+}
+
 template <typename T, typename TO, int MODE>
 static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
     auto go = [&](auto kernel) {
-        kernel<<<grid_persistent(kernel, kRowThreads, 0), kRowThreads, 0, s>>>(p);
+        const int grid = grid_for_tasks(grid_persistent(kernel, kRowThreads, 0), p.task_bound, kRowThreads / 32);
+        kernel<<<grid, kRowThreads, 0, s>>>(p);
         return cudaGetLastError();
     };
     cudaError_t e;
@@ -952,7 +970,8 @@ static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParam
         return GTATTN_ERR_UNSUPPORTED;
     }
     auto go = [&](auto kernel) {
-        kernel<<<grid_persistent(kernel, kGenWarps * 32, 0), kGenWarps * 32, 0, s>>>(p);
+        const int grid = grid_for_tasks(grid_persistent(kernel, kGenWarps * 32, 0), p.task_bound, kGenWarps);
+        kernel<<<grid, kGenWarps * 32, 0, s>>>(p);
         return cudaGetLastError();
     };
     auto by_kpl = [&](auto kpl4, auto kpl8, auto kpl32) {

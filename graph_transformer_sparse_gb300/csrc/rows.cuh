@@ -20,7 +20,16 @@ struct RowParams {
     int G, lph;             // vector kernel: lanes per feature row, lanes per head
     TaskLists lists;
     Partials part;
+    int task_bound;         // upper bound on the warp tasks of the lists (<= 0: unknown)
 };
+
+// Upper bound on the warp tasks binning makes: a task is one row or more
+// (rows of up to long_min entries), or one chunk of a split row (at most
+// nnz / chunk + 1 per row).
+inline int row_task_bound(int64_t N, int64_t nnz, int chunk) {
+    const int64_t b = N + nnz / (chunk > 0 ? chunk : 1) + 1;
+    return b > 0x7fffffff ? 0x7fffffff : static_cast<int>(b);
+}
 
 enum class RowKernel { kVector, kGeneric };
 

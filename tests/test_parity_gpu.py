@@ -428,3 +428,26 @@ def test_dense_path_large_scores():
     assert plan.info()["device_error"] == 0
     plan.close()
     check_out(w, out_to_numpy(d["out"]), ref, "dense large scores", out32=True)
+
+
+@pytest.mark.parametrize("n", [4096, 4097])
+def test_small_graph_binning_threshold(n):
+    # one-block binning (n <= 4096) and the three-kernel binning (n > 4096),
+    # with hub rows that are split into chunks, empty rows and degree-1 rows
+    rng = np.random.default_rng(n)
+    deg = rng.integers(0, 6, n)
+    deg[rng.choice(n, 6, replace=False)] = [257, 300, 512, 513, 1000, 2500]
+    deg[:3] = [0, 1, 0]
+    indptr = np.zeros(n + 1, np.int64)
+    np.cumsum(deg, out=indptr[1:])
+    indices = rng.integers(0, n, int(indptr[-1])).astype(np.int32)
+    H, D = 2, 16
+    Q, K, V = (rng.standard_normal((n, H, D)).astype(np.float32) for _ in range(3))
+    w = wl.Workload("threshold", n, H, D, "f32", indptr.astype(np.int32), indices, Q, K, V,
+                    float(np.float32(1 / np.sqrt(D))))
+    ref = oracle_rows(w, want_probs=True)
+    for path in ("fwd", "probs", "plan"):
+        got, _, pr = run(w, to_device(w), path)
+        check_out(w, got, ref["out"], f"n={n} {path}")
+        if path == "probs":
+            assert_close(pr, ref["probs"], w.dtype, "probs", PROB_TOL)

@@ -57,8 +57,13 @@ struct HdrLayout {
     static constexpr int kCurDense = kCurChunk + 1;            // cursor: dense rows
     static constexpr int kDenseSeg = kCurDense + 1;            // start of dense segment in row list
     static constexpr int kErr = kDenseSeg + 1;                 // device-side error bits (bounded waits)
+    static constexpr int kBig = kDenseSeg + 2;                 // split rows of more than kBigChunks chunks
+    static constexpr int kCurBig = kDenseSeg + 3;              // cursor: those rows
     static constexpr int kWords = kDenseSeg + 8;
 };
+// Split rows of more than this many chunks are listed first in the split-row
+// list (combined a block per row); the others a warp per row.
+constexpr int kBigChunks = 32;
 
 // Work lists consumed by the row kernels.
 struct TaskLists {

@@ -26,9 +26,9 @@ __device__ __forceinline__ void bin_count_part(const int* __restrict__ indptr, i
                                                const int* __restrict__ dense_flag, int* __restrict__ hdr, int bid,
                                                int nb) {
     __shared__ int hist[kNumBuckets];
-    __shared__ int s_long, s_chunks, s_dense, s_max;
+    __shared__ int s_long, s_chunks, s_dense, s_max, s_big;
     for (int b = threadIdx.x; b < kNumBuckets; b += blockDim.x) hist[b] = 0;
-    if (threadIdx.x == 0) { s_long = 0; s_chunks = 0; s_dense = 0; s_max = 0; }
+    if (threadIdx.x == 0) { s_long = 0; s_chunks = 0; s_dense = 0; s_max = 0; s_big = 0; }
     __syncthreads();
     for (int i = bid * blockDim.x + threadIdx.x; i < N; i += nb * blockDim.x) {
         int deg = indptr[i + 1] - indptr[i];
@@ -36,8 +36,10 @@ __device__ __forceinline__ void bin_count_part(const int* __restrict__ indptr, i
         if (dense_flag && dense_flag[i]) {
             atomicAdd(&s_dense, 1);
         } else if (is_long(deg, long_min)) {
+            const int nch = (deg + chunk - 1) / chunk;
             atomicAdd(&s_long, 1);
-            atomicAdd(&s_chunks, (deg + chunk - 1) / chunk);
+            atomicAdd(&s_chunks, nch);
+            if (nch > kBigChunks) atomicAdd(&s_big, 1);
         } else {
             atomicAdd(&hist[bucket_of(deg)], 1);
         }
@@ -49,6 +51,7 @@ __device__ __forceinline__ void bin_count_part(const int* __restrict__ indptr, i
         if (s_long) atomicAdd(&hdr[HdrLayout::kLong], s_long);
         if (s_chunks) atomicAdd(&hdr[HdrLayout::kChunks], s_chunks);
         if (s_dense) atomicAdd(&hdr[HdrLayout::kDenseRows], s_dense);
+        if (s_big) atomicAdd(&hdr[HdrLayout::kBig], s_big);
         atomicMax(&hdr[HdrLayout::kMaxDeg], s_max);
     }
 }
@@ -77,7 +80,14 @@ __global__ void k_bin_offsets(int* hdr) {
 // global atomic, and rows take their place from shared-memory cursors (about
 // 25 global atomics per 512 rows instead of one per warp and key).
 constexpr int kScatterThreads = 512;
-constexpr int kScatterKeys = kNumBuckets + 3;   // buckets, split rows (NB), dense segment (NB + 2)
+// keys: buckets, split rows of at most kBigChunks chunks (NB), the dense
+// segment (NB + 2), split rows of more chunks (NB + 3); NB + 1 is unused (its
+// cursor word counts chunks)
+constexpr int kKeyBig = kNumBuckets + 3;
+constexpr int kScatterKeys = kNumBuckets + 4;
+__device__ __forceinline__ int cursor_word(int key) {
+    return key == kKeyBig ? HdrLayout::kCurBig : HdrLayout::kCursor + key;
+}
 
 __device__ __forceinline__ void bin_scatter_part(const int* __restrict__ indptr, int N, int long_min, int chunk,
                                                  const int* __restrict__ dense_flag, int* __restrict__ hdr,
@@ -97,26 +107,27 @@ __device__ __forceinline__ void bin_scatter_part(const int* __restrict__ indptr,
             // key: bucket id, NB (split row) or NB+2 (dense segment); the
             // cursors are laid out the same way
             if (dense_flag && dense_flag[i]) key = kNumBuckets + 2;
-            else if (is_long(deg, long_min)) key = kNumBuckets;
+            else if (is_long(deg, long_min)) key = (deg + chunk - 1) / chunk > kBigChunks ? kKeyBig : kNumBuckets;
             else key = bucket_of(deg);
             local = atomicAdd(&cnt[key], 1);
-            if (key == kNumBuckets) {
+            if (key == kNumBuckets || key == kKeyBig) {
                 nch = (deg + chunk - 1) / chunk;
                 chunk_local = atomicAdd(&s_chunks, nch);
             }
         }
         __syncthreads();
         for (int k = threadIdx.x; k < kScatterKeys; k += blockDim.x)
-            if (cnt[k]) base[k] = atomicAdd(&hdr[HdrLayout::kCursor + k], cnt[k]);
+            if (cnt[k]) base[k] = atomicAdd(&hdr[cursor_word(k)], cnt[k]);
         if (threadIdx.x == 0 && s_chunks) s_chunk_base = atomicAdd(&hdr[HdrLayout::kCurChunk], s_chunks);
         __syncthreads();
         if (key >= 0) {
             const int pos = base[key] + local;
             if (key < kNumBuckets) {
                 rows[hdr[HdrLayout::kOffset + key] + pos] = i;
-            } else if (key == kNumBuckets) {
+            } else if (key == kNumBuckets || key == kKeyBig) {
+                // split rows of many chunks first, then the others
                 const int c0 = s_chunk_base + chunk_local;
-                longs[pos] = make_int2(i, c0);
+                longs[key == kKeyBig ? pos : hdr[HdrLayout::kBig] + pos] = make_int2(i, c0);
                 for (int c = 0; c < nch; ++c) chunks[c0 + c] = make_int2(i, beg + c * chunk);
             } else {
                 rows[hdr[HdrLayout::kDenseSeg] + pos] = i;
@@ -145,10 +156,11 @@ static_assert(kSmallRowsPerThread * kSmallThreads == kBinSmallRows, "small binni
 __global__ void __launch_bounds__(kSmallThreads)
 k_bin_small(const int* __restrict__ indptr, int N, int long_min, int chunk, int* __restrict__ hdr,
             int* __restrict__ rows, int2* __restrict__ chunks, int2* __restrict__ longs) {
-    __shared__ int cnt[kNumBuckets + 1];   // rows per bucket, then split rows
+    // rows per bucket, then split rows of at most kBigChunks chunks, then the others
+    __shared__ int cnt[kNumBuckets + 2];
     __shared__ int off[kNumBuckets];
     __shared__ int s_chunks, s_max;
-    for (int k = threadIdx.x; k <= kNumBuckets; k += blockDim.x) cnt[k] = 0;
+    for (int k = threadIdx.x; k < kNumBuckets + 2; k += blockDim.x) cnt[k] = 0;
     if (threadIdx.x == 0) { s_chunks = 0; s_max = 0; }
     __syncthreads();
     int beg[kSmallRowsPerThread], deg[kSmallRowsPerThread];
@@ -165,9 +177,10 @@ k_bin_small(const int* __restrict__ indptr, int N, int long_min, int chunk, int*
         pos[r] = c0[r] = 0;
         if (deg[r] < 0) continue;
         atomicMax(&s_max, deg[r]);
-        key[r] = is_long(deg[r], long_min) ? kNumBuckets : bucket_of(deg[r]);
+        const int nch = (deg[r] + chunk - 1) / chunk;
+        key[r] = is_long(deg[r], long_min) ? (nch > kBigChunks ? kNumBuckets + 1 : kNumBuckets) : bucket_of(deg[r]);
         pos[r] = atomicAdd(&cnt[key[r]], 1);
-        if (key[r] == kNumBuckets) c0[r] = atomicAdd(&s_chunks, (deg[r] + chunk - 1) / chunk);
+        if (key[r] >= kNumBuckets) c0[r] = atomicAdd(&s_chunks, nch);
     }
     __syncthreads();
     if (threadIdx.x == 0) {   // bucket lists laid out from the heaviest bucket down
@@ -180,7 +193,9 @@ k_bin_small(const int* __restrict__ indptr, int N, int long_min, int chunk, int*
     __syncthreads();
     for (int k = threadIdx.x; k < HdrLayout::kWords; k += blockDim.x) {
         int v = 0;
-        if (k == HdrLayout::kLong || k == HdrLayout::kCurLong) v = cnt[kNumBuckets];
+        if (k == HdrLayout::kLong) v = cnt[kNumBuckets] + cnt[kNumBuckets + 1];
+        else if (k == HdrLayout::kCurLong) v = cnt[kNumBuckets];
+        else if (k == HdrLayout::kBig || k == HdrLayout::kCurBig) v = cnt[kNumBuckets + 1];
         else if (k == HdrLayout::kChunks || k == HdrLayout::kCurChunk) v = s_chunks;
         else if (k == HdrLayout::kMaxDeg) v = s_max;
         else if (k >= HdrLayout::kCount && k < HdrLayout::kCount + kNumBuckets) v = cnt[k - HdrLayout::kCount];
@@ -195,8 +210,8 @@ k_bin_small(const int* __restrict__ indptr, int N, int long_min, int chunk, int*
         if (key[r] < 0) continue;
         if (key[r] < kNumBuckets) {
             rows[off[key[r]] + pos[r]] = i;
-        } else {
-            longs[pos[r]] = make_int2(i, c0[r]);
+        } else {   // split rows of many chunks first, then the others
+            longs[key[r] == kNumBuckets + 1 ? pos[r] : cnt[kNumBuckets + 1] + pos[r]] = make_int2(i, c0[r]);
             const int nch = (deg[r] + chunk - 1) / chunk;
             for (int c = 0; c < nch; ++c) chunks[c0[r] + c] = make_int2(i, beg[r] + c * chunk);
         }

@@ -620,10 +620,10 @@ k_rows_generic(RowParams p) {
 // over groups of threads (a group per head for the statistics, per output
 // element for the sums) whose partials meet in shared memory, so a hub row
 // of hundreds of chunks costs a few chunk loads per thread.  Phase 2, a warp
-// per split row of at most kWarpCombineMax chunks (when H divides 32; else
-// phase 1 takes every split row).
+// per split row of at most kBigChunks chunks (when H divides 32; else phase 1
+// takes every split row).  Binning lists the rows of more chunks first, so
+// phase 1 walks only those.
 constexpr int kCombThreads = 512;
-constexpr int kWarpCombineMax = 32;   // split rows up to this many chunks: a warp each (phase 2)
 
 template <typename TO, int MODE>
 __global__ void __launch_bounds__(kCombThreads)
@@ -632,15 +632,15 @@ k_combine(RowParams p, int warp_rows) {
     __shared__ float sS[kGenMaxH];
     __shared__ float red[kCombThreads];
     const int n_long = p.lists.hdr[HdrLayout::kLong];
+    const int n_big = warp_rows ? p.lists.hdr[HdrLayout::kBig] : n_long;   // phase 1 rows: [0, n_big)
     const int H = p.H, D = p.D, HD = p.HD;
     const int t = threadIdx.x;
     TO* __restrict__ O = static_cast<TO*>(p.out);
-    for (int li = blockIdx.x; li < n_long; li += gridDim.x) {
+    for (int li = blockIdx.x; li < n_big; li += gridDim.x) {
         const int2 lr = p.lists.longs[li];
         const int row = lr.x, c0 = lr.y;
         const int deg = p.indptr[row + 1] - p.indptr[row];
         const int nch = (deg + p.lists.chunk_edges - 1) / p.lists.chunk_edges;
-        if (warp_rows && nch <= kWarpCombineMax) continue;   // done by a warp in phase 2
         if (MODE == kFused) {
             // per head: M = max_c m_c, S = sum_c s_c 2^(m_c - M)
             const int G = kCombThreads / H;   // H <= 256: at least two groups
@@ -722,18 +722,17 @@ k_combine(RowParams p, int warp_rows) {
         }
         __syncthreads();
     }
-    // phase 2: rows of at most kWarpCombineMax chunks (most of them), a warp
+    // phase 2: rows of at most kBigChunks chunks (most of them), a warp
     // per row: lanes over (chunk, head) pairs for the statistics (H divides
     // 32), over output elements for the sums
     if (warp_rows) {
         const int lane = t & 31;
         const int warps = gridDim.x * (blockDim.x >> 5);
-        for (int li = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); li < n_long; li += warps) {
+        for (int li = n_big + blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); li < n_long; li += warps) {
             const int2 lr = p.lists.longs[li];
             const int row = lr.x, c0 = lr.y;
             const int deg = p.indptr[row + 1] - p.indptr[row];
-            const int nch = (deg + p.lists.chunk_edges - 1) / p.lists.chunk_edges;
-            if (nch > kWarpCombineMax) continue;
+            const int nch = (deg + p.lists.chunk_edges - 1) / p.lists.chunk_edges;   // <= kBigChunks
             // lane l: head l % H, chunks l / H, l / H + 32 / H, ...; lanes H
             // apart combine, so lane h < H ends with head h's (M, S)
             float M = -INFINITY, S = 0.f;

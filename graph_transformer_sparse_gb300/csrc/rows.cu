@@ -813,6 +813,121 @@ k_softmax_short(const int* __restrict__ indptr, const int* __restrict__ hdr, con
     }
 }
 
+// Ordinary rows when H divides 32: a lane group of gs lanes per row (gs a
+// power of two and a multiple of H, sized to the widest row of the bucket,
+// at most 32), rows of a bucket side by side, 32/gs rows per warp.  A row's
+// logits are contiguous (entry-major, head-minor), so element j belongs to
+// lane j % gs and head j % H: the group reads the row coalesced and reduces
+// each head's maximum and sum over its lanes with xor shuffles.  Rows of at
+// most gs elements (most rows of a sparse graph) are held in registers: one
+// load and one expf per element; longer rows take three coalesced walks.
+struct SmaxSeg {
+    int first_task, list_begin, count, gs;
+};
+
+__global__ void __launch_bounds__(256)
+k_softmax_rows(const int* __restrict__ indptr, const int* __restrict__ hdr, const int* __restrict__ rows,
+               int H, const float* __restrict__ logits, float* __restrict__ probs) {
+    __shared__ SmaxSeg segs[kNumBuckets];
+    __shared__ int s_nseg, s_total;
+    if (threadIdx.x == 0) {
+        int t = 0, k = 0;
+        for (int b = kNumBuckets - 1; b >= 0; --b) {
+            const int cnt = hdr[HdrLayout::kCount + b];
+            if (cnt == 0) continue;
+            const int lb = b - kExactBuckets;
+            const int64_t hi = b < kExactBuckets ? b : (lb < kLogBuckets - 1 ? log_bucket_hi(lb) : 0x7fffffff);
+            int gs = H;
+            while (gs < 32 && gs < hi * H) gs <<= 1;
+            segs[k++] = SmaxSeg{t, hdr[HdrLayout::kOffset + b], cnt, gs};
+            t += (cnt + 32 / gs - 1) / (32 / gs);
+        }
+        s_nseg = k;
+        s_total = t;
+    }
+    __syncthreads();
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    int sidx = 0;
+    for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < s_total; t += gridDim.x * wpb) {
+        while (sidx + 1 < s_nseg && segs[sidx + 1].first_task <= t) ++sidx;
+        const SmaxSeg sg = segs[sidx];
+        const int gs = sg.gs, grp = lane / gs, lig = lane - grp * gs;
+        const int pos = (t - sg.first_task) * (32 / gs) + grp;
+        int beg = 0, n = 0;
+        if (pos < sg.count) {
+            const int row = rows[sg.list_begin + pos];
+            beg = indptr[row];
+            n = (indptr[row + 1] - beg) * H;
+        }
+        const float* lr = logits + static_cast<int64_t>(beg) * H;
+        float* pr = probs + static_cast<int64_t>(beg) * H;
+        const bool inreg = n <= gs;   // the row fits the group: one element per lane
+        const float x0 = lig < n ? lr[lig] : -INFINITY;
+        float m = x0;
+        if (!inreg)
+            for (int j = lig + gs; j < n; j += gs) m = fmaxf(m, lr[j]);
+        for (int o = H; o < gs; o <<= 1) m = fmaxf(m, __shfl_xor_sync(full, m, o));
+        const float e0 = lig < n ? expf(x0 - m) : 0.f;
+        float sum = e0;
+        if (!inreg)
+            for (int j = lig + gs; j < n; j += gs) sum += expf(lr[j] - m);
+        for (int o = H; o < gs; o <<= 1) sum += __shfl_xor_sync(full, sum, o);
+        const float inv = 1.f / sum;
+        if (lig < n) pr[lig] = e0 * inv;
+        if (!inreg)
+            for (int j = lig + gs; j < n; j += gs) pr[j] = expf(lr[j] - m) * inv;
+    }
+}
+
+// Split rows' chunks when H divides 32: a warp per chunk, lanes over the
+// chunk's contiguous (entry, head) logits (element j: head j % H), heads
+// reduced over lanes H apart.  Step 1: the chunk's (M_c, S_c) per head.
+__global__ void __launch_bounds__(256)
+k_softmax_chunk_stats_w(const int* __restrict__ indptr, const int* __restrict__ hdr, const int2* __restrict__ chunks,
+                        int chunk_edges, int H, const float* __restrict__ logits, Partials part) {
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+    const int n_chunks = hdr[HdrLayout::kChunks];
+    for (int c = blockIdx.x * wpb + (threadIdx.x >> 5); c < n_chunks; c += gridDim.x * wpb) {
+        const int2 ck = chunks[c];
+        const int n = (min(ck.y + chunk_edges, indptr[ck.x + 1]) - ck.y) * H;
+        const float* lr = logits + static_cast<int64_t>(ck.y) * H;
+        float m = -INFINITY;
+        for (int j = lane; j < n; j += 32) m = fmaxf(m, lr[j]);
+        for (int o = H; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(full, m, o));
+        float sum = 0.f;
+        for (int j = lane; j < n; j += 32) sum += expf(lr[j] - m);
+        for (int o = H; o < 32; o <<= 1) sum += __shfl_xor_sync(full, sum, o);
+        if (lane < H) {
+            part.m[static_cast<int64_t>(c) * H + lane] = m;
+            part.s[static_cast<int64_t>(c) * H + lane] = sum;
+        }
+    }
+}
+
+// Step 3 (H divides 32), a warp per chunk: p = exp(l - M) / S with the row's
+// (M, 1/S) from its first chunk.
+__global__ void __launch_bounds__(256)
+k_softmax_chunk_write_w(const int* __restrict__ indptr, const int* __restrict__ hdr, const int2* __restrict__ chunks,
+                        int chunk_edges, int H, const float* __restrict__ logits, float* __restrict__ probs,
+                        Partials part) {
+    const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+    const int n_chunks = hdr[HdrLayout::kChunks];
+    for (int c = blockIdx.x * wpb + (threadIdx.x >> 5); c < n_chunks; c += gridDim.x * wpb) {
+        const int2 ck = chunks[c];
+        const int rbeg = indptr[ck.x];
+        const int n = (min(ck.y + chunk_edges, indptr[ck.x + 1]) - ck.y) * H;
+        const int c0 = c - (ck.y - rbeg) / chunk_edges;
+        const int h = lane % H;   // the head of every element this lane touches
+        const float M = part.m[static_cast<int64_t>(c0) * H + h], inv = part.s[static_cast<int64_t>(c0) * H + h];
+        const float* lr = logits + static_cast<int64_t>(ck.y) * H;
+        float* pr = probs + static_cast<int64_t>(ck.y) * H;
+        for (int j = lane; j < n; j += 32) pr[j] = expf(lr[j] - M) * inv;
+    }
+}
+
 // Split rows, in their chunks (a thread per (chunk, head)): step 1, each
 // chunk's maximum M_c and sum S_c = sum exp(l - M_c) into the partials.
 __global__ void __launch_bounds__(256)
@@ -1023,13 +1138,25 @@ gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cud
 gtattn_status launch_edge_softmax(const int* indptr, int N, int H, const TaskLists& L, const Partials& part,
                                   const float* logits, float* probs, cudaStream_t s) {
     if (N == 0) return GTATTN_OK;
-    k_softmax_short<<<grid_persistent(k_softmax_short, 256, 0), 256, 0, s>>>(indptr, L.hdr, L.rows, H, logits, probs);
-    k_softmax_chunk_stats<<<grid_persistent(k_softmax_chunk_stats, 256, 0), 256, 0, s>>>(
-        indptr, L.hdr, L.chunks, L.chunk_edges, H, logits, part);
+    if (32 % H == 0)
+        k_softmax_rows<<<grid_persistent(k_softmax_rows, 256, 0), 256, 0, s>>>(indptr, L.hdr, L.rows, H, logits, probs);
+    else
+        k_softmax_short<<<grid_persistent(k_softmax_short, 256, 0), 256, 0, s>>>(indptr, L.hdr, L.rows, H, logits,
+                                                                                  probs);
+    if (32 % H == 0)
+        k_softmax_chunk_stats_w<<<grid_persistent(k_softmax_chunk_stats_w, 256, 0), 256, 0, s>>>(
+            indptr, L.hdr, L.chunks, L.chunk_edges, H, logits, part);
+    else
+        k_softmax_chunk_stats<<<grid_persistent(k_softmax_chunk_stats, 256, 0), 256, 0, s>>>(
+            indptr, L.hdr, L.chunks, L.chunk_edges, H, logits, part);
     k_softmax_long_merge<<<grid_persistent(k_softmax_long_merge, 256, 0), 256, 0, s>>>(
         indptr, L.hdr, L.longs, L.chunk_edges, H, part);
-    k_softmax_chunk_write<<<grid_persistent(k_softmax_chunk_write, 256, 0), 256, 0, s>>>(
-        indptr, L.hdr, L.chunks, L.chunk_edges, H, logits, probs, part);
+    if (32 % H == 0)
+        k_softmax_chunk_write_w<<<grid_persistent(k_softmax_chunk_write_w, 256, 0), 256, 0, s>>>(
+            indptr, L.hdr, L.chunks, L.chunk_edges, H, logits, probs, part);
+    else
+        k_softmax_chunk_write<<<grid_persistent(k_softmax_chunk_write, 256, 0), 256, 0, s>>>(
+            indptr, L.hdr, L.chunks, L.chunk_edges, H, logits, probs, part);
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
 }

@@ -451,3 +451,33 @@ def test_small_graph_binning_threshold(n):
         check_out(w, got, ref["out"], f"n={n} {path}")
         if path == "probs":
             assert_close(pr, ref["probs"], w.dtype, "probs", PROB_TOL)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_wide_logit_range_raises_running_max(dtype):
+    # logits spread over tens of log2 units inside rows, in random order: the
+    # row kernels' running maximum (raised only past a slack) moves mid-row,
+    # in whole rows, in split rows' chunks and across edge slots
+    rng = np.random.default_rng(21)
+    n, H, D = 3000, 4, 32
+    deg = rng.integers(1, 48, n)
+    deg[rng.choice(n, 20, replace=False)] = rng.integers(257, 1500, 20)
+    indptr = np.zeros(n + 1, np.int64)
+    np.cumsum(deg, out=indptr[1:])
+    indices = rng.integers(0, n, int(indptr[-1]))
+    Q = rng.standard_normal((n, H, D))
+    K = rng.standard_normal((n, H, D)) * np.linspace(0.2, 4.0, n)[:, None, None]
+    V = rng.standard_normal((n, H, D))
+    w = _mk(indptr, indices, Q, K, V, dtype)
+    # the spread this gives, in log2 units, inside the longer rows
+    dst = np.repeat(np.arange(n), deg)
+    lg = np.einsum("ehd,ehd->eh", w.Q[dst].astype(np.float64), w.K[w.indices].astype(np.float64)) * w.scale
+    spans = [np.ptp(lg[indptr[r]:indptr[r + 1]]) * np.log2(np.e) for r in range(n) if deg[r] >= 20]
+    assert np.median(spans) > 16
+    ref = oracle_rows(w, want_probs=True)
+    for path, kw in (("fwd", {}), ("plan", dict(long_row_min=8, chunk_edges=5)), ("probs", {})):
+        d = to_device(w, out32=(dtype == "bf16"))
+        got, _, pr = run(w, d, path, **kw)
+        check_out(w, got, ref["out"], f"wide logits {path}", out32=True)
+        if path == "probs":
+            assert_close(pr, ref["probs"], w.dtype, "probs", PROB_TOL)

@@ -37,6 +37,18 @@
  *  - the max is subtracted before exp (does not change the result);
  *  - no dropout (evaluation mode).
  *
+ * Optional per-edge additive bias (the Graphormer spatial encoding):
+ *   e_ij = q_i . k_j / sqrt(d_k) + b_{d(i,j)}
+ *     -- "Graph Transformer theory, derivation and implementation", section
+ *        "shortest-path bias and degree encoding (Graphormer type)",
+ *        subsection "spatial encoding: shortest-path distance bias" (a
+ *        learnable scalar per distance, optionally per head, added to the
+ *        logit before the softmax; b_inf = -inf removes a pair).
+ *   Reading: the caller supplies the bias already looked up per CSR entry
+ *   and head, bias[e*H + h] (float32, promoted to double); it is added to
+ *   scale * (q . k).  A row whose logits are all -inf (every entry removed)
+ *   gives exact zeros, like a row with no entries, and probabilities 0.
+ *
  * Arithmetic: inputs are float32 (bf16 inputs arrive as their exact float32
  * widening), every operation is double, the reductions run in index order,
  * exp is the C library's double exp.  Two passes per (row, head): logits and
@@ -70,13 +82,14 @@ int gto_check_csr(int64_t N, int64_t nnz, const int32_t* indptr, const int32_t* 
  *   Q, K, V : float32 [N, H, D] row-major (D innermost).
  *   rows    : the rows to compute (NULL: rows 0..N-1, then nrows must be N).
  *   out     : double [nrows, H, D], row r of the list at out + r*H*D.
+ *   bias    : float32 [nnz, H] added to the logits, or NULL for none.
  *   logits, probs : double [nnz, H] indexed by CSR position (may be NULL);
  *             only the entries of the listed rows are written.
  * Returns 0, or a negative code for bad arguments / bad CSR / no memory.
  */
 int gto_sparse_mha_rows(int64_t N, int64_t nnz, int32_t H, int32_t D,
                         const int32_t* indptr, const int32_t* indices,
-                        const float* Q, const float* K, const float* V, double scale,
+                        const float* Q, const float* K, const float* V, const float* bias, double scale,
                         const int64_t* rows, int64_t nrows,
                         double* out, double* logits, double* probs)
 {
@@ -116,7 +129,13 @@ int gto_sparse_mha_rows(int64_t N, int64_t nnz, int32_t H, int32_t D,
                 double dot = 0.0;
                 for (int32_t d = 0; d < D; ++d) dot += (double)q[d] * (double)kj[d];
                 l[k] = scale * dot;
+                if (bias) l[k] += (double)bias[(beg + k) * H + h];
                 if (l[k] > m) m = l[k];
+            }
+            if (m == -INFINITY) {                         /* every entry removed: zeros */
+                if (logits) for (int64_t k = 0; k < deg; ++k) logits[(beg + k) * H + h] = l[k];
+                if (probs) for (int64_t k = 0; k < deg; ++k) probs[(beg + k) * H + h] = 0.0;
+                continue;
             }
             /* pass 2: softmax weights over the row's stored entries */
             double S = 0.0;

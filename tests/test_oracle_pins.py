@@ -76,6 +76,29 @@ def brute_force(src, dst, n, Q, K, V, scale):
     return out
 
 
+def brute_force_bias(indptr, indices, n, Q, K, V, scale, bias):
+    """Dense route with a per-edge additive bias: B[h, i, j] = bias of the
+    entry j -> i (graphs without duplicate entries), non-edges -inf; logits
+    scale * q_i.k_j + B, row softmax, times V; rows whose logits are all
+    -inf give 0."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (Q, K, V))
+    H = q.shape[1]
+    B = np.full((H, n, n), -np.inf)
+    dst = np.repeat(np.arange(n), np.diff(indptr))
+    for e in range(len(indices)):
+        B[:, dst[e], indices[e]] = np.asarray(bias, dtype=np.float64)[e]
+    logits = scale * np.einsum("ihd,jhd->hij", q, k) + B
+    out = np.zeros_like(q)
+    for h in range(H):
+        for i in range(n):
+            row = logits[h, i]
+            if not np.isfinite(row).any():
+                continue
+            w = np.exp(row - row[np.isfinite(row)].max())
+            out[i, h] = (w / w.sum()) @ v[:, h]
+    return out
+
+
 def _csr_coo(indptr, indices):
     dst = np.repeat(np.arange(len(indptr) - 1), np.diff(indptr))
     return np.asarray(indices, dtype=np.int64), dst
@@ -312,18 +335,18 @@ def _compile_mutant(src_text, tmpdir, name):
     subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", path, "-o", so, "-lm"], check=True)
     lib = ctypes.CDLL(so)
     i64, i32, vp, dbl = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_double
-    lib.gto_sparse_mha_rows.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, dbl, vp, i64, vp, vp, vp]
+    lib.gto_sparse_mha_rows.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, dbl, vp, i64, vp, vp, vp]
     lib.gto_sparse_mha_rows.restype = ctypes.c_int
     return lib
 
 
-def _run_mutant(lib, indptr, indices, Q, K, V, scale):
+def _run_mutant(lib, indptr, indices, Q, K, V, scale, bias=None):
     N, H, D = Q.shape
     out = np.zeros((N, H, D))
-    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    p = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
     indptr = np.ascontiguousarray(indptr, np.int32)
     indices = np.ascontiguousarray(indices, np.int32)
-    rc = lib.gto_sparse_mha_rows(N, int(indptr[-1]), H, D, p(indptr), p(indices), p(Q), p(K), p(V),
+    rc = lib.gto_sparse_mha_rows(N, int(indptr[-1]), H, D, p(indptr), p(indices), p(Q), p(K), p(V), p(bias),
                                  float(scale), None, N, p(out), None, None)
     assert rc == 0
     return out
@@ -346,4 +369,119 @@ def test_pins_catch_planted_mistakes(name):
     with tempfile.TemporaryDirectory() as td:
         lib = _compile_mutant(mutant, td, name)
         got = _run_mutant(lib, indptr, indices, Q, K, V, 0.7)
+    assert not np.allclose(got, ref, rtol=1e-9, atol=1e-12), f"pin missed mutation {name}"
+
+
+# --------------------------------------------------------------------------
+# per-edge additive bias (Graphormer spatial encoding)
+# --------------------------------------------------------------------------
+def _bias_graph(rng, n, e, H, D):
+    pick = rng.choice(n * n, size=e, replace=False)
+    indptr, indices = wl.csr_by_destination(pick // n, pick % n, n)
+    Q, K, V = _rand_feats(rng, n, H, D)
+    return indptr, indices, Q, K, V
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_bias_brute_force(seed):
+    rng = np.random.default_rng(300 + seed)
+    n, H, D = int(rng.integers(3, 40)), int(rng.integers(1, 5)), int(rng.integers(1, 9))
+    indptr, indices, Q, K, V = _bias_graph(rng, n, int(rng.integers(1, n * n // 2 + 1)), H, D)
+    bias = (rng.standard_normal((len(indices), H)) * 2).astype(np.float32)
+    bias[rng.random(bias.shape) < 0.15] = -np.inf          # some pairs removed
+    scale = float(np.float32(1 / math.sqrt(D)))
+    got = oracle.sparse_mha(indptr, indices, Q, K, V, scale, bias=bias)["out"]
+    ref = brute_force_bias(indptr, indices, n, Q, K, V, scale, bias)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_zero_bias_is_no_bias():
+    rng = np.random.default_rng(310)
+    indptr, indices, Q, K, V = _bias_graph(rng, 30, 300, 3, 8)
+    a = oracle.sparse_mha(indptr, indices, Q, K, V, 0.35, want_probs=True)
+    b = oracle.sparse_mha(indptr, indices, Q, K, V, 0.35, want_probs=True,
+                          bias=np.zeros((len(indices), 3), np.float32))
+    for key in ("out", "logits", "probs"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_row_constant_bias_cancels():
+    # softmax is shift-invariant: a bias constant over a row's entries (per head)
+    # changes the logits but not the probabilities or the output
+    rng = np.random.default_rng(311)
+    n, H = 30, 3
+    indptr, indices, Q, K, V = _bias_graph(rng, n, 320, H, 8)
+    c = rng.standard_normal((n, H)).astype(np.float32) * 3
+    bias = np.repeat(c, np.diff(indptr), axis=0)
+    a = oracle.sparse_mha(indptr, indices, Q, K, V, 0.35, want_probs=True)
+    b = oracle.sparse_mha(indptr, indices, Q, K, V, 0.35, want_probs=True, bias=bias)
+    np.testing.assert_allclose(b["out"], a["out"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b["probs"], a["probs"], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(b["logits"] - a["logits"], bias.astype(np.float64), rtol=0, atol=1e-12)
+
+
+def test_minus_inf_bias_removes_entries():
+    # b = -inf removes the pair: the same as deleting those CSR entries; a row
+    # with every entry removed gives zeros and probabilities 0
+    rng = np.random.default_rng(312)
+    n, H = 25, 2
+    indptr, indices, Q, K, V = _bias_graph(rng, n, 200, H, 6)
+    deg = np.diff(indptr)
+    keep = rng.random(len(indices)) < 0.6
+    row_of = np.repeat(np.arange(n), deg)
+    full_row = int(np.argmax(deg))
+    keep[row_of == full_row] = False                         # one row loses every entry
+    bias = np.where(keep[:, None], 0.0, -np.inf).astype(np.float32).repeat(H, axis=1)
+    got = oracle.sparse_mha(indptr, indices, Q, K, V, 0.4, want_probs=True, bias=bias)
+    kept_ptr = np.zeros(n + 1, np.int64)
+    np.cumsum(np.bincount(row_of[keep], minlength=n), out=kept_ptr[1:])
+    ref = oracle.sparse_mha(kept_ptr.astype(np.int32), indices[keep], Q, K, V, 0.4, want_probs=True)
+    np.testing.assert_allclose(got["out"], ref["out"], rtol=1e-12, atol=1e-14)
+    assert np.all(got["out"][full_row] == 0.0)
+    assert np.all(got["probs"][~keep] == 0.0)
+    np.testing.assert_allclose(got["probs"][keep], ref["probs"], rtol=1e-12, atol=1e-15)
+
+
+def test_log_weight_bias_with_zero_query_is_weighted_mean():
+    # q = 0: the logit is the bias alone, so b = ln w gives out = sum w v / sum w
+    rng = np.random.default_rng(313)
+    n, H, D = 20, 2, 4
+    indptr, indices, Q, K, V = _bias_graph(rng, n, 150, H, D)
+    Q[:] = 0
+    w = rng.uniform(0.1, 5.0, (len(indices), H))
+    got = oracle.sparse_mha(indptr, indices, Q, K, V, 0.5, bias=np.log(w).astype(np.float32))["out"]
+    wf = np.exp(np.log(w).astype(np.float32).astype(np.float64))
+    ref = np.zeros((n, H, D))
+    for i in range(n):
+        b, e = indptr[i], indptr[i + 1]
+        if e > b:
+            for h in range(H):
+                ref[i, h] = (wf[b:e, h, None] * V[indices[b:e], h].astype(np.float64)).sum(0) / wf[b:e, h].sum()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+BIAS_MUTATIONS = {
+    "bias_sign": ("if (bias) l[k] += (double)bias[(beg + k) * H + h];",
+                  "if (bias) l[k] -= (double)bias[(beg + k) * H + h];"),
+    "bias_transposed_index": ("if (bias) l[k] += (double)bias[(beg + k) * H + h];",
+                              "if (bias) l[k] += (double)bias[(int64_t)h * nnz + beg + k];"),
+    "bias_scaled_with_dot": ("if (bias) l[k] += (double)bias[(beg + k) * H + h];",
+                             "if (bias) l[k] += scale * (double)bias[(beg + k) * H + h];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BIAS_MUTATIONS))
+def test_bias_pins_catch_planted_mistakes(name):
+    text = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    old, new = BIAS_MUTATIONS[name]
+    assert text.count(old) == 1, f"anchor for {name} missing"
+    mutant = text.replace(old, new, 1)
+    rng = np.random.default_rng(4321)
+    n, H, D = 17, 3, 5
+    indptr, indices, Q, K, V = _bias_graph(rng, n, 90, H, D)
+    bias = (rng.standard_normal((len(indices), H)) * 3).astype(np.float32)
+    ref = brute_force_bias(indptr, indices, n, Q, K, V, 0.7, bias)
+    with tempfile.TemporaryDirectory() as td:
+        lib = _compile_mutant(mutant, td, name)
+        got = _run_mutant(lib, indptr, indices, Q, K, V, 0.7, bias)
     assert not np.allclose(got, ref, rtol=1e-9, atol=1e-12), f"pin missed mutation {name}"

@@ -7,7 +7,7 @@ row kernel, the split-row combine) over the whole R-MAT graph (2^20 nodes,
 JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--path fwd|plan|probs] [--impl ours|reference]
+                    [--path fwd|plan|probs|bias] [--impl ours|reference]
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload
 (weak scaling, no collective on the data path); the timed region is
@@ -214,6 +214,10 @@ def make_step(w, d, path, gt, plan=None, probs_bufs=None):
         lg, pr = probs_bufs
         return lambda: gt.gtattn_fwd_probs(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], lg, pr,
                                            w.N, w.nnz, w.H, w.D, w.scale, dt)
+    if path == "bias":
+        (bias,) = probs_bufs
+        return lambda: gt.gtattn_fwd_bias(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], bias, d["out"],
+                                          w.N, w.nnz, w.H, w.D, w.scale, dt)
     raise ValueError(path)
 
 
@@ -242,6 +246,10 @@ def run_gpu_workload(w, path, steps, warmup, gt, dev, flush, want_profile=True, 
         plan = gt.Plan(d["indptr"], d["indices"], detect_dense=detect_dense)
     if path == "probs":
         probs_bufs = (torch.empty(w.nnz, w.H, device=dev), torch.empty(w.nnz, w.H, device=dev))
+    if path == "bias":   # per-edge, per-head additive bias: seeded N(0, 1), fp32 [nnz, H]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(12345)
+        probs_bufs = (torch.randn(w.nnz, w.H, device=dev, generator=gen),)
     step = make_step(w, d, path, gt, plan, probs_bufs)
     if soak_s > 0:   # untimed load so the clock record covers a loaded GPU
         t0 = time.perf_counter()
@@ -358,6 +366,8 @@ def gpu_arm(args):
     value, worst_ms, _ = job_throughput(units, local_ms)
     ms_per_step = worst_ms / args.steps
     cbytes = compulsory_bytes(w.N, w.nnz, w.H, w.D, esize)
+    if args.path == "bias":
+        cbytes += 4 * w.nnz * w.H   # the fp32 bias, read once per entry and head
     ubytes = unique_bytes(w.N, w.nnz, w.H, w.D, esize)
 
     launches_per_step = sum(v["launches"] for v in prof.values()) / args.steps
@@ -379,7 +389,7 @@ def gpu_arm(args):
         achieved = cbytes / (kern_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "kernel": "k_rows_vec (fused row kernel)", "achieved": round(achieved, 1),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                    "traffic": ncu_traffic("k_rows_vec", name),
+                    "traffic": ncu_traffic("k_rows_vec", name) if args.path == "fwd" else None,
                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
                     if peaks["source"] == "measured" else "fallback 6.8 TB/s",
                     "algorithmic_bytes_per_launch": cbytes, "unique_bytes_floor": ubytes,
@@ -412,7 +422,7 @@ def gpu_arm(args):
     if rank == 0 and not args.no_extra:
         extra = {}
         for other, pth in (("erdos_renyi", "fwd"), ("molecules", "fwd"), ("tiny_random", "fwd"),
-                           ("dense_blocks", "plan"), ("rmat", "probs")):
+                           ("dense_blocks", "plan"), ("rmat", "probs"), ("rmat", "bias")):
             if other == name and pth == args.path:
                 continue
             try:
@@ -425,6 +435,8 @@ def gpu_arm(args):
             ms = statistics.median(t_o)
             es = 2 if wo.dtype == "bf16" else 4
             cb = compulsory_bytes(wo.N, wo.nnz, wo.H, wo.D, es)
+            if pth == "bias":
+                cb += 4 * wo.nnz * wo.H   # the fp32 bias, read once per entry and head
             ent = {"ms": round(ms, 5), "edge_heads_per_s": round(wo.nnz * wo.H / (ms / 1e3), 1),
                    "gbs_compulsory": round(cb / (ms / 1e3) / 1e9, 1),
                    "hbm_frac": round(cb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -490,7 +502,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="rmat", choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs"])
+    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias"])
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up (clock record under load)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")

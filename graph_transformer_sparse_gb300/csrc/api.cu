@@ -237,9 +237,11 @@ extern "C" gtattn_status gtattn_profile_read(gtattn_profile* out, int reset) {
     return st;
 }
 
-extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indices, const void* Q,
-                                    const void* K, const void* V, void* out, int64_t N, int64_t nnz,
-                                    int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
+// The fused forward on the fly (binning, fused rows, combine), with an
+// optional per-entry additive bias.
+static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                               const void* V, const float* bias, void* out, int64_t N, int64_t nnz, int H, int D,
+                               float scale, gtattn_dtype dtype, cudaStream_t stream) {
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
     RowChoice c;
     if (!choose_row_kernel(H, D, dtype, Q, K, V, out, GTATTN_KERNEL_AUTO, &c)) return GTATTN_ERR_UNSUPPORTED;
@@ -257,6 +259,7 @@ extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indice
         st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
     }
     RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale * kLog2e, c, sc.lists, sc.part);
+    p.bias = bias;
     if (st == GTATTN_OK) {
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
         st = launch_rows(kFused, dtype, c, p, stream);
@@ -267,6 +270,12 @@ extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indice
     }
     pool_free(sc.base, stream);
     return st;
+}
+
+extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indices, const void* Q,
+                                    const void* K, const void* V, void* out, int64_t N, int64_t nnz,
+                                    int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
+    return fwd_fused(indptr, indices, Q, K, V, nullptr, out, N, nnz, H, D, scale, dtype, stream);
 }
 
 extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t* indptr,
@@ -322,10 +331,12 @@ extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t*
     return st;
 }
 
-extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* indices, const void* Q,
-                                          const void* K, const void* V, void* out, float* logits,
-                                          float* probs, int64_t N, int64_t nnz, int H, int D, float scale,
-                                          gtattn_dtype dtype, cudaStream_t stream) {
+// The unfused trio (SDDMM, edge softmax, SpMM), with an optional per-entry
+// additive bias in the SDDMM.
+static gtattn_status fwd_unfused(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                                 const void* V, const float* bias, void* out, float* logits, float* probs,
+                                 int64_t N, int64_t nnz, int H, int D, float scale, gtattn_dtype dtype,
+                                 cudaStream_t stream) {
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
     if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(probs)) & 3u)
         return GTATTN_ERR_INVALID_ARG;
@@ -349,6 +360,7 @@ extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* 
     RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, c, sc.lists, sc.part);
     p.logits = lg;
     p.probs = pr;
+    p.bias = bias;
     // (1) SDDMM: logits
     if (st == GTATTN_OK && nnz > 0) {
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
@@ -370,4 +382,21 @@ extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* 
     }
     pool_free(sc.base, stream);
     return st;
+}
+
+extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* indices, const void* Q,
+                                          const void* K, const void* V, void* out, float* logits,
+                                          float* probs, int64_t N, int64_t nnz, int H, int D, float scale,
+                                          gtattn_dtype dtype, cudaStream_t stream) {
+    return fwd_unfused(indptr, indices, Q, K, V, nullptr, out, logits, probs, N, nnz, H, D, scale, dtype, stream);
+}
+
+extern "C" gtattn_status gtattn_fwd_bias(const int32_t* indptr, const int32_t* indices, const void* Q,
+                                         const void* K, const void* V, const float* bias, void* out,
+                                         float* logits, float* probs, int64_t N, int64_t nnz, int H, int D,
+                                         float scale, gtattn_dtype dtype, cudaStream_t stream) {
+    if ((nnz > 0 && !bias) || (reinterpret_cast<uintptr_t>(bias) & 3u)) return GTATTN_ERR_INVALID_ARG;
+    if (logits || probs)
+        return fwd_unfused(indptr, indices, Q, K, V, bias, out, logits, probs, N, nnz, H, D, scale, dtype, stream);
+    return fwd_fused(indptr, indices, Q, K, V, bias, out, N, nnz, H, D, scale, dtype, stream);
 }

@@ -206,7 +206,8 @@ constexpr int rows_min_blocks() {
     return VPL == 1 ? GT_ROWS_MIN_BLOCKS1 : VPL == 2 ? GT_ROWS_MIN_BLOCKS2 : 4;
 }
 
-template <typename T, typename TO, int VPL, int MODE>
+// BIAS: the logits get p.bias[e*H + h] added (fused and SDDMM modes).
+template <typename T, typename TO, int VPL, int MODE, bool BIAS = false>
 __global__ void __launch_bounds__(kRowThreads, rows_min_blocks<T, VPL>())
 k_rows_vec(RowParams p) {
     using F = Frag<T, VPL>;
@@ -276,6 +277,14 @@ k_rows_vec(RowParams p) {
                 float x[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e) x[e] = fv.get(e);
+                if constexpr (BIAS) {
+                    // the weight is 1 for a finite bias, 0 for -inf (the entry
+                    // removed: a zero row), NaN for NaN or +inf
+                    const float b = __ldg(p.bias + static_cast<int64_t>(cur.beg) * p.H + head);
+                    const float wgt = b == -INFINITY ? 0.f : (b - b) + 1.f;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) x[e] *= wgt;
+                }
                 store_frag<TO, E>(O + (int64_t)cur.row * HD + lane_off, x);
             }
             continue;
@@ -313,10 +322,12 @@ k_rows_vec(RowParams p) {
         int jn[U];
         bool okc[U];
         F kc[U], vc[U];
+        float bc[U];   // bias of the current iteration's entries (BIAS)
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int e = beg + u * S + sl;
             okc[u] = e < end;
+            if constexpr (BIAS) bc[u] = okc[u] ? __ldg(p.bias + static_cast<int64_t>(e) * p.H + head) : 0.f;
             const int j = okc[u] ? __ldg(p.indices + e) : 0;
             if (kNeedK) { if (okc[u]) kc[u].load(K + (int64_t)j * HD + lane_off); else kc[u].zero(); }
             if (kNeedV) { if (okc[u]) vc[u].load(V + (int64_t)j * HD + lane_off); else vc[u].zero(); }
@@ -328,10 +339,12 @@ k_rows_vec(RowParams p) {
             // issue iteration it+1's gathers and iteration it+2's indices
             bool okn[U];
             F kn[U], vn[U];
+            float bn[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int e1 = e0 + step + u * S;
                 okn[u] = e1 < end;
+                if constexpr (BIAS) bn[u] = okn[u] ? __ldg(p.bias + static_cast<int64_t>(e1) * p.H + head) : 0.f;
                 if (kNeedK) { if (okn[u]) kn[u].load(K + (int64_t)jn[u] * HD + lane_off); else kn[u].zero(); }
                 if (kNeedV) { if (okn[u]) vn[u].load(V + (int64_t)jn[u] * HD + lane_off); else vn[u].zero(); }
                 const int e2 = e1 + step;
@@ -361,12 +374,16 @@ k_rows_vec(RowParams p) {
 #pragma unroll
                 for (int u = 0; u < U; ++u)
                     for (int o = 1; o < p.lph; o <<= 1) l[u] += __shfl_xor_sync(kFull, l[u], o);
+                if constexpr (BIAS && MODE == kFused) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) l[u] = fmaf(bc[u], kLog2e, l[u]);   // logits in log2 units
+                }
             }
             if constexpr (MODE == kSddmm) {
                 if (gl % p.lph == 0) {
 #pragma unroll
                     for (int u = 0; u < U; ++u)
-                        if (okc[u]) p.logits[(int64_t)(e0 + u * S) * p.H + head] = l[u] * p.qscale;
+                        if (okc[u]) p.logits[(int64_t)(e0 + u * S) * p.H + head] = BIAS ? fmaf(l[u], p.qscale, bc[u]) : l[u] * p.qscale;
                 }
             } else if constexpr (MODE == kFused) {
                 // The running maximum m is raised only when a score exceeds it
@@ -421,6 +438,7 @@ k_rows_vec(RowParams p) {
                 okc[u] = okn[u];
                 kc[u] = kn[u];
                 vc[u] = vn[u];
+                if constexpr (BIAS) bc[u] = bn[u];
             }
         }
         if constexpr (MODE != kSddmm) {
@@ -555,12 +573,15 @@ k_rows_generic(RowParams p) {
                     l = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
                 }
                 if constexpr (MODE == kSddmm) {
-                    p.logits[(int64_t)e * H + h] = l * p.qscale;
+                    p.logits[(int64_t)e * H + h] = p.bias ? fmaf(l, p.qscale, p.bias[(int64_t)e * H + h])
+                                                          : l * p.qscale;
                 } else if constexpr (MODE == kFused) {
+                    if (p.bias) l = fmaf(p.bias[(int64_t)e * H + h], kLog2e, l);   // log2 units
                     const float mo = hm[h];
                     const float mn = fmaxf(mo, l);
-                    const float c = ex2(mo - mn);
-                    const float w = ex2(l - mn);
+                    const float mref = mn == -INFINITY ? 0.f : mn;   // no finite logit yet
+                    const float c = ex2(mo - mref);
+                    const float w = ex2(l - mref);
                     hs[h] = hs[h] * c + w;
                     hm[h] = mn;
                     hc[h] = c;
@@ -653,7 +674,7 @@ k_combine(RowParams p, int warp_rows) {
             if (t < H) {
                 float M = -INFINITY;
                 for (int k = 0; k < G; ++k) M = fmaxf(M, red[k * H + t]);
-                sM[t] = M;
+                sM[t] = M == -INFINITY ? 0.f : M;   // no finite logit in the row: a zero row
             }
             __syncthreads();
             float sum = 0.f;
@@ -703,7 +724,7 @@ k_combine(RowParams p, int warp_rows) {
             if (t < HD) {
                 float tot = 0.f;
                 for (int k = 0; k < Ge; ++k) tot += red[k * HD + t];
-                if (MODE == kFused) tot /= sS[h];
+                if (MODE == kFused) tot = sS[h] > 0.f ? tot / sS[h] : 0.f;
                 store_elem(O, (int64_t)row * HD + t, tot);
             }
         } else {
@@ -716,7 +737,7 @@ k_combine(RowParams p, int warp_rows) {
                     const float a = p.part.acc[(int64_t)(c0 + c) * HD + el];
                     v += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M) : a;
                 }
-                if (MODE == kFused) v /= sS[h];
+                if (MODE == kFused) v = sS[h] > 0.f ? v / sS[h] : 0.f;
                 store_elem(O, (int64_t)row * HD + el, v);
             }
         }
@@ -740,6 +761,7 @@ k_combine(RowParams p, int warp_rows) {
                 const int h = lane % H, step = 32 / H;
                 for (int c = lane / H; c < nch; c += step) M = fmaxf(M, p.part.m[(int64_t)(c0 + c) * H + h]);
                 for (int o = H; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+                if (M == -INFINITY) M = 0.f;   // no finite logit in the row: a zero row
                 for (int c = lane / H; c < nch; c += step) {
                     const int64_t k = (int64_t)(c0 + c) * H + h;
                     S += p.part.s[k] * ex2(p.part.m[k] - M);
@@ -767,7 +789,7 @@ k_combine(RowParams p, int warp_rows) {
                         v4[0] += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - Mh) : a;
                     }
                     float v = (v4[0] + v4[1]) + (v4[2] + v4[3]);
-                    if (MODE == kFused) v /= Sh;
+                    if (MODE == kFused) v = Sh > 0.f ? v / Sh : 0.f;
                     store_elem(O, (int64_t)row * HD + el, v);
                 }
             }
@@ -806,9 +828,10 @@ k_softmax_short(const int* __restrict__ indptr, const int* __restrict__ hdr, con
         float* pr = probs + (int64_t)beg * H + h;
         float m = -INFINITY;
         for (int e = 0; e < deg; ++e) m = fmaxf(m, lr[(int64_t)e * H]);
+        if (m == -INFINITY) m = 0.f;   // every logit -inf (entries removed): probabilities 0
         float sum = 0.f;
         for (int e = 0; e < deg; ++e) sum += expf(lr[(int64_t)e * H] - m);
-        const float inv = 1.f / sum;
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
         for (int e = 0; e < deg; ++e) pr[(int64_t)e * H] = expf(lr[(int64_t)e * H] - m) * inv;
     }
 }
@@ -869,12 +892,13 @@ k_softmax_rows(const int* __restrict__ indptr, const int* __restrict__ hdr, cons
         if (!inreg)
             for (int j = lig + gs; j < n; j += gs) m = fmaxf(m, lr[j]);
         for (int o = H; o < gs; o <<= 1) m = fmaxf(m, __shfl_xor_sync(full, m, o));
+        if (m == -INFINITY) m = 0.f;   // every logit -inf (entries removed): probabilities 0
         const float e0 = lig < n ? expf(x0 - m) : 0.f;
         float sum = e0;
         if (!inreg)
             for (int j = lig + gs; j < n; j += gs) sum += expf(lr[j] - m);
         for (int o = H; o < gs; o <<= 1) sum += __shfl_xor_sync(full, sum, o);
-        const float inv = 1.f / sum;
+        const float inv = sum > 0.f ? 1.f / sum : 0.f;
         if (lig < n) pr[lig] = e0 * inv;
         if (!inreg)
             for (int j = lig + gs; j < n; j += gs) pr[j] = expf(lr[j] - m) * inv;
@@ -897,8 +921,9 @@ k_softmax_chunk_stats_w(const int* __restrict__ indptr, const int* __restrict__ 
         float m = -INFINITY;
         for (int j = lane; j < n; j += 32) m = fmaxf(m, lr[j]);
         for (int o = H; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(full, m, o));
+        const float mref = m == -INFINITY ? 0.f : m;   // every logit -inf: S_c = 0
         float sum = 0.f;
-        for (int j = lane; j < n; j += 32) sum += expf(lr[j] - m);
+        for (int j = lane; j < n; j += 32) sum += expf(lr[j] - mref);
         for (int o = H; o < 32; o <<= 1) sum += __shfl_xor_sync(full, sum, o);
         if (lane < H) {
             part.m[static_cast<int64_t>(c) * H + lane] = m;
@@ -942,8 +967,9 @@ k_softmax_chunk_stats(const int* __restrict__ indptr, const int* __restrict__ hd
         const float* lr = logits + (int64_t)beg * H + h;
         float m = -INFINITY;
         for (int e = 0; e < n; ++e) m = fmaxf(m, lr[(int64_t)e * H]);
+        const float mref = m == -INFINITY ? 0.f : m;   // every logit -inf: S_c = 0
         float sum = 0.f;
-        for (int e = 0; e < n; ++e) sum += expf(lr[(int64_t)e * H] - m);
+        for (int e = 0; e < n; ++e) sum += expf(lr[(int64_t)e * H] - mref);
         part.m[t] = m;
         part.s[t] = sum;
     }
@@ -964,13 +990,14 @@ k_softmax_long_merge(const int* __restrict__ indptr, const int* __restrict__ hdr
         const int nch = (deg + chunk_edges - 1) / chunk_edges;
         float M = -INFINITY;
         for (int c = 0; c < nch; ++c) M = fmaxf(M, part.m[(int64_t)(lg.y + c) * H + h]);
+        if (M == -INFINITY) M = 0.f;   // every logit -inf (entries removed): probabilities 0
         float S = 0.f;
         for (int c = 0; c < nch; ++c) {
             const int64_t k = (int64_t)(lg.y + c) * H + h;
             S += part.s[k] * expf(part.m[k] - M);
         }
         part.m[(int64_t)lg.y * H + h] = M;
-        part.s[(int64_t)lg.y * H + h] = 1.f / S;
+        part.s[(int64_t)lg.y * H + h] = S > 0.f ? 1.f / S : 0.f;
     }
 }
 
@@ -1054,7 +1081,7 @@ static int grid_for_tasks(int persistent, int task_bound, int warps_per_block) {
     return need < persistent ? need : persistent;
 }
 
-template <typename T, typename TO, int MODE>
+template <typename T, typename TO, int MODE, bool BIAS = false>
 static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
     auto go = [&](auto kernel) {
         const int grid = grid_for_tasks(grid_persistent(kernel, kRowThreads, 0), p.task_bound, kRowThreads / 32);
@@ -1063,10 +1090,10 @@ static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
     };
     cudaError_t e;
     switch (vpl) {
-        case 1: e = go(k_rows_vec<T, TO, 1, MODE>); break;
-        case 2: e = go(k_rows_vec<T, TO, 2, MODE>); break;
+        case 1: e = go(k_rows_vec<T, TO, 1, MODE, BIAS>); break;
+        case 2: e = go(k_rows_vec<T, TO, 2, MODE, BIAS>); break;
         case 4:
-            if constexpr (sizeof(T) == 4) { e = go(k_rows_vec<T, TO, 4, MODE>); break; }
+            if constexpr (sizeof(T) == 4) { e = go(k_rows_vec<T, TO, 4, MODE, BIAS>); break; }
             return GTATTN_ERR_UNSUPPORTED;
         default: return GTATTN_ERR_UNSUPPORTED;
     }
@@ -1076,10 +1103,13 @@ static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
 template <typename T, typename TO>
 static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParams& p, cudaStream_t s) {
     if (c.kind == RowKernel::kVector) {
+        const bool bias = p.bias != nullptr;
         switch (mode) {
-            case kFused: return launch_vec_t<T, TO, kFused>(c.vpl, p, s);
+            case kFused:
+                return bias ? launch_vec_t<T, TO, kFused, true>(c.vpl, p, s) : launch_vec_t<T, TO, kFused>(c.vpl, p, s);
             case kSpmm: return launch_vec_t<T, TO, kSpmm>(c.vpl, p, s);
-            case kSddmm: return launch_vec_t<T, TO, kSddmm>(c.vpl, p, s);
+            case kSddmm:
+                return bias ? launch_vec_t<T, TO, kSddmm, true>(c.vpl, p, s) : launch_vec_t<T, TO, kSddmm>(c.vpl, p, s);
         }
         return GTATTN_ERR_UNSUPPORTED;
     }

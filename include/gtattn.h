@@ -202,6 +202,28 @@ gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* indices, co
                                float scale, gtattn_dtype dtype, cudaStream_t stream);
 
 /*
+ * gtattn_fwd_bias -- the forward with a per-edge, per-head additive bias on
+ * the logits: e = scale * q_i.k_j + bias[e, h] ("Graph Transformer theory,
+ * derivation and implementation", section on the shortest-path bias and
+ * degree encoding (Graphormer type), spatial encoding: e_ij = q_i.k_j /
+ * sqrt(d_k) + b_d(i,j), optionally one bias per head; b = -inf removes the
+ * pair).  The caller looks the bias up per CSR entry.
+ *   bias:   fp32 [nnz, H] in CSR order, device memory, 4-byte aligned
+ *           (required when nnz > 0; entries may be -inf).
+ *   logits, probs: as gtattn_fwd_probs; logits include the bias.  When both
+ *           are NULL the fused kernels run (no per-edge values in memory),
+ *           else the unfused trio.
+ *   Other arguments and errors: as gtattn_fwd; INVALID_ARG for a missing or
+ *   misaligned bias.
+ * A row whose logits are all -inf (every entry removed) gives zeros, like a
+ * row without entries, and probabilities 0.
+ */
+gtattn_status gtattn_fwd_bias(const int32_t* indptr, const int32_t* indices, const void* Q,
+                              const void* K, const void* V, const float* bias, void* out,
+                              float* logits, float* probs, int64_t N, int64_t nnz, int H, int D,
+                              float scale, gtattn_dtype dtype, cudaStream_t stream);
+
+/*
  * gtattn_fwd_noalloc -- gtattn_fwd without any allocation.  The pages have
  * no counterpart: this exists for callers that cannot allocate device memory
  * when they run attention -- code running inside an allocator or memory-pool

@@ -401,7 +401,8 @@ def gpu_arm(args):
         "config": {"workload": f"{name}: {w.desc}", "N": w.N, "nnz": w.nnz, "H": w.H, "D": w.D,
                    "path": {"fwd": "gtattn_fwd (binning on the fly + fused rows + combine)",
                             "plan": "gtattn_fwd_plan (prebuilt plan)",
-                            "probs": "gtattn_fwd_probs (unfused SDDMM/softmax/SpMM)"}[args.path],
+                            "probs": "gtattn_fwd_probs (unfused SDDMM/softmax/SpMM)",
+                            "bias": "gtattn_fwd_bias (fused, per-edge per-head additive bias, fp32 N(0,1))"}[args.path],
                    "l2": "flushed before every timed step (512 MiB memset, outside the events)",
                    "clock_soak": f"{args.soak:g} s of untimed steps before the warm-up; clocks sampled from "
                                  f"then to the end",

@@ -49,6 +49,19 @@ struct Seg {
 constexpr int kMaxSegs = kNumBuckets + 2;
 constexpr float kLazyMax = 8.f;   // fused row kernel: slack of the running maximum (log2 units)
 
+// Loads of data read once per call (the bias, and with GT_STREAM_HINTS the
+// indices and Q rows) use the streaming cache policy (evict first), so they
+// do not push the reused K/V rows out of the L2.
+__device__ __forceinline__ float ld_stream(const float* p) { return __ldcs(p); }
+__device__ __forceinline__ int ld_stream(const int* p) { return __ldcs(p); }
+#ifndef GT_STREAM_HINTS
+#define GT_STREAM_HINTS 0
+#endif
+__device__ __forceinline__ int ld_index(const int* p) {
+    if constexpr (GT_STREAM_HINTS) return __ldcs(p);
+    else return __ldg(p);
+}
+
 // Builds the task table of a launch in shared memory (one warp).
 // P = edge slots per warp; U = edges per slot per loop iteration.
 __device__ void build_segments(const TaskLists& L, int P, int U, Seg* segs, int* nseg, int* total,
@@ -107,6 +120,14 @@ struct Frag {
 #pragma unroll
         for (int k = 0; k < VPL; ++k) v[k] = __ldg(q + k);
     }
+    __device__ __forceinline__ void load_once(const T* p) {   // read once per call (Q rows)
+        const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            if constexpr (GT_STREAM_HINTS) v[k] = __ldcs(q + k);
+            else v[k] = __ldg(q + k);
+        }
+    }
     __device__ __forceinline__ void zero() {
 #pragma unroll
         for (int k = 0; k < VPL; ++k) v[k] = make_uint4(0, 0, 0, 0);
@@ -161,13 +182,20 @@ __device__ __forceinline__ void store_frag(T* p, const float* x) {
     if constexpr (sizeof(T) == 4) {
         float4* q = reinterpret_cast<float4*>(p);
 #pragma unroll
-        for (int k = 0; k < E / 4; ++k) q[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+        for (int k = 0; k < E / 4; ++k) {
+            const float4 v = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+            if constexpr (GT_STREAM_HINTS) __stcs(q + k, v);
+            else q[k] = v;
+        }
     } else {
         uint4* q = reinterpret_cast<uint4*>(p);
 #pragma unroll
-        for (int k = 0; k < E / 8; ++k)
-            q[k] = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
-                              pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+        for (int k = 0; k < E / 8; ++k) {
+            const uint4 v = make_uint4(pack_bf16x2(x[8 * k], x[8 * k + 1]), pack_bf16x2(x[8 * k + 2], x[8 * k + 3]),
+                                       pack_bf16x2(x[8 * k + 4], x[8 * k + 5]), pack_bf16x2(x[8 * k + 6], x[8 * k + 7]));
+            if constexpr (GT_STREAM_HINTS) __stcs(q + k, v);
+            else q[k] = v;
+        }
     }
 }
 
@@ -271,7 +299,7 @@ k_rows_vec(RowParams p) {
         if (MODE == kFused && sg.kind == kSegCopy) {   // uniform over the warp (one task)
             // a row of one entry: its softmax weight is 1, out = V[j]
             if (cur.valid) {
-                const int j = __ldg(p.indices + cur.beg);
+                const int j = ld_index(p.indices + cur.beg);
                 F fv;
                 fv.load(V + (int64_t)j * HD + lane_off);
                 float x[E];
@@ -302,7 +330,7 @@ k_rows_vec(RowParams p) {
         float q[E];          // fp32 inputs: q pre-scaled
         F fq;                // bf16 inputs: q kept packed, the scale multiplies the dot
         if constexpr (MODE != kSpmm) {
-            if (valid) fq.load(Q + (int64_t)row * HD + lane_off); else fq.zero();
+            if (valid) fq.load_once(Q + (int64_t)row * HD + lane_off); else fq.zero();
             if constexpr (!kBf16) {
                 const float qs = MODE == kFused ? p.qscale : 1.f;   // SDDMM scales at the store
 #pragma unroll
@@ -322,17 +350,23 @@ k_rows_vec(RowParams p) {
         int jn[U];
         bool okc[U];
         F kc[U], vc[U];
-        float bc[U];   // bias of the current iteration's entries (BIAS)
+        // bias (BIAS): like the indices it comes from DRAM (read once, in CSR
+        // order), so it is fetched two iterations ahead: bc for iteration it,
+        // bx for it+1
+        float bc[U], bx[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int e = beg + u * S + sl;
             okc[u] = e < end;
-            if constexpr (BIAS) bc[u] = okc[u] ? __ldg(p.bias + static_cast<int64_t>(e) * p.H + head) : 0.f;
-            const int j = okc[u] ? __ldg(p.indices + e) : 0;
+            if constexpr (BIAS) {
+                bc[u] = okc[u] ? ld_stream(p.bias + static_cast<int64_t>(e) * p.H + head) : 0.f;
+                bx[u] = e + step < end ? ld_stream(p.bias + static_cast<int64_t>(e + step) * p.H + head) : 0.f;
+            }
+            const int j = okc[u] ? ld_index(p.indices + e) : 0;
             if (kNeedK) { if (okc[u]) kc[u].load(K + (int64_t)j * HD + lane_off); else kc[u].zero(); }
             if (kNeedV) { if (okc[u]) vc[u].load(V + (int64_t)j * HD + lane_off); else vc[u].zero(); }
             const int e1 = e + step;
-            jn[u] = e1 < end ? __ldg(p.indices + e1) : 0;
+            jn[u] = e1 < end ? ld_index(p.indices + e1) : 0;
         }
         for (int it = 0; it < n_iter; ++it) {
             const int e0 = beg + it * step + sl;
@@ -344,11 +378,15 @@ k_rows_vec(RowParams p) {
             for (int u = 0; u < U; ++u) {
                 const int e1 = e0 + step + u * S;
                 okn[u] = e1 < end;
-                if constexpr (BIAS) bn[u] = okn[u] ? __ldg(p.bias + static_cast<int64_t>(e1) * p.H + head) : 0.f;
+                if constexpr (BIAS) {
+                    bn[u] = bx[u];
+                    const int e2b = e1 + step;
+                    bx[u] = e2b < end ? ld_stream(p.bias + static_cast<int64_t>(e2b) * p.H + head) : 0.f;
+                }
                 if (kNeedK) { if (okn[u]) kn[u].load(K + (int64_t)jn[u] * HD + lane_off); else kn[u].zero(); }
                 if (kNeedV) { if (okn[u]) vn[u].load(V + (int64_t)jn[u] * HD + lane_off); else vn[u].zero(); }
                 const int e2 = e1 + step;
-                jn[u] = e2 < end ? __ldg(p.indices + e2) : 0;
+                jn[u] = e2 < end ? ld_index(p.indices + e2) : 0;
             }
             float l[U];
             if constexpr (kNeedK) {

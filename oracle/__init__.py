@@ -53,7 +53,7 @@ def _load():
             i64, i32, vp, dbl = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_double
             lib.gto_check_csr.argtypes = [i64, i64, vp, vp]
             lib.gto_check_csr.restype = ctypes.c_int
-            lib.gto_sparse_mha_rows.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, dbl,
+            lib.gto_sparse_mha_rows.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, dbl,
                                                 vp, i64, vp, vp, vp]
             lib.gto_sparse_mha_rows.restype = ctypes.c_int
             lib.gto_dense_attention.argtypes = [i64, i32, i32, vp, vp, vp, dbl, vp]
@@ -79,7 +79,7 @@ def check_csr(indptr, indices, n: int) -> bool:
 
 
 def sparse_mha(indptr, indices, Q, K, V, scale, rows=None, want_probs=False,
-               threads: int = 1, bias=None):
+               threads: int = 1, bias=None, values=None):
     """Sparse MHA forward in fp64.
 
     ``indptr`` int32 [N+1], ``indices`` int32 [nnz] (CSR by destination),
@@ -92,6 +92,8 @@ def sparse_mha(indptr, indices, Q, K, V, scale, rows=None, want_probs=False,
     same single-threaded C routine on a contiguous slice of rows).
     ``bias``: optional float32 [nnz, H] added to each logit (per-edge,
     per-head additive bias; -inf removes an entry).
+    ``values``: optional float32 [nnz], the weighted adjacency's stored
+    values; each logit is scale * (q.k * value).
     """
     lib = _load()
     indptr = np.ascontiguousarray(indptr, dtype=np.int32)
@@ -105,6 +107,10 @@ def sparse_mha(indptr, indices, Q, K, V, scale, rows=None, want_probs=False,
         bias = np.ascontiguousarray(bias, dtype=np.float32)
         if bias.shape != (nnz, H):
             raise OracleError(f"bias must be [nnz, H] = {(nnz, H)}, got {bias.shape}")
+    if values is not None:
+        values = np.ascontiguousarray(values, dtype=np.float32)
+        if values.shape != (nnz,):
+            raise OracleError(f"values must be [nnz] = {(nnz,)}, got {values.shape}")
     if rows is None:
         rows_arr = np.arange(N, dtype=np.int64)
     else:
@@ -117,7 +123,7 @@ def sparse_mha(indptr, indices, Q, K, V, scale, rows=None, want_probs=False,
 
     def run(r0, r1):
         rc = lib.gto_sparse_mha_rows(
-            N, nnz, H, D, _ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(bias), s,
+            N, nnz, H, D, _ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(values), _ptr(bias), s,
             _ptr(rows_arr[r0:r1]), r1 - r0, _ptr(out[r0:r1]),
             _ptr(logits), _ptr(probs))
         if rc != 0:

@@ -27,7 +27,8 @@
  *  - the softmax runs over the stored entries of the row only; non-edges are
  *    excluded (weight 0, i.e. logit -inf as in the same page's shortest-path
  *    bias section, b_inf = -inf), not treated as logit 0;
- *  - A is binary (the spmatrix is built from an edge list with no values);
+ *  - A is binary (the spmatrix is built from an edge list with no values)
+ *    unless the caller passes its stored values (below);
  *  - row i lists the nodes j it attends to (CSR by destination: node i
  *    aggregates over its in-edges j -> i);
  *  - a row with no entries gives exact zeros;
@@ -48,6 +49,15 @@
  *   and head, bias[e*H + h] (float32, promoted to double); it is added to
  *   scale * (q . k).  A row whose logits are all -inf (every entry removed)
  *   gives exact zeros, like a row with no entries, and probabilities 0.
+ *
+ * Optional weighted adjacency:
+ *   SparseAttn(Q, K, V, A) = softmax(((Q K^T) o A) / sqrt(d)) V, A in [0,1]^{NxN}
+ *     -- "Graph Transformer in a Nutshell", section "Sparse Multi-head
+ *        Attention" (the Hadamard product with A's values).
+ *   Reading: values[e] (float32, one per CSR entry, shared by the heads) is
+ *   A's stored value; the logit is scale * ((q . k) * values[e]); the
+ *   softmax still runs over the stored entries only (a stored 0 gives
+ *   logit 0, it does not remove the entry).
  *
  * Arithmetic: inputs are float32 (bf16 inputs arrive as their exact float32
  * widening), every operation is double, the reductions run in index order,
@@ -82,6 +92,7 @@ int gto_check_csr(int64_t N, int64_t nnz, const int32_t* indptr, const int32_t* 
  *   Q, K, V : float32 [N, H, D] row-major (D innermost).
  *   rows    : the rows to compute (NULL: rows 0..N-1, then nrows must be N).
  *   out     : double [nrows, H, D], row r of the list at out + r*H*D.
+ *   values  : float32 [nnz], A's stored values (weighted A), or NULL (binary A).
  *   bias    : float32 [nnz, H] added to the logits, or NULL for none.
  *   logits, probs : double [nnz, H] indexed by CSR position (may be NULL);
  *             only the entries of the listed rows are written.
@@ -89,7 +100,8 @@ int gto_check_csr(int64_t N, int64_t nnz, const int32_t* indptr, const int32_t* 
  */
 int gto_sparse_mha_rows(int64_t N, int64_t nnz, int32_t H, int32_t D,
                         const int32_t* indptr, const int32_t* indices,
-                        const float* Q, const float* K, const float* V, const float* bias, double scale,
+                        const float* Q, const float* K, const float* V, const float* values,
+                        const float* bias, double scale,
                         const int64_t* rows, int64_t nrows,
                         double* out, double* logits, double* probs)
 {
@@ -128,6 +140,7 @@ int gto_sparse_mha_rows(int64_t N, int64_t nnz, int32_t H, int32_t D,
                 const float* kj = K + j * HD + (int64_t)h * D;
                 double dot = 0.0;
                 for (int32_t d = 0; d < D; ++d) dot += (double)q[d] * (double)kj[d];
+                if (values) dot *= (double)values[beg + k];
                 l[k] = scale * dot;
                 if (bias) l[k] += (double)bias[(beg + k) * H + h];
                 if (l[k] > m) m = l[k];

@@ -335,18 +335,18 @@ def _compile_mutant(src_text, tmpdir, name):
     subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", path, "-o", so, "-lm"], check=True)
     lib = ctypes.CDLL(so)
     i64, i32, vp, dbl = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_double
-    lib.gto_sparse_mha_rows.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, dbl, vp, i64, vp, vp, vp]
+    lib.gto_sparse_mha_rows.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, dbl, vp, i64, vp, vp, vp]
     lib.gto_sparse_mha_rows.restype = ctypes.c_int
     return lib
 
 
-def _run_mutant(lib, indptr, indices, Q, K, V, scale, bias=None):
+def _run_mutant(lib, indptr, indices, Q, K, V, scale, bias=None, values=None):
     N, H, D = Q.shape
     out = np.zeros((N, H, D))
     p = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
     indptr = np.ascontiguousarray(indptr, np.int32)
     indices = np.ascontiguousarray(indices, np.int32)
-    rc = lib.gto_sparse_mha_rows(N, int(indptr[-1]), H, D, p(indptr), p(indices), p(Q), p(K), p(V), p(bias),
+    rc = lib.gto_sparse_mha_rows(N, int(indptr[-1]), H, D, p(indptr), p(indices), p(Q), p(K), p(V), p(values), p(bias),
                                  float(scale), None, N, p(out), None, None)
     assert rc == 0
     return out
@@ -484,4 +484,101 @@ def test_bias_pins_catch_planted_mistakes(name):
     with tempfile.TemporaryDirectory() as td:
         lib = _compile_mutant(mutant, td, name)
         got = _run_mutant(lib, indptr, indices, Q, K, V, 0.7, bias)
+    assert not np.allclose(got, ref, rtol=1e-9, atol=1e-12), f"pin missed mutation {name}"
+
+
+# --------------------------------------------------------------------------
+# weighted adjacency: logits scale * (q.k * a_e)
+# --------------------------------------------------------------------------
+def brute_force_weighted(indptr, indices, n, Q, K, V, scale, values):
+    """Dense route: A[i, j] = stored value of the entry j -> i (no duplicate
+    entries), logits scale * (q_i.k_j) * A[i, j] on stored entries, the others
+    -inf, row softmax, times V; rows without entries give 0."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (Q, K, V))
+    A = np.zeros((n, n))
+    M = np.zeros((n, n), bool)
+    dst = np.repeat(np.arange(n), np.diff(indptr))
+    A[dst, indices] = np.asarray(values, dtype=np.float64)
+    M[dst, indices] = True
+    logits = scale * np.einsum("ihd,jhd->hij", q, k) * A[None]
+    logits[:, ~M] = -np.inf
+    out = np.zeros_like(q)
+    has = M.any(1)
+    lg = logits[:, has, :]
+    w = np.exp(lg - lg.max(axis=2, keepdims=True))
+    out[has] = np.einsum("hij,jhd->ihd", w / w.sum(axis=2, keepdims=True), v)
+    return out
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_weighted_brute_force(seed):
+    rng = np.random.default_rng(400 + seed)
+    n, H, D = int(rng.integers(3, 40)), int(rng.integers(1, 5)), int(rng.integers(1, 9))
+    indptr, indices, Q, K, V = _bias_graph(rng, n, int(rng.integers(1, n * n // 2 + 1)), H, D)
+    values = rng.uniform(0.0, 1.0, len(indices)).astype(np.float32)
+    values[rng.random(len(values)) < 0.1] = 0.0                # stored zeros stay in the softmax
+    scale = float(np.float32(1 / math.sqrt(D)))
+    got = oracle.sparse_mha(indptr, indices, Q, K, V, scale, values=values)["out"]
+    ref = brute_force_weighted(indptr, indices, n, Q, K, V, scale, values)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_unit_values_are_binary_adjacency():
+    rng = np.random.default_rng(410)
+    indptr, indices, Q, K, V = _bias_graph(rng, 30, 300, 3, 8)
+    a = oracle.sparse_mha(indptr, indices, Q, K, V, 0.35, want_probs=True)
+    b = oracle.sparse_mha(indptr, indices, Q, K, V, 0.35, want_probs=True,
+                          values=np.ones(len(indices), np.float32))
+    for key in ("out", "logits", "probs"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_zero_values_give_neighbour_mean():
+    # every stored value 0: every logit 0, uniform weights over the stored entries
+    rng = np.random.default_rng(411)
+    n, H, D = 25, 2, 5
+    indptr, indices, Q, K, V = _bias_graph(rng, n, 200, H, D)
+    got = oracle.sparse_mha(indptr, indices, Q, K, V, 0.5, values=np.zeros(len(indices), np.float32))["out"]
+    ref = np.zeros((n, H, D))
+    for i in range(n):
+        if indptr[i + 1] > indptr[i]:
+            ref[i] = V[indices[indptr[i]:indptr[i + 1]]].astype(np.float64).mean(0)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_constant_values_rescale_the_logits():
+    # A = c on every stored entry: the same as the binary graph with scale * c
+    rng = np.random.default_rng(412)
+    indptr, indices, Q, K, V = _bias_graph(rng, 30, 280, 3, 6)
+    c = np.float32(0.375)
+    got = oracle.sparse_mha(indptr, indices, Q, K, V, 0.5, values=np.full(len(indices), c))["out"]
+    ref = oracle.sparse_mha(indptr, indices, Q, K, V, 0.5 * float(c))["out"]
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+WEIGHT_MUTATIONS = {
+    "value_of_source_node": ("if (values) dot *= (double)values[beg + k];",
+                             "if (values) dot *= (double)values[indices[beg + k] % (int64_t)nnz];"),
+    "value_added": ("if (values) dot *= (double)values[beg + k];",
+                    "if (values) dot += (double)values[beg + k];"),
+    "zero_value_removes_entry": ("if (values) dot *= (double)values[beg + k];",
+                                 "if (values) dot = values[beg + k] == 0.0f ? -INFINITY : dot * (double)values[beg + k];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(WEIGHT_MUTATIONS))
+def test_weight_pins_catch_planted_mistakes(name):
+    text = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    old, new = WEIGHT_MUTATIONS[name]
+    assert text.count(old) == 1, f"anchor for {name} missing"
+    mutant = text.replace(old, new, 1)
+    rng = np.random.default_rng(4322)
+    n, H, D = 17, 3, 5
+    indptr, indices, Q, K, V = _bias_graph(rng, n, 90, H, D)
+    values = rng.uniform(0.0, 1.0, len(indices)).astype(np.float32)
+    values[::7] = 0.0
+    ref = brute_force_weighted(indptr, indices, n, Q, K, V, 0.7, values)
+    with tempfile.TemporaryDirectory() as td:
+        lib = _compile_mutant(mutant, td, name)
+        got = _run_mutant(lib, indptr, indices, Q, K, V, 0.7, values=values)
     assert not np.allclose(got, ref, rtol=1e-9, atol=1e-12), f"pin missed mutation {name}"

@@ -21,7 +21,7 @@ import threading
 from ._build import LIB, build
 
 __all__ = [
-    "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs", "gtattn_fwd_bias",
+    "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs", "gtattn_fwd_bias", "gtattn_fwd_weighted",
     "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_csr_build", "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
     "gtattn_csr_validate", "gtattn_status_string", "gtattn_profile_enable", "gtattn_profile_read",
     "sparse_mha", "GTATTN_F32", "GTATTN_BF16", "GTATTN_BF16_OUT_F32",
@@ -37,7 +37,7 @@ EXPORTED_SYMBOLS = (
     "gtattn_status_string", "gtattn_last_error", "gtattn_csr_build", "gtattn_plan_destroy",
     "gtattn_plan_get_info", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
     "gtattn_coo_to_csr", "gtattn_csr_validate", "gtattn_profile_enable", "gtattn_profile_read",
-    "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_bias",
+    "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_bias", "gtattn_fwd_weighted",
 )
 KCAT_NAMES = ("bin", "rows", "combine", "softmax", "dense")
 
@@ -100,6 +100,7 @@ def load(path: str | None = None):
             "gtattn_fwd_plan": ([vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp], i32),
             "gtattn_fwd_probs": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
             "gtattn_fwd_bias": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
+            "gtattn_fwd_weighted": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
             "gtattn_coo_to_csr": ([vp, vp, i64, i64, vp, vp, vp], i32),
             "gtattn_csr_validate": ([vp, vp, i64, i64, vp], i32),
             "gtattn_fwd_noalloc": ([vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
@@ -225,6 +226,15 @@ def gtattn_fwd_bias(indptr, indices, Q, K, V, bias, out, N, nnz, H, D, scale, dt
     _check(load().gtattn_fwd_bias(_ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(bias), _ptr(out),
                                   _ptr(logits), _ptr(probs), int(N), int(nnz), int(H), int(D), float(scale),
                                   int(dtype), _stream(stream)), "gtattn_fwd_bias")
+
+
+def gtattn_fwd_weighted(indptr, indices, values, Q, K, V, out, N, nnz, H, D, scale, dtype, logits=None, probs=None,
+                        stream=None):
+    """Forward on a weighted adjacency (values: fp32 [nnz] device tensor, A's
+    stored values); logits/probs (optional) select the unfused path."""
+    _check(load().gtattn_fwd_weighted(_ptr(indptr), _ptr(indices), _ptr(values), _ptr(Q), _ptr(K), _ptr(V),
+                                      _ptr(out), _ptr(logits), _ptr(probs), int(N), int(nnz), int(H), int(D),
+                                      float(scale), int(dtype), _stream(stream)), "gtattn_fwd_weighted")
 
 
 def gtattn_csr_build(indptr, indices, N, nnz, opts=None, stream=None):

@@ -238,10 +238,10 @@ extern "C" gtattn_status gtattn_profile_read(gtattn_profile* out, int reset) {
 }
 
 // The fused forward on the fly (binning, fused rows, combine), with an
-// optional per-entry additive bias.
+// optional per-entry additive bias or per-entry adjacency values.
 static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
-                               const void* V, const float* bias, void* out, int64_t N, int64_t nnz, int H, int D,
-                               float scale, gtattn_dtype dtype, cudaStream_t stream) {
+                               const void* V, const float* values, const float* bias, void* out, int64_t N,
+                               int64_t nnz, int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
     RowChoice c;
     if (!choose_row_kernel(H, D, dtype, Q, K, V, out, GTATTN_KERNEL_AUTO, &c)) return GTATTN_ERR_UNSUPPORTED;
@@ -260,6 +260,7 @@ static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, co
     }
     RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale * kLog2e, c, sc.lists, sc.part);
     p.bias = bias;
+    p.values = values;
     if (st == GTATTN_OK) {
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
         st = launch_rows(kFused, dtype, c, p, stream);
@@ -275,7 +276,7 @@ static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, co
 extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indices, const void* Q,
                                     const void* K, const void* V, void* out, int64_t N, int64_t nnz,
                                     int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
-    return fwd_fused(indptr, indices, Q, K, V, nullptr, out, N, nnz, H, D, scale, dtype, stream);
+    return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream);
 }
 
 extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t* indptr,
@@ -332,11 +333,11 @@ extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t*
 }
 
 // The unfused trio (SDDMM, edge softmax, SpMM), with an optional per-entry
-// additive bias in the SDDMM.
+// additive bias or per-entry adjacency values in the SDDMM.
 static gtattn_status fwd_unfused(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
-                                 const void* V, const float* bias, void* out, float* logits, float* probs,
-                                 int64_t N, int64_t nnz, int H, int D, float scale, gtattn_dtype dtype,
-                                 cudaStream_t stream) {
+                                 const void* V, const float* values, const float* bias, void* out, float* logits,
+                                 float* probs, int64_t N, int64_t nnz, int H, int D, float scale,
+                                 gtattn_dtype dtype, cudaStream_t stream) {
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
     if ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(probs)) & 3u)
         return GTATTN_ERR_INVALID_ARG;
@@ -361,6 +362,7 @@ static gtattn_status fwd_unfused(const int32_t* indptr, const int32_t* indices, 
     p.logits = lg;
     p.probs = pr;
     p.bias = bias;
+    p.values = values;
     // (1) SDDMM: logits
     if (st == GTATTN_OK && nnz > 0) {
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
@@ -388,7 +390,8 @@ extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* 
                                           const void* K, const void* V, void* out, float* logits,
                                           float* probs, int64_t N, int64_t nnz, int H, int D, float scale,
                                           gtattn_dtype dtype, cudaStream_t stream) {
-    return fwd_unfused(indptr, indices, Q, K, V, nullptr, out, logits, probs, N, nnz, H, D, scale, dtype, stream);
+    return fwd_unfused(indptr, indices, Q, K, V, nullptr, nullptr, out, logits, probs, N, nnz, H, D, scale, dtype,
+                       stream);
 }
 
 extern "C" gtattn_status gtattn_fwd_bias(const int32_t* indptr, const int32_t* indices, const void* Q,
@@ -397,6 +400,18 @@ extern "C" gtattn_status gtattn_fwd_bias(const int32_t* indptr, const int32_t* i
                                          float scale, gtattn_dtype dtype, cudaStream_t stream) {
     if ((nnz > 0 && !bias) || (reinterpret_cast<uintptr_t>(bias) & 3u)) return GTATTN_ERR_INVALID_ARG;
     if (logits || probs)
-        return fwd_unfused(indptr, indices, Q, K, V, bias, out, logits, probs, N, nnz, H, D, scale, dtype, stream);
-    return fwd_fused(indptr, indices, Q, K, V, bias, out, N, nnz, H, D, scale, dtype, stream);
+        return fwd_unfused(indptr, indices, Q, K, V, nullptr, bias, out, logits, probs, N, nnz, H, D, scale, dtype,
+                           stream);
+    return fwd_fused(indptr, indices, Q, K, V, nullptr, bias, out, N, nnz, H, D, scale, dtype, stream);
+}
+
+extern "C" gtattn_status gtattn_fwd_weighted(const int32_t* indptr, const int32_t* indices, const float* values,
+                                             const void* Q, const void* K, const void* V, void* out, float* logits,
+                                             float* probs, int64_t N, int64_t nnz, int H, int D, float scale,
+                                             gtattn_dtype dtype, cudaStream_t stream) {
+    if ((nnz > 0 && !values) || (reinterpret_cast<uintptr_t>(values) & 3u)) return GTATTN_ERR_INVALID_ARG;
+    if (logits || probs)
+        return fwd_unfused(indptr, indices, Q, K, V, values, nullptr, out, logits, probs, N, nnz, H, D, scale, dtype,
+                           stream);
+    return fwd_fused(indptr, indices, Q, K, V, values, nullptr, out, N, nnz, H, D, scale, dtype, stream);
 }

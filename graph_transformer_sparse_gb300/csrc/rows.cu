@@ -234,10 +234,15 @@ constexpr int rows_min_blocks() {
     return VPL == 1 ? GT_ROWS_MIN_BLOCKS1 : VPL == 2 ? GT_ROWS_MIN_BLOCKS2 : 4;
 }
 
-// BIAS: the logits get p.bias[e*H + h] added (fused and SDDMM modes).
-template <typename T, typename TO, int VPL, int MODE, bool BIAS = false>
+// EXT (fused and SDDMM modes): kExtBias -- the logits get p.bias[e*H + h]
+// added; kExtValues -- the dot products are multiplied by p.values[e] (the
+// weighted adjacency's stored values).
+constexpr int kExtBias = 1, kExtValues = 2;
+template <typename T, typename TO, int VPL, int MODE, int EXT = 0>
 __global__ void __launch_bounds__(kRowThreads, rows_min_blocks<T, VPL>())
 k_rows_vec(RowParams p) {
+    constexpr bool BIAS = (EXT & kExtBias) != 0;
+    constexpr bool VALS = (EXT & kExtValues) != 0;
     using F = Frag<T, VPL>;
     constexpr int E = F::E;
     constexpr int U = (GT_ROWS_UNROLL / VPL) > 0 ? (GT_ROWS_UNROLL / VPL) : 1;
@@ -353,7 +358,8 @@ k_rows_vec(RowParams p) {
         // bias (BIAS): like the indices it comes from DRAM (read once, in CSR
         // order), so it is fetched two iterations ahead: bc for iteration it,
         // bx for it+1
-        float bc[U], bx[U];
+        float bc[U], bx[U];   // (the values (VALS) likewise: ac, ax)
+        float ac[U], ax[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int e = beg + u * S + sl;
@@ -361,6 +367,10 @@ k_rows_vec(RowParams p) {
             if constexpr (BIAS) {
                 bc[u] = okc[u] ? ld_stream(p.bias + static_cast<int64_t>(e) * p.H + head) : 0.f;
                 bx[u] = e + step < end ? ld_stream(p.bias + static_cast<int64_t>(e + step) * p.H + head) : 0.f;
+            }
+            if constexpr (VALS) {
+                ac[u] = okc[u] ? ld_stream(p.values + e) : 0.f;
+                ax[u] = e + step < end ? ld_stream(p.values + e + step) : 0.f;
             }
             const int j = okc[u] ? ld_index(p.indices + e) : 0;
             if (kNeedK) { if (okc[u]) kc[u].load(K + (int64_t)j * HD + lane_off); else kc[u].zero(); }
@@ -373,7 +383,7 @@ k_rows_vec(RowParams p) {
             // issue iteration it+1's gathers and iteration it+2's indices
             bool okn[U];
             F kn[U], vn[U];
-            float bn[U];
+            float bn[U], an[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int e1 = e0 + step + u * S;
@@ -382,6 +392,11 @@ k_rows_vec(RowParams p) {
                     bn[u] = bx[u];
                     const int e2b = e1 + step;
                     bx[u] = e2b < end ? ld_stream(p.bias + static_cast<int64_t>(e2b) * p.H + head) : 0.f;
+                }
+                if constexpr (VALS) {
+                    an[u] = ax[u];
+                    const int e2a = e1 + step;
+                    ax[u] = e2a < end ? ld_stream(p.values + e2a) : 0.f;
                 }
                 if (kNeedK) { if (okn[u]) kn[u].load(K + (int64_t)jn[u] * HD + lane_off); else kn[u].zero(); }
                 if (kNeedV) { if (okn[u]) vn[u].load(V + (int64_t)jn[u] * HD + lane_off); else vn[u].zero(); }
@@ -412,6 +427,10 @@ k_rows_vec(RowParams p) {
 #pragma unroll
                 for (int u = 0; u < U; ++u)
                     for (int o = 1; o < p.lph; o <<= 1) l[u] += __shfl_xor_sync(kFull, l[u], o);
+                if constexpr (VALS) {   // weighted adjacency: (q.k) * a_e (scaled or not alike)
+#pragma unroll
+                    for (int u = 0; u < U; ++u) l[u] *= ac[u];
+                }
                 if constexpr (BIAS && MODE == kFused) {
 #pragma unroll
                     for (int u = 0; u < U; ++u) l[u] = fmaf(bc[u], kLog2e, l[u]);   // logits in log2 units
@@ -477,6 +496,7 @@ k_rows_vec(RowParams p) {
                 kc[u] = kn[u];
                 vc[u] = vn[u];
                 if constexpr (BIAS) bc[u] = bn[u];
+                if constexpr (VALS) ac[u] = an[u];
             }
         }
         if constexpr (MODE != kSddmm) {
@@ -609,6 +629,7 @@ k_rows_generic(RowParams p) {
                     }
                     for (; d < D; ++d) a[0] += pr[d];
                     l = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+                    if (p.values) l *= p.values[e];   // weighted adjacency
                 }
                 if constexpr (MODE == kSddmm) {
                     p.logits[(int64_t)e * H + h] = p.bias ? fmaf(l, p.qscale, p.bias[(int64_t)e * H + h])
@@ -1119,7 +1140,7 @@ static int grid_for_tasks(int persistent, int task_bound, int warps_per_block) {
     return need < persistent ? need : persistent;
 }
 
-template <typename T, typename TO, int MODE, bool BIAS = false>
+template <typename T, typename TO, int MODE, int EXT = 0>
 static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
     auto go = [&](auto kernel) {
         const int grid = grid_for_tasks(grid_persistent(kernel, kRowThreads, 0), p.task_bound, kRowThreads / 32);
@@ -1128,10 +1149,10 @@ static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
     };
     cudaError_t e;
     switch (vpl) {
-        case 1: e = go(k_rows_vec<T, TO, 1, MODE, BIAS>); break;
-        case 2: e = go(k_rows_vec<T, TO, 2, MODE, BIAS>); break;
+        case 1: e = go(k_rows_vec<T, TO, 1, MODE, EXT>); break;
+        case 2: e = go(k_rows_vec<T, TO, 2, MODE, EXT>); break;
         case 4:
-            if constexpr (sizeof(T) == 4) { e = go(k_rows_vec<T, TO, 4, MODE, BIAS>); break; }
+            if constexpr (sizeof(T) == 4) { e = go(k_rows_vec<T, TO, 4, MODE, EXT>); break; }
             return GTATTN_ERR_UNSUPPORTED;
         default: return GTATTN_ERR_UNSUPPORTED;
     }
@@ -1141,13 +1162,18 @@ static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
 template <typename T, typename TO>
 static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParams& p, cudaStream_t s) {
     if (c.kind == RowKernel::kVector) {
-        const bool bias = p.bias != nullptr;
+        // one of the bias or the values at a time (the entry points take one)
+        if (p.bias && p.values) return GTATTN_ERR_UNSUPPORTED;
         switch (mode) {
             case kFused:
-                return bias ? launch_vec_t<T, TO, kFused, true>(c.vpl, p, s) : launch_vec_t<T, TO, kFused>(c.vpl, p, s);
+                if (p.bias) return launch_vec_t<T, TO, kFused, kExtBias>(c.vpl, p, s);
+                if (p.values) return launch_vec_t<T, TO, kFused, kExtValues>(c.vpl, p, s);
+                return launch_vec_t<T, TO, kFused>(c.vpl, p, s);
             case kSpmm: return launch_vec_t<T, TO, kSpmm>(c.vpl, p, s);
             case kSddmm:
-                return bias ? launch_vec_t<T, TO, kSddmm, true>(c.vpl, p, s) : launch_vec_t<T, TO, kSddmm>(c.vpl, p, s);
+                if (p.bias) return launch_vec_t<T, TO, kSddmm, kExtBias>(c.vpl, p, s);
+                if (p.values) return launch_vec_t<T, TO, kSddmm, kExtValues>(c.vpl, p, s);
+                return launch_vec_t<T, TO, kSddmm>(c.vpl, p, s);
         }
         return GTATTN_ERR_UNSUPPORTED;
     }

@@ -15,6 +15,7 @@ struct RowParams {
     void* out;
     const float* probs;     // SpMM mode: fp32 [nnz, H]
     const float* bias;      // fused / SDDMM modes: fp32 [nnz, H] added to the logits, or null
+    const float* values;    // fused / SDDMM modes: fp32 [nnz] multiplying the dot products, or null
     float* logits;          // SDDMM mode: fp32 [nnz, H]
     float qscale;           // fused: scale*log2(e); SDDMM: scale
     int N, H, D, HD;

@@ -224,6 +224,26 @@ gtattn_status gtattn_fwd_bias(const int32_t* indptr, const int32_t* indices, con
                               float scale, gtattn_dtype dtype, cudaStream_t stream);
 
 /*
+ * gtattn_fwd_weighted -- the forward on a weighted adjacency:
+ * SparseAttn(Q, K, V, A) = softmax(((Q K^T) o A) / sqrt(d)) V with
+ * A in [0,1] ("Graph Transformer in a Nutshell", section Sparse Multi-head
+ * Attention: the Hadamard product with the adjacency matrix's values).
+ *   values: fp32 [nnz], A's stored value of each CSR entry (shared by the
+ *           heads), device memory, 4-byte aligned (required when nnz > 0).
+ *           The logit of entry e is scale * (q.k) * values[e]; the softmax
+ *           still runs over the stored entries only (a stored 0 gives logit
+ *           0, it does not remove the entry).
+ *   logits, probs: as gtattn_fwd_probs (logits include the values); both
+ *           NULL: the fused kernels, else the unfused trio.
+ *   Other arguments and errors: as gtattn_fwd; INVALID_ARG for missing or
+ *   misaligned values.
+ */
+gtattn_status gtattn_fwd_weighted(const int32_t* indptr, const int32_t* indices, const float* values,
+                                  const void* Q, const void* K, const void* V, void* out, float* logits,
+                                  float* probs, int64_t N, int64_t nnz, int H, int D, float scale,
+                                  gtattn_dtype dtype, cudaStream_t stream);
+
+/*
  * gtattn_fwd_noalloc -- gtattn_fwd without any allocation.  The pages have
  * no counterpart: this exists for callers that cannot allocate device memory
  * when they run attention -- code running inside an allocator or memory-pool

@@ -58,6 +58,8 @@ def _load():
             lib.gto_sparse_mha_rows.restype = ctypes.c_int
             lib.gto_dense_attention.argtypes = [i64, i32, i32, vp, vp, vp, dbl, vp]
             lib.gto_dense_attention.restype = ctypes.c_int
+            lib.gto_sparse_mha_bwd.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, dbl, vp, vp, vp]
+            lib.gto_sparse_mha_bwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -170,3 +172,20 @@ def dense_attention(Q, K, V, scale):
     if rc != 0:
         raise OracleError(f"gto_dense_attention failed with code {rc}")
     return out
+
+
+def sparse_mha_bwd(indptr, indices, Q, K, V, dO, scale):
+    """Gradients of sum(out * dO) with respect to Q, K, V (fp64), for the
+    sparse forward with binary A.  Returns ``dict(dQ=, dK=, dV=)``, each
+    float64 [N, H, D]."""
+    lib = _load()
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    Q, K, V, dO = (np.ascontiguousarray(x, dtype=np.float32) for x in (Q, K, V, dO))
+    N, H, D = Q.shape
+    dQ, dK, dV = (np.zeros((N, H, D), dtype=np.float64) for _ in range(3))
+    rc = lib.gto_sparse_mha_bwd(N, int(indptr[-1]), H, D, _ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V),
+                                _ptr(dO), float(np.float32(scale)), _ptr(dQ), _ptr(dK), _ptr(dV))
+    if rc != 0:
+        raise OracleError(f"gto_sparse_mha_bwd failed with code {rc}")
+    return dict(dQ=dQ, dK=dK, dV=dV)

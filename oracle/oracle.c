@@ -211,3 +211,84 @@ int gto_dense_attention(int64_t n, int32_t H, int32_t D, const float* Q, const f
     free(w);
     return GTO_OK;
 }
+
+/*
+ * Backward pass of the sparse forward (binary A, no bias): the gradients
+ * of L = sum_{i,h,d} out[i,h,d] * dO[i,h,d] with respect to Q, K and V.
+ * The pages train this block (the molhiv loop of "Graph Transformer in a
+ * Nutshell" calls loss.backward() through SparseMHA) but print no backward
+ * formula; this is the chain rule applied to the definition above, per row
+ * i and head h, with s_e = scale * q_i . k_j and p_e the row softmax:
+ *   dp_e  = dO_i . v_j
+ *   Dlt   = sum_e p_e dp_e
+ *   ds_e  = p_e (dp_e - Dlt)                     (softmax Jacobian)
+ *   dQ_i += scale * sum_e ds_e k_j
+ *   dK_j += scale * ds_e q_i                     (for each entry e = (i <- j))
+ *   dV_j += p_e dO_i
+ * Q, K, V, dO float32 [N, H, D]; dQ, dK, dV double [N, H, D], overwritten.
+ * Rows without entries contribute nothing.  Every operation is double, the
+ * sums run in index order.
+ */
+int gto_sparse_mha_bwd(int64_t N, int64_t nnz, int32_t H, int32_t D,
+                       const int32_t* indptr, const int32_t* indices,
+                       const float* Q, const float* K, const float* V, const float* dO, double scale,
+                       double* dQ, double* dK, double* dV)
+{
+    if (N < 0 || nnz < 0 || H <= 0 || D <= 0 || !indptr || !dQ || !dK || !dV) return GTO_BAD_ARG;
+    if (nnz > 0 && (!indices || !K || !V)) return GTO_BAD_ARG;
+    if (N > 0 && (!Q || !dO)) return GTO_BAD_ARG;
+    if (gto_check_csr(N, nnz, indptr, indices) != GTO_OK) return GTO_BAD_CSR;
+    const int64_t HD = (int64_t)H * D;
+    for (int64_t x = 0; x < N * HD; ++x) { dQ[x] = 0.0; dK[x] = 0.0; dV[x] = 0.0; }
+    int64_t max_deg = 0;
+    for (int64_t i = 0; i < N; ++i)
+        if ((int64_t)indptr[i + 1] - indptr[i] > max_deg) max_deg = (int64_t)indptr[i + 1] - indptr[i];
+    double* p = (double*)malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    double* dp = (double*)malloc(sizeof(double) * (size_t)(max_deg > 0 ? max_deg : 1));
+    if (!p || !dp) { free(p); free(dp); return GTO_NO_MEMORY; }
+    for (int64_t i = 0; i < N; ++i) {
+        const int64_t beg = indptr[i], deg = (int64_t)indptr[i + 1] - beg;
+        if (deg == 0) continue;
+        for (int32_t h = 0; h < H; ++h) {
+            const float* q = Q + i * HD + (int64_t)h * D;
+            const float* g = dO + i * HD + (int64_t)h * D;
+            /* forward again: logits, their max, softmax weights */
+            double m = -INFINITY;
+            for (int64_t k = 0; k < deg; ++k) {
+                const float* kj = K + (int64_t)indices[beg + k] * HD + (int64_t)h * D;
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += (double)q[d] * (double)kj[d];
+                p[k] = scale * dot;
+                if (p[k] > m) m = p[k];
+            }
+            double S = 0.0;
+            for (int64_t k = 0; k < deg; ++k) { p[k] = exp(p[k] - m); S += p[k]; }
+            for (int64_t k = 0; k < deg; ++k) p[k] /= S;
+            /* dp_e = dO_i . v_j and its p-weighted mean */
+            double Dlt = 0.0;
+            for (int64_t k = 0; k < deg; ++k) {
+                const float* vj = V + (int64_t)indices[beg + k] * HD + (int64_t)h * D;
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += (double)g[d] * (double)vj[d];
+                dp[k] = dot;
+                Dlt += p[k] * dot;
+            }
+            double* dq = dQ + i * HD + (int64_t)h * D;
+            for (int64_t k = 0; k < deg; ++k) {
+                const int64_t j = indices[beg + k];
+                const double ds = p[k] * (dp[k] - Dlt);
+                const float* kj = K + j * HD + (int64_t)h * D;
+                double* dk = dK + j * HD + (int64_t)h * D;
+                double* dv = dV + j * HD + (int64_t)h * D;
+                for (int32_t d = 0; d < D; ++d) {
+                    dq[d] += scale * ds * (double)kj[d];
+                    dk[d] += scale * ds * (double)q[d];
+                    dv[d] += p[k] * (double)g[d];
+                }
+            }
+        }
+    }
+    free(p);
+    free(dp);
+    return GTO_OK;
+}

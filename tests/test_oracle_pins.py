@@ -582,3 +582,95 @@ def test_weight_pins_catch_planted_mistakes(name):
         lib = _compile_mutant(mutant, td, name)
         got = _run_mutant(lib, indptr, indices, Q, K, V, 0.7, values=values)
     assert not np.allclose(got, ref, rtol=1e-9, atol=1e-12), f"pin missed mutation {name}"
+
+
+# --------------------------------------------------------------------------
+# backward pass: gradients of sum(out * dO)
+# --------------------------------------------------------------------------
+def _loss(indptr, indices, Q, K, V, G, scale):
+    return float((oracle.sparse_mha(indptr, indices, Q, K, V, scale)["out"] * G.astype(np.float64)).sum())
+
+
+def _fd_grads(indptr, indices, Q, K, V, G, scale):
+    """Central differences of the forward oracle at every element of Q, K, V
+    (the step actually taken is the difference of the two float32 values)."""
+    res = {}
+    for name, X in (("dQ", Q), ("dK", K), ("dV", V)):
+        fd = np.zeros(X.shape)
+        for idx in np.ndindex(X.shape):
+            x0 = X[idx]
+            xp, xm = np.float32(x0 + 1e-3), np.float32(x0 - 1e-3)
+            X[idx] = xp
+            lp = _loss(indptr, indices, Q, K, V, G, scale)
+            X[idx] = xm
+            lm = _loss(indptr, indices, Q, K, V, G, scale)
+            X[idx] = x0
+            fd[idx] = (lp - lm) / (float(xp) - float(xm))
+        res[name] = fd
+    return res
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_backward_matches_finite_differences(seed):
+    rng = np.random.default_rng(500 + seed)
+    n, H, D = 7, 2, 3
+    indptr, indices, Q, K, V = _bias_graph(rng, n, 20, H, D)
+    G = rng.standard_normal((n, H, D)).astype(np.float32)
+    got = oracle.sparse_mha_bwd(indptr, indices, Q, K, V, G, 0.6)
+    fd = _fd_grads(indptr, indices, Q, K, V, G, 0.6)
+    for name in fd:
+        np.testing.assert_allclose(got[name], fd[name], rtol=1e-5, atol=1e-6, err_msg=name)
+
+
+def test_backward_single_neighbour_and_constant_values():
+    rng = np.random.default_rng(510)
+    n, H, D = 12, 2, 4
+    src = rng.integers(0, n, n)
+    indptr, indices = wl.csr_by_destination(src, np.arange(n), n)   # one entry per row
+    Q, K, V = _rand_feats(rng, n, H, D)
+    G = rng.standard_normal((n, H, D)).astype(np.float32)
+    r = oracle.sparse_mha_bwd(indptr, indices, Q, K, V, G, 0.5)
+    assert np.all(r["dQ"] == 0.0) and np.all(r["dK"] == 0.0)     # p = 1 whatever the logits
+    ref = np.zeros((n, H, D))
+    np.add.at(ref, indices, G.astype(np.float64))                  # dV_j = sum of dO_i over i <- j
+    np.testing.assert_allclose(r["dV"], ref, rtol=0, atol=1e-15)
+    # constant V: out does not depend on the weights, so dQ = dK = 0
+    indptr, indices, Q, K, V = _bias_graph(rng, n, 60, H, D)
+    V[:] = 0.75
+    r = oracle.sparse_mha_bwd(indptr, indices, Q, K, V, G, 0.5)
+    np.testing.assert_allclose(r["dQ"], 0.0, atol=1e-14)
+    np.testing.assert_allclose(r["dK"], 0.0, atol=1e-14)
+
+
+BWD_MUTATIONS = {
+    "softmax_jacobian_without_mean": ("const double ds = p[k] * (dp[k] - Dlt);", "const double ds = p[k] * dp[k];"),
+    "dk_to_the_row": ("double* dk = dK + j * HD + (int64_t)h * D;", "double* dk = dK + i * HD + (int64_t)h * D;"),
+    "dq_without_scale": ("dq[d] += scale * ds * (double)kj[d];", "dq[d] += ds * (double)kj[d];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTATIONS))
+def test_backward_pins_catch_planted_mistakes(name):
+    text = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    old, new = BWD_MUTATIONS[name]
+    assert text.count(old) == 1, f"anchor for {name} missing"
+    mutant = text.replace(old, new, 1)
+    rng = np.random.default_rng(520)
+    n, H, D = 7, 2, 3
+    indptr, indices, Q, K, V = _bias_graph(rng, n, 20, H, D)
+    G = rng.standard_normal((n, H, D)).astype(np.float32)
+    ref = _fd_grads(indptr, indices, Q, K, V, G, 0.6)   # the independent pin
+    with tempfile.TemporaryDirectory() as td:
+        path = os.path.join(td, name + ".c")
+        open(path, "w").write(mutant)
+        so = os.path.join(td, name + ".so")
+        subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", path, "-o", so, "-lm"], check=True)
+        lib = ctypes.CDLL(so)
+        i64, i32, vp, dbl = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_double
+        lib.gto_sparse_mha_bwd.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, dbl, vp, vp, vp]
+        out = {k: np.zeros((n, H, D)) for k in ("dQ", "dK", "dV")}
+        p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+        ip, ix = np.ascontiguousarray(indptr, np.int32), np.ascontiguousarray(indices, np.int32)
+        assert lib.gto_sparse_mha_bwd(n, int(ip[-1]), H, D, p(ip), p(ix), p(Q), p(K), p(V), p(G), 0.6,
+                                      p(out["dQ"]), p(out["dK"]), p(out["dV"])) == 0
+    assert any(not np.allclose(out[k], ref[k], rtol=1e-5, atol=1e-6) for k in out), f"pin missed mutation {name}"

@@ -7,7 +7,7 @@ row kernel, the split-row combine) over the whole R-MAT graph (2^20 nodes,
 JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--path fwd|plan|probs|bias|weighted] [--impl ours|reference]
+                    [--path fwd|plan|probs|bias|weighted|bwd] [--impl ours|reference]
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload
 (weak scaling, no collective on the data path); the timed region is
@@ -222,6 +222,10 @@ def make_step(w, d, path, gt, plan=None, probs_bufs=None):
         (values,) = probs_bufs
         return lambda: gt.gtattn_fwd_weighted(d["indptr"], d["indices"], values, d["Q"], d["K"], d["V"], d["out"],
                                               w.N, w.nnz, w.H, w.D, w.scale, dt)
+    if path == "bwd":
+        dO, dQ, dK, dV = probs_bufs
+        return lambda: gt.gtattn_bwd(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], dO, dQ, dK, dV,
+                                     w.N, w.nnz, w.H, w.D, w.scale, dt)
     raise ValueError(path)
 
 
@@ -254,6 +258,11 @@ def run_gpu_workload(w, path, steps, warmup, gt, dev, flush, want_profile=True, 
         gen = torch.Generator(device=dev)
         gen.manual_seed(12345)
         probs_bufs = (torch.randn(w.nnz, w.H, device=dev, generator=gen),)
+    if path == "bwd":   # backward: seeded N(0, 1) output gradient in the input dtype, fp32 gradients
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(34567)
+        dO = torch.randn(w.N, w.H, w.D, device=dev, generator=gen).to(d["Q"].dtype)
+        probs_bufs = (dO,) + tuple(torch.empty(w.N, w.H, w.D, device=dev) for _ in range(3))
     if path == "weighted":   # weighted adjacency: seeded U(0, 1) stored values, fp32 [nnz]
         gen = torch.Generator(device=dev)
         gen.manual_seed(23456)
@@ -378,6 +387,8 @@ def gpu_arm(args):
         cbytes += 4 * w.nnz * w.H   # the fp32 bias, read once per entry and head
     if args.path == "weighted":
         cbytes += 4 * w.nnz         # the fp32 adjacency values, read once per entry
+    if args.path == "bwd":          # + dO rows read, fp32 dQ / dK / dV written once each
+        cbytes += w.N * w.H * w.D * esize + 3 * 4 * w.N * w.H * w.D
     ubytes = unique_bytes(w.N, w.nnz, w.H, w.D, esize)
 
     launches_per_step = sum(v["launches"] for v in prof.values()) / args.steps
@@ -413,7 +424,8 @@ def gpu_arm(args):
                             "plan": "gtattn_fwd_plan (prebuilt plan)",
                             "probs": "gtattn_fwd_probs (unfused SDDMM/softmax/SpMM)",
                             "bias": "gtattn_fwd_bias (fused, per-edge per-head additive bias, fp32 N(0,1))",
-                            "weighted": "gtattn_fwd_weighted (fused, weighted adjacency, fp32 U(0,1))"}[args.path],
+                            "weighted": "gtattn_fwd_weighted (fused, weighted adjacency, fp32 U(0,1))",
+                            "bwd": "gtattn_bwd (dQ, dK, dV of sum(out * dO), dO ~ N(0,1))"}[args.path],
                    "l2": "flushed before every timed step (512 MiB memset, outside the events)",
                    "clock_soak": f"{args.soak:g} s of untimed steps before the warm-up; clocks sampled from "
                                  f"then to the end",
@@ -434,7 +446,8 @@ def gpu_arm(args):
     if rank == 0 and not args.no_extra:
         extra = {}
         for other, pth in (("erdos_renyi", "fwd"), ("molecules", "fwd"), ("tiny_random", "fwd"),
-                           ("dense_blocks", "plan"), ("rmat", "probs"), ("rmat", "bias"), ("rmat", "weighted")):
+                           ("dense_blocks", "plan"), ("rmat", "probs"), ("rmat", "bias"), ("rmat", "weighted"),
+                           ("rmat", "bwd")):
             if other == name and pth == args.path:
                 continue
             try:
@@ -451,6 +464,8 @@ def gpu_arm(args):
                 cb += 4 * wo.nnz * wo.H   # the fp32 bias, read once per entry and head
             if pth == "weighted":
                 cb += 4 * wo.nnz          # the fp32 adjacency values, read once per entry
+            if pth == "bwd":              # + dO rows read, fp32 dQ / dK / dV written once each
+                cb += wo.N * wo.H * wo.D * es + 3 * 4 * wo.N * wo.H * wo.D
             ent = {"ms": round(ms, 5), "edge_heads_per_s": round(wo.nnz * wo.H / (ms / 1e3), 1),
                    "gbs_compulsory": round(cb / (ms / 1e3) / 1e9, 1),
                    "hbm_frac": round(cb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -516,7 +531,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="rmat", choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias", "weighted"])
+    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias", "weighted", "bwd"])
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up (clock record under load)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")

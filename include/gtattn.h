@@ -244,6 +244,26 @@ gtattn_status gtattn_fwd_weighted(const int32_t* indptr, const int32_t* indices,
                                   gtattn_dtype dtype, cudaStream_t stream);
 
 /*
+ * gtattn_bwd -- the backward pass of gtattn_fwd (binary A, no bias): the
+ * gradients of L = sum(out * dO) with respect to Q, K and V.  The pages
+ * train the block (loss.backward() in the "Graph Transformer in a Nutshell"
+ * training loop) without printing a backward; this is the chain rule on the
+ * forward's definition: with s = scale q_i.k_j, p the row softmax,
+ * dp = dO_i.v_j and ds = p (dp - sum_row p dp):
+ *   dQ_i = scale sum_j ds k_j,  dK_j = scale sum_i ds q_i,  dV_j = sum_i p dO_i.
+ *   Q, K, V, dO: [N, H, D] in dtype (F32, or BF16 / BF16_OUT_F32 for bf16
+ *           inputs), device memory.
+ *   dQ, dK, dV: fp32 [N, H, D], device memory, 4-byte aligned; overwritten
+ *           (dK and dV are zeroed by the library on `stream` first).
+ *   H <= 128.  Other arguments: as gtattn_fwd.  Asynchronous on `stream`.
+ * dK and dV accumulate with fp32 atomic adds, so their last bits depend on
+ * the order of the additions (not deterministic run to run).
+ */
+gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                         const void* V, const void* dO, float* dQ, float* dK, float* dV, int64_t N,
+                         int64_t nnz, int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
+
+/*
  * gtattn_fwd_noalloc -- gtattn_fwd without any allocation.  The pages have
  * no counterpart: this exists for callers that cannot allocate device memory
  * when they run attention -- code running inside an allocator or memory-pool

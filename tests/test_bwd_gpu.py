@@ -1,0 +1,84 @@
+"""Backward pass (gtattn_bwd): the gradients of sum(out * dO) with respect to
+Q, K, V from the CUDA path against the fp64 oracle backward (itself pinned
+by finite differences of the forward oracle) on the same inputs.
+
+Tolerance (the pages state none for gradients): |g - o| <= 1e-4 |o| + 1e-5
+max|o| per tensor.  The gradients are fp32 sums of many signed terms (dK and
+dV accumulated by atomic adds in no fixed order, ds = p (dp - sum p dp) with
+cancellation), so their error is relative to the size of the terms rather
+than to each element."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from gpu_helpers import to_device
+
+torch = pytest.importorskip("torch")
+gt = pytest.importorskip("graph_transformer_sparse_gb300")
+
+pytestmark = pytest.mark.gpu
+
+
+def _grad_close(got, ref, what):
+    bound = 1e-4 * np.abs(ref) + 1e-5 * max(float(np.abs(ref).max()), 1e-30)
+    err = np.abs(got - ref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outside; worst got "
+                           f"{got.flat[np.argmax(err - bound)]!r} ref {ref.flat[np.argmax(err - bound)]!r}")
+
+
+def _dO(w, seed):
+    rng = np.random.default_rng(seed)
+    g = rng.standard_normal((w.N, w.H, w.D)).astype(np.float32)
+    if w.dtype == "bf16":
+        vals, bits = wl.bf16_round(g)
+        return vals, torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    return g, torch.from_numpy(g).cuda()
+
+
+def _bwd(w, d, dO_t):
+    grads = {k: torch.full((w.N, w.H, w.D), float("nan"), device="cuda") for k in ("dQ", "dK", "dV")}
+    dt = gt.GTATTN_F32 if w.dtype == "f32" else gt.GTATTN_BF16
+    gt.gtattn_bwd(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], dO_t, grads["dQ"], grads["dK"], grads["dV"],
+                  w.N, w.nnz, w.H, w.D, w.scale, dt)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy().astype(np.float64) for k, v in grads.items()}
+
+
+@pytest.mark.parametrize("name", ["tiny_random", "molecules", "erdos_renyi", "rmat", "dense_blocks"])
+def test_backward_matches_oracle(name):
+    w = wl.small_workload(name)
+    g, g_t = _dO(w, seed=sum(map(ord, name)))
+    ref = oracle.sparse_mha_bwd(w.indptr, w.indices, w.Q, w.K, w.V, g, w.scale)
+    got = _bwd(w, to_device(w), g_t)
+    for k in ("dQ", "dK", "dV"):
+        _grad_close(got[k], ref[k], f"{name} {k}")
+    # rows without entries have no query gradient
+    empty = np.diff(w.indptr) == 0
+    assert np.all(got["dQ"][empty] == 0.0)
+
+
+def test_backward_single_neighbour_rows():
+    # p = 1 exactly: no query or key gradient, dV_j the sum of dO_i over i <- j
+    rng = np.random.default_rng(3)
+    n, H, D = 500, 4, 32
+    src = rng.integers(0, n, n)
+    indptr, indices = wl.csr_by_destination(src, np.arange(n), n)
+    Q, K, V = (rng.standard_normal((n, H, D)).astype(np.float32) for _ in range(3))
+    w = wl.Workload("single", n, H, D, "f32", indptr.astype(np.int32), indices.astype(np.int32), Q, K, V, 0.2)
+    g, g_t = _dO(w, 4)
+    got = _bwd(w, to_device(w), g_t)
+    assert np.all(got["dQ"] == 0.0) and np.all(got["dK"] == 0.0)
+    ref = np.zeros((n, H, D))
+    np.add.at(ref, indices, g.astype(np.float64))
+    _grad_close(got["dV"], ref, "single-neighbour dV")
+
+
+def test_backward_argument_errors():
+    w = wl.make_workload("tiny_random")
+    d = to_device(w)
+    z = torch.zeros((w.N, 200, 1), device="cuda")
+    with pytest.raises(gt.GtattnError) as e:   # more heads than the backward supports
+        gt.gtattn_bwd(d["indptr"], d["indices"], z, z, z, z, z, z, z, w.N, w.nnz, 200, 1, 1.0, gt.GTATTN_F32)
+    assert e.value.status == gt.GTATTN_ERR_INVALID_ARG

@@ -8,6 +8,7 @@
 #include "dense.cuh"
 #include "plan.cuh"
 #include "rows.cuh"
+#include "bwd.cuh"
 
 namespace gt {
 
@@ -414,4 +415,76 @@ extern "C" gtattn_status gtattn_fwd_weighted(const int32_t* indptr, const int32_
         return fwd_unfused(indptr, indices, Q, K, V, values, nullptr, out, logits, probs, N, nnz, H, D, scale, dtype,
                            stream);
     return fwd_fused(indptr, indices, Q, K, V, values, nullptr, out, N, nnz, H, D, scale, dtype, stream);
+}
+
+
+extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                                    const void* V, const void* dO, float* dQ, float* dK, float* dV, int64_t N,
+                                    int64_t nnz, int H, int D, float scale, gtattn_dtype dtype,
+                                    cudaStream_t stream) {
+    if (N < 0 || nnz < 0 || N >= (1ll << 31) - 1 || nnz >= (1ll << 31) - 1) return GTATTN_ERR_INVALID_ARG;
+    if (H < 1 || D < 1 || (int64_t)H * D > kMaxHD || H > kBwdMaxHeads) return GTATTN_ERR_INVALID_ARG;
+    if (dtype != GTATTN_F32 && dtype != GTATTN_BF16 && dtype != GTATTN_BF16_OUT_F32) return GTATTN_ERR_INVALID_ARG;
+    if (!indptr) return GTATTN_ERR_INVALID_ARG;
+    if (N > 0 && (!Q || !dO || !dQ || !dK || !dV)) return GTATTN_ERR_INVALID_ARG;
+    if (nnz > 0 && (!indices || !K || !V)) return GTATTN_ERR_INVALID_ARG;
+    const uintptr_t esz = dtype == GTATTN_F32 ? 4 : 2;
+    const uintptr_t in_al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                            reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(dO);
+    const uintptr_t out_al = reinterpret_cast<uintptr_t>(dQ) | reinterpret_cast<uintptr_t>(dK) |
+                             reinterpret_cast<uintptr_t>(dV) | reinterpret_cast<uintptr_t>(indptr) |
+                             reinterpret_cast<uintptr_t>(indices);
+    if ((in_al & (esz - 1)) || (out_al & 3u)) return GTATTN_ERR_INVALID_ARG;
+    if (N == 0) return GTATTN_OK;
+    const int HD = H * D;
+    const size_t grad_bytes = sizeof(float) * static_cast<size_t>(N) * HD;
+    GT_CUDA(cudaMemsetAsync(dQ, 0, grad_bytes, stream));
+    GT_CUDA(cudaMemsetAsync(dK, 0, grad_bytes, stream));
+    GT_CUDA(cudaMemsetAsync(dV, 0, grad_bytes, stream));
+    const void* ptrs[7] = {Q, K, V, dO, dQ, dK, dV};
+    const gtattn_dtype fdt = dtype == GTATTN_F32 ? GTATTN_F32 : GTATTN_BF16_OUT_F32;   // fp32 forward output
+    RowChoice c;
+    if (!bwd_tasks_supported(H, D, dtype, ptrs, 7) || !choose_row_kernel(H, D, fdt, Q, K, V, dQ, GTATTN_KERNEL_AUTO, &c)) {
+        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+        return launch_bwd_rows(indptr, indices, Q, K, V, dO, dQ, dK, dV, (int)N, H, D, scale, dtype, stream);
+    }
+    // the forward again, keeping its fp32 output and row log-sum-exp
+    gtattn_plan_opts o;
+    resolve_opts(nullptr, &o);
+    Scratch sc;
+    int *hdr, *rows;
+    int2 *chunks, *longs;
+    GT_TRY(scratch_alloc(N, nnz, H, HD, o.long_row_min, o.chunk_edges, false, false, &sc, &hdr, &rows, &chunks,
+                         &longs, stream));
+    void* ol = nullptr;
+    const size_t o_bytes = align_up(grad_bytes), l_bytes = align_up(sizeof(float) * static_cast<size_t>(N) * H);
+    gtattn_status st = pool_alloc(&ol, o_bytes + l_bytes, stream);
+    if (st != GTATTN_OK) {
+        pool_free(sc.base, stream);
+        return st;
+    }
+    float* O = static_cast<float*>(ol);
+    float* lse = reinterpret_cast<float*>(static_cast<char*>(ol) + o_bytes);
+    {
+        ProfScope ps(GTATTN_KCAT_BIN, bin_launches((int)N, nullptr), stream);
+        st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
+    }
+    RowParams p = make_params(indptr, indices, Q, K, V, O, N, nnz, H, D, scale * kLog2e, c, sc.lists, sc.part);
+    p.lse = lse;
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+        st = launch_rows(kFused, fdt, c, p, stream);
+    }
+    if (st == GTATTN_OK && nnz > o.long_row_min) {
+        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
+        st = launch_combine(kFused, fdt, p, stream);
+    }
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+        st = launch_bwd_tasks(indptr, indices, sc.lists, Q, K, V, dO, O, lse, dQ, dK, dV, (int)N, H, D, scale, dtype,
+                              stream);
+    }
+    pool_free(ol, stream);
+    pool_free(sc.base, stream);
+    return st;
 }

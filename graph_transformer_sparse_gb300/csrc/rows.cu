@@ -535,6 +535,8 @@ k_rows_vec(RowParams p) {
                 const float inv = ssum > 0.f ? 1.f / ssum : 0.f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) acc[e] = ssum > 0.f ? acc[e] * inv : 0.f;
+                // the row's log-sum-exp (log2 units) when the caller asks for it
+                if (p.lse && gl % p.lph == 0) p.lse[(int64_t)row * p.H + head] = m + log2f(ssum);
             }
             store_frag<TO, E>(O + (int64_t)row * HD + lane_off, acc);
         }
@@ -688,6 +690,8 @@ k_rows_generic(RowParams p) {
                     store_elem(O, (int64_t)row * HD + el, v);
                 }
             }
+            if (MODE == kFused && p.lse)   // the row's log-sum-exp (log2 units)
+                for (int h = lane; h < H; h += 32) p.lse[(int64_t)row * H + h] = hm[h] + log2f(hs[h]);
         }
         __syncwarp();
     }
@@ -751,6 +755,7 @@ k_combine(RowParams p, int warp_rows) {
                 float S = 0.f;
                 for (int k = 0; k < G; ++k) S += red[k * H + t];
                 sS[t] = S;
+                if (p.lse) p.lse[(int64_t)row * H + t] = sM[t] + log2f(S);   // log-sum-exp, log2 units
             }
             __syncthreads();
         }
@@ -826,6 +831,7 @@ k_combine(RowParams p, int warp_rows) {
                     S += p.part.s[k] * ex2(p.part.m[k] - M);
                 }
                 for (int o = H; o < 32; o <<= 1) S += __shfl_xor_sync(kFull, S, o);
+                if (p.lse && lane < H) p.lse[(int64_t)row * H + lane] = M + log2f(S);   // log-sum-exp, log2 units
             }
             for (int el0 = 0; el0 < HD; el0 += 32) {
                 const int el = el0 + lane;

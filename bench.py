@@ -7,7 +7,7 @@ row kernel, the split-row combine) over the whole R-MAT graph (2^20 nodes,
 JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--path fwd|plan|probs|bias|weighted|bwd] [--impl ours|reference]
+                    [--path fwd|plan|probs|bias|weighted|bwd|ndh] [--impl ours|reference]
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload
 (weak scaling, no collective on the data path); the timed region is
@@ -222,6 +222,9 @@ def make_step(w, d, path, gt, plan=None, probs_bufs=None):
         (values,) = probs_bufs
         return lambda: gt.gtattn_fwd_weighted(d["indptr"], d["indices"], values, d["Q"], d["K"], d["V"], d["out"],
                                               w.N, w.nnz, w.H, w.D, w.scale, dt)
+    if path == "ndh":   # the same synthetic rows read as [N, D, H] (head innermost)
+        return lambda: gt.gtattn_fwd_ndh(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], w.N, w.nnz,
+                                         w.H, w.D, w.scale, dt)
     if path == "bwd":
         dO, dQ, dK, dV = probs_bufs
         return lambda: gt.gtattn_bwd(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], dO, dQ, dK, dV,
@@ -425,7 +428,8 @@ def gpu_arm(args):
                             "probs": "gtattn_fwd_probs (unfused SDDMM/softmax/SpMM)",
                             "bias": "gtattn_fwd_bias (fused, per-edge per-head additive bias, fp32 N(0,1))",
                             "weighted": "gtattn_fwd_weighted (fused, weighted adjacency, fp32 U(0,1))",
-                            "bwd": "gtattn_bwd (dQ, dK, dV of sum(out * dO), dO ~ N(0,1))"}[args.path],
+                            "bwd": "gtattn_bwd (dQ, dK, dV of sum(out * dO), dO ~ N(0,1))",
+                            "ndh": "gtattn_fwd_ndh (head-innermost [N, D, H] rows, generic kernel)"}[args.path],
                    "l2": "flushed before every timed step (512 MiB memset, outside the events)",
                    "clock_soak": f"{args.soak:g} s of untimed steps before the warm-up; clocks sampled from "
                                  f"then to the end",
@@ -447,7 +451,7 @@ def gpu_arm(args):
         extra = {}
         for other, pth in (("erdos_renyi", "fwd"), ("molecules", "fwd"), ("tiny_random", "fwd"),
                            ("dense_blocks", "plan"), ("rmat", "probs"), ("rmat", "bias"), ("rmat", "weighted"),
-                           ("rmat", "bwd")):
+                           ("rmat", "bwd"), ("rmat", "ndh")):
             if other == name and pth == args.path:
                 continue
             try:
@@ -531,7 +535,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="rmat", choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias", "weighted", "bwd"])
+    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias", "weighted", "bwd", "ndh"])
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up (clock record under load)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")

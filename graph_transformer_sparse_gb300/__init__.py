@@ -21,7 +21,7 @@ import threading
 from ._build import LIB, build
 
 __all__ = [
-    "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs", "gtattn_fwd_bias", "gtattn_fwd_weighted", "gtattn_bwd",
+    "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs", "gtattn_fwd_bias", "gtattn_fwd_weighted", "gtattn_bwd", "gtattn_fwd_ndh",
     "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_csr_build", "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
     "gtattn_csr_validate", "gtattn_status_string", "gtattn_profile_enable", "gtattn_profile_read",
     "sparse_mha", "GTATTN_F32", "GTATTN_BF16", "GTATTN_BF16_OUT_F32",
@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "gtattn_plan_get_info", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
     "gtattn_coo_to_csr", "gtattn_csr_validate", "gtattn_profile_enable", "gtattn_profile_read",
     "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_bias", "gtattn_fwd_weighted", "gtattn_bwd",
+    "gtattn_fwd_ndh",
 )
 KCAT_NAMES = ("bin", "rows", "combine", "softmax", "dense")
 
@@ -102,6 +103,7 @@ def load(path: str | None = None):
             "gtattn_fwd_bias": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
             "gtattn_fwd_weighted": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
             "gtattn_bwd": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
+            "gtattn_fwd_ndh": ([vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
             "gtattn_coo_to_csr": ([vp, vp, i64, i64, vp, vp, vp], i32),
             "gtattn_csr_validate": ([vp, vp, i64, i64, vp], i32),
             "gtattn_fwd_noalloc": ([vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
@@ -244,6 +246,12 @@ def gtattn_bwd(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, nnz, H, D, scale, dt
     _check(load().gtattn_bwd(_ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), _ptr(dK),
                              _ptr(dV), int(N), int(nnz), int(H), int(D), float(scale), int(dtype), _stream(stream)),
            "gtattn_bwd")
+
+
+def gtattn_fwd_ndh(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, stream=None):
+    """gtattn_fwd on head-innermost [N, D, H] tensors."""
+    _check(load().gtattn_fwd_ndh(_ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(out), int(N), int(nnz),
+                                 int(H), int(D), float(scale), int(dtype), _stream(stream)), "gtattn_fwd_ndh")
 
 
 def gtattn_csr_build(indptr, indices, N, nnz, opts=None, stream=None):

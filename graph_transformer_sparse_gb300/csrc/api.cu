@@ -242,10 +242,14 @@ extern "C" gtattn_status gtattn_profile_read(gtattn_profile* out, int reset) {
 // optional per-entry additive bias or per-entry adjacency values.
 static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
                                const void* V, const float* values, const float* bias, void* out, int64_t N,
-                               int64_t nnz, int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
+                               int64_t nnz, int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream,
+                               int ndh = 0) {
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
     RowChoice c;
-    if (!choose_row_kernel(H, D, dtype, Q, K, V, out, GTATTN_KERNEL_AUTO, &c)) return GTATTN_ERR_UNSUPPORTED;
+    // head-innermost rows ([N, D, H]): the generic kernel (the vector kernel's
+    // lane groups assume head-major rows)
+    if (!choose_row_kernel(H, D, dtype, Q, K, V, out, ndh ? GTATTN_KERNEL_GENERIC : GTATTN_KERNEL_AUTO, &c))
+        return GTATTN_ERR_UNSUPPORTED;
     if (N == 0) return GTATTN_OK;
     gtattn_plan_opts o;
     resolve_opts(nullptr, &o);
@@ -262,6 +266,7 @@ static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, co
     RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale * kLog2e, c, sc.lists, sc.part);
     p.bias = bias;
     p.values = values;
+    p.ndh = ndh;
     if (st == GTATTN_OK) {
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
         st = launch_rows(kFused, dtype, c, p, stream);
@@ -278,6 +283,12 @@ extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indice
                                     const void* K, const void* V, void* out, int64_t N, int64_t nnz,
                                     int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
     return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream);
+}
+
+extern "C" gtattn_status gtattn_fwd_ndh(const int32_t* indptr, const int32_t* indices, const void* Q,
+                                        const void* K, const void* V, void* out, int64_t N, int64_t nnz, int H,
+                                        int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
+    return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream, 1);
 }
 
 extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t* indptr,

@@ -49,6 +49,10 @@ struct Seg {
 constexpr int kMaxSegs = kNumBuckets + 2;
 constexpr float kLazyMax = 8.f;   // fused row kernel: slack of the running maximum (log2 units)
 
+// Head of feature element el of a node row: [N, H, D] rows are head-major
+// (el / D), [N, D, H] rows head-innermost (el % H).
+__device__ __forceinline__ int head_of(int el, int D, int H, int ndh) { return ndh ? el % H : el / D; }
+
 // Loads of data read once per call (the bias, and with GT_STREAM_HINTS the
 // indices and Q rows) use the streaming cache policy (evict first), so they
 // do not push the reused K/V rows out of the L2.
@@ -622,14 +626,16 @@ k_rows_generic(RowParams p) {
                 if constexpr (MODE != kSpmm) {
                     // eight interleaved partial sums, combined pairwise (error
                     // grows with D/8 instead of D)
-                    const float* pr = prod + h * D;
+                    // head h's D products: contiguous ([N, H, D]) or H apart ([N, D, H])
+                    const int st = p.ndh ? H : 1;
+                    const float* pr = prod + (p.ndh ? h : h * D);
                     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                     int d = 0;
                     for (; d + 8 <= D; d += 8) {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) a[k] += pr[d + k];
+                        for (int k = 0; k < 8; ++k) a[k] += pr[(d + k) * st];
                     }
-                    for (; d < D; ++d) a[0] += pr[d];
+                    for (; d < D; ++d) a[0] += pr[d * st];
                     l = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
                     if (p.values) l *= p.values[e];   // weighted adjacency
                 }
@@ -658,7 +664,7 @@ k_rows_generic(RowParams p) {
                 for (int k = 0; k < KPL; ++k) {
                     const int el = lane + 32 * k;
                     if (el < HD) {
-                        const int h = el / D;
+                        const int h = head_of(el, D, H, p.ndh);
                         acc[k] = acc[k] * hc[h] + hw[h] * load_elem(V, j * HD + el);
                     }
                 }
@@ -684,7 +690,7 @@ k_rows_generic(RowParams p) {
                 if (el < HD) {
                     float v = acc[k];
                     if (MODE == kFused) {
-                        const float s = hs[el / D];
+                        const float s = hs[head_of(el, D, H, p.ndh)];
                         v = s > 0.f ? v / s : 0.f;
                     }
                     store_elem(O, (int64_t)row * HD + el, v);
@@ -762,7 +768,7 @@ k_combine(RowParams p, int warp_rows) {
         const int Ge = kCombThreads / HD;   // element groups over the chunks
         if (Ge >= 2) {
             const int el = t % HD, g = t / HD;
-            const int h = el / D;
+            const int h = head_of(el, D, H, p.ndh);
             float v = 0.f;
             if (g < Ge) {
                 const float M = MODE == kFused ? sM[h] : 0.f;
@@ -793,7 +799,7 @@ k_combine(RowParams p, int warp_rows) {
             }
         } else {
             for (int el = t; el < HD; el += kCombThreads) {
-                const int h = el / D;
+                const int h = head_of(el, D, H, p.ndh);
                 const float M = MODE == kFused ? sM[h] : 0.f;
                 float v = 0.f;
 #pragma unroll 4
@@ -835,7 +841,7 @@ k_combine(RowParams p, int warp_rows) {
             }
             for (int el0 = 0; el0 < HD; el0 += 32) {
                 const int el = el0 + lane;
-                const int h = min(el, HD - 1) / D;
+                const int h = head_of(min(el, HD - 1), D, H, p.ndh);
                 const float Mh = __shfl_sync(kFull, M, h);
                 const float Sh = __shfl_sync(kFull, S, h);
                 if (el < HD) {

@@ -16,6 +16,7 @@ struct RowParams {
     const float* probs;     // SpMM mode: fp32 [nnz, H]
     const float* bias;      // fused / SDDMM modes: fp32 [nnz, H] added to the logits, or null
     const float* values;    // fused / SDDMM modes: fp32 [nnz] multiplying the dot products, or null
+    int ndh;                // 1: node rows are [D, H] (head innermost; generic kernel only)
     float* lse;             // fused mode: fp32 [N, H] row log-sum-exp (log2 units) written, or null;
                             // rows of one entry (copied) and of none are not written
     float* logits;          // SDDMM mode: fp32 [nnz, H]

@@ -175,6 +175,18 @@ gtattn_status gtattn_fwd_host(const int32_t* indptr, const int32_t* indices, con
                               int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
 
 /*
+ * gtattn_fwd_ndh -- gtattn_fwd on head-innermost node rows: Q, K, V and out
+ * are [N, D, H] (element (h, d) of row i at i*H*D + d*H + h), the layout the
+ * SparseMHA of "Graph Transformer in a Nutshell" reshapes its projections to
+ * (q.reshape(N, head_dim, num_heads)), so such callers need no transpose.
+ * Same arguments, results (up to rounding order) and errors as gtattn_fwd;
+ * runs the generic row kernel.
+ */
+gtattn_status gtattn_fwd_ndh(const int32_t* indptr, const int32_t* indices, const void* Q,
+                             const void* K, const void* V, void* out, int64_t N, int64_t nnz,
+                             int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
+
+/*
  * gtattn_fwd_plan -- as gtattn_fwd with a prebuilt plan: no binning per
  * call, and complete blocks (if the plan found any) go to the dense
  * tensor-core kernel when dtype is bf16 and D == 64.  indptr/indices must be

@@ -285,10 +285,82 @@ extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indice
     return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream);
 }
 
+// Row-local transpose between [N, D, H] and [N, H, D] (to_hd: from the
+// former): a warp per node row, the row read into shared memory with 16-byte
+// loads, each lane then gathering 16 bytes of the permuted row and storing
+// them at once (rows of 16-byte multiples, 16-byte aligned: the shapes the
+// vector row kernel takes).
+template <typename T>
+__global__ void __launch_bounds__(256)
+k_transpose_rows(const T* __restrict__ src, T* __restrict__ dst, int64_t n, int H, int D, int to_hd) {
+    constexpr int kPer = 16 / sizeof(T);   // elements per 16-byte piece
+    __shared__ __align__(16) T sm[8][kMaxHD];
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int HD = H * D, pieces = HD / kPer;
+    T* row_sm = sm[wid];
+    for (int64_t row = blockIdx.x * 8 + wid; row < n; row += static_cast<int64_t>(gridDim.x) * 8) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + row * HD);
+        for (int i = lane; i < pieces; i += 32) reinterpret_cast<uint4*>(row_sm)[i] = __ldg(s4 + i);
+        __syncwarp();
+        uint4* d4 = reinterpret_cast<uint4*>(dst + row * HD);
+        for (int i = lane; i < pieces; i += 32) {
+            __align__(16) T v[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int el = i * kPer + u;
+                int from;
+                if (to_hd) { const int h = el / D, d = el - h * D; from = d * H + h; }
+                else { const int d = el / H, h = el - d * H; from = h * D + d; }
+                v[u] = row_sm[from];
+            }
+            d4[i] = *reinterpret_cast<const uint4*>(v);
+        }
+        __syncwarp();
+    }
+}
+
+template <typename T>
+static cudaError_t transpose_rows(const void* src, void* dst, int64_t n, int H, int D, int to_hd, cudaStream_t s) {
+    const int blocks = static_cast<int>(std::min<int64_t>((n + 7) / 8, static_cast<int64_t>(num_sms()) * 8));
+    k_transpose_rows<T><<<std::max(blocks, 1), 256, 0, s>>>(static_cast<const T*>(src), static_cast<T*>(dst), n, H, D,
+                                                              to_hd);
+    return cudaGetLastError();
+}
+
 extern "C" gtattn_status gtattn_fwd_ndh(const int32_t* indptr, const int32_t* indices, const void* Q,
                                         const void* K, const void* V, void* out, int64_t N, int64_t nnz, int H,
                                         int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
-    return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream, 1);
+    GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    if (N == 0) return GTATTN_OK;
+    // Shapes the vector kernel tiles: transpose to [N, H, D] in scratch, the
+    // head-major forward, transpose the output back (four row-local copies,
+    // far cheaper than the generic kernel on head-innermost rows).  Others:
+    // the generic kernel reads the [N, D, H] rows directly.
+    const size_t esz = dtype == GTATTN_F32 ? 4 : 2, osz = dtype == GTATTN_BF16 ? 2 : 4;
+    const size_t in_bytes = align_up(esz * static_cast<size_t>(N) * H * D);
+    const size_t out_bytes = align_up(osz * static_cast<size_t>(N) * H * D);
+    RowChoice c;
+    void* buf = nullptr;
+    if (!choose_row_kernel(H, D, dtype, Q, K, V, out, GTATTN_KERNEL_AUTO, &c) || c.kind != RowKernel::kVector ||
+        pool_alloc(&buf, 3 * in_bytes + out_bytes, stream) != GTATTN_OK)
+        return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream, 1);
+    char* b = static_cast<char*>(buf);
+    void *q2 = b, *k2 = b + in_bytes, *v2 = b + 2 * in_bytes, *o2 = b + 3 * in_bytes;
+    auto tr = [&](const void* src, void* dst, size_t sz, int to_hd) {
+        return sz == 4 ? transpose_rows<float>(src, dst, N, H, D, to_hd, stream)
+                       : transpose_rows<__nv_bfloat16>(src, dst, N, H, D, to_hd, stream);
+    };
+    cudaError_t e = tr(Q, q2, esz, 1);
+    if (e == cudaSuccess) e = tr(K, k2, esz, 1);
+    if (e == cudaSuccess) e = tr(V, v2, esz, 1);
+    gtattn_status st = e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+    if (st == GTATTN_OK) st = fwd_fused(indptr, indices, q2, k2, v2, nullptr, nullptr, o2, N, nnz, H, D, scale, dtype, stream);
+    if (st == GTATTN_OK) {
+        e = tr(o2, out, osz, 0);
+        if (e != cudaSuccess) st = cuda_status(e);
+    }
+    pool_free(buf, stream);
+    return st;
 }
 
 extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t* indptr,

@@ -521,13 +521,13 @@ extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indice
     if (N == 0) return GTATTN_OK;
     const int HD = H * D;
     const size_t grad_bytes = sizeof(float) * static_cast<size_t>(N) * HD;
-    GT_CUDA(cudaMemsetAsync(dQ, 0, grad_bytes, stream));
-    GT_CUDA(cudaMemsetAsync(dK, 0, grad_bytes, stream));
-    GT_CUDA(cudaMemsetAsync(dV, 0, grad_bytes, stream));
     const void* ptrs[7] = {Q, K, V, dO, dQ, dK, dV};
     const gtattn_dtype fdt = dtype == GTATTN_F32 ? GTATTN_F32 : GTATTN_BF16_OUT_F32;   // fp32 forward output
     RowChoice c;
     if (!bwd_tasks_supported(H, D, dtype, ptrs, 7) || !choose_row_kernel(H, D, fdt, Q, K, V, dQ, GTATTN_KERNEL_AUTO, &c)) {
+        GT_CUDA(cudaMemsetAsync(dQ, 0, grad_bytes, stream));
+        GT_CUDA(cudaMemsetAsync(dK, 0, grad_bytes, stream));
+        GT_CUDA(cudaMemsetAsync(dV, 0, grad_bytes, stream));
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
         return launch_bwd_rows(indptr, indices, Q, K, V, dO, dQ, dK, dV, (int)N, H, D, scale, dtype, stream);
     }
@@ -539,15 +539,41 @@ extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indice
     int2 *chunks, *longs;
     GT_TRY(scratch_alloc(N, nnz, H, HD, o.long_row_min, o.chunk_edges, false, false, &sc, &hdr, &rows, &chunks,
                          &longs, stream));
+    // the backward's own scratch: O, L, (L, Dlt), the source-major pattern
+    // and its binning
+    int64_t n_long = 0, n_chunks = 0;
+    worst_case_sizes(N, nnz, o.long_row_min, o.chunk_edges, &n_long, &n_chunks);
+    size_t off = 0;
+    const size_t o_O = off; off = align_up(off + grad_bytes);
+    const size_t o_L = off; off = align_up(off + sizeof(float) * static_cast<size_t>(N) * H);
+    const size_t o_LD = off; off = align_up(off + sizeof(float2) * static_cast<size_t>(N) * H);
+    const size_t o_cp = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N + 1));
+    const size_t o_cur = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N));
+    const size_t o_ts = off; off = align_up(off + sizeof(int) * static_cast<size_t>(bwd_scan_tiles(N) + 1));
+    const size_t o_rid = off; off = align_up(off + sizeof(int) * static_cast<size_t>(nnz));
+    const size_t o_ch = off; off = align_up(off + sizeof(int) * HdrLayout::kWords);
+    const size_t o_cr = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N));
+    const size_t o_cc = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_chunks));
+    const size_t o_cl = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_long));
     void* ol = nullptr;
-    const size_t o_bytes = align_up(grad_bytes), l_bytes = align_up(sizeof(float) * static_cast<size_t>(N) * H);
-    gtattn_status st = pool_alloc(&ol, o_bytes + l_bytes, stream);
+    gtattn_status st = pool_alloc(&ol, off, stream);
     if (st != GTATTN_OK) {
         pool_free(sc.base, stream);
         return st;
     }
-    float* O = static_cast<float*>(ol);
-    float* lse = reinterpret_cast<float*>(static_cast<char*>(ol) + o_bytes);
+    char* bb = static_cast<char*>(ol);
+    float* O = reinterpret_cast<float*>(bb + o_O);
+    float* lse = reinterpret_cast<float*>(bb + o_L);
+    float2* LD = reinterpret_cast<float2*>(bb + o_LD);
+    int* colptr = reinterpret_cast<int*>(bb + o_cp);
+    int* cursor = reinterpret_cast<int*>(bb + o_cur);
+    int* tsum = reinterpret_cast<int*>(bb + o_ts);
+    int* rowid = reinterpret_cast<int*>(bb + o_rid);
+    int* chdr = reinterpret_cast<int*>(bb + o_ch);
+    int* ccols = reinterpret_cast<int*>(bb + o_cr);
+    int2* cchunks = reinterpret_cast<int2*>(bb + o_cc);
+    int2* clongs = reinterpret_cast<int2*>(bb + o_cl);
+    const TaskLists col_lists{chdr, ccols, cchunks, clongs, o.chunk_edges, 1};
     {
         ProfScope ps(GTATTN_KCAT_BIN, bin_launches((int)N, nullptr), stream);
         st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
@@ -563,9 +589,16 @@ extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indice
         st = launch_combine(kFused, fdt, p, stream);
     }
     if (st == GTATTN_OK) {
-        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
-        st = launch_bwd_tasks(indptr, indices, sc.lists, Q, K, V, dO, O, lse, dQ, dK, dV, (int)N, H, D, scale, dtype,
-                              stream);
+        ProfScope ps(GTATTN_KCAT_BIN, 4 + (nnz > 0) + bin_launches((int)N, nullptr), stream);
+        st = build_csc(indptr, indices, sc.lists, (int)N, nnz, colptr, cursor, tsum, rowid, dQ, HD, stream);
+        if (st == GTATTN_OK)
+            st = bin_rows(colptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, chdr, ccols, cchunks, clongs,
+                          stream);
+    }
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_ROWS, 2, stream);
+        st = launch_bwd_passes(indptr, indices, sc.lists, colptr, rowid, col_lists, clongs, Q, K, V, dO, O, lse, LD,
+                               dQ, dK, dV, (int)N, nnz, H, D, scale, dtype, stream);
     }
     pool_free(ol, stream);
     pool_free(sc.base, stream);

@@ -19,6 +19,11 @@
 #include "bwd.cuh"
 
 #include <algorithm>
+#include <mutex>
+#include <type_traits>
+#include <unordered_map>
+
+#include "rows.cuh"
 
 namespace gt {
 namespace {
@@ -146,41 +151,93 @@ gtattn_status launch_bwd_t(const int* indptr, const int* indices, const void* Q,
 
 
 // ---------------------------------------------------------------------------
-// task-parallel backward (the shapes the fused row kernel tiles)
+// two passes (the shapes the fused row kernel tiles)
 // ---------------------------------------------------------------------------
 // With the forward's output O and row log-sum-exp L (log2 units) at hand,
-//   p_e = 2^(s_e log2 e - L),   Dlt = sum_e p_e dp_e = dO_i . O_i,
-// so each entry's p and ds need only that entry: the work splits like the
-// forward's -- ordinary rows whole, rows above the split threshold in
-// 256-entry chunks -- one task per warp.  A lane holds E contiguous
-// features of a row (lph = D/E lanes per head, dot products reduced by xor
-// shuffles), loads them as 16-byte vectors and adds its dQ, dK, dV pieces
-// with float4 atomics (dQ once per task, dK_j and dV_j per entry).  A row of
-// one entry has p = 1 and ds = 0 (the forward wrote no L for it).
-template <typename T> struct Vec;
-template <> struct Vec<float> {
-    template <int E> __device__ static void load(const float* p, float* x) {
+//   p_e = 2^(s_e log2 e - L_i),   Dlt_i = sum_e p_e dp_e = dO_i . O_i,
+// so each entry's p and ds need only that entry and its row's (L_i, Dlt_i).
+// The gradients then split by where they are summed:
+//   pass 1, over destination rows (the forward's task lists): Dlt_i and
+//           dQ_i = scale sum_e ds_e k_j, summed in registers;
+//   pass 2, over source nodes, on a source-major copy of the pattern (colptr
+//           over sources, the destination row of every entry):
+//           dK_j = scale sum_e ds_e q_i and dV_j = sum_e p_e dO_i, summed in
+//           registers.
+// No gradient is scattered entry by entry.  Rows and sources above the split
+// threshold come in 256-entry chunks whose partial sums are added with float4
+// atomics (one per lane per chunk) onto rows zeroed beforehand; all others
+// are stored.  A row of one entry has p = 1 and ds = 0 exactly: pass 1 stores
+// dQ_i = 0 without reading K or V and marks the row with L_i = +inf, which
+// pass 2 reads as p = 1, ds = 0.
+//
+// A lane holds E contiguous features of a node row, loaded as 8- or 16-byte
+// vectors; a row spans G = H D / E lanes (a lane group), a head lph = D / E
+// of them, and per-head dot products are reduced by xor shuffles within the
+// group.
+
+// E features of one node row as loaded (bf16 stays packed: dot products as
+// mixed bf16 x bf16 -> fp32 FMAs, accumulation as f32x2 FMAs).
+template <typename T, int E> struct Raw;
+template <int E> struct Raw<float, E> {
+    float w[E];
+    __device__ __forceinline__ void load(const float* p) {
 #pragma unroll
         for (int k = 0; k < E / 4; ++k) {
             const float4 v = __ldg(reinterpret_cast<const float4*>(p) + k);
-            x[4 * k] = v.x; x[4 * k + 1] = v.y; x[4 * k + 2] = v.z; x[4 * k + 3] = v.w;
+            w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
         }
     }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int k = 0; k < E; ++k) w[k] = 0.f;
+    }
+    __device__ __forceinline__ float operator[](int k) const { return w[k]; }
+    // this . b (two interleaved fp32 sums)
+    __device__ __forceinline__ float dot(const Raw& b) const {
+        float x = 0.f, y = 0.f;
+#pragma unroll
+        for (int k = 0; k < E; k += 2) fma2(x, y, w[k], w[k + 1], b.w[k], b.w[k + 1]);
+        return x + y;
+    }
+    // acc += c * this
+    __device__ __forceinline__ void axpy(float* acc, float c) const {
+#pragma unroll
+        for (int k = 0; k < E; k += 2) fma2(acc[k], acc[k + 1], c, c, w[k], w[k + 1]);
+    }
 };
-template <> struct Vec<__nv_bfloat16> {
-    template <int E> __device__ static void load(const __nv_bfloat16* p, float* x) {
+template <int E> struct Raw<__nv_bfloat16, E> {
+    uint32_t w[E / 2];
+    __device__ __forceinline__ void load(const __nv_bfloat16* p) {
         if constexpr (E == 4) {
             const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
-            x[0] = bf16lo(v.x); x[1] = bf16hi(v.x); x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
+            w[0] = v.x; w[1] = v.y;
         } else {
 #pragma unroll
             for (int k = 0; k < E / 8; ++k) {
                 const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + k);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u) { x[8 * k + 2 * u] = bf16lo(w[u]); x[8 * k + 2 * u + 1] = bf16hi(w[u]); }
+                w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
             }
         }
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int k = 0; k < E / 2; ++k) w[k] = 0u;
+    }
+    __device__ __forceinline__ float operator[](int k) const {
+        return (k & 1) ? bf16hi(w[k >> 1]) : bf16lo(w[k >> 1]);
+    }
+    __device__ __forceinline__ float dot(const Raw& b) const {
+        float x = 0.f, y = 0.f;
+#pragma unroll
+        for (int k = 0; k < E / 2; k += 2) {
+            x = dot2_bf16(w[k], b.w[k], x);
+            y = dot2_bf16(w[k + 1], b.w[k + 1], y);
+        }
+        return x + y;
+    }
+    __device__ __forceinline__ void axpy(float* acc, float c) const {
+#pragma unroll
+        for (int k = 0; k < E / 2; ++k) axpy2_bf16(acc[2 * k], acc[2 * k + 1], c, w[k]);
     }
 };
 
@@ -192,81 +249,381 @@ __device__ __forceinline__ void atomic_add_vec(float* dst, const float* x, float
                   make_float4(c * x[4 * k], c * x[4 * k + 1], c * x[4 * k + 2], c * x[4 * k + 3]));
 }
 
+template <int E>
+__device__ __forceinline__ void store_vec(float* dst, const float* x, float c) {
+#pragma unroll
+    for (int k = 0; k < E / 4; ++k)
+        reinterpret_cast<float4*>(dst)[k] =
+            make_float4(c * x[4 * k], c * x[4 * k + 1], c * x[4 * k + 2], c * x[4 * k + 3]);
+}
+
+// zeroes node row `r` (HD floats) with the warp's lanes
+__device__ __forceinline__ void zero_row(float* a, int64_t r, int HD, int lane) {
+    float4* p = reinterpret_cast<float4*>(a + r * HD);
+    for (int k = lane; k < HD / 4; k += 32) p[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 constexpr int kTaskWarps = 8;
 
-template <typename T, int E>
+// One task of a binning's lists: a whole row (t < n_rows) or one chunk of a
+// split row.  `whole` is false for chunks; `first` for whole rows and the
+// first chunk of a split row.
+struct Task {
+    int row, beg, end;
+    bool whole, first;
+};
+__device__ __forceinline__ Task task_at(int t, int n_rows, const int* __restrict__ ptr, const int* __restrict__ rows,
+                                        const int2* __restrict__ chunks, int chunk_edges) {
+    Task k;
+    if (t < n_rows) {
+        k.row = rows[t];
+        k.beg = ptr[k.row];
+        k.end = ptr[k.row + 1];
+        k.whole = k.first = true;
+    } else {
+        const int2 c = chunks[t - n_rows];
+        k.row = c.x;
+        k.beg = c.y;
+        const int re = ptr[c.x + 1];
+        k.end = min(c.y + chunk_edges, re);
+        k.whole = false;
+        k.first = c.y == ptr[c.x];
+    }
+    return k;
+}
+
+// ---- source-major copy of the pattern -------------------------------------
+// entries per source: cnt[j] += 1 (cnt zeroed); indices outside [0, N) are
+// skipped here and by the scatter alike
+__global__ void k_col_count(const int* __restrict__ indices, int64_t nnz, int N, int* __restrict__ cnt) {
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < nnz; e += (int64_t)gridDim.x * blockDim.x) {
+        const int j = __ldg(indices + e);
+        if ((unsigned)j < (unsigned)N) atomicAdd(cnt + j, 1);
+    }
+}
+
+constexpr int kScanThreads = 256;
+constexpr int kScanItems = 8;
+constexpr int kScanTile = kScanThreads * kScanItems;
+
+// exclusive scan of one value per thread over a kScanThreads block; *total
+// receives the block's sum
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total) {
+    __shared__ int warp_sum[kScanThreads / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sum[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int w = lane < kScanThreads / 32 ? warp_sum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < kScanThreads / 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kScanThreads / 32) warp_sum[lane] = w;   // inclusive warp prefix
+    }
+    __syncthreads();
+    const int before = wid > 0 ? warp_sum[wid - 1] : 0;
+    *total = warp_sum[kScanThreads / 32 - 1];
+    __syncthreads();   // warp_sum is reused by the next call
+    return before + x - v;
+}
+
+// per-tile sums of cnt
+__global__ void __launch_bounds__(kScanThreads) k_scan_sums(const int* __restrict__ cnt, int N, int* __restrict__ tsum) {
+    const int64_t base = (int64_t)blockIdx.x * kScanTile + threadIdx.x * kScanItems;
+    int v = 0;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k)
+        if (base + k < N) v += cnt[base + k];
+    int total;
+    block_exclusive_scan(v, &total);
+    if (threadIdx.x == 0) tsum[blockIdx.x] = total;
+}
+
+// exclusive scan of the tile sums in place (one block); colptr[N] = total
+__global__ void __launch_bounds__(kScanThreads) k_scan_top(int* __restrict__ tsum, int n_tiles,
+                                                          int* __restrict__ colptr, int N) {
+    int carry = 0;
+    for (int b0 = 0; b0 < n_tiles; b0 += kScanTile) {
+        const int base = b0 + threadIdx.x * kScanItems;
+        int x[kScanItems], v = 0;
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            x[k] = base + k < n_tiles ? tsum[base + k] : 0;
+            v += x[k];
+        }
+        int total;
+        int run = carry + block_exclusive_scan(v, &total);
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            if (base + k < n_tiles) tsum[base + k] = run;
+            run += x[k];
+        }
+        carry += total;
+    }
+    if (threadIdx.x == 0) colptr[N] = carry;
+}
+
+// colptr[j] = cursor[j] = exclusive prefix of cnt (cnt may alias cursor)
+__global__ void __launch_bounds__(kScanThreads) k_scan_apply(const int* cnt, int N, const int* __restrict__ tsum,
+                                                            int* __restrict__ colptr, int* cursor) {
+    const int64_t base = (int64_t)blockIdx.x * kScanTile + threadIdx.x * kScanItems;
+    int x[kScanItems], v = 0;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+        x[k] = base + k < N ? cnt[base + k] : 0;
+        v += x[k];
+    }
+    int total;
+    int run = tsum[blockIdx.x] + block_exclusive_scan(v, &total);
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+        if (base + k < N) {
+            colptr[base + k] = run;
+            cursor[base + k] = run;
+        }
+        run += x[k];
+    }
+}
+
+// rowid[slot] = destination row of each entry, slots taken per source from
+// cursor (so the order within a source is arbitrary); also zeroes dQ of the
+// split rows, which pass 1 adds to
 __global__ void __launch_bounds__(kTaskWarps * 32)
-k_bwd_tasks(const int* __restrict__ indptr, const int* __restrict__ indices, const int* __restrict__ hdr,
-            const int* __restrict__ rows, const int2* __restrict__ chunks, int chunk_edges,
-            const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
-            const float* __restrict__ O, const float* __restrict__ L, float* __restrict__ dQ,
-            float* __restrict__ dK, float* __restrict__ dV, int H, int lph, float scale) {
-    const unsigned full = 0xffffffffu;
+k_csc_scatter(const int* __restrict__ indptr, const int* __restrict__ indices, const int* __restrict__ hdr,
+              const int* __restrict__ rows, const int2* __restrict__ chunks, int chunk_edges, int N,
+              int* __restrict__ cursor, int* __restrict__ rowid, float* __restrict__ dQ, int HD) {
     const int lane = threadIdx.x & 31;
-    const int HD = 32 * E;
-    const int head = lane / lph;
-    const float sl2 = scale * kLog2e;
-    const int n_rows = hdr[HdrLayout::kDenseSeg];   // the bucketed rows (no dense segment here)
+    const int n_rows = hdr[HdrLayout::kDenseSeg];
     const int n_tasks = n_rows + hdr[HdrLayout::kChunks];
+    for (int t = blockIdx.x * kTaskWarps + (threadIdx.x >> 5); t < n_tasks; t += gridDim.x * kTaskWarps) {
+        const Task k = task_at(t, n_rows, indptr, rows, chunks, chunk_edges);
+        for (int e0 = k.beg + lane; e0 < k.end; e0 += 4 * 32) {   // four slots in flight a lane
+            int j[4], at[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) j[u] = e0 + 32 * u < k.end ? __ldg(indices + e0 + 32 * u) : -1;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) at[u] = (unsigned)j[u] < (unsigned)N ? atomicAdd(cursor + j[u], 1) : -1;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (at[u] >= 0) rowid[at[u]] = k.row;
+        }
+        if (!k.whole && k.first) zero_row(dQ, k.row, HD, lane);
+    }
+}
+
+// Both passes give each lane group (G lanes, E features a lane) a task of
+// its own: the warp takes S = 32 / G consecutive tasks -- split-row chunks
+// first, then the rows from the heaviest bucket down, so the S tasks have
+// nearly the same length -- and walks them side by side in one warp-uniform
+// loop, U entries a group per step with the next step's indices in flight.
+// A group whose task is shorter (or absent) runs its remaining steps with
+// every load predicated off.
+__device__ __forceinline__ Task group_task(int t, int n_tasks, int n_chunks, const int* __restrict__ ptr,
+                                           const int* __restrict__ rows, const int2* __restrict__ chunks,
+                                           int chunk_edges) {
+    if (t >= n_tasks) return Task{-1, 0, 0, false, false};
+    if (t < n_chunks) return task_at(n_tasks + t - n_chunks, n_tasks - n_chunks, ptr, rows, chunks, chunk_edges);
+    return task_at(t - n_chunks, n_tasks - n_chunks, ptr, rows, chunks, chunk_edges);
+}
+
+// ---- pass 1: by destination row ------------------------------------------
+// Also zeroes dK and dV of the split sources (listed by the source binning),
+// which pass 2 adds to.
+template <typename T, int E, int U>
+__global__ void __launch_bounds__(kTaskWarps * 32)
+k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const int* __restrict__ hdr,
+         const int* __restrict__ rows, const int2* __restrict__ chunks, int chunk_edges,
+         const int* __restrict__ col_hdr, const int2* __restrict__ col_longs, const T* __restrict__ Q,
+         const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO, const float* __restrict__ O,
+         const float* __restrict__ L, float2* __restrict__ LD, float* __restrict__ dQ, float* __restrict__ dK,
+         float* __restrict__ dV, int H, int G, int lph, float scale) {
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gl = lane & (G - 1), slot = lane / G, S = 32 / G;
+    const int HD = G * E;
+    const int head = gl / lph;
+    const bool head_lead = gl % lph == 0;
+    const float sl2 = scale * kLog2e;
     auto reduce = [&](float v) {
         for (int o = 1; o < lph; o <<= 1) v += __shfl_xor_sync(full, v, o);
         return v;
     };
-    for (int t = blockIdx.x * kTaskWarps + (threadIdx.x >> 5); t < n_tasks; t += gridDim.x * kTaskWarps) {
-        int row, beg, end;
-        if (t < n_rows) {
-            row = rows[t];
-            beg = indptr[row];
-            end = indptr[row + 1];
+    const int n_chunks = hdr[HdrLayout::kChunks];
+    const int n_tasks = hdr[HdrLayout::kDenseSeg] + n_chunks;
+    for (int t0 = (blockIdx.x * kTaskWarps + warp) * S; t0 < n_tasks; t0 += gridDim.x * kTaskWarps * S) {
+        Task k = group_task(t0 + slot, n_tasks, n_chunks, indptr, rows, chunks, chunk_edges);
+        const int64_t off = static_cast<int64_t>(k.row) * HD + gl * E;
+        const int deg = k.row >= 0 ? indptr[k.row + 1] - indptr[k.row] : 0;
+        if (k.row >= 0 && deg <= 1) {   // never split: dQ_i = 0; a row of one entry is marked for pass 2
+            float z[E];
+#pragma unroll
+            for (int u = 0; u < E; ++u) z[u] = 0.f;
+            store_vec<E>(dQ + off, z, 0.f);
+            if (deg == 1 && head_lead) LD[static_cast<int64_t>(k.row) * H + head] = make_float2(INFINITY, 0.f);
+        }
+        const bool walk = deg > 1;
+        if (!walk) k.beg = k.end = 0;
+        Raw<T, E> q, g;
+        Raw<float, E> o;
+        float lse = 0.f;
+        if (walk) {
+            q.load(Q + off);
+            g.load(dO + off);
+            o.load(O + off);
+            lse = L[static_cast<int64_t>(k.row) * H + head];
         } else {
-            const int2 c = chunks[t - n_rows];
-            row = c.x;
-            beg = c.y;
-            end = min(beg + chunk_edges, indptr[row + 1]);
+            q.zero();
+            g.zero();
+            o.zero();
         }
-        if (end <= beg) continue;   // uniform over the warp (one task per warp)
-        const bool single = indptr[row + 1] - indptr[row] == 1;
-        const int64_t off = static_cast<int64_t>(row) * HD + lane * E;
-        float q[E], g[E], o[E], dq[E];
-        Vec<T>::template load<E>(Q + off, q);
-        Vec<T>::template load<E>(dO + off, g);
-        Vec<float>::template load<E>(O + off, o);
-        // Dlt = dO_i . O_i (this head), summed exactly as dp below, so that a
-        // row of one entry (O_i = v_j) gets dp - Dlt = 0 exactly
-        float la = 0.f, lb = 0.f;
+        // Dlt = dO_i . O_i (this head)
+        float dl;
+        {
+            float x = 0.f, y = 0.f;
 #pragma unroll
-        for (int k = 0; k < E; k += 2) {
-            la = fmaf(g[k], o[k], la);
-            lb = fmaf(g[k + 1], o[k + 1], lb);
-        }
-#pragma unroll
-        for (int k = 0; k < E; ++k) dq[k] = 0.f;
-        const float dl = reduce(la + lb);
-        const float lse = single ? 0.f : L[static_cast<int64_t>(row) * H + head];
-        int jn = __ldg(indices + beg);
-        for (int e = beg; e < end; ++e) {
-            const int64_t j = jn;
-            if (e + 1 < end) jn = __ldg(indices + e + 1);      // the next index, off the critical path
-            float kx[E], vx[E];
-            Vec<T>::template load<E>(K + j * HD + lane * E, kx);
-            Vec<T>::template load<E>(V + j * HD + lane * E, vx);
-            float sa = 0.f, sb = 0.f, da = 0.f, db = 0.f;
-#pragma unroll
-            for (int k = 0; k < E; k += 2) {
-                sa = fmaf(q[k], kx[k], sa);
-                sb = fmaf(q[k + 1], kx[k + 1], sb);
-                da = fmaf(g[k], vx[k], da);
-                db = fmaf(g[k + 1], vx[k + 1], db);
+            for (int u = 0; u < E; u += 2) {
+                x = fmaf(g[u], o[u], x);
+                y = fmaf(g[u + 1], o[u + 1], y);
             }
-            const float s = reduce(sa + sb), dp = reduce(da + db);
-            const float p = single ? 1.f : exp2f(s * sl2 - lse);
-            const float ds = p * (dp - dl);
-#pragma unroll
-            for (int k = 0; k < E; ++k) dq[k] = fmaf(ds, kx[k], dq[k]);
-            atomic_add_vec<E>(dK + j * HD + lane * E, q, scale * ds);
-            atomic_add_vec<E>(dV + j * HD + lane * E, g, p);
+            dl = reduce(x + y);
         }
-        atomic_add_vec<E>(dQ + off, dq, scale);
+        if (walk && k.first && head_lead) LD[static_cast<int64_t>(k.row) * H + head] = make_float2(lse, dl);
+        float dq[E];
+#pragma unroll
+        for (int u = 0; u < E; ++u) dq[u] = 0.f;
+        const int steps = __reduce_max_sync(full, (k.end - k.beg + U - 1) / U);
+        int jn[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) jn[u] = k.beg + u < k.end ? __ldg(indices + k.beg + u) : -1;
+        for (int it = 0; it < steps; ++it) {
+            const int b = k.beg + it * U;
+            int j[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                j[u] = jn[u];
+                jn[u] = b + U + u < k.end ? __ldg(indices + b + U + u) : -1;
+            }
+            Raw<T, E> kx[U], vx[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (j[u] >= 0) {
+                    kx[u].load(K + static_cast<int64_t>(j[u]) * HD + gl * E);
+                    vx[u].load(V + static_cast<int64_t>(j[u]) * HD + gl * E);
+                } else {
+                    kx[u].zero();
+                    vx[u].zero();
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float s = reduce(q.dot(kx[u])), dp = reduce(g.dot(vx[u]));
+                const float p = exp2f(s * sl2 - lse);
+                const float ds = j[u] >= 0 ? p * (dp - dl) : 0.f;
+                kx[u].axpy(dq, ds);
+            }
+        }
+        if (walk) {
+            if (k.whole) store_vec<E>(dQ + off, dq, scale);
+            else atomic_add_vec<E>(dQ + off, dq, scale);
+        }
+    }
+    // split sources: zero their dK, dV rows for pass 2's atomics
+    const int n_long = col_hdr[HdrLayout::kLong];
+    for (int c = blockIdx.x * kTaskWarps + warp; c < n_long; c += gridDim.x * kTaskWarps) {
+        const int j = col_longs[c].x;
+        zero_row(dK, j, HD, lane);
+        zero_row(dV, j, HD, lane);
+    }
+}
+
+// ---- pass 2: by source node ------------------------------------------------
+template <typename T, int E, int U>
+__global__ void __launch_bounds__(kTaskWarps * 32)
+k_bwd_dkv(const int* __restrict__ colptr, const int* __restrict__ rowid, const int* __restrict__ hdr,
+          const int* __restrict__ cols, const int2* __restrict__ chunks, int chunk_edges,
+          const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
+          const float2* __restrict__ LD, float* __restrict__ dK, float* __restrict__ dV, int H, int G, int lph,
+          float scale) {
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gl = lane & (G - 1), slot = lane / G, S = 32 / G;
+    const int HD = G * E;
+    const int head = gl / lph;
+    const float sl2 = scale * kLog2e;
+    auto reduce = [&](float v) {
+        for (int o = 1; o < lph; o <<= 1) v += __shfl_xor_sync(full, v, o);
+        return v;
+    };
+    const int n_chunks = hdr[HdrLayout::kChunks];
+    const int n_tasks = hdr[HdrLayout::kDenseSeg] + n_chunks;
+    for (int t0 = (blockIdx.x * kTaskWarps + warp) * S; t0 < n_tasks; t0 += gridDim.x * kTaskWarps * S) {
+        const Task k = group_task(t0 + slot, n_tasks, n_chunks, colptr, cols, chunks, chunk_edges);
+        const int64_t off = static_cast<int64_t>(k.row) * HD + gl * E;
+        float dk[E], dv[E];
+#pragma unroll
+        for (int u = 0; u < E; ++u) dk[u] = dv[u] = 0.f;
+        Raw<T, E> kj, vj;
+        if (k.end > k.beg) {
+            kj.load(K + off);
+            vj.load(V + off);
+        } else {
+            kj.zero();
+            vj.zero();
+        }
+        const int steps = __reduce_max_sync(full, (k.end - k.beg + U - 1) / U);
+        int in[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) in[u] = k.beg + u < k.end ? __ldg(rowid + k.beg + u) : -1;
+        for (int it = 0; it < steps; ++it) {
+            const int b = k.beg + it * U;
+            int i[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                i[u] = in[u];
+                in[u] = b + U + u < k.end ? __ldg(rowid + b + U + u) : -1;
+            }
+            Raw<T, E> qx[U], gx[U];
+            float2 ld[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (i[u] >= 0) {
+                    qx[u].load(Q + static_cast<int64_t>(i[u]) * HD + gl * E);
+                    gx[u].load(dO + static_cast<int64_t>(i[u]) * HD + gl * E);
+                    ld[u] = __ldg(LD + static_cast<int64_t>(i[u]) * H + head);
+                } else {
+                    qx[u].zero();
+                    gx[u].zero();
+                    ld[u] = make_float2(0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float s = reduce(qx[u].dot(kj)), dp = reduce(gx[u].dot(vj));
+                const bool single = ld[u].x == INFINITY;
+                float p = single ? 1.f : exp2f(s * sl2 - ld[u].x);
+                float ds = single ? 0.f : p * (dp - ld[u].y);
+                if (i[u] < 0) p = ds = 0.f;
+                qx[u].axpy(dk, ds);
+                gx[u].axpy(dv, p);
+            }
+        }
+        if (k.row >= 0) {
+            if (k.whole) {
+                store_vec<E>(dK + off, dk, scale);
+                store_vec<E>(dV + off, dv, 1.f);
+            } else {
+                atomic_add_vec<E>(dK + off, dk, scale);
+                atomic_add_vec<E>(dV + off, dv, 1.f);
+            }
+        }
     }
 }
 }  // namespace
@@ -281,43 +638,127 @@ gtattn_status launch_bwd_rows(const int* indptr, const int* indices, const void*
     return launch_bwd_t<__nv_bfloat16>(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, H, D, scale, s);
 }
 
-bool bwd_tasks_supported(int H, int D, gtattn_dtype dtype, const void* const* ptrs, int n_ptrs) {
+// Features a lane holds (E) and lanes a node row spans (G = H D / E): 16
+// features where the row is 16 to 512 wide and splits into whole heads of
+// power-of-two lane counts, else the row over the whole warp.
+static bool bwd_layout(int H, int D, int* E, int* G) {
+    auto pow2 = [](int x) { return x > 0 && (x & (x - 1)) == 0; };
     const int HD = H * D;
+    for (int e : {16, 32}) {
+        if (HD % e == 0 && D % e == 0 && pow2(HD / e) && HD / e <= 32 && pow2(D / e)) {
+            *E = e;
+            *G = HD / e;
+            return true;
+        }
+    }
     if (HD % 32 != 0) return false;
-    const int E = HD / 32;
-    if ((E != 4 && E != 8 && E != 16 && E != 32) || D % E != 0) return false;
-    const int lph = D / E;
-    if (lph & (lph - 1)) return false;
-    if (dtype == GTATTN_F32 && E < 4) return false;
+    const int e = HD / 32;
+    if ((e != 4 && e != 8) || D % e != 0 || !pow2(D / e)) return false;
+    *E = e;
+    *G = 32;
+    return true;
+}
+
+bool bwd_tasks_supported(int H, int D, gtattn_dtype dtype, const void* const* ptrs, int n_ptrs) {
+    int E, G;
+    if (!bwd_layout(H, D, &E, &G)) return false;
+    (void)dtype;
     uintptr_t al = 0;
     for (int i = 0; i < n_ptrs; ++i) al |= reinterpret_cast<uintptr_t>(ptrs[i]);
     return (al & 15u) == 0;
 }
 
-gtattn_status launch_bwd_tasks(const int* indptr, const int* indices, const TaskLists& L, const void* Q,
-                               const void* K, const void* V, const void* dO, const float* O, const float* lse,
-                               float* dQ, float* dK, float* dV, int N, int H, int D, float scale, gtattn_dtype dtype,
-                               cudaStream_t s) {
-    const int E = H * D / 32, lph = D / E;
-    const int blocks = num_sms() * 8;
-    auto go = [&](auto kernel, auto tag) {
+int64_t bwd_scan_tiles(int64_t N) { return (N + kScanTile - 1) / kScanTile; }
+
+// resident blocks of `kernel` on the whole GPU (cached per kernel), capped by
+// the tasks there can be (a warp per task)
+template <typename Kern>
+static int task_grid(Kern kernel, int task_bound) {
+    static std::mutex mu;
+    static std::unordered_map<const void*, int> cache;
+    int grid;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(reinterpret_cast<const void*>(kernel));
+        if (it != cache.end()) {
+            grid = it->second;
+        } else {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kTaskWarps * 32, 0) != cudaSuccess ||
+                per_sm < 1)
+                per_sm = 1;
+            grid = per_sm * num_sms();
+            cache[reinterpret_cast<const void*>(kernel)] = grid;
+        }
+    }
+    const int need = (task_bound + kTaskWarps - 1) / kTaskWarps;
+    return std::max(1, std::min(grid, need));
+}
+
+gtattn_status build_csc(const int* indptr, const int* indices, const TaskLists& L, int N, int64_t nnz,
+                        int* colptr, int* cursor, int* tsum, int* rowid, float* dQ, int HD, cudaStream_t s) {
+    GT_CUDA(cudaMemsetAsync(cursor, 0, sizeof(int) * static_cast<size_t>(N), s));
+    if (nnz > 0) {
+        const int64_t want = (nnz + 255) / 256;
+        const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(num_sms()) * 8));
+        k_col_count<<<blocks, 256, 0, s>>>(indices, nnz, N, cursor);
+        GT_CUDA(cudaGetLastError());
+    }
+    const int nt = static_cast<int>(bwd_scan_tiles(N));
+    k_scan_sums<<<nt, kScanThreads, 0, s>>>(cursor, N, tsum);
+    GT_CUDA(cudaGetLastError());
+    k_scan_top<<<1, kScanThreads, 0, s>>>(tsum, nt, colptr, N);
+    GT_CUDA(cudaGetLastError());
+    k_scan_apply<<<nt, kScanThreads, 0, s>>>(cursor, N, tsum, colptr, cursor);
+    GT_CUDA(cudaGetLastError());
+    const int grid = task_grid(k_csc_scatter, row_task_bound(N, nnz, L.chunk_edges));
+    k_csc_scatter<<<grid, kTaskWarps * 32, 0, s>>>(indptr, indices, L.hdr, L.rows, L.chunks, L.chunk_edges, N,
+                                                   cursor, rowid, dQ, HD);
+    GT_CUDA(cudaGetLastError());
+    return GTATTN_OK;
+}
+
+gtattn_status launch_bwd_passes(const int* indptr, const int* indices, const TaskLists& rows, const int* colptr,
+                                const int* rowid, const TaskLists& cols, const int2* col_longs, const void* Q,
+                                const void* K, const void* V, const void* dO, const float* O, const float* lse,
+                                float2* LD, float* dQ, float* dK, float* dV, int N, int64_t nnz, int H, int D,
+                                float scale, gtattn_dtype dtype, cudaStream_t s) {
+    int E = 0, G = 0;
+    if (!bwd_layout(H, D, &E, &G)) return GTATTN_ERR_UNSUPPORTED;
+    const int lph = D / E;
+    const int bound_r = row_task_bound(N, nnz, rows.chunk_edges), bound_c = row_task_bound(N, nnz, cols.chunk_edges);
+    auto go = [&](auto tag, auto e_tag) -> cudaError_t {
         using T = decltype(tag);
-        kernel<<<blocks, kTaskWarps * 32, 0, s>>>(indptr, indices, L.hdr, L.rows, L.chunks, L.chunk_edges,
-                                                   static_cast<const T*>(Q), static_cast<const T*>(K),
-                                                   static_cast<const T*>(V), static_cast<const T*>(dO), O, lse, dQ,
-                                                   dK, dV, H, lph, scale);
+        constexpr int EE = decltype(e_tag)::value;
+        // entries in flight per lane group: the registers of U packed rows
+        constexpr int U = sizeof(T) == 2 ? (EE <= 16 ? 2 : 1) : (EE <= 8 ? 2 : 1);
+        const T* q = static_cast<const T*>(Q);
+        const T* k = static_cast<const T*>(K);
+        const T* v = static_cast<const T*>(V);
+        const T* g = static_cast<const T*>(dO);
+        auto k1 = k_bwd_dq<T, EE, U>;
+        k1<<<task_grid(k1, bound_r), kTaskWarps * 32, 0, s>>>(indptr, indices, rows.hdr, rows.rows, rows.chunks,
+                                                               rows.chunk_edges, cols.hdr, col_longs, q, k, v, g, O,
+                                                               lse, LD, dQ, dK, dV, H, G, lph, scale);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        auto k2 = k_bwd_dkv<T, EE, U>;
+        k2<<<task_grid(k2, bound_c), kTaskWarps * 32, 0, s>>>(colptr, rowid, cols.hdr, cols.rows, cols.chunks,
+                                                               cols.chunk_edges, q, k, v, g, LD, dK, dV, H, G, lph,
+                                                               scale);
         return cudaGetLastError();
     };
+    using B = __nv_bfloat16;
+    using I4 = std::integral_constant<int, 4>;
+    using I8 = std::integral_constant<int, 8>;
+    using I16 = std::integral_constant<int, 16>;
+    using I32 = std::integral_constant<int, 32>;
     cudaError_t e;
     if (dtype == GTATTN_F32) {
-        e = E == 4 ? go(k_bwd_tasks<float, 4>, float{}) : E == 8 ? go(k_bwd_tasks<float, 8>, float{})
-          : E == 16 ? go(k_bwd_tasks<float, 16>, float{}) : go(k_bwd_tasks<float, 32>, float{});
+        e = E == 4 ? go(float{}, I4{}) : E == 8 ? go(float{}, I8{}) : E == 16 ? go(float{}, I16{}) : go(float{}, I32{});
     } else {
-        using B = __nv_bfloat16;
-        e = E == 4 ? go(k_bwd_tasks<B, 4>, B{}) : E == 8 ? go(k_bwd_tasks<B, 8>, B{})
-          : E == 16 ? go(k_bwd_tasks<B, 16>, B{}) : go(k_bwd_tasks<B, 32>, B{});
+        e = E == 4 ? go(B{}, I4{}) : E == 8 ? go(B{}, I8{}) : E == 16 ? go(B{}, I16{}) : go(B{}, I32{});
     }
-    (void)N;
     return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
 }
 

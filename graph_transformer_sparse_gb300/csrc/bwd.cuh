@@ -13,17 +13,31 @@ gtattn_status launch_bwd_rows(const int* indptr, const int* indices, const void*
                               const void* dO, float* dQ, float* dK, float* dV, int N, int H, int D, float scale,
                               gtattn_dtype dtype, cudaStream_t s);
 
-// Whether the task-parallel backward handles the shape: H*D = 32 E with E in
+// Whether the two-pass backward handles the shape: H*D = 32 E with E in
 // {4, 8, 16, 32}, D a multiple of E with D/E a power of two, every pointer
 // 16-byte aligned.
 bool bwd_tasks_supported(int H, int D, gtattn_dtype dtype, const void* const* ptrs, int n_ptrs);
 
-// Task-parallel backward over the binning's task lists, given the forward's
-// fp32 output O and row log-sum-exp (log2 units).  dQ, dK, dV are added to
-// (zero them first).
-gtattn_status launch_bwd_tasks(const int* indptr, const int* indices, const TaskLists& L, const void* Q,
-                               const void* K, const void* V, const void* dO, const float* O, const float* lse,
-                               float* dQ, float* dK, float* dV, int N, int H, int D, float scale, gtattn_dtype dtype,
-                               cudaStream_t s);
+// Tiles of the scan that lays out the source-major pattern (the size of its
+// tile-sum array).
+int64_t bwd_scan_tiles(int64_t N);
+
+// Source-major copy of the pattern on stream s: colptr [N+1] over sources and
+// rowid [nnz], the destination row of each entry, in arbitrary order within a
+// source.  cursor [N] and tsum [bwd_scan_tiles(N)] are scratch; L are the
+// destination binning's task lists.  Also zeroes dQ of L's split rows.
+gtattn_status build_csc(const int* indptr, const int* indices, const TaskLists& L, int N, int64_t nnz,
+                        int* colptr, int* cursor, int* tsum, int* rowid, float* dQ, int HD, cudaStream_t s);
+
+// The two passes, given the forward's fp32 output O and row log-sum-exp
+// (log2 units): dQ by destination row over `rows`, dK and dV by source over
+// `cols` (the binning of colptr; col_longs its split sources).  LD [N*H] is
+// scratch, (L_i, Dlt_i) per row and head.  Every row of dQ, dK and dV is
+// written; only dQ's split rows must be zero beforehand (build_csc does it).
+gtattn_status launch_bwd_passes(const int* indptr, const int* indices, const TaskLists& rows, const int* colptr,
+                                const int* rowid, const TaskLists& cols, const int2* col_longs, const void* Q,
+                                const void* K, const void* V, const void* dO, const float* O, const float* lse,
+                                float2* LD, float* dQ, float* dK, float* dV, int N, int64_t nnz, int H, int D,
+                                float scale, gtattn_dtype dtype, cudaStream_t s);
 
 }  // namespace gt

@@ -143,35 +143,6 @@ struct Frag {
     }
 };
 
-// c + a.lo*b.lo + a.hi*b.hi for two packed bf16 pairs: products of bf16
-// values are exact in fp32, the sums are fp32 (mixed-precision FMA).
-__device__ __forceinline__ float dot2_bf16(uint32_t a, uint32_t b, float c) {
-    float r;
-    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
-        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, al, bl, %3;\n\t"
-        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
-        : "=f"(r)
-        : "r"(a), "r"(b), "f"(c));
-    return r;
-}
-// (a0, a1) += w * (v.lo, v.hi) for a packed bf16 pair v: one f32x2 FMA.
-__device__ __forceinline__ void axpy2_bf16(float& a0, float& a1, float w, uint32_t v) {
-    asm("{\n\t.reg .b64 rv, rw, ra;\n\t.reg .b32 lo, hi;\n\t"
-        "shl.b32 lo, %3, 16;\n\tand.b32 hi, %3, 0xffff0000;\n\t"
-        "mov.b64 rv, {lo, hi};\n\tmov.b64 rw, {%2, %2};\n\tmov.b64 ra, {%0, %1};\n\t"
-        "fma.rn.f32x2 ra, rv, rw, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(w), "r"(v));
-}
-// (a0, a1) += (x0, x1) * (y0, y1): one f32x2 FMA.
-__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float y0, float y1) {
-    asm("{\n\t.reg .b64 rx, ry, ra;\n\t"
-        "mov.b64 rx, {%2, %3};\n\tmov.b64 ry, {%4, %5};\n\tmov.b64 ra, {%0, %1};\n\t"
-        "fma.rn.f32x2 ra, rx, ry, ra;\n\tmov.b64 {%0, %1}, ra;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
-}
 // (a0, a1) *= c: one f32x2 multiply.
 __device__ __forceinline__ void scale2(float& a0, float& a1, float c) {
     asm("{\n\t.reg .b64 rc, ra;\n\t"

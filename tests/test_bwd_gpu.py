@@ -3,10 +3,10 @@ Q, K, V from the CUDA path against the fp64 oracle backward (itself pinned
 by finite differences of the forward oracle) on the same inputs.
 
 Tolerance (the pages state none for gradients): |g - o| <= 1e-4 |o| + 1e-5
-max|o| per tensor.  The gradients are fp32 sums of many signed terms (dK and
-dV accumulated by atomic adds in no fixed order, ds = p (dp - sum p dp) with
-cancellation), so their error is relative to the size of the terms rather
-than to each element."""
+max|o| per tensor.  The gradients are fp32 sums of many signed terms
+(ds = p (dp - sum p dp) with cancellation; dK and dV summed per source in an
+arbitrary order of its entries), so their error is relative to the size of
+the terms rather than to each element."""
 import numpy as np
 import pytest
 
@@ -73,6 +73,54 @@ def test_backward_single_neighbour_rows():
     ref = np.zeros((n, H, D))
     np.add.at(ref, indices, g.astype(np.float64))
     _grad_close(got["dV"], ref, "single-neighbour dV")
+
+
+def _hub_graph(n, seed):
+    # random entries, one destination fed by n/2 sources (a split row), one
+    # source feeding n/2 destinations (a split source), nodes past 0.95 n
+    # without entries either way
+    rng = np.random.default_rng(seed)
+    m = int(0.95 * n)
+    src = np.concatenate([rng.integers(0, m, 6 * n), rng.integers(0, m, n // 2), np.full(n // 2, 1)])
+    dst = np.concatenate([rng.integers(0, m, 6 * n), np.zeros(n // 2, np.int64), rng.integers(0, m, n // 2)])
+    key = np.unique(dst * n + src)
+    return wl.csr_by_destination(key % n, key // n, n)
+
+
+@pytest.mark.parametrize("H,D,dtype", [(8, 32, "f32"), (2, 128, "bf16"), (16, 64, "bf16"), (4, 256, "f32"),
+                                       (4, 32, "bf16"), (8, 64, "f32")])
+def test_backward_shapes_with_hubs(H, D, dtype):
+    # every lane width of the two passes (4, 8, 16, 32 features per lane),
+    # split rows and split sources, rows and sources without entries
+    n = 3000
+    indptr, indices = _hub_graph(n, H * D)
+    rng = np.random.default_rng(D)
+    feats = {k: rng.standard_normal((n, H, D)).astype(np.float32) for k in ("Q", "K", "V")}
+    bits = {}
+    if dtype == "bf16":
+        for k in feats:
+            feats[k], bits[k] = wl.bf16_round(feats[k])
+    w = wl.Workload("hubs", n, H, D, dtype, indptr.astype(np.int32), indices.astype(np.int32), feats["Q"],
+                    feats["K"], feats["V"], float(np.float32(1.0 / np.sqrt(D))), bits)
+    g, g_t = _dO(w, 7)
+    ref = oracle.sparse_mha_bwd(w.indptr, w.indices, w.Q, w.K, w.V, g, w.scale)
+    got = _bwd(w, to_device(w), g_t)
+    for k in ("dQ", "dK", "dV"):
+        _grad_close(got[k], ref[k], f"H={H} D={D} {dtype} {k}")
+    no_in = np.bincount(w.indices, minlength=n) == 0
+    assert np.all(got["dK"][no_in] == 0.0) and np.all(got["dV"][no_in] == 0.0)
+    assert np.all(got["dQ"][np.diff(w.indptr) == 0] == 0.0)
+
+
+def test_backward_no_entries():
+    n, H, D = 100, 4, 32
+    rng = np.random.default_rng(5)
+    Q, K, V = (rng.standard_normal((n, H, D)).astype(np.float32) for _ in range(3))
+    w = wl.Workload("empty", n, H, D, "f32", np.zeros(n + 1, np.int32), np.zeros(0, np.int32), Q, K, V, 0.2)
+    g, g_t = _dO(w, 6)
+    got = _bwd(w, to_device(w), g_t)
+    for k in ("dQ", "dK", "dV"):
+        assert np.all(got[k] == 0.0), k
 
 
 def test_backward_argument_errors():

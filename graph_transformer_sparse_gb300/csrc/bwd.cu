@@ -264,6 +264,10 @@ __device__ __forceinline__ void zero_row(float* a, int64_t r, int HD, int lane) 
 }
 
 constexpr int kTaskWarps = 8;
+// the two passes: 128-thread blocks; bf16 rows of up to 16 features a lane
+// capped at 102 registers (five blocks, 20 warps an SM)
+constexpr int kPassWarps = 4;
+template <typename T, int E> constexpr int pass_min_blocks() { return sizeof(T) == 2 && E <= 16 ? 5 : 2; }
 
 // One task of a binning's lists: a whole row (t < n_rows) or one chunk of a
 // split row.  `whole` is false for chunks; `first` for whole rows and the
@@ -438,7 +442,7 @@ __device__ __forceinline__ Task group_task(int t, int n_tasks, int n_chunks, con
 // Also zeroes dK and dV of the split sources (listed by the source binning),
 // which pass 2 adds to.
 template <typename T, int E, int U>
-__global__ void __launch_bounds__(kTaskWarps * 32)
+__global__ void __launch_bounds__(kPassWarps * 32, pass_min_blocks<T, E>())
 k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const int* __restrict__ hdr,
          const int* __restrict__ rows, const int2* __restrict__ chunks, int chunk_edges,
          const int* __restrict__ col_hdr, const int2* __restrict__ col_longs, const T* __restrict__ Q,
@@ -458,7 +462,7 @@ k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const 
     };
     const int n_chunks = hdr[HdrLayout::kChunks];
     const int n_tasks = hdr[HdrLayout::kDenseSeg] + n_chunks;
-    for (int t0 = (blockIdx.x * kTaskWarps + warp) * S; t0 < n_tasks; t0 += gridDim.x * kTaskWarps * S) {
+    for (int t0 = (blockIdx.x * kPassWarps + warp) * S; t0 < n_tasks; t0 += gridDim.x * kPassWarps * S) {
         Task k = group_task(t0 + slot, n_tasks, n_chunks, indptr, rows, chunks, chunk_edges);
         const int64_t off = static_cast<int64_t>(k.row) * HD + gl * E;
         const int deg = k.row >= 0 ? indptr[k.row + 1] - indptr[k.row] : 0;
@@ -537,7 +541,7 @@ k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const 
     }
     // split sources: zero their dK, dV rows for pass 2's atomics
     const int n_long = col_hdr[HdrLayout::kLong];
-    for (int c = blockIdx.x * kTaskWarps + warp; c < n_long; c += gridDim.x * kTaskWarps) {
+    for (int c = blockIdx.x * kPassWarps + warp; c < n_long; c += gridDim.x * kPassWarps) {
         const int j = col_longs[c].x;
         zero_row(dK, j, HD, lane);
         zero_row(dV, j, HD, lane);
@@ -546,7 +550,7 @@ k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const 
 
 // ---- pass 2: by source node ------------------------------------------------
 template <typename T, int E, int U>
-__global__ void __launch_bounds__(kTaskWarps * 32)
+__global__ void __launch_bounds__(kPassWarps * 32, pass_min_blocks<T, E>())
 k_bwd_dkv(const int* __restrict__ colptr, const int* __restrict__ rowid, const int* __restrict__ hdr,
           const int* __restrict__ cols, const int2* __restrict__ chunks, int chunk_edges,
           const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
@@ -564,7 +568,7 @@ k_bwd_dkv(const int* __restrict__ colptr, const int* __restrict__ rowid, const i
     };
     const int n_chunks = hdr[HdrLayout::kChunks];
     const int n_tasks = hdr[HdrLayout::kDenseSeg] + n_chunks;
-    for (int t0 = (blockIdx.x * kTaskWarps + warp) * S; t0 < n_tasks; t0 += gridDim.x * kTaskWarps * S) {
+    for (int t0 = (blockIdx.x * kPassWarps + warp) * S; t0 < n_tasks; t0 += gridDim.x * kPassWarps * S) {
         const Task k = group_task(t0 + slot, n_tasks, n_chunks, colptr, cols, chunks, chunk_edges);
         const int64_t off = static_cast<int64_t>(k.row) * HD + gl * E;
         float dk[E], dv[E];
@@ -670,10 +674,10 @@ bool bwd_tasks_supported(int H, int D, gtattn_dtype dtype, const void* const* pt
 
 int64_t bwd_scan_tiles(int64_t N) { return (N + kScanTile - 1) / kScanTile; }
 
-// resident blocks of `kernel` on the whole GPU (cached per kernel), capped by
-// the tasks there can be (a warp per task)
+// resident blocks of `kernel` (blocks of `warps` warps) on the whole GPU,
+// cached per kernel, capped by the tasks there can be (at least one a warp)
 template <typename Kern>
-static int task_grid(Kern kernel, int task_bound) {
+static int task_grid(Kern kernel, int task_bound, int warps) {
     static std::mutex mu;
     static std::unordered_map<const void*, int> cache;
     int grid;
@@ -684,14 +688,14 @@ static int task_grid(Kern kernel, int task_bound) {
             grid = it->second;
         } else {
             int per_sm = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kTaskWarps * 32, 0) != cudaSuccess ||
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, warps * 32, 0) != cudaSuccess ||
                 per_sm < 1)
                 per_sm = 1;
             grid = per_sm * num_sms();
             cache[reinterpret_cast<const void*>(kernel)] = grid;
         }
     }
-    const int need = (task_bound + kTaskWarps - 1) / kTaskWarps;
+    const int need = (task_bound + warps - 1) / warps;
     return std::max(1, std::min(grid, need));
 }
 
@@ -711,7 +715,7 @@ gtattn_status build_csc(const int* indptr, const int* indices, const TaskLists& 
     GT_CUDA(cudaGetLastError());
     k_scan_apply<<<nt, kScanThreads, 0, s>>>(cursor, N, tsum, colptr, cursor);
     GT_CUDA(cudaGetLastError());
-    const int grid = task_grid(k_csc_scatter, row_task_bound(N, nnz, L.chunk_edges));
+    const int grid = task_grid(k_csc_scatter, row_task_bound(N, nnz, L.chunk_edges), kTaskWarps);
     k_csc_scatter<<<grid, kTaskWarps * 32, 0, s>>>(indptr, indices, L.hdr, L.rows, L.chunks, L.chunk_edges, N,
                                                    cursor, rowid, dQ, HD);
     GT_CUDA(cudaGetLastError());
@@ -737,15 +741,15 @@ gtattn_status launch_bwd_passes(const int* indptr, const int* indices, const Tas
         const T* v = static_cast<const T*>(V);
         const T* g = static_cast<const T*>(dO);
         auto k1 = k_bwd_dq<T, EE, U>;
-        k1<<<task_grid(k1, bound_r), kTaskWarps * 32, 0, s>>>(indptr, indices, rows.hdr, rows.rows, rows.chunks,
-                                                               rows.chunk_edges, cols.hdr, col_longs, q, k, v, g, O,
-                                                               lse, LD, dQ, dK, dV, H, G, lph, scale);
+        k1<<<task_grid(k1, bound_r, kPassWarps), kPassWarps * 32, 0, s>>>(
+            indptr, indices, rows.hdr, rows.rows, rows.chunks, rows.chunk_edges, cols.hdr, col_longs, q, k, v, g, O,
+            lse, LD, dQ, dK, dV, H, G, lph, scale);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         auto k2 = k_bwd_dkv<T, EE, U>;
-        k2<<<task_grid(k2, bound_c), kTaskWarps * 32, 0, s>>>(colptr, rowid, cols.hdr, cols.rows, cols.chunks,
-                                                               cols.chunk_edges, q, k, v, g, LD, dK, dV, H, G, lph,
-                                                               scale);
+        k2<<<task_grid(k2, bound_c, kPassWarps), kPassWarps * 32, 0, s>>>(
+            colptr, rowid, cols.hdr, cols.rows, cols.chunks, cols.chunk_edges, q, k, v, g, LD, dK, dV, H, G, lph,
+            scale);
         return cudaGetLastError();
     };
     using B = __nv_bfloat16;

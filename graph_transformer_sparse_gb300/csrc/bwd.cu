@@ -264,10 +264,14 @@ __device__ __forceinline__ void zero_row(float* a, int64_t r, int HD, int lane) 
 }
 
 constexpr int kTaskWarps = 8;
-// the two passes: 128-thread blocks; bf16 rows of up to 16 features a lane
-// capped at 102 registers (five blocks, 20 warps an SM)
+// the two passes: 128-thread blocks; with bf16 rows of up to 16 features a
+// lane, pass 1 is capped at 96 registers (five blocks, 20 warps an SM) and
+// pass 2, which holds twice the accumulators, at 128 (four blocks; at 96 it
+// spills and runs slower)
 constexpr int kPassWarps = 4;
-template <typename T, int E> constexpr int pass_min_blocks() { return sizeof(T) == 2 && E <= 16 ? 5 : 2; }
+template <typename T, int E, int PASS> constexpr int pass_min_blocks() {
+    return sizeof(T) == 2 && E <= 16 ? (PASS == 1 ? 5 : 4) : 2;
+}
 
 // One task of a binning's lists: a whole row (t < n_rows) or one chunk of a
 // split row.  `whole` is false for chunks; `first` for whole rows and the
@@ -442,7 +446,7 @@ __device__ __forceinline__ Task group_task(int t, int n_tasks, int n_chunks, con
 // Also zeroes dK and dV of the split sources (listed by the source binning),
 // which pass 2 adds to.
 template <typename T, int E, int U>
-__global__ void __launch_bounds__(kPassWarps * 32, pass_min_blocks<T, E>())
+__global__ void __launch_bounds__(kPassWarps * 32, pass_min_blocks<T, E, 1>())
 k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const int* __restrict__ hdr,
          const int* __restrict__ rows, const int2* __restrict__ chunks, int chunk_edges,
          const int* __restrict__ col_hdr, const int2* __restrict__ col_longs, const T* __restrict__ Q,
@@ -550,7 +554,7 @@ k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const 
 
 // ---- pass 2: by source node ------------------------------------------------
 template <typename T, int E, int U>
-__global__ void __launch_bounds__(kPassWarps * 32, pass_min_blocks<T, E>())
+__global__ void __launch_bounds__(kPassWarps * 32, pass_min_blocks<T, E, 2>())
 k_bwd_dkv(const int* __restrict__ colptr, const int* __restrict__ rowid, const int* __restrict__ hdr,
           const int* __restrict__ cols, const int2* __restrict__ chunks, int chunk_edges,
           const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,

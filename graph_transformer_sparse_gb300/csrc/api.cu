@@ -286,33 +286,41 @@ extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indice
 }
 
 // Row-local transpose between [N, D, H] and [N, H, D] (to_hd: from the
-// former): a warp per node row, the row read into shared memory with 16-byte
-// loads, each lane then gathering 16 bytes of the permuted row and storing
-// them at once (rows of 16-byte multiples, 16-byte aligned: the shapes the
-// vector row kernel takes).
+// former).  A warp moves R = kMaxHD / (H D) consecutive node rows at a time:
+// one contiguous span read into shared memory with 16-byte loads, then each
+// lane gathers 16 bytes of a permuted row through the block's permutation
+// table and stores them at once (rows of 16-byte multiples, 16-byte
+// aligned: the shapes the vector row kernel takes).
 template <typename T>
 __global__ void __launch_bounds__(256)
 k_transpose_rows(const T* __restrict__ src, T* __restrict__ dst, int64_t n, int H, int D, int to_hd) {
     constexpr int kPer = 16 / sizeof(T);   // elements per 16-byte piece
     __shared__ __align__(16) T sm[8][kMaxHD];
+    __shared__ short perm[kMaxHD];          // source element of each destination element
     const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int HD = H * D, pieces = HD / kPer;
-    T* row_sm = sm[wid];
-    for (int64_t row = blockIdx.x * 8 + wid; row < n; row += static_cast<int64_t>(gridDim.x) * 8) {
-        const uint4* s4 = reinterpret_cast<const uint4*>(src + row * HD);
-        for (int i = lane; i < pieces; i += 32) reinterpret_cast<uint4*>(row_sm)[i] = __ldg(s4 + i);
+    const int HD = H * D, R = kMaxHD / HD, per_row = HD / kPer;
+    for (int el = threadIdx.x; el < HD; el += blockDim.x) {
+        int from;
+        if (to_hd) { const int h = el / D, d = el - h * D; from = d * H + h; }
+        else { const int d = el / H, h = el - d * H; from = h * D + d; }
+        perm[el] = static_cast<short>(from);
+    }
+    __syncthreads();
+    T* buf = sm[wid];
+    const int64_t spans = (n + R - 1) / R;
+    for (int64_t sp = blockIdx.x * 8 + wid; sp < spans; sp += static_cast<int64_t>(gridDim.x) * 8) {
+        const int64_t row0 = sp * R;
+        const int pieces = static_cast<int>(min(static_cast<int64_t>(R), n - row0)) * per_row;
+        const uint4* s4 = reinterpret_cast<const uint4*>(src + row0 * HD);
+        for (int i = lane; i < pieces; i += 32) reinterpret_cast<uint4*>(buf)[i] = __ldg(s4 + i);
         __syncwarp();
-        uint4* d4 = reinterpret_cast<uint4*>(dst + row * HD);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + row0 * HD);
         for (int i = lane; i < pieces; i += 32) {
+            const int r = i / per_row, el0 = (i - r * per_row) * kPer;
+            const T* rs = buf + r * HD;
             __align__(16) T v[kPer];
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const int el = i * kPer + u;
-                int from;
-                if (to_hd) { const int h = el / D, d = el - h * D; from = d * H + h; }
-                else { const int d = el / H, h = el - d * H; from = h * D + d; }
-                v[u] = row_sm[from];
-            }
+            for (int u = 0; u < kPer; ++u) v[u] = rs[perm[el0 + u]];
             d4[i] = *reinterpret_cast<const uint4*>(v);
         }
         __syncwarp();
@@ -321,7 +329,8 @@ k_transpose_rows(const T* __restrict__ src, T* __restrict__ dst, int64_t n, int 
 
 template <typename T>
 static cudaError_t transpose_rows(const void* src, void* dst, int64_t n, int H, int D, int to_hd, cudaStream_t s) {
-    const int blocks = static_cast<int>(std::min<int64_t>((n + 7) / 8, static_cast<int64_t>(num_sms()) * 8));
+    const int64_t spans = (n + kMaxHD / (H * D) - 1) / (kMaxHD / (H * D));
+    const int blocks = static_cast<int>(std::min<int64_t>((spans + 7) / 8, static_cast<int64_t>(num_sms()) * 8));
     k_transpose_rows<T><<<std::max(blocks, 1), 256, 0, s>>>(static_cast<const T*>(src), static_cast<T*>(dst), n, H, D,
                                                               to_hd);
     return cudaGetLastError();

@@ -265,11 +265,16 @@ gtattn_status gtattn_fwd_weighted(const int32_t* indptr, const int32_t* indices,
  *   dQ_i = scale sum_j ds k_j,  dK_j = scale sum_i ds q_i,  dV_j = sum_i p dO_i.
  *   Q, K, V, dO: [N, H, D] in dtype (F32, or BF16 / BF16_OUT_F32 for bf16
  *           inputs), device memory.
- *   dQ, dK, dV: fp32 [N, H, D], device memory, 4-byte aligned; overwritten
- *           (dK and dV are zeroed by the library on `stream` first).
- *   H <= 128.  Other arguments: as gtattn_fwd.  Asynchronous on `stream`.
- * dK and dV accumulate with fp32 atomic adds, so their last bits depend on
- * the order of the additions (not deterministic run to run).
+ *   dQ, dK, dV: fp32 [N, H, D], device memory, 4-byte aligned; every row
+ *           is overwritten (rows without entries get zeros).
+ *   H <= 128.  Other arguments: as gtattn_fwd.  Asynchronous on `stream`;
+ *   the temporaries (the forward's fp32 output and log-sum-exp, a
+ *   source-major copy of the pattern: about 4 N H D + 12 N H + 8 N + 4 nnz
+ *   bytes plus the binnings) come from the library's stream-ordered pool.
+ *   indices must lie in [0, N), as for gtattn_fwd (csr_validate checks).
+ * dK and dV are summed per source over its entries in an order set by
+ * atomic slot claims, and split rows and sources add their chunks with fp32
+ * atomics, so the last bits are not deterministic run to run.
  */
 gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
                          const void* V, const void* dO, float* dQ, float* dK, float* dV, int64_t N,

@@ -8,14 +8,19 @@
 //   dp_e = dO_i . v_j,   Dlt = sum_e p_e dp_e,   ds_e = p_e (dp_e - Dlt)
 //   dQ_i = scale sum_e ds_e k_j,   dK_j += scale ds_e q_i,   dV_j += p_e dO_i
 //
-// One warp per destination row (CSR by destination), lanes over the row's
-// H*D features (KPL per lane), per-head dot products summed through shared
-// memory.  Two walks over the row's entries: the first recomputes the
-// softmax statistics online (max m, sum l, and a = sum exp(s - m) dp, so
-// Dlt = a / l without storing anything per entry); the second forms p and
-// ds per entry, accumulates dQ_i in registers (written once) and scatters
-// dK_j and dV_j with fp32 atomic adds (a source row gathers from all the
-// rows it feeds).  The gradients are fp32 whatever the input type.
+// The gradients are fp32 whatever the input type.  Two implementations:
+//  * the two passes (second half of this file), for rows that split into
+//    lane groups of 4..32 features a lane: the forward's output and
+//    log-sum-exp make every entry's p and ds local, so dQ is summed by
+//    destination row and dK, dV by source over a source-major copy of the
+//    pattern, each in registers and stored once;
+//  * for other shapes, a warp per destination row, lanes over the row's H*D
+//    features (KPL a lane), per-head dot products summed through shared
+//    memory, two walks over the row's entries: the first recomputes the
+//    softmax statistics online (max m, sum l, and a = sum exp(s - m) dp, so
+//    Dlt = a / l without storing anything per entry); the second forms p and
+//    ds per entry, accumulates dQ_i in registers (written once) and scatters
+//    dK_j and dV_j with fp32 atomic adds.
 #include "bwd.cuh"
 
 #include <algorithm>

@@ -130,3 +130,42 @@ def test_backward_argument_errors():
     with pytest.raises(gt.GtattnError) as e:   # more heads than the backward supports
         gt.gtattn_bwd(d["indptr"], d["indices"], z, z, z, z, z, z, z, w.N, w.nnz, 200, 1, 1.0, gt.GTATTN_F32)
     assert e.value.status == gt.GTATTN_ERR_INVALID_ARG
+
+
+def _sampled_sources(w, n_random=200, n_top=8, seed=1):
+    rng = np.random.default_rng(seed)
+    cdeg = np.bincount(w.indices, minlength=w.N)
+    top = np.argsort(cdeg)[-n_top:]
+    rnd = rng.choice(w.N, size=min(n_random, w.N), replace=False)
+    return np.unique(np.concatenate([top, rnd]))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["erdos_renyi", "rmat"])
+def test_backward_full_size_sampled(name):
+    # Full-size workload on the GPU; the oracle on the subgraph of every
+    # destination row that a sampled output depends on: dQ_i needs row i's
+    # entries, dK_j and dV_j every row holding source j (each with all its
+    # entries, for that row's softmax), so on that subgraph the sampled
+    # outputs are exact.
+    w = wl.make_workload(name)
+    deg = np.diff(w.indptr)
+    q_rows = np.unique(np.concatenate([np.argsort(deg)[-16:], np.flatnonzero(deg == 1)[:32],
+                                       np.random.default_rng(2).choice(w.N, 300, replace=False)]))
+    srcs = _sampled_sources(w)
+    row_of = np.repeat(np.arange(w.N), deg)
+    keep = np.zeros(w.N, bool)
+    keep[q_rows] = True
+    keep[row_of[np.isin(w.indices, srcs)]] = True
+    sub_deg = np.where(keep, deg, 0)
+    sub_ptr = np.zeros(w.N + 1, np.int64)
+    np.cumsum(sub_deg, out=sub_ptr[1:])
+    sub_idx = w.indices[np.repeat(keep, deg)]
+    g, g_t = _dO(w, seed=11)
+    ref = oracle.sparse_mha_bwd(sub_ptr.astype(np.int32), sub_idx, w.Q, w.K, w.V, g, w.scale)
+    got = _bwd(w, to_device(w), g_t)
+    _grad_close(got["dQ"][q_rows], ref["dQ"][q_rows], f"{name} dQ (sampled rows)")
+    for k in ("dK", "dV"):
+        _grad_close(got[k][srcs], ref[k][srcs], f"{name} {k} (sampled sources)")
+    for k in ("dQ", "dK", "dV"):
+        assert np.isfinite(got[k]).all(), k

@@ -65,6 +65,33 @@ def test_host_argument_checks(lib):
     assert lib.gtattn_plan_get_info(None, None) == INV
 
 
+def test_host_argument_checks_bias_weighted_bwd_ndh(lib):
+    # the entry points beyond the plain forward, rejected before device work
+    INV, OK = gt.GTATTN_ERR_INVALID_ARG, gt.GTATTN_OK
+    fb = lib.gtattn_fwd_bias   # indptr indices Q K V bias out logits probs N nnz H D scale dtype stream
+    assert fb(16, 16, 16, 16, 16, None, 16, None, None, 4, 4, 2, 8, 1.0, 0, None) == INV   # null bias, nnz > 0
+    assert fb(16, 16, 16, 16, 16, 18, 16, None, None, 4, 4, 2, 8, 1.0, 0, None) == INV     # misaligned bias
+    assert fb(None, 16, 16, 16, 16, 16, 16, None, None, 4, 4, 2, 8, 1.0, 0, None) == INV   # null indptr
+    fw = lib.gtattn_fwd_weighted   # indptr indices values Q K V out logits probs N nnz H D scale dtype stream
+    assert fw(16, 16, None, 16, 16, 16, 16, None, None, 4, 4, 2, 8, 1.0, 0, None) == INV   # null values
+    assert fw(16, 16, 18, 16, 16, 16, 16, None, None, 4, 4, 2, 8, 1.0, 0, None) == INV     # misaligned values
+    assert fw(16, 16, 16, 16, 16, 16, 16, None, None, 4, 4, 0, 8, 1.0, 0, None) == INV     # H < 1
+    fg = lib.gtattn_bwd   # indptr indices Q K V dO dQ dK dV N nnz H D scale dtype stream
+    assert fg(16, 16, 16, 16, 16, 16, 16, 16, 16, -1, 4, 2, 8, 1.0, 0, None) == INV        # N < 0
+    assert fg(16, 16, 16, 16, 16, 16, 16, 16, 16, 4, 4, 200, 1, 1.0, 0, None) == INV       # H > 128
+    assert fg(16, 16, 16, 16, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 7, None) == INV         # dtype
+    assert fg(16, 16, 16, 16, 16, 16, None, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV       # null dQ
+    assert fg(16, 16, 16, 16, 16, 18, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV         # misaligned dO
+    assert fg(16, 18, 16, 16, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV         # misaligned indices
+    assert fg(16, 16, 16, None, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV       # null K, nnz > 0
+    assert fg(None, 16, 16, 16, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV       # null indptr
+    assert fg(16, None, None, None, None, None, None, None, None, 0, 0, 2, 8, 1.0, 0, None) == OK   # N = 0
+    fn = lib.gtattn_fwd_ndh   # indptr indices Q K V out N nnz H D scale dtype stream
+    assert fn(None, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV                   # null indptr
+    assert fn(16, 16, 16, 16, 16, 16, 4, 4, 2, 1000, 1.0, 0, None) == INV                  # H*D > 1024
+    assert fn(16, 16, 16, 16, 16, None, 4, 4, 2, 8, 1.0, 0, None) == INV                   # null out
+
+
 def test_product_path_has_no_oracle_dependency():
     # the package and its sources never import or link the oracle
     pkg = os.path.join(ROOT, "graph_transformer_sparse_gb300")

@@ -704,8 +704,8 @@ static int task_grid(Kern kernel, int task_bound, int warps) {
             cache[reinterpret_cast<const void*>(kernel)] = grid;
         }
     }
-    const int need = (task_bound + warps - 1) / warps;
-    return std::max(1, std::min(grid, need));
+    const int64_t need = (static_cast<int64_t>(task_bound) + warps - 1) / warps;
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(grid, need)));
 }
 
 gtattn_status build_csc(const int* indptr, const int* indices, const TaskLists& L, int N, int64_t nnz,

@@ -642,6 +642,35 @@ def test_backward_single_neighbour_and_constant_values():
     np.testing.assert_allclose(r["dK"], 0.0, atol=1e-14)
 
 
+def test_backward_invariants_on_a_larger_graph():
+    # exact consequences of the chain rule at sizes finite differences cannot
+    # reach: for every row with entries sum_j p_ij = 1 and sum_j ds_ij = 0, so
+    #   sum_j dV_j = sum over rows with entries of dO_i,
+    #   sum_j dK_j = scale sum_i q_i sum_j ds_ij = 0,
+    # and adding one vector c to every K row shifts each row's logits by a
+    # constant (softmax unchanged: same dV) while dQ_i gains
+    # scale c sum_j ds_ij = 0 (same dQ).
+    rng = np.random.default_rng(530)
+    n, H, D, m = 300, 3, 8, 280            # rows m..n-1 have no entries
+    src = rng.integers(0, n, 4000)
+    dst = rng.integers(0, m, 4000)
+    indptr, indices = wl.csr_by_destination(src, dst, n)
+    Q, K, V = _rand_feats(rng, n, H, D)
+    # K and the shift on a 2^-10 grid, so K + c is exact in float32 and the
+    # logits move by exactly scale q_i.c
+    K = (np.round(np.clip(K, -4, 4) * 1024) / 1024).astype(np.float32)
+    c = (rng.integers(-256, 257, (1, H, D)) / 1024).astype(np.float32)
+    G = rng.standard_normal((n, H, D)).astype(np.float32)
+    r = oracle.sparse_mha_bwd(indptr, indices, Q, K, V, G, 0.4)
+    has = np.diff(indptr) > 0
+    assert not has[m:].any() and has[:m].sum() > 250
+    np.testing.assert_allclose(r["dV"].sum(axis=0), G[has].astype(np.float64).sum(axis=0), rtol=1e-12, atol=1e-11)
+    assert np.all(np.abs(r["dK"].sum(axis=0)) <= 1e-12 * np.abs(r["dK"]).sum(axis=0) + 1e-13)
+    r2 = oracle.sparse_mha_bwd(indptr, indices, Q, (K + c).astype(np.float32), V, G, 0.4)
+    np.testing.assert_allclose(r2["dV"], r["dV"], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(r2["dQ"], r["dQ"], rtol=1e-10, atol=1e-12)
+
+
 BWD_MUTATIONS = {
     "softmax_jacobian_without_mean": ("const double ds = p[k] * (dp[k] - Dlt);", "const double ds = p[k] * dp[k];"),
     "dk_to_the_row": ("double* dk = dK + j * HD + (int64_t)h * D;", "double* dk = dK + i * HD + (int64_t)h * D;"),

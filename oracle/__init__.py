@@ -10,8 +10,10 @@ compiles it with gcc on first use and wraps it with ctypes.  See ``oracle.c``
 for the passages each function follows and the readings taken.
 
 Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
-brute-force dense masked softmax, closed forms and invariants (no function is
-unpinned).
+brute-force dense masked softmax, closed forms and invariants; the linear
+layer against a hand-worked example and a library matmul, the storage
+rounding against a nearest-neighbour search, the projected block against a
+dense numpy route (no function is unpinned).
 """
 from __future__ import annotations
 
@@ -60,6 +62,10 @@ def _load():
             lib.gto_dense_attention.restype = ctypes.c_int
             lib.gto_sparse_mha_bwd.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, vp, vp, dbl, vp, vp, vp]
             lib.gto_sparse_mha_bwd.restype = ctypes.c_int
+            lib.gto_linear.argtypes = [i64, i32, i32, vp, vp, vp, vp]
+            lib.gto_linear.restype = ctypes.c_int
+            lib.gto_round_store.argtypes = [i64, vp, i32, vp]
+            lib.gto_round_store.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -189,3 +195,127 @@ def sparse_mha_bwd(indptr, indices, Q, K, V, dO, scale):
     if rc != 0:
         raise OracleError(f"gto_sparse_mha_bwd failed with code {rc}")
     return dict(dQ=dQ, dK=dK, dV=dV)
+
+
+def linear(X, W, b=None, threads: int = 1):
+    """Y = X W^T + b in fp64 (``gto_linear``): X float32 [M, Kin], W float32
+    [Nout, Kin] (nn.Linear's weight), b float32 [Nout] or None.  Returns
+    float64 [M, Nout].  ``threads`` > 1 splits the rows over host threads."""
+    lib = _load()
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    M, Kin = X.shape
+    Nout, K2 = W.shape
+    if K2 != Kin:
+        raise OracleError(f"W must be [Nout, {Kin}], got {W.shape}")
+    if b is not None:
+        b = np.ascontiguousarray(b, dtype=np.float32)
+        if b.shape != (Nout,):
+            raise OracleError(f"b must be [{Nout}], got {b.shape}")
+    Y = np.zeros((M, Nout), dtype=np.float64)
+
+    def run(r0, r1):
+        rc = lib.gto_linear(r1 - r0, Kin, Nout, _ptr(X[r0:r1]), _ptr(W), _ptr(b), _ptr(Y[r0:r1]))
+        if rc != 0:
+            raise OracleError(f"gto_linear failed with code {rc}")
+
+    threads = max(1, min(int(threads), M if M > 0 else 1))
+    if threads == 1:
+        run(0, M)
+    else:
+        cuts = [M * t // threads for t in range(threads + 1)]
+        ts = [threading.Thread(target=run, args=(cuts[t], cuts[t + 1])) for t in range(threads)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+    return Y
+
+
+def round_store(x, precision: str):
+    """The value an intermediate holds once stored (``gto_round_store``):
+    "f32" the nearest float32; "bf16" that float32, then the nearest bf16
+    (as float32).  Returns float32 of the same shape."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.float32)
+    mode = {"f32": 0, "bf16": 1}[precision]
+    rc = lib.gto_round_store(x.size, _ptr(x), mode, _ptr(out))
+    if rc != 0:
+        raise OracleError(f"gto_round_store failed with code {rc}")
+    return out
+
+
+def _split_heads(Y, H, D, heads_inner):
+    """[M, H*D] projection output -> [M, H, D].  Heads-major features
+    (f = h*D + d): TransLayer's view(-1, h, d_qkv).  Heads-inner features
+    (f = d*H + h): SparseMHA's reshape(N, head_dim, num_heads)."""
+    M = Y.shape[0]
+    if heads_inner:
+        return Y.reshape(M, D, H).transpose(0, 2, 1)
+    return Y.reshape(M, H, D)
+
+
+def _merge_heads(O, heads_inner):
+    """[M, H, D] -> [M, H*D] in the same feature order (the out projection's
+    input: out.reshape(N, -1) / wv.view(-1, h * d_qkv))."""
+    M, H, D = O.shape
+    if heads_inner:
+        return O.transpose(0, 2, 1).reshape(M, D * H)
+    return O.reshape(M, H * D)
+
+
+def sparse_mha_proj(indptr, indices, X, Wq, Wk, Wv, Wo, bq, bk, bv, bo, H, D, scale,
+                    heads_inner=False, store="f32", rows=None, threads: int = 1):
+    """The attention block with its projections, in fp64:
+
+        q, k, v = X Wq^T + bq, X Wk^T + bk, X Wv^T + bv   (split into H heads of D)
+        o       = SparseAttn(q, k, v, A)                    (sparse_mha)
+        Y       = o Wo^T + bo                               (o's heads merged back)
+
+    -- SparseMHA.forward of "Graph Transformer in a Nutshell" (nn.Linear maps
+    with biases, features split head-inner: ``heads_inner=True``) and the
+    attention part of TransLayer.forward in "Efficient Sparse Transformer
+    implementation with DGL's builtin operators" (bias=False: pass None;
+    head-major view).  The scale is an argument applied to q.k, as in
+    sparse_mha (SparseMHA folds head_dim**-0.5 into q; the product is the
+    same).
+
+    ``store``: the precision the intermediates q, k, v and o are held in
+    between the stages ("f32" or "bf16", see ``round_store``); the arithmetic
+    of every stage is fp64.  ``rows``: compute Y for these rows only (the
+    projections of their neighbours are computed, nothing else).
+    Returns float64 [len(rows) or N, Nout]."""
+    indptr = np.ascontiguousarray(indptr, dtype=np.int32)
+    indices = np.ascontiguousarray(indices, dtype=np.int32)
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    N = X.shape[0]
+    if rows is None:
+        need = np.arange(N, dtype=np.int64)
+        sel = np.arange(N, dtype=np.int64)
+        lindptr, lindices = indptr, indices
+    else:
+        rows = np.asarray(rows, dtype=np.int64)
+        starts, ends = indptr[rows].astype(np.int64), indptr[rows + 1].astype(np.int64)
+        nbr = np.concatenate([indices[a:b] for a, b in zip(starts, ends)] + [np.zeros(0, np.int32)])
+        need = np.unique(np.concatenate([rows, nbr.astype(np.int64)]))
+        local = np.full(N, -1, dtype=np.int64)
+        local[need] = np.arange(len(need))
+        # a CSR over the needed nodes: the sampled rows keep their entries,
+        # the other needed nodes (neighbours only) get none
+        deg = np.zeros(len(need), dtype=np.int64)
+        deg[local[rows]] = ends - starts
+        lindptr = np.zeros(len(need) + 1, dtype=np.int64)
+        np.cumsum(deg, out=lindptr[1:])
+        lindices = np.empty(int(lindptr[-1]), dtype=np.int32)
+        for r, a, b in zip(rows, starts, ends):
+            o = lindptr[local[r]]
+            lindices[o:o + (b - a)] = local[indices[a:b]]
+        lindptr = lindptr.astype(np.int32)
+        sel = local[rows]
+    Xn = X[need]
+    q, k, v = (round_store(_split_heads(linear(Xn, W, b, threads), H, D, heads_inner), store)
+               for W, b in ((Wq, bq), (Wk, bk), (Wv, bv)))
+    o = sparse_mha(lindptr, lindices, q, k, v, scale, rows=sel, threads=threads)["out"]
+    o = round_store(o, store)
+    return linear(_merge_heads(o, heads_inner), Wo, bo, threads)

@@ -59,6 +59,12 @@
  *   softmax still runs over the stored entries only (a stored 0 gives
  *   logit 0, it does not remove the entry).
  *
+ * Projections around the attention (gto_linear, gto_round_store; the
+ * composition is in oracle/__init__.py, sparse_mha_proj): Y = X W^T + b for
+ * the nn.Linear maps of SparseMHA / TransLayer, and the precision an
+ * intermediate is stored in between the stages (float32, or bf16 from the
+ * float32 value, ties to even).
+ *
  * Arithmetic: inputs are float32 (bf16 inputs arrive as their exact float32
  * widening), every operation is double, the reductions run in index order,
  * exp is the C library's double exp.  Two passes per (row, head): logits and
@@ -290,5 +296,61 @@ int gto_sparse_mha_bwd(int64_t N, int64_t nnz, int32_t H, int32_t D,
     }
     free(p);
     free(dp);
+    return GTO_OK;
+}
+
+/*
+ * Linear layer: Y = X W^T + b, the nn.Linear maps around the attention --
+ * q_proj, k_proj, v_proj and out_proj of SparseMHA ("Graph Transformer in a
+ * Nutshell", section "Sparse Multi-head Attention"; nn.Linear keeps a bias)
+ * and proj_q, proj_k, proj_v, proj_o of TransLayer ("Efficient Sparse
+ * Transformer implementation with DGL's builtin operators"; bias=False).
+ * X float32 [M, Kin]; W float32 [Nout, Kin] (nn.Linear's weight: one row per
+ * output feature); b float32 [Nout] or NULL (no bias); Y double [M, Nout],
+ * overwritten.  Each output is b[n] + sum_k X[m,k] W[n,k] in double, k in
+ * index order.
+ */
+int gto_linear(int64_t M, int32_t Kin, int32_t Nout, const float* X, const float* W, const float* b, double* Y)
+{
+    if (M < 0 || Kin <= 0 || Nout <= 0 || !Y) return GTO_BAD_ARG;
+    if (M == 0) return GTO_OK;
+    if (!X || !W) return GTO_BAD_ARG;
+    for (int64_t m = 0; m < M; ++m) {
+        const float* x = X + m * Kin;
+        for (int32_t n = 0; n < Nout; ++n) {
+            const float* w = W + (int64_t)n * Kin;
+            double acc = 0.0;
+            for (int32_t k = 0; k < Kin; ++k) acc += (double)x[k] * (double)w[k];
+            Y[m * Nout + n] = (b ? (double)b[n] : 0.0) + acc;
+        }
+    }
+    return GTO_OK;
+}
+
+/*
+ * Storage precision of intermediate results (the projected Q, K, V and the
+ * attention output, which a module keeps in its working type between the
+ * layers).  mode 0: the nearest float32 (ties to even, the C conversion
+ * under the default rounding mode).  mode 1: that float32, then the nearest
+ * bf16 (8 significant bits, ties to even), returned as its float32 value --
+ * the two steps of a float32 accumulator stored as bf16.  Infinities and
+ * NaNs pass through (a NaN stays a NaN).
+ */
+int gto_round_store(int64_t n, const double* in, int32_t mode, float* out)
+{
+    if (n < 0 || (n > 0 && (!in || !out)) || (mode != 0 && mode != 1)) return GTO_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        float f = (float)in[i];
+        if (mode == 1 && isfinite(f)) {
+            uint32_t u;
+            memcpy(&u, &f, sizeof(u));
+            const uint32_t low = u & 0xFFFFu;          /* the 16 bits dropped */
+            uint32_t hi = u & 0xFFFF0000u;
+            const uint32_t lsb = (u >> 16) & 1u;       /* last kept bit: ties go to even */
+            if (low > 0x8000u || (low == 0x8000u && lsb)) hi += 0x10000u;   /* may carry into the exponent */
+            memcpy(&f, &hi, sizeof(f));
+        }
+        out[i] = f;
+    }
     return GTO_OK;
 }

@@ -703,3 +703,187 @@ def test_backward_pins_catch_planted_mistakes(name):
         assert lib.gto_sparse_mha_bwd(n, int(ip[-1]), H, D, p(ip), p(ix), p(Q), p(K), p(V), p(G), 0.6,
                                       p(out["dQ"]), p(out["dK"]), p(out["dV"])) == 0
     assert any(not np.allclose(out[k], ref[k], rtol=1e-5, atol=1e-6) for k in out), f"pin missed mutation {name}"
+
+
+# --------------------------------------------------------------------------
+# projections around the attention (SparseMHA's q/k/v/out_proj, TransLayer's
+# proj_q/k/v/o): the linear layer, the storage rounding, the whole block
+# --------------------------------------------------------------------------
+def test_linear_hand_example():
+    # [1 2] times W^T with W = [[3, 4], [5, 6]], plus b = [7, 8]: [18, 25]
+    X = np.array([[1.0, 2.0]], np.float32)
+    W = np.array([[3.0, 4.0], [5.0, 6.0]], np.float32)
+    b = np.array([7.0, 8.0], np.float32)
+    assert oracle.linear(X, W, b).tolist() == [[18.0, 25.0]]
+    assert oracle.linear(X, W).tolist() == [[11.0, 17.0]]
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_linear_matches_library_matmul(seed):
+    rng = np.random.default_rng(seed)
+    M, Kin, Nout = 37, 19, 23
+    X = rng.standard_normal((M, Kin)).astype(np.float32)
+    W = rng.standard_normal((Nout, Kin)).astype(np.float32)
+    b = rng.standard_normal(Nout).astype(np.float32)
+    ref = X.astype(np.float64) @ W.astype(np.float64).T + b.astype(np.float64)
+    assert np.allclose(oracle.linear(X, W, b), ref, rtol=1e-13, atol=1e-13)
+    assert np.allclose(oracle.linear(X, W, b, threads=4), ref, rtol=1e-13, atol=1e-13)
+    # identity weights give X back
+    assert np.array_equal(oracle.linear(X, np.eye(Kin, dtype=np.float32)), X.astype(np.float64))
+
+
+def _nearest_bf16(x64):
+    """Nearest bf16 of the nearest float32 of x (ties to even), by comparing
+    the two bf16 neighbours of the float32 value (not bit arithmetic)."""
+    f = np.float32(x64)
+    if not np.isfinite(f):
+        return f
+    bits = np.array([f], np.float32).view(np.uint32)[0]
+    down = np.array([bits & np.uint32(0xFFFF0000)], np.uint32).view(np.float32)[0]
+    step = np.array([(bits & np.uint32(0xFFFF0000)) + np.uint32(0x10000)], np.uint32).view(np.float32)[0]
+    lo, hi = (down, step) if abs(step) >= abs(down) else (step, down)
+    dl, dh = abs(float(f) - float(lo)), abs(float(hi) - float(f))
+    if dl < dh:
+        return lo
+    if dh < dl:
+        return hi
+    lo_even = (np.array([lo], np.float32).view(np.uint32)[0] >> 16) % 2 == 0
+    return lo if lo_even else hi
+
+
+def test_round_store_matches_nearest_neighbour_search():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-6, 6, 4000),
+                        [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 0.0, -0.0,
+                         3.3895313892515355e38, 1e300, -np.inf, np.inf]])
+    got = oracle.round_store(x, "bf16")
+    ref = np.array([_nearest_bf16(v) for v in x], np.float32)
+    assert np.array_equal(got, ref)
+    # the ties: 1 + 2^-8 rounds down to 1 (even), 1 + 3 * 2^-8 up to 1 + 2^-6
+    assert got[4000] == 1.0 and got[4001] == 1.0 + 2.0 ** -6
+    assert np.array_equal(oracle.round_store(x, "f32"), x.astype(np.float32))
+    assert np.isnan(oracle.round_store(np.array([np.nan]), "bf16")[0])
+
+
+def _proj_case(rng, n, e, d_in, H, D, d_out, bias=True):
+    pick = rng.choice(n * n, size=e, replace=False)
+    src, dst = pick // n, pick % n
+    indptr, indices = wl.csr_by_destination(src, dst, n)
+    X = rng.standard_normal((n, d_in)).astype(np.float32)
+    Ws = [(rng.standard_normal((H * D, d_in)) / np.sqrt(d_in)).astype(np.float32) for _ in range(3)]
+    Wo = (rng.standard_normal((d_out, H * D)) / np.sqrt(H * D)).astype(np.float32)
+    bs = [rng.standard_normal(H * D).astype(np.float32) * 0.1 if bias else None for _ in range(3)]
+    bo = rng.standard_normal(d_out).astype(np.float32) * 0.1 if bias else None
+    return src, dst, indptr, indices, X, Ws, Wo, bs, bo
+
+
+def _brute_proj(src, dst, n, X, Ws, Wo, bs, bo, H, D, scale, heads_inner, store):
+    """The block by dense numpy: projections by matmul, heads split by
+    reshape, masked dense softmax attention, heads merged, out projection;
+    intermediates stored as float32 (or bf16 by neighbour search)."""
+    def st(a):
+        if store == "f32":
+            return a.astype(np.float32)
+        return np.vectorize(_nearest_bf16, otypes=[np.float32])(a)
+
+    X64 = X.astype(np.float64)
+
+    def lin(W, b):
+        # products summed over the inputs in index order, then the bias, so
+        # that both sides hold the same double before rounding it for storage
+        acc = np.zeros((X64.shape[0], W.shape[0]))
+        for k in range(X64.shape[1]):
+            acc += np.outer(X64[:, k], W[:, k].astype(np.float64))
+        return (0.0 if b is None else b.astype(np.float64)) + acc
+
+    qkv = []
+    for W, b in zip(Ws, bs):
+        y = lin(W, b)
+        y = y.reshape(n, D, H).transpose(0, 2, 1) if heads_inner else y.reshape(n, H, D)
+        qkv.append(st(y))
+    o = st(brute_force(src, dst, n, *qkv, scale))
+    of = o.transpose(0, 2, 1).reshape(n, D * H) if heads_inner else o.reshape(n, H * D)
+    return of.astype(np.float64) @ Wo.astype(np.float64).T + (0.0 if bo is None else bo.astype(np.float64))
+
+
+@pytest.mark.parametrize("heads_inner", [False, True])
+@pytest.mark.parametrize("store", ["f32", "bf16"])
+@pytest.mark.parametrize("bias", [True, False])
+def test_proj_block_brute_force(heads_inner, store, bias):
+    rng = np.random.default_rng(7)
+    n, H, D, d_in, d_out = 19, 3, 4, 10, 6
+    src, dst, indptr, indices, X, Ws, Wo, bs, bo = _proj_case(rng, n, 90, d_in, H, D, d_out, bias)
+    scale = 0.625   # exact in float32 (the oracle takes the scale as a float32 value)
+    got = oracle.sparse_mha_proj(indptr, indices, X, *Ws, Wo, *bs, bo, H, D, scale, heads_inner=heads_inner,
+                                 store=store)
+    ref = _brute_proj(src, dst, n, X, Ws, Wo, bs, bo, H, D, scale, heads_inner, store)
+    # the stored intermediates are rounded alike on both sides; what is left
+    # is double rounding order
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_proj_layouts_are_a_feature_permutation():
+    # a heads-inner block equals the heads-major block whose q/k/v weight
+    # rows and out-projection columns are permuted by f = d*H + h -> h*D + d
+    rng = np.random.default_rng(8)
+    n, H, D, d_in, d_out = 15, 2, 3, 5, 4
+    src, dst, indptr, indices, X, Ws, Wo, bs, bo = _proj_case(rng, n, 60, d_in, H, D, d_out)
+    perm = np.array([d * H + h for h in range(H) for d in range(D)])   # major position -> inner feature
+    inner = oracle.sparse_mha_proj(indptr, indices, X, *Ws, Wo, *bs, bo, H, D, 0.5, heads_inner=True)
+    major = oracle.sparse_mha_proj(indptr, indices, X, *[W[perm] for W in Ws], Wo[:, perm], *[b[perm] for b in bs],
+                                   bo, H, D, 0.5, heads_inner=False)
+    assert np.allclose(inner, major, rtol=1e-13, atol=1e-13)
+    # ... and differs from the unpermuted heads-major block
+    plain = oracle.sparse_mha_proj(indptr, indices, X, *Ws, Wo, *bs, bo, H, D, 0.5, heads_inner=False)
+    assert not np.allclose(inner, plain, rtol=1e-6, atol=1e-6)
+
+
+def test_proj_rows_subset_matches_full():
+    rng = np.random.default_rng(9)
+    n, H, D, d_in, d_out = 40, 2, 4, 8, 8
+    src, dst, indptr, indices, X, Ws, Wo, bs, bo = _proj_case(rng, n, 300, d_in, H, D, d_out)
+    full = oracle.sparse_mha_proj(indptr, indices, X, *Ws, Wo, *bs, bo, H, D, 0.375, store="bf16")
+    rows = np.array([0, 3, 17, 39, 22])
+    sub = oracle.sparse_mha_proj(indptr, indices, X, *Ws, Wo, *bs, bo, H, D, 0.375, store="bf16", rows=rows)
+    assert np.array_equal(sub, full[rows])
+
+
+LINEAR_MUTATIONS = {
+    # W read as [Kin, Nout] (a transposed weight)
+    "transposed_weight": ("const float* w = W + (int64_t)n * Kin;", "const float* w = W + n;"),
+    "bias_dropped": ("Y[m * Nout + n] = (b ? (double)b[n] : 0.0) + acc;", "Y[m * Nout + n] = acc;"),
+    "last_input_dropped": ("for (int32_t k = 0; k < Kin; ++k) acc +=", "for (int32_t k = 0; k + 1 < Kin; ++k) acc +="),
+    "ties_away_from_zero": ("if (low > 0x8000u || (low == 0x8000u && lsb)) hi += 0x10000u;",
+                            "if (low >= 0x8000u) hi += 0x10000u;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LINEAR_MUTATIONS))
+def test_proj_pins_catch_planted_mistakes(name):
+    text = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    old, new = LINEAR_MUTATIONS[name]
+    assert text.count(old) == 1, f"anchor for {name} missing"
+    mutant = text.replace(old, new)
+    rng = np.random.default_rng(11)
+    M, Kin, Nout = 9, 7, 5
+    X = rng.standard_normal((M, Kin)).astype(np.float32)
+    W = rng.standard_normal((Nout, Kin)).astype(np.float32)
+    b = rng.standard_normal(Nout).astype(np.float32)
+    ties = np.array([1.0 + 2.0 ** -8, 2.0 + 2.0 ** -7, -(4.0 + 2.0 ** -6)])
+    with tempfile.TemporaryDirectory() as td:
+        path = os.path.join(td, name + ".c")
+        open(path, "w").write(mutant)
+        so = os.path.join(td, name + ".so")
+        subprocess.run(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", path, "-o", so, "-lm"], check=True)
+        lib = ctypes.CDLL(so)
+        vp = ctypes.c_void_p
+        lib.gto_linear.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp]
+        lib.gto_round_store.argtypes = [ctypes.c_int64, vp, ctypes.c_int32, vp]
+        Y = np.zeros((M, Nout))
+        lib.gto_linear(M, Kin, Nout, X.ctypes.data_as(vp), W.ctypes.data_as(vp), b.ctypes.data_as(vp),
+                       Y.ctypes.data_as(vp))
+        r = np.zeros(3, np.float32)
+        lib.gto_round_store(3, ties.ctypes.data_as(vp), 1, r.ctypes.data_as(vp))
+    ok_linear = np.allclose(Y, X.astype(np.float64) @ W.astype(np.float64).T + b, rtol=1e-12, atol=1e-12)
+    ok_round = np.array_equal(r, np.array([_nearest_bf16(v) for v in ties], np.float32))
+    assert not (ok_linear and ok_round), f"pin missed mutation {name}"

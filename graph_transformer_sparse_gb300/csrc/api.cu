@@ -108,10 +108,9 @@ ProfScope::~ProfScope() {
 
 static size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Checks shared by the forward entry points.
-static gtattn_status check_fwd(const int32_t* indptr, const int32_t* indices, const void* Q,
-                               const void* K, const void* V, const void* out, int64_t N, int64_t nnz,
-                               int H, int D, gtattn_dtype dtype) {
+// Checks shared by the forward entry points (gtattn_fwd_noalloc too).
+gtattn_status check_fwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                        const void* V, const void* out, int64_t N, int64_t nnz, int H, int D, gtattn_dtype dtype) {
     if (N < 0 || nnz < 0 || N >= (1ll << 31) - 1 || nnz >= (1ll << 31) - 1) return GTATTN_ERR_INVALID_ARG;
     if (H < 1 || D < 1 || (int64_t)H * D > kMaxHD) return GTATTN_ERR_INVALID_ARG;
     if (dtype != GTATTN_F32 && dtype != GTATTN_BF16 && dtype != GTATTN_BF16_OUT_F32)

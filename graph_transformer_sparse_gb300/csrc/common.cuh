@@ -155,6 +155,10 @@ int num_sms();
 cudaMemPool_t pool();
 gtattn_status pool_alloc(void** p, size_t bytes, cudaStream_t s);
 void pool_free(void* p, cudaStream_t s);
+// Host-side argument checks of the forward entry points (null pointers,
+// sizes, dtype, alignment): GTATTN_OK or GTATTN_ERR_INVALID_ARG.
+gtattn_status check_fwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                        const void* V, const void* out, int64_t N, int64_t nnz, int H, int D, gtattn_dtype dtype);
 
 // Benchmark instrumentation: brackets a launch group with CUDA events when
 // profiling is enabled (see gtattn_profile_enable).

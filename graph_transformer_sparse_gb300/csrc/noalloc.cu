@@ -13,6 +13,8 @@
 #include "plan.cuh"
 #include "rows.cuh"
 
+#include <cuda.h>
+
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -44,22 +46,62 @@ static size_t noalloc_bytes(int64_t N, int64_t nnz, int H, int HD, int64_t* n_lo
     return b;
 }
 
-// Device address of the scratch array, looked up once per device with that
-// device current (in host code the array's name is only a host-side handle).
+// Device address of the scratch array in the current context.  In host code
+// the array's name is only a host-side handle; its device address is looked
+// up (cudaGetSymbolAddress) with the device current and kept per device
+// together with the id of the context it belongs to (cuCtxGetId: unique for
+// the life of the process, never reused).  When the device's primary context
+// has been torn down and made again (cudaDeviceReset, or a context destroyed
+// through the driver API), the module is loaded anew and the array may sit
+// elsewhere: the new context's id differs, the lookup runs again, and a stale
+// address is never used.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+static Fn driver_fn(const char* name) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        p = nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// Id of the current context, 0 when none is current (or it cannot be read).
+static unsigned long long current_ctx_id() {
+    static const CtxGetCurrentFn get = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get || !get_id || get(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 static gtattn_status scratch_address(unsigned char** out) {
     constexpr int kMaxDev = 64;
     static std::mutex mu;
     static unsigned char* addr[kMaxDev] = {};
+    static unsigned long long ctx_of[kMaxDev] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_status(e);
     if (dev < 0 || dev >= kMaxDev) return GTATTN_ERR_UNSUPPORTED;
+    // (on a thread that has made no runtime call on this device no context
+    // is current yet, id 0: the symbol lookup below sets up the primary one)
+    unsigned long long id = current_ctx_id();
     std::lock_guard<std::mutex> g(mu);
-    if (!addr[dev]) {
+    if (id == 0 || !addr[dev] || ctx_of[dev] != id) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return cuda_status(e);
+        id = current_ctx_id();
+        if (id == 0) {
+            set_last_error("gtattn_fwd_noalloc: the current CUDA context could not be identified");
+            return GTATTN_ERR_CUDA;
+        }
         addr[dev] = static_cast<unsigned char*>(p);
+        ctx_of[dev] = id;
     }
     *out = addr[dev];
     return GTATTN_OK;
@@ -74,18 +116,7 @@ extern "C" gtattn_status gtattn_fwd_noalloc(const int32_t* indptr, const int32_t
                                             int H, int D, float scale, gtattn_dtype dtype,
                                             cudaStream_t stream) {
     // the same argument rules as gtattn_fwd
-    if (N < 0 || nnz < 0 || N >= (1ll << 31) - 1 || nnz >= (1ll << 31) - 1) return GTATTN_ERR_INVALID_ARG;
-    if (H < 1 || D < 1 || (int64_t)H * D > kMaxHD) return GTATTN_ERR_INVALID_ARG;
-    if (dtype != GTATTN_F32 && dtype != GTATTN_BF16 && dtype != GTATTN_BF16_OUT_F32)
-        return GTATTN_ERR_INVALID_ARG;
-    if (!indptr || (N > 0 && (!Q || !out)) || (nnz > 0 && (!indices || !K || !V))) return GTATTN_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(indptr) | reinterpret_cast<uintptr_t>(indices)) & 3u)
-        return GTATTN_ERR_INVALID_ARG;
-    const uintptr_t esz = dtype == GTATTN_F32 ? 4 : 2;
-    const uintptr_t osz = dtype == GTATTN_BF16 ? 2 : 4;
-    if (((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V)) &
-         (esz - 1)) || (reinterpret_cast<uintptr_t>(out) & (osz - 1)))
-        return GTATTN_ERR_INVALID_ARG;
+    GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
 
     const int HD = H * D;
     int64_t n_long = 0, n_chunks = 0;

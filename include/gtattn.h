@@ -298,7 +298,10 @@ gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indices, const vo
  *   how many bytes were needed).  Example: 2^20 rows, 17.1M entries, 4x32 fits.
  *   Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept with the id of the
+ *   context it was found in: after the device's context is destroyed and
+ *   made again (cudaDeviceReset), the next call finds the array anew (and is
+ *   again a first call in this sense).
  *   Concurrency: every call shares the one array and leaves its contents
  *   behind (each call re-initialises what it reads), so calls whose GPU work
  *   may overlap -- on different streams, or from different threads -- race

@@ -22,7 +22,8 @@ from ._build import LIB, build
 
 __all__ = [
     "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs", "gtattn_fwd_bias", "gtattn_fwd_weighted", "gtattn_bwd", "gtattn_fwd_ndh",
-    "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_csr_build", "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
+    "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_proj", "gtattn_device_errors", "gtattn_csr_build",
+    "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
     "gtattn_csr_validate", "gtattn_status_string", "gtattn_profile_enable", "gtattn_profile_read",
     "sparse_mha", "GTATTN_F32", "GTATTN_BF16", "GTATTN_BF16_OUT_F32",
     "GTATTN_KERNEL_AUTO", "GTATTN_KERNEL_VECTOR", "GTATTN_KERNEL_GENERIC", "EXPORTED_SYMBOLS",
@@ -38,9 +39,9 @@ EXPORTED_SYMBOLS = (
     "gtattn_plan_get_info", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
     "gtattn_coo_to_csr", "gtattn_csr_validate", "gtattn_profile_enable", "gtattn_profile_read",
     "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_bias", "gtattn_fwd_weighted", "gtattn_bwd",
-    "gtattn_fwd_ndh",
+    "gtattn_fwd_ndh", "gtattn_fwd_proj", "gtattn_device_errors",
 )
-KCAT_NAMES = ("bin", "rows", "combine", "softmax", "dense")
+KCAT_NAMES = ("bin", "rows", "combine", "softmax", "dense", "gemm")
 
 
 class GtattnError(RuntimeError):
@@ -108,6 +109,9 @@ def load(path: str | None = None):
             "gtattn_csr_validate": ([vp, vp, i64, i64, vp], i32),
             "gtattn_fwd_noalloc": ([vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
             "gtattn_fwd_host": ([vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, f32, i32, vp], i32),
+            "gtattn_fwd_proj": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, i32, i32, f32,
+                                 i32, vp], i32),
+            "gtattn_device_errors": ([vp, i32], i32),
             "gtattn_profile_enable": ([i32], i32),
             "gtattn_profile_read": ([vp, i32], i32),
         }
@@ -207,6 +211,27 @@ def gtattn_fwd_host(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, s
                                   _host_ptr(V), _host_ptr(out),
                                   int(N), int(nnz), int(H), int(D), float(scale), int(dtype),
                                   _stream(stream)), "gtattn_fwd_host")
+
+
+def gtattn_fwd_proj(indptr, indices, X, Wqkv, bqkv, Wo, bo, Y, N, nnz, F_in, H, D, F_out, scale, dtype,
+                    heads_inner=False, qkv=None, attn=None, stream=None):
+    """The attention block with its projections: q, k, v = X Wqkv^T + bqkv
+    (weights of the three maps stacked, nn.Linear layout), the sparse
+    attention, Y = o Wo^T + bo.  bqkv / bo: fp32 device tensors or None;
+    qkv ([3, N, H, D]) and attn ([N, H, D]) optionally receive the
+    intermediates; heads_inner: SparseMHA's feature order (d*H + h)."""
+    _check(load().gtattn_fwd_proj(_ptr(indptr), _ptr(indices), _ptr(X), _ptr(Wqkv), _ptr(bqkv), _ptr(Wo), _ptr(bo),
+                                  _ptr(Y), _ptr(qkv), _ptr(attn), int(N), int(nnz), int(F_in), int(H), int(D),
+                                  int(F_out), 1 if heads_inner else 0, float(scale), int(dtype), _stream(stream)),
+           "gtattn_fwd_proj")
+
+
+def gtattn_device_errors(reset: bool = True) -> int:
+    """Error codes recorded on the current device by the plan-less
+    tensor-core kernels (1: a bounded wait gave up); synchronises."""
+    code = ctypes.c_int(0)
+    _check(load().gtattn_device_errors(ctypes.byref(code), 1 if reset else 0), "gtattn_device_errors")
+    return code.value
 
 
 def gtattn_fwd_plan(plan, indptr, indices, Q, K, V, out, H, D, scale, dtype, stream=None):

@@ -6,6 +6,7 @@
 #include <vector>
 
 #include "dense.cuh"
+#include "gemm.cuh"
 #include "plan.cuh"
 #include "rows.cuh"
 #include "bwd.cuh"
@@ -610,5 +611,79 @@ extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indice
     }
     pool_free(ol, stream);
     pool_free(sc.base, stream);
+    return st;
+}
+
+// The attention block with its projections: q, k, v = X W^T + b (one GEMM
+// over the stacked weights, written as three [N, H, D] matrices), the fused
+// sparse attention, Y = o Wo^T + bo.
+extern "C" gtattn_status gtattn_fwd_proj(const int32_t* indptr, const int32_t* indices, const void* X,
+                                         const void* Wqkv, const float* bqkv, const void* Wo, const float* bo,
+                                         void* Y, void* qkv, void* attn, int64_t N, int64_t nnz, int F_in, int H,
+                                         int D, int F_out, int heads_inner, float scale, gtattn_dtype dtype,
+                                         cudaStream_t stream) {
+    if (N < 0 || nnz < 0 || N >= (1ll << 31) - 1 || nnz >= (1ll << 31) - 1) return GTATTN_ERR_INVALID_ARG;
+    if (F_in < 1 || F_out < 1 || H < 1 || D < 1 || (int64_t)H * D > kMaxHD) return GTATTN_ERR_INVALID_ARG;
+    if (dtype != GTATTN_F32 && dtype != GTATTN_BF16 && dtype != GTATTN_BF16_OUT_F32) return GTATTN_ERR_INVALID_ARG;
+    if (heads_inner != 0 && heads_inner != 1) return GTATTN_ERR_INVALID_ARG;
+    if (!indptr || (nnz > 0 && !indices)) return GTATTN_ERR_INVALID_ARG;
+    if (N > 0 && (!X || !Wqkv || !Wo || !Y)) return GTATTN_ERR_INVALID_ARG;
+    const bool bf = dtype != GTATTN_F32;
+    const size_t esz = bf ? 2 : 4, osz = dtype == GTATTN_BF16 ? 2 : 4;
+    const uintptr_t in_al = reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Wqkv) |
+                            reinterpret_cast<uintptr_t>(Wo) | reinterpret_cast<uintptr_t>(qkv) |
+                            reinterpret_cast<uintptr_t>(attn);
+    const uintptr_t f_al = reinterpret_cast<uintptr_t>(bqkv) | reinterpret_cast<uintptr_t>(bo) |
+                           reinterpret_cast<uintptr_t>(indptr) | reinterpret_cast<uintptr_t>(indices);
+    if ((in_al & (esz - 1)) || (f_al & 3u) || (reinterpret_cast<uintptr_t>(Y) & (osz - 1)))
+        return GTATTN_ERR_INVALID_ARG;
+    if (N == 0) return GTATTN_OK;
+    const int HD = H * D;
+    const int64_t nhd = N * HD;
+    // temporaries: q, k, v and the attention output unless the caller keeps
+    // them; the weights in head-major feature order for head-inner features
+    size_t off = 0;
+    const size_t o_qkv = off; if (!qkv) off = align_up(off + 3 * esz * static_cast<size_t>(nhd));
+    const size_t o_att = off; if (!attn) off = align_up(off + esz * static_cast<size_t>(nhd));
+    const size_t o_w1 = off, o_b1 = align_up(off + esz * 3 * static_cast<size_t>(HD) * F_in);
+    const size_t o_w2 = align_up(o_b1 + 4 * 3 * static_cast<size_t>(HD));
+    if (heads_inner) off = align_up(o_w2 + esz * static_cast<size_t>(F_out) * HD);
+    void* buf = nullptr;
+    if (off > 0) GT_TRY(pool_alloc(&buf, off, stream));
+    char* b = static_cast<char*>(buf);
+    char* q = qkv ? static_cast<char*>(qkv) : b + o_qkv;
+    void* o = attn ? attn : b + o_att;
+    const void* W1 = Wqkv;
+    const float* b1 = bqkv;
+    const void* W2 = Wo;
+    gtattn_status st = GTATTN_OK;
+    if (heads_inner) {   // SparseMHA's reshape(N, head_dim, num_heads): feature d*H + h is head h, element d
+        ProfScope ps(GTATTN_KCAT_GEMM, 2, stream);
+        st = launch_permute_rows(Wqkv, b + o_w1, bqkv, bqkv ? reinterpret_cast<float*>(b + o_b1) : nullptr, 3, H, D,
+                                 F_in, static_cast<int>(esz), stream);
+        if (st == GTATTN_OK) st = launch_permute_cols(Wo, b + o_w2, F_out, H, D, static_cast<int>(esz), stream);
+        W1 = b + o_w1;
+        b1 = bqkv ? reinterpret_cast<const float*>(b + o_b1) : nullptr;
+        W2 = b + o_w2;
+    }
+    // q, k, v: column c of X W^T goes to matrix c / HD, column c % HD
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_GEMM, 1, stream);
+        const GemmOut o1{q, nhd, HD, HD};
+        st = bf && gemm_tc_supported(X, W1, F_in, o1, false)
+                 ? launch_gemm_tc(X, W1, b1, N, 3 * HD, F_in, o1, false, stream)
+                 : launch_gemm_simt(X, W1, b1, N, 3 * HD, F_in, bf, o1, !bf, stream);
+    }
+    if (st == GTATTN_OK)
+        st = fwd_fused(indptr, indices, q, q + esz * nhd, q + 2 * esz * nhd, nullptr, nullptr, o, N, nnz, H, D, scale,
+                       bf ? GTATTN_BF16 : GTATTN_F32, stream);
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_GEMM, 1, stream);
+        const GemmOut o2{Y, 0, F_out, F_out};
+        const bool y32 = osz == 4;
+        st = bf && gemm_tc_supported(o, W2, HD, o2, y32) ? launch_gemm_tc(o, W2, bo, N, F_out, HD, o2, y32, stream)
+                                                          : launch_gemm_simt(o, W2, bo, N, F_out, HD, bf, o2, y32, stream);
+    }
+    pool_free(buf, stream);
     return st;
 }

@@ -312,6 +312,59 @@ gtattn_status gtattn_fwd_noalloc(const int32_t* indptr, const int32_t* indices, 
                                  int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
 
 /*
+ * gtattn_fwd_proj -- the attention block with its linear projections, as
+ * SparseMHA.forward of "Graph Transformer in a Nutshell" (section "Sparse
+ * Multi-head Attention": q_proj, k_proj, v_proj, the sparse attention,
+ * out_proj; nn.Linear maps with biases) and the attention part of
+ * TransLayer.forward of "Efficient Sparse Transformer implementation with
+ * DGL's builtin operators" (proj_q, proj_k, proj_v, u_dot_v / edge_softmax /
+ * u_mul_e_sum, proj_o; no biases):
+ *   q = X Wq^T + bq,  k = X Wk^T + bk,  v = X Wv^T + bv   (H heads of D)
+ *   o = SparseAttn(q, k, v, A)                             (as gtattn_fwd)
+ *   Y = o Wo^T + bo                                        (o's heads merged)
+ *   X:    [N, F_in] node features, of the input type of `dtype` (fp32, or
+ *         bf16 for GTATTN_BF16 and GTATTN_BF16_OUT_F32).
+ *   Wqkv: [3*H*D, F_in], the weights of the q, k and v maps stacked in that
+ *         order (each an nn.Linear weight [out features, in features]), input
+ *         type.  bqkv: fp32 [3*H*D] in the same order, or NULL (no biases).
+ *   Wo:   [F_out, H*D], input type.  bo: fp32 [F_out] or NULL.
+ *   Y:    [N, F_out], the output type of `dtype` (bf16 for GTATTN_BF16, else
+ *         fp32).
+ *   heads_inner: how projection features map to heads.  0: feature h*D + d
+ *         is element d of head h (TransLayer's view(-1, h, d_qkv)); 1:
+ *         feature d*H + h is element d of head h (SparseMHA's
+ *         reshape(N, head_dim, num_heads)); the out map reads o's features in
+ *         the same order.
+ *   qkv:  NULL, or [3, N, H, D] (input type, head-major whatever heads_inner
+ *         says) receiving q, k, v; attn: NULL, or [N, H, D] receiving o.
+ *         When NULL, library temporaries hold them.
+ *   scale: multiplies q.k (SparseMHA folds head_dim**-0.5 into q; the
+ *         product is the same).
+ * q, k, v and o are held in the input type between the stages (bf16 values
+ * rounded to nearest even from the fp32 accumulators); every product
+ * accumulates in fp32.  bf16 maps with F_in and H*D multiples of 8 (and
+ * 16-byte aligned arrays) run on the tensor cores (tcgen05); the others on
+ * the CUDA cores.  Pointers are device memory aligned to their element size;
+ * library temporaries come from the stream-ordered pool.  Asynchronous on
+ * `stream`.  Errors: INVALID_ARG (null pointer, sizes, dtype, heads_inner,
+ * alignment), NO_MEMORY, CUDA.  A bounded device wait of the tensor-core
+ * maps that gives up is reported by gtattn_device_errors.
+ */
+gtattn_status gtattn_fwd_proj(const int32_t* indptr, const int32_t* indices, const void* X, const void* Wqkv,
+                              const float* bqkv, const void* Wo, const float* bo, void* Y, void* qkv, void* attn,
+                              int64_t N, int64_t nnz, int F_in, int H, int D, int F_out, int heads_inner,
+                              float scale, gtattn_dtype dtype, cudaStream_t stream);
+
+/*
+ * gtattn_device_errors -- error codes recorded on the current device by
+ * kernels that have no plan to report into (the tensor-core projections of
+ * gtattn_fwd_proj): the bitwise OR since the last reset, 1 = a bounded wait
+ * gave up (its results are not valid).  Synchronises the device; with
+ * `reset`, clears the record.
+ */
+gtattn_status gtattn_device_errors(int* code, int reset);
+
+/*
  * gtattn_coo_to_csr -- builds CSR by destination from a COO edge list
  * (src[e] -> dst[e]); within a row, entries are sorted by source and
  * duplicates are kept ("Graph Transformer in a Nutshell" builds A from
@@ -346,6 +399,7 @@ typedef enum {
     GTATTN_KCAT_COMBINE = 2,  /* split-row combine */
     GTATTN_KCAT_SOFTMAX = 3,  /* unfused edge softmax */
     GTATTN_KCAT_DENSE = 4,    /* dense-block tensor-core kernel */
+    GTATTN_KCAT_GEMM = 5,     /* projections around the attention (and their weight permutations) */
     GTATTN_KCAT_COUNT = 8
 } gtattn_kernel_category;
 

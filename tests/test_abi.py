@@ -92,6 +92,25 @@ def test_host_argument_checks_bias_weighted_bwd_ndh(lib):
     assert fn(16, 16, 16, 16, 16, None, 4, 4, 2, 8, 1.0, 0, None) == INV                   # null out
 
 
+def test_host_argument_checks_proj(lib):
+    # gtattn_fwd_proj and gtattn_device_errors, rejected before device work
+    INV, OK = gt.GTATTN_ERR_INVALID_ARG, gt.GTATTN_OK
+    f = lib.gtattn_fwd_proj   # indptr indices X Wqkv bqkv Wo bo Y qkv attn N nnz F_in H D F_out heads_inner scale dtype stream
+    assert f(None, 16, 16, 16, None, 16, None, 16, None, None, 4, 4, 8, 2, 4, 8, 0, 1.0, 0, None) == INV  # null indptr
+    assert f(16, 16, None, 16, None, 16, None, 16, None, None, 4, 4, 8, 2, 4, 8, 0, 1.0, 0, None) == INV  # null X
+    assert f(16, 16, 16, 16, None, None, None, 16, None, None, 4, 4, 8, 2, 4, 8, 0, 1.0, 0, None) == INV  # null Wo
+    assert f(16, 16, 16, 16, None, 16, None, 16, None, None, 4, 4, 0, 2, 4, 8, 0, 1.0, 0, None) == INV    # F_in 0
+    assert f(16, 16, 16, 16, None, 16, None, 16, None, None, 4, 4, 8, 2, 4, 0, 0, 1.0, 0, None) == INV    # F_out 0
+    assert f(16, 16, 16, 16, None, 16, None, 16, None, None, 4, 4, 8, 2, 600, 8, 0, 1.0, 0, None) == INV  # H*D
+    assert f(16, 16, 16, 16, None, 16, None, 16, None, None, 4, 4, 8, 2, 4, 8, 3, 1.0, 0, None) == INV    # heads_inner
+    assert f(16, 16, 16, 16, None, 16, None, 16, None, None, 4, 4, 8, 2, 4, 8, 0, 1.0, 9, None) == INV    # dtype
+    assert f(16, 16, 18, 16, None, 16, None, 16, None, None, 4, 4, 8, 2, 4, 8, 0, 1.0, 0, None) == INV    # fp32 X
+    assert f(16, 16, 16, 16, 18, 16, None, 16, None, None, 4, 4, 8, 2, 4, 8, 0, 1.0, 0, None) == INV     # bias
+    assert f(16, 16, 16, 16, None, 16, None, 17, None, None, 4, 4, 8, 2, 4, 8, 0, 1.0, 1, None) == INV    # bf16 Y
+    assert f(16, 16, None, None, None, None, None, None, None, None, 0, 0, 8, 2, 4, 8, 0, 1.0, 0, None) == OK
+    assert lib.gtattn_device_errors(None, 0) == INV
+
+
 def test_product_path_has_no_oracle_dependency():
     # the package and its sources never import or link the oracle
     pkg = os.path.join(ROOT, "graph_transformer_sparse_gb300")

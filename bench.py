@@ -7,7 +7,7 @@ row kernel, the split-row combine) over the whole R-MAT graph (2^20 nodes,
 JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--path fwd|plan|probs|bias|weighted|bwd|ndh] [--impl ours|reference]
+                    [--path fwd|plan|probs|bias|weighted|bwd|ndh|proj] [--impl ours|reference]
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload
 (weak scaling, no collective on the data path); the timed region is
@@ -48,6 +48,60 @@ def unique_bytes(N, nnz, H, D, esize):
     """Each array touched once: the DRAM floor when L2 holds every reuse."""
     row = H * D * esize
     return 4 * (N + 1) + 4 * nnz + 4 * N * row
+
+
+def path_bytes(path, N, nnz, H, D, esize):
+    """(compulsory, unique-floor) bytes of one call of `path`: the forward's
+    figures plus what the variant reads or writes on top -- the fp32 bias
+    [nnz, H], the fp32 adjacency values [nnz], the fp32 logits and
+    probabilities [nnz, H] written by the unfused path; for the backward the
+    dO rows read and the fp32 dQ, dK, dV rows written."""
+    cb = compulsory_bytes(N, nnz, H, D, esize)
+    ub = unique_bytes(N, nnz, H, D, esize)
+    if path == "bias":
+        cb += 4 * nnz * H
+        ub += 4 * nnz * H
+    elif path == "weighted":
+        cb += 4 * nnz
+        ub += 4 * nnz
+    elif path == "probs":
+        cb += 2 * 4 * nnz * H
+        ub += 2 * 4 * nnz * H
+    elif path == "bwd":
+        extra = N * H * D * esize + 3 * 4 * N * H * D
+        cb += extra
+        ub += extra
+    elif path == "proj":   # hidden F = H*D in and out: X read, q/k/v and o written and read back, Y written
+        F = H * D
+        extra = N * F * esize + 2 * 3 * N * F * esize + 2 * N * F * esize + N * F * esize + 4 * F * F * esize
+        cb += extra - 4 * N * H * D * esize   # (the attention's Q, K, V, out are the q/k/v/o counted here)
+        ub += extra - 4 * N * H * D * esize
+    return cb, ub
+
+
+def proj_flops(N, H, D):
+    """Multiply-add flops of the block's two linear maps (hidden H*D)."""
+    F = H * D
+    return 2.0 * N * F * 3 * F + 2.0 * N * F * F
+
+
+def cpu_model():
+    """The host CPU's model string (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def dense_flops(n_blocks, n, H, D):
@@ -229,17 +283,23 @@ def make_step(w, d, path, gt, plan=None, probs_bufs=None):
         dO, dQ, dK, dV = probs_bufs
         return lambda: gt.gtattn_bwd(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], dO, dQ, dK, dV,
                                      w.N, w.nnz, w.H, w.D, w.scale, dt)
+    if path == "proj":   # the block with its projections (SparseMHA: biases, head-inner features)
+        X, W, b, Wo, bo, Y = probs_bufs
+        F = w.H * w.D
+        return lambda: gt.gtattn_fwd_proj(d["indptr"], d["indices"], X, W, b, Wo, bo, Y, w.N, w.nnz, F, w.H, w.D, F,
+                                          w.scale, dt, heads_inner=True)
     raise ValueError(path)
 
 
 def time_steps(step, steps, flush):
     """Per-step CUDA-event times (ms) on the current stream, L2 flushed
-    before every step (outside the events)."""
+    before every step (outside the events) unless `flush` is None."""
     import torch
     s = torch.cuda.current_stream()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in evs:
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         a.record(s)
         step()
         b.record(s)
@@ -266,6 +326,17 @@ def run_gpu_workload(w, path, steps, warmup, gt, dev, flush, want_profile=True, 
         gen.manual_seed(34567)
         dO = torch.randn(w.N, w.H, w.D, device=dev, generator=gen).to(d["Q"].dtype)
         probs_bufs = (dO,) + tuple(torch.empty(w.N, w.H, w.D, device=dev) for _ in range(3))
+    if path == "proj":   # X ~ N(0, 1), weights and biases ~ U(-1/sqrt(F), 1/sqrt(F)) (nn.Linear's init)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(45678)
+        F = w.H * w.D
+        a = 1.0 / math.sqrt(F)
+        X = torch.randn(w.N, F, device=dev, generator=gen).to(d["Q"].dtype)
+        W = ((torch.rand(3 * F, F, device=dev, generator=gen) * 2 - 1) * a).to(d["Q"].dtype)
+        Wo = ((torch.rand(F, F, device=dev, generator=gen) * 2 - 1) * a).to(d["Q"].dtype)
+        b = (torch.rand(3 * F, device=dev, generator=gen) * 2 - 1) * a
+        bo = (torch.rand(F, device=dev, generator=gen) * 2 - 1) * a
+        probs_bufs = (X, W, b, Wo, bo, torch.empty(w.N, F, dtype=d["Q"].dtype, device=dev))
     if path == "weighted":   # weighted adjacency: seeded U(0, 1) stored values, fp32 [nnz]
         gen = torch.Generator(device=dev)
         gen.manual_seed(23456)
@@ -333,10 +404,11 @@ def e2e_measure(w, gt, dev, steps, warmup):
     return statistics.median(times), h2d, d2h
 
 
-def cpu_baseline(w, min_seconds=10.0):
+def cpu_baseline(w, min_seconds=10.0, single_seconds=5.0):
     """The fp64 oracle as it stands, on the host cores: the whole workload,
-    repeated until at least `min_seconds` of wall time (about 10-30 s of
-    CPU work per core set)."""
+    repeated until at least `min_seconds` of wall time with the rows split
+    over every core; then single-threaded on a bounded random sample of rows
+    (at least `single_seconds`)."""
     import oracle
     cores = os.cpu_count() or 1
     reps = 0
@@ -348,9 +420,61 @@ def cpu_baseline(w, min_seconds=10.0):
         if dt >= min_seconds or reps >= 50:
             break
     eh = float(w.nnz) * w.H * reps
-    return dict(value=round(eh / dt, 1), unit=UNIT, cores=cores, kind="oracle",
+    # single thread: random rows (a fixed sample), repeated for the time budget
+    rng = np.random.default_rng(0)
+    deg = np.diff(w.indptr)
+    rows = np.sort(rng.choice(w.N, size=min(w.N, max(1, w.N // 64)), replace=False))
+    eh1, reps1 = float(deg[rows].sum()) * w.H, 0
+    t1 = time.perf_counter()
+    while True:
+        oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, rows=rows, threads=1)
+        reps1 += 1
+        dt1 = time.perf_counter() - t1
+        if dt1 >= single_seconds or reps1 >= 50:
+            break
+    return dict(value=round(eh / dt, 1), unit=UNIT, cores=cores, kind="oracle", cpu_model=cpu_model(),
                 sample=f"whole workload x{reps} ({dt:.1f} s wall), fp64 C oracle, rows split over "
-                       f"{cores} host threads")
+                       f"{cores} host threads",
+                single_thread={"value": round(eh1 * reps1 / dt1, 1), "unit": UNIT, "cores": 1,
+                               "sample": f"{len(rows)} random rows of {w.N} ({eh1 / (w.nnz * w.H):.2%} of the "
+                                         f"edge-heads) x{reps1} ({dt1:.1f} s wall), one host thread"})
+
+
+def link_rates(dev, nbytes=256 << 20):
+    """Pinned host <-> device copy rates (GB/s) over `nbytes`, best of 5."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+    res = {}
+    for name, fn in (("h2d_gbs", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h_gbs", lambda: h.copy_(d, non_blocking=True))):
+        best = None
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        res[name] = round(nbytes / (best / 1e3) / 1e9, 1)
+    return res
+
+
+def plan_build_ms(w, d, gt, reps=3):
+    """Host wall time of gtattn_csr_build on the workload (it synchronises
+    once), median of `reps`."""
+    import torch
+    ts = []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        pl = gt.Plan(d["indptr"], d["indices"], detect_dense=(w.name == "dense_blocks"))
+        torch.cuda.synchronize()
+        ts.append((time.perf_counter() - t0) * 1e3)
+        pl.close()
+    return round(statistics.median(ts), 4)
 
 
 def gpu_arm(args):
@@ -385,14 +509,7 @@ def gpu_arm(args):
     units = float(w.nnz) * w.H * args.steps
     value, worst_ms, _ = job_throughput(units, local_ms)
     ms_per_step = worst_ms / args.steps
-    cbytes = compulsory_bytes(w.N, w.nnz, w.H, w.D, esize)
-    if args.path == "bias":
-        cbytes += 4 * w.nnz * w.H   # the fp32 bias, read once per entry and head
-    if args.path == "weighted":
-        cbytes += 4 * w.nnz         # the fp32 adjacency values, read once per entry
-    if args.path == "bwd":          # + dO rows read, fp32 dQ / dK / dV written once each
-        cbytes += w.N * w.H * w.D * esize + 3 * 4 * w.N * w.H * w.D
-    ubytes = unique_bytes(w.N, w.nnz, w.H, w.D, esize)
+    cbytes, ubytes = path_bytes(args.path, w.N, w.nnz, w.H, w.D, esize)
 
     launches_per_step = sum(v["launches"] for v in prof.values()) / args.steps
     total_prof_ms = max(sum(x["ms"] for x in prof.values()), 1e-9)
@@ -410,14 +527,28 @@ def gpu_arm(args):
                     "algorithmic_flops_per_launch": flops, "kernel_ms": round(kern_ms, 5),
                     "kernel_shares": shares}
     else:
-        achieved = cbytes / (kern_ms / 1e3) / 1e9
+        # achieved: the unique-bytes floor (each array crosses HBM once) over
+        # the kernel's time; the compulsory figure (every K/V gather counted,
+        # most served by the L2) and the ncu DRAM bytes sit beside it
+        achieved = ubytes / (kern_ms / 1e3) / 1e9
+        traffic = ncu_traffic("k_rows_vec", name) if args.path == "fwd" else None
         roofline = {"bound": "hbm", "kernel": "k_rows_vec (fused row kernel)", "achieved": round(achieved, 1),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                    "traffic": ncu_traffic("k_rows_vec", name) if args.path == "fwd" else None,
+                    "traffic": traffic,
                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)"
                     if peaks["source"] == "measured" else "fallback 6.8 TB/s",
-                    "algorithmic_bytes_per_launch": cbytes, "unique_bytes_floor": ubytes,
+                    "algorithmic_bytes_per_launch": ubytes,
+                    "algorithmic_bytes": "unique floor: indptr, indices, Q, K, V and out once each",
+                    "compulsory_bytes_per_launch": cbytes,
+                    "frac_compulsory": round(cbytes / (kern_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                    "frac_dram": (round(traffic / (kern_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
+                                  if traffic else None),
+                    "traffic_over_unique": round(traffic / ubytes, 3) if traffic else None,
                     "kernel_ms": round(kern_ms, 5), "kernel_shares": shares}
+    # the same step with a warm L2 (no flush between steps)
+    warm = time_steps(step, args.steps, None)
+    warm_ms = statistics.median(warm)
+    build_ms = plan_build_ms(w, d, gt)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
@@ -429,13 +560,18 @@ def gpu_arm(args):
                             "bias": "gtattn_fwd_bias (fused, per-edge per-head additive bias, fp32 N(0,1))",
                             "weighted": "gtattn_fwd_weighted (fused, weighted adjacency, fp32 U(0,1))",
                             "bwd": "gtattn_bwd (dQ, dK, dV of sum(out * dO), dO ~ N(0,1))",
-                            "ndh": "gtattn_fwd_ndh (head-innermost [N, D, H] rows, generic kernel)"}[args.path],
+                            "ndh": "gtattn_fwd_ndh (head-innermost [N, D, H] rows, generic kernel)",
+                            "proj": "gtattn_fwd_proj (q/k/v and output projections around the attention, "
+                                    "hidden H*D, biases, head-inner features)"}[args.path],
                    "l2": "flushed before every timed step (512 MiB memset, outside the events)",
                    "clock_soak": f"{args.soak:g} s of untimed steps before the warm-up; clocks sampled from "
                                  f"then to the end",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
-        "achieved_gbs_step": round(cbytes / (ms_per_step / 1e3) / 1e9, 1),
-        "hbm_frac_step": round(cbytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+        "achieved_gbs_step": round(ubytes / (ms_per_step / 1e3) / 1e9, 1),
+        "hbm_frac_step": round(ubytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+        "hbm_frac_step_compulsory": round(cbytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+        "ms_per_step_warm_l2": round(warm_ms, 5),
+        "plan_build_ms": build_ms,
         "roofline": roofline,
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clocks,
@@ -446,12 +582,18 @@ def gpu_arm(args):
     if rank == 0 and not args.no_e2e:
         e_ms, h2d, d2h = e2e_measure(w, gt, dev, max(3, min(args.steps, 9)), 2)
         line["e2e"] = {"value": round(w.nnz * w.H / (e_ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                       "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4)}
+                       "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4),
+                       "link": link_rates(dev)}
+        # the copies alone at the measured link rates (the two directions
+        # overlap, so the longer one): the floor of the end-to-end step
+        ln = line["e2e"]["link"]
+        line["e2e"]["copy_floor_ms"] = round(max(h2d / (ln["h2d_gbs"] * 1e9), d2h / (ln["d2h_gbs"] * 1e9)) * 1e3, 4)
     if rank == 0 and not args.no_extra:
         extra = {}
         for other, pth in (("erdos_renyi", "fwd"), ("molecules", "fwd"), ("tiny_random", "fwd"),
                            ("dense_blocks", "plan"), ("rmat", "probs"), ("rmat", "bias"), ("rmat", "weighted"),
-                           ("rmat", "bwd"), ("rmat", "ndh")):
+                           ("rmat", "bwd"), ("rmat", "ndh"), ("rmat", "proj"), ("erdos_renyi", "proj"),
+                           ("molecules", "proj")):
             if other == name and pth == args.path:
                 continue
             try:
@@ -463,17 +605,26 @@ def gpu_arm(args):
                 continue
             ms = statistics.median(t_o)
             es = 2 if wo.dtype == "bf16" else 4
-            cb = compulsory_bytes(wo.N, wo.nnz, wo.H, wo.D, es)
-            if pth == "bias":
-                cb += 4 * wo.nnz * wo.H   # the fp32 bias, read once per entry and head
-            if pth == "weighted":
-                cb += 4 * wo.nnz          # the fp32 adjacency values, read once per entry
-            if pth == "bwd":              # + dO rows read, fp32 dQ / dK / dV written once each
-                cb += wo.N * wo.H * wo.D * es + 3 * 4 * wo.N * wo.H * wo.D
+            cb, ub = path_bytes(pth, wo.N, wo.nnz, wo.H, wo.D, es)
+            kms = {k: round(v["ms"] / max(v["groups"], 1), 5) for k, v in p_o.items() if v["groups"]}
             ent = {"ms": round(ms, 5), "edge_heads_per_s": round(wo.nnz * wo.H / (ms / 1e3), 1),
-                   "gbs_compulsory": round(cb / (ms / 1e3) / 1e9, 1),
-                   "hbm_frac": round(cb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-                   "kernel_ms": {k: round(v["ms"] / max(v["groups"], 1), 5) for k, v in p_o.items() if v["groups"]}}
+                   "gbs_unique": round(ub / (ms / 1e3) / 1e9, 1),
+                   "hbm_frac": round(ub / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                   "hbm_frac_compulsory": round(cb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                   "kernel_ms": kms}
+            if "rows" in kms and pth in ("fwd", "bias", "weighted"):
+                ent["rows_kernel_hbm_frac"] = round(ub / (kms["rows"] / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
+                tr = ncu_traffic("k_rows_vec", other) if pth == "fwd" else None
+                if tr:
+                    ent["rows_kernel_traffic"] = tr
+                    ent["rows_kernel_frac_dram"] = round(tr / (kms["rows"] / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
+                    ent["traffic_over_unique"] = round(tr / ub, 3)
+            if pth == "proj" and "gemm" in kms:
+                # the two linear maps' launches (permutations of the weights included)
+                tf = proj_flops(wo.N, wo.H, wo.D) / (kms["gemm"] * 3 / 1e3) / 1e12
+                ent["gemm_ms_per_call"] = round(kms["gemm"] * 3, 5)
+                ent["gemm_tflops"] = round(tf, 1)
+                ent["gemm_tensor_frac"] = round(tf / peaks["bf16_tflops"], 4) if wo.dtype == "bf16" else None
             if other == "dense_blocks" and inf_o and inf_o.get("n_dense_blocks"):
                 tf = dense_flops(inf_o["n_dense_blocks"], 512, wo.H, wo.D) / (ms / 1e3) / 1e12
                 ent["tflops"] = round(tf, 1)
@@ -535,7 +686,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="rmat", choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias", "weighted", "bwd", "ndh"])
+    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias", "weighted", "bwd", "ndh",
+                                                       "proj"])
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up (clock record under load)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")

@@ -7,7 +7,7 @@ row kernel, the split-row combine) over the whole R-MAT graph (2^20 nodes,
 JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--path fwd|plan|probs|bias|weighted|bwd|ndh|proj] [--impl ours|reference]
+                    [--path fwd|plan|probs|bias|weighted|bwd|bwd_plan|ndh|proj] [--impl ours|reference]
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload
 (weak scaling, no collective on the data path); the timed region is
@@ -67,7 +67,7 @@ def path_bytes(path, N, nnz, H, D, esize):
     elif path == "probs":
         cb += 2 * 4 * nnz * H
         ub += 2 * 4 * nnz * H
-    elif path == "bwd":
+    elif path in ("bwd", "bwd_plan"):
         extra = N * H * D * esize + 3 * 4 * N * H * D
         cb += extra
         ub += extra
@@ -283,6 +283,10 @@ def make_step(w, d, path, gt, plan=None, probs_bufs=None):
         dO, dQ, dK, dV = probs_bufs
         return lambda: gt.gtattn_bwd(d["indptr"], d["indices"], d["Q"], d["K"], d["V"], dO, dQ, dK, dV,
                                      w.N, w.nnz, w.H, w.D, w.scale, dt)
+    if path == "bwd_plan":   # training on a fixed graph: the plan keeps the source-major pattern
+        dO, dQ, dK, dV = probs_bufs
+        return lambda: gt.gtattn_bwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], dO, dQ, dK, dV,
+                                          w.H, w.D, w.scale, dt)
     if path == "proj":   # the block with its projections (SparseMHA: biases, head-inner features)
         X, W, b, Wo, bo, Y = probs_bufs
         F = w.H * w.D
@@ -313,15 +317,15 @@ def run_gpu_workload(w, path, steps, warmup, gt, dev, flush, want_profile=True, 
     d = device_inputs(w, dev)
     plan = None
     probs_bufs = None
-    if path == "plan":
-        plan = gt.Plan(d["indptr"], d["indices"], detect_dense=detect_dense)
+    if path in ("plan", "bwd_plan"):
+        plan = gt.Plan(d["indptr"], d["indices"], detect_dense=detect_dense and path == "plan")
     if path == "probs":
         probs_bufs = (torch.empty(w.nnz, w.H, device=dev), torch.empty(w.nnz, w.H, device=dev))
     if path == "bias":   # per-edge, per-head additive bias: seeded N(0, 1), fp32 [nnz, H]
         gen = torch.Generator(device=dev)
         gen.manual_seed(12345)
         probs_bufs = (torch.randn(w.nnz, w.H, device=dev, generator=gen),)
-    if path == "bwd":   # backward: seeded N(0, 1) output gradient in the input dtype, fp32 gradients
+    if path in ("bwd", "bwd_plan"):   # backward: seeded N(0, 1) output gradient in the input dtype, fp32 gradients
         gen = torch.Generator(device=dev)
         gen.manual_seed(34567)
         dO = torch.randn(w.N, w.H, w.D, device=dev, generator=gen).to(d["Q"].dtype)
@@ -560,6 +564,7 @@ def gpu_arm(args):
                             "bias": "gtattn_fwd_bias (fused, per-edge per-head additive bias, fp32 N(0,1))",
                             "weighted": "gtattn_fwd_weighted (fused, weighted adjacency, fp32 U(0,1))",
                             "bwd": "gtattn_bwd (dQ, dK, dV of sum(out * dO), dO ~ N(0,1))",
+                            "bwd_plan": "gtattn_bwd_plan (as bwd, source-major pattern kept in the plan)",
                             "ndh": "gtattn_fwd_ndh (head-innermost [N, D, H] rows, generic kernel)",
                             "proj": "gtattn_fwd_proj (q/k/v and output projections around the attention, "
                                     "hidden H*D, biases, head-inner features)"}[args.path],
@@ -592,7 +597,8 @@ def gpu_arm(args):
         extra = {}
         for other, pth in (("erdos_renyi", "fwd"), ("molecules", "fwd"), ("tiny_random", "fwd"),
                            ("dense_blocks", "plan"), ("rmat", "probs"), ("rmat", "bias"), ("rmat", "weighted"),
-                           ("rmat", "bwd"), ("rmat", "ndh"), ("rmat", "proj"), ("erdos_renyi", "proj"),
+                           ("rmat", "bwd"), ("rmat", "bwd_plan"), ("rmat", "ndh"), ("rmat", "proj"),
+                           ("erdos_renyi", "proj"),
                            ("molecules", "proj")):
             if other == name and pth == args.path:
                 continue
@@ -686,8 +692,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="rmat", choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias", "weighted", "bwd", "ndh",
-                                                       "proj"])
+    ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias", "weighted", "bwd", "bwd_plan",
+                                                       "ndh", "proj"])
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up (clock record under load)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")

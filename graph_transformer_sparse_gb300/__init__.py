@@ -22,7 +22,8 @@ from ._build import LIB, build
 
 __all__ = [
     "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs", "gtattn_fwd_bias", "gtattn_fwd_weighted", "gtattn_bwd", "gtattn_fwd_ndh",
-    "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_proj", "gtattn_device_errors", "gtattn_csr_build",
+    "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_proj", "gtattn_device_errors", "gtattn_bwd_plan",
+    "gtattn_csr_build",
     "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
     "gtattn_csr_validate", "gtattn_status_string", "gtattn_profile_enable", "gtattn_profile_read",
     "sparse_mha", "GTATTN_F32", "GTATTN_BF16", "GTATTN_BF16_OUT_F32",
@@ -39,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "gtattn_plan_get_info", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
     "gtattn_coo_to_csr", "gtattn_csr_validate", "gtattn_profile_enable", "gtattn_profile_read",
     "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_bias", "gtattn_fwd_weighted", "gtattn_bwd",
-    "gtattn_fwd_ndh", "gtattn_fwd_proj", "gtattn_device_errors",
+    "gtattn_fwd_ndh", "gtattn_fwd_proj", "gtattn_device_errors", "gtattn_bwd_plan",
 )
 KCAT_NAMES = ("bin", "rows", "combine", "softmax", "dense", "gemm")
 
@@ -55,7 +56,8 @@ class GtattnError(RuntimeError):
 
 class PlanOpts(ctypes.Structure):
     _fields_ = [("long_row_min", ctypes.c_int32), ("chunk_edges", ctypes.c_int32),
-                ("detect_dense", ctypes.c_int32), ("kernel", ctypes.c_int32)]
+                ("detect_dense", ctypes.c_int32), ("kernel", ctypes.c_int32), ("wait_cycles", ctypes.c_int32),
+                ("test_stall", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -112,6 +114,7 @@ def load(path: str | None = None):
             "gtattn_fwd_proj": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, i32, i32, f32,
                                  i32, vp], i32),
             "gtattn_device_errors": ([vp, i32], i32),
+            "gtattn_bwd_plan": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp], i32),
             "gtattn_profile_enable": ([i32], i32),
             "gtattn_profile_read": ([vp, i32], i32),
         }
@@ -226,6 +229,14 @@ def gtattn_fwd_proj(indptr, indices, X, Wqkv, bqkv, Wo, bo, Y, N, nnz, F_in, H, 
            "gtattn_fwd_proj")
 
 
+def gtattn_bwd_plan(plan, indptr, indices, Q, K, V, dO, dQ, dK, dV, H, D, scale, dtype, stream=None):
+    """gtattn_bwd on a plan's binning; the plan keeps the source-major
+    pattern built by its first backward call."""
+    _check(load().gtattn_bwd_plan(plan.handle if isinstance(plan, Plan) else plan, _ptr(indptr), _ptr(indices),
+                                  _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), int(H), int(D),
+                                  float(scale), int(dtype), _stream(stream)), "gtattn_bwd_plan")
+
+
 def gtattn_device_errors(reset: bool = True) -> int:
     """Error codes recorded on the current device by the plan-less
     tensor-core kernels (1: a bounded wait gave up); synchronises."""
@@ -329,10 +340,12 @@ class Plan:
     """Owns a plan built by ``gtattn_csr_build`` (freed on close/GC)."""
 
     def __init__(self, indptr, indices, N=None, nnz=None, long_row_min=0, chunk_edges=0,
-                 detect_dense=False, kernel=GTATTN_KERNEL_AUTO, stream=None):
+                 detect_dense=False, kernel=GTATTN_KERNEL_AUTO, wait_cycles=0, test_stall=False,
+                 stream=None):
         N = int(indptr.numel() - 1) if N is None else int(N)
         nnz = int(indices.numel()) if nnz is None else int(nnz)
-        self.opts = PlanOpts(int(long_row_min), int(chunk_edges), int(bool(detect_dense)), int(kernel))
+        self.opts = PlanOpts(int(long_row_min), int(chunk_edges), int(bool(detect_dense)), int(kernel),
+                             int(wait_cycles), int(bool(test_stall)))
         self.handle = gtattn_csr_build(indptr, indices, N, nnz, self.opts, stream)
         self.N, self.nnz = N, nnz
         self._keep = (indptr, indices)

@@ -410,7 +410,7 @@ extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t*
     if (dense) {
         ProfScope ps(GTATTN_KCAT_DENSE, 1, stream);
         st = launch_dense(plan->dense_tiles, plan->n_dense_tiles, N, Q, K, V, out, H, D, scale, dtype,
-                          plan->hdr + HdrLayout::kErr, stream);
+                          plan->hdr + HdrLayout::kErr, plan->opts.wait_cycles, plan->opts.test_stall, stream);
     }
     int row_tasks = n_chunks + (dense ? 0 : plan->hdr_host[HdrLayout::kDenseRows]);
     for (int b = 0; b < kNumBuckets; ++b) row_tasks += plan->hdr_host[HdrLayout::kCount + b];
@@ -510,10 +510,66 @@ extern "C" gtattn_status gtattn_fwd_weighted(const int32_t* indptr, const int32_
 }
 
 
-extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
-                                    const void* V, const void* dO, float* dQ, float* dK, float* dV, int64_t N,
-                                    int64_t nnz, int H, int D, float scale, gtattn_dtype dtype,
-                                    cudaStream_t stream) {
+// ---------------------------------------------------------------------------
+// backward
+// ---------------------------------------------------------------------------
+// The source-major copy of a graph's pattern (colptr over sources, rowid:
+// the destination rows, ascending within a source) and the binning of its
+// sources, carved from one block; and the scratch its build needs.
+struct SourceMajor {
+    int* colptr = nullptr;
+    int* rowid = nullptr;
+    TaskLists cols{};
+    int64_t max_chunks = 0;   // capacity of the source chunk list
+};
+
+static size_t source_major_carve(char* base, int64_t N, int64_t nnz, const gtattn_plan_opts& o, SourceMajor* sm) {
+    int64_t n_long = 0, n_chunks = 0;
+    worst_case_sizes(N, nnz, o.long_row_min, o.chunk_edges, &n_long, &n_chunks);
+    size_t off = 0;
+    const size_t o_cp = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N + 1));
+    const size_t o_rid = off; off = align_up(off + sizeof(int) * static_cast<size_t>(nnz));
+    const size_t o_h = off; off = align_up(off + sizeof(int) * HdrLayout::kWords);
+    const size_t o_r = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N));
+    const size_t o_c = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_chunks));
+    const size_t o_l = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_long));
+    if (base && sm) {
+        sm->colptr = reinterpret_cast<int*>(base + o_cp);
+        sm->rowid = reinterpret_cast<int*>(base + o_rid);
+        sm->cols = TaskLists{reinterpret_cast<int*>(base + o_h), reinterpret_cast<int*>(base + o_r),
+                             reinterpret_cast<int2*>(base + o_c), reinterpret_cast<int2*>(base + o_l), o.chunk_edges, 1};
+        sm->max_chunks = n_chunks;
+    }
+    return off;
+}
+
+// Builds *sm (carved already) from the destination binning `rows`: counts,
+// scan, scatter, segment sort, then the source binning.  Scratch from the pool.
+static gtattn_status source_major_build(const int32_t* indptr, const int32_t* indices, const TaskLists& rows,
+                                        int64_t N, int64_t nnz, const gtattn_plan_opts& o, const SourceMajor& sm,
+                                        cudaStream_t stream) {
+    size_t off = 0;
+    const size_t o_cur = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N));
+    const size_t o_ts = off; off = align_up(off + sizeof(int) * static_cast<size_t>(bwd_scan_tiles(N) + 1));
+    const size_t o_tmp = off; off = align_up(off + sizeof(int) * static_cast<size_t>(nnz));
+    void* scr = nullptr;
+    GT_TRY(pool_alloc(&scr, off, stream));
+    char* b = static_cast<char*>(scr);
+    gtattn_status st;
+    {
+        ProfScope ps(GTATTN_KCAT_BIN, 5 + (nnz > 0) + 4 * (nnz > 0) + bin_launches((int)N, nullptr), stream);
+        st = build_csc(indptr, indices, rows, (int)N, nnz, sm.colptr, reinterpret_cast<int*>(b + o_cur),
+                       reinterpret_cast<int*>(b + o_ts), sm.rowid, reinterpret_cast<int*>(b + o_tmp), sm.cols,
+                       o.long_row_min, stream);
+    }
+    pool_free(scr, stream);
+    return st;
+}
+
+// Host-side checks of the backward entry points.
+static gtattn_status check_bwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                               const void* V, const void* dO, const float* dQ, const float* dK, const float* dV,
+                               int64_t N, int64_t nnz, int H, int D, gtattn_dtype dtype) {
     if (N < 0 || nnz < 0 || N >= (1ll << 31) - 1 || nnz >= (1ll << 31) - 1) return GTATTN_ERR_INVALID_ARG;
     if (H < 1 || D < 1 || (int64_t)H * D > kMaxHD || H > kBwdMaxHeads) return GTATTN_ERR_INVALID_ARG;
     if (dtype != GTATTN_F32 && dtype != GTATTN_BF16 && dtype != GTATTN_BF16_OUT_F32) return GTATTN_ERR_INVALID_ARG;
@@ -527,91 +583,144 @@ extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indice
                              reinterpret_cast<uintptr_t>(dV) | reinterpret_cast<uintptr_t>(indptr) |
                              reinterpret_cast<uintptr_t>(indices);
     if ((in_al & (esz - 1)) || (out_al & 3u)) return GTATTN_ERR_INVALID_ARG;
-    if (N == 0) return GTATTN_OK;
+    return GTATTN_OK;
+}
+
+// The two-pass backward given the destination binning (rows, with row_chunks
+// chunk slots) and the source-major pattern: the forward again for its fp32
+// output and log-sum-exp, then the passes.
+static gtattn_status bwd_run(const int32_t* indptr, const int32_t* indices, const TaskLists& rows, int64_t row_chunks,
+                             const SourceMajor& sm, const void* Q, const void* K, const void* V, const void* dO,
+                             float* dQ, float* dK, float* dV, int64_t N, int64_t nnz, int H, int D, float scale,
+                             gtattn_dtype dtype, const RowChoice& c, cudaStream_t stream) {
     const int HD = H * D;
-    const size_t grad_bytes = sizeof(float) * static_cast<size_t>(N) * HD;
-    const void* ptrs[7] = {Q, K, V, dO, dQ, dK, dV};
     const gtattn_dtype fdt = dtype == GTATTN_F32 ? GTATTN_F32 : GTATTN_BF16_OUT_F32;   // fp32 forward output
-    RowChoice c;
-    if (!bwd_tasks_supported(H, D, dtype, ptrs, 7) || !choose_row_kernel(H, D, fdt, Q, K, V, dQ, GTATTN_KERNEL_AUTO, &c)) {
-        GT_CUDA(cudaMemsetAsync(dQ, 0, grad_bytes, stream));
-        GT_CUDA(cudaMemsetAsync(dK, 0, grad_bytes, stream));
-        GT_CUDA(cudaMemsetAsync(dV, 0, grad_bytes, stream));
+    const size_t grad_bytes = sizeof(float) * static_cast<size_t>(N) * HD;
+    size_t off = 0;
+    const size_t o_O = off; off = align_up(off + grad_bytes);
+    const size_t o_L = off; off = align_up(off + sizeof(float) * static_cast<size_t>(N) * H);
+    const size_t o_LD = off; off = align_up(off + sizeof(float2) * static_cast<size_t>(N) * H);
+    const size_t o_m = off; off = align_up(off + sizeof(float) * static_cast<size_t>(row_chunks) * H);
+    const size_t o_s = off; off = align_up(off + sizeof(float) * static_cast<size_t>(row_chunks) * H);
+    const size_t o_acc = off; off = align_up(off + sizeof(float) * static_cast<size_t>(row_chunks) * HD);
+    const size_t o_pq = off; off = align_up(off + sizeof(float) * static_cast<size_t>(row_chunks) * HD);
+    const size_t o_pk = off; off = align_up(off + sizeof(float) * static_cast<size_t>(sm.max_chunks) * HD);
+    const size_t o_pv = off; off = align_up(off + sizeof(float) * static_cast<size_t>(sm.max_chunks) * HD);
+    void* buf = nullptr;
+    GT_TRY(pool_alloc(&buf, off, stream));
+    char* b = static_cast<char*>(buf);
+    float* O = reinterpret_cast<float*>(b + o_O);
+    float* lse = reinterpret_cast<float*>(b + o_L);
+    Partials part{reinterpret_cast<float*>(b + o_m), reinterpret_cast<float*>(b + o_s),
+                  reinterpret_cast<float*>(b + o_acc)};
+    RowParams p = make_params(indptr, indices, Q, K, V, O, N, nnz, H, D, scale * kLog2e, c, rows, part);
+    p.lse = lse;
+    gtattn_status st;
+    {
         ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
-        return launch_bwd_rows(indptr, indices, Q, K, V, dO, dQ, dK, dV, (int)N, H, D, scale, dtype, stream);
+        st = launch_rows(kFused, fdt, c, p, stream);
     }
-    // the forward again, keeping its fp32 output and row log-sum-exp
+    if (st == GTATTN_OK && row_chunks > 0) {
+        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
+        st = launch_combine(kFused, fdt, p, stream);
+    }
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_ROWS, 4, stream);
+        st = launch_bwd_passes(indptr, indices, rows, sm.colptr, sm.rowid, sm.cols, Q, K, V, dO, O, lse,
+                               reinterpret_cast<float2*>(b + o_LD), dQ, dK, dV, reinterpret_cast<float*>(b + o_pq),
+                               reinterpret_cast<float*>(b + o_pk), reinterpret_cast<float*>(b + o_pv), (int)N, nnz, H,
+                               D, scale, dtype, stream);
+    }
+    pool_free(buf, stream);
+    return st;
+}
+
+// Shapes the two passes do not take: a warp per row with scalar atomics.
+static gtattn_status bwd_fallback(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                                  const void* V, const void* dO, float* dQ, float* dK, float* dV, int64_t N, int H,
+                                  int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
+    const size_t grad_bytes = sizeof(float) * static_cast<size_t>(N) * H * D;
+    GT_CUDA(cudaMemsetAsync(dQ, 0, grad_bytes, stream));
+    GT_CUDA(cudaMemsetAsync(dK, 0, grad_bytes, stream));
+    GT_CUDA(cudaMemsetAsync(dV, 0, grad_bytes, stream));
+    ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+    return launch_bwd_rows(indptr, indices, Q, K, V, dO, dQ, dK, dV, (int)N, H, D, scale, dtype, stream);
+}
+
+static bool bwd_two_pass(int H, int D, gtattn_dtype dtype, const void* Q, const void* K, const void* V,
+                         const void* dO, const float* dQ, const float* dK, const float* dV, RowChoice* c) {
+    const void* ptrs[7] = {Q, K, V, dO, dQ, dK, dV};
+    const gtattn_dtype fdt = dtype == GTATTN_F32 ? GTATTN_F32 : GTATTN_BF16_OUT_F32;
+    return bwd_tasks_supported(H, D, dtype, ptrs, 7) &&
+           choose_row_kernel(H, D, fdt, Q, K, V, dQ, GTATTN_KERNEL_AUTO, c);
+}
+
+extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                                    const void* V, const void* dO, float* dQ, float* dK, float* dV, int64_t N,
+                                    int64_t nnz, int H, int D, float scale, gtattn_dtype dtype,
+                                    cudaStream_t stream) {
+    GT_TRY(check_bwd(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, nnz, H, D, dtype));
+    if (N == 0) return GTATTN_OK;
+    RowChoice c;
+    if (!bwd_two_pass(H, D, dtype, Q, K, V, dO, dQ, dK, dV, &c))
+        return bwd_fallback(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, H, D, scale, dtype, stream);
     gtattn_plan_opts o;
     resolve_opts(nullptr, &o);
     Scratch sc;
     int *hdr, *rows;
     int2 *chunks, *longs;
-    GT_TRY(scratch_alloc(N, nnz, H, HD, o.long_row_min, o.chunk_edges, false, false, &sc, &hdr, &rows, &chunks,
+    GT_TRY(scratch_alloc(N, nnz, H, H * D, o.long_row_min, o.chunk_edges, false, false, &sc, &hdr, &rows, &chunks,
                          &longs, stream));
-    // the backward's own scratch: O, L, (L, Dlt), the source-major pattern
-    // and its binning
-    int64_t n_long = 0, n_chunks = 0;
-    worst_case_sizes(N, nnz, o.long_row_min, o.chunk_edges, &n_long, &n_chunks);
-    size_t off = 0;
-    const size_t o_O = off; off = align_up(off + grad_bytes);
-    const size_t o_L = off; off = align_up(off + sizeof(float) * static_cast<size_t>(N) * H);
-    const size_t o_LD = off; off = align_up(off + sizeof(float2) * static_cast<size_t>(N) * H);
-    const size_t o_cp = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N + 1));
-    const size_t o_cur = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N));
-    const size_t o_ts = off; off = align_up(off + sizeof(int) * static_cast<size_t>(bwd_scan_tiles(N) + 1));
-    const size_t o_rid = off; off = align_up(off + sizeof(int) * static_cast<size_t>(nnz));
-    const size_t o_ch = off; off = align_up(off + sizeof(int) * HdrLayout::kWords);
-    const size_t o_cr = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N));
-    const size_t o_cc = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_chunks));
-    const size_t o_cl = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_long));
-    void* ol = nullptr;
-    gtattn_status st = pool_alloc(&ol, off, stream);
-    if (st != GTATTN_OK) {
-        pool_free(sc.base, stream);
-        return st;
-    }
-    char* bb = static_cast<char*>(ol);
-    float* O = reinterpret_cast<float*>(bb + o_O);
-    float* lse = reinterpret_cast<float*>(bb + o_L);
-    float2* LD = reinterpret_cast<float2*>(bb + o_LD);
-    int* colptr = reinterpret_cast<int*>(bb + o_cp);
-    int* cursor = reinterpret_cast<int*>(bb + o_cur);
-    int* tsum = reinterpret_cast<int*>(bb + o_ts);
-    int* rowid = reinterpret_cast<int*>(bb + o_rid);
-    int* chdr = reinterpret_cast<int*>(bb + o_ch);
-    int* ccols = reinterpret_cast<int*>(bb + o_cr);
-    int2* cchunks = reinterpret_cast<int2*>(bb + o_cc);
-    int2* clongs = reinterpret_cast<int2*>(bb + o_cl);
-    const TaskLists col_lists{chdr, ccols, cchunks, clongs, o.chunk_edges, 1};
-    {
+    int64_t n_long = 0, row_chunks = 0;
+    worst_case_sizes(N, nnz, o.long_row_min, o.chunk_edges, &n_long, &row_chunks);
+    void* smb = nullptr;
+    gtattn_status st = pool_alloc(&smb, source_major_carve(nullptr, N, nnz, o, nullptr), stream);
+    SourceMajor sm;
+    if (st == GTATTN_OK) {
+        source_major_carve(static_cast<char*>(smb), N, nnz, o, &sm);
         ProfScope ps(GTATTN_KCAT_BIN, bin_launches((int)N, nullptr), stream);
         st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
     }
-    RowParams p = make_params(indptr, indices, Q, K, V, O, N, nnz, H, D, scale * kLog2e, c, sc.lists, sc.part);
-    p.lse = lse;
-    if (st == GTATTN_OK) {
-        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
-        st = launch_rows(kFused, fdt, c, p, stream);
-    }
-    if (st == GTATTN_OK && nnz > o.long_row_min) {
-        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
-        st = launch_combine(kFused, fdt, p, stream);
-    }
-    if (st == GTATTN_OK) {
-        ProfScope ps(GTATTN_KCAT_BIN, 4 + (nnz > 0) + bin_launches((int)N, nullptr), stream);
-        st = build_csc(indptr, indices, sc.lists, (int)N, nnz, colptr, cursor, tsum, rowid, dQ, HD, stream);
-        if (st == GTATTN_OK)
-            st = bin_rows(colptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, chdr, ccols, cchunks, clongs,
-                          stream);
-    }
-    if (st == GTATTN_OK) {
-        ProfScope ps(GTATTN_KCAT_ROWS, 2, stream);
-        st = launch_bwd_passes(indptr, indices, sc.lists, colptr, rowid, col_lists, clongs, Q, K, V, dO, O, lse, LD,
-                               dQ, dK, dV, (int)N, nnz, H, D, scale, dtype, stream);
-    }
-    pool_free(ol, stream);
+    if (st == GTATTN_OK) st = source_major_build(indptr, indices, sc.lists, N, nnz, o, sm, stream);
+    if (st == GTATTN_OK)
+        st = bwd_run(indptr, indices, sc.lists, row_chunks, sm, Q, K, V, dO, dQ, dK, dV, N, nnz, H, D, scale, dtype, c,
+                     stream);
+    pool_free(smb, stream);
     pool_free(sc.base, stream);
     return st;
+}
+
+extern "C" gtattn_status gtattn_bwd_plan(const gtattn_plan* plan, const int32_t* indptr, const int32_t* indices,
+                                         const void* Q, const void* K, const void* V, const void* dO, float* dQ,
+                                         float* dK, float* dV, int H, int D, float scale, gtattn_dtype dtype,
+                                         cudaStream_t stream) {
+    if (!plan) return GTATTN_ERR_INVALID_ARG;
+    const int64_t N = plan->N, nnz = plan->nnz;
+    GT_TRY(check_bwd(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, nnz, H, D, dtype));
+    if (N == 0) return GTATTN_OK;
+    RowChoice c;
+    if (!bwd_two_pass(H, D, dtype, Q, K, V, dO, dQ, dK, dV, &c))
+        return bwd_fallback(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, H, D, scale, dtype, stream);
+    // the plan's destination binning, dense segment included (the forward
+    // is recomputed by the row kernels for every row)
+    const TaskLists rows{plan->hdr, plan->rows, plan->chunks, plan->longs, plan->opts.chunk_edges, 1};
+    const int64_t row_chunks = plan->hdr_host[HdrLayout::kChunks];
+    SourceMajor sm;
+    if (!plan->bwd_pattern) {   // first backward with this plan: the source-major pattern, kept
+        void* p = nullptr;
+        GT_CUDA(cudaMalloc(&p, source_major_carve(nullptr, N, nnz, plan->opts, nullptr)));
+        source_major_carve(static_cast<char*>(p), N, nnz, plan->opts, &sm);
+        const gtattn_status st = source_major_build(indptr, indices, rows, N, nnz, plan->opts, sm, stream);
+        if (st != GTATTN_OK) {
+            cudaStreamSynchronize(stream);
+            cudaFree(p);
+            return st;
+        }
+        plan->bwd_pattern = p;
+    }
+    source_major_carve(static_cast<char*>(plan->bwd_pattern), N, nnz, plan->opts, &sm);
+    return bwd_run(indptr, indices, rows, row_chunks, sm, Q, K, V, dO, dQ, dK, dV, N, nnz, H, D, scale, dtype, c,
+                   stream);
 }
 
 // The attention block with its projections: q, k, v = X W^T + b (one GEMM

@@ -28,6 +28,7 @@
 #include <type_traits>
 #include <unordered_map>
 
+#include "plan.cuh"
 #include "rows.cuh"
 
 namespace gt {
@@ -247,25 +248,11 @@ template <int E> struct Raw<__nv_bfloat16, E> {
 };
 
 template <int E>
-__device__ __forceinline__ void atomic_add_vec(float* dst, const float* x, float c) {
-#pragma unroll
-    for (int k = 0; k < E / 4; ++k)
-        atomicAdd(reinterpret_cast<float4*>(dst) + k,
-                  make_float4(c * x[4 * k], c * x[4 * k + 1], c * x[4 * k + 2], c * x[4 * k + 3]));
-}
-
-template <int E>
 __device__ __forceinline__ void store_vec(float* dst, const float* x, float c) {
 #pragma unroll
     for (int k = 0; k < E / 4; ++k)
         reinterpret_cast<float4*>(dst)[k] =
             make_float4(c * x[4 * k], c * x[4 * k + 1], c * x[4 * k + 2], c * x[4 * k + 3]);
-}
-
-// zeroes node row `r` (HD floats) with the warp's lanes
-__device__ __forceinline__ void zero_row(float* a, int64_t r, int HD, int lane) {
-    float4* p = reinterpret_cast<float4*>(a + r * HD);
-    for (int k = lane; k < HD / 4; k += 32) p[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 constexpr int kTaskWarps = 8;
@@ -284,6 +271,7 @@ template <typename T, int E, int PASS> constexpr int pass_min_blocks() {
 struct Task {
     int row, beg, end;
     bool whole, first;
+    int chunk;   // index in the chunk list (split rows), else -1
 };
 __device__ __forceinline__ Task task_at(int t, int n_rows, const int* __restrict__ ptr, const int* __restrict__ rows,
                                         const int2* __restrict__ chunks, int chunk_edges) {
@@ -293,8 +281,10 @@ __device__ __forceinline__ Task task_at(int t, int n_rows, const int* __restrict
         k.beg = ptr[k.row];
         k.end = ptr[k.row + 1];
         k.whole = k.first = true;
+        k.chunk = -1;
     } else {
-        const int2 c = chunks[t - n_rows];
+        k.chunk = t - n_rows;
+        const int2 c = chunks[k.chunk];
         k.row = c.x;
         k.beg = c.y;
         const int re = ptr[c.x + 1];
@@ -407,14 +397,14 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_apply(const int* cnt, int
 }
 
 // rowid[slot] = destination row of each entry, slots taken per source from
-// cursor (so the order within a source is arbitrary); also zeroes dQ of the
-// split rows, which pass 1 adds to
+// cursor (the order within a source is that of the slot claims; the
+// segment sort below makes it ascending)
 __global__ void __launch_bounds__(kTaskWarps * 32)
 k_csc_scatter(const int* __restrict__ indptr, const int* __restrict__ indices, const int* __restrict__ hdr,
               const int* __restrict__ rows, const int2* __restrict__ chunks, int chunk_edges, int N,
-              int* __restrict__ cursor, int* __restrict__ rowid, float* __restrict__ dQ, int HD) {
+              int* __restrict__ cursor, int* __restrict__ rowid) {
     const int lane = threadIdx.x & 31;
-    const int n_rows = hdr[HdrLayout::kDenseSeg];
+    const int n_rows = hdr[HdrLayout::kDenseSeg] + hdr[HdrLayout::kDenseRows];   // the dense segment too
     const int n_tasks = n_rows + hdr[HdrLayout::kChunks];
     for (int t = blockIdx.x * kTaskWarps + (threadIdx.x >> 5); t < n_tasks; t += gridDim.x * kTaskWarps) {
         const Task k = task_at(t, n_rows, indptr, rows, chunks, chunk_edges);
@@ -428,7 +418,166 @@ k_csc_scatter(const int* __restrict__ indptr, const int* __restrict__ indices, c
             for (int u = 0; u < 4; ++u)
                 if (at[u] >= 0) rowid[at[u]] = k.row;
         }
-        if (!k.whole && k.first) zero_row(dQ, k.row, HD, lane);
+    }
+}
+
+// ---- segment sort: each source's destination rows in ascending order ------
+// The slot claims of the scatter come in no fixed order; sorted segments make
+// the source-major pattern, and so every sum pass 2 forms, the same on every
+// run.  Bitonic sorting networks, by segment length:
+//   <= 32      a warp each, one value a lane (shuffles)
+//   <= 256     a warp each, eight values a lane (shuffles and registers)
+//   <= 2048    a block each, in shared memory
+//   longer     a block each, runs of 32768 in shared memory; runs merged
+//              pairwise through `tmp` (merge path: each thread finds its share
+//              of the merged output by a binary search of the two runs)
+constexpr int kSortThreads = 256;
+constexpr int kSortMid = 2048;      // segments a block sorts in static shared memory
+constexpr int kSortRun = 32768;     // runs a block sorts in dynamic shared memory (128 KB)
+
+// Bitonic sort of the warp's 32*R values, value index x = r*32 + lane.
+template <int R>
+__device__ __forceinline__ void warp_bitonic(int (&v)[R], int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32 * R; k <<= 1) {
+#pragma unroll
+        for (int m = k >> 1; m > 0; m >>= 1) {
+            if (m >= 32) {   // partner in register r ^ (m / 32), same lane
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int p = r ^ (m >> 5);
+                    if (p > r) {
+                        const bool up = ((r * 32 + lane) & k) == 0;
+                        const int a = v[r], b = v[p];
+                        if ((a > b) == up) { v[r] = b; v[p] = a; }
+                    }
+                }
+            } else {         // partner in lane lane ^ m, same register
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int o = __shfl_xor_sync(0xffffffffu, v[r], m);
+                    const bool lower = (lane & m) == 0, up = ((r * 32 + lane) & k) == 0;
+                    v[r] = (lower == up) ? min(v[r], o) : max(v[r], o);
+                }
+            }
+        }
+    }
+}
+
+// A warp per source with lo < length <= 32*R.
+template <int R>
+__global__ void __launch_bounds__(256)
+k_seg_sort_warp(const int* __restrict__ colptr, int N, int lo, int* __restrict__ rowid) {
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); j < N; j += warps) {
+        const int beg = colptr[j], len = colptr[j + 1] - beg;
+        if (len <= lo || len > 32 * R) continue;   // uniform over the warp
+        int v[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) v[r] = r * 32 + lane < len ? rowid[beg + r * 32 + lane] : 0x7fffffff;
+        warp_bitonic<R>(v, lane);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (r * 32 + lane < len) rowid[beg + r * 32 + lane] = v[r];
+    }
+}
+
+// position in the merge of sorted a[0, na) and b[0, nb) at which output
+// index d falls: the number of elements taken from a (ties: a first)
+__device__ __forceinline__ int merge_split(const int* a, int na, const int* b, int nb, int d) {
+    int lo = max(0, d - nb), hi = min(d, na);
+    while (lo < hi) {
+        const int m = (lo + hi) >> 1;
+        if (a[m] <= b[d - m - 1]) lo = m + 1;
+        else hi = m;
+    }
+    return lo;
+}
+
+// Bitonic sort of buf[0, p2) (p2 a power of two) by the block.
+__device__ __forceinline__ void block_bitonic(int* buf, int p2) {
+    for (int k = 2; k <= p2; k <<= 1) {
+        for (int m = k >> 1; m > 0; m >>= 1) {
+            for (int i = threadIdx.x; i < p2 / 2; i += kSortThreads) {
+                // the i-th pair of this step: lower index x, partner x + m
+                const int x = (i / m) * 2 * m + (i % m);
+                const int a = buf[x], b = buf[x + m];
+                const bool up = (x & k) == 0;
+                if ((a > b) == up) {
+                    buf[x] = b;
+                    buf[x + m] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// List positions, in a binning's row list (heaviest bucket first), of the
+// rows of degree lo+1 .. hi (hi = 0: no upper limit): [first, last).
+__device__ __forceinline__ int2 bucket_span(const int* hdr, int lo, int hi) {
+    auto end_of = [&](int b) { return hdr[HdrLayout::kOffset + b] + hdr[HdrLayout::kCount + b]; };
+    const int last = end_of(bucket_of(lo + 1));
+    const int first = hi > 0 && hi + 1 <= 0x3fffffff ? end_of(bucket_of(hi + 1)) : 0;
+    return make_int2(hi > 0 ? first : 0, last);
+}
+
+// A block per source of degree lo+1 .. hi (hi = 0: any above lo), taken from
+// the source binning: its split sources (the longs list) and the sources of
+// its row list's buckets in that degree range; runs of RUN values sorted in
+// shared memory (static for RUN <= kSortMid, else dynamic), merged pairwise
+// through tmp when the segment is longer than one run.
+template <int RUN>
+__global__ void __launch_bounds__(kSortThreads)
+k_seg_sort_block(const int* __restrict__ colptr, const int* __restrict__ hdr, const int* __restrict__ cols,
+                 const int2* __restrict__ longs, int lo, int hi, int* __restrict__ rowid, int* __restrict__ tmp) {
+    extern __shared__ int dyn[];
+    __shared__ int stat[RUN <= kSortMid ? RUN : 1];
+    int* buf = RUN <= kSortMid ? stat : dyn;
+    const int n_long = hdr[HdrLayout::kLong];
+    const int2 span = bucket_span(hdr, lo, hi);
+    const int n_sel = n_long + (span.y - span.x);
+    for (int t = blockIdx.x; t < n_sel; t += gridDim.x) {
+        const int j = t < n_long ? longs[t].x : cols[span.x + t - n_long];
+        const int beg = colptr[j], len = colptr[j + 1] - beg;
+        if (len <= lo || (hi > 0 && len > hi)) continue;   // uniform over the block
+        for (int r0 = 0; r0 < len; r0 += RUN) {
+            const int n = min(RUN, len - r0);
+            int p2 = 64;
+            while (p2 < n) p2 <<= 1;
+            for (int i = threadIdx.x; i < p2; i += kSortThreads) buf[i] = i < n ? rowid[beg + r0 + i] : 0x7fffffff;
+            __syncthreads();
+            block_bitonic(buf, p2);
+            for (int i = threadIdx.x; i < n; i += kSortThreads) rowid[beg + r0 + i] = buf[i];
+            __syncthreads();
+        }
+        // merge runs pairwise: width w -> 2w, alternating rowid and tmp
+        int* src = rowid + beg;
+        int* dst = tmp + beg;
+        for (int w = RUN; w < len; w <<= 1) {
+            for (int a0 = 0; a0 < len; a0 += 2 * w) {
+                const int na = min(w, len - a0), nb = max(0, min(w, len - a0 - w));
+                const int tot = na + nb;
+                const int* A = src + a0;
+                const int* B = A + na;
+                const int per = (tot + kSortThreads - 1) / kSortThreads;
+                const int d0 = min(tot, static_cast<int>(threadIdx.x) * per), d1 = min(tot, d0 + per);
+                int ia = merge_split(A, na, B, nb, d0);
+                int ib = d0 - ia;
+                for (int d = d0; d < d1; ++d) {
+                    const bool take_a = ib >= nb || (ia < na && A[ia] <= B[ib]);
+                    dst[a0 + d] = take_a ? A[ia++] : B[ib++];
+                }
+            }
+            __syncthreads();
+            int* t = src;
+            src = dst;
+            dst = t;
+        }
+        if (src != rowid + beg)   // the last merge landed in tmp
+            for (int i = threadIdx.x; i < len; i += kSortThreads) rowid[beg + i] = src[i];
+        __syncthreads();
     }
 }
 
@@ -448,16 +597,15 @@ __device__ __forceinline__ Task group_task(int t, int n_tasks, int n_chunks, con
 }
 
 // ---- pass 1: by destination row ------------------------------------------
-// Also zeroes dK and dV of the split sources (listed by the source binning),
-// which pass 2 adds to.
+// A chunk of a split row stores its partial sum in part_dq[chunk]; the
+// combine adds a row's chunks in chunk order.
 template <typename T, int E, int U>
 __global__ void __launch_bounds__(kPassWarps * 32, pass_min_blocks<T, E, 1>())
 k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const int* __restrict__ hdr,
-         const int* __restrict__ rows, const int2* __restrict__ chunks, int chunk_edges,
-         const int* __restrict__ col_hdr, const int2* __restrict__ col_longs, const T* __restrict__ Q,
+         const int* __restrict__ rows, const int2* __restrict__ chunks, int chunk_edges, const T* __restrict__ Q,
          const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO, const float* __restrict__ O,
-         const float* __restrict__ L, float2* __restrict__ LD, float* __restrict__ dQ, float* __restrict__ dK,
-         float* __restrict__ dV, int H, int G, int lph, float scale) {
+         const float* __restrict__ L, float2* __restrict__ LD, float* __restrict__ dQ, float* __restrict__ part_dq,
+         int H, int G, int lph, float scale) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gl = lane & (G - 1), slot = lane / G, S = 32 / G;
@@ -470,7 +618,7 @@ k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const 
         return v;
     };
     const int n_chunks = hdr[HdrLayout::kChunks];
-    const int n_tasks = hdr[HdrLayout::kDenseSeg] + n_chunks;
+    const int n_tasks = hdr[HdrLayout::kDenseSeg] + hdr[HdrLayout::kDenseRows] + n_chunks;
     for (int t0 = (blockIdx.x * kPassWarps + warp) * S; t0 < n_tasks; t0 += gridDim.x * kPassWarps * S) {
         Task k = group_task(t0 + slot, n_tasks, n_chunks, indptr, rows, chunks, chunk_edges);
         const int64_t off = static_cast<int64_t>(k.row) * HD + gl * E;
@@ -545,15 +693,8 @@ k_bwd_dq(const int* __restrict__ indptr, const int* __restrict__ indices, const 
         }
         if (walk) {
             if (k.whole) store_vec<E>(dQ + off, dq, scale);
-            else atomic_add_vec<E>(dQ + off, dq, scale);
+            else store_vec<E>(part_dq + static_cast<int64_t>(k.chunk) * HD + gl * E, dq, scale);
         }
-    }
-    // split sources: zero their dK, dV rows for pass 2's atomics
-    const int n_long = col_hdr[HdrLayout::kLong];
-    for (int c = blockIdx.x * kPassWarps + warp; c < n_long; c += gridDim.x * kPassWarps) {
-        const int j = col_longs[c].x;
-        zero_row(dK, j, HD, lane);
-        zero_row(dV, j, HD, lane);
     }
 }
 
@@ -563,8 +704,8 @@ __global__ void __launch_bounds__(kPassWarps * 32, pass_min_blocks<T, E, 2>())
 k_bwd_dkv(const int* __restrict__ colptr, const int* __restrict__ rowid, const int* __restrict__ hdr,
           const int* __restrict__ cols, const int2* __restrict__ chunks, int chunk_edges,
           const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
-          const float2* __restrict__ LD, float* __restrict__ dK, float* __restrict__ dV, int H, int G, int lph,
-          float scale) {
+          const float2* __restrict__ LD, float* __restrict__ dK, float* __restrict__ dV, float* __restrict__ part_dk,
+          float* __restrict__ part_dv, int H, int G, int lph, float scale) {
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gl = lane & (G - 1), slot = lane / G, S = 32 / G;
@@ -576,7 +717,7 @@ k_bwd_dkv(const int* __restrict__ colptr, const int* __restrict__ rowid, const i
         return v;
     };
     const int n_chunks = hdr[HdrLayout::kChunks];
-    const int n_tasks = hdr[HdrLayout::kDenseSeg] + n_chunks;
+    const int n_tasks = hdr[HdrLayout::kDenseSeg] + hdr[HdrLayout::kDenseRows] + n_chunks;
     for (int t0 = (blockIdx.x * kPassWarps + warp) * S; t0 < n_tasks; t0 += gridDim.x * kPassWarps * S) {
         const Task k = group_task(t0 + slot, n_tasks, n_chunks, colptr, cols, chunks, chunk_edges);
         const int64_t off = static_cast<int64_t>(k.row) * HD + gl * E;
@@ -632,10 +773,42 @@ k_bwd_dkv(const int* __restrict__ colptr, const int* __restrict__ rowid, const i
             if (k.whole) {
                 store_vec<E>(dK + off, dk, scale);
                 store_vec<E>(dV + off, dv, 1.f);
-            } else {
-                atomic_add_vec<E>(dK + off, dk, scale);
-                atomic_add_vec<E>(dV + off, dv, 1.f);
+            } else {   // a chunk of a split source: its partial sums
+                const int64_t po = static_cast<int64_t>(k.chunk) * HD + gl * E;
+                store_vec<E>(part_dk + po, dk, scale);
+                store_vec<E>(part_dv + po, dv, 1.f);
             }
+        }
+    }
+}
+
+// ---- split rows and sources: their chunks' partial sums, in chunk order ----
+// A warp per split row (longs: (row, first chunk)); out[row] = sum over the
+// row's chunks of part[chunk], a float4 a lane.  Up to two arrays at once
+// (dK and dV of a split source).
+__global__ void __launch_bounds__(256)
+k_bwd_chunk_sum(const int* __restrict__ ptr, const int* __restrict__ hdr, const int2* __restrict__ longs,
+                int chunk_edges, int HD, const float* __restrict__ part0, float* __restrict__ out0,
+                const float* __restrict__ part1, float* __restrict__ out1) {
+    const int lane = threadIdx.x & 31;
+    const int n_long = hdr[HdrLayout::kLong];
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int li = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); li < n_long; li += warps) {
+        const int2 lr = longs[li];
+        const int nch = (ptr[lr.x + 1] - ptr[lr.x] + chunk_edges - 1) / chunk_edges;
+        for (int q = lane; q < HD / 4; q += 32) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            for (int c = 0; c < nch; ++c) {
+                const int64_t o = static_cast<int64_t>(lr.y + c) * HD;
+                const float4 x = reinterpret_cast<const float4*>(part0 + o)[q];
+                a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+                if (part1) {
+                    const float4 y = reinterpret_cast<const float4*>(part1 + o)[q];
+                    b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+                }
+            }
+            reinterpret_cast<float4*>(out0 + static_cast<int64_t>(lr.x) * HD)[q] = a;
+            if (part1) reinterpret_cast<float4*>(out1 + static_cast<int64_t>(lr.x) * HD)[q] = b;
         }
     }
 }
@@ -709,7 +882,8 @@ static int task_grid(Kern kernel, int task_bound, int warps) {
 }
 
 gtattn_status build_csc(const int* indptr, const int* indices, const TaskLists& L, int N, int64_t nnz,
-                        int* colptr, int* cursor, int* tsum, int* rowid, float* dQ, int HD, cudaStream_t s) {
+                        int* colptr, int* cursor, int* tsum, int* rowid, int* tmp, const TaskLists& C,
+                        int long_min, cudaStream_t s) {
     GT_CUDA(cudaMemsetAsync(cursor, 0, sizeof(int) * static_cast<size_t>(N), s));
     if (nnz > 0) {
         const int64_t want = (nnz + 255) / 256;
@@ -726,16 +900,42 @@ gtattn_status build_csc(const int* indptr, const int* indices, const TaskLists& 
     GT_CUDA(cudaGetLastError());
     const int grid = task_grid(k_csc_scatter, row_task_bound(N, nnz, L.chunk_edges), kTaskWarps);
     k_csc_scatter<<<grid, kTaskWarps * 32, 0, s>>>(indptr, indices, L.hdr, L.rows, L.chunks, L.chunk_edges, N,
-                                                   cursor, rowid, dQ, HD);
+                                                   cursor, rowid);
     GT_CUDA(cudaGetLastError());
+    // the source binning, whose degree buckets pick the segments of each sort class
+    GT_TRY(bin_rows(colptr, N, long_min, C.chunk_edges, nullptr, const_cast<int*>(C.hdr), const_cast<int*>(C.rows),
+                    const_cast<int2*>(C.chunks), const_cast<int2*>(C.longs), s));
+    if (nnz > 0 && N > 0) {   // segment sort, by length class
+        const int wg = static_cast<int>(std::min<int64_t>((N + 7) / 8, static_cast<int64_t>(num_sms()) * 16));
+        k_seg_sort_warp<1><<<wg, 256, 0, s>>>(colptr, N, 1, rowid);
+        k_seg_sort_warp<8><<<wg, 256, 0, s>>>(colptr, N, 32, rowid);
+        k_seg_sort_block<kSortMid><<<num_sms() * 8, kSortThreads, 0, s>>>(colptr, C.hdr, C.rows, C.longs, 256,
+                                                                          kSortMid, rowid, tmp);
+        GT_CUDA(cudaGetLastError());
+        static std::mutex mu;
+        static bool set[64] = {};
+        int dev = 0;
+        GT_CUDA(cudaGetDevice(&dev));
+        {
+            std::lock_guard<std::mutex> g(mu);
+            if (dev < 0 || dev >= 64 || !set[dev]) {
+                GT_CUDA(cudaFuncSetAttribute(k_seg_sort_block<kSortRun>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(sizeof(int) * kSortRun)));
+                if (dev >= 0 && dev < 64) set[dev] = true;
+            }
+        }
+        k_seg_sort_block<kSortRun><<<num_sms(), kSortThreads, sizeof(int) * kSortRun, s>>>(
+            colptr, C.hdr, C.rows, C.longs, kSortMid, 0, rowid, tmp);
+        GT_CUDA(cudaGetLastError());
+    }
     return GTATTN_OK;
 }
 
 gtattn_status launch_bwd_passes(const int* indptr, const int* indices, const TaskLists& rows, const int* colptr,
-                                const int* rowid, const TaskLists& cols, const int2* col_longs, const void* Q,
-                                const void* K, const void* V, const void* dO, const float* O, const float* lse,
-                                float2* LD, float* dQ, float* dK, float* dV, int N, int64_t nnz, int H, int D,
-                                float scale, gtattn_dtype dtype, cudaStream_t s) {
+                                const int* rowid, const TaskLists& cols, const void* Q, const void* K, const void* V,
+                                const void* dO, const float* O, const float* lse, float2* LD, float* dQ, float* dK,
+                                float* dV, float* part_dq, float* part_dk, float* part_dv, int N, int64_t nnz, int H,
+                                int D, float scale, gtattn_dtype dtype, cudaStream_t s) {
     int E = 0, G = 0;
     if (!bwd_layout(H, D, &E, &G)) return GTATTN_ERR_UNSUPPORTED;
     const int lph = D / E;
@@ -751,14 +951,22 @@ gtattn_status launch_bwd_passes(const int* indptr, const int* indices, const Tas
         const T* g = static_cast<const T*>(dO);
         auto k1 = k_bwd_dq<T, EE, U>;
         k1<<<task_grid(k1, bound_r, kPassWarps), kPassWarps * 32, 0, s>>>(
-            indptr, indices, rows.hdr, rows.rows, rows.chunks, rows.chunk_edges, cols.hdr, col_longs, q, k, v, g, O,
-            lse, LD, dQ, dK, dV, H, G, lph, scale);
+            indptr, indices, rows.hdr, rows.rows, rows.chunks, rows.chunk_edges, q, k, v, g, O, lse, LD, dQ, part_dq,
+            H, G, lph, scale);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         auto k2 = k_bwd_dkv<T, EE, U>;
         k2<<<task_grid(k2, bound_c, kPassWarps), kPassWarps * 32, 0, s>>>(
-            colptr, rowid, cols.hdr, cols.rows, cols.chunks, cols.chunk_edges, q, k, v, g, LD, dK, dV, H, G, lph,
-            scale);
+            colptr, rowid, cols.hdr, cols.rows, cols.chunks, cols.chunk_edges, q, k, v, g, LD, dK, dV, part_dk,
+            part_dv, H, G, lph, scale);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        // split rows and sources: their chunks summed in chunk order
+        const int cg = num_sms() * 4;
+        k_bwd_chunk_sum<<<cg, 256, 0, s>>>(indptr, rows.hdr, rows.longs, rows.chunk_edges, G * EE, part_dq, dQ,
+                                           nullptr, nullptr);
+        k_bwd_chunk_sum<<<cg, 256, 0, s>>>(colptr, cols.hdr, cols.longs, cols.chunk_edges, G * EE, part_dk, dK,
+                                           part_dv, dV);
         return cudaGetLastError();
     };
     using B = __nv_bfloat16;

@@ -51,7 +51,7 @@ namespace {
 constexpr int kTile = 128;              // rows per Q / K / V tile
 constexpr int kD = 64;                  // head width handled here
 constexpr uint32_t kTileBytes = kTile * kD * 2;   // 16 KB bf16
-constexpr long long kWaitCycles = kTcWaitCycles;
+constexpr long long kWaitCycles = kTcWaitCycles;   // drains (and the default bound of the other waits)
 
 
 // Non-blocking test (never suspends the thread).  The MMA warp issues it
@@ -213,6 +213,7 @@ struct WsBars {
                          // (MMA -> softmax g, waited at a rescale and the epilogue)
     uint64_t o_free[2];  // softmax g has read O_g in its epilogue (-> MMA), 4 arrivals
     uint64_t drain;
+    uint64_t stall;      // never completed: the softmax warps' first wait when a test asks for a stall
 };
 
 // Work item w -> (block row, block size, first query row, query tiles) and head.
@@ -274,7 +275,7 @@ template <typename TO>
 __global__ void __launch_bounds__(kThreadsWS, 1)
 k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ items, int n_work, int H,
-             TO* __restrict__ out, int HD, float sl2, int* __restrict__ err) {
+             TO* __restrict__ out, int HD, float sl2, int* __restrict__ err, long long wait_limit, int test_stall) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -315,6 +316,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             mbar_init(&bars.o_free[g], 4);
         }
         mbar_init(&bars.drain, 1);
+        mbar_init(&bars.stall, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     tc_fence_before();
@@ -339,13 +341,13 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 if (w + gridDim.x < n_work) it_next = item_of(items, w + gridDim.x, H, &h_next);
                 const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = n / kTile, xh = h * kD;
                 const int qb = local & 1;
-                if (local >= 2) ok = mbar_wait(&bars.q_empty[qb], ((local >> 1) - 1) & 1);
+                if (local >= 2) ok = mbar_wait(&bars.q_empty[qb], ((local >> 1) - 1) & 1, wait_limit);
                 if (!ok) break;
                 mbar_expect_tx(&bars.q_full[qb], nq * kTileBytes);
                 for (int g = 0; g < nq; ++g) tma_load_2d(sQ(qb, g), &tmQ, xh, q0 + g * kTile, &bars.q_full[qb]);
                 for (int j = 0; j < T; ++j, ++kv_tile) {
                     const int st = kv_tile % kStages;
-                    if (kv_tile >= kStages) ok = mbar_wait(&bars.kv_empty[st], ((kv_tile / kStages) - 1) & 1);
+                    if (kv_tile >= kStages) ok = mbar_wait(&bars.kv_empty[st], ((kv_tile / kStages) - 1) & 1, wait_limit);
                     if (!ok) break;
                     mbar_expect_tx(&bars.kv_full[st], 2 * kTileBytes);
                     tma_load_2d(sK(st), &tmK, xh, r0 + j * kTile, &bars.kv_full[st]);
@@ -417,7 +419,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 auto kv_wait = [&](int j, uint32_t probed) {
                     const int kt = kv_tile + j;
                     if (warp_any_ordered(probed)) return true;
-                    return mbar_wait_warp(&bars.kv_full[kt % kStages], (kt / kStages) & 1);
+                    return mbar_wait_warp(&bars.kv_full[kt % kStages], (kt / kStages) & 1, wait_limit);
                 };
                 auto p_probe = [&](int g) {
                     const int pc = g == 0 ? p_cnt0 : p_cnt1;
@@ -426,11 +428,12 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 // P_g(j) written (probe answer `probed`, else a blocking wait)
                 auto p_wait = [&](int g, uint32_t probed) {
                     int& pc = g == 0 ? p_cnt0 : p_cnt1;
-                    const bool r = warp_any_ordered(probed) || mbar_wait_warp(&bars.p[g][pc & 1], (pc >> 1) & 1);
+                    const bool r =
+                        warp_any_ordered(probed) || mbar_wait_warp(&bars.p[g][pc & 1], (pc >> 1) & 1, wait_limit);
                     ++pc;
                     return r;
                 };
-                ok = mbar_wait_warp(&bars.q_full[qb], (local >> 1) & 1);
+                ok = mbar_wait_warp(&bars.q_full[qb], (local >> 1) & 1, wait_limit);
                 if (!ok) break;
                 // S tiles ahead of the loop: A0 (B0) and A1
                 ok = kv_wait(0, 0u);
@@ -453,7 +456,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     // the first product of an item overwrites O_g: the previous
                     // item's epilogue must have read it
                     ok = p_wait(0, pa);
-                    if (ok && j == 0 && items0 > 0) ok = mbar_wait_warp(&bars.o_free[0], (items0 - 1) & 1);
+                    if (ok && j == 0 && items0 > 0) ok = mbar_wait_warp(&bars.o_free[0], (items0 - 1) & 1, wait_limit);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t pb = nq > 1 ? p_probe(1) : 0u;
@@ -471,7 +474,8 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     if (j + 2 < T) ok = kv_wait(j + 2, kv);
                     if (ok && nq > 1) {
                         ok = p_wait(1, pb);
-                        if (ok && j == 0 && items1 > 0) ok = mbar_wait_warp(&bars.o_free[1], (items1 - 1) & 1);
+                        if (ok && j == 0 && items1 > 0)
+                            ok = mbar_wait_warp(&bars.o_free[1], (items1 - 1) & 1, wait_limit);
                     }
                     if (!ok) break;
                     tc_fence_after();
@@ -522,9 +526,16 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         // whose S was issued after PV_g(n-2) (S_g(j) follows PV_g(j-2) in the
         // MMA order, and the S commit tracks every earlier MMA), so the
         // previous phase of barrier o[g][n & 1] has completed.
-        auto o_wait = [&](int n) { return mbar_wait(&bars.o[g][n & 1], (n >> 1) & 1); };
+        auto o_wait = [&](int n) { return mbar_wait(&bars.o[g][n & 1], (n >> 1) & 1, wait_limit); };
         int snum = 0;   // S tiles of the CTA's sequence before the current item (both query tiles)
         bool failed = false;
+        if (test_stall) {
+            // tests of the bounded-wait path: a wait on a barrier nothing
+            // completes runs out, the CTA is marked aborted, the other warps'
+            // waits for this warpgroup's P run out in turn and every role drains
+            if (!mbar_wait(&bars.stall, 0, wait_limit)) atomicExch(&s_abort, 1);
+            failed = true;
+        }
         int h_next = 0;
         int4 it_next = blockIdx.x < n_work ? item_of(items, blockIdx.x, H, &h_next) : make_int4(0, 0, 0, 0);
         for (int w = blockIdx.x; !failed && w < n_work; w += gridDim.x) {
@@ -540,7 +551,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 const uint32_t tS = tmem + col_buf((s0 + nq * j + g) % 3) + lane_base;
                 // a wait that runs out marks the CTA aborted; the warp leaves
                 // its loop (the decision is uniform over the warp)
-                const bool bad = !mbar_wait(&bars.s[g][s_cnt & 1], (s_cnt >> 1) & 1);
+                const bool bad = !mbar_wait(&bars.s[g][s_cnt & 1], (s_cnt >> 1) & 1, wait_limit);
                 ++s_cnt;
                 if (bad) atomicExch(&s_abort, 1);
                 if (__any_sync(0xffffffffu, bad || *reinterpret_cast<volatile int*>(&s_abort) != 0)) {
@@ -764,7 +775,8 @@ bool dense_supported(int H, int D, gtattn_dtype dt, const void* Q, const void* K
 
 gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void* Q, const void* K,
                            const void* V, void* out, int H, int D, float scale, gtattn_dtype dt, int* err,
-                           cudaStream_t s) {
+                           long long wait_cycles, int test_stall, cudaStream_t s) {
+    const long long wait_limit = wait_cycles > 0 ? wait_cycles : kWaitCycles;
     if (n_tiles <= 0) return GTATTN_OK;
     const int HD = H * D;
     CUtensorMap mq, mk, mv;
@@ -780,7 +792,8 @@ gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
         if (e == cudaSuccess) {
             k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, n_work, H,
-                                                     static_cast<__nv_bfloat16*>(out), HD, sl2, err);
+                                                     static_cast<__nv_bfloat16*>(out), HD, sl2, err, wait_limit,
+                                                     test_stall);
             e = cudaGetLastError();
         }
     } else {
@@ -789,7 +802,7 @@ gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
         if (e == cudaSuccess) {
             k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, n_work, H, static_cast<float*>(out), HD,
-                                                     sl2, err);
+                                                     sl2, err, wait_limit, test_stall);
             e = cudaGetLastError();
         }
     }

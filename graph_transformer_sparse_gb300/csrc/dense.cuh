@@ -14,9 +14,14 @@ bool dense_supported(int H, int D, gtattn_dtype dt, const void* Q, const void* K
 // persistent grid (one CTA per SM).  tiles: device array of work items
 // (first row of the block, block size, first row of the item's query rows,
 // number of 128-row query tiles (1 or 2)); block sizes are multiples of 128.
-// A bounded device wait that times out ORs an error code into *err.
+// A bounded device wait that times out ORs an error code into *err and the
+// CTA drains what it issued and returns.  wait_cycles bounds each wait for
+// data from another warp (SM clock cycles; <= 0: about one second); the
+// drains keep their own bound of about half a second.  test_stall != 0
+// (tests only): the softmax warps first wait on a barrier nothing completes,
+// so every CTA takes the timeout path.
 gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void* Q, const void* K,
                            const void* V, void* out, int H, int D, float scale, gtattn_dtype dt, int* err,
-                           cudaStream_t s);
+                           long long wait_cycles, int test_stall, cudaStream_t s);
 
 }  // namespace gt

@@ -432,6 +432,7 @@ extern "C" gtattn_status gtattn_plan_destroy(gtattn_plan* p) {
     cudaFree(p->dense_tiles);
     cudaFree(p->dense_flag);
     if (p->ws) cudaFree(p->ws);
+    if (p->bwd_pattern) cudaFree(p->bwd_pattern);
     if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
     delete p;
     return GTATTN_OK;
@@ -454,6 +455,10 @@ extern "C" gtattn_status gtattn_plan_get_info(const gtattn_plan* p, gtattn_plan_
     cudaError_t e = cudaMemcpy(&dev_err, p->hdr + HdrLayout::kErr, sizeof(int), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_status(e);
     info->device_error = dev_err;
+    if (dev_err != 0) {   // read and cleared: a later call's record starts empty
+        e = cudaMemset(p->hdr + HdrLayout::kErr, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_status(e);
+    }
     return GTATTN_OK;
 }
 

@@ -19,6 +19,7 @@ struct gtattn_plan {
     int* dense_flag = nullptr;              // 1 for rows inside a dense block
     mutable void* ws = nullptr;             // split-row partials workspace
     mutable size_t ws_bytes = 0;
+    mutable void* bwd_pattern = nullptr;    // source-major pattern and source binning (first backward)
 };
 
 namespace gt {

@@ -85,6 +85,15 @@ typedef struct {
     int32_t chunk_edges;    /* entries per chunk of a split row (default 256) */
     int32_t detect_dense;   /* 1: find complete blocks for the dense tensor-core path */
     int32_t kernel;         /* a gtattn_kernel value */
+    int32_t wait_cycles;    /* bound of each device-side wait of the dense-block
+                               kernel for another warp's data, in SM clock cycles
+                               (0: about one second).  A wait that runs out makes
+                               the kernel drain what it issued, record
+                               device_error and return. */
+    int32_t test_stall;     /* tests of that path only: 1 makes the dense-block
+                               kernel wait first on a barrier that nothing
+                               completes, so every wait runs out and the call's
+                               output is not valid */
 } gtattn_plan_opts;
 
 /* What a plan found (host copy). */
@@ -99,7 +108,9 @@ typedef struct {
     int32_t n_buckets;       /* entries of bucket_rows used */
     int32_t bucket_rows[64]; /* rows per degree bucket (bucket b < 33: degree b) */
     int32_t device_error;    /* nonzero if a bounded device wait of a forward
-                                call with this plan gave up (1: timeout) */
+                                call with this plan gave up since the last
+                                gtattn_plan_get_info (1: timeout; the output of
+                                that call is not valid) */
 } gtattn_plan_info;
 
 typedef struct gtattn_plan gtattn_plan;   /* opaque, library-owned */
@@ -131,8 +142,8 @@ gtattn_status gtattn_csr_build(const int32_t* indptr, const int32_t* indices, in
  * NULL is accepted. */
 gtattn_status gtattn_plan_destroy(gtattn_plan* plan);
 
-/* Copies the plan's counts to *info (host).  Reads the plan's device error
- * word, so it waits for work already queued that uses the plan. */
+/* Copies the plan's counts to *info (host).  Reads and clears the plan's
+ * device error word, so it waits for work already queued that uses the plan. */
 gtattn_status gtattn_plan_get_info(const gtattn_plan* plan, gtattn_plan_info* info);
 
 /*
@@ -269,16 +280,33 @@ gtattn_status gtattn_fwd_weighted(const int32_t* indptr, const int32_t* indices,
  *           is overwritten (rows without entries get zeros).
  *   H <= 128.  Other arguments: as gtattn_fwd.  Asynchronous on `stream`;
  *   the temporaries (the forward's fp32 output and log-sum-exp, a
- *   source-major copy of the pattern: about 4 N H D + 12 N H + 8 N + 4 nnz
- *   bytes plus the binnings) come from the library's stream-ordered pool.
+ *   source-major copy of the pattern, the split rows' and sources' partial
+ *   sums: about 4 N H D + 12 N H + 12 N + 8 nnz bytes plus the binnings and
+ *   the partials) come from the library's stream-ordered pool.
  *   indices must lie in [0, N), as for gtattn_fwd (csr_validate checks).
- * dK and dV are summed per source over its entries in an order set by
- * atomic slot claims, and split rows and sources add their chunks with fp32
- * atomics, so the last bits are not deterministic run to run.
+ * Deterministic: the source-major copy lists each source's destination rows
+ * in ascending order, every row and source is summed in one fixed order,
+ * and the chunks of split rows and sources are added in chunk order, so two
+ * calls on the same inputs give the same bits (shapes whose H*D the two
+ * passes do not tile -- see below -- fall back to a warp per row with fp32
+ * atomics, which is not deterministic).
  */
 gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
                          const void* V, const void* dO, float* dQ, float* dK, float* dV, int64_t N,
                          int64_t nnz, int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
+
+/*
+ * gtattn_bwd_plan -- gtattn_bwd with a prebuilt plan, for training on a
+ * fixed graph: the plan's destination binning is used as it stands, and the
+ * source-major copy of the pattern with its binning is built by the first
+ * backward call with the plan and kept in it (about 8 N + 4 nnz bytes plus
+ * the binning, freed by gtattn_plan_destroy), so later calls skip it.  Same
+ * results, bit for bit, as gtattn_bwd.  indptr/indices must be the arrays
+ * the plan was built from.  One plan must not be used by concurrent calls.
+ */
+gtattn_status gtattn_bwd_plan(const gtattn_plan* plan, const int32_t* indptr, const int32_t* indices,
+                              const void* Q, const void* K, const void* V, const void* dO, float* dQ, float* dK,
+                              float* dV, int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
 
 /*
  * gtattn_fwd_noalloc -- gtattn_fwd without any allocation.  The pages have

@@ -86,6 +86,8 @@ def test_host_argument_checks_bias_weighted_bwd_ndh(lib):
     assert fg(16, 16, 16, None, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV       # null K, nnz > 0
     assert fg(None, 16, 16, 16, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV       # null indptr
     assert fg(16, None, None, None, None, None, None, None, None, 0, 0, 2, 8, 1.0, 0, None) == OK   # N = 0
+    fp = lib.gtattn_bwd_plan   # plan indptr indices Q K V dO dQ dK dV H D scale dtype stream
+    assert fp(None, 16, 16, 16, 16, 16, 16, 16, 16, 16, 2, 8, 1.0, 0, None) == INV                 # null plan
     fn = lib.gtattn_fwd_ndh   # indptr indices Q K V out N nnz H D scale dtype stream
     assert fn(None, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV                   # null indptr
     assert fn(16, 16, 16, 16, 16, 16, 4, 4, 2, 1000, 1.0, 0, None) == INV                  # H*D > 1024

@@ -481,3 +481,27 @@ def test_wide_logit_range_raises_running_max(dtype):
         check_out(w, got, ref["out"], f"wide logits {path}", out32=True)
         if path == "probs":
             assert_close(pr, ref["probs"], w.dtype, "probs", PROB_TOL)
+
+
+def test_dense_wait_timeout_is_reported_and_a_later_call_is_correct():
+    # The plan's test hook makes the dense-block kernel's softmax warps wait
+    # first on a barrier nothing completes, with every wait for another
+    # warp's data bounded by 2000 SM cycles: that wait runs out, the MMA
+    # warp's waits for P and the TMA warp's waits for free stages run out in
+    # turn, each CTA drains the copies and products it issued (those waits
+    # keep their own half-second bound), frees its tensor memory and returns.
+    # The call returns, the plan reports the timeout once (the record is
+    # cleared when read), and the context stays usable: a plan without the
+    # hook then gives the oracle's result.
+    w = small("dense_blocks")
+    d = to_device(w, out32=True)
+    plan = gt.Plan(d["indptr"], d["indices"], detect_dense=True, wait_cycles=2000, test_stall=True)
+    assert plan.info()["n_dense_blocks"] > 0
+    gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], w.H, w.D, w.scale,
+                       _dt(d))
+    torch.cuda.synchronize()
+    assert plan.info()["device_error"] == 1
+    assert plan.info()["device_error"] == 0
+    plan.close()
+    got, _, _ = run(w, d, "plan", detect_dense=True)
+    check_out(w, got, oracle_rows(w)["out"], "dense after a timeout", out32=True)

@@ -434,6 +434,7 @@ k_csc_scatter(const int* __restrict__ indptr, const int* __restrict__ indices, c
 constexpr int kSortThreads = 256;
 constexpr int kSortMid = 2048;      // segments a block sorts in static shared memory
 constexpr int kSortRun = 32768;     // runs a block sorts in dynamic shared memory (128 KB)
+constexpr int kSortBigThreads = 1024;   // threads of the blocks sorting those
 
 // Bitonic sort of the warp's 32*R values, value index x = r*32 + lane.
 template <int R>
@@ -495,13 +496,15 @@ __device__ __forceinline__ int merge_split(const int* a, int na, const int* b, i
     return lo;
 }
 
-// Bitonic sort of buf[0, p2) (p2 a power of two) by the block.
+// Bitonic sort of buf[0, p2) (p2 a power of two) by the block's THREADS threads.
+template <int THREADS>
 __device__ __forceinline__ void block_bitonic(int* buf, int p2) {
     for (int k = 2; k <= p2; k <<= 1) {
         for (int m = k >> 1; m > 0; m >>= 1) {
-            for (int i = threadIdx.x; i < p2 / 2; i += kSortThreads) {
+            const int lm = __ffs(m) - 1;   // m = 2^lm
+            for (int i = threadIdx.x; i < p2 / 2; i += THREADS) {
                 // the i-th pair of this step: lower index x, partner x + m
-                const int x = (i / m) * 2 * m + (i % m);
+                const int x = ((i >> lm) << (lm + 1)) + (i & (m - 1));
                 const int a = buf[x], b = buf[x + m];
                 const bool up = (x & k) == 0;
                 if ((a > b) == up) {
@@ -528,8 +531,8 @@ __device__ __forceinline__ int2 bucket_span(const int* hdr, int lo, int hi) {
 // its row list's buckets in that degree range; runs of RUN values sorted in
 // shared memory (static for RUN <= kSortMid, else dynamic), merged pairwise
 // through tmp when the segment is longer than one run.
-template <int RUN>
-__global__ void __launch_bounds__(kSortThreads)
+template <int RUN, int THREADS>
+__global__ void __launch_bounds__(THREADS)
 k_seg_sort_block(const int* __restrict__ colptr, const int* __restrict__ hdr, const int* __restrict__ cols,
                  const int2* __restrict__ longs, int lo, int hi, int* __restrict__ rowid, int* __restrict__ tmp) {
     extern __shared__ int dyn[];
@@ -546,10 +549,10 @@ k_seg_sort_block(const int* __restrict__ colptr, const int* __restrict__ hdr, co
             const int n = min(RUN, len - r0);
             int p2 = 64;
             while (p2 < n) p2 <<= 1;
-            for (int i = threadIdx.x; i < p2; i += kSortThreads) buf[i] = i < n ? rowid[beg + r0 + i] : 0x7fffffff;
+            for (int i = threadIdx.x; i < p2; i += THREADS) buf[i] = i < n ? rowid[beg + r0 + i] : 0x7fffffff;
             __syncthreads();
-            block_bitonic(buf, p2);
-            for (int i = threadIdx.x; i < n; i += kSortThreads) rowid[beg + r0 + i] = buf[i];
+            block_bitonic<THREADS>(buf, p2);
+            for (int i = threadIdx.x; i < n; i += THREADS) rowid[beg + r0 + i] = buf[i];
             __syncthreads();
         }
         // merge runs pairwise: width w -> 2w, alternating rowid and tmp
@@ -561,7 +564,7 @@ k_seg_sort_block(const int* __restrict__ colptr, const int* __restrict__ hdr, co
                 const int tot = na + nb;
                 const int* A = src + a0;
                 const int* B = A + na;
-                const int per = (tot + kSortThreads - 1) / kSortThreads;
+                const int per = (tot + THREADS - 1) / THREADS;
                 const int d0 = min(tot, static_cast<int>(threadIdx.x) * per), d1 = min(tot, d0 + per);
                 int ia = merge_split(A, na, B, nb, d0);
                 int ib = d0 - ia;
@@ -576,7 +579,7 @@ k_seg_sort_block(const int* __restrict__ colptr, const int* __restrict__ hdr, co
             dst = t;
         }
         if (src != rowid + beg)   // the last merge landed in tmp
-            for (int i = threadIdx.x; i < len; i += kSortThreads) rowid[beg + i] = src[i];
+            for (int i = threadIdx.x; i < len; i += THREADS) rowid[beg + i] = src[i];
         __syncthreads();
     }
 }
@@ -909,8 +912,9 @@ gtattn_status build_csc(const int* indptr, const int* indices, const TaskLists& 
         const int wg = static_cast<int>(std::min<int64_t>((N + 7) / 8, static_cast<int64_t>(num_sms()) * 16));
         k_seg_sort_warp<1><<<wg, 256, 0, s>>>(colptr, N, 1, rowid);
         k_seg_sort_warp<8><<<wg, 256, 0, s>>>(colptr, N, 32, rowid);
-        k_seg_sort_block<kSortMid><<<num_sms() * 8, kSortThreads, 0, s>>>(colptr, C.hdr, C.rows, C.longs, 256,
-                                                                          kSortMid, rowid, tmp);
+        k_seg_sort_block<kSortMid, kSortThreads><<<num_sms() * 8, kSortThreads, 0, s>>>(colptr, C.hdr, C.rows,
+                                                                                        C.longs, 256, kSortMid,
+                                                                                        rowid, tmp);
         GT_CUDA(cudaGetLastError());
         static std::mutex mu;
         static bool set[64] = {};
@@ -919,12 +923,13 @@ gtattn_status build_csc(const int* indptr, const int* indices, const TaskLists& 
         {
             std::lock_guard<std::mutex> g(mu);
             if (dev < 0 || dev >= 64 || !set[dev]) {
-                GT_CUDA(cudaFuncSetAttribute(k_seg_sort_block<kSortRun>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                GT_CUDA(cudaFuncSetAttribute(k_seg_sort_block<kSortRun, kSortBigThreads>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(sizeof(int) * kSortRun)));
                 if (dev >= 0 && dev < 64) set[dev] = true;
             }
         }
-        k_seg_sort_block<kSortRun><<<num_sms(), kSortThreads, sizeof(int) * kSortRun, s>>>(
+        k_seg_sort_block<kSortRun, kSortBigThreads><<<num_sms(), kSortBigThreads, sizeof(int) * kSortRun, s>>>(
             colptr, C.hdr, C.rows, C.longs, kSortMid, 0, rowid, tmp);
         GT_CUDA(cudaGetLastError());
     }

@@ -18,7 +18,7 @@ constexpr int kExactBuckets = 33;
 constexpr int kLogBuckets = 15;
 constexpr int kNumBuckets = kExactBuckets + kLogBuckets;   // 48
 constexpr int kMaxHD = 1024;
-constexpr int kDenseTile = 128;   // dense blocks: size multiple of this
+constexpr int kDenseTile = 128;   // dense blocks: tiles of this many rows (blocks of at least one)
 
 // upper bounds (inclusive) of the log buckets
 __host__ __device__ inline int log_bucket_hi(int k) {

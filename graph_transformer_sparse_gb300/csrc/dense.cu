@@ -339,7 +339,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 const int h = h_next;
                 const int4 it = it_next;   // the next item's entry is loaded one item ahead
                 if (w + gridDim.x < n_work) it_next = item_of(items, w + gridDim.x, H, &h_next);
-                const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = n / kTile, xh = h * kD;
+                const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = (n + kTile - 1) / kTile, xh = h * kD;
                 const int qb = local & 1;
                 if (local >= 2) ok = mbar_wait(&bars.q_empty[qb], ((local >> 1) - 1) & 1, wait_limit);
                 if (!ok) break;
@@ -397,7 +397,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             for (int w = blockIdx.x; ok && w < n_work; w += gridDim.x, ++local) {
                 int h;
                 const int4 it = item_of(items, w, H, &h);
-                const int nq = it.w, T = it.y / kTile;
+                const int nq = it.w, T = (it.y + kTile - 1) / kTile;
                 const int qb = local & 1;
                 const int s0 = snum;   // S number of (g, j) = s0 + nq*j + g
                 auto bufk = [&](int g, int j) { return (s0 + nq * j + g) % 3; };
@@ -542,7 +542,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             const int h = h_next;
             const int4 it = it_next;   // the next item's entry is loaded one item ahead
             if (w + gridDim.x < n_work) it_next = item_of(items, w + gridDim.x, H, &h_next);
-            const int n = it.y, q0 = it.z, nq = it.w, T = n / kTile, xh = h * kD;
+            const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = (n + kTile - 1) / kTile, xh = h * kD;
             const int s0 = snum;
             snum += nq * T;
             if (g >= nq) continue;
@@ -565,6 +565,16 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, r + 32 * c);
                 tmem_ld_wait();
+                // a block of n keys ends inside its last key tile: the columns
+                // past it (another block's keys) become -inf logits (+inf for a
+                // negative scale), so their P is 0 and they never set the maximum
+                const int n_last = n - (T - 1) * kTile;
+                if (j == T - 1 && n_last < kTile) {
+                    const uint32_t masked = __float_as_uint(pos ? -INFINITY : INFINITY);
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= n_last) r[c] = masked;
+                }
                 // the row's largest t = s*scale*log2e over the tile (from its
                 // largest s for a positive scale, its smallest for a negative one)
                 auto tile_top = [&]() {
@@ -680,8 +690,12 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             if (lane == 0) mbar_arrive(&bars.o_free[g]);
             const float inv = 1.f / (l0 + l1);
             // rows of this lane's quad after each transpose: quad base + k
-            TO* op = out + static_cast<int64_t>(q0 + g * kTile + (row & ~3)) * HD + xh;
+            // (rows past the block's end, in a ragged last query tile, are
+            // computed but not stored)
+            const int qrow = q0 + g * kTile + (row & ~3);
+            TO* op = out + static_cast<int64_t>(qrow) * HD + xh;
             const int ql = lane & 3;
+            const int rows_left = r0 + n - qrow;   // rows k < rows_left of the quad are the block's
             if constexpr (sizeof(TO) == 2) {
 #pragma unroll
                 for (int gg = 0; gg < 2; ++gg) {   // 16-byte chunks 4gg..4gg+3 (columns 32gg..32gg+31)
@@ -698,7 +712,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     quad_transpose(c, lane);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD)[4 * gg + ql] = c[k];
+                        if (k < rows_left) reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD)[4 * gg + ql] = c[k];
                 }
             } else {
 #pragma unroll
@@ -715,7 +729,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     quad_transpose(c, lane);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD)[4 * gg + ql] = c[k];
+                        if (k < rows_left) reinterpret_cast<uint4*>(op + static_cast<int64_t>(k) * HD)[4 * gg + ql] = c[k];
                 }
             }
         }

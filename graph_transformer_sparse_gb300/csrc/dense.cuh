@@ -13,7 +13,8 @@ bool dense_supported(int H, int D, gtattn_dtype dt, const void* Q, const void* K
 // out = softmax(scale * Q K^T) V per head over complete blocks on a
 // persistent grid (one CTA per SM).  tiles: device array of work items
 // (first row of the block, block size, first row of the item's query rows,
-// number of 128-row query tiles (1 or 2)); block sizes are multiples of 128.
+// number of 128-row query tiles (1 or 2)); blocks of at least 128 rows, a
+// ragged last tile masked.
 // A bounded device wait that times out ORs an error code into *err and the
 // CTA drains what it issued and returns.  wait_cycles bounds each wait for
 // data from another warp (SM clock cycles; <= 0: about one second); the

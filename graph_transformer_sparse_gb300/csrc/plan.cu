@@ -222,8 +222,8 @@ static_assert(HdrLayout::kCurDense == HdrLayout::kCursor + kNumBuckets + 2, "cur
 
 // ---------------------------------------------------------------------------
 // dense-block detection: a block is rows r0..r0+n-1 whose entries are exactly
-// r0, r0+1, ..., r0+n-1 (a complete graph with self-loops, sorted), n a
-// multiple of kDenseTile.
+// r0, r0+1, ..., r0+n-1 (a complete graph with self-loops, sorted), n at
+// least kDenseTile (the kernel masks a ragged last tile).
 // ---------------------------------------------------------------------------
 __global__ void k_dense_candidates(const int* __restrict__ indptr, const int* __restrict__ indices,
                                    int N, int* __restrict__ cand) {
@@ -232,7 +232,7 @@ __global__ void k_dense_candidates(const int* __restrict__ indptr, const int* __
     for (int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < N; i += warps) {
         int beg = indptr[i], deg = indptr[i + 1] - beg;
         int first = -1;
-        if (deg >= kDenseTile && deg % kDenseTile == 0) {
+        if (deg >= kDenseTile) {
             int f = indices[beg];
             bool ok = (i >= f) && (i < f + deg);
             for (int k = lane; ok && k < deg; k += 32) ok = indices[beg + k] == f + k;
@@ -407,7 +407,7 @@ extern "C" gtattn_status gtattn_csr_build(const int32_t* indptr, const int32_t* 
         std::vector<int4> tiles;
         for (const int2& b : hb)
             for (int q0 = b.x; q0 < b.x + b.y; q0 += 2 * kDenseTile)
-                tiles.push_back(make_int4(b.x, b.y, q0, std::min(2, (b.x + b.y - q0) / kDenseTile)));
+                tiles.push_back(make_int4(b.x, b.y, q0, std::min(2, (b.x + b.y - q0 + kDenseTile - 1) / kDenseTile)));
         if ((st = chk(cudaMalloc(&p->dense_tiles, sizeof(int4) * tiles.size()))) != GTATTN_OK) return fail(st);
         if ((st = chk(cudaMemcpy(p->dense_tiles, tiles.data(), sizeof(int4) * tiles.size(),
                                  cudaMemcpyHostToDevice))) != GTATTN_OK)

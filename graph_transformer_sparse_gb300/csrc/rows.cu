@@ -66,6 +66,12 @@ __device__ __forceinline__ int ld_index(const int* p) {
     else return __ldg(p);
 }
 
+// Programmatic dependent launch: the row and combine kernels are launched
+// while the kernel before them in the stream (binning, rows) is still
+// running, and wait here until it has finished and its writes are visible
+// (a no-op for a launch without the attribute).
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Builds the task table of a launch in shared memory (one warp).
 // P = edge slots per warp; U = edges per slot per loop iteration.
 __device__ void build_segments(const TaskLists& L, int P, int U, Seg* segs, int* nseg, int* total,
@@ -216,6 +222,7 @@ constexpr int kExtBias = 1, kExtValues = 2;
 template <typename T, typename TO, int VPL, int MODE, int EXT = 0>
 __global__ void __launch_bounds__(kRowThreads, rows_min_blocks<T, VPL>())
 k_rows_vec(RowParams p) {
+    wait_prior_grid();
     constexpr bool BIAS = (EXT & kExtBias) != 0;
     constexpr bool VALS = (EXT & kExtValues) != 0;
     using F = Frag<T, VPL>;
@@ -532,6 +539,7 @@ constexpr int kGenMaxH = 256;
 template <typename T, typename TO, int MODE, int KPL>
 __global__ void __launch_bounds__(kGenWarps * 32)
 k_rows_generic(RowParams p) {
+    wait_prior_grid();
     __shared__ Seg segs[kMaxSegs];
     __shared__ int s_nseg, s_total;
     __shared__ float sm_prod[kGenWarps][KPL * 32];
@@ -689,6 +697,7 @@ constexpr int kCombThreads = 512;
 template <typename TO, int MODE>
 __global__ void __launch_bounds__(kCombThreads)
 k_combine(RowParams p, int warp_rows) {
+    wait_prior_grid();
     __shared__ float sM[kGenMaxH];
     __shared__ float sS[kGenMaxH];
     __shared__ float red[kCombThreads];
@@ -1115,6 +1124,23 @@ static int grid_persistent(K kernel, int threads, size_t smem) {
     return grid;
 }
 
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel of the stream finishes (it waits in wait_prior_grid).
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern kernel, int grid, int threads, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // The persistent grid, but no more blocks than the tasks can occupy (small
 // graphs: a few blocks instead of several per SM).
 static int grid_for_tasks(int persistent, int task_bound, int warps_per_block) {
@@ -1127,8 +1153,7 @@ template <typename T, typename TO, int MODE, int EXT = 0>
 static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
     auto go = [&](auto kernel) {
         const int grid = grid_for_tasks(grid_persistent(kernel, kRowThreads, 0), p.task_bound, kRowThreads / 32);
-        kernel<<<grid, kRowThreads, 0, s>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(kernel, grid, kRowThreads, 0, s, p);
     };
     cudaError_t e;
     switch (vpl) {
@@ -1162,8 +1187,7 @@ static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParam
     }
     auto go = [&](auto kernel) {
         const int grid = grid_for_tasks(grid_persistent(kernel, kGenWarps * 32, 0), p.task_bound, kGenWarps);
-        kernel<<<grid, kGenWarps * 32, 0, s>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(kernel, grid, kGenWarps * 32, 0, s, p);
     };
     auto by_kpl = [&](auto kpl4, auto kpl8, auto kpl32) {
         const int kpl = (p.HD + 31) / 32;
@@ -1201,8 +1225,7 @@ gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cud
     // rows of few chunks a warp each (when H divides 32), the others a block each
     const int warp_rows = (32 % p.H == 0) ? 1 : 0;
     auto go = [&](auto kernel) {
-        kernel<<<grid_persistent(kernel, kCombThreads, 0), kCombThreads, 0, s>>>(p, warp_rows);
-        return cudaGetLastError();
+        return launch_pdl(kernel, grid_persistent(kernel, kCombThreads, 0), kCombThreads, 0, s, p, warp_rows);
     };
     cudaError_t e;
     if (dt == GTATTN_BF16)

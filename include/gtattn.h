@@ -125,7 +125,7 @@ const char* gtattn_last_error(void);
  * gtattn_csr_build -- degree binning of a CSR graph (the plan).
  * Sorts rows into degree buckets, lists split chunks for long rows and, with
  * opts->detect_dense, finds complete blocks (rows r0..r0+n-1 whose entries are
- * exactly r0..r0+n-1 in order, n a multiple of 128).  Binning is this
+ * exactly r0..r0+n-1 in order, n >= 128).  Binning is this
  * library's design; the pages define only the operation.
  *   indptr, indices: device CSR as above (not copied: the same arrays must be
  *   passed to the forward calls that use the plan).

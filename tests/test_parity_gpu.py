@@ -8,6 +8,7 @@ full-size workloads are compared on sampled rows (hub rows included).
 import numpy as np
 import pytest
 
+import oracle
 import workloads as wl
 from gpu_helpers import (PROB_TOL, TOL, assert_close, oracle_rows, out_to_numpy, sample_rows,
                          to_device)
@@ -405,6 +406,37 @@ def test_dense_path_mixed_graph(out32):
     plan.close()
     got = out_to_numpy(d["out"])
     check_out(w, got, ref, f"mixed dense+sparse out32={out32}", out32=out32)
+
+
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_dense_path_ragged_blocks(sign):
+    # complete blocks whose sizes are not multiples of the 128-row tile: the
+    # last key tile of each is masked (a negative scale flips the mask's
+    # sign), rows past a block's end in its last query tile are not stored
+    rng = np.random.default_rng(78)
+    sizes = [200, 128, 300, 511, 129]
+    src, dst, n = _mixed_dense_graph(rng, sizes, 400, 5000)
+    ip, ix = wl.csr_by_destination(src, dst, n)
+    Q, K, V = (0.5 * rng.standard_normal((n, 8, 64)) for _ in range(3))
+    w = _mk(ip, ix, Q, K, V, "bf16")
+    scale = sign * w.scale
+    ref = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, scale, threads=8)["out"]
+    for out32 in (True, False):
+        d = to_device(w, out32=out32)
+        plan = gt.Plan(d["indptr"], d["indices"], detect_dense=True)
+        info = plan.info()
+        assert info["n_dense_blocks"] == len(sizes) and info["n_dense_rows"] == sum(sizes)
+        gt.gtattn_profile_enable(True)
+        gt.gtattn_profile_read(reset=True)
+        d["out"].fill_(float("nan"))
+        gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], 8, 64, scale, _dt(d))
+        torch.cuda.synchronize()
+        prof = gt.gtattn_profile_read(reset=True)
+        gt.gtattn_profile_enable(False)
+        assert prof["dense"]["launches"] == 1, prof
+        assert plan.info()["device_error"] == 0
+        plan.close()
+        check_out(w, out_to_numpy(d["out"]), ref, f"ragged dense blocks sign={sign} out32={out32}", out32=out32)
 
 
 def test_dense_path_large_scores():

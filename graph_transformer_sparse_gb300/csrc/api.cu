@@ -253,6 +253,39 @@ static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, co
     if (N == 0) return GTATTN_OK;
     gtattn_plan_opts o;
     resolve_opts(nullptr, &o);
+    {
+        // small graphs: one cooperative launch that bins in shared memory and
+        // combines split rows itself (no binning or combine launches)
+        int64_t nl = 0, nc = 0;
+        worst_case_sizes(N, nnz, o.long_row_min, o.chunk_edges, &nl, &nc);
+        if (N <= kSmallMaxRows && nnz <= kSmallMaxNnz && nc <= kSmallMaxChunks && nl <= kSmallMaxLong) {
+            const int HD = H * D;
+            void* part_buf = nullptr;
+            Partials part{};
+            if (nnz > o.long_row_min) {   // a row may be split: its chunks' partials
+                const size_t a = align_up(sizeof(float) * static_cast<size_t>(nc) * H);
+                GT_TRY(pool_alloc(&part_buf, 2 * a + sizeof(float) * static_cast<size_t>(nc) * HD, stream));
+                char* b = static_cast<char*>(part_buf);
+                part = Partials{reinterpret_cast<float*>(b), reinterpret_cast<float*>(b + a),
+                                reinterpret_cast<float*>(b + 2 * a)};
+            }
+            TaskLists none{nullptr, nullptr, nullptr, nullptr, o.chunk_edges, 1};
+            RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale * kLog2e, c, none, part);
+            p.bias = bias;
+            p.values = values;
+            p.ndh = ndh;
+            p.long_min = o.long_row_min;
+            p.small_max_chunks = kSmallMaxChunks;
+            p.small_max_long = kSmallMaxLong;
+            gtattn_status st;
+            {
+                ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+                st = launch_rows_small(dtype, c, p, stream);
+            }
+            pool_free(part_buf, stream);
+            return st;
+        }
+    }
     Scratch sc;
     int *hdr, *rows;
     int2 *chunks, *longs;

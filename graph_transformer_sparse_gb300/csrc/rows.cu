@@ -25,6 +25,8 @@
 // out = sum acc_c 2^(m_c-m*) / s*.
 #include "rows.cuh"
 
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <mutex>
 #include <unordered_map>
@@ -47,6 +49,7 @@ struct Seg {
 };
 
 constexpr int kMaxSegs = kNumBuckets + 2;
+constexpr int kRowBlockMax = 256;   // threads a row-kernel block has at most
 constexpr float kLazyMax = 8.f;   // fused row kernel: slack of the running maximum (log2 units)
 
 // Head of feature element el of a node row: [N, H, D] rows are head-major
@@ -112,6 +115,105 @@ __device__ void build_segments(const TaskLists& L, int P, int U, Seg* segs, int*
         *total = t;
     }
     __syncthreads();
+}
+
+// Block-wide exclusive scan of two counts (every thread of the block calls
+// it); *tot_a / *tot_b receive the block's totals.
+__device__ __forceinline__ int2 block_scan2(int a, int b, int* tot_a, int* tot_b) {
+    __shared__ int wa[kRowBlockMax / 32], wb[kRowBlockMax / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = a, y = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int xo = __shfl_up_sync(0xffffffffu, x, o), yo = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) { x += xo; y += yo; }
+    }
+    if (lane == 31) { wa[wid] = x; wb[wid] = y; }
+    __syncthreads();
+    int pa = 0, pb = 0, ta = 0, tb = 0;
+    for (int k = 0; k < nw; ++k) {
+        if (k < wid) { pa += wa[k]; pb += wb[k]; }
+        ta += wa[k];
+        tb += wb[k];
+    }
+    *tot_a = ta;
+    *tot_b = tb;
+    __syncthreads();   // wa / wb are reused by the next call
+    return make_int2(pa + x - a, pb + y - b);
+}
+
+// The one-launch path for small graphs: the block's own binning, the same in
+// every block.  A first coalesced walk over indptr finds whether any row is
+// split (more than long_min entries); only then are the split rows and
+// their chunks listed, in row order (rounds of blockDim rows, offsets by
+// block scans), into s_longs / s_chunks (counts in s_counts[0..1]).  The
+// task table: the chunks, then every row of the graph, R = P rows a task
+// with one slot each (a split row is skipped there).
+__device__ void build_segments_small(const RowParams& p, int P, Seg* segs, int* nseg, int* total, int2* s_chunks,
+                                     int2* s_longs, int* s_counts) {
+    const int N = p.N, nt = blockDim.x, chunk = p.lists.chunk_edges;
+    auto split = [&](int deg) { return deg > 0 && deg > p.long_min; };
+    int any = 0;
+    for (int i = threadIdx.x; i < N; i += nt) any |= split(p.indptr[i + 1] - p.indptr[i]);
+    any = __syncthreads_or(any);
+    int n_long = 0, n_chunks = 0;
+    if (any) {
+        for (int r0 = 0; r0 < N; r0 += nt) {
+            const int i = r0 + threadIdx.x;
+            const int beg = i < N ? p.indptr[i] : 0;
+            const int deg = i < N ? p.indptr[i + 1] - beg : 0;
+            const bool sp = split(deg);
+            const int nch = sp ? (deg + chunk - 1) / chunk : 0;
+            int tl, tc;
+            const int2 ex = block_scan2(sp ? 1 : 0, nch, &tl, &tc);
+            if (sp) {
+                const int c0 = n_chunks + ex.y;
+                s_longs[n_long + ex.x] = make_int2(i, c0);
+                for (int c = 0; c < nch; ++c) s_chunks[c0 + c] = make_int2(i, beg + c * chunk);
+            }
+            n_long += tl;
+            n_chunks += tc;
+        }
+    }
+    if (threadIdx.x == 0) {
+        s_counts[0] = n_long;
+        s_counts[1] = n_chunks;
+        int t = 0, k = 0;
+        if (n_chunks > 0) { segs[k++] = Seg{t, 0, n_chunks, 1, P, kSegChunk}; t += n_chunks; }
+        segs[k++] = Seg{t, 0, N, P, 1, kSegRows};
+        t += (N + P - 1) / P;
+        *nseg = k;
+        *total = t;
+    }
+    __syncthreads();
+}
+
+// After the grid-wide sync of the one-launch path: a warp per split row
+// merges its chunks' (m, s, acc) partials in chunk order into the output.
+template <typename TO>
+__device__ void small_combine(const RowParams& p, const int2* longs, int n_long) {
+    const int lane = threadIdx.x & 31;
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    const int H = p.H, D = p.D, HD = p.HD, chunk = p.lists.chunk_edges;
+    TO* O = static_cast<TO*>(p.out);
+    for (int li = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); li < n_long; li += nw) {
+        const int row = longs[li].x, c0 = longs[li].y;
+        const int nch = (p.indptr[row + 1] - p.indptr[row] + chunk - 1) / chunk;
+        for (int el = lane; el < HD; el += 32) {
+            const int h = p.ndh ? el % H : el / D;
+            float M = -INFINITY;
+            for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part.m[static_cast<int64_t>(c0 + c) * H + h]);
+            const float Mr = M == -INFINITY ? 0.f : M;   // no finite logit in the row: a zero row
+            float S = 0.f, v = 0.f;
+            for (int c = 0; c < nch; ++c) {
+                const int64_t k = static_cast<int64_t>(c0 + c) * H + h;
+                const float w = ex2(p.part.m[k] - Mr);
+                S += p.part.s[k] * w;
+                v += p.part.acc[static_cast<int64_t>(c0 + c) * HD + el] * w;
+            }
+            store_elem(O, static_cast<int64_t>(row) * HD + el, S > 0.f ? v / S : 0.f);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -219,9 +321,10 @@ constexpr int rows_min_blocks() {
 // added; kExtValues -- the dot products are multiplied by p.values[e] (the
 // weighted adjacency's stored values).
 constexpr int kExtBias = 1, kExtValues = 2;
-template <typename T, typename TO, int VPL, int MODE, int EXT = 0>
+template <typename T, typename TO, int VPL, int MODE, int EXT = 0, bool SMALL = false>
 __global__ void __launch_bounds__(kRowThreads, rows_min_blocks<T, VPL>())
 k_rows_vec(RowParams p) {
+    static_assert(!SMALL || MODE == kFused, "the one-launch path is the fused forward");
     wait_prior_grid();
     constexpr bool BIAS = (EXT & kExtBias) != 0;
     constexpr bool VALS = (EXT & kExtValues) != 0;
@@ -231,9 +334,19 @@ k_rows_vec(RowParams p) {
 
     __shared__ Seg segs[kMaxSegs];
     __shared__ int s_nseg, s_total;
+    __shared__ int s_small[2];            // one-launch path: split rows, chunks
+    extern __shared__ int2 small_lists[];   // one-launch path: chunks, then split rows
     const int G = p.G;
     const int P = 32 / G;
-    build_segments(p.lists, P, U, segs, &s_nseg, &s_total, MODE == kFused);
+    TaskLists L = p.lists;
+    if constexpr (SMALL) {
+        L.chunks = small_lists;
+        L.longs = small_lists + p.small_max_chunks;
+        build_segments_small(p, P, segs, &s_nseg, &s_total, small_lists, small_lists + p.small_max_chunks,
+                             s_small);
+    } else {
+        build_segments(p.lists, P, U, segs, &s_nseg, &s_total, MODE == kFused);
+    }
 
     const int lane = threadIdx.x & 31;
     const int grp = lane / G;
@@ -263,14 +376,22 @@ k_rows_vec(RowParams p) {
         if (m.valid) {
             if (sg.kind == kSegChunk) {
                 m.chunk = sg.list_begin + pos;
-                const int2 c = p.lists.chunks[m.chunk];
+                const int2 c = L.chunks[m.chunk];
                 m.row = c.x;
                 m.beg = c.y;
-                m.end = min(m.beg + p.lists.chunk_edges, p.indptr[m.row + 1]);
+                m.end = min(m.beg + L.chunk_edges, p.indptr[m.row + 1]);
             } else {
-                m.row = p.lists.rows[sg.list_begin + pos];
-                m.beg = p.indptr[m.row];
-                m.end = p.indptr[m.row + 1];
+                if constexpr (SMALL) {
+                    m.row = sg.list_begin + pos;   // every row, in index order
+                    m.beg = p.indptr[m.row];
+                    m.end = p.indptr[m.row + 1];
+                    // a split row is walked by its chunks
+                    if (m.end - m.beg > 0 && m.end - m.beg > p.long_min) m.valid = false;
+                } else {
+                    m.row = L.rows[sg.list_begin + pos];
+                    m.beg = p.indptr[m.row];
+                    m.end = p.indptr[m.row + 1];
+                }
             }
         }
     };
@@ -524,6 +645,14 @@ k_rows_vec(RowParams p) {
         }
         }   // MODE != kSddmm
     }
+    if constexpr (SMALL) {
+        if (s_small[0] > 0) {   // uniform over the grid
+            // split rows: every chunk's partial is written once the whole
+            // (cooperatively launched) grid arrives here
+            cooperative_groups::this_grid().sync();
+            small_combine<TO>(p, L.longs, s_small[0]);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -536,9 +665,10 @@ constexpr int kGenMaxH = 256;
 
 // KPL: elements of the feature row per lane (ceil(H*D/32) rounded up to 4,
 // 8 or 32), so small rows keep few registers per lane.
-template <typename T, typename TO, int MODE, int KPL>
+template <typename T, typename TO, int MODE, int KPL, bool SMALL = false>
 __global__ void __launch_bounds__(kGenWarps * 32)
 k_rows_generic(RowParams p) {
+    static_assert(!SMALL || MODE == kFused, "the one-launch path is the fused forward");
     wait_prior_grid();
     __shared__ Seg segs[kMaxSegs];
     __shared__ int s_nseg, s_total;
@@ -547,7 +677,16 @@ k_rows_generic(RowParams p) {
     __shared__ float sm_s[kGenWarps][kGenMaxH];
     __shared__ float sm_w[kGenWarps][kGenMaxH];
     __shared__ float sm_c[kGenWarps][kGenMaxH];
-    build_segments(p.lists, 1, 1, segs, &s_nseg, &s_total);
+    __shared__ int s_small[2];              // one-launch path: split rows, chunks
+    extern __shared__ int2 small_lists[];   // one-launch path: chunks, then split rows
+    TaskLists L = p.lists;
+    if constexpr (SMALL) {
+        L.chunks = small_lists;
+        L.longs = small_lists + p.small_max_chunks;
+        build_segments_small(p, 1, segs, &s_nseg, &s_total, small_lists, small_lists + p.small_max_chunks, s_small);
+    } else {
+        build_segments(p.lists, 1, 1, segs, &s_nseg, &s_total);
+    }
 
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5;
@@ -571,14 +710,16 @@ k_rows_generic(RowParams p) {
         int row, beg, end, chunk = -1;
         if (sg.kind == kSegChunk) {
             chunk = sg.list_begin + pos;
-            int2 c = p.lists.chunks[chunk];
+            int2 c = L.chunks[chunk];
             row = c.x;
             beg = c.y;
-            end = min(beg + p.lists.chunk_edges, p.indptr[row + 1]);
+            end = min(beg + L.chunk_edges, p.indptr[row + 1]);
         } else {
-            row = p.lists.rows[sg.list_begin + pos];
+            row = SMALL ? sg.list_begin + pos : L.rows[sg.list_begin + pos];
             beg = p.indptr[row];
             end = p.indptr[row + 1];
+            // one-launch path: a split row is walked by its chunks (uniform over the warp)
+            if (SMALL && end - beg > 0 && end - beg > p.long_min) continue;
         }
         float q[KPL], acc[KPL];
         const float qs = MODE == kFused ? p.qscale : 1.f;   // SDDMM scales at the store
@@ -590,13 +731,48 @@ k_rows_generic(RowParams p) {
         }
         for (int h = lane; h < H; h += 32) { hm[h] = -INFINITY; hs[h] = 0.f; }
         __syncwarp();
+        // Rows of few features a lane (KPL <= 8) keep the next entry's K and V
+        // values and the index after it in flight while this entry is
+        // computed; wider rows load per entry (their registers go to the row).
+        constexpr bool kPipe = KPL <= 8;
+        constexpr int KP = kPipe ? KPL : 1;
+        float kn[KP], vn[KP];
+        int64_t jn = 0, jn2 = 0;
+        auto fetch = [&](int64_t jj) {
+#pragma unroll
+            for (int k = 0; k < KP; ++k) {
+                const int el = lane + 32 * k;
+                kn[k] = (MODE != kSpmm && el < HD) ? load_elem(K, jj * HD + el) : 0.f;
+                vn[k] = (MODE != kSddmm && el < HD) ? load_elem(V, jj * HD + el) : 0.f;
+            }
+        };
+        if constexpr (kPipe) {
+            if (beg < end) {
+                jn = __ldg(p.indices + beg);
+                fetch(jn);
+            }
+            jn2 = beg + 1 < end ? __ldg(p.indices + beg + 1) : 0;
+        }
         for (int e = beg; e < end; ++e) {
-            const int64_t j = __ldg(p.indices + e);
+            int64_t j;
+            float kc[KP], vc[KP];
+            if constexpr (kPipe) {
+                j = jn;
+#pragma unroll
+                for (int k = 0; k < KP; ++k) { kc[k] = kn[k]; vc[k] = vn[k]; }
+                if (e + 1 < end) {   // the next entry's values, the index after it
+                    jn = jn2;
+                    fetch(jn);
+                    jn2 = e + 2 < end ? __ldg(p.indices + e + 2) : 0;
+                }
+            } else {
+                j = __ldg(p.indices + e);
+            }
             if constexpr (MODE != kSpmm) {
 #pragma unroll
                 for (int k = 0; k < KPL; ++k) {
                     const int el = lane + 32 * k;
-                    if (el < HD) prod[el] = q[k] * load_elem(K, j * HD + el);
+                    if (el < HD) prod[el] = q[k] * (kPipe ? kc[k < KP ? k : 0] : load_elem(K, j * HD + el));
                 }
                 __syncwarp();
             }
@@ -644,7 +820,7 @@ k_rows_generic(RowParams p) {
                     const int el = lane + 32 * k;
                     if (el < HD) {
                         const int h = head_of(el, D, H, p.ndh);
-                        acc[k] = acc[k] * hc[h] + hw[h] * load_elem(V, j * HD + el);
+                        acc[k] = acc[k] * hc[h] + hw[h] * (kPipe ? vc[k < KP ? k : 0] : load_elem(V, j * HD + el));
                     }
                 }
             }
@@ -679,6 +855,12 @@ k_rows_generic(RowParams p) {
                 for (int h = lane; h < H; h += 32) p.lse[(int64_t)row * H + h] = hm[h] + log2f(hs[h]);
         }
         __syncwarp();
+    }
+    if constexpr (SMALL) {
+        if (s_small[0] > 0) {   // uniform over the grid
+            cooperative_groups::this_grid().sync();
+            small_combine<TO>(p, L.longs, s_small[0]);
+        }
     }
 }
 
@@ -1209,6 +1391,88 @@ static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParam
             break;
     }
     return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+}
+
+// Cooperative launch (every block resident at once, so the grid can sync).
+template <typename Kern, typename... Args>
+static cudaError_t launch_coop(Kern kernel, int grid, int threads, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Blocks of `kernel` (threads, smem dynamic bytes) resident on the whole GPU
+// at once: the bound of a cooperative grid.  Cached per kernel.
+template <typename K>
+static int coop_grid(K kernel, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::unordered_map<const void*, int> cache;
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(reinterpret_cast<const void*>(kernel));
+    if (it != cache.end()) return it->second;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int grid = per_sm * num_sms();
+    cache[reinterpret_cast<const void*>(kernel)] = grid;
+    return grid;
+}
+
+template <typename T, typename TO>
+static gtattn_status launch_small_t(const RowChoice& c, const RowParams& p, cudaStream_t s) {
+    const size_t smem = sizeof(int2) * static_cast<size_t>(p.small_max_chunks + p.small_max_long);
+    auto go = [&](auto kernel, int threads) {
+        const int grid = grid_for_tasks(coop_grid(kernel, threads, smem), p.task_bound, threads / 32);
+        return launch_coop(kernel, std::max(grid, 1), threads, smem, s, p);
+    };
+    cudaError_t e;
+    if (c.kind == RowKernel::kVector) {
+        if (p.bias && p.values) return GTATTN_ERR_UNSUPPORTED;
+        auto by_ext = [&](auto k0, auto kb, auto kv) {
+            return p.bias ? go(kb, kRowThreads) : p.values ? go(kv, kRowThreads) : go(k0, kRowThreads);
+        };
+        switch (c.vpl) {
+            case 1:
+                e = by_ext(k_rows_vec<T, TO, 1, kFused, 0, true>, k_rows_vec<T, TO, 1, kFused, kExtBias, true>,
+                           k_rows_vec<T, TO, 1, kFused, kExtValues, true>);
+                break;
+            case 2:
+                e = by_ext(k_rows_vec<T, TO, 2, kFused, 0, true>, k_rows_vec<T, TO, 2, kFused, kExtBias, true>,
+                           k_rows_vec<T, TO, 2, kFused, kExtValues, true>);
+                break;
+            case 4:
+                if constexpr (sizeof(T) == 4) {
+                    e = by_ext(k_rows_vec<T, TO, 4, kFused, 0, true>, k_rows_vec<T, TO, 4, kFused, kExtBias, true>,
+                               k_rows_vec<T, TO, 4, kFused, kExtValues, true>);
+                    break;
+                }
+                return GTATTN_ERR_UNSUPPORTED;
+            default: return GTATTN_ERR_UNSUPPORTED;
+        }
+    } else {
+        const int kpl = (p.HD + 31) / 32;
+        e = kpl <= 4 ? go(k_rows_generic<T, TO, kFused, 4, true>, kGenWarps * 32)
+            : kpl <= 8 ? go(k_rows_generic<T, TO, kFused, 8, true>, kGenWarps * 32)
+                       : go(k_rows_generic<T, TO, kFused, 32, true>, kGenWarps * 32);
+    }
+    return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+}
+
+gtattn_status launch_rows_small(gtattn_dtype dt, const RowChoice& c, const RowParams& p, cudaStream_t s) {
+    switch (dt) {
+        case GTATTN_BF16: return launch_small_t<__nv_bfloat16, __nv_bfloat16>(c, p, s);
+        case GTATTN_BF16_OUT_F32: return launch_small_t<__nv_bfloat16, float>(c, p, s);
+        case GTATTN_F32: return launch_small_t<float, float>(c, p, s);
+    }
+    return GTATTN_ERR_INVALID_ARG;
 }
 
 gtattn_status launch_rows(Mode mode, gtattn_dtype dt, const RowChoice& c, const RowParams& p,

@@ -26,7 +26,22 @@ struct RowParams {
     TaskLists lists;
     Partials part;
     int task_bound;         // upper bound on the warp tasks of the lists (<= 0: unknown)
+    // Small graphs in one launch (launch_rows_small): `lists` is unused;
+    // every block bins the rows itself into shared memory (rows of more
+    // than long_min entries split into lists.chunk_edges-entry chunks, at
+    // most small_max_chunks chunks and small_max_long split rows), and when
+    // a row is split the grid -- launched cooperatively -- synchronises and
+    // the split rows are combined in the same launch.
+    int long_min;
+    int small_max_chunks, small_max_long;
 };
+
+// Bounds of the one-launch path: rows, entries, and the shared-memory lists
+// (chunks and split rows) each block builds.
+constexpr int kSmallMaxRows = 4096;
+constexpr int kSmallMaxNnz = 65536;
+constexpr int kSmallMaxChunks = 512;
+constexpr int kSmallMaxLong = 256;
 
 // Upper bound on the warp tasks binning makes: a task is one row or more
 // (rows of up to long_min entries), or one chunk of a split row (at most
@@ -52,6 +67,11 @@ bool choose_row_kernel(int H, int D, gtattn_dtype dt, const void* Q, const void*
 // Launches the persistent row kernel over every task of `p.lists`.
 gtattn_status launch_rows(Mode mode, gtattn_dtype dt, const RowChoice& c, const RowParams& p,
                           cudaStream_t s);
+
+// The fused forward in one launch for a small graph (p.small set by the
+// caller; N <= kSmallMaxRows, nnz <= kSmallMaxNnz, worst-case chunk and
+// split-row counts within the shared-memory lists).
+gtattn_status launch_rows_small(gtattn_dtype dt, const RowChoice& c, const RowParams& p, cudaStream_t s);
 
 // Combines split-row partials into `out` for every split row (mode kFused or kSpmm).
 gtattn_status launch_combine(Mode mode, gtattn_dtype dt, const RowParams& p, cudaStream_t s);

@@ -537,3 +537,29 @@ def test_dense_wait_timeout_is_reported_and_a_later_call_is_correct():
     plan.close()
     got, _, _ = run(w, d, "plan", detect_dense=True)
     check_out(w, got, oracle_rows(w)["out"], "dense after a timeout", out32=True)
+
+
+@pytest.mark.parametrize("H,D,dtype", [(4, 32, "bf16"), (8, 64, "f32"), (3, 5, "f32"), (2, 8, "bf16")])
+def test_small_graph_one_launch_with_split_rows(H, D, dtype):
+    # N <= 4096 and nnz <= 65536: the plan-less forward is one cooperative
+    # launch that bins in shared memory; rows of more than 256 entries are
+    # split into chunks whose partials are combined after the grid-wide sync
+    rng = np.random.default_rng(H * 100 + D)
+    n = 3000
+    src = np.concatenate([rng.integers(0, n, 12000), rng.integers(0, n, 1500), rng.integers(0, n, 700)])
+    dst = np.concatenate([rng.integers(0, n, 12000), np.full(1500, 5), np.full(700, 2999)])
+    key = np.unique(dst * n + src)
+    ip, ix = wl.csr_by_destination(key % n, key // n, n)
+    assert np.diff(ip).max() > 256 and ip[-1] <= 65536
+    Q, K, V = (rng.standard_normal((n, H, D)) for _ in range(3))
+    w = _mk(ip, ix, Q, K, V, dtype)
+    ref = oracle_rows(w)["out"]
+    for out32 in ((True, False) if dtype == "bf16" else (False,)):
+        d = to_device(w, out32=out32)
+        gt.gtattn_profile_enable(True)
+        gt.gtattn_profile_read(reset=True)
+        got, _, _ = run(w, d, "fwd")
+        prof = gt.gtattn_profile_read(reset=True)
+        gt.gtattn_profile_enable(False)
+        assert prof["rows"]["launches"] == 1 and prof["bin"]["launches"] == 0 and prof["combine"]["launches"] == 0
+        check_out(w, got, ref, f"one-launch H={H} D={D} {dtype} out32={out32}", out32=out32)

@@ -71,6 +71,18 @@ def path_bytes(path, N, nnz, H, D, esize):
         extra = N * H * D * esize + 3 * 4 * N * H * D
         cb += extra
         ub += extra
+    elif path in ("bwd_saved", "train"):
+        # the backward given the forward's fp32 output and row statistics:
+        # those read instead of the output written, dO read, dQ/dK/dV written;
+        # the training step adds the forward that writes them
+        nhd = N * H * D
+        extra = -nhd * esize + 4 * nhd + 4 * N * H + nhd * esize + 3 * 4 * nhd
+        if path == "train":
+            fc, fu = compulsory_bytes(N, nnz, H, D, esize), unique_bytes(N, nnz, H, D, esize)
+            cb += fc - nhd * esize + 4 * nhd + 4 * N * H
+            ub += fu - nhd * esize + 4 * nhd + 4 * N * H
+        cb += extra
+        ub += extra
     elif path == "proj":   # hidden F = H*D in and out: X read, q/k/v and o written and read back, Y written
         F = H * D
         extra = N * F * esize + 2 * 3 * N * F * esize + 2 * N * F * esize + N * F * esize + 4 * F * F * esize
@@ -287,6 +299,22 @@ def make_step(w, d, path, gt, plan=None, probs_bufs=None):
         dO, dQ, dK, dV = probs_bufs
         return lambda: gt.gtattn_bwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], dO, dQ, dK, dV,
                                           w.H, w.D, w.scale, dt)
+    if path in ("bwd_saved", "train"):   # the backward reusing the forward's output and row statistics
+        dO, dQ, dK, dV, O, stats = probs_bufs
+        fdt = gt.GTATTN_F32 if dt == gt.GTATTN_F32 else gt.GTATTN_BF16_OUT_F32
+
+        def fwd():
+            gt.gtattn_fwd_plan_stats(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], O, stats, w.H, w.D,
+                                     w.scale, fdt)
+
+        def bwd():
+            gt.gtattn_bwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], dO, dQ, dK, dV, w.H, w.D,
+                               w.scale, dt, O=O, stats=stats)
+
+        if path == "bwd_saved":
+            fwd()   # once, outside the timed steps
+            return bwd
+        return lambda: (fwd(), bwd())
     if path == "proj":   # the block with its projections (SparseMHA: biases, head-inner features)
         X, W, b, Wo, bo, Y = probs_bufs
         F = w.H * w.D
@@ -317,7 +345,7 @@ def run_gpu_workload(w, path, steps, warmup, gt, dev, flush, want_profile=True, 
     d = device_inputs(w, dev)
     plan = None
     probs_bufs = None
-    if path in ("plan", "bwd_plan"):
+    if path in ("plan", "bwd_plan", "bwd_saved", "train"):
         plan = gt.Plan(d["indptr"], d["indices"], detect_dense=detect_dense and path == "plan")
     if path == "probs":
         probs_bufs = (torch.empty(w.nnz, w.H, device=dev), torch.empty(w.nnz, w.H, device=dev))
@@ -325,11 +353,14 @@ def run_gpu_workload(w, path, steps, warmup, gt, dev, flush, want_profile=True, 
         gen = torch.Generator(device=dev)
         gen.manual_seed(12345)
         probs_bufs = (torch.randn(w.nnz, w.H, device=dev, generator=gen),)
-    if path in ("bwd", "bwd_plan"):   # backward: seeded N(0, 1) output gradient in the input dtype, fp32 gradients
+    if path in ("bwd", "bwd_plan", "bwd_saved", "train"):
+        # backward: seeded N(0, 1) output gradient in the input dtype, fp32 gradients
         gen = torch.Generator(device=dev)
         gen.manual_seed(34567)
         dO = torch.randn(w.N, w.H, w.D, device=dev, generator=gen).to(d["Q"].dtype)
         probs_bufs = (dO,) + tuple(torch.empty(w.N, w.H, w.D, device=dev) for _ in range(3))
+        if path in ("bwd_saved", "train"):   # the forward's fp32 output and row statistics
+            probs_bufs += (torch.empty(w.N, w.H, w.D, device=dev), torch.empty(w.N, w.H, device=dev))
     if path == "proj":   # X ~ N(0, 1), weights and biases ~ U(-1/sqrt(F), 1/sqrt(F)) (nn.Linear's init)
         gen = torch.Generator(device=dev)
         gen.manual_seed(45678)
@@ -565,6 +596,10 @@ def gpu_arm(args):
                             "weighted": "gtattn_fwd_weighted (fused, weighted adjacency, fp32 U(0,1))",
                             "bwd": "gtattn_bwd (dQ, dK, dV of sum(out * dO), dO ~ N(0,1))",
                             "bwd_plan": "gtattn_bwd_plan (as bwd, source-major pattern kept in the plan)",
+                            "bwd_saved": "gtattn_bwd_plan given the fp32 output and row statistics of "
+                                         "gtattn_fwd_plan_stats (no forward recompute)",
+                            "train": "gtattn_fwd_plan_stats + gtattn_bwd_plan on its output and statistics "
+                                     "(one training step of the attention)",
                             "ndh": "gtattn_fwd_ndh (head-innermost [N, D, H] rows, generic kernel)",
                             "proj": "gtattn_fwd_proj (q/k/v and output projections around the attention, "
                                     "hidden H*D, biases, head-inner features)"}[args.path],
@@ -597,15 +632,17 @@ def gpu_arm(args):
         extra = {}
         for other, pth in (("erdos_renyi", "fwd"), ("molecules", "fwd"), ("tiny_random", "fwd"),
                            ("dense_blocks", "plan"), ("rmat", "probs"), ("rmat", "bias"), ("rmat", "weighted"),
-                           ("rmat", "bwd"), ("rmat", "bwd_plan"), ("rmat", "ndh"), ("rmat", "proj"),
+                           ("rmat", "bwd"), ("rmat", "bwd_plan"), ("rmat", "bwd_saved"), ("rmat", "train"),
+                           ("rmat", "ndh"), ("rmat", "proj"),
                            ("erdos_renyi", "proj"),
                            ("molecules", "proj")):
             if other == name and pth == args.path:
                 continue
+            # (microsecond-scale graphs: more steps for a stable median)
+            n_o = 50 if other in ("tiny_random", "molecules") else max(3, args.steps // 2)
             try:
-                wo, _, _, t_o, p_o, inf_o, pl_o = run_gpu_workload(wl.make_workload(other), pth,
-                                                                   max(3, args.steps // 2), 3, gt, dev, flush,
-                                                                   detect_dense=True)
+                wo, _, _, t_o, p_o, inf_o, pl_o = run_gpu_workload(wl.make_workload(other), pth, n_o, 3, gt, dev,
+                                                                   flush, detect_dense=True)
             except Exception as exc:  # report, do not hide
                 extra[f"{other}/{pth}"] = {"error": str(exc)}
                 continue
@@ -693,7 +730,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="rmat", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--path", default="fwd", choices=["fwd", "plan", "probs", "bias", "weighted", "bwd", "bwd_plan",
-                                                       "ndh", "proj"])
+                                                       "bwd_saved", "train", "ndh", "proj"])
     ap.add_argument("--soak", type=float, default=2.0,
                     help="seconds of untimed steps before the warm-up (clock record under load)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")

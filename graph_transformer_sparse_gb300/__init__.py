@@ -23,24 +23,25 @@ from ._build import LIB, build
 __all__ = [
     "GtattnError", "Plan", "build", "load", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs", "gtattn_fwd_bias", "gtattn_fwd_weighted", "gtattn_bwd", "gtattn_fwd_ndh",
     "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_proj", "gtattn_device_errors", "gtattn_bwd_plan",
-    "gtattn_csr_build",
+    "gtattn_fwd_plan_stats", "gtattn_csr_build",
     "gtattn_plan_destroy", "gtattn_plan_get_info", "gtattn_coo_to_csr",
     "gtattn_csr_validate", "gtattn_status_string", "gtattn_profile_enable", "gtattn_profile_read",
     "sparse_mha", "GTATTN_F32", "GTATTN_BF16", "GTATTN_BF16_OUT_F32",
-    "GTATTN_KERNEL_AUTO", "GTATTN_KERNEL_VECTOR", "GTATTN_KERNEL_GENERIC", "EXPORTED_SYMBOLS",
+    "GTATTN_KERNEL_AUTO", "GTATTN_KERNEL_VECTOR", "GTATTN_KERNEL_GENERIC", "GTATTN_KERNEL_NARROW",
+    "EXPORTED_SYMBOLS",
 ]
 
 GTATTN_OK, GTATTN_ERR_INVALID_ARG, GTATTN_ERR_BAD_CSR, GTATTN_ERR_UNSUPPORTED = 0, 1, 2, 3
 GTATTN_ERR_CUDA, GTATTN_ERR_NO_MEMORY, GTATTN_ERR_TIMEOUT = 4, 5, 6
 GTATTN_F32, GTATTN_BF16, GTATTN_BF16_OUT_F32 = 0, 1, 2
-GTATTN_KERNEL_AUTO, GTATTN_KERNEL_VECTOR, GTATTN_KERNEL_GENERIC = 0, 1, 2
+GTATTN_KERNEL_AUTO, GTATTN_KERNEL_VECTOR, GTATTN_KERNEL_GENERIC, GTATTN_KERNEL_NARROW = 0, 1, 2, 3
 
 EXPORTED_SYMBOLS = (
     "gtattn_status_string", "gtattn_last_error", "gtattn_csr_build", "gtattn_plan_destroy",
     "gtattn_plan_get_info", "gtattn_fwd", "gtattn_fwd_plan", "gtattn_fwd_probs",
     "gtattn_coo_to_csr", "gtattn_csr_validate", "gtattn_profile_enable", "gtattn_profile_read",
     "gtattn_fwd_noalloc", "gtattn_fwd_host", "gtattn_fwd_bias", "gtattn_fwd_weighted", "gtattn_bwd",
-    "gtattn_fwd_ndh", "gtattn_fwd_proj", "gtattn_device_errors", "gtattn_bwd_plan",
+    "gtattn_fwd_ndh", "gtattn_fwd_proj", "gtattn_device_errors", "gtattn_bwd_plan", "gtattn_fwd_plan_stats",
 )
 KCAT_NAMES = ("bin", "rows", "combine", "softmax", "dense", "gemm")
 
@@ -114,7 +115,8 @@ def load(path: str | None = None):
             "gtattn_fwd_proj": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, i32, i32, i32, f32,
                                  i32, vp], i32),
             "gtattn_device_errors": ([vp, i32], i32),
-            "gtattn_bwd_plan": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp], i32),
+            "gtattn_bwd_plan": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp], i32),
+            "gtattn_fwd_plan_stats": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, f32, i32, vp], i32),
             "gtattn_profile_enable": ([i32], i32),
             "gtattn_profile_read": ([vp, i32], i32),
         }
@@ -229,12 +231,16 @@ def gtattn_fwd_proj(indptr, indices, X, Wqkv, bqkv, Wo, bo, Y, N, nnz, F_in, H, 
            "gtattn_fwd_proj")
 
 
-def gtattn_bwd_plan(plan, indptr, indices, Q, K, V, dO, dQ, dK, dV, H, D, scale, dtype, stream=None):
+def gtattn_bwd_plan(plan, indptr, indices, Q, K, V, dO, dQ, dK, dV, H, D, scale, dtype, O=None, stats=None,
+                    stream=None):
     """gtattn_bwd on a plan's binning; the plan keeps the source-major
-    pattern built by its first backward call."""
+    pattern built by its first backward call.  O and stats: the fp32 output
+    and row statistics of gtattn_fwd_plan_stats (both or neither); given,
+    the forward is not recomputed."""
     _check(load().gtattn_bwd_plan(plan.handle if isinstance(plan, Plan) else plan, _ptr(indptr), _ptr(indices),
-                                  _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), int(H), int(D),
-                                  float(scale), int(dtype), _stream(stream)), "gtattn_bwd_plan")
+                                  _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(stats), _ptr(dO), _ptr(dQ), _ptr(dK),
+                                  _ptr(dV), int(H), int(D), float(scale), int(dtype), _stream(stream)),
+           "gtattn_bwd_plan")
 
 
 def gtattn_device_errors(reset: bool = True) -> int:
@@ -249,6 +255,14 @@ def gtattn_fwd_plan(plan, indptr, indices, Q, K, V, out, H, D, scale, dtype, str
     _check(load().gtattn_fwd_plan(plan.handle if isinstance(plan, Plan) else plan, _ptr(indptr),
                                   _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(out), int(H), int(D),
                                   float(scale), int(dtype), _stream(stream)), "gtattn_fwd_plan")
+
+
+def gtattn_fwd_plan_stats(plan, indptr, indices, Q, K, V, out, stats, H, D, scale, dtype, stream=None):
+    """gtattn_fwd_plan that also writes the rows' log2-sum-exp (fp32 [N, H])."""
+    _check(load().gtattn_fwd_plan_stats(plan.handle if isinstance(plan, Plan) else plan, _ptr(indptr),
+                                        _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), _ptr(out), _ptr(stats), int(H),
+                                        int(D), float(scale), int(dtype), _stream(stream)),
+           "gtattn_fwd_plan_stats")
 
 
 def gtattn_fwd_probs(indptr, indices, Q, K, V, out, logits, probs, N, nnz, H, D, scale, dtype,

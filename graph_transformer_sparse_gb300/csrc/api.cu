@@ -277,6 +277,7 @@ static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, co
             p.long_min = o.long_row_min;
             p.small_max_chunks = kSmallMaxChunks;
             p.small_max_long = kSmallMaxLong;
+            p.small_no_split = nnz <= o.long_row_min;
             gtattn_status st;
             {
                 ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
@@ -374,16 +375,16 @@ extern "C" gtattn_status gtattn_fwd_ndh(const int32_t* indptr, const int32_t* in
                                         int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
     if (N == 0) return GTATTN_OK;
-    // Shapes the vector kernel tiles: transpose to [N, H, D] in scratch, the
-    // head-major forward, transpose the output back (four row-local copies,
-    // far cheaper than the generic kernel on head-innermost rows).  Others:
-    // the generic kernel reads the [N, D, H] rows directly.
+    // Shapes the vector or narrow-head kernel takes: transpose to [N, H, D]
+    // in scratch, the head-major forward, transpose the output back (four
+    // row-local copies, far cheaper than the generic kernel on head-innermost
+    // rows).  Others: the generic kernel reads the [N, D, H] rows directly.
     const size_t esz = dtype == GTATTN_F32 ? 4 : 2, osz = dtype == GTATTN_BF16 ? 2 : 4;
     const size_t in_bytes = align_up(esz * static_cast<size_t>(N) * H * D);
     const size_t out_bytes = align_up(osz * static_cast<size_t>(N) * H * D);
     RowChoice c;
     void* buf = nullptr;
-    if (!choose_row_kernel(H, D, dtype, Q, K, V, out, GTATTN_KERNEL_AUTO, &c) || c.kind != RowKernel::kVector ||
+    if (!choose_row_kernel(H, D, dtype, Q, K, V, out, GTATTN_KERNEL_AUTO, &c) || c.kind == RowKernel::kGeneric ||
         pool_alloc(&buf, 3 * in_bytes + out_bytes, stream) != GTATTN_OK)
         return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream, 1);
     char* b = static_cast<char*>(buf);
@@ -405,10 +406,28 @@ extern "C" gtattn_status gtattn_fwd_ndh(const int32_t* indptr, const int32_t* in
     return st;
 }
 
+static gtattn_status fwd_plan(const gtattn_plan* plan, const int32_t* indptr, const int32_t* indices, const void* Q,
+                              const void* K, const void* V, void* out, float* stats, int H, int D, float scale,
+                              gtattn_dtype dtype, cudaStream_t stream);
+
 extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t* indptr,
                                          const int32_t* indices, const void* Q, const void* K,
                                          const void* V, void* out, int H, int D, float scale,
                                          gtattn_dtype dtype, cudaStream_t stream) {
+    return fwd_plan(plan, indptr, indices, Q, K, V, out, nullptr, H, D, scale, dtype, stream);
+}
+
+extern "C" gtattn_status gtattn_fwd_plan_stats(const gtattn_plan* plan, const int32_t* indptr,
+                                               const int32_t* indices, const void* Q, const void* K,
+                                               const void* V, void* out, float* stats, int H, int D, float scale,
+                                               gtattn_dtype dtype, cudaStream_t stream) {
+    if (!stats || (reinterpret_cast<uintptr_t>(stats) & 3u)) return GTATTN_ERR_INVALID_ARG;
+    return fwd_plan(plan, indptr, indices, Q, K, V, out, stats, H, D, scale, dtype, stream);
+}
+
+static gtattn_status fwd_plan(const gtattn_plan* plan, const int32_t* indptr, const int32_t* indices, const void* Q,
+                              const void* K, const void* V, void* out, float* stats, int H, int D, float scale,
+                              gtattn_dtype dtype, cudaStream_t stream) {
     if (!plan) return GTATTN_ERR_INVALID_ARG;
     const int64_t N = plan->N, nnz = plan->nnz;
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
@@ -419,7 +438,9 @@ extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t*
     const int n_chunks = plan->hdr_host[HdrLayout::kChunks];
     const int n_long = plan->hdr_host[HdrLayout::kLong];
     const int n_blocks = plan->hdr_host[HdrLayout::kDenseBlocks];
-    const bool dense = n_blocks > 0 && dense_supported(H, D, dtype, Q, K, V, out);
+    // (the dense-block kernel writes no row statistics: with stats, every row
+    // goes through the row kernels)
+    const bool dense = n_blocks > 0 && !stats && dense_supported(H, D, dtype, Q, K, V, out);
 
     Partials part{};
     if (n_chunks > 0) {
@@ -439,6 +460,7 @@ extern "C" gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t*
     }
     TaskLists L{plan->hdr, plan->rows, plan->chunks, plan->longs, plan->opts.chunk_edges, dense ? 0 : 1};
     RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale * kLog2e, c, L, part);
+    p.lse = stats;
     gtattn_status st = GTATTN_OK;
     if (dense) {
         ProfScope ps(GTATTN_KCAT_DENSE, 1, stream);
@@ -621,21 +643,24 @@ static gtattn_status check_bwd(const int32_t* indptr, const int32_t* indices, co
 
 // The two-pass backward given the destination binning (rows, with row_chunks
 // chunk slots) and the source-major pattern: the forward again for its fp32
-// output and log-sum-exp, then the passes.
+// output and log-sum-exp (unless the caller saved both), then the passes.
 static gtattn_status bwd_run(const int32_t* indptr, const int32_t* indices, const TaskLists& rows, int64_t row_chunks,
-                             const SourceMajor& sm, const void* Q, const void* K, const void* V, const void* dO,
-                             float* dQ, float* dK, float* dV, int64_t N, int64_t nnz, int H, int D, float scale,
-                             gtattn_dtype dtype, const RowChoice& c, cudaStream_t stream) {
+                             const SourceMajor& sm, const void* Q, const void* K, const void* V, const float* O_saved,
+                             const float* stats_saved, const void* dO, float* dQ, float* dK, float* dV, int64_t N,
+                             int64_t nnz, int H, int D, float scale, gtattn_dtype dtype, const RowChoice& c,
+                             cudaStream_t stream) {
     const int HD = H * D;
     const gtattn_dtype fdt = dtype == GTATTN_F32 ? GTATTN_F32 : GTATTN_BF16_OUT_F32;   // fp32 forward output
     const size_t grad_bytes = sizeof(float) * static_cast<size_t>(N) * HD;
     size_t off = 0;
-    const size_t o_O = off; off = align_up(off + grad_bytes);
-    const size_t o_L = off; off = align_up(off + sizeof(float) * static_cast<size_t>(N) * H);
+    const bool saved = O_saved != nullptr;
+    const size_t o_O = off; if (!saved) off = align_up(off + grad_bytes);
+    const size_t o_L = off; if (!saved) off = align_up(off + sizeof(float) * static_cast<size_t>(N) * H);
     const size_t o_LD = off; off = align_up(off + sizeof(float2) * static_cast<size_t>(N) * H);
-    const size_t o_m = off; off = align_up(off + sizeof(float) * static_cast<size_t>(row_chunks) * H);
-    const size_t o_s = off; off = align_up(off + sizeof(float) * static_cast<size_t>(row_chunks) * H);
-    const size_t o_acc = off; off = align_up(off + sizeof(float) * static_cast<size_t>(row_chunks) * HD);
+    const int64_t fwd_chunks = saved ? 0 : row_chunks;   // the forward's partials
+    const size_t o_m = off; off = align_up(off + sizeof(float) * static_cast<size_t>(fwd_chunks) * H);
+    const size_t o_s = off; off = align_up(off + sizeof(float) * static_cast<size_t>(fwd_chunks) * H);
+    const size_t o_acc = off; off = align_up(off + sizeof(float) * static_cast<size_t>(fwd_chunks) * HD);
     const size_t o_pq = off; off = align_up(off + sizeof(float) * static_cast<size_t>(row_chunks) * HD);
     const size_t o_pk = off; off = align_up(off + sizeof(float) * static_cast<size_t>(sm.max_chunks) * HD);
     const size_t o_pv = off; off = align_up(off + sizeof(float) * static_cast<size_t>(sm.max_chunks) * HD);
@@ -646,16 +671,21 @@ static gtattn_status bwd_run(const int32_t* indptr, const int32_t* indices, cons
     float* lse = reinterpret_cast<float*>(b + o_L);
     Partials part{reinterpret_cast<float*>(b + o_m), reinterpret_cast<float*>(b + o_s),
                   reinterpret_cast<float*>(b + o_acc)};
-    RowParams p = make_params(indptr, indices, Q, K, V, O, N, nnz, H, D, scale * kLog2e, c, rows, part);
-    p.lse = lse;
-    gtattn_status st;
-    {
-        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
-        st = launch_rows(kFused, fdt, c, p, stream);
-    }
-    if (st == GTATTN_OK && row_chunks > 0) {
-        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
-        st = launch_combine(kFused, fdt, p, stream);
+    gtattn_status st = GTATTN_OK;
+    if (saved) {   // the forward's fp32 output and row statistics, kept by the caller
+        O = const_cast<float*>(O_saved);
+        lse = const_cast<float*>(stats_saved);
+    } else {          // the forward again
+        RowParams p = make_params(indptr, indices, Q, K, V, O, N, nnz, H, D, scale * kLog2e, c, rows, part);
+        p.lse = lse;
+        {
+            ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+            st = launch_rows(kFused, fdt, c, p, stream);
+        }
+        if (st == GTATTN_OK && row_chunks > 0) {
+            ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
+            st = launch_combine(kFused, fdt, p, stream);
+        }
     }
     if (st == GTATTN_OK) {
         ProfScope ps(GTATTN_KCAT_ROWS, 4, stream);
@@ -716,20 +746,24 @@ extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indice
     }
     if (st == GTATTN_OK) st = source_major_build(indptr, indices, sc.lists, N, nnz, o, sm, stream);
     if (st == GTATTN_OK)
-        st = bwd_run(indptr, indices, sc.lists, row_chunks, sm, Q, K, V, dO, dQ, dK, dV, N, nnz, H, D, scale, dtype, c,
-                     stream);
+        st = bwd_run(indptr, indices, sc.lists, row_chunks, sm, Q, K, V, nullptr, nullptr, dO, dQ, dK, dV, N, nnz, H, D,
+                     scale, dtype, c, stream);
     pool_free(smb, stream);
     pool_free(sc.base, stream);
     return st;
 }
 
 extern "C" gtattn_status gtattn_bwd_plan(const gtattn_plan* plan, const int32_t* indptr, const int32_t* indices,
-                                         const void* Q, const void* K, const void* V, const void* dO, float* dQ,
-                                         float* dK, float* dV, int H, int D, float scale, gtattn_dtype dtype,
-                                         cudaStream_t stream) {
+                                         const void* Q, const void* K, const void* V, const float* O,
+                                         const float* stats, const void* dO, float* dQ, float* dK, float* dV, int H,
+                                         int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
     if (!plan) return GTATTN_ERR_INVALID_ARG;
     const int64_t N = plan->N, nnz = plan->nnz;
     GT_TRY(check_bwd(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, nnz, H, D, dtype));
+    // O is read as whole float4 rows by the passes
+    if ((O == nullptr) != (stats == nullptr) || (reinterpret_cast<uintptr_t>(O) & 15u) ||
+        (reinterpret_cast<uintptr_t>(stats) & 3u))
+        return GTATTN_ERR_INVALID_ARG;
     if (N == 0) return GTATTN_OK;
     RowChoice c;
     if (!bwd_two_pass(H, D, dtype, Q, K, V, dO, dQ, dK, dV, &c))
@@ -752,8 +786,8 @@ extern "C" gtattn_status gtattn_bwd_plan(const gtattn_plan* plan, const int32_t*
         plan->bwd_pattern = p;
     }
     source_major_carve(static_cast<char*>(plan->bwd_pattern), N, nnz, plan->opts, &sm);
-    return bwd_run(indptr, indices, rows, row_chunks, sm, Q, K, V, dO, dQ, dK, dV, N, nnz, H, D, scale, dtype, c,
-                   stream);
+    return bwd_run(indptr, indices, rows, row_chunks, sm, Q, K, V, O, stats, dO, dQ, dK, dV, N, nnz, H, D, scale,
+                   dtype, c, stream);
 }
 
 // The attention block with its projections: q, k, v = X W^T + b (one GEMM

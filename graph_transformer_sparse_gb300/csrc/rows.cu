@@ -154,7 +154,23 @@ __device__ void build_segments_small(const RowParams& p, int P, Seg* segs, int* 
     const int N = p.N, nt = blockDim.x, chunk = p.lists.chunk_edges;
     auto split = [&](int deg) { return deg > 0 && deg > p.long_min; };
     int any = 0;
-    for (int i = threadIdx.x; i < N; i += nt) any |= split(p.indptr[i + 1] - p.indptr[i]);
+    if (!p.small_no_split) {   // (the host knows no row can be split when nnz <= long_min)
+        int i0 = 0;
+        if ((reinterpret_cast<uintptr_t>(p.indptr) & 15u) == 0) {
+            // four rows per 16-byte load (and the next group's first offset),
+            // several loads in flight per thread
+            const int n4 = N / 4;
+            const int4* ip4 = reinterpret_cast<const int4*>(p.indptr);
+#pragma unroll 4
+            for (int k = threadIdx.x; k < n4; k += nt) {
+                const int4 a = __ldg(ip4 + k);
+                const int b = __ldg(p.indptr + 4 * k + 4);
+                any |= split(a.y - a.x) | split(a.z - a.y) | split(a.w - a.z) | split(b - a.w);
+            }
+            i0 = 4 * n4;
+        }
+        for (int i = i0 + threadIdx.x; i < N; i += nt) any |= split(p.indptr[i + 1] - p.indptr[i]);
+    }
     any = __syncthreads_or(any);
     int n_long = 0, n_chunks = 0;
     if (any) {
@@ -345,7 +361,8 @@ k_rows_vec(RowParams p) {
         build_segments_small(p, P, segs, &s_nseg, &s_total, small_lists, small_lists + p.small_max_chunks,
                              s_small);
     } else {
-        build_segments(p.lists, P, U, segs, &s_nseg, &s_total, MODE == kFused);
+        // (rows of one entry are copied unless their statistics are wanted)
+        build_segments(p.lists, P, U, segs, &s_nseg, &s_total, MODE == kFused && p.lse == nullptr);
     }
 
     const int lane = threadIdx.x & 31;
@@ -865,6 +882,211 @@ k_rows_generic(RowParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// narrow-head kernel: heads of at most kNarrowMaxD features, fused mode,
+// [N, H, D] rows, with the per-entry bias or values of the other kernels
+// when given (the molecule configuration of "Graph
+// Transformer in a Nutshell": hidden 80 over 8 heads, head width 10, which
+// no 16-byte lane split fits).  One lane per head: a row is G lanes (H
+// rounded up to a power of two), each holding its head's q, running maximum,
+// sum and accumulators, so the dot product and the softmax update are one
+// lane's work with no shuffle or shared memory; P = 32 / G rows per warp,
+// and rows of many entries get S lane groups (slots) merged at the end.
+// PAIR: D even, so a head's features are read two at a time (8-byte fp32,
+// 4-byte bf16 loads).
+// ---------------------------------------------------------------------------
+template <typename T, bool PAIR>
+__device__ __forceinline__ void load_head(const T* __restrict__ p, int D, float (&x)[kNarrowMaxD]) {
+    if constexpr (PAIR) {
+#pragma unroll
+        for (int d = 0; d < kNarrowMaxD; d += 2) {
+            if (d < D) {
+                if constexpr (sizeof(T) == 4) {
+                    const float2 v = __ldg(reinterpret_cast<const float2*>(p + d));
+                    x[d] = v.x;
+                    x[d + 1] = v.y;
+                } else {
+                    const uint32_t w = __ldg(reinterpret_cast<const unsigned*>(p + d));
+                    x[d] = bf16lo(w);
+                    x[d + 1] = bf16hi(w);
+                }
+            } else {
+                x[d] = 0.f;
+                x[d + 1] = 0.f;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int d = 0; d < kNarrowMaxD; ++d) x[d] = d < D ? load_elem(p, d) : 0.f;
+    }
+}
+
+template <typename T, typename TO, bool PAIR, bool SMALL = false>
+__global__ void __launch_bounds__(kRowThreads)
+k_rows_narrow(RowParams p) {
+    wait_prior_grid();
+    __shared__ Seg segs[kMaxSegs];
+    __shared__ int s_nseg, s_total;
+    __shared__ int s_small[2];              // one-launch path: split rows, chunks
+    extern __shared__ int2 small_lists[];   // one-launch path: chunks, then split rows
+    const int G = p.G;
+    const int P = 32 / G;
+    TaskLists L = p.lists;
+    if constexpr (SMALL) {
+        L.chunks = small_lists;
+        L.longs = small_lists + p.small_max_chunks;
+        build_segments_small(p, P, segs, &s_nseg, &s_total, small_lists, small_lists + p.small_max_chunks, s_small);
+    } else {
+        // (rows of one entry are copied unless their statistics are wanted)
+        build_segments(p.lists, P, 1, segs, &s_nseg, &s_total, p.lse == nullptr);
+    }
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / G;
+    const int h = lane - grp * G;           // this lane's head
+    const bool on = h < p.H;                // lanes past H (H not a power of two) idle
+    const int D = p.D, H = p.H;
+    const int64_t HD = p.HD;
+    const int off = h * D;
+    const T* __restrict__ Q = static_cast<const T*>(p.Q);
+    const T* __restrict__ K = static_cast<const T*>(p.K);
+    const T* __restrict__ V = static_cast<const T*>(p.V);
+    TO* __restrict__ O = static_cast<TO*>(p.out);
+
+    const int warps_total = gridDim.x * (blockDim.x >> 5);
+    int seg = 0;
+    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < s_total; t += warps_total) {
+        while (seg + 1 < s_nseg && segs[seg + 1].first_task <= t) ++seg;
+        const Seg sg = segs[seg];
+        const int S = sg.S;
+        const int r = grp / S, sl = grp - r * S;
+        const int pos = (t - sg.first_task) * sg.R + r;
+        bool valid = pos < sg.count;
+        int row = 0, beg = 0, end = 0, chunk = -1;
+        if (valid) {
+            if (sg.kind == kSegChunk) {
+                chunk = sg.list_begin + pos;
+                const int2 c = L.chunks[chunk];
+                row = c.x;
+                beg = c.y;
+                end = min(beg + L.chunk_edges, p.indptr[row + 1]);
+            } else {
+                row = SMALL ? sg.list_begin + pos : L.rows[sg.list_begin + pos];
+                beg = p.indptr[row];
+                end = p.indptr[row + 1];
+                // one-launch path: a split row is walked by its chunks
+                if (SMALL && end - beg > 0 && end - beg > p.long_min) valid = false;
+            }
+        }
+        if (sg.kind == kSegCopy) {   // a row of one entry: its softmax weight is 1, out = V[j]
+            if (valid && on) {
+                float x[kNarrowMaxD];
+                load_head<T, PAIR>(V + static_cast<int64_t>(ld_index(p.indices + beg)) * HD + off, D, x);
+                // with a bias: weight 1 for a finite bias, 0 for -inf (the
+                // entry removed), NaN for NaN or +inf
+                float wgt = 1.f;
+                if (p.bias) {
+                    const float b = __ldg(p.bias + static_cast<int64_t>(beg) * H + h);
+                    wgt = b == -INFINITY ? 0.f : (b - b) + 1.f;
+                }
+#pragma unroll
+                for (int d = 0; d < kNarrowMaxD; ++d)
+                    if (d < D) store_elem(O, static_cast<int64_t>(row) * HD + off + d, x[d] * wgt);
+            }
+            continue;
+        }
+        const bool live = valid && on;
+        float q[kNarrowMaxD], acc[kNarrowMaxD];
+        if (live) load_head<T, PAIR>(Q + static_cast<int64_t>(row) * HD + off, D, q);
+#pragma unroll
+        for (int d = 0; d < kNarrowMaxD; ++d) {
+            q[d] = live ? q[d] * p.qscale : 0.f;   // logits in log2 units
+            acc[d] = 0.f;
+        }
+        float m = -INFINITY, ssum = 0.f;
+        // Two-stage pipeline: the next entry's K and V values and the index
+        // after it are in flight while this entry is computed.
+        int e = beg + sl;
+        float kc[kNarrowMaxD], vc[kNarrowMaxD];
+        if (live && e < end) {
+            const int64_t j = ld_index(p.indices + e);
+            load_head<T, PAIR>(K + j * HD + off, D, kc);
+            load_head<T, PAIR>(V + j * HD + off, D, vc);
+        }
+        int jn = (live && e + S < end) ? ld_index(p.indices + e + S) : 0;
+        for (; live && e < end; e += S) {
+            const int e1 = e + S;
+            float kn[kNarrowMaxD], vn[kNarrowMaxD];
+            if (e1 < end) {
+                load_head<T, PAIR>(K + static_cast<int64_t>(jn) * HD + off, D, kn);
+                load_head<T, PAIR>(V + static_cast<int64_t>(jn) * HD + off, D, vn);
+                jn = e1 + S < end ? ld_index(p.indices + e1 + S) : 0;
+            }
+            float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+            for (int d = 0; d < kNarrowMaxD; d += 2) {
+                d0 = fmaf(q[d], kc[d], d0);
+                d1 = fmaf(q[d + 1], kc[d + 1], d1);
+            }
+            float l = d0 + d1;
+            if (p.values) l *= ld_stream(p.values + e);   // weighted adjacency
+            if (p.bias) l = fmaf(ld_stream(p.bias + static_cast<int64_t>(e) * H + h), kLog2e, l);   // log2 units
+            if (l > m) {   // a new maximum: rescale what is accumulated (m = -inf: c = 0)
+                const float c = ex2(m - l);
+                ssum *= c;
+#pragma unroll
+                for (int d = 0; d < kNarrowMaxD; ++d) acc[d] *= c;
+                m = l;
+            }
+            const float w = ex2(l - (m == -INFINITY ? 0.f : m));   // (all logits -inf so far: w = 0)
+            ssum += w;
+#pragma unroll
+            for (int d = 0; d < kNarrowMaxD; ++d) acc[d] = fmaf(w, vc[d], acc[d]);
+#pragma unroll
+            for (int d = 0; d < kNarrowMaxD; ++d) {
+                kc[d] = kn[d];
+                vc[d] = vn[d];
+            }
+        }
+        // merge the S slots of each row (lane groups G, 2G, ... apart)
+        for (int o = G; o < S * G; o <<= 1) {
+            const float m2 = __shfl_xor_sync(kFull, m, o);
+            const float s2 = __shfl_xor_sync(kFull, ssum, o);
+            const float M = fmaxf(m, m2);
+            const float Mref = M == -INFINITY ? 0.f : M;
+            const float c1 = ex2(m - Mref), c2 = ex2(m2 - Mref);
+            ssum = ssum * c1 + s2 * c2;
+#pragma unroll
+            for (int d = 0; d < kNarrowMaxD; ++d) {
+                const float a2 = __shfl_xor_sync(kFull, acc[d], o);
+                acc[d] = acc[d] * c1 + a2 * c2;
+            }
+            m = M;
+        }
+        if (!live || sl != 0) continue;
+        if (chunk >= 0) {
+            float* pa = p.part.acc + static_cast<int64_t>(chunk) * HD + off;
+#pragma unroll
+            for (int d = 0; d < kNarrowMaxD; ++d)
+                if (d < D) pa[d] = acc[d];
+            p.part.m[static_cast<int64_t>(chunk) * H + h] = m;
+            p.part.s[static_cast<int64_t>(chunk) * H + h] = ssum;
+        } else {
+            const float inv = ssum > 0.f ? 1.f / ssum : 0.f;
+#pragma unroll
+            for (int d = 0; d < kNarrowMaxD; ++d)
+                if (d < D) store_elem(O, static_cast<int64_t>(row) * HD + off + d, ssum > 0.f ? acc[d] * inv : 0.f);
+            // the row's log-sum-exp (log2 units) when the caller asks for it
+            if (p.lse) p.lse[static_cast<int64_t>(row) * H + h] = m + log2f(ssum);
+        }
+    }
+    if constexpr (SMALL) {
+        if (s_small[0] > 0) {   // uniform over the grid
+            cooperative_groups::this_grid().sync();
+            small_combine<TO>(p, L.longs, s_small[0]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // combine split-row partials
 // ---------------------------------------------------------------------------
 // Phase 1, a block per split row of many chunks: the row's chunks are spread
@@ -1286,9 +1508,33 @@ bool choose_row_kernel(int H, int D, gtattn_dtype dt, const void* Q, const void*
         }
     }
     if (force == GTATTN_KERNEL_VECTOR) return false;
+    // heads too narrow for a 16-byte lane split: one lane per head
+    if ((force == GTATTN_KERNEL_AUTO || force == GTATTN_KERNEL_NARROW) && D <= kNarrowMaxD && H <= 32) {
+        int G = 1;
+        while (G < H) G <<= 1;
+        const bool pair = D % 2 == 0 && (al & static_cast<uintptr_t>(2 * esz - 1)) == 0;
+        *c = RowChoice{RowKernel::kNarrow, pair ? 1 : 0, G, 1};
+        return true;
+    }
+    if (force == GTATTN_KERNEL_NARROW) return false;
     if (H > kGenMaxH || HD > kMaxHD) return false;
     *c = RowChoice{RowKernel::kGeneric, 0, 0, 0};
     return true;
+}
+
+// Warp tasks of the narrow kernel: P = 32 / G rows per warp, one task per
+// chunk, at most one part-filled task per segment.
+static int narrow_task_bound(const RowParams& p) {
+    if (p.task_bound <= 0) return 0;
+    const int P = 32 / p.G;
+    const int64_t b = (static_cast<int64_t>(p.N) + P - 1) / P + (p.task_bound - p.N) + kMaxSegs;
+    return b < p.task_bound ? static_cast<int>(b) : p.task_bound;
+}
+
+// The narrow kernel takes the fused mode on [N, H, D] rows; other calls with
+// that choice go to the generic kernel.
+static bool narrow_applies(const RowChoice& c, Mode mode, const RowParams& p) {
+    return c.kind == RowKernel::kNarrow && mode == kFused && !p.ndh && !(p.bias && p.values);
 }
 
 template <typename K>
@@ -1351,6 +1597,15 @@ static gtattn_status launch_vec_t(int vpl, const RowParams& p, cudaStream_t s) {
 
 template <typename T, typename TO>
 static gtattn_status launch_rows_t(Mode mode, const RowChoice& c, const RowParams& p, cudaStream_t s) {
+    if (narrow_applies(c, mode, p)) {
+        auto go = [&](auto kernel) {
+            const int grid = grid_for_tasks(grid_persistent(kernel, kRowThreads, 0), narrow_task_bound(p),
+                                            kRowThreads / 32);
+            return launch_pdl(kernel, grid, kRowThreads, 0, s, p);
+        };
+        const cudaError_t e = c.vpl ? go(k_rows_narrow<T, TO, true>) : go(k_rows_narrow<T, TO, false>);
+        return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+    }
     if (c.kind == RowKernel::kVector) {
         // one of the bias or the values at a time (the entry points take one)
         if (p.bias && p.values) return GTATTN_ERR_UNSUPPORTED;
@@ -1434,7 +1689,14 @@ static gtattn_status launch_small_t(const RowChoice& c, const RowParams& p, cuda
         return launch_coop(kernel, std::max(grid, 1), threads, smem, s, p);
     };
     cudaError_t e;
-    if (c.kind == RowKernel::kVector) {
+    if (narrow_applies(c, kFused, p)) {
+        auto go_n = [&](auto kernel) {
+            const int grid = grid_for_tasks(coop_grid(kernel, kRowThreads, smem), narrow_task_bound(p),
+                                            kRowThreads / 32);
+            return launch_coop(kernel, std::max(grid, 1), kRowThreads, smem, s, p);
+        };
+        e = c.vpl ? go_n(k_rows_narrow<T, TO, true, true>) : go_n(k_rows_narrow<T, TO, false, true>);
+    } else if (c.kind == RowKernel::kVector) {
         if (p.bias && p.values) return GTATTN_ERR_UNSUPPORTED;
         auto by_ext = [&](auto k0, auto kb, auto kv) {
             return p.bias ? go(kb, kRowThreads) : p.values ? go(kv, kRowThreads) : go(k0, kRowThreads);

@@ -17,8 +17,8 @@ struct RowParams {
     const float* bias;      // fused / SDDMM modes: fp32 [nnz, H] added to the logits, or null
     const float* values;    // fused / SDDMM modes: fp32 [nnz] multiplying the dot products, or null
     int ndh;                // 1: node rows are [D, H] (head innermost; generic kernel only)
-    float* lse;             // fused mode: fp32 [N, H] row log-sum-exp (log2 units) written, or null;
-                            // rows of one entry (copied) and of none are not written
+    float* lse;             // fused mode: fp32 [N, H] row log-sum-exp (log2 units) written for every
+                            // row (-inf for a row without entries), or null
     float* logits;          // SDDMM mode: fp32 [nnz, H]
     float qscale;           // fused: scale*log2(e); SDDMM: scale
     int N, H, D, HD;
@@ -34,6 +34,7 @@ struct RowParams {
     // the split rows are combined in the same launch.
     int long_min;
     int small_max_chunks, small_max_long;
+    int small_no_split;     // nnz <= long_min: no row is split (the blocks skip the check)
 };
 
 // Bounds of the one-launch path: rows, entries, and the shared-memory lists
@@ -51,13 +52,16 @@ inline int row_task_bound(int64_t N, int64_t nnz, int chunk) {
     return b > 0x7fffffff ? 0x7fffffff : static_cast<int>(b);
 }
 
-enum class RowKernel { kVector, kGeneric };
+enum class RowKernel { kVector, kGeneric, kNarrow };
 
 struct RowChoice {
     RowKernel kind;
-    int vpl;    // 16-byte vectors per lane (vector kernel)
+    int vpl;    // 16-byte vectors per lane (vector kernel); narrow kernel: 1 = features read in pairs
     int G, lph;
 };
+
+// Widest head the narrow-head kernel takes (one lane per head).
+constexpr int kNarrowMaxD = 16;
 
 // Picks the row kernel for a shape; `force` is a gtattn_kernel value.
 // Returns false when no kernel supports the shape (or the forced one does not).

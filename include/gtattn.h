@@ -74,7 +74,10 @@ typedef enum { GTATTN_F32 = 0, GTATTN_BF16 = 1, GTATTN_BF16_OUT_F32 = 2 } gtattn
 typedef enum {
     GTATTN_KERNEL_AUTO = 0,
     GTATTN_KERNEL_VECTOR = 1,   /* 16-byte gathers, lanes split a feature row */
-    GTATTN_KERNEL_GENERIC = 2   /* any H, D; one warp per row */
+    GTATTN_KERNEL_GENERIC = 2,  /* any H, D; one warp per row */
+    GTATTN_KERNEL_NARROW = 3    /* D <= 16, H <= 32: one lane per head (the fused
+                                   forward; the unfused variants run the
+                                   generic kernel) */
 } gtattn_kernel;
 
 /* Plan-building options.  Zero-initialise and set what you need; a field
@@ -210,6 +213,24 @@ gtattn_status gtattn_fwd_plan(const gtattn_plan* plan, const int32_t* indptr,
                               gtattn_dtype dtype, cudaStream_t stream);
 
 /*
+ * gtattn_fwd_plan_stats -- gtattn_fwd_plan that also writes each row's
+ * softmax statistic, for a training step whose backward (gtattn_bwd_plan)
+ * then skips the forward recompute.
+ *   stats: fp32 [N, H], device memory, 4-byte aligned (required):
+ *          stats[i, h] = log2 sum_j 2^(scale * log2(e) * q_i.k_j) over row
+ *          i's entries, i.e. the natural log-sum-exp of the row's logits
+ *          divided by ln 2; -inf for a row without entries.
+ *   Other arguments, results and errors: as gtattn_fwd_plan, except that
+ *   complete blocks go through the row kernels (the dense-block kernel
+ *   writes no statistics).  For the backward, out must be fp32 (dtype F32,
+ *   or BF16_OUT_F32 for bf16 inputs).
+ */
+gtattn_status gtattn_fwd_plan_stats(const gtattn_plan* plan, const int32_t* indptr,
+                                    const int32_t* indices, const void* Q, const void* K,
+                                    const void* V, void* out, float* stats, int H, int D, float scale,
+                                    gtattn_dtype dtype, cudaStream_t stream);
+
+/*
  * gtattn_fwd_probs -- the unfused path: SDDMM (logits), edge softmax
  * (probs), SpMM (out) as three kernel stages with the per-edge values
  * materialised in global memory -- the bsddmm / softmax / bspmm and
@@ -303,10 +324,18 @@ gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indices, const vo
  * the binning, freed by gtattn_plan_destroy), so later calls skip it.  Same
  * results, bit for bit, as gtattn_bwd.  indptr/indices must be the arrays
  * the plan was built from.  One plan must not be used by concurrent calls.
+ *   O, stats: the fp32 output (16-byte aligned) and statistics that
+ *           gtattn_fwd_plan_stats wrote for the same plan, Q, K, V, scale
+ *           and (bf16 inputs: BF16_OUT_F32) dtype, or both NULL.  Given,
+ *           the backward skips its forward recompute and, with the plan's
+ *           default kernel choice, gives the same bits as without them;
+ *           NULL, it recomputes both.  One given without the other, or
+ *           misaligned: INVALID_ARG.
  */
 gtattn_status gtattn_bwd_plan(const gtattn_plan* plan, const int32_t* indptr, const int32_t* indices,
-                              const void* Q, const void* K, const void* V, const void* dO, float* dQ, float* dK,
-                              float* dV, int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream);
+                              const void* Q, const void* K, const void* V, const float* O, const float* stats,
+                              const void* dO, float* dQ, float* dK, float* dV, int H, int D, float scale,
+                              gtattn_dtype dtype, cudaStream_t stream);
 
 /*
  * gtattn_fwd_noalloc -- gtattn_fwd without any allocation.  The pages have

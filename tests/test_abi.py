@@ -86,8 +86,13 @@ def test_host_argument_checks_bias_weighted_bwd_ndh(lib):
     assert fg(16, 16, 16, None, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV       # null K, nnz > 0
     assert fg(None, 16, 16, 16, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV       # null indptr
     assert fg(16, None, None, None, None, None, None, None, None, 0, 0, 2, 8, 1.0, 0, None) == OK   # N = 0
-    fp = lib.gtattn_bwd_plan   # plan indptr indices Q K V dO dQ dK dV H D scale dtype stream
-    assert fp(None, 16, 16, 16, 16, 16, 16, 16, 16, 16, 2, 8, 1.0, 0, None) == INV                 # null plan
+    fp = lib.gtattn_bwd_plan   # plan indptr indices Q K V O stats dO dQ dK dV H D scale dtype stream
+    assert fp(None, 16, 16, 16, 16, 16, None, None, 16, 16, 16, 16, 2, 8, 1.0, 0, None) == INV     # null plan
+    assert fp(None, 16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 2, 8, 1.0, 0, None) == INV         # null plan
+    fs = lib.gtattn_fwd_plan_stats   # plan indptr indices Q K V out stats H D scale dtype stream
+    assert fs(None, 16, 16, 16, 16, 16, 16, 16, 2, 8, 1.0, 0, None) == INV                 # null plan
+    assert fs(16, 16, 16, 16, 16, 16, 16, None, 2, 8, 1.0, 0, None) == INV                 # null stats
+    assert fs(16, 16, 16, 16, 16, 16, 16, 18, 2, 8, 1.0, 0, None) == INV                   # misaligned stats
     fn = lib.gtattn_fwd_ndh   # indptr indices Q K V out N nnz H D scale dtype stream
     assert fn(None, 16, 16, 16, 16, 16, 4, 4, 2, 8, 1.0, 0, None) == INV                   # null indptr
     assert fn(16, 16, 16, 16, 16, 16, 4, 4, 2, 1000, 1.0, 0, None) == INV                  # H*D > 1024

@@ -231,11 +231,11 @@ def test_backward_full_size_sampled(name):
         assert np.isfinite(got[k]).all(), k
 
 
-def _bwd_plan(w, d, dO_t, plan):
+def _bwd_plan(w, d, dO_t, plan, O=None, stats=None):
     grads = {k: torch.full((w.N, w.H, w.D), float("nan"), device="cuda") for k in ("dQ", "dK", "dV")}
     dt = gt.GTATTN_F32 if w.dtype == "f32" else gt.GTATTN_BF16
     gt.gtattn_bwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], dO_t, grads["dQ"], grads["dK"],
-                       grads["dV"], w.H, w.D, w.scale, dt)
+                       grads["dV"], w.H, w.D, w.scale, dt, O=O, stats=stats)
     torch.cuda.synchronize()
     return {k: v.cpu().numpy().astype(np.float64) for k, v in grads.items()}
 
@@ -301,3 +301,57 @@ def test_backward_plan_with_dense_blocks():
     cond = _bwd_cond(w.indptr, w.indices, w.Q, w.K, w.V, g, w.scale)
     for k in ("dQ", "dK", "dV"):
         _grad_close(got[k], ref[k], cond[k], f"dense blocks {k}")
+
+
+def _row_log2sumexp(indptr, logits):
+    # natural log-sum-exp of each row's logits over ln 2; -inf for empty rows
+    N, H = len(indptr) - 1, logits.shape[1]
+    deg = np.diff(indptr)
+    out = np.full((N, H), -np.inf)
+    rows = np.flatnonzero(deg > 0)
+    if len(rows):
+        starts = indptr[:-1][rows]
+        m = np.maximum.reduceat(logits, starts, axis=0)
+        row_of = np.repeat(np.arange(len(rows)), deg[rows])
+        ssum = np.add.reduceat(np.exp(logits - m[row_of]), starts, axis=0)
+        out[rows] = (m + np.log(ssum)) / np.log(2.0)
+    return out
+
+
+@pytest.mark.parametrize("name", ["rmat", "erdos_renyi", "tiny_random", "dense_blocks"])
+def test_backward_reuses_the_saved_forward(name):
+    # the forward with row statistics: its output equals the plain planned
+    # forward's (fp32 output), its statistics the rows' log2-sum-exp from the
+    # oracle's logits; the backward given both skips the recompute and gives
+    # the same bits as the backward without them
+    w = wl.small_workload(name)
+    g, g_t = _dO(w, 29)
+    d = to_device(w)
+    plan = gt.Plan(d["indptr"], d["indices"], detect_dense=True)
+    if name == "dense_blocks":
+        assert plan.info()["n_dense_blocks"] > 0
+    dt = gt.GTATTN_F32 if w.dtype == "f32" else gt.GTATTN_BF16_OUT_F32
+    O = torch.full((w.N, w.H, w.D), float("nan"), device="cuda")
+    stats = torch.full((w.N, w.H), float("nan"), device="cuda")
+    gt.gtattn_fwd_plan_stats(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], O, stats, w.H, w.D,
+                             w.scale, dt)
+    plain = torch.full_like(O, float("nan"))
+    gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], plain, w.H, w.D, w.scale, dt)
+    recomputed = _bwd_plan(w, d, g_t, plan)
+    reused = _bwd_plan(w, d, g_t, plan, O=O, stats=stats)
+    with pytest.raises(gt.GtattnError):   # one without the other
+        _bwd_plan(w, d, g_t, plan, O=O)
+    plan.close()
+    for k in ("dQ", "dK", "dV"):
+        assert np.array_equal(recomputed[k], reused[k]), f"{name} {k}: saved forward changes the bits"
+    ref = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, want_probs=True)
+    O_h = O.cpu().numpy().astype(np.float64)
+    if name != "dense_blocks":   # (there the plain forward takes the dense kernel)
+        assert np.array_equal(O_h, plain.cpu().numpy().astype(np.float64))
+    assert np.allclose(O_h, ref["out"], rtol=1e-4, atol=1e-5)
+    want = _row_log2sumexp(w.indptr, ref["logits"])
+    got = stats.cpu().numpy().astype(np.float64)
+    empty = np.isinf(want)
+    assert (got[empty] == -np.inf).all()
+    err = np.abs(got[~empty] - want[~empty])
+    assert (err <= 1e-5 * (1 + np.abs(want[~empty]))).all(), float(err.max())

@@ -563,3 +563,61 @@ def test_small_graph_one_launch_with_split_rows(H, D, dtype):
         gt.gtattn_profile_enable(False)
         assert prof["rows"]["launches"] == 1 and prof["bin"]["launches"] == 0 and prof["combine"]["launches"] == 0
         check_out(w, got, ref, f"one-launch H={H} D={D} {dtype} out32={out32}", out32=out32)
+
+
+@pytest.mark.parametrize("H,D,dtype", [(8, 10, "f32"), (8, 10, "bf16"), (5, 7, "f32"), (32, 16, "bf16"),
+                                        (1, 2, "f32"), (3, 1, "bf16"), (16, 3, "f32")])
+def test_narrow_head_kernel(H, D, dtype):
+    # one lane per head (heads of at most 16 features): rows whole, rows of
+    # many entries over several lane groups, rows split into chunks, the
+    # one-launch small-graph path, and the row statistics
+    rng = np.random.default_rng(H * 37 + D)
+    n = 900
+    ip, ix = wl.random_csr(rng, n, 14000, self_loops=True, degree_skew=1.2)
+    assert np.diff(ip).max() > 256
+    Q, K, V = (rng.standard_normal((n, H, D)) for _ in range(3))
+    w = _mk(ip, ix, Q, K, V, dtype)
+    ref = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, w.scale, want_probs=True)
+    d = to_device(w)
+    runs = [("fwd", {}), ("plan", {}), ("plan", dict(kernel=gt.GTATTN_KERNEL_NARROW)),
+            ("plan", dict(kernel=gt.GTATTN_KERNEL_NARROW, long_row_min=30, chunk_edges=11)),
+            ("plan", dict(kernel=gt.GTATTN_KERNEL_NARROW, long_row_min=-1, chunk_edges=4))]
+    for path, kw in runs:
+        got, _, _ = run(w, d, path, **kw)
+        check_out(w, got, ref["out"], f"narrow H={H} D={D} {dtype} {path} {kw}")
+    # statistics: log2-sum-exp of each row's logits
+    plan = gt.Plan(d["indptr"], d["indices"], kernel=gt.GTATTN_KERNEL_NARROW, long_row_min=30, chunk_edges=11)
+    o32 = torch.full((n, H, D), float("nan"), device="cuda")
+    stats = torch.full((n, H), float("nan"), device="cuda")
+    gt.gtattn_fwd_plan_stats(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], o32, stats, H, D, w.scale,
+                             gt.GTATTN_F32 if dtype == "f32" else gt.GTATTN_BF16_OUT_F32)
+    torch.cuda.synchronize()
+    plan.close()
+    check_out(w, o32.cpu().numpy().astype(np.float64), ref["out"], "narrow stats-forward output", out32=True)
+    lg = ref["logits"]
+    deg = np.diff(w.indptr)
+    want = np.full((n, H), -np.inf)
+    rows = np.flatnonzero(deg > 0)
+    m = np.maximum.reduceat(lg, w.indptr[:-1][rows], axis=0)
+    ssum = np.add.reduceat(np.exp(lg - np.repeat(m, deg[rows], axis=0)), w.indptr[:-1][rows], axis=0)
+    want[rows] = (m + np.log(ssum)) / np.log(2.0)
+    got = stats.cpu().numpy().astype(np.float64)
+    assert (got[deg == 0] == -np.inf).all()
+    err = np.abs(got[rows] - want[rows])
+    assert (err <= 1e-5 * (1 + np.abs(want[rows]))).all(), float(err.max())
+
+
+def test_narrow_kernel_refuses_wide_shapes():
+    # forcing the narrow kernel on heads wider than 16 or more than 32 heads
+    rng = np.random.default_rng(3)
+    n = 64
+    ip, ix = wl.random_csr(rng, n, 300, self_loops=True)
+    for H, D in ((2, 17), (33, 4)):
+        Q = rng.standard_normal((n, H, D))
+        w = _mk(ip, ix, Q, Q, Q)
+        d = to_device(w)
+        plan = gt.Plan(d["indptr"], d["indices"], kernel=gt.GTATTN_KERNEL_NARROW)
+        with pytest.raises(gt.GtattnError):
+            gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], H, D, w.scale,
+                               gt.GTATTN_F32)
+        plan.close()

@@ -631,7 +631,8 @@ def gpu_arm(args):
     if rank == 0 and not args.no_extra:
         extra = {}
         for other, pth in (("erdos_renyi", "fwd"), ("molecules", "fwd"), ("tiny_random", "fwd"),
-                           ("dense_blocks", "plan"), ("rmat", "probs"), ("rmat", "bias"), ("rmat", "weighted"),
+                           ("dense_blocks", "plan"), ("dense_blocks_d32", "plan"), ("dense_blocks_d128", "plan"),
+                           ("rmat", "probs"), ("rmat", "bias"), ("rmat", "weighted"),
                            ("rmat", "bwd"), ("rmat", "bwd_plan"), ("rmat", "bwd_saved"), ("rmat", "train"),
                            ("rmat", "ndh"), ("rmat", "proj"),
                            ("erdos_renyi", "proj"),
@@ -641,8 +642,14 @@ def gpu_arm(args):
             # (microsecond-scale graphs: more steps for a stable median)
             n_o = 50 if other in ("tiny_random", "molecules") else max(3, args.steps // 2)
             try:
-                wo, _, _, t_o, p_o, inf_o, pl_o = run_gpu_workload(wl.make_workload(other), pth, n_o, 3, gt, dev,
-                                                                   flush, detect_dense=True)
+                if other.startswith("dense_blocks_d"):   # the dense-block graph with heads of another width
+                    hd = int(other[len("dense_blocks_d"):])
+                    w_o = wl.make_workload("dense_blocks", D=hd)
+                    w_o.desc = f"64 disjoint complete graphs of 512 nodes, 8x{hd} bf16, 0.5*N(0,1)"
+                else:
+                    w_o = wl.make_workload(other)
+                wo, _, _, t_o, p_o, inf_o, pl_o = run_gpu_workload(w_o, pth, n_o, 3, gt, dev, flush,
+                                                                   detect_dense=True)
             except Exception as exc:  # report, do not hide
                 extra[f"{other}/{pth}"] = {"error": str(exc)}
                 continue
@@ -668,7 +675,7 @@ def gpu_arm(args):
                 ent["gemm_ms_per_call"] = round(kms["gemm"] * 3, 5)
                 ent["gemm_tflops"] = round(tf, 1)
                 ent["gemm_tensor_frac"] = round(tf / peaks["bf16_tflops"], 4) if wo.dtype == "bf16" else None
-            if other == "dense_blocks" and inf_o and inf_o.get("n_dense_blocks"):
+            if other.startswith("dense_blocks") and inf_o and inf_o.get("n_dense_blocks"):
                 tf = dense_flops(inf_o["n_dense_blocks"], 512, wo.H, wo.D) / (ms / 1e3) / 1e12
                 ent["tflops"] = round(tf, 1)
                 ent["tensor_frac"] = round(tf / peaks["bf16_tflops"], 4)

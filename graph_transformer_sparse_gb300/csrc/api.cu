@@ -464,7 +464,8 @@ static gtattn_status fwd_plan(const gtattn_plan* plan, const int32_t* indptr, co
     gtattn_status st = GTATTN_OK;
     if (dense) {
         ProfScope ps(GTATTN_KCAT_DENSE, 1, stream);
-        st = launch_dense(plan->dense_tiles, plan->n_dense_tiles, N, Q, K, V, out, H, D, scale, dtype,
+        st = launch_dense(plan->dense_tiles, plan->dense_tiles1, plan->n_dense_tiles, plan->n_dense_tiles1, N, Q, K,
+                          V, out, H, D, scale, dtype,
                           plan->hdr + HdrLayout::kErr, plan->opts.wait_cycles, plan->opts.test_stall, stream);
     }
     int row_tasks = n_chunks + (dense ? 0 : plan->hdr_host[HdrLayout::kDenseRows]);

@@ -49,10 +49,61 @@ namespace gt {
 namespace {
 
 constexpr int kTile = 128;              // rows per Q / K / V tile
-constexpr int kD = 64;                  // head width handled here
-constexpr uint32_t kTileBytes = kTile * kD * 2;   // 16 KB bf16
 constexpr long long kWaitCycles = kTcWaitCycles;   // drains (and the default bound of the other waits)
 
+// Per head width D (32, 64 or 128).  Tensor memory holds three 128-column
+// S/P buffers and O (D columns) for each query tile of an item, so D = 128
+// takes one query tile per item; shared memory holds the Q buffers and the
+// K/V ring, so D = 128 keeps one Q buffer and three stages (224 KB).  Rows of
+// 64 bytes (D = 32) use the 64-byte swizzle; rows of 256 bytes (D = 128) are
+// two 128-byte-swizzled 64-column sub-tiles, 16 KB apart.
+template <int D>
+struct Cfg {
+    static_assert(D == 32 || D == 64 || D == 128, "head widths of the dense kernel");
+    static constexpr uint32_t kTB = kTile * D * 2;          // one tile, bf16
+    static constexpr int kNq = D == 128 ? 1 : 2;            // query tiles per work item
+    static constexpr int kQBufs = D == 128 ? 1 : 2;
+    static constexpr int kStages = D == 128 ? 3 : 4;        // K/V ring
+    static constexpr int kSub = D == 128 ? 2 : 1;           // 64-column sub-tiles of a row
+    static constexpr int kBoxX = D == 32 ? 32 : 64;         // TMA box width (elements)
+    static constexpr size_t kSmemQ = 0;
+    static constexpr size_t kSmemKV = static_cast<size_t>(kQBufs) * kNq * kTB;
+    static constexpr size_t kSmemBytes = kSmemKV + static_cast<size_t>(kStages) * 2 * kTB;
+    static constexpr size_t kSmemAlloc = kSmemBytes + 1024;
+    // descriptor start-address units (16 bytes) between K/V stages and Q tiles
+    static constexpr uint64_t kStageUnits = (2 * kTB) >> 4;
+    static constexpr uint64_t kQUnits = kTB >> 4;
+    static constexpr uint64_t kSubUnits = (kTB / 2) >> 4;   // D = 128: second sub-tile
+    static constexpr int kVStep = D == 32 ? 64 : 128;        // units per 16 keys of V (16 rows)
+    static constexpr uint32_t kSbo = D == 32 ? 512 : 1024;   // 8-row group stride (bytes)
+    static constexpr uint32_t kVLbo = D == 128 ? kTB / 2 : 8192;   // V: stride between 64-column atoms
+    static_assert(kSubUnits > 0 && kVStep > 0, "(every instance names its constants)");
+};
+
+
+// Shared-memory descriptor of a 64-byte-swizzled operand (layout type 4):
+// start address, leading and stride byte offsets in 16-byte units.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(4) << 61;
+    return d;
+}
+// K-major operand (Q, K: rows of D features) and MN-major operand (V: rows
+// of D features read along the keys) descriptors for head width D.
+template <int D>
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
+    if constexpr (D == 32) return smem_desc_sw64(saddr, 16, Cfg<D>::kSbo);
+    else return smem_desc_sw128(saddr, 16, Cfg<D>::kSbo);
+}
+template <int D>
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) {
+    if constexpr (D == 32) return smem_desc_sw64(saddr, Cfg<D>::kVLbo, Cfg<D>::kSbo);
+    else return smem_desc_sw128(saddr, Cfg<D>::kVLbo, Cfg<D>::kSbo);
+}
 
 // Non-blocking test (never suspends the thread).  The MMA warp issues it
 // before a batch of MMAs and reads the answer after the batch, so the test's
@@ -147,6 +198,92 @@ __device__ __forceinline__ void mma_half_step(uint32_t d_o, uint32_t a_p, uint64
         : "memory");
 }
 
+// S = Q K^T over K = D for D = 32 (two 16-element steps) or D = 128 (eight:
+// four in each 64-column sub-tile), by one elected lane of the converged
+// warp; `pred` != 0 to issue (uniform over the warp).
+template <int D>
+__device__ __forceinline__ void mma_s_batch_d(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t pred) {
+    if constexpr (D == 32) {
+        asm volatile(
+            "{\n\t.reg .pred f, q, e, ps;\n\tsetp.ne.b32 f, 0, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\tsetp.ne.and.b32 ps, %4, 0, e;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %3, q;\n\t}"
+            ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(pred), "l"(a + 2), "l"(b + 2)
+            : "memory");
+    } else {
+        constexpr uint64_t S = Cfg<D>::kSubUnits;
+        asm volatile(
+            "{\n\t.reg .pred f, q, e, ps;\n\t.reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n\t"
+            "setp.ne.b32 f, 0, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+            "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\tadd.s64 a4, %1, %5;\n\t"
+            "add.s64 a5, a4, 2;\n\tadd.s64 a6, a4, 4;\n\tadd.s64 a7, a4, 6;\n\t"
+            "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\tadd.s64 b4, %2, %5;\n\t"
+            "add.s64 b5, b4, 2;\n\tadd.s64 b6, b4, 4;\n\tadd.s64 b7, b4, 6;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\tsetp.ne.and.b32 ps, %4, 0, e;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, f;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, q;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, q;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, q;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %3, q;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %3, q;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %3, q;\n\t"
+            "@ps tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %3, q;\n\t}"
+            ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(pred), "n"(S)
+            : "memory");
+    }
+}
+// Commit of everything the elected lane issued so far to an mbarrier, when
+// `pred` != 0 (uniform over the warp).
+__device__ __forceinline__ void tc_commit_if(uint32_t bar, uint32_t pred) {
+    asm volatile(
+        "{\n\t.reg .pred e, pc;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.and.b32 pc, %1, 0, e;\n\t"
+        "@pc tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        ::"r"(bar), "r"(pred)
+        : "memory");
+}
+// The half key-tile step of mma_half_step for D = 32 or 128: O (+)= P_hi V +
+// P_lo V with N = D (V's 16-key steps kVStep units apart), the commits, then
+// S over K = D.
+template <int D>
+__device__ __forceinline__ void mma_half_step_d(uint32_t d_o, uint32_t a_p, uint64_t b_v, uint32_t id_o, uint32_t acc,
+                                                uint32_t bar_o, uint32_t do_pv, uint32_t bar_x, uint32_t do_x,
+                                                uint32_t d_s, uint64_t a_q, uint64_t b_k, uint32_t id_s,
+                                                uint32_t bar_s, uint32_t do_s) {
+    constexpr int VS = Cfg<D>::kVStep;
+    asm volatile(
+        "{\n\t.reg .pred p, q, e, pv, px;\n\t"
+        ".reg .b64 v1, v2, v3, v4, v5, v6, v7;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+        "add.s64 v1, %2, %9;\n\tadd.s64 v2, %2, %10;\n\tadd.s64 v3, %2, %11;\n\tadd.s64 v4, %2, %12;\n\t"
+        "add.s64 v5, %2, %13;\n\tadd.s64 v6, %2, %14;\n\tadd.s64 v7, %2, %15;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.and.b32 pv, %6, 0, e;\n\tsetp.ne.and.b32 px, %8, 0, e;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+0], %2, %3, p;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], %2, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], v1, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], v1, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+32], v2, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+48], v2, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+40], v3, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+56], v3, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+64], v4, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+80], v4, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+72], v5, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+88], v5, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+96], v6, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+112], v6, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+104], v7, %3, q;\n\t"
+        "@pv tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+120], v7, %3, q;\n\t"
+        "@pv tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t"
+        "@px tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}"
+        ::"r"(d_o), "r"(a_p), "l"(b_v), "r"(id_o), "r"(acc), "r"(bar_o), "r"(do_pv), "r"(bar_x), "r"(do_x),
+          "n"(VS), "n"(2 * VS), "n"(3 * VS), "n"(4 * VS), "n"(5 * VS), "n"(6 * VS), "n"(7 * VS)
+        : "memory");
+    mma_s_batch_d<D>(d_s, a_q, b_k, id_s, do_s);
+    tc_commit_if(bar_s, do_s);
+}
+
 struct DenseErr {
     static constexpr int kTimeout = 1;
 };
@@ -179,28 +316,29 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kRegsLaunch * kThread
 // A tile's P sum above this (or not finite) makes the softmax take the exact
 // tile maximum and raise its running maximum (P <= 2^12 otherwise).
 constexpr float kTileSumLimit = 4096.f;
-constexpr int kStages = 4;                        // K/V ring
+constexpr int kMaxStages = 4;                     // K/V ring (Cfg<D>::kStages of them used)
 constexpr uint32_t kTmemAll = 512;
 // TMEM: three S/P buffers (128 columns each) used in rotation by the S tiles
-// of both query tiles -- S number k (A0, B0, A1, B1, ... within the CTA's
-// sequence) lives in buffer k % 3 and its P is written over it -- then O_A, O_B.
+// of the item's query tiles -- S number k (A0, B0, A1, B1, ... within the
+// CTA's sequence) lives in buffer k % 3 and its P is written over it -- then
+// O_A (and O_B), D columns each.
 __host__ __device__ constexpr uint32_t col_buf(int b) { return 128u * static_cast<uint32_t>(b); }
-__host__ __device__ constexpr uint32_t col_o(int g) { return g == 0 ? 384u : 448u; }
-constexpr size_t kWsSmemQ = 0;                    // 2 buffers x 2 query tiles
-constexpr size_t kWsSmemKV = 4 * kTileBytes;      // stage s: K at +0, V at +kTileBytes
-constexpr size_t kWsSmemBytes = 4 * kTileBytes + kStages * 2 * kTileBytes;   // 192 KB
-constexpr size_t kWsSmemAlloc = kWsSmemBytes + 1024;
-// Descriptor start-address units (16 bytes) between K/V stages and between Q tiles.
-constexpr uint64_t kStageUnits = (2 * kTileBytes) >> 4;
-constexpr uint64_t kQUnits = kTileBytes >> 4;
-static_assert((kStages & (kStages - 1)) == 0, "stages are stepped with a mask");
-static_assert((kWsSmemAlloc + 1024) >> 4 < (1u << 14), "descriptor start addresses fit 14 bits");
+template <int D>
+__host__ __device__ constexpr uint32_t col_o(int g) { return 384u + static_cast<uint32_t>(g * D); }
+static_assert(384 + 2 * 64 <= 512 && 384 + 2 * 32 <= 512 && 384 + 128 <= 512, "O fits beside the S/P buffers");
+// (shared memory: Q buffers x query tiles at 0, then stage s: K at
+// kSmemKV + 2 s kTB, V kTB after it)
+static_assert((Cfg<64>::kSmemAlloc + 1024) >> 4 < (1u << 14) && (Cfg<128>::kSmemAlloc + 1024) >> 4 < (1u << 14),
+              "descriptor start addresses fit 14 bits");
+static_assert(Cfg<128>::kSmemAlloc <= 227 * 1024 - 512, "shared memory of the widest heads");
 __device__ __forceinline__ int mod3(int x) { return x >= 3 ? x - 3 : x; }   // x < 6
+template <int NS>
+__device__ __forceinline__ int stage_add(int st, int k) { return (st + k) % NS; }
 
 struct WsBars {
     uint64_t q_full[2], q_empty[2];   // Q buffers (TMA <-> MMA)
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
+    uint64_t kv_full[kMaxStages];
+    uint64_t kv_empty[kMaxStages];
     uint64_t s[2][2];    // S tile n of query tile g is in TMEM: barrier s[g][n & 1]
                          // (MMA -> softmax g; two barriers because an S tile
                          // can run two ahead of its softmax)
@@ -271,11 +409,26 @@ __device__ __forceinline__ void quad_transpose(uint4 (&c)[4], int lane) {
         if (b1) c[q] = r; else c[q + 2] = r;
     }
 }
-template <typename TO>
+// One tile (128 rows of one head) by TMA: one box, or two 64-column boxes
+// into the two sub-tiles (D = 128).
+template <int D>
+__device__ __forceinline__ void tma_tile(unsigned char* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    tma_load_2d(dst, map, x, y, bar);
+    if constexpr (Cfg<D>::kSub == 2) tma_load_2d(dst + Cfg<D>::kTB / 2, map, x + 64, y, bar);
+}
+
+template <typename TO, int D>
 __global__ void __launch_bounds__(kThreadsWS, 1)
 k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const int4* __restrict__ items, int n_work, int H,
              TO* __restrict__ out, int HD, float sl2, int* __restrict__ err, long long wait_limit, int test_stall) {
+    using C = Cfg<D>;
+    constexpr uint32_t kTileBytes = C::kTB;
+    constexpr int kStages = C::kStages;
+    constexpr int kQB = C::kQBufs;
+    constexpr int kNqMax = C::kNq;
+    constexpr uint64_t kStageUnits = C::kStageUnits;
+    constexpr uint64_t kQUnits = C::kQUnits;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -286,9 +439,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    auto sQ = [&](int buf, int g) { return smem + kWsSmemQ + (2 * buf + g) * kTileBytes; };
-    auto sK = [&](int st) { return smem + kWsSmemKV + st * 2 * kTileBytes; };
-    auto sV = [&](int st) { return smem + kWsSmemKV + st * 2 * kTileBytes + kTileBytes; };
+    auto sQ = [&](int buf, int g) { return smem + C::kSmemQ + (kNqMax * buf + g) * kTileBytes; };
+    auto sK = [&](int st) { return smem + C::kSmemKV + st * 2 * kTileBytes; };
+    auto sV = [&](int st) { return smem + C::kSmemKV + st * 2 * kTileBytes + kTileBytes; };
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&s_tmem)),
@@ -339,19 +492,19 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 const int h = h_next;
                 const int4 it = it_next;   // the next item's entry is loaded one item ahead
                 if (w + gridDim.x < n_work) it_next = item_of(items, w + gridDim.x, H, &h_next);
-                const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = (n + kTile - 1) / kTile, xh = h * kD;
-                const int qb = local & 1;
-                if (local >= 2) ok = mbar_wait(&bars.q_empty[qb], ((local >> 1) - 1) & 1, wait_limit);
+                const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = (n + kTile - 1) / kTile, xh = h * D;
+                const int qb = local % kQB;
+                if (local >= kQB) ok = mbar_wait(&bars.q_empty[qb], ((local / kQB) - 1) & 1, wait_limit);
                 if (!ok) break;
                 mbar_expect_tx(&bars.q_full[qb], nq * kTileBytes);
-                for (int g = 0; g < nq; ++g) tma_load_2d(sQ(qb, g), &tmQ, xh, q0 + g * kTile, &bars.q_full[qb]);
+                for (int g = 0; g < nq; ++g) tma_tile<D>(sQ(qb, g), &tmQ, xh, q0 + g * kTile, &bars.q_full[qb]);
                 for (int j = 0; j < T; ++j, ++kv_tile) {
                     const int st = kv_tile % kStages;
                     if (kv_tile >= kStages) ok = mbar_wait(&bars.kv_empty[st], ((kv_tile / kStages) - 1) & 1, wait_limit);
                     if (!ok) break;
                     mbar_expect_tx(&bars.kv_full[st], 2 * kTileBytes);
-                    tma_load_2d(sK(st), &tmK, xh, r0 + j * kTile, &bars.kv_full[st]);
-                    tma_load_2d(sV(st), &tmV, xh, r0 + j * kTile, &bars.kv_full[st]);
+                    tma_tile<D>(sK(st), &tmK, xh, r0 + j * kTile, &bars.kv_full[st]);
+                    tma_tile<D>(sV(st), &tmV, xh, r0 + j * kTile, &bars.kv_full[st]);
                 }
             }
             if (!ok) {
@@ -363,8 +516,8 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     const int uses = kv_tile / kStages + (st < kv_tile % kStages ? 1 : 0);
                     if (uses > 0) mbar_wait(&bars.kv_full[st], (uses - 1) & 1, kWaitCycles / 4);
                 }
-                for (int b = 0; b < 2; ++b) {
-                    const int uses = (local + 1 - b) / 2;
+                for (int b = 0; b < kQB; ++b) {
+                    const int uses = (local + kQB - 1 - b) / kQB;
                     if (uses > 0) mbar_wait(&bars.q_full[b], (uses - 1) & 1, kWaitCycles / 4);
                 }
             }
@@ -383,10 +536,10 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         // before it (non-blocking) and read after it.
         {
             const uint32_t idS = idesc_bf16(128, 128, 0);
-            const uint32_t idO = idesc_bf16(128, 64, 1);
-            const uint64_t dQ0 = smem_desc_sw128(su32(sQ(0, 0)), 16, 1024);
-            const uint64_t dK0 = smem_desc_sw128(su32(sK(0)), 16, 1024);
-            const uint64_t dV0 = smem_desc_sw128(su32(sV(0)), 8192, 1024);
+            const uint32_t idO = idesc_bf16(128, D, 1);
+            const uint64_t dQ0 = desc_kmajor<D>(su32(sQ(0, 0)));
+            const uint64_t dK0 = desc_kmajor<D>(su32(sK(0)));
+            const uint64_t dV0 = desc_mnmajor<D>(su32(sV(0)));
             bool ok = true;
             int kv_tile = 0;   // first K/V tile of the current item in the CTA's sequence
             int snum = 0;      // S tiles issued so far (buffer = snum % 3)
@@ -398,15 +551,16 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 int h;
                 const int4 it = item_of(items, w, H, &h);
                 const int nq = it.w, T = (it.y + kTile - 1) / kTile;
-                const int qb = local & 1;
+                const int qb = local % kQB;
                 const int s0 = snum;   // S number of (g, j) = s0 + nq*j + g
                 auto bufk = [&](int g, int j) { return (s0 + nq * j + g) % 3; };
                 // S_g(j); the K tile's readiness was established before
                 auto issue_s = [&](int g, int j) {
                     const int kt = kv_tile + j;
-                    const uint64_t dQ = smem_desc_sw128(su32(sQ(qb, g)), 16, 1024);
-                    const uint64_t dK = smem_desc_sw128(su32(sK(kt % kStages)), 16, 1024);
-                    mma_s_batch(tmem + col_buf(bufk(g, j)), dQ, dK, idS);
+                    const uint64_t dQ = desc_kmajor<D>(su32(sQ(qb, g)));
+                    const uint64_t dK = desc_kmajor<D>(su32(sK(kt % kStages)));
+                    if constexpr (D == 64) mma_s_batch(tmem + col_buf(bufk(g, j)), dQ, dK, idS);
+                    else mma_s_batch_d<D>(tmem + col_buf(bufk(g, j)), dQ, dK, idS, 1u);
                     int& sn = g == 0 ? sg0 : sg1;
                     tc_commit(&bars.s[g][sn & 1]);
                     ++sn;
@@ -433,7 +587,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     ++pc;
                     return r;
                 };
-                ok = mbar_wait_warp(&bars.q_full[qb], (local >> 1) & 1, wait_limit);
+                ok = mbar_wait_warp(&bars.q_full[qb], (local / kQB) & 1, wait_limit);
                 if (!ok) break;
                 // S tiles ahead of the loop: A0 (B0) and A1
                 ok = kv_wait(0, 0u);
@@ -448,11 +602,11 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 }
                 // descriptors: the bases plus a stage's or a Q buffer's offset
                 // (the start address field is linear in the byte address)
-                const uint64_t dQa = dQ0 + static_cast<uint64_t>(2 * qb) * kQUnits, dQb = dQa + kQUnits;
-                int st = kv_tile & (kStages - 1);   // stage of K_j, V_j
+                const uint64_t dQa = dQ0 + static_cast<uint64_t>(kNqMax * qb) * kQUnits, dQb = dQa + kQUnits;
+                int st = kv_tile % kStages;   // stage of K_j, V_j
                 int bA = s0 % 3;                    // buffer of S_A(j); S_B(j) is in the next one
                 uint32_t pa = p_probe(0);
-                for (int j = 0; ok && j < T; ++j, st = (st + 1) & (kStages - 1), bA = mod3(bA + nq)) {
+                for (int j = 0; ok && j < T; ++j, st = stage_add<kStages>(st, 1), bA = mod3(bA + nq)) {
                     // the first product of an item overwrites O_g: the previous
                     // item's epilogue must have read it
                     ok = p_wait(0, pa);
@@ -464,10 +618,15 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                     const uint64_t dVj = dV0 + static_cast<uint64_t>(st) * kStageUnits;
                     {   // PV_A(j), then S_B(j+1) into the buffer PV_A(j) has just read
                         const bool sb = nq > 1 && j + 1 < T;
-                        mma_half_step(tmem + col_o(0), tmem + col_buf(bA), dVj, idO, j > 0 ? 1u : 0u,
-                                      su32(&bars.o[0][pv0 & 1]), 1u, 0u, 0u, tmem + col_buf(bA), dQb,
-                                      dK0 + static_cast<uint64_t>((st + 1) & (kStages - 1)) * kStageUnits, idS,
-                                      su32(&bars.s[1][sg1 & 1]), sb ? 1u : 0u);
+                        const uint64_t dKn = dK0 + static_cast<uint64_t>(stage_add<kStages>(st, 1)) * kStageUnits;
+                        if constexpr (D == 64)
+                            mma_half_step(tmem + col_o<D>(0), tmem + col_buf(bA), dVj, idO, j > 0 ? 1u : 0u,
+                                          su32(&bars.o[0][pv0 & 1]), 1u, 0u, 0u, tmem + col_buf(bA), dQb, dKn, idS,
+                                          su32(&bars.s[1][sg1 & 1]), sb ? 1u : 0u);
+                        else
+                            mma_half_step_d<D>(tmem + col_o<D>(0), tmem + col_buf(bA), dVj, idO, j > 0 ? 1u : 0u,
+                                               su32(&bars.o[0][pv0 & 1]), 1u, 0u, 0u, tmem + col_buf(bA), dQb, dKn,
+                                               idS, su32(&bars.s[1][sg1 & 1]), sb ? 1u : 0u);
                         ++pv0;
                         if (sb) { ++sg1; ++snum; }
                     }
@@ -484,11 +643,18 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                         // into the buffer of S_B(j) (one query tile: of S_A(j+1)'s successor)
                         const bool sa = j + 2 < T;
                         const int bS = (bA + 2 * nq) % 3;
-                        mma_half_step(tmem + col_o(1), tmem + col_buf(mod3(bA + 1)), dVj, idO, j > 0 ? 1u : 0u,
-                                      su32(&bars.o[1][pv1 & 1]), nq > 1 ? 1u : 0u, su32(&bars.kv_empty[st]), 1u,
-                                      tmem + col_buf(bS), dQa,
-                                      dK0 + static_cast<uint64_t>((st + 2) & (kStages - 1)) * kStageUnits, idS,
-                                      su32(&bars.s[0][sg0 & 1]), sa ? 1u : 0u);
+                        const uint64_t dKn = dK0 + static_cast<uint64_t>(stage_add<kStages>(st, 2)) * kStageUnits;
+                        // (O_B's columns exist only when an item holds two query tiles)
+                        const uint32_t dOb = tmem + col_o<D>(kNqMax > 1 ? 1 : 0);
+                        if constexpr (D == 64)
+                            mma_half_step(dOb, tmem + col_buf(mod3(bA + 1)), dVj, idO, j > 0 ? 1u : 0u,
+                                          su32(&bars.o[1][pv1 & 1]), nq > 1 ? 1u : 0u, su32(&bars.kv_empty[st]), 1u,
+                                          tmem + col_buf(bS), dQa, dKn, idS, su32(&bars.s[0][sg0 & 1]), sa ? 1u : 0u);
+                        else
+                            mma_half_step_d<D>(dOb, tmem + col_buf(mod3(bA + 1)), dVj, idO, j > 0 ? 1u : 0u,
+                                               su32(&bars.o[1][pv1 & 1]), nq > 1 ? 1u : 0u,
+                                               su32(&bars.kv_empty[st]), 1u, tmem + col_buf(bS), dQa, dKn, idS,
+                                               su32(&bars.s[0][sg0 & 1]), sa ? 1u : 0u);
                         if (nq > 1) ++pv1;
                         if (sa) { ++sg0; ++snum; }
                     }
@@ -516,7 +682,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         const int g = warp >> 2;                       // query tile
         const int row = (warp & 3) * 32 + lane;        // row of the query tile (= TMEM lane)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tO = tmem + col_o(g) + lane_base;
+        const uint32_t tO = tmem + col_o<D>(g) + lane_base;
         const bool pos = sl2 >= 0.f;
         int s_cnt = 0;      // S tiles of this query tile consumed so far
         int o_cnt = 0;      // PV_g products of finished items
@@ -542,7 +708,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             const int h = h_next;
             const int4 it = it_next;   // the next item's entry is loaded one item ahead
             if (w + gridDim.x < n_work) it_next = item_of(items, w + gridDim.x, H, &h_next);
-            const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = (n + kTile - 1) / kTile, xh = h * kD;
+            const int r0 = it.x, n = it.y, q0 = it.z, nq = it.w, T = (n + kTile - 1) / kTile, xh = h * D;
             const int s0 = snum;
             snum += nq * T;
             if (g >= nq) continue;
@@ -655,7 +821,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                         l0 *= alpha;
                         l1 *= alpha;
 #pragma unroll 1
-                        for (int c = 0; c < 2; ++c) {
+                        for (int c = 0; c < D / 32; ++c) {
                             uint32_t o[32];
                             tmem_ld32(tO + 32 * c, o);
                             tmem_ld_wait();
@@ -681,9 +847,9 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             if (bad) atomicExch(&s_abort, 1);
             if (__any_sync(0xffffffffu, bad)) { failed = true; break; }
             tc_fence_after();
-            uint32_t o[64];
-            tmem_ld32(tO, o);
-            tmem_ld32(tO + 32, o + 32);
+            uint32_t o[D];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, o + 32 * c);
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
@@ -698,7 +864,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
             const int rows_left = r0 + n - qrow;   // rows k < rows_left of the quad are the block's
             if constexpr (sizeof(TO) == 2) {
 #pragma unroll
-                for (int gg = 0; gg < 2; ++gg) {   // 16-byte chunks 4gg..4gg+3 (columns 32gg..32gg+31)
+                for (int gg = 0; gg < D / 32; ++gg) {   // 16-byte chunks 4gg..4gg+3 (columns 32gg..32gg+31)
                     uint4 c[4];
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -716,7 +882,7 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                 }
             } else {
 #pragma unroll
-                for (int gg = 0; gg < 4; ++gg) {   // 16-byte chunks 4gg..4gg+3 (columns 16gg..16gg+15)
+                for (int gg = 0; gg < D / 16; ++gg) {   // 16-byte chunks 4gg..4gg+3 (columns 16gg..16gg+15)
                     uint4 c[4];
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
@@ -747,16 +913,20 @@ k_dense_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
 }
 
 // ---- host ------------------------------------------------------------------
-// [N, HD] bf16 matrix, box 64 (one head) x 128 rows, 128-byte swizzle.
+// [N, HD] bf16 matrix, boxes of 128 rows: one head of 32 columns with the
+// 64-byte swizzle, or 64 columns (a whole head of 64, half of one of 128)
+// with the 128-byte swizzle.
+template <int D>
 bool make_map(CUtensorMap* m, const void* base, int64_t N, int HD) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(N)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(HD) * 2};
-    cuuint32_t box[2] = {kD, kTile};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(Cfg<D>::kBoxX), kTile};
     cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -780,47 +950,55 @@ bool regs_fit(K kernel) {
 bool dense_supported(int H, int D, gtattn_dtype dt, const void* Q, const void* K, const void* V,
                      const void* out) {
     if (dt != GTATTN_BF16 && dt != GTATTN_BF16_OUT_F32) return false;
-    if (D != kD || H < 1 || H * D > kMaxHD) return false;
+    if ((D != 32 && D != 64 && D != 128) || H < 1 || H * D > kMaxHD) return false;
     const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                          reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(out);
     if (al & 15u) return false;
     return encode_fn() != nullptr;
 }
 
-gtattn_status launch_dense(const int4* tiles, int n_tiles, int64_t N, const void* Q, const void* K,
-                           const void* V, void* out, int H, int D, float scale, gtattn_dtype dt, int* err,
-                           long long wait_cycles, int test_stall, cudaStream_t s) {
-    const long long wait_limit = wait_cycles > 0 ? wait_cycles : kWaitCycles;
-    if (n_tiles <= 0) return GTATTN_OK;
+template <int D>
+static gtattn_status launch_dense_d(const int4* tiles, int n_tiles, int64_t N, const void* Q, const void* K,
+                                    const void* V, void* out, int H, float scale, gtattn_dtype dt, int* err,
+                                    long long wait_limit, int test_stall, cudaStream_t s) {
     const int HD = H * D;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, Q, N, HD) || !make_map(&mk, K, N, HD) || !make_map(&mv, V, N, HD))
+    if (!make_map<D>(&mq, Q, N, HD) || !make_map<D>(&mk, K, N, HD) || !make_map<D>(&mv, V, N, HD))
         return GTATTN_ERR_UNSUPPORTED;
     const float sl2 = scale * kLog2e;
     const int n_work = n_tiles * H;
     const int grid = std::min(n_work, num_sms());
-    cudaError_t e;
-    if (dt == GTATTN_BF16) {
-        auto k = k_dense_attn<__nv_bfloat16>;
+    constexpr int smem = static_cast<int>(Cfg<D>::kSmemAlloc);
+    auto go = [&](auto k, auto* o) {
         if (!regs_fit(k)) return GTATTN_ERR_UNSUPPORTED;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess) {
-            k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, n_work, H,
-                                                     static_cast<__nv_bfloat16*>(out), HD, sl2, err, wait_limit,
-                                                     test_stall);
+            k<<<grid, kThreadsWS, smem, s>>>(mq, mk, mv, tiles, n_work, H, o, HD, sl2, err, wait_limit, test_stall);
             e = cudaGetLastError();
         }
-    } else {
-        auto k = k_dense_attn<float>;
-        if (!regs_fit(k)) return GTATTN_ERR_UNSUPPORTED;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kWsSmemAlloc);
-        if (e == cudaSuccess) {
-            k<<<grid, kThreadsWS, kWsSmemAlloc, s>>>(mq, mk, mv, tiles, n_work, H, static_cast<float*>(out), HD,
-                                                     sl2, err, wait_limit, test_stall);
-            e = cudaGetLastError();
-        }
+        return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+    };
+    if (dt == GTATTN_BF16) return go(k_dense_attn<__nv_bfloat16, D>, static_cast<__nv_bfloat16*>(out));
+    return go(k_dense_attn<float, D>, static_cast<float*>(out));
+}
+
+gtattn_status launch_dense(const int4* tiles, const int4* tiles1, int n_tiles, int n_tiles1, int64_t N,
+                           const void* Q, const void* K, const void* V, void* out, int H, int D, float scale,
+                           gtattn_dtype dt, int* err, long long wait_cycles, int test_stall, cudaStream_t s) {
+    const long long wait_limit = wait_cycles > 0 ? wait_cycles : kWaitCycles;
+    switch (D) {
+        case 32:
+            if (n_tiles <= 0) return GTATTN_OK;
+            return launch_dense_d<32>(tiles, n_tiles, N, Q, K, V, out, H, scale, dt, err, wait_limit, test_stall, s);
+        case 64:
+            if (n_tiles <= 0) return GTATTN_OK;
+            return launch_dense_d<64>(tiles, n_tiles, N, Q, K, V, out, H, scale, dt, err, wait_limit, test_stall, s);
+        case 128:   // one query tile per work item
+            if (n_tiles1 <= 0) return GTATTN_OK;
+            return launch_dense_d<128>(tiles1, n_tiles1, N, Q, K, V, out, H, scale, dt, err, wait_limit, test_stall,
+                                       s);
     }
-    return e == cudaSuccess ? GTATTN_OK : cuda_status(e);
+    return GTATTN_ERR_UNSUPPORTED;
 }
 
 }  // namespace gt

@@ -404,15 +404,23 @@ extern "C" gtattn_status gtattn_csr_build(const int32_t* indptr, const int32_t* 
             return fail(st);
         // one work item per pair of 128-row query tiles: (block row, block size,
         // first query row, query tiles in the item)
-        std::vector<int4> tiles;
-        for (const int2& b : hb)
+        std::vector<int4> tiles, tiles1;
+        for (const int2& b : hb) {
             for (int q0 = b.x; q0 < b.x + b.y; q0 += 2 * kDenseTile)
                 tiles.push_back(make_int4(b.x, b.y, q0, std::min(2, (b.x + b.y - q0 + kDenseTile - 1) / kDenseTile)));
+            // (the widest heads take one query tile per item)
+            for (int q0 = b.x; q0 < b.x + b.y; q0 += kDenseTile) tiles1.push_back(make_int4(b.x, b.y, q0, 1));
+        }
         if ((st = chk(cudaMalloc(&p->dense_tiles, sizeof(int4) * tiles.size()))) != GTATTN_OK) return fail(st);
         if ((st = chk(cudaMemcpy(p->dense_tiles, tiles.data(), sizeof(int4) * tiles.size(),
                                  cudaMemcpyHostToDevice))) != GTATTN_OK)
             return fail(st);
         p->n_dense_tiles = static_cast<int>(tiles.size());
+        if ((st = chk(cudaMalloc(&p->dense_tiles1, sizeof(int4) * tiles1.size()))) != GTATTN_OK) return fail(st);
+        if ((st = chk(cudaMemcpy(p->dense_tiles1, tiles1.data(), sizeof(int4) * tiles1.size(),
+                                 cudaMemcpyHostToDevice))) != GTATTN_OK)
+            return fail(st);
+        p->n_dense_tiles1 = static_cast<int>(tiles1.size());
     }
     *plan_out = p;
     return GTATTN_OK;
@@ -430,6 +438,7 @@ extern "C" gtattn_status gtattn_plan_destroy(gtattn_plan* p) {
     cudaFree(p->longs);
     cudaFree(p->blocks);
     cudaFree(p->dense_tiles);
+    cudaFree(p->dense_tiles1);
     cudaFree(p->dense_flag);
     if (p->ws) cudaFree(p->ws);
     if (p->bwd_pattern) cudaFree(p->bwd_pattern);

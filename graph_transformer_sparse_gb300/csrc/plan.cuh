@@ -16,6 +16,8 @@ struct gtattn_plan {
     int2* blocks = nullptr;                 // (first row, size) per dense block
     int4* dense_tiles = nullptr;            // (block row, block size, first query row, query tiles)
     int n_dense_tiles = 0;
+    int4* dense_tiles1 = nullptr;           // the same blocks, one query tile per item
+    int n_dense_tiles1 = 0;
     int* dense_flag = nullptr;              // 1 for rows inside a dense block
     mutable void* ws = nullptr;             // split-row partials workspace
     mutable size_t ws_bytes = 0;

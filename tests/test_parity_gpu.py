@@ -381,12 +381,13 @@ def _mixed_dense_graph(rng, sizes, n_sparse, sparse_edges):
     return np.concatenate(src), np.concatenate(dst), n_total
 
 
+@pytest.mark.parametrize("D", [32, 64, 128])
 @pytest.mark.parametrize("out32", [True, False])
-def test_dense_path_mixed_graph(out32):
+def test_dense_path_mixed_graph(out32, D):
     rng = np.random.default_rng(77)
     src, dst, n = _mixed_dense_graph(rng, [128, 384, 256], 500, 6000)
     ip, ix = wl.csr_by_destination(src, dst, n)
-    Q, K, V = (0.5 * rng.standard_normal((n, 8, 64)) for _ in range(3))
+    Q, K, V = (0.5 * rng.standard_normal((n, 8, D)) for _ in range(3))
     w = _mk(ip, ix, Q, K, V, "bf16")
     ref = oracle_rows(w)["out"]
     d = to_device(w, out32=out32)
@@ -396,7 +397,7 @@ def test_dense_path_mixed_graph(out32):
     gt.gtattn_profile_enable(True)
     gt.gtattn_profile_read(reset=True)
     d["out"].fill_(float("nan"))
-    gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], 8, 64, w.scale,
+    gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], 8, D, w.scale,
                        _dt(d))
     torch.cuda.synchronize()
     prof = gt.gtattn_profile_read(reset=True)
@@ -405,11 +406,12 @@ def test_dense_path_mixed_graph(out32):
     assert plan.info()["device_error"] == 0
     plan.close()
     got = out_to_numpy(d["out"])
-    check_out(w, got, ref, f"mixed dense+sparse out32={out32}", out32=out32)
+    check_out(w, got, ref, f"mixed dense+sparse D={D} out32={out32}", out32=out32)
 
 
+@pytest.mark.parametrize("D", [32, 64, 128])
 @pytest.mark.parametrize("sign", [1.0, -1.0])
-def test_dense_path_ragged_blocks(sign):
+def test_dense_path_ragged_blocks(sign, D):
     # complete blocks whose sizes are not multiples of the 128-row tile: the
     # last key tile of each is masked (a negative scale flips the mask's
     # sign), rows past a block's end in its last query tile are not stored
@@ -417,7 +419,7 @@ def test_dense_path_ragged_blocks(sign):
     sizes = [200, 128, 300, 511, 129]
     src, dst, n = _mixed_dense_graph(rng, sizes, 400, 5000)
     ip, ix = wl.csr_by_destination(src, dst, n)
-    Q, K, V = (0.5 * rng.standard_normal((n, 8, 64)) for _ in range(3))
+    Q, K, V = (0.5 * rng.standard_normal((n, 8, D)) for _ in range(3))
     w = _mk(ip, ix, Q, K, V, "bf16")
     scale = sign * w.scale
     ref = oracle.sparse_mha(w.indptr, w.indices, w.Q, w.K, w.V, scale, threads=8)["out"]
@@ -429,37 +431,39 @@ def test_dense_path_ragged_blocks(sign):
         gt.gtattn_profile_enable(True)
         gt.gtattn_profile_read(reset=True)
         d["out"].fill_(float("nan"))
-        gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], 8, 64, scale, _dt(d))
+        gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], 8, D, scale, _dt(d))
         torch.cuda.synchronize()
         prof = gt.gtattn_profile_read(reset=True)
         gt.gtattn_profile_enable(False)
         assert prof["dense"]["launches"] == 1, prof
         assert plan.info()["device_error"] == 0
         plan.close()
-        check_out(w, out_to_numpy(d["out"]), ref, f"ragged dense blocks sign={sign} out32={out32}", out32=out32)
+        check_out(w, out_to_numpy(d["out"]), ref, f"ragged dense blocks D={D} sign={sign} out32={out32}",
+                  out32=out32)
 
 
-def test_dense_path_large_scores():
+@pytest.mark.parametrize("D", [32, 64, 128])
+def test_dense_path_large_scores(D):
     # logits spread over a wide range: the running max is raised mid-row and
     # O is rescaled
     rng = np.random.default_rng(5)
     n = 512
     src, dst, _ = _mixed_dense_graph(rng, [n], 0, 0)
     ip, ix = wl.csr_by_destination(src, dst, n)
-    Q = rng.standard_normal((n, 2, 64)) * 3
-    K = rng.standard_normal((n, 2, 64)) * 3
+    Q = rng.standard_normal((n, 2, D)) * 3 * np.sqrt(64 / D)
+    K = rng.standard_normal((n, 2, D)) * 3
     K[:, :, :] *= np.linspace(0.1, 2.0, n)[:, None, None]     # later keys larger: max grows across tiles
-    V = rng.standard_normal((n, 2, 64))
+    V = rng.standard_normal((n, 2, D))
     w = _mk(ip, ix, Q, K, V, "bf16")
     ref = oracle_rows(w)["out"]
     d = to_device(w, out32=True)
     plan = gt.Plan(d["indptr"], d["indices"], detect_dense=True)
-    gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], 2, 64, w.scale,
+    gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], 2, D, w.scale,
                        _dt(d))
     torch.cuda.synchronize()
     assert plan.info()["device_error"] == 0
     plan.close()
-    check_out(w, out_to_numpy(d["out"]), ref, "dense large scores", out32=True)
+    check_out(w, out_to_numpy(d["out"]), ref, f"dense large scores D={D}", out32=True)
 
 
 @pytest.mark.parametrize("n", [4096, 4097])

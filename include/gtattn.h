@@ -203,7 +203,8 @@ gtattn_status gtattn_fwd_ndh(const int32_t* indptr, const int32_t* indices, cons
 /*
  * gtattn_fwd_plan -- as gtattn_fwd with a prebuilt plan: no binning per
  * call, and complete blocks (if the plan found any) go to the dense
- * tensor-core kernel when dtype is bf16 and D == 64.  indptr/indices must be
+ * tensor-core kernel when dtype is bf16 (or bf16 in, fp32 out), D is 32, 64
+ * or 128 and the pointers are 16-byte aligned.  indptr/indices must be
  * the arrays the plan was built from.  Grows the plan's workspace on demand
  * (stream-ordered).
  */

@@ -19,6 +19,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libgtattn.so")
+# The checking build: every call that takes a CSR validates it on the device
+# first (GTATTN_DEBUG) and returns GTATTN_ERR_BAD_CSR instead of running.
+LIB_DEBUG = os.path.join(LIB_DIR, "libgtattn_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -58,21 +61,26 @@ def _stamp(extra) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link ``lib/libgtattn.so``; skips work when the sources,
-    headers and flags are unchanged since the last build."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile and link ``lib/libgtattn.so`` (``debug``: the checking build
+    ``lib/libgtattn_debug.so``, objects kept apart); skips work when the
+    sources, headers and flags are unchanged since the last build."""
+    build_dir = BUILD + "_debug" if debug else BUILD
+    lib_path = LIB_DEBUG if debug else LIB
+    if debug:
+        extra_flags = tuple(extra_flags) + ("-DGTATTN_DEBUG",)
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
-    stamp_file = os.path.join(BUILD, "stamp")
+    stamp_file = os.path.join(build_dir, "stamp")
     stamp = _stamp(extra_flags)
-    if (not force and os.path.exists(LIB) and os.path.exists(stamp_file)
+    if (not force and os.path.exists(lib_path) and os.path.exists(stamp_file)
             and open(stamp_file).read() == stamp):
-        return LIB
+        return lib_path
     nvcc = _nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *_flags(extra_flags), "-c", src, "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
@@ -87,16 +95,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             if verbose and err:
                 print(err)
     cuda_lib = os.path.join(_cuda_home(nvcc), "lib64")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", f"-rpath,{cuda_lib}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

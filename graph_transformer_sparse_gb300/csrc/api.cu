@@ -316,6 +316,14 @@ static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, co
 extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indices, const void* Q,
                                     const void* K, const void* V, void* out, int64_t N, int64_t nnz,
                                     int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
+    GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
+    return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream);
+}
+
+gtattn_status gt::fwd_view(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                           const void* V, void* out, int64_t N, int64_t nnz, int H, int D, float scale,
+                           gtattn_dtype dtype, cudaStream_t stream) {
     return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream);
 }
 
@@ -375,6 +383,7 @@ extern "C" gtattn_status gtattn_fwd_ndh(const int32_t* indptr, const int32_t* in
                                         int D, float scale, gtattn_dtype dtype, cudaStream_t stream) {
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
     if (N == 0) return GTATTN_OK;
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
     // Shapes the vector or narrow-head kernel takes: transpose to [N, H, D]
     // in scratch, the head-major forward, transpose the output back (four
     // row-local copies, far cheaper than the generic kernel on head-innermost
@@ -431,6 +440,7 @@ static gtattn_status fwd_plan(const gtattn_plan* plan, const int32_t* indptr, co
     if (!plan) return GTATTN_ERR_INVALID_ARG;
     const int64_t N = plan->N, nnz = plan->nnz;
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
     RowChoice c;
     if (!choose_row_kernel(H, D, dtype, Q, K, V, out, plan->opts.kernel, &c)) return GTATTN_ERR_UNSUPPORTED;
     if (N == 0) return GTATTN_OK;
@@ -539,6 +549,8 @@ extern "C" gtattn_status gtattn_fwd_probs(const int32_t* indptr, const int32_t* 
                                           const void* K, const void* V, void* out, float* logits,
                                           float* probs, int64_t N, int64_t nnz, int H, int D, float scale,
                                           gtattn_dtype dtype, cudaStream_t stream) {
+    GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
     return fwd_unfused(indptr, indices, Q, K, V, nullptr, nullptr, out, logits, probs, N, nnz, H, D, scale, dtype,
                        stream);
 }
@@ -548,6 +560,8 @@ extern "C" gtattn_status gtattn_fwd_bias(const int32_t* indptr, const int32_t* i
                                          float* logits, float* probs, int64_t N, int64_t nnz, int H, int D,
                                          float scale, gtattn_dtype dtype, cudaStream_t stream) {
     if ((nnz > 0 && !bias) || (reinterpret_cast<uintptr_t>(bias) & 3u)) return GTATTN_ERR_INVALID_ARG;
+    GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
     if (logits || probs)
         return fwd_unfused(indptr, indices, Q, K, V, nullptr, bias, out, logits, probs, N, nnz, H, D, scale, dtype,
                            stream);
@@ -559,6 +573,8 @@ extern "C" gtattn_status gtattn_fwd_weighted(const int32_t* indptr, const int32_
                                              float* probs, int64_t N, int64_t nnz, int H, int D, float scale,
                                              gtattn_dtype dtype, cudaStream_t stream) {
     if ((nnz > 0 && !values) || (reinterpret_cast<uintptr_t>(values) & 3u)) return GTATTN_ERR_INVALID_ARG;
+    GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
     if (logits || probs)
         return fwd_unfused(indptr, indices, Q, K, V, values, nullptr, out, logits, probs, N, nnz, H, D, scale, dtype,
                            stream);
@@ -725,6 +741,7 @@ extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indice
                                     cudaStream_t stream) {
     GT_TRY(check_bwd(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, nnz, H, D, dtype));
     if (N == 0) return GTATTN_OK;
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
     RowChoice c;
     if (!bwd_two_pass(H, D, dtype, Q, K, V, dO, dQ, dK, dV, &c))
         return bwd_fallback(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, H, D, scale, dtype, stream);
@@ -766,6 +783,7 @@ extern "C" gtattn_status gtattn_bwd_plan(const gtattn_plan* plan, const int32_t*
         (reinterpret_cast<uintptr_t>(stats) & 3u))
         return GTATTN_ERR_INVALID_ARG;
     if (N == 0) return GTATTN_OK;
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
     RowChoice c;
     if (!bwd_two_pass(H, D, dtype, Q, K, V, dO, dQ, dK, dV, &c))
         return bwd_fallback(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, H, D, scale, dtype, stream);
@@ -815,6 +833,7 @@ extern "C" gtattn_status gtattn_fwd_proj(const int32_t* indptr, const int32_t* i
     if ((in_al & (esz - 1)) || (f_al & 3u) || (reinterpret_cast<uintptr_t>(Y) & (osz - 1)))
         return GTATTN_ERR_INVALID_ARG;
     if (N == 0) return GTATTN_OK;
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
     const int HD = H * D;
     const int64_t nhd = N * HD;
     // temporaries: q, k, v and the attention output unless the caller keeps

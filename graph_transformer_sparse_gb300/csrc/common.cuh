@@ -159,6 +159,17 @@ void pool_free(void* p, cudaStream_t s);
 // sizes, dtype, alignment): GTATTN_OK or GTATTN_ERR_INVALID_ARG.
 gtattn_status check_fwd(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
                         const void* V, const void* out, int64_t N, int64_t nnz, int H, int D, gtattn_dtype dtype);
+// The checking build (GTATTN_DEBUG): validates a device CSR (offsets from 0
+// to nnz, non-decreasing; indices in [0, N)) before the call's first other
+// kernel, synchronously, and returns GTATTN_ERR_BAD_CSR if it fails; one
+// flag in device memory, so concurrent calls race on it.  Defined in plan.cu.
+gtattn_status debug_csr_check(const int32_t* indptr, const int32_t* indices, int64_t N, int64_t nnz,
+                              cudaStream_t s);
+// gtattn_fwd without that check, for calls on views of a checked CSR (the
+// host-buffer path's row chunks).  Defined in api.cu.
+gtattn_status fwd_view(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K, const void* V,
+                       void* out, int64_t N, int64_t nnz, int H, int D, float scale, gtattn_dtype dtype,
+                       cudaStream_t stream);
 
 // Benchmark instrumentation: brackets a launch group with CUDA events when
 // profiling is enabled (see gtattn_profile_enable).
@@ -184,3 +195,13 @@ class ProfScope {
         gtattn_status _s = (call);                              \
         if (_s != GTATTN_OK) return _s;                         \
     } while (0)
+
+// CSR check of the checking build at an entry point (nothing otherwise).
+#ifdef GTATTN_DEBUG
+#define GT_DEBUG_CSR(indptr, indices, N, nnz, s)                                        \
+    do {                                                                                \
+        if ((N) > 0) GT_TRY(gt::debug_csr_check((indptr), (indices), (N), (nnz), (s)));  \
+    } while (0)
+#else
+#define GT_DEBUG_CSR(indptr, indices, N, nnz, s) do { } while (0)
+#endif

@@ -88,6 +88,13 @@ extern "C" gtattn_status gtattn_fwd_host(const int32_t* indptr, const int32_t* i
     if (N == 0) return GTATTN_OK;
     // indptr is read here on the host (chunk boundaries): check its ends
     if (indptr[0] != 0 || indptr[N] != nnz) return GTATTN_ERR_BAD_CSR;
+#ifdef GTATTN_DEBUG
+    // the checking build validates the whole CSR, here on the host
+    for (int64_t i = 0; i < N; ++i)
+        if (indptr[i + 1] < indptr[i]) return GTATTN_ERR_BAD_CSR;
+    for (int64_t e = 0; e < nnz; ++e)
+        if (indices[e] < 0 || indices[e] >= N) return GTATTN_ERR_BAD_CSR;
+#endif
 
     const size_t esz = dtype == GTATTN_F32 ? 4 : 2;
     const size_t osz = dtype == GTATTN_BF16 ? 2 : 4;
@@ -153,7 +160,7 @@ extern "C" gtattn_status gtattn_fwd_host(const int32_t* indptr, const int32_t* i
         const int64_t r0 = b[c], r1 = b[c + 1];
         if (!ok(cudaStreamWaitEvent(stream, ev[1 + c], 0))) break;
         if (r1 > r0) {
-            st = gtattn_fwd(ip_d + r0, nnz > 0 ? idx_d : nullptr, q_d + r0 * HD * esz, nnz > 0 ? k_d : nullptr,
+            st = fwd_view(ip_d + r0, nnz > 0 ? idx_d : nullptr, q_d + r0 * HD * esz, nnz > 0 ? k_d : nullptr,
                             nnz > 0 ? v_d : nullptr, out_d + r0 * HD * osz, r1 - r0, indptr[r1] - indptr[r0], H,
                             D, scale, dtype, stream);
             if (st != GTATTN_OK) break;

@@ -117,6 +117,7 @@ extern "C" gtattn_status gtattn_fwd_noalloc(const int32_t* indptr, const int32_t
                                             cudaStream_t stream) {
     // the same argument rules as gtattn_fwd
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);   // (the checking build: a device flag, no allocation)
 
     const int HD = H * D;
     int64_t n_long = 0, n_chunks = 0;

@@ -329,6 +329,7 @@ extern "C" gtattn_status gtattn_csr_build(const int32_t* indptr, const int32_t* 
     if (!indptr || (nnz > 0 && !indices)) return GTATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(indptr) | reinterpret_cast<uintptr_t>(indices)) & 3u)
         return GTATTN_ERR_INVALID_ARG;
+    GT_DEBUG_CSR(indptr, indices, N, nnz, stream);
 
     gtattn_plan* p = new (std::nothrow) gtattn_plan();
     if (!p) return GTATTN_ERR_NO_MEMORY;
@@ -490,6 +491,28 @@ __global__ void k_validate(const int* __restrict__ indptr, const int* __restrict
     }
     if (local) atomicOr(bad, 1);
 }
+
+#ifdef GTATTN_DEBUG
+__device__ int g_debug_bad_csr;   // the checking build's validation flag
+
+gtattn_status gt::debug_csr_check(const int32_t* indptr, const int32_t* indices, int64_t N, int64_t nnz,
+                              cudaStream_t s) {
+    int* bad = nullptr;
+    GT_CUDA(cudaGetSymbolAddress(reinterpret_cast<void**>(&bad), g_debug_bad_csr));
+    GT_CUDA(cudaMemsetAsync(bad, 0, sizeof(int), s));
+    k_validate<<<grid_for(std::max<int64_t>(N + 1, nnz), 256), 256, 0, s>>>(indptr, indices, (int)N, (int)nnz, bad);
+    GT_CUDA(cudaGetLastError());
+    int h_bad = 0;
+    GT_CUDA(cudaMemcpyAsync(&h_bad, bad, sizeof(int), cudaMemcpyDeviceToHost, s));
+    GT_CUDA(cudaStreamSynchronize(s));
+    if (h_bad) {
+        set_last_error("checking build: the CSR failed validation (offsets from 0 to nnz, non-decreasing; "
+                       "indices in [0, N)); nothing else ran");
+        return GTATTN_ERR_BAD_CSR;
+    }
+    return GTATTN_OK;
+}
+#endif
 
 extern "C" gtattn_status gtattn_csr_validate(const int32_t* indptr, const int32_t* indices,
                                              int64_t N, int64_t nnz, cudaStream_t stream) {

@@ -40,6 +40,13 @@
  *            ABI.  Argument checks run on the host before any launch.  CSR
  *            contents are NOT checked on the fast path (use
  *            gtattn_csr_validate); an invalid CSR gives undefined results.
+ *            The checking build of the library (compiled with GTATTN_DEBUG:
+ *            lib/libgtattn_debug.so) validates the CSR of every call that
+ *            takes one on the device first (gtattn_fwd_host: on the host),
+ *            synchronously, and returns GTATTN_ERR_BAD_CSR without running
+ *            anything else; its one device flag is shared, so calls of the
+ *            checking build must not overlap, and it cannot be captured in
+ *            a CUDA graph.
  *            GTATTN_ERR_CUDA reports a CUDA runtime error (the last CUDA
  *            error string is available from gtattn_last_error).
  * Threads:   entry points are thread-safe, except that one plan must not be

@@ -1681,19 +1681,30 @@ static int coop_grid(K kernel, int threads, size_t smem) {
     return grid;
 }
 
+// The one-launch path's launch: cooperative when a row may be split (the
+// grid then synchronises before the combine), else an ordinary launch
+// (programmatic dependent launch: it may start while the previous kernel of
+// the stream finishes).
+template <typename Kern>
+static cudaError_t launch_small(Kern kernel, int grid, int threads, size_t smem, cudaStream_t s,
+                                const RowParams& p) {
+    if (p.small_no_split) return launch_pdl(kernel, grid, threads, smem, s, p);
+    return launch_coop(kernel, grid, threads, smem, s, p);
+}
+
 template <typename T, typename TO>
 static gtattn_status launch_small_t(const RowChoice& c, const RowParams& p, cudaStream_t s) {
     const size_t smem = sizeof(int2) * static_cast<size_t>(p.small_max_chunks + p.small_max_long);
     auto go = [&](auto kernel, int threads) {
         const int grid = grid_for_tasks(coop_grid(kernel, threads, smem), p.task_bound, threads / 32);
-        return launch_coop(kernel, std::max(grid, 1), threads, smem, s, p);
+        return launch_small(kernel, std::max(grid, 1), threads, smem, s, p);
     };
     cudaError_t e;
     if (narrow_applies(c, kFused, p)) {
         auto go_n = [&](auto kernel) {
             const int grid = grid_for_tasks(coop_grid(kernel, kRowThreads, smem), narrow_task_bound(p),
                                             kRowThreads / 32);
-            return launch_coop(kernel, std::max(grid, 1), kRowThreads, smem, s, p);
+            return launch_small(kernel, std::max(grid, 1), kRowThreads, smem, s, p);
         };
         e = c.vpl ? go_n(k_rows_narrow<T, TO, true, true>) : go_n(k_rows_narrow<T, TO, false, true>);
     } else if (c.kind == RowKernel::kVector) {

@@ -550,7 +550,10 @@ def gpu_arm(args):
     total_prof_ms = max(sum(x["ms"] for x in prof.values()), 1e-9)
     shares = {k: round(v["ms"] / total_prof_ms, 4) for k, v in prof.items() if v["launches"]}
     dominant = max(prof, key=lambda k: prof[k]["ms"])
-    kern_ms = prof[dominant]["ms"] / max(prof[dominant]["groups"], 1)
+    # the dominant kernel's time per step (the sum over its launches: one,
+    # or one per head group when the forward runs the heads in groups)
+    kern_ms = prof[dominant]["ms"] / args.steps
+    kern_launches = prof[dominant]["launches"] / args.steps
     if dominant == "dense":
         flops = dense_flops(info["n_dense_blocks"], w.N // max(info["n_dense_blocks"], 1), w.H, w.D)
         achieved = flops / (kern_ms / 1e3) / 1e12
@@ -566,7 +569,10 @@ def gpu_arm(args):
         # the kernel's time; the compulsory figure (every K/V gather counted,
         # most served by the L2) and the ncu DRAM bytes sit beside it
         achieved = ubytes / (kern_ms / 1e3) / 1e9
+        # (the capture is one launch: a step of head groups launches the kernel once per group)
         traffic = ncu_traffic("k_rows_vec", name) if args.path == "fwd" else None
+        if traffic:
+            traffic *= kern_launches
         roofline = {"bound": "hbm", "kernel": "k_rows_vec (fused row kernel)", "achieved": round(achieved, 1),
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                     "traffic": traffic,
@@ -579,7 +585,8 @@ def gpu_arm(args):
                     "frac_dram": (round(traffic / (kern_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
                                   if traffic else None),
                     "traffic_over_unique": round(traffic / ubytes, 3) if traffic else None,
-                    "kernel_ms": round(kern_ms, 5), "kernel_shares": shares}
+                    "kernel_ms": round(kern_ms, 5), "kernel_launches_per_step": kern_launches,
+                    "kernel_shares": shares}
     # the same step with a warm L2 (no flush between steps)
     warm = time_steps(step, args.steps, None)
     warm_ms = statistics.median(warm)
@@ -656,7 +663,9 @@ def gpu_arm(args):
             ms = statistics.median(t_o)
             es = 2 if wo.dtype == "bf16" else 4
             cb, ub = path_bytes(pth, wo.N, wo.nnz, wo.H, wo.D, es)
-            kms = {k: round(v["ms"] / max(v["groups"], 1), 5) for k, v in p_o.items() if v["groups"]}
+            # per step (all of a category's launches in the step)
+            kms = {k: round(v["ms"] / n_o, 5) for k, v in p_o.items() if v["groups"]}
+            kl = {k: v["launches"] / n_o for k, v in p_o.items() if v["groups"]}
             ent = {"ms": round(ms, 5), "edge_heads_per_s": round(wo.nnz * wo.H / (ms / 1e3), 1),
                    "gbs_unique": round(ub / (ms / 1e3) / 1e9, 1),
                    "hbm_frac": round(ub / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
@@ -666,13 +675,14 @@ def gpu_arm(args):
                 ent["rows_kernel_hbm_frac"] = round(ub / (kms["rows"] / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
                 tr = ncu_traffic("k_rows_vec", other) if pth == "fwd" else None
                 if tr:
+                    tr *= kl["rows"]   # (one capture is one launch: per step, one per head group)
                     ent["rows_kernel_traffic"] = tr
                     ent["rows_kernel_frac_dram"] = round(tr / (kms["rows"] / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
                     ent["traffic_over_unique"] = round(tr / ub, 3)
             if pth == "proj" and "gemm" in kms:
                 # the two linear maps' launches (permutations of the weights included)
-                tf = proj_flops(wo.N, wo.H, wo.D) / (kms["gemm"] * 3 / 1e3) / 1e12
-                ent["gemm_ms_per_call"] = round(kms["gemm"] * 3, 5)
+                tf = proj_flops(wo.N, wo.H, wo.D) / (kms["gemm"] / 1e3) / 1e12
+                ent["gemm_ms_per_call"] = round(kms["gemm"], 5)
                 ent["gemm_tflops"] = round(tf, 1)
                 ent["gemm_tensor_frac"] = round(tf / peaks["bf16_tflops"], 4) if wo.dtype == "bf16" else None
             if other.startswith("dense_blocks") and inf_o and inf_o.get("n_dense_blocks"):

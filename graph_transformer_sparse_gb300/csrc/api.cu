@@ -39,6 +39,19 @@ int num_sms() {
     return cache[dev];
 }
 
+// L2 bytes of the current device (cached per device).
+static int64_t l2_bytes() {
+    static int64_t cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) n = 1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 // One library-owned memory pool per device; freed blocks stay cached in the
 // pool (release threshold: unlimited) so per-call temporaries cost no
 // driver allocation after the first call.
@@ -183,6 +196,7 @@ static RowParams make_params(const int32_t* indptr, const int32_t* indices, cons
     p.H = H;
     p.D = D;
     p.HD = H * D;
+    p.ld = H * D;
     p.G = c.G;
     p.lph = c.lph;
     p.lists = L;
@@ -240,10 +254,70 @@ extern "C" gtattn_status gtattn_profile_read(gtattn_profile* out, int reset) {
 
 // The fused forward on the fly (binning, fused rows, combine), with an
 // optional per-entry additive bias or per-entry adjacency values.
+// Head groups run one after another over the same rows (each head's softmax
+// is its own, so the groups are independent).  A group's gathers touch only
+// its columns of the K and V rows, so when K and V together exceed the L2 a
+// group's share may fit and its gathers stop going to DRAM once per entry
+// (Erdos-Renyi, 8 x 64 bf16, 205 MB of K and V: one pass 0.464 ms, two
+// passes 0.410).  Groups are halved while K and V exceed 85 % of the L2 and
+// a group's share of a row stays at least 512 bytes: rows of a few hundred
+// bytes lose more to the repeated task set-up than the L2 wins (R-MAT, 256-
+// byte rows: 0.96 ms in one pass, 1.24 in two).  Vector kernel, plain fused
+// forward (no bias, values, head-innermost rows or row statistics).
+static int head_passes(int64_t n_src, int H, int D, gtattn_dtype dtype, const RowChoice& c, const float* bias,
+                       const float* values, int ndh) {
+    if (bias || values || ndh || c.kind != RowKernel::kVector) return 1;
+    const double row = static_cast<double>(H) * D * (dtype == GTATTN_F32 ? 4 : 2);
+    const double kv = 2.0 * static_cast<double>(n_src) * row;
+    const double budget = 0.85 * static_cast<double>(l2_bytes());
+    int n = 1;
+    while (kv / n > budget && H % (2 * n) == 0 && row / (2 * n) >= 512.0) n *= 2;
+    return n;
+}
+
+// The fused rows and (when a row may be split) the combine, over head groups
+// (head_passes; one group when row statistics are written).
+static gtattn_status rows_in_groups(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
+                                    const void* V, void* out, int64_t N, int64_t nnz, int H, int D, float scale,
+                                    gtattn_dtype dtype, const RowChoice& c, const TaskLists& L, const Partials& part,
+                                    const float* bias, const float* values, int ndh, float* lse, bool run_rows,
+                                    bool run_combine, int64_t n_src, cudaStream_t stream) {
+    // (n_src: the rows of K and V the entries point into, which decide the
+    // head groups; a call on a view of some rows passes the whole graph's)
+    int passes = lse ? 1 : head_passes(n_src, H, D, dtype, c, bias, values, ndh);
+    RowChoice cs = c;
+    if (passes > 1 && !choose_row_kernel(H / passes, D, dtype, Q, K, V, out, GTATTN_KERNEL_VECTOR, &cs)) passes = 1;
+    const int Hs = H / passes;
+    const size_t esz = dtype == GTATTN_F32 ? 4 : 2, osz = dtype == GTATTN_BF16 ? 2 : 4;
+    gtattn_status st = GTATTN_OK;
+    for (int g = 0; g < passes && st == GTATTN_OK; ++g) {
+        // head group g: heads g*Hs .. g*Hs+Hs-1, the same rows at the full stride
+        const size_t off = static_cast<size_t>(g) * Hs * D;
+        const RowChoice& cg = passes > 1 ? cs : c;
+        RowParams p = make_params(indptr, indices, static_cast<const char*>(Q) + off * esz,
+                                  static_cast<const char*>(K) + off * esz, static_cast<const char*>(V) + off * esz,
+                                  static_cast<char*>(out) + off * osz, N, nnz, Hs, D, scale * kLog2e, cg, L, part);
+        p.ld = H * D;
+        p.bias = bias;
+        p.values = values;
+        p.ndh = ndh;
+        p.lse = lse;
+        if (run_rows) {
+            ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+            st = launch_rows(kFused, dtype, cg, p, stream);
+        }
+        if (st == GTATTN_OK && run_combine) {
+            ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
+            st = launch_combine(kFused, dtype, p, stream);
+        }
+    }
+    return st;
+}
+
 static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
                                const void* V, const float* values, const float* bias, void* out, int64_t N,
                                int64_t nnz, int H, int D, float scale, gtattn_dtype dtype, cudaStream_t stream,
-                               int ndh = 0) {
+                               int ndh = 0, int64_t n_src = -1) {
     GT_TRY(check_fwd(indptr, indices, Q, K, V, out, N, nnz, H, D, dtype));
     RowChoice c;
     // head-innermost rows ([N, D, H]): the generic kernel (the vector kernel's
@@ -297,18 +371,9 @@ static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, co
         ProfScope ps(GTATTN_KCAT_BIN, bin_launches((int)N, nullptr), stream);
         st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
     }
-    RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale * kLog2e, c, sc.lists, sc.part);
-    p.bias = bias;
-    p.values = values;
-    p.ndh = ndh;
-    if (st == GTATTN_OK) {
-        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
-        st = launch_rows(kFused, dtype, c, p, stream);
-    }
-    if (st == GTATTN_OK && nnz > o.long_row_min) {   // else no row is split
-        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
-        st = launch_combine(kFused, dtype, p, stream);
-    }
+    if (st == GTATTN_OK)
+        st = rows_in_groups(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, c, sc.lists, sc.part, bias,
+                            values, ndh, nullptr, true, nnz > o.long_row_min, n_src < 0 ? N : n_src, stream);
     pool_free(sc.base, stream);
     return st;
 }
@@ -323,8 +388,8 @@ extern "C" gtattn_status gtattn_fwd(const int32_t* indptr, const int32_t* indice
 
 gtattn_status gt::fwd_view(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
                            const void* V, void* out, int64_t N, int64_t nnz, int H, int D, float scale,
-                           gtattn_dtype dtype, cudaStream_t stream) {
-    return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream);
+                           gtattn_dtype dtype, int64_t n_src, cudaStream_t stream) {
+    return fwd_fused(indptr, indices, Q, K, V, nullptr, nullptr, out, N, nnz, H, D, scale, dtype, stream, 0, n_src);
 }
 
 // Row-local transpose between [N, D, H] and [N, H, D] (to_hd: from the
@@ -469,8 +534,6 @@ static gtattn_status fwd_plan(const gtattn_plan* plan, const int32_t* indptr, co
         part.acc = reinterpret_cast<float*>(b + 2 * align_up(sizeof(float) * (size_t)n_chunks * H));
     }
     TaskLists L{plan->hdr, plan->rows, plan->chunks, plan->longs, plan->opts.chunk_edges, dense ? 0 : 1};
-    RowParams p = make_params(indptr, indices, Q, K, V, out, N, nnz, H, D, scale * kLog2e, c, L, part);
-    p.lse = stats;
     gtattn_status st = GTATTN_OK;
     if (dense) {
         ProfScope ps(GTATTN_KCAT_DENSE, 1, stream);
@@ -480,14 +543,9 @@ static gtattn_status fwd_plan(const gtattn_plan* plan, const int32_t* indptr, co
     }
     int row_tasks = n_chunks + (dense ? 0 : plan->hdr_host[HdrLayout::kDenseRows]);
     for (int b = 0; b < kNumBuckets; ++b) row_tasks += plan->hdr_host[HdrLayout::kCount + b];
-    if (st == GTATTN_OK && row_tasks > 0) {
-        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
-        st = launch_rows(kFused, dtype, c, p, stream);
-    }
-    if (st == GTATTN_OK && n_long > 0) {
-        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
-        st = launch_combine(kFused, dtype, p, stream);
-    }
+    if (st == GTATTN_OK && (row_tasks > 0 || n_long > 0))
+        st = rows_in_groups(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, c, L, part, nullptr, nullptr,
+                            0, stats, row_tasks > 0, n_long > 0, N, stream);
     return st;
 }
 

@@ -166,10 +166,12 @@ gtattn_status check_fwd(const int32_t* indptr, const int32_t* indices, const voi
 gtattn_status debug_csr_check(const int32_t* indptr, const int32_t* indices, int64_t N, int64_t nnz,
                               cudaStream_t s);
 // gtattn_fwd without that check, for calls on views of a checked CSR (the
-// host-buffer path's row chunks).  Defined in api.cu.
+// host-buffer path's row chunks); n_src: the rows of K and V (the whole
+// graph's), which the kernel choices depend on as in the whole call.
+// Defined in api.cu.
 gtattn_status fwd_view(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K, const void* V,
                        void* out, int64_t N, int64_t nnz, int H, int D, float scale, gtattn_dtype dtype,
-                       cudaStream_t stream);
+                       int64_t n_src, cudaStream_t stream);
 
 // Benchmark instrumentation: brackets a launch group with CUDA events when
 // profiling is enabled (see gtattn_profile_enable).

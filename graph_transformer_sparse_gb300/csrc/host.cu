@@ -162,7 +162,7 @@ extern "C" gtattn_status gtattn_fwd_host(const int32_t* indptr, const int32_t* i
         if (r1 > r0) {
             st = fwd_view(ip_d + r0, nnz > 0 ? idx_d : nullptr, q_d + r0 * HD * esz, nnz > 0 ? k_d : nullptr,
                             nnz > 0 ? v_d : nullptr, out_d + r0 * HD * osz, r1 - r0, indptr[r1] - indptr[r0], H,
-                            D, scale, dtype, stream);
+                            D, scale, dtype, N, stream);
             if (st != GTATTN_OK) break;
         }
         ok(cudaEventRecord(ev[1 + n_chunks + c], stream)) &&

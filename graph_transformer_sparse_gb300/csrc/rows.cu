@@ -227,7 +227,7 @@ __device__ void small_combine(const RowParams& p, const int2* longs, int n_long)
                 S += p.part.s[k] * w;
                 v += p.part.acc[static_cast<int64_t>(c0 + c) * HD + el] * w;
             }
-            store_elem(O, static_cast<int64_t>(row) * HD + el, S > 0.f ? v / S : 0.f);
+            store_elem(O, static_cast<int64_t>(row) * p.ld + el, S > 0.f ? v / S : 0.f);
         }
     }
 }
@@ -374,6 +374,7 @@ k_rows_vec(RowParams p) {
     const T* __restrict__ V = static_cast<const T*>(p.V);
     TO* __restrict__ O = static_cast<TO*>(p.out);
     const int64_t HD = p.HD;
+    const int64_t LD = p.ld;   // row stride of Q, K, V and out (elements; a 32-bit value)
     const int lane_off = gl * E;
 
     const int warps_total = gridDim.x * (blockDim.x >> 5);
@@ -426,7 +427,7 @@ k_rows_vec(RowParams p) {
             if (cur.valid) {
                 const int j = ld_index(p.indices + cur.beg);
                 F fv;
-                fv.load(V + (int64_t)j * HD + lane_off);
+                fv.load(V + (int64_t)j * LD + lane_off);
                 float x[E];
 #pragma unroll
                 for (int e = 0; e < E; ++e) x[e] = fv.get(e);
@@ -438,7 +439,7 @@ k_rows_vec(RowParams p) {
 #pragma unroll
                     for (int e = 0; e < E; ++e) x[e] *= wgt;
                 }
-                store_frag<TO, E>(O + (int64_t)cur.row * HD + lane_off, x);
+                store_frag<TO, E>(O + (int64_t)cur.row * LD + lane_off, x);
             }
             continue;
         }
@@ -455,7 +456,7 @@ k_rows_vec(RowParams p) {
         float q[E];          // fp32 inputs: q pre-scaled
         F fq;                // bf16 inputs: q kept packed, the scale multiplies the dot
         if constexpr (MODE != kSpmm) {
-            if (valid) fq.load_once(Q + (int64_t)row * HD + lane_off); else fq.zero();
+            if (valid) fq.load_once(Q + (int64_t)row * LD + lane_off); else fq.zero();
             if constexpr (!kBf16) {
                 const float qs = MODE == kFused ? p.qscale : 1.f;   // SDDMM scales at the store
 #pragma unroll
@@ -493,8 +494,8 @@ k_rows_vec(RowParams p) {
                 ax[u] = e + step < end ? ld_stream(p.values + e + step) : 0.f;
             }
             const int j = okc[u] ? ld_index(p.indices + e) : 0;
-            if (kNeedK) { if (okc[u]) kc[u].load(K + (int64_t)j * HD + lane_off); else kc[u].zero(); }
-            if (kNeedV) { if (okc[u]) vc[u].load(V + (int64_t)j * HD + lane_off); else vc[u].zero(); }
+            if (kNeedK) { if (okc[u]) kc[u].load(K + (int64_t)j * LD + lane_off); else kc[u].zero(); }
+            if (kNeedV) { if (okc[u]) vc[u].load(V + (int64_t)j * LD + lane_off); else vc[u].zero(); }
             const int e1 = e + step;
             jn[u] = e1 < end ? ld_index(p.indices + e1) : 0;
         }
@@ -518,8 +519,8 @@ k_rows_vec(RowParams p) {
                     const int e2a = e1 + step;
                     ax[u] = e2a < end ? ld_stream(p.values + e2a) : 0.f;
                 }
-                if (kNeedK) { if (okn[u]) kn[u].load(K + (int64_t)jn[u] * HD + lane_off); else kn[u].zero(); }
-                if (kNeedV) { if (okn[u]) vn[u].load(V + (int64_t)jn[u] * HD + lane_off); else vn[u].zero(); }
+                if (kNeedK) { if (okn[u]) kn[u].load(K + (int64_t)jn[u] * LD + lane_off); else kn[u].zero(); }
+                if (kNeedV) { if (okn[u]) vn[u].load(V + (int64_t)jn[u] * LD + lane_off); else vn[u].zero(); }
                 const int e2 = e1 + step;
                 jn[u] = e2 < end ? ld_index(p.indices + e2) : 0;
             }
@@ -658,7 +659,7 @@ k_rows_vec(RowParams p) {
                 // the row's log-sum-exp (log2 units) when the caller asks for it
                 if (p.lse && gl % p.lph == 0) p.lse[(int64_t)row * p.H + head] = m + log2f(ssum);
             }
-            store_frag<TO, E>(O + (int64_t)row * HD + lane_off, acc);
+            store_frag<TO, E>(O + (int64_t)row * LD + lane_off, acc);
         }
         }   // MODE != kSddmm
     }
@@ -1179,7 +1180,7 @@ k_combine(RowParams p, int warp_rows) {
                 float tot = 0.f;
                 for (int k = 0; k < Ge; ++k) tot += red[k * HD + t];
                 if (MODE == kFused) tot = sS[h] > 0.f ? tot / sS[h] : 0.f;
-                store_elem(O, (int64_t)row * HD + t, tot);
+                store_elem(O, (int64_t)row * p.ld + t, tot);
             }
         } else {
             for (int el = t; el < HD; el += kCombThreads) {
@@ -1192,7 +1193,7 @@ k_combine(RowParams p, int warp_rows) {
                     v += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M) : a;
                 }
                 if (MODE == kFused) v = sS[h] > 0.f ? v / sS[h] : 0.f;
-                store_elem(O, (int64_t)row * HD + el, v);
+                store_elem(O, (int64_t)row * p.ld + el, v);
             }
         }
         __syncthreads();
@@ -1245,7 +1246,7 @@ k_combine(RowParams p, int warp_rows) {
                     }
                     float v = (v4[0] + v4[1]) + (v4[2] + v4[3]);
                     if (MODE == kFused) v = Sh > 0.f ? v / Sh : 0.f;
-                    store_elem(O, (int64_t)row * HD + el, v);
+                    store_elem(O, (int64_t)row * p.ld + el, v);
                 }
             }
         }

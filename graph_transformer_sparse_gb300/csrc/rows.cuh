@@ -22,6 +22,9 @@ struct RowParams {
     float* logits;          // SDDMM mode: fp32 [nnz, H]
     float qscale;           // fused: scale*log2(e); SDDMM: scale
     int N, H, D, HD;
+    int ld;                 // row stride of Q, K, V and out in elements (HD, or more for a head group
+                            // of wider rows: vector kernel, combine); an int, so that index * ld is
+                            // one widening multiply
     int G, lph;             // vector kernel: lanes per feature row, lanes per head
     TaskLists lists;
     Partials part;

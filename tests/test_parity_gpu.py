@@ -625,3 +625,39 @@ def test_narrow_kernel_refuses_wide_shapes():
             gt.gtattn_fwd_plan(plan, d["indptr"], d["indices"], d["Q"], d["K"], d["V"], d["out"], H, D, w.scale,
                                gt.GTATTN_F32)
         plan.close()
+
+
+def test_head_groups_on_a_graph_whose_k_and_v_exceed_the_l2():
+    # K and V together above 85 % of the L2, 1 KB rows: the forward runs the
+    # heads in groups (one launch of the row kernel per group), each group
+    # reading its columns of the rows; sampled rows against the oracle, and
+    # the same bits from the host-buffer path (its row chunks decide the
+    # groups from the whole graph)
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    H, D = 8, 64
+    n = int(0.5 * l2 / (H * D * 2)) + 1000   # K + V = 2 n H D 2 bytes: about the whole L2
+    rng = np.random.default_rng(91)
+    ip, ix = wl.random_csr(rng, n, 6 * n, self_loops=True)
+    Q, K, V = (rng.standard_normal((n, H, D)).astype(np.float32) for _ in range(3))
+    w = _mk(ip, ix, Q, K, V, "bf16")
+    d = to_device(w, out32=True)
+    gt.gtattn_profile_enable(True)
+    gt.gtattn_profile_read(reset=True)
+    got, _, _ = run(w, d, "fwd")
+    prof = gt.gtattn_profile_read(reset=True)
+    gt.gtattn_profile_enable(False)
+    kv = 2 * n * H * D * 2
+    groups = 1
+    while kv / groups > 0.85 * l2 and H % (2 * groups) == 0 and H * D * 2 / (2 * groups) >= 512:
+        groups *= 2
+    assert groups > 1 and prof["rows"]["launches"] == groups, (groups, prof["rows"])
+    rows = sample_rows(w, n_random=800)
+    ref = oracle_rows(w, rows=rows)["out"]
+    check_out(w, got[rows], ref, f"head groups x{groups}", out32=True)
+    # the host-buffer call: same bits
+    out_h = torch.empty(n, H, D, dtype=torch.float32).pin_memory()
+    qh, kh, vh = (d[k].cpu().pin_memory() for k in ("Q", "K", "V"))
+    gt.gtattn_fwd_host(torch.from_numpy(w.indptr), torch.from_numpy(w.indices), qh, kh, vh, out_h, n, w.nnz, H, D,
+                       w.scale, gt.GTATTN_BF16_OUT_F32)
+    torch.cuda.synchronize()
+    assert np.array_equal(out_h.numpy().astype(np.float64), got)

@@ -651,6 +651,11 @@ struct SourceMajor {
     int* rowid = nullptr;
     TaskLists cols{};
     int64_t max_chunks = 0;   // capacity of the source chunk list
+    // the destination rows binned with the same thresholds, for the
+    // by-destination pass (rows cut into chunks of the backward's size: a
+    // lane group walks a task's entries in order, so long tasks become a tail)
+    TaskLists dq{};
+    int64_t dq_chunks = 0;    // capacity of its chunk list
 };
 
 static size_t source_major_carve(char* base, int64_t N, int64_t nnz, const gtattn_plan_opts& o, SourceMajor* sm) {
@@ -663,18 +668,27 @@ static size_t source_major_carve(char* base, int64_t N, int64_t nnz, const gtatt
     const size_t o_r = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N));
     const size_t o_c = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_chunks));
     const size_t o_l = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_long));
+    const size_t o_dh = off; off = align_up(off + sizeof(int) * HdrLayout::kWords);
+    const size_t o_dr = off; off = align_up(off + sizeof(int) * static_cast<size_t>(N));
+    const size_t o_dc = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_chunks));
+    const size_t o_dl = off; off = align_up(off + sizeof(int2) * static_cast<size_t>(n_long));
     if (base && sm) {
         sm->colptr = reinterpret_cast<int*>(base + o_cp);
         sm->rowid = reinterpret_cast<int*>(base + o_rid);
         sm->cols = TaskLists{reinterpret_cast<int*>(base + o_h), reinterpret_cast<int*>(base + o_r),
                              reinterpret_cast<int2*>(base + o_c), reinterpret_cast<int2*>(base + o_l), o.chunk_edges, 1};
         sm->max_chunks = n_chunks;
+        sm->dq = TaskLists{reinterpret_cast<int*>(base + o_dh), reinterpret_cast<int*>(base + o_dr),
+                           reinterpret_cast<int2*>(base + o_dc), reinterpret_cast<int2*>(base + o_dl), o.chunk_edges, 1};
+        sm->dq_chunks = n_chunks;   // (same thresholds, N and nnz: the same worst case)
     }
     return off;
 }
 
 // Builds *sm (carved already) from the destination binning `rows`: counts,
-// scan, scatter, segment sort, then the source binning.  Scratch from the pool.
+// scan, scatter, segment sort, the source binning, then the destination
+// rows binned again with the source thresholds (for the by-destination
+// pass).  Scratch from the pool.
 static gtattn_status source_major_build(const int32_t* indptr, const int32_t* indices, const TaskLists& rows,
                                         int64_t N, int64_t nnz, const gtattn_plan_opts& o, const SourceMajor& sm,
                                         cudaStream_t stream) {
@@ -692,8 +706,27 @@ static gtattn_status source_major_build(const int32_t* indptr, const int32_t* in
                        reinterpret_cast<int*>(b + o_ts), sm.rowid, reinterpret_cast<int*>(b + o_tmp), sm.cols,
                        o.long_row_min, stream);
     }
+    if (st == GTATTN_OK) {
+        ProfScope ps(GTATTN_KCAT_BIN, bin_launches((int)N, nullptr), stream);
+        // (the lists are this pattern's own memory, carved writable)
+        st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, const_cast<int*>(sm.dq.hdr),
+                      const_cast<int*>(sm.dq.rows), const_cast<int2*>(sm.dq.chunks), const_cast<int2*>(sm.dq.longs),
+                      stream);
+    }
     pool_free(scr, stream);
     return st;
+}
+
+// The source binning's split thresholds: the backward's own (a task per
+// source of up to kBwdLongMin entries, kBwdChunk-entry chunks above) unless
+// the plan's thresholds were set away from the forward's defaults.
+static gtattn_plan_opts source_opts(const gtattn_plan_opts& o) {
+    gtattn_plan_opts s = o;
+    if (s.long_row_min == kDefaultLongMin && s.chunk_edges == kDefaultChunk) {
+        s.long_row_min = kBwdLongMin;
+        s.chunk_edges = kBwdChunk;
+    }
+    return s;
 }
 
 // Host-side checks of the backward entry points.
@@ -716,9 +749,11 @@ static gtattn_status check_bwd(const int32_t* indptr, const int32_t* indices, co
     return GTATTN_OK;
 }
 
-// The two-pass backward given the destination binning (rows, with row_chunks
-// chunk slots) and the source-major pattern: the forward again for its fp32
-// output and log-sum-exp (unless the caller saved both), then the passes.
+// The two-pass backward given the forward's destination binning (rows, with
+// row_chunks chunk slots) and the source-major pattern: the forward again for
+// its fp32 output and log-sum-exp (unless the caller saved both), then the
+// passes (by destination over the pattern's own destination binning, by
+// source over its source binning).
 static gtattn_status bwd_run(const int32_t* indptr, const int32_t* indices, const TaskLists& rows, int64_t row_chunks,
                              const SourceMajor& sm, const void* Q, const void* K, const void* V, const float* O_saved,
                              const float* stats_saved, const void* dO, float* dQ, float* dK, float* dV, int64_t N,
@@ -736,7 +771,7 @@ static gtattn_status bwd_run(const int32_t* indptr, const int32_t* indices, cons
     const size_t o_m = off; off = align_up(off + sizeof(float) * static_cast<size_t>(fwd_chunks) * H);
     const size_t o_s = off; off = align_up(off + sizeof(float) * static_cast<size_t>(fwd_chunks) * H);
     const size_t o_acc = off; off = align_up(off + sizeof(float) * static_cast<size_t>(fwd_chunks) * HD);
-    const size_t o_pq = off; off = align_up(off + sizeof(float) * static_cast<size_t>(row_chunks) * HD);
+    const size_t o_pq = off; off = align_up(off + sizeof(float) * static_cast<size_t>(sm.dq_chunks) * HD);
     const size_t o_pk = off; off = align_up(off + sizeof(float) * static_cast<size_t>(sm.max_chunks) * HD);
     const size_t o_pv = off; off = align_up(off + sizeof(float) * static_cast<size_t>(sm.max_chunks) * HD);
     void* buf = nullptr;
@@ -764,7 +799,7 @@ static gtattn_status bwd_run(const int32_t* indptr, const int32_t* indices, cons
     }
     if (st == GTATTN_OK) {
         ProfScope ps(GTATTN_KCAT_ROWS, 4, stream);
-        st = launch_bwd_passes(indptr, indices, rows, sm.colptr, sm.rowid, sm.cols, Q, K, V, dO, O, lse,
+        st = launch_bwd_passes(indptr, indices, sm.dq, sm.colptr, sm.rowid, sm.cols, Q, K, V, dO, O, lse,
                                reinterpret_cast<float2*>(b + o_LD), dQ, dK, dV, reinterpret_cast<float*>(b + o_pq),
                                reinterpret_cast<float*>(b + o_pk), reinterpret_cast<float*>(b + o_pv), (int)N, nnz, H,
                                D, scale, dtype, stream);
@@ -805,6 +840,7 @@ extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indice
         return bwd_fallback(indptr, indices, Q, K, V, dO, dQ, dK, dV, N, H, D, scale, dtype, stream);
     gtattn_plan_opts o;
     resolve_opts(nullptr, &o);
+    const gtattn_plan_opts so = source_opts(o);
     Scratch sc;
     int *hdr, *rows;
     int2 *chunks, *longs;
@@ -813,14 +849,14 @@ extern "C" gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indice
     int64_t n_long = 0, row_chunks = 0;
     worst_case_sizes(N, nnz, o.long_row_min, o.chunk_edges, &n_long, &row_chunks);
     void* smb = nullptr;
-    gtattn_status st = pool_alloc(&smb, source_major_carve(nullptr, N, nnz, o, nullptr), stream);
+    gtattn_status st = pool_alloc(&smb, source_major_carve(nullptr, N, nnz, so, nullptr), stream);
     SourceMajor sm;
     if (st == GTATTN_OK) {
-        source_major_carve(static_cast<char*>(smb), N, nnz, o, &sm);
+        source_major_carve(static_cast<char*>(smb), N, nnz, so, &sm);
         ProfScope ps(GTATTN_KCAT_BIN, bin_launches((int)N, nullptr), stream);
         st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
     }
-    if (st == GTATTN_OK) st = source_major_build(indptr, indices, sc.lists, N, nnz, o, sm, stream);
+    if (st == GTATTN_OK) st = source_major_build(indptr, indices, sc.lists, N, nnz, so, sm, stream);
     if (st == GTATTN_OK)
         st = bwd_run(indptr, indices, sc.lists, row_chunks, sm, Q, K, V, nullptr, nullptr, dO, dQ, dK, dV, N, nnz, H, D,
                      scale, dtype, c, stream);
@@ -850,11 +886,12 @@ extern "C" gtattn_status gtattn_bwd_plan(const gtattn_plan* plan, const int32_t*
     const TaskLists rows{plan->hdr, plan->rows, plan->chunks, plan->longs, plan->opts.chunk_edges, 1};
     const int64_t row_chunks = plan->hdr_host[HdrLayout::kChunks];
     SourceMajor sm;
+    const gtattn_plan_opts so = source_opts(plan->opts);
     if (!plan->bwd_pattern) {   // first backward with this plan: the source-major pattern, kept
         void* p = nullptr;
-        GT_CUDA(cudaMalloc(&p, source_major_carve(nullptr, N, nnz, plan->opts, nullptr)));
-        source_major_carve(static_cast<char*>(p), N, nnz, plan->opts, &sm);
-        const gtattn_status st = source_major_build(indptr, indices, rows, N, nnz, plan->opts, sm, stream);
+        GT_CUDA(cudaMalloc(&p, source_major_carve(nullptr, N, nnz, so, nullptr)));
+        source_major_carve(static_cast<char*>(p), N, nnz, so, &sm);
+        const gtattn_status st = source_major_build(indptr, indices, rows, N, nnz, so, sm, stream);
         if (st != GTATTN_OK) {
             cudaStreamSynchronize(stream);
             cudaFree(p);
@@ -862,7 +899,7 @@ extern "C" gtattn_status gtattn_bwd_plan(const gtattn_plan* plan, const int32_t*
         }
         plan->bwd_pattern = p;
     }
-    source_major_carve(static_cast<char*>(plan->bwd_pattern), N, nnz, plan->opts, &sm);
+    source_major_carve(static_cast<char*>(plan->bwd_pattern), N, nnz, so, &sm);
     return bwd_run(indptr, indices, rows, row_chunks, sm, Q, K, V, O, stats, dO, dQ, dK, dV, N, nnz, H, D, scale,
                    dtype, c, stream);
 }

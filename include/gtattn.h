@@ -91,8 +91,8 @@ typedef enum {
  * left at 0 takes its default. */
 typedef struct {
     int32_t long_row_min;   /* rows with more entries than this are split into
-                               chunks (default 256; -1: split every non-empty row) */
-    int32_t chunk_edges;    /* entries per chunk of a split row (default 256) */
+                               chunks (default 1024; -1: split every non-empty row) */
+    int32_t chunk_edges;    /* entries per chunk of a split row (default 1024) */
     int32_t detect_dense;   /* 1: find complete blocks for the dense tensor-core path */
     int32_t kernel;         /* a gtattn_kernel value */
     int32_t wait_cycles;    /* bound of each device-side wait of the dense-block
@@ -327,9 +327,10 @@ gtattn_status gtattn_bwd(const int32_t* indptr, const int32_t* indices, const vo
 /*
  * gtattn_bwd_plan -- gtattn_bwd with a prebuilt plan, for training on a
  * fixed graph: the plan's destination binning is used as it stands, and the
- * source-major copy of the pattern with its binning is built by the first
+ * source-major copy of the pattern with its binning (and the rows binned
+ * again with the backward's own split thresholds) is built by the first
  * backward call with the plan and kept in it (about 8 N + 4 nnz bytes plus
- * the binning, freed by gtattn_plan_destroy), so later calls skip it.  Same
+ * the binnings, freed by gtattn_plan_destroy), so later calls skip it.  Same
  * results, bit for bit, as gtattn_bwd.  indptr/indices must be the arrays
  * the plan was built from.  One plan must not be used by concurrent calls.
  *   O, stats: the fp32 output (16-byte aligned) and statistics that

@@ -101,10 +101,11 @@ def test_small_workloads_all_paths(name, path, kw):
 
 
 def test_probs_split_row_boundaries():
-    # degrees on both sides of the 256-entry split threshold and of chunk
-    # boundaries (the unfused softmax merges chunk statistics per split row)
+    # degrees on both sides of the default 1024-entry split threshold and of
+    # chunk boundaries (the unfused softmax merges chunk statistics per split
+    # row)
     rng = np.random.default_rng(21)
-    degs = [0, 1, 2, 255, 256, 257, 511, 512, 513, 768, 2000, 3]
+    degs = [0, 1, 2, 255, 256, 257, 1023, 1024, 1025, 2048, 2049, 3000, 3]
     n = 2400
     indptr = np.zeros(n + 1, np.int64)
     deg = np.zeros(n, np.int64)
@@ -546,15 +547,16 @@ def test_dense_wait_timeout_is_reported_and_a_later_call_is_correct():
 @pytest.mark.parametrize("H,D,dtype", [(4, 32, "bf16"), (8, 64, "f32"), (3, 5, "f32"), (2, 8, "bf16")])
 def test_small_graph_one_launch_with_split_rows(H, D, dtype):
     # N <= 4096 and nnz <= 65536: the plan-less forward is one cooperative
-    # launch that bins in shared memory; rows of more than 256 entries are
-    # split into chunks whose partials are combined after the grid-wide sync
+    # launch that bins in shared memory; rows of more than 1024 entries (the
+    # default threshold) are split into chunks whose partials are combined
+    # after the grid-wide sync
     rng = np.random.default_rng(H * 100 + D)
     n = 3000
-    src = np.concatenate([rng.integers(0, n, 12000), rng.integers(0, n, 1500), rng.integers(0, n, 700)])
-    dst = np.concatenate([rng.integers(0, n, 12000), np.full(1500, 5), np.full(700, 2999)])
+    src = np.concatenate([rng.integers(0, n, 12000), rng.integers(0, n, 2500), rng.integers(0, n, 4000)])
+    dst = np.concatenate([rng.integers(0, n, 12000), np.full(2500, 5), np.full(4000, 2999)])
     key = np.unique(dst * n + src)
     ip, ix = wl.csr_by_destination(key % n, key // n, n)
-    assert np.diff(ip).max() > 256 and ip[-1] <= 65536
+    assert np.sort(np.diff(ip))[-2] > 1024 and ip[-1] <= 65536
     Q, K, V = (rng.standard_normal((n, H, D)) for _ in range(3))
     w = _mk(ip, ix, Q, K, V, dtype)
     ref = oracle_rows(w)["out"]

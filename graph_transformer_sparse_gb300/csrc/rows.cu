@@ -75,6 +75,12 @@ __device__ __forceinline__ int ld_index(const int* p) {
 // (a no-op for a launch without the attribute).
 __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Iterations a slot of a row's entries is sized for (more slots per row:
+// fewer iterations, more slot merges).
+#ifndef GT_SLOT_ITERS
+#define GT_SLOT_ITERS 128
+#endif
+
 // Builds the task table of a launch in shared memory (one warp).
 // P = edge slots per warp; U = edges per slot per loop iteration.
 __device__ void build_segments(const TaskLists& L, int P, int U, Seg* segs, int* nseg, int* total,
@@ -95,12 +101,14 @@ __device__ void build_segments(const TaskLists& L, int P, int U, Seg* segs, int*
                 t += (cnt + P - 1) / P;
                 continue;
             }
-            // slots: enough to cover the row in about 32 iterations, so short
-            // rows get one lane group each (4 rows per warp on R-MAT) and
-            // walk their entries in order; more slots per row cost slot
-            // merges and idle slots on the last iteration (R-MAT: 1.16 ms
-            // with one iteration per row, 1.00 ms with 32)
-            int need = (lo + 32 * U - 1) / (32 * U);
+            // slots: enough to cover the row in about GT_SLOT_ITERS (128)
+            // iterations, so short rows get one lane group each (4 rows per
+            // warp on R-MAT) and walk their entries in order; more slots per
+            // row cost slot merges and idle slots on the last iteration
+            // (R-MAT: 1.16 ms with one iteration per row, 1.00 ms with 32;
+            // with 1024-entry chunks, 0.921 ms at 32, 0.903 at 128, 0.924 at
+            // 256, 0.96 at 512)
+            int need = (lo + GT_SLOT_ITERS * U - 1) / (GT_SLOT_ITERS * U);
             int S = 1;
             while (S < need && S < P) S <<= 1;
             int R = P / S;

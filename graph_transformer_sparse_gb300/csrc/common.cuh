@@ -62,8 +62,11 @@ struct HdrLayout {
     static constexpr int kWords = kDenseSeg + 8;
 };
 // Split rows of more than this many chunks are listed first in the split-row
-// list (combined a block per row); the others a warp per row.
-constexpr int kBigChunks = 32;
+// list (combined a block per row, its threads over the chunks); the others a
+// warp per row, whose lanes walk the chunks one after another for each 32
+// output elements (R-MAT, 1024-entry chunks: 32 chunks a warp left the
+// combine 26 us long on a few such rows; 8 a warp cut it to the launch).
+constexpr int kBigChunks = 8;
 
 // Work lists consumed by the row kernels.
 struct TaskLists {

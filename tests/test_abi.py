@@ -36,6 +36,21 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_checking_build_links_and_exports_every_declared_symbol():
+    # the GTATTN_DEBUG build resolves every symbol it uses (loaded with
+    # RTLD_NOW, no call is made) and exports the same boundary
+    from graph_transformer_sparse_gb300 import _build
+    path = _build.build(debug=True)
+    dlib = ctypes.CDLL(path, mode=os.RTLD_NOW)
+    for name in _declared():
+        assert hasattr(dlib, name), name
+    # (without a GPU every call stops at the host checks)
+    fn = dlib.gtattn_status_string
+    fn.restype = ctypes.c_char_p
+    fn.argtypes = [ctypes.c_int]
+    assert fn(gt.GTATTN_ERR_BAD_CSR)
+
+
 def test_status_strings(lib):
     assert gt.gtattn_status_string(0) == "ok"
     assert gt.gtattn_status_string(2) == "malformed CSR"

@@ -39,15 +39,16 @@ int num_sms() {
     return cache[dev];
 }
 
-// L2 bytes of the current device (cached per device).
+// L2 bytes of the current device (cached per device); when unknown, a size
+// no graph exceeds (the head groups then stay one).
 static int64_t l2_bytes() {
+    constexpr int64_t kUnknown = int64_t(1) << 50;
     static int64_t cache[kMaxDevices] = {};
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kUnknown;
     if (cache[dev] == 0) {
         int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) n = 1;
-        cache[dev] = n;
+        cache[dev] = cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) == cudaSuccess && n > 0 ? n : kUnknown;
     }
     return cache[dev];
 }

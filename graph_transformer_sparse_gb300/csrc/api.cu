@@ -148,6 +148,7 @@ struct Scratch {
     void* base = nullptr;
     TaskLists lists{};
     Partials part{};
+    int64_t part_chunks = 0;   // chunk slots of the partials
     float* logits = nullptr;
     float* probs = nullptr;
 };
@@ -176,6 +177,7 @@ static gtattn_status scratch_alloc(int64_t N, int64_t nnz, int H, int HD, int lo
     sc->part.m = reinterpret_cast<float*>(b + o_m);
     sc->part.s = reinterpret_cast<float*>(b + o_s);
     sc->part.acc = reinterpret_cast<float*>(b + o_acc);
+    sc->part_chunks = n_chunks;
     if (need_logits) sc->logits = reinterpret_cast<float*>(b + o_lg);
     if (need_probs) sc->probs = reinterpret_cast<float*>(b + o_pr);
     sc->lists = TaskLists{*hdr, *rows, *chunks, *longs, chunk, 1};
@@ -198,6 +200,7 @@ static RowParams make_params(const int32_t* indptr, const int32_t* indices, cons
     p.D = D;
     p.HD = H * D;
     p.ld = H * D;
+    p.groups = 1;
     p.G = c.G;
     p.lph = c.lph;
     p.lists = L;
@@ -281,36 +284,49 @@ static int head_passes(int64_t n_src, int H, int D, gtattn_dtype dtype, const Ro
 static gtattn_status rows_in_groups(const int32_t* indptr, const int32_t* indices, const void* Q, const void* K,
                                     const void* V, void* out, int64_t N, int64_t nnz, int H, int D, float scale,
                                     gtattn_dtype dtype, const RowChoice& c, const TaskLists& L, const Partials& part,
-                                    const float* bias, const float* values, int ndh, float* lse, bool run_rows,
-                                    bool run_combine, int64_t n_src, cudaStream_t stream) {
+                                    int64_t part_chunks, const float* bias, const float* values, int ndh, float* lse,
+                                    bool run_rows, bool run_combine, int64_t n_src, cudaStream_t stream) {
     // (n_src: the rows of K and V the entries point into, which decide the
-    // head groups; a call on a view of some rows passes the whole graph's)
+    // head groups; a call on a view of some rows passes the whole graph's.
+    // part_chunks: the chunk slots `part` holds at H heads; each group's
+    // partials take a block of its own, so one combine after all the groups'
+    // rows serves them all)
     int passes = lse ? 1 : head_passes(n_src, H, D, dtype, c, bias, values, ndh);
     RowChoice cs = c;
     if (passes > 1 && !choose_row_kernel(H / passes, D, dtype, Q, K, V, out, GTATTN_KERNEL_VECTOR, &cs)) passes = 1;
     const int Hs = H / passes;
     const size_t esz = dtype == GTATTN_F32 ? 4 : 2, osz = dtype == GTATTN_BF16 ? 2 : 4;
-    gtattn_status st = GTATTN_OK;
-    for (int g = 0; g < passes && st == GTATTN_OK; ++g) {
+    const int64_t step_m = part_chunks * Hs, step_acc = part_chunks * Hs * D;
+    const RowChoice& cg = passes > 1 ? cs : c;
+    auto group_params = [&](int g) {
         // head group g: heads g*Hs .. g*Hs+Hs-1, the same rows at the full stride
         const size_t off = static_cast<size_t>(g) * Hs * D;
-        const RowChoice& cg = passes > 1 ? cs : c;
+        const Partials pg{part.m ? part.m + g * step_m : nullptr, part.s ? part.s + g * step_m : nullptr,
+                          part.acc ? part.acc + g * step_acc : nullptr};
         RowParams p = make_params(indptr, indices, static_cast<const char*>(Q) + off * esz,
                                   static_cast<const char*>(K) + off * esz, static_cast<const char*>(V) + off * esz,
-                                  static_cast<char*>(out) + off * osz, N, nnz, Hs, D, scale * kLog2e, cg, L, part);
+                                  static_cast<char*>(out) + off * osz, N, nnz, Hs, D, scale * kLog2e, cg, L, pg);
         p.ld = H * D;
         p.bias = bias;
         p.values = values;
         p.ndh = ndh;
         p.lse = lse;
-        if (run_rows) {
-            ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
-            st = launch_rows(kFused, dtype, cg, p, stream);
-        }
-        if (st == GTATTN_OK && run_combine) {
-            ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
-            st = launch_combine(kFused, dtype, p, stream);
-        }
+        return p;
+    };
+    gtattn_status st = GTATTN_OK;
+    for (int g = 0; g < passes && st == GTATTN_OK && run_rows; ++g) {
+        RowParams p = group_params(g);
+        ProfScope ps(GTATTN_KCAT_ROWS, 1, stream);
+        st = launch_rows(kFused, dtype, cg, p, stream);
+    }
+    if (st == GTATTN_OK && run_combine) {
+        RowParams p = group_params(0);
+        p.groups = passes;
+        p.gstep_m = step_m;
+        p.gstep_acc = step_acc;
+        p.gstep_out = Hs * D;
+        ProfScope ps(GTATTN_KCAT_COMBINE, 1, stream);
+        st = launch_combine(kFused, dtype, p, stream);
     }
     return st;
 }
@@ -373,8 +389,9 @@ static gtattn_status fwd_fused(const int32_t* indptr, const int32_t* indices, co
         st = bin_rows(indptr, (int)N, o.long_row_min, o.chunk_edges, nullptr, hdr, rows, chunks, longs, stream);
     }
     if (st == GTATTN_OK)
-        st = rows_in_groups(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, c, sc.lists, sc.part, bias,
-                            values, ndh, nullptr, true, nnz > o.long_row_min, n_src < 0 ? N : n_src, stream);
+        st = rows_in_groups(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, c, sc.lists, sc.part,
+                            sc.part_chunks, bias, values, ndh, nullptr, true, nnz > o.long_row_min,
+                            n_src < 0 ? N : n_src, stream);
     pool_free(sc.base, stream);
     return st;
 }
@@ -545,8 +562,8 @@ static gtattn_status fwd_plan(const gtattn_plan* plan, const int32_t* indptr, co
     int row_tasks = n_chunks + (dense ? 0 : plan->hdr_host[HdrLayout::kDenseRows]);
     for (int b = 0; b < kNumBuckets; ++b) row_tasks += plan->hdr_host[HdrLayout::kCount + b];
     if (st == GTATTN_OK && (row_tasks > 0 || n_long > 0))
-        st = rows_in_groups(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, c, L, part, nullptr, nullptr,
-                            0, stats, row_tasks > 0, n_long > 0, N, stream);
+        st = rows_in_groups(indptr, indices, Q, K, V, out, N, nnz, H, D, scale, dtype, c, L, part, n_chunks, nullptr,
+                            nullptr, 0, stats, row_tasks > 0, n_long > 0, N, stream);
     return st;
 }
 

@@ -170,6 +170,7 @@ extern "C" gtattn_status gtattn_fwd_noalloc(const int32_t* indptr, const int32_t
     p.D = D;
     p.HD = HD;
     p.ld = HD;
+    p.groups = 1;
     p.G = c.G;
     p.lph = c.lph;
     p.lists = TaskLists{hdr, rows, chunks, longs, kNoAllocChunk, 1};

@@ -1118,7 +1118,15 @@ k_combine(RowParams p, int warp_rows) {
     const int n_big = warp_rows ? p.lists.hdr[HdrLayout::kBig] : n_long;   // phase 1 rows: [0, n_big)
     const int H = p.H, D = p.D, HD = p.HD;
     const int t = threadIdx.x;
-    TO* __restrict__ O = static_cast<TO*>(p.out);
+    // head groups run one after another had their partials in blocks of
+    // their own: each group's rows, its partials and its output columns
+    const int groups = p.groups > 0 ? p.groups : 1;
+    for (int gi = 0; gi < groups; ++gi) {
+    Partials part = p.part;
+    part.m += gi * p.gstep_m;
+    part.s += gi * p.gstep_m;
+    part.acc += gi * p.gstep_acc;
+    TO* __restrict__ O = static_cast<TO*>(p.out) + static_cast<int64_t>(gi) * p.gstep_out;
     for (int li = blockIdx.x; li < n_big; li += gridDim.x) {
         const int2 lr = p.lists.longs[li];
         const int row = lr.x, c0 = lr.y;
@@ -1130,7 +1138,7 @@ k_combine(RowParams p, int warp_rows) {
             const int h = t % H, g = t / H;
             float m = -INFINITY;
             if (g < G)
-                for (int c = g; c < nch; c += G) m = fmaxf(m, p.part.m[(int64_t)(c0 + c) * H + h]);
+                for (int c = g; c < nch; c += G) m = fmaxf(m, part.m[(int64_t)(c0 + c) * H + h]);
             red[t] = m;
             __syncthreads();
             if (t < H) {
@@ -1144,7 +1152,7 @@ k_combine(RowParams p, int warp_rows) {
                 const float M = sM[h];
                 for (int c = g; c < nch; c += G) {
                     const int64_t k = (int64_t)(c0 + c) * H + h;
-                    sum += p.part.s[k] * ex2(p.part.m[k] - M);
+                    sum += part.s[k] * ex2(part.m[k] - M);
                 }
             }
             __syncthreads();   // everyone has read red[] for M
@@ -1172,13 +1180,13 @@ k_combine(RowParams p, int warp_rows) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int cu = c + u * Ge;
-                        const float a = p.part.acc[(int64_t)(c0 + cu) * HD + el];
-                        v4[u] += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + cu) * H + h] - M) : a;
+                        const float a = part.acc[(int64_t)(c0 + cu) * HD + el];
+                        v4[u] += MODE == kFused ? a * ex2(part.m[(int64_t)(c0 + cu) * H + h] - M) : a;
                     }
                 }
                 for (; c < nch; c += Ge) {
-                    const float a = p.part.acc[(int64_t)(c0 + c) * HD + el];
-                    v4[0] += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M) : a;
+                    const float a = part.acc[(int64_t)(c0 + c) * HD + el];
+                    v4[0] += MODE == kFused ? a * ex2(part.m[(int64_t)(c0 + c) * H + h] - M) : a;
                 }
                 v = (v4[0] + v4[1]) + (v4[2] + v4[3]);
             }
@@ -1197,8 +1205,8 @@ k_combine(RowParams p, int warp_rows) {
                 float v = 0.f;
 #pragma unroll 4
                 for (int c = 0; c < nch; ++c) {
-                    const float a = p.part.acc[(int64_t)(c0 + c) * HD + el];
-                    v += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - M) : a;
+                    const float a = part.acc[(int64_t)(c0 + c) * HD + el];
+                    v += MODE == kFused ? a * ex2(part.m[(int64_t)(c0 + c) * H + h] - M) : a;
                 }
                 if (MODE == kFused) v = sS[h] > 0.f ? v / sS[h] : 0.f;
                 store_elem(O, (int64_t)row * p.ld + el, v);
@@ -1222,12 +1230,12 @@ k_combine(RowParams p, int warp_rows) {
             float M = -INFINITY, S = 0.f;
             if (MODE == kFused) {
                 const int h = lane % H, step = 32 / H;
-                for (int c = lane / H; c < nch; c += step) M = fmaxf(M, p.part.m[(int64_t)(c0 + c) * H + h]);
+                for (int c = lane / H; c < nch; c += step) M = fmaxf(M, part.m[(int64_t)(c0 + c) * H + h]);
                 for (int o = H; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
                 if (M == -INFINITY) M = 0.f;   // no finite logit in the row: a zero row
                 for (int c = lane / H; c < nch; c += step) {
                     const int64_t k = (int64_t)(c0 + c) * H + h;
-                    S += p.part.s[k] * ex2(p.part.m[k] - M);
+                    S += part.s[k] * ex2(part.m[k] - M);
                 }
                 for (int o = H; o < 32; o <<= 1) S += __shfl_xor_sync(kFull, S, o);
                 if (p.lse && lane < H) p.lse[(int64_t)row * H + lane] = M + log2f(S);   // log-sum-exp, log2 units
@@ -1244,13 +1252,13 @@ k_combine(RowParams p, int warp_rows) {
                     for (; c + 3 < nch; c += 4) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const float a = p.part.acc[(int64_t)(c0 + c + u) * HD + el];
-                            v4[u] += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c + u) * H + h] - Mh) : a;
+                            const float a = part.acc[(int64_t)(c0 + c + u) * HD + el];
+                            v4[u] += MODE == kFused ? a * ex2(part.m[(int64_t)(c0 + c + u) * H + h] - Mh) : a;
                         }
                     }
                     for (; c < nch; ++c) {
-                        const float a = p.part.acc[(int64_t)(c0 + c) * HD + el];
-                        v4[0] += MODE == kFused ? a * ex2(p.part.m[(int64_t)(c0 + c) * H + h] - Mh) : a;
+                        const float a = part.acc[(int64_t)(c0 + c) * HD + el];
+                        v4[0] += MODE == kFused ? a * ex2(part.m[(int64_t)(c0 + c) * H + h] - Mh) : a;
                     }
                     float v = (v4[0] + v4[1]) + (v4[2] + v4[3]);
                     if (MODE == kFused) v = Sh > 0.f ? v / Sh : 0.f;
@@ -1259,6 +1267,7 @@ k_combine(RowParams p, int warp_rows) {
             }
         }
     }
+    }   // head groups
 }
 
 // (rows of few chunks: phase 2 of k_combine)

@@ -22,6 +22,9 @@ struct RowParams {
     float* logits;          // SDDMM mode: fp32 [nnz, H]
     float qscale;           // fused: scale*log2(e); SDDMM: scale
     int N, H, D, HD;
+    int groups;             // combine: head groups (1 but for one launch after several groups' rows);
+    int64_t gstep_m, gstep_acc;   // group gi's partials at m/s + gi*gstep_m, acc + gi*gstep_acc
+    int gstep_out;          // and its output columns at out + gi*gstep_out (elements)
     int ld;                 // row stride of Q, K, V and out in elements (HD, or more for a head group
                             // of wider rows: vector kernel, combine); an int, so that index * ld is
                             // one widening multiply

@@ -632,14 +632,19 @@ def test_narrow_kernel_refuses_wide_shapes():
 def test_head_groups_on_a_graph_whose_k_and_v_exceed_the_l2():
     # K and V together above 85 % of the L2, 1 KB rows: the forward runs the
     # heads in groups (one launch of the row kernel per group), each group
-    # reading its columns of the rows; sampled rows against the oracle, and
-    # the same bits from the host-buffer path (its row chunks decide the
-    # groups from the whole graph)
+    # reading its columns of the rows, and one combine for the split rows of
+    # every group (three hub rows of a few thousand entries); sampled rows
+    # (the hubs among them) against the oracle, and the same bits from the
+    # host-buffer path (its row chunks decide the groups from the whole graph)
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     H, D = 8, 64
     n = int(0.5 * l2 / (H * D * 2)) + 1000   # K + V = 2 n H D 2 bytes: about the whole L2
     rng = np.random.default_rng(91)
-    ip, ix = wl.random_csr(rng, n, 6 * n, self_loops=True)
+    src = np.concatenate([rng.integers(0, n, 6 * n), rng.integers(0, n, 9000)])
+    dst = np.concatenate([rng.integers(0, n, 6 * n), np.repeat([7, n // 2, n - 3], 3000)])
+    key = np.unique(dst.astype(np.int64) * n + src)
+    ip, ix = wl.csr_by_destination(key % n, key // n, n)
+    assert np.sort(np.diff(ip))[-3] > 2048
     Q, K, V = (rng.standard_normal((n, H, D)).astype(np.float32) for _ in range(3))
     w = _mk(ip, ix, Q, K, V, "bf16")
     d = to_device(w, out32=True)
@@ -653,7 +658,8 @@ def test_head_groups_on_a_graph_whose_k_and_v_exceed_the_l2():
     while kv / groups > 0.85 * l2 and H % (2 * groups) == 0 and H * D * 2 / (2 * groups) >= 512:
         groups *= 2
     assert groups > 1 and prof["rows"]["launches"] == groups, (groups, prof["rows"])
-    rows = sample_rows(w, n_random=800)
+    assert prof["combine"]["launches"] == 1, prof["combine"]
+    rows = np.union1d(sample_rows(w, n_random=800), [7, n // 2, n - 3])
     ref = oracle_rows(w, rows=rows)["out"]
     check_out(w, got[rows], ref, f"head groups x{groups}", out32=True)
     # the host-buffer call: same bits
